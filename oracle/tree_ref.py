@@ -1,0 +1,189 @@
+"""Reference radix tree: a per-token trie that records radix-node boundaries.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+Follows "SGLang: Efficient Execution of Structured Language Model Programs"
+(unite.ai, es):
+  * section "Introducción a SGLang", RadixAttention bullet: the KV cache of
+    finished calls is kept as an LRU cache inside a radix tree that supports
+    matching, insertion and eviction;
+  * section "SGLang: Modelo de programación y metodología", the nine-step
+    walkthrough: every edge carries a token sequence; a request that extends
+    a cached sequence adds its new tokens as a new node (step 3) hung after
+    the node it continues (step 5); a partial share splits a node in two
+    (steps 4 and 7); under memory pressure least-recently-used nodes are
+    evicted, one node or several (steps 5, 8, 9), and a request's own
+    matched prefix is not among them (step 8 evicts the second session while
+    the first session's system prompt is reused).
+
+Storage is one trie node per token (page size 1).  Each trie node carries a
+``head`` flag that is set on the first token of every radix node; a radix
+node is a head token plus the run of non-head single children below it.  A
+radix node's last-access value lives on its head.
+
+Readings taken where the pages are silent:
+  * a logical clock advances once per ``match_prefix`` or ``insert`` call;
+    every radix node that holds at least one token of that call's matched
+    path takes the new value (a partially matched node counts as used);
+  * ``match_prefix`` never changes the structure;
+  * ``insert`` splits a node only when new tokens diverge strictly inside it;
+    the lower part keeps the node's value from before the call, the upper
+    part is on the path and takes the new value; all new tokens form one new
+    leaf node;
+  * eviction removes whole leaf radix nodes, the one with the smallest
+    last-access value first, one after another until at least the requested
+    number of tokens is free or nothing is left (the last node may
+    overshoot); a parent left without children becomes a leaf and competes
+    in the same call.  Nodes holding a given value always lie on one root
+    path (the path of the call that set it, and splits keep both parts on
+    it), so two leaves never tie and no tie-break is needed;
+  * freed slots are reported node by node, each node in token order.
+"""
+from __future__ import annotations
+
+from typing import Dict, List, Optional, Sequence, Tuple
+
+
+class _Tok:
+    __slots__ = ("token", "slot", "head", "last", "parent", "children")
+
+    def __init__(self, token, slot, parent, head, last):
+        self.token = token
+        self.slot = slot
+        self.head = head          # first token of a radix node
+        self.last = last          # meaningful on heads only
+        self.parent = parent
+        self.children: Dict[int, "_Tok"] = {}
+
+
+class CapacityError(Exception):
+    """Raised when the caller's output capacity cannot hold the next node."""
+
+
+class RadixTreeRef:
+    def __init__(self):
+        self.root = _Tok(None, -1, None, True, 0)
+        self.clock = 0
+        self.cached_tokens = 0
+
+    # -- helpers ---------------------------------------------------------
+    def _walk(self, tokens: Sequence[int]) -> List[_Tok]:
+        node, path = self.root, []
+        for t in tokens:
+            nxt = node.children.get(int(t))
+            if nxt is None:
+                break
+            path.append(nxt)
+            node = nxt
+        return path
+
+    def _head_of(self, tok: _Tok) -> _Tok:
+        while not tok.head:
+            tok = tok.parent
+        return tok
+
+    def _tick(self, path: List[_Tok]) -> None:
+        # every radix node on a root path starts on that path, so the heads
+        # among the path's tokens are exactly the nodes it touches
+        for t in path:
+            if t.head:
+                t.last = self.clock
+
+    def _leaf_nodes(self) -> List[Tuple[_Tok, _Tok]]:
+        """(head, last token) of every radix node without children."""
+        out, stack = [], [self.root]
+        while stack:
+            n = stack.pop()
+            if n.children:
+                stack.extend(n.children.values())
+            elif n is not self.root:
+                out.append((self._head_of(n), n))
+        return out
+
+    # -- API ---------------------------------------------------------------
+    def match_prefix(self, tokens: Sequence[int]) -> Tuple[int, List[int]]:
+        """Longest cached prefix of ``tokens``: (length, its slot ids)."""
+        self.clock += 1
+        path = self._walk(tokens)
+        self._tick(path)
+        return len(path), [t.slot for t in path]
+
+    def insert(self, tokens: Sequence[int], slots: Sequence[int]) -> int:
+        """Cache ``tokens`` with ``slots``; returns how many leading tokens
+        were already cached (those keep the tree's slots)."""
+        assert len(tokens) == len(slots)
+        self.clock += 1
+        path = self._walk(tokens)
+        k = len(path)
+        end = path[-1] if path else self.root
+        if k < len(tokens) and end is not self.root and len(end.children) == 1:
+            only = next(iter(end.children.values()))
+            if not only.head:
+                # new tokens leave a node strictly inside it: split there
+                only.head = True
+                only.last = self._head_of(end).last
+        self._tick(path)
+        node = end
+        for i in range(k, len(tokens)):
+            tok = _Tok(int(tokens[i]), int(slots[i]), node, i == k, self.clock)
+            node.children[int(tokens[i])] = tok
+            node = tok
+            self.cached_tokens += 1
+        return k
+
+    def evict(self, num_tokens: int, cap: Optional[int] = None) -> List[int]:
+        """Remove leaf radix nodes, least recently used first, until at least
+        ``num_tokens`` slots are freed or the tree is empty.  Returns the
+        freed slots.  If ``cap`` is given and the next node would not fit,
+        raises CapacityError with the slots freed so far in ``err.args[0]``."""
+        freed: List[int] = []
+        while len(freed) < num_tokens:
+            leaves = self._leaf_nodes()
+            if not leaves:
+                break
+            head, last_tok = min(leaves, key=lambda hl: hl[0].last)
+            run, n = [], last_tok
+            while True:
+                run.append(n)
+                if n is head:
+                    break
+                n = n.parent
+            run.reverse()
+            if cap is not None and len(freed) + len(run) > cap:
+                raise CapacityError(freed)
+            del head.parent.children[head.token]
+            freed.extend(t.slot for t in run)
+            self.cached_tokens -= len(run)
+        return freed
+
+    # -- structure (for assertions) ----------------------------------------
+    def nodes(self) -> List[Tuple[Tuple[int, ...], Tuple[int, ...]]]:
+        """Every radix node as (token path before it, its own tokens), sorted."""
+        out, stack = [], [(self.root, ())]
+        while stack:
+            n, before = stack.pop()
+            for c in n.children.values():
+                own, t = [c.token], c
+                while len(t.children) == 1:
+                    nxt = next(iter(t.children.values()))
+                    if nxt.head:
+                        break
+                    own.append(nxt.token)
+                    t = nxt
+                out.append((before, tuple(own)))
+                stack.append((t, before + tuple(own)))
+        return sorted(out)
+
+    def num_nodes(self) -> int:
+        return len(self.nodes())
+
+    def sequences(self) -> List[Tuple[int, ...]]:
+        """All root-to-leaf token sequences."""
+        out, stack = [], [(self.root, ())]
+        while stack:
+            n, acc = stack.pop()
+            if not n.children and n is not self.root:
+                out.append(acc)
+            for t, c in n.children.items():
+                stack.append((c, acc + (t,)))
+        return sorted(out)

@@ -1,0 +1,390 @@
+"""Seeded synthetic inputs for the slot-indexed attention path.
+
+This module only *draws* inputs: token ids, bf16 Q/K/V values, slot ids and
+the per-request slot lists (``req_to_token``).  It holds none of the
+method's arithmetic (no attention, no radix tree, no scatter), so both the
+fp64 oracle and the CUDA path can be fed from it.
+
+Workload families stand in for the ones the article "SGLang: Efficient
+Execution of Structured Language Model Programs" (unite.ai) evaluates in its
+section "Introducción a SGLang" (few-shot benchmarks, multi-turn chat) and
+"SGLang: Modelo de programación y metodología" (fork/branching programs,
+the radix-tree walkthrough).  None of those suites' items are used: token
+ids are random integers and every value is N(0, 1).
+
+Recipe (shared by every family):
+  * ``rng = numpy.random.default_rng(seed)``; draws happen in a fixed order:
+    token ids, slot permutation, cached K/V, new K/V, queries.
+  * values ~ N(0, 1) drawn in float32 and rounded to bf16 round-to-nearest-
+    even by ``bf16_round`` below.
+  * slot ids: a seeded random permutation of ``[0, num_slots)``, handed out
+    in order of first use (shared prefix tokens first, then each request's
+    private tokens in request order, then the step's new tokens).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional
+
+import numpy as np
+
+# -------------------------------------------------------------------------
+# bf16 helpers (bit manipulation only)
+# -------------------------------------------------------------------------
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bits (uint16), round to nearest, ties to even."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_to_f32(h: np.ndarray) -> np.ndarray:
+    """bf16 bits (uint16) -> float32, exact."""
+    return (np.ascontiguousarray(h, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def randn_bf16(rng: np.random.Generator, shape, chunk: int = 1 << 24) -> np.ndarray:
+    """N(0,1) values rounded to bf16, drawn in float32 in fixed-size chunks."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        out[s:e] = bf16_round(rng.standard_normal(e - s, dtype=np.float32))
+    return out.reshape(shape)
+
+
+# -------------------------------------------------------------------------
+# Problem description
+# -------------------------------------------------------------------------
+
+
+@dataclasses.dataclass
+class Problem:
+    """One batch of the slot-indexed attention path.
+
+    Pool rows ``cached_slots`` hold ``cached_k/v`` before the step; the step
+    first stores ``new_k/v`` at ``new_slots`` and then runs attention:
+      * extend rows: request ``ext_req_idx[b]`` (a row of ``req_to_token``)
+        has ``ext_prefix_len[b]`` cached tokens and ``ext_extend_len[b]``
+        new ones, queries packed along ``qo_indptr``;
+      * decode rows: request ``dec_req_idx[b]`` has ``dec_seq_len[b]``
+        tokens including its new one, one query each.
+    """
+
+    name: str
+    hq: int
+    hkv: int
+    d: int
+    num_slots: int
+    req_to_token: np.ndarray          # int32 [R, stride]
+    tokens: List[np.ndarray]          # int64 token ids per req_to_token row
+    cached_slots: np.ndarray          # int32 [Nc]
+    cached_k: np.ndarray              # uint16 (bf16) [Nc, hkv, d]
+    cached_v: np.ndarray
+    new_slots: np.ndarray             # int32 [Nn]
+    new_k: np.ndarray                 # uint16 [Nn, hkv, d]
+    new_v: np.ndarray
+    ext_req_idx: np.ndarray           # int32 [Be]
+    ext_prefix_len: np.ndarray        # int32 [Be]
+    ext_extend_len: np.ndarray        # int32 [Be]
+    qo_indptr: np.ndarray             # int32 [Be + 1]
+    q_ext: np.ndarray                 # uint16 [sum E, hq, d]
+    dec_req_idx: np.ndarray           # int32 [Bd]
+    dec_seq_len: np.ndarray           # int32 [Bd]
+    q_dec: np.ndarray                 # uint16 [Bd, hq, d]
+    seed: int = 0
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / float(np.sqrt(self.d))
+
+    @property
+    def rtt_stride(self) -> int:
+        return int(self.req_to_token.shape[1])
+
+    @property
+    def kv_row_bytes(self) -> int:
+        """Bytes of K plus V for one token (all kv heads)."""
+        return 2 * self.hkv * self.d * 2
+
+    def decode_unique_tokens(self) -> int:
+        """Distinct pool slots that the decode rows read."""
+        if len(self.dec_req_idx) == 0:
+            return 0
+        s = set()
+        for r, L in zip(self.dec_req_idx, self.dec_seq_len):
+            s.update(self.req_to_token[r, :L].tolist())
+        return len(s)
+
+    def decode_dense_tokens(self) -> int:
+        return int(np.sum(self.dec_seq_len, dtype=np.int64))
+
+    def extend_flops(self) -> int:
+        """4*d per unmasked (query, key, q-head) triple: 2*d for QK^T, 2*d for PV."""
+        pairs = 0
+        for P, E in zip(self.ext_prefix_len.tolist(), self.ext_extend_len.tolist()):
+            pairs += E * P + E * (E + 1) // 2
+        return 4 * self.d * self.hq * pairs
+
+    def decode_flops(self) -> int:
+        return 4 * self.d * self.hq * self.decode_dense_tokens()
+
+
+class _SlotSource:
+    """Hands out a seeded permutation of [0, num_slots) in order of use."""
+
+    def __init__(self, rng: np.random.Generator, num_slots: int):
+        self.perm = rng.permutation(num_slots).astype(np.int32)
+        self.next = 0
+
+    def take(self, n: int) -> np.ndarray:
+        if self.next + n > len(self.perm):
+            raise ValueError("workload needs more slots than the pool holds")
+        out = self.perm[self.next:self.next + n]
+        self.next += n
+        return out
+
+
+def _tokens(rng: np.random.Generator, n: int, lo: int) -> np.ndarray:
+    """n distinct-looking token ids from a disjoint range starting at lo."""
+    return (lo + rng.permutation(n)).astype(np.int64)
+
+
+def _empty_i32():
+    return np.zeros(0, dtype=np.int32)
+
+
+def _finish(name, seed, rng, hq, hkv, d, num_slots, rows, cached_slots, new_slots,
+            ext, dec) -> Problem:
+    """Draw values and assemble a Problem.
+
+    rows: list of (token ids int64, slot ids int32) per req_to_token row.
+    ext:  list of (row, prefix_len, extend_len).
+    dec:  list of (row, seq_len).
+    """
+    stride = max(len(s) for _, s in rows)
+    stride = (stride + 15) // 16 * 16
+    rtt = np.full((len(rows), stride), -1, dtype=np.int32)
+    for i, (_, s) in enumerate(rows):
+        rtt[i, :len(s)] = s
+    cached_k = randn_bf16(rng, (len(cached_slots), hkv, d))
+    cached_v = randn_bf16(rng, (len(cached_slots), hkv, d))
+    new_k = randn_bf16(rng, (len(new_slots), hkv, d))
+    new_v = randn_bf16(rng, (len(new_slots), hkv, d))
+    ext_req = np.array([e[0] for e in ext], dtype=np.int32) if ext else _empty_i32()
+    ext_P = np.array([e[1] for e in ext], dtype=np.int32) if ext else _empty_i32()
+    ext_E = np.array([e[2] for e in ext], dtype=np.int32) if ext else _empty_i32()
+    qo = np.zeros(len(ext) + 1, dtype=np.int32)
+    if ext:
+        qo[1:] = np.cumsum(ext_E)
+    q_ext = randn_bf16(rng, (int(qo[-1]), hq, d))
+    dec_req = np.array([x[0] for x in dec], dtype=np.int32) if dec else _empty_i32()
+    dec_L = np.array([x[1] for x in dec], dtype=np.int32) if dec else _empty_i32()
+    q_dec = randn_bf16(rng, (len(dec), hq, d))
+    return Problem(name=name, hq=hq, hkv=hkv, d=d, num_slots=num_slots,
+                   req_to_token=rtt, tokens=[t for t, _ in rows],
+                   cached_slots=np.asarray(cached_slots, dtype=np.int32),
+                   cached_k=cached_k, cached_v=cached_v,
+                   new_slots=np.asarray(new_slots, dtype=np.int32), new_k=new_k, new_v=new_v,
+                   ext_req_idx=ext_req, ext_prefix_len=ext_P, ext_extend_len=ext_E,
+                   qo_indptr=qo, q_ext=q_ext, dec_req_idx=dec_req, dec_seq_len=dec_L,
+                   q_dec=q_dec, seed=seed)
+
+
+# -------------------------------------------------------------------------
+# Workload families (defaults = the full-size configurations)
+# -------------------------------------------------------------------------
+
+
+def tiny_extend(seed: int = 1001, hq: int = 4, hkv: int = 4, d: int = 64, batch: int = 4,
+                prefix: int = 64, extend: int = 16, num_slots: int = 512) -> Problem:
+    """Requests sharing one cached prefix, each extending it causally.
+
+    Full size: 4 q heads = 4 kv heads, head_dim 64, 4 requests on one
+    64-token prefix, 16 new tokens each, 512-slot pool.
+    """
+    rng = np.random.default_rng(seed)
+    shared_tok = _tokens(rng, prefix, 1_000_000)
+    new_tok = [_tokens(rng, extend, 2_000_000 + 10_000 * b) for b in range(batch)]
+    src = _SlotSource(rng, num_slots)
+    shared_slots = src.take(prefix)
+    rows, new_slots = [], []
+    for b in range(batch):
+        s_new = src.take(extend)
+        new_slots.append(s_new)
+        rows.append((np.concatenate([shared_tok, new_tok[b]]), np.concatenate([shared_slots, s_new])))
+    ext = [(b, prefix, extend) for b in range(batch)]
+    return _finish("tiny_extend", seed, rng, hq, hkv, d, num_slots, rows, shared_slots,
+                   np.concatenate(new_slots), ext, [])
+
+
+def few_shot_decode(seed: int = 1002, hq: int = 32, hkv: int = 32, d: int = 128, batch: int = 64,
+                    shared: int = 1024, private: int = 256, num_slots: int = 2 * 1024 * 1024) -> Problem:
+    """Few-shot batch: one shared example prefix, a private question each, one decode token.
+
+    Full size: Llama-2-7B attention shape (32 = 32 heads, head_dim 128),
+    64 requests of 1024 shared + 256 private + 1 new token, 2M-slot pool.
+    """
+    rng = np.random.default_rng(seed)
+    shared_tok = _tokens(rng, shared, 1_000_000)
+    priv_tok = [_tokens(rng, private + 1, 3_000_000 + 100_000 * b) for b in range(batch)]
+    src = _SlotSource(rng, num_slots)
+    shared_slots = src.take(shared)
+    priv_slots = [src.take(private) for _ in range(batch)]
+    new_slots = src.take(batch)
+    rows = []
+    for b in range(batch):
+        rows.append((np.concatenate([shared_tok, priv_tok[b]]),
+                     np.concatenate([shared_slots, priv_slots[b], new_slots[b:b + 1]])))
+    cached = np.concatenate([shared_slots] + priv_slots)
+    dec = [(b, shared + private + 1) for b in range(batch)]
+    return _finish("few_shot_decode", seed, rng, hq, hkv, d, num_slots, rows, cached, new_slots, [], dec)
+
+
+def cached_prefix_extend(seed: int = 1003, hq: int = 32, hkv: int = 8, d: int = 128,
+                         n_prefix: int = 8, per_prefix: int = 4, prefix: int = 2048, extend: int = 512,
+                         num_slots: int = 1024 * 1024) -> Problem:
+    """Requests extending cached prefixes (several requests per prefix).
+
+    Full size: Llama-3-8B GQA (32 q / 8 kv heads, head_dim 128), 8 distinct
+    2048-token prefixes with 4 requests each, 512 new causal tokens per request.
+    """
+    rng = np.random.default_rng(seed)
+    pre_tok = [_tokens(rng, prefix, 1_000_000 + 100_000 * i) for i in range(n_prefix)]
+    new_tok = [_tokens(rng, extend, 50_000_000 + 100_000 * b) for b in range(n_prefix * per_prefix)]
+    src = _SlotSource(rng, num_slots)
+    pre_slots = [src.take(prefix) for _ in range(n_prefix)]
+    rows, new_slots, ext = [], [], []
+    for b in range(n_prefix * per_prefix):
+        p = b // per_prefix
+        s_new = src.take(extend)
+        new_slots.append(s_new)
+        rows.append((np.concatenate([pre_tok[p], new_tok[b]]), np.concatenate([pre_slots[p], s_new])))
+        ext.append((b, prefix, extend))
+    return _finish("cached_prefix_extend", seed, rng, hq, hkv, d, num_slots, rows,
+                   np.concatenate(pre_slots), np.concatenate(new_slots), ext, [])
+
+
+def tree_of_thought_decode(seed: int = 1004, hq: int = 32, hkv: int = 8, d: int = 128, depth: int = 4,
+                           fanout: int = 4, edge: int = 256, num_slots: int = 1024 * 1024) -> Problem:
+    """Branching program: a full tree of thoughts, one decode token per leaf.
+
+    Full size: GQA 32/8, head_dim 128, depth 4, fanout 4, 256 tokens per edge
+    (340 edges, 256 leaves with 1024-token contexts), shared ancestors' KV
+    stored once.
+    """
+    rng = np.random.default_rng(seed)
+    # edges in BFS order; edge e at level l (1-based) is child (e's index) of its parent
+    levels = []
+    n_edges = 0
+    for lvl in range(1, depth + 1):
+        cnt = fanout ** lvl
+        levels.append(list(range(n_edges, n_edges + cnt)))
+        n_edges += cnt
+    edge_tok = [_tokens(rng, edge, 1_000_000 + 1_000 * e) for e in range(n_edges)]
+    n_leaves = fanout ** depth
+    leaf_new_tok = [_tokens(rng, 1, 900_000_000 + b) for b in range(n_leaves)]
+    src = _SlotSource(rng, num_slots)
+    edge_slots = [src.take(edge) for _ in range(n_edges)]
+    new_slots = src.take(n_leaves)
+    rows, dec = [], []
+    for leaf in range(n_leaves):
+        path = []
+        idx = leaf
+        for lvl in range(depth - 1, -1, -1):
+            path.append(levels[lvl][idx])
+            idx //= fanout
+        path.reverse()
+        toks = np.concatenate([edge_tok[e] for e in path] + [leaf_new_tok[leaf]])
+        sl = np.concatenate([edge_slots[e] for e in path] + [new_slots[leaf:leaf + 1]])
+        rows.append((toks, sl))
+        dec.append((leaf, depth * edge + 1))
+    return _finish("tree_of_thought_decode", seed, rng, hq, hkv, d, num_slots, rows,
+                   np.concatenate(edge_slots), new_slots, [], dec)
+
+
+def mixed_chat(seed: int = 1005, hq: int = 64, hkv: int = 8, d: int = 128, n_dec: int = 16,
+               system: int = 8192, history: int = 24576, n_ext: int = 16, ext_prefix: int = 4096,
+               ext_new: int = 1024, num_slots: int = 1024 * 1024) -> Problem:
+    """Long multi-turn chat: decode rows on long shared-system-prompt contexts
+    plus concurrent extend rows on their own cached prefixes.
+
+    Full size: Llama-70B attention shape (64 q / 8 kv heads, head_dim 128);
+    16 decode requests of 8192 shared + 24576 private + 1 new tokens, 16
+    extend requests of 1024 new tokens on distinct 4096-token cached
+    prefixes, 1M-slot pool.
+    """
+    rng = np.random.default_rng(seed)
+    sys_tok = _tokens(rng, system, 1_000_000)
+    hist_tok = [_tokens(rng, history + 1, 10_000_000 + 100_000 * b) for b in range(n_dec)]
+    epre_tok = [_tokens(rng, ext_prefix, 100_000_000 + 10_000 * b) for b in range(n_ext)]
+    enew_tok = [_tokens(rng, ext_new, 200_000_000 + 10_000 * b) for b in range(n_ext)]
+    src = _SlotSource(rng, num_slots)
+    sys_slots = src.take(system)
+    hist_slots = [src.take(history) for _ in range(n_dec)]
+    epre_slots = [src.take(ext_prefix) for _ in range(n_ext)]
+    dec_new = src.take(n_dec)
+    ext_new_slots = [src.take(ext_new) for _ in range(n_ext)]
+    rows, dec, ext = [], [], []
+    for b in range(n_dec):
+        rows.append((np.concatenate([sys_tok, hist_tok[b]]),
+                     np.concatenate([sys_slots, hist_slots[b], dec_new[b:b + 1]])))
+        dec.append((b, system + history + 1))
+    for b in range(n_ext):
+        rows.append((np.concatenate([epre_tok[b], enew_tok[b]]),
+                     np.concatenate([epre_slots[b], ext_new_slots[b]])))
+        ext.append((n_dec + b, ext_prefix, ext_new))
+    cached = np.concatenate([sys_slots] + hist_slots + epre_slots)
+    new = np.concatenate([dec_new] + ext_new_slots)
+    return _finish("mixed_chat", seed, rng, hq, hkv, d, num_slots, rows, cached, new, ext, dec)
+
+
+def ragged(seed: int, hq: int, hkv: int, d: int, n_groups: int, per_group: int, shared_max: int,
+           private_max: int, extend_max: int, decode: bool, num_slots: int,
+           allow_empty_prefix: bool = True) -> Problem:
+    """Random ragged batch: groups of requests sharing a random-length prefix,
+    random private parts, either one decode token or a random extend each."""
+    rng = np.random.default_rng(seed)
+    src_tok = 1_000_000
+    g_len = rng.integers(0 if allow_empty_prefix else 1, shared_max + 1, size=n_groups)
+    B = n_groups * per_group
+    p_len = rng.integers(0, private_max + 1, size=B)
+    e_len = rng.integers(1, extend_max + 1, size=B)
+    if decode:
+        e_len = np.ones(B, dtype=np.int64)
+    shared_tok = [_tokens(rng, int(n), src_tok + 1_000_000 * i) for i, n in enumerate(g_len)]
+    own_tok = [_tokens(rng, int(p_len[b] + e_len[b]), 500_000_000 + 100_000 * b) for b in range(B)]
+    src = _SlotSource(rng, num_slots)
+    shared_slots = [src.take(int(n)) for n in g_len]
+    priv_slots = [src.take(int(n)) for n in p_len]
+    new_slots = [src.take(int(n)) for n in e_len]
+    rows, ext, dec = [], [], []
+    for b in range(B):
+        g = b // per_group
+        rows.append((np.concatenate([shared_tok[g], own_tok[b]]),
+                     np.concatenate([shared_slots[g], priv_slots[b], new_slots[b]])))
+        P = int(g_len[g] + p_len[b])
+        if decode:
+            dec.append((b, P + 1))
+        else:
+            ext.append((b, P, int(e_len[b])))
+    cached = np.concatenate(shared_slots + priv_slots) if B else _empty_i32()
+    return _finish("ragged", seed, rng, hq, hkv, d, num_slots, rows, cached,
+                   np.concatenate(new_slots), ext, dec)
+
+
+FULL_SIZE = {
+    "tiny_extend": tiny_extend,
+    "few_shot_decode": few_shot_decode,
+    "cached_prefix_extend": cached_prefix_extend,
+    "tree_of_thought_decode": tree_of_thought_decode,
+    "mixed_chat": mixed_chat,
+}
+
+
+def token_stream(rng_seed: int, n: int, lo: int = 0, hi: int = 1 << 40) -> np.ndarray:
+    """Uniform int64 token ids (for radix-tree operation sequences)."""
+    rng = np.random.default_rng(rng_seed)
+    return rng.integers(lo, hi, size=n, dtype=np.int64)
