@@ -1,0 +1,509 @@
+"""Benchmark of the prefix-shared KV attention path on one or more GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole path over one batch of synthetic input: the
+KV store of the step's new tokens, then the attention the workload needs
+(decode with its decode plan, and/or extend).  Inputs are resident in HBM
+before timing starts; a 256 MiB buffer is written between timed steps so that
+no KV survives in L2 (129 MB); each step is timed with CUDA events on the
+launching stream.  The decode plan is built once, before timing, from the
+host copy of req_to_token (the sharing structure is fixed for the batch).
+
+Workloads (default: few_shot_decode, the configuration the headline metric
+is quoted on):
+  few_shot_decode         64 x (1024 shared + 256 private + 1), MHA 32x128, 2M slots
+  tree_of_thought_decode  256 leaves of a depth-4 fanout-4 tree, GQA 32/8
+  cached_prefix_extend    32 x (2048 cached + 512 new), GQA 32/8
+  mixed_chat              16 decode x 32k + 16 extend x (4096 + 1024), 64/8
+  tiny_extend             4 x (64 cached + 16 new), 4 heads, head_dim 64
+
+One JSON line is printed by rank 0.  Under torchrun every rank runs the same
+workload on its own GPU (independent replicas, no collective on the data
+path); value = work of all ranks / the slowest rank's time.
+
+--impl reference times the fp64 oracle (the plain CPU definition) on the host
+cores, on a bounded sample of the same workload, in the same units.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from prefix_shared_kv_radixattention_gb300 import inputs  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+DECODE_KINDS = ("few_shot_decode", "tree_of_thought_decode")
+EXTEND_KINDS = ("cached_prefix_extend", "tiny_extend")
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        time.sleep(0.15)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, busy_from: int = 0):
+        rows = []
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), hw=parts[5], hwt=parts[6],
+                                 swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+
+class GpuStep:
+    """Device state of one workload and the step that runs the path on it."""
+
+    def __init__(self, prob: inputs.Problem, torch, rx):
+        self.torch, self.rx, self.prob = torch, rx, prob
+        dev = "cuda"
+        p = prob
+
+        def bf(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+        def i32(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+        self.k_pool = torch.empty((p.num_slots, p.hkv, p.d), dtype=torch.bfloat16, device=dev)
+        self.v_pool = torch.empty_like(self.k_pool)
+        idx = torch.from_numpy(p.cached_slots.astype(np.int64)).to(dev)
+        for pool, src in ((self.k_pool, p.cached_k), (self.v_pool, p.cached_v)):
+            for s in range(0, len(idx), 1 << 16):
+                pool.index_copy_(0, idx[s:s + (1 << 16)], bf(src[s:s + (1 << 16)]))
+        self.rtt = i32(p.req_to_token)
+        self.k_new, self.v_new, self.slots = bf(p.new_k), bf(p.new_v), i32(p.new_slots)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.has_dec = len(p.dec_req_idx) > 0
+        self.has_ext = len(p.ext_req_idx) > 0
+        self.launches = 1
+        if self.has_dec:
+            B = len(p.dec_req_idx)
+            self.q_dec = bf(p.q_dec)
+            self.o_dec = torch.empty_like(self.q_dec)
+            self.dec_req, self.dec_len = i32(p.dec_req_idx), i32(p.dec_seq_len)
+            self.max_len = int(p.dec_seq_len.max())
+            buf, info = rx.rx_decode_plan_build(p.req_to_token, p.dec_req_idx, p.dec_seq_len, p.hq, p.hkv)
+            self.plan_info = info
+            self.plan = rx.plan_to_device(buf, info, B)
+            ws = rx.rx_attn_decode_workspace(B, p.hq, p.hkv, p.d, self.max_len, self.plan)
+            self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev) if ws else None
+            self.launches += 1 + (1 if info.max_parts > 1 else 0)
+        if self.has_ext:
+            self.q_ext = bf(p.q_ext)
+            self.o_ext = torch.empty_like(self.q_ext)
+            self.qo, self.ext_req = i32(p.qo_indptr), i32(p.ext_req_idx)
+            self.ext_P, self.ext_E = i32(p.ext_prefix_len), i32(p.ext_extend_len)
+            self.max_E = int(p.ext_extend_len.max())
+            self.launches += 1
+
+    def kv_store(self):
+        self.rx.rx_kv_store(self.k_pool, self.v_pool, self.k_new, self.v_new, self.slots, self.status)
+
+    def decode(self):
+        p = self.prob
+        self.rx.rx_attn_decode(self.k_pool, self.v_pool, self.q_dec, self.o_dec, None, self.dec_req,
+                               self.dec_len, self.rtt, self.max_len, p.sm_scale, self.plan, self.ws,
+                               self.status)
+
+    def extend(self):
+        p = self.prob
+        self.rx.rx_attn_extend(self.k_pool, self.v_pool, self.q_ext, self.o_ext, None, self.qo,
+                               self.ext_req, self.ext_P, self.ext_E, self.rtt, self.max_E, p.sm_scale,
+                               self.status)
+
+    def step(self, marks=None):
+        """The whole path; ``marks`` (dict of event pairs) brackets the parts."""
+        if marks:
+            marks["store"][0].record()
+        self.kv_store()
+        if marks:
+            marks["store"][1].record()
+        if self.has_ext:
+            if marks:
+                marks["extend"][0].record()
+            self.extend()
+            if marks:
+                marks["extend"][1].record()
+        if self.has_dec:
+            if marks:
+                marks["decode"][0].record()
+            self.decode()
+            if marks:
+                marks["decode"][1].record()
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    prob = inputs.FULL_SIZE[args.workload]()
+    st = GpuStep(prob, torch, rx)
+    flush = torch.empty(L2_FLUSH_BYTES // 2, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        st.step()
+    torch.cuda.synchronize()
+    if int(st.status.item()) != 0:
+        raise RuntimeError(f"device status {int(st.status.item())} after warm-up")
+
+    E = torch.cuda.Event
+    parts = ["store"] + (["extend"] if st.has_ext else []) + (["decode"] if st.has_dec else [])
+    marks = [{k: (E(enable_timing=True), E(enable_timing=True)) for k in parts}
+             for _ in range(args.steps)]
+    steps_ev = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            steps_ev[i][0].record()
+            st.step(marks[i])
+            steps_ev[i][1].record()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in steps_ev]
+    part_ms = {k: [m[k][0].elapsed_time(m[k][1]) for m in marks] for k in parts}
+    tot_ms = float(sum(step_ms))
+    if dist:
+        t = torch.tensor([tot_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    ms_per_step = tot_ms / args.steps
+
+    # end to end through the public API: pinned host inputs in, result out
+    e2e = run_e2e(st, torch, rx, args.steps, flush)
+
+    if dist:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    hbm, tflops, tflops_sus, peak_src = measured_peaks()
+    B_dec = len(prob.dec_req_idx)
+    flops_ext = prob.extend_flops()
+    kv_row = prob.kv_row_bytes
+    out = {}
+    if st.has_dec:
+        toks = B_dec * world * args.steps
+        value = toks / (tot_ms / 1e3)
+        metric, unit = "decode tok/s", "tok/s"
+        dec_ms = statistics.mean(part_ms["decode"])
+        uniq_bytes = st.plan_info.tokens_read * kv_row
+        achieved = uniq_bytes / (dec_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": None,
+                "kernel": "rx_attn_decode (attn_rows_kernel + merge_kernel)",
+                "algorithmic_bytes_per_launch": int(uniq_bytes), "launch_ms": round(dec_ms, 5),
+                "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)",
+                "frac_of_8000": round(achieved / 8000.0, 4)}
+        out["decode"] = {"tok_s": B_dec / (dec_ms / 1e3), "hbm_gbs_unique": achieved,
+                         "unique_kv_bytes": int(uniq_bytes),
+                         "dense_kv_bytes": int(prob.decode_dense_tokens() * kv_row),
+                         "ms": dec_ms, "segments": st.plan_info.n_segments,
+                         "work_items": st.plan_info.n_items, "kv_chunk": st.plan_info.kv_chunk}
+    if st.has_ext:
+        ext_ms = statistics.mean(part_ms["extend"])
+        tf = flops_ext / (ext_ms / 1e3) / 1e12
+        out["extend"] = {"tflops": tf, "ms": ext_ms, "tok_s": float(np.sum(prob.ext_extend_len)) / (ext_ms / 1e3),
+                         "flops": int(flops_ext), "frac_of_burst": tf / tflops}
+        if not st.has_dec:
+            metric, unit = "extend TFLOPS", "TFLOP/s"
+            value = flops_ext * world * args.steps / (tot_ms / 1e3) / 1e12
+            roof = {"bound": "tensor", "achieved": round(tf, 2), "peak": tflops, "unit": "TFLOP/s",
+                    "frac": round(tf / tflops, 4), "traffic": None, "kernel": "rx_attn_extend",
+                    "algorithmic_flops_per_launch": int(flops_ext), "launch_ms": round(ext_ms, 5),
+                    "peak_source": f"{peak_src} bf16_tflops (burst)"}
+    out["kv_store"] = {"ms": statistics.mean(part_ms["store"]),
+                       "gbs": 2 * len(prob.new_slots) * kv_row / (statistics.mean(part_ms["store"]) / 1e3) / 1e9}
+    line = {
+        "metric": f"prefix-shared attn: {metric}", "value": round(value, 3), "unit": unit,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random slot permutation)",
+        "config": workload_config(prob, args.workload, world),
+        "roofline": roof, "e2e": e2e, "gpu_launches": st.launches * args.steps,
+        "clocks": clk.summary(), "parts": out, "wall_s_timed_loop": round(t_wall, 3),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(prob, args.workload, budget_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(st, torch, rx, steps, flush):
+    """Per step: pinned host -> device copies of the step's inputs, the path,
+    device -> host copy of its outputs; timed with events on the stream."""
+    p = st.prob
+    s = torch.cuda.current_stream()
+    h_in = [st.k_new.cpu().pin_memory(), st.v_new.cpu().pin_memory(), st.slots.cpu().pin_memory()]
+    d_in = [st.k_new, st.v_new, st.slots]
+    outs = []
+    if st.has_ext:
+        h_in.append(st.q_ext.cpu().pin_memory())
+        d_in.append(st.q_ext)
+        outs.append(st.o_ext)
+    if st.has_dec:
+        h_in.append(st.q_dec.cpu().pin_memory())
+        d_in.append(st.q_dec)
+        outs.append(st.o_dec)
+    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    n = max(3, min(steps, 200))
+    E = torch.cuda.Event
+    ev = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        ev[i][0].record()
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        st.step()
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / n
+    h2d = sum(h.numel() * h.element_size() for h in h_in)
+    d2h = sum(h.numel() * h.element_size() for h in h_out)
+    if st.has_dec:
+        val, unit = len(p.dec_req_idx) / (ms / 1e3), "tok/s"
+    else:
+        val, unit = p.extend_flops() / (ms / 1e3) / 1e12, "TFLOP/s"
+    return {"value": round(val, 3), "unit": unit, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 5), "steps": n}
+
+
+def workload_config(prob, name, world):
+    cfg = {"workload": name, "hq": prob.hq, "hkv": prob.hkv, "head_dim": prob.d,
+           "pool_slots": prob.num_slots, "decode_requests": int(len(prob.dec_req_idx)),
+           "extend_requests": int(len(prob.ext_req_idx)),
+           "l2": "256 MiB buffer written between timed steps",
+           "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+    if len(prob.dec_req_idx):
+        cfg["decode_context"] = int(prob.dec_seq_len.max())
+    if len(prob.ext_req_idx):
+        cfg["extend_prefix"] = int(prob.ext_prefix_len.max())
+        cfg["extend_new"] = int(prob.ext_extend_len.max())
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+
+def _oracle_pools(prob):
+    import oracle
+    slots = np.concatenate([prob.cached_slots, prob.new_slots])
+    uniq = np.unique(slots)
+    kp = np.zeros((len(uniq), prob.hkv, prob.d), np.uint16)
+    vp = np.zeros_like(kp)
+    pos = np.searchsorted(uniq, prob.cached_slots)
+    kp[pos], vp[pos] = prob.cached_k, prob.cached_v
+    oracle.kv_store(kp, vp, prob.new_k, prob.new_v, np.searchsorted(uniq, prob.new_slots).astype(np.int32))
+    rtt = prob.req_to_token
+    loc = np.minimum(np.searchsorted(uniq, np.maximum(rtt, 0)), len(uniq) - 1)
+    rtt_c = np.where((rtt >= 0) & (uniq[loc] == rtt), loc, -1).astype(np.int32)
+    return kp, vp, rtt_c
+
+
+def oracle_sample(prob, rows_dec, rows_ext_tokens, threads):
+    """One bounded oracle pass: the first rows_dec decode rows and the last
+    rows_ext_tokens extend tokens of each extend request.  Returns
+    (seconds, decode rows done, extend flops done)."""
+    import oracle
+    kp, vp, rtt = _oracle_pools(prob)
+    t0 = time.perf_counter()
+    flops = 0
+    nd = 0
+    if len(prob.dec_req_idx) and rows_dec:
+        nd = min(rows_dec, len(prob.dec_req_idx))
+        oracle.decode(prob.q_dec[:nd], kp, vp, rtt, prob.dec_req_idx[:nd], prob.dec_seq_len[:nd],
+                      prob.sm_scale, n_threads=threads)
+    if len(prob.ext_req_idx) and rows_ext_tokens:
+        q_rows, kend, qi = [], [], []
+        for b in range(len(prob.ext_req_idx)):
+            E, P = int(prob.ext_extend_len[b]), int(prob.ext_prefix_len[b])
+            for i in range(max(0, E - rows_ext_tokens), E):
+                qi.append(int(prob.qo_indptr[b]) + i)
+                q_rows.append(int(prob.ext_req_idx[b]))
+                kend.append(P + i + 1)
+        kend = np.array(kend, np.int32)
+        oracle.attention(prob.q_ext[qi], kp, vp, rtt, np.array(q_rows, np.int32), np.zeros_like(kend),
+                         kend, prob.sm_scale, n_threads=threads)
+        flops = int(4 * prob.d * prob.hq * kend.astype(np.int64).sum())
+    return time.perf_counter() - t0, nd, flops
+
+
+def cpu_baseline(prob, name, budget_s=15.0):
+    threads = cores()
+    if len(prob.dec_req_idx):
+        rows, _ = 1, 0
+        sec, nd, _ = oracle_sample(prob, 1, 0, threads)
+        rows = int(max(1, min(len(prob.dec_req_idx), budget_s / max(sec, 1e-3))))
+        sec, nd, _ = oracle_sample(prob, rows, 0, threads)
+        return {"value": round(nd / sec, 3), "unit": "tok/s", "cores": threads, "kind": "oracle",
+                "sample": f"{nd} of {len(prob.dec_req_idx)} decode rows of {name}, all heads, fp64",
+                "seconds": round(sec, 3)}
+    sec, _, fl = oracle_sample(prob, 0, 1, threads)
+    toks = int(max(1, min(int(prob.ext_extend_len.min()), budget_s / max(sec, 1e-3))))
+    sec, _, fl = oracle_sample(prob, 0, toks, threads)
+    return {"value": round(fl / sec / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"last {toks} extend tokens of each of {len(prob.ext_req_idx)} requests of {name}, fp64",
+            "seconds": round(sec, 3)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    prob = inputs.FULL_SIZE[args.workload]()
+    threads = cores()
+    has_dec = len(prob.dec_req_idx) > 0
+    # a step = a bounded sample of the workload, sized to a few seconds
+    sec1, _, _ = oracle_sample(prob, 1 if has_dec else 0, 0 if has_dec else 1, threads)
+    budget = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
+    n = int(max(1, budget / max(sec1, 1e-3)))
+    secs, work = [], []
+    for i in range(args.warmup + args.steps):
+        if has_dec:
+            s, nd, _ = oracle_sample(prob, min(n, len(prob.dec_req_idx)), 0, threads)
+            w = nd
+        else:
+            s, _, fl = oracle_sample(prob, 0, min(n, int(prob.ext_extend_len.min())), threads)
+            w = fl
+        if i >= args.warmup:
+            secs.append(s)
+            work.append(w)
+    tot = sum(secs)
+    if has_dec:
+        value, unit, metric = sum(work) / tot, "tok/s", "decode tok/s"
+        sample = f"{work[0]} of {len(prob.dec_req_idx)} decode rows per step, all heads, fp64"
+    else:
+        value, unit, metric = sum(work) / tot / 1e12, "TFLOP/s", "extend TFLOPS"
+        sample = f"last {min(n, int(prob.ext_extend_len.min()))} extend tokens per request per step, fp64"
+    line = {"impl": "reference", "metric": f"prefix-shared attn: {metric}", "value": round(value, 6),
+            "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16, random slot permutation)",
+            "config": workload_config(prob, args.workload, world),
+            "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="few_shot_decode", choices=sorted(inputs.FULL_SIZE))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

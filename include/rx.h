@@ -1,0 +1,292 @@
+/*
+ * rx.h -- C ABI of the prefix-shared KV attention library (librx.so).
+ *
+ * What the library does.  "SGLang: Efficient Execution of Structured Language
+ * Model Programs" (unite.ai, es), section "Introducción a SGLang", describes
+ * RadixAttention: the KV cache of finished generation calls is kept, as an
+ * LRU cache inside a radix tree with matching, insertion and eviction, so that
+ * calls sharing a prefix reuse its KV instead of recomputing it.  This library
+ * is the data-parallel hot path under that cache:
+ *
+ *   - a token-slot KV pool on the GPU: K and V are separate bf16 arrays of
+ *     shape [num_slots, num_kv_heads, head_dim], row-major, one row per token;
+ *   - per-request slot lists (req_to_token): row r of an int32 matrix with
+ *     leading dimension rtt_stride lists the pool slots of request r's tokens
+ *     in position order; requests that share a prefix list the same slots;
+ *   - rx_kv_store: scatter of new K/V rows into the pool;
+ *   - rx_attn_extend: new tokens attend causally to their cached prefix plus
+ *     themselves;
+ *   - rx_attn_decode: one query per request over its whole slotted context,
+ *     reading KV shared by several requests once per group when a decode plan
+ *     says which requests share which positions;
+ *   - a host radix tree (rx_match_prefix / rx_insert / rx_evict_lru) and a
+ *     slot free list, which only produce slot ids and prefix lengths.
+ *
+ * Attention definition (all attention entry points).  For a query row of
+ * request b at absolute position p, q-head h, with G = num_q_heads /
+ * num_kv_heads and kv-head g = h / G:
+ *     s_j = sm_scale * sum_c q[c] * K[req_to_token[b][j]][g][c],  j = 0 .. p
+ *     o   = sum_j softmax(s)_j * V[req_to_token[b][j]][g]
+ *     lse = log(sum_j exp(s_j))            (natural log)
+ * Inputs are bf16; products, sums and the softmax run in fp32; o is rounded
+ * to bf16 (round to nearest even).  The causal mask is the "j <= p" bound.
+ *
+ * Conventions.
+ *   - Every function returns an int status: RX_OK (0) or a negative RX_ERR_*.
+ *     rx_last_error() returns a thread-local message for the last failure.
+ *   - No exception, abort or device trap crosses this ABI.
+ *   - "device" pointers are CUDA global memory on the current device; "host"
+ *     pointers are ordinary process memory.  The caller owns every buffer;
+ *     the library allocates no device memory.
+ *   - GPU entry points are asynchronous on `stream` (a cudaStream_t passed as
+ *     void*, NULL = legacy default stream) and return after validation and
+ *     launch.  Errors found by kernels (an out-of-range slot id or length) are OR-ed as
+ *     RX_DEV_* bits into *dev_status, a device int32 the caller zeroes; a row
+ *     with a bad slot reads as zeros and nothing outside the buffers is
+ *     touched.  dev_status may be NULL (bad slots are then skipped silently).
+ *   - Host tree functions are not thread-safe per tree; distinct trees are
+ *     independent.
+ */
+#ifndef RX_H
+#define RX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status ------------------------------------------------------------ */
+
+#define RX_OK 0
+#define RX_ERR_INVALID (-1)     /* null pointer, bad size or shape            */
+#define RX_ERR_CAPACITY (-2)    /* caller's output array too small            */
+#define RX_ERR_NOMEM (-3)       /* host allocation failed                      */
+#define RX_ERR_NOT_ENOUGH (-4)  /* fewer slots/tokens available than asked     */
+#define RX_ERR_CUDA (-5)        /* a CUDA runtime call failed                  */
+#define RX_ERR_UNSUPPORTED (-6) /* shape the kernels are not built for         */
+
+#define RX_DEV_BAD_SLOT 1       /* a kernel met a slot id outside the pool     */
+#define RX_DEV_BAD_LEN 2        /* a device length exceeded its host bound or  
+                                   the req_to_token stride; rows left unwritten */
+
+/* Message for the last failed call on this thread ("" if none). */
+const char *rx_last_error(void);
+
+/* ABI version (bumped on any signature change). */
+int rx_version(void);
+
+/* ---- radix tree (host) --------------------------------------------------
+ * Source: "SGLang: Efficient Execution of Structured Language Model
+ * Programs" (unite.ai, es), "Introducción a SGLang" (RadixAttention bullet:
+ * LRU cache of KV inside a radix tree with matching, insertion, eviction) and
+ * "SGLang: Modelo de programación y metodología" (nine-step walkthrough:
+ * edges labelled with token sequences; an extension becomes a new node; a
+ * partial share splits a node; least recently used nodes are evicted).
+ *
+ * Keys are int64 token ids; values are int32 pool slots, one per token.
+ * Node boundaries follow the history of inserts: an insert that extends a
+ * cached sequence adds its new tokens as one new leaf node; an insert that
+ * leaves a node strictly inside it splits the node there; nodes are never
+ * merged.  A logical clock advances once per rx_match_prefix / rx_insert /
+ * rx_lock_prefix call, and every node holding at least one token of that
+ * call's matched path takes the new value.  rx_evict_lru removes whole leaf
+ * nodes with no lock, least recently used first.
+ */
+typedef struct rx_tree rx_tree;
+
+int rx_tree_create(rx_tree **out);
+void rx_tree_destroy(rx_tree *tree);
+
+/* Longest cached prefix of tokens[0..n).  Writes its slot ids to
+ * out_slots[0..prefix_len) (host, capacity out_cap) and its length to
+ * *out_prefix_len.  Touches the LRU clock on the matched path; never changes
+ * the tree's shape.  RX_ERR_CAPACITY if out_cap < prefix_len (nothing written
+ * to out_slots, *out_prefix_len still set). */
+int rx_match_prefix(rx_tree *tree, const int64_t *tokens, int64_t n, int32_t *out_slots,
+                    int64_t out_cap, int64_t *out_prefix_len);
+
+/* Cache tokens[0..n) with slots[0..n).  *out_already_cached = length of the
+ * leading part that was cached before the call; that part keeps the tree's
+ * slots and the caller owns (and should free) its own slots[0..already). */
+int rx_insert(rx_tree *tree, const int64_t *tokens, const int32_t *slots, int64_t n,
+              int64_t *out_already_cached);
+
+/* Evict leaf nodes, least recently used first, until at least num_tokens
+ * slots are freed or nothing unlocked is left.  Freed slot ids go to
+ * out_freed (host, capacity out_cap), node by node, each node in token
+ * order; *out_num_freed is their count.  The last node may overshoot
+ * num_tokens.  Returns RX_ERR_NOT_ENOUGH when fewer than num_tokens could be
+ * freed (what was freed is still reported) and RX_ERR_CAPACITY when the next
+ * node would not fit in out_cap (the nodes before it are evicted and
+ * reported; call again with room). */
+int rx_evict_lru(rx_tree *tree, int64_t num_tokens, int32_t *out_freed, int64_t out_cap,
+                 int64_t *out_num_freed);
+
+/* Lock (delta = +1) or unlock (delta = -1) the cached prefix of
+ * tokens[0..n): each of its tokens gets its lock count changed by delta, and a
+ * node holding any locked token is never evicted.  Locking touches the LRU
+ * clock like a match; unlocking does not.  *out_len gets the prefix length.
+ * Unlock with exactly the tokens a lock reported (n = its *out_len): more may
+ * be cached by then.  RX_ERR_INVALID (nothing changed) when unlocking a token
+ * whose count is zero. */
+int rx_lock_prefix(rx_tree *tree, const int64_t *tokens, int64_t n, int32_t delta,
+                   int64_t *out_len);
+
+/* Cached token count, node count (root excluded) and evictable token count. */
+int rx_tree_stats(rx_tree *tree, int64_t *cached_tokens, int64_t *num_nodes,
+                  int64_t *evictable_tokens);
+
+/* Structure dump for tests and tools: for every node in depth-first order
+ * (children by ascending first token) writes the int64 record
+ *   [node_id, parent_id (-1 under the root), last_access, n_tokens,
+ *    tokens[n_tokens], slots[n_tokens], lock_counts[n_tokens]]
+ * to out (host, capacity out_cap words).  *out_len = words written, or needed
+ * when RX_ERR_CAPACITY is returned. */
+int rx_tree_dump(rx_tree *tree, int64_t *out, int64_t out_cap, int64_t *out_len);
+
+/* ---- slot free list (host) ----------------------------------------------
+ * Hands out pool slots in the order given at creation, takes freed slots back
+ * at the tail (first in, first out). */
+typedef struct rx_slot_alloc rx_slot_alloc;
+
+/* free_order: host int32 [n], distinct values in [0, num_slots). */
+int rx_slot_alloc_create(const int32_t *free_order, int64_t n, int64_t num_slots,
+                         rx_slot_alloc **out);
+void rx_slot_alloc_destroy(rx_slot_alloc *a);
+/* Takes n slots into out (host).  RX_ERR_NOT_ENOUGH (nothing taken) if fewer are free. */
+int rx_slot_alloc_take(rx_slot_alloc *a, int64_t n, int32_t *out);
+/* Returns n slots.  RX_ERR_INVALID (nothing returned) on an out-of-range id. */
+int rx_slot_alloc_give(rx_slot_alloc *a, const int32_t *slots, int64_t n);
+int64_t rx_slot_alloc_free_count(const rx_slot_alloc *a);
+
+/* ---- request admission (host) -------------------------------------------
+ * Prefix match and slot assignment for one request, in one call:
+ * matches tokens[0..n), locks the matched path, takes n - prefix_len fresh
+ * slots from `alloc` (first evicting least recently used unlocked nodes into
+ * `alloc` when it is short) and writes the request's full slot list to
+ * out_row[0..n) (host): cached slots first, then the fresh ones.
+ * *out_prefix_len = cached length, *out_evicted = tokens evicted.
+ * RX_ERR_NOT_ENOUGH (lock released, nothing taken) if the pool cannot hold
+ * the request. */
+int rx_admit(rx_tree *tree, rx_slot_alloc *alloc, const int64_t *tokens, int64_t n,
+             int32_t *out_row, int64_t *out_prefix_len, int64_t *out_evicted);
+
+/* After the request's KV is in the pool: unlocks the path locked by rx_admit
+ * (prefix_len tokens), inserts tokens[0..n) with row[0..n), and returns to
+ * `alloc` the fresh slots whose tokens turned out to be cached already. */
+int rx_commit(rx_tree *tree, rx_slot_alloc *alloc, const int64_t *tokens, const int32_t *row,
+              int64_t n, int64_t prefix_len);
+
+/* ---- KV pool (device) ---------------------------------------------------- */
+typedef struct {
+    void *k;              /* device bf16 [num_slots, num_kv_heads, head_dim] */
+    void *v;              /* device bf16, same shape                         */
+    int64_t num_slots;
+    int32_t num_kv_heads;
+    int32_t head_dim;     /* 64 or 128                                       */
+} rx_kv_pool;
+
+/* KV slot scatter: K[slots[i]] = k_new[i], V[slots[i]] = v_new[i] for i < n.
+ * k_new, v_new: device bf16 [n, num_kv_heads, head_dim]; slots: device int32
+ * [n], distinct (duplicates race: one of the rows wins).  16-byte aligned
+ * pointers required.  Source: the reuse of stored KV across calls,
+ * "SGLang: Efficient Execution of Structured Language Model Programs",
+ * "Introducción a SGLang", RadixAttention bullet. */
+int rx_kv_store(const rx_kv_pool *pool, const void *k_new, const void *v_new, const int32_t *slots,
+                int64_t n, int32_t *dev_status, void *stream);
+
+/* Extend attention.  Request b (b < batch) has prefix_len[b] cached tokens and
+ * extend_len[b] new ones whose K/V are already in the pool; the slot list is
+ * req_to_token row req_idx[b], positions 0 .. prefix_len[b]+extend_len[b]-1.
+ * New token i of request b sits at position prefix_len[b] + i and attends to
+ * positions 0 .. prefix_len[b] + i.
+ *   q:  device bf16 [sum(extend_len), num_q_heads, head_dim], request b's
+ *       tokens at rows qo_indptr[b] .. qo_indptr[b+1]-1;
+ *   o:  device bf16, same shape as q;  lse_or_null: device fp32
+ *       [sum(extend_len), num_q_heads] or NULL;
+ *   qo_indptr: device int32 [batch+1]; req_idx, prefix_len, extend_len:
+ *       device int32 [batch]; req_to_token: device int32, row stride
+ *       rtt_stride;
+ *   max_extend_len: host bound on extend_len[b] (sizes the grid; larger
+ *       device values are an error that leaves rows unwritten).
+ * Requires head_dim == 128, num_q_heads % num_kv_heads == 0 and
+ * 128 % (num_q_heads / num_kv_heads) == 0. */
+int rx_attn_extend(const rx_kv_pool *pool, const void *q, void *o, float *lse_or_null,
+                   int32_t num_q_heads, const int32_t *qo_indptr, const int32_t *req_idx,
+                   const int32_t *prefix_len, const int32_t *extend_len,
+                   const int32_t *req_to_token, int64_t rtt_stride, int32_t batch,
+                   int32_t max_extend_len, float sm_scale, int32_t *dev_status, void *stream);
+
+/* ---- decode -------------------------------------------------------------
+ * Decode plan: which requests of the batch share which positions, so that a
+ * shared segment's KV is read once for all of them.  Built on the host by
+ * rx_decode_plan_build from the host copy of req_to_token; the caller copies
+ * the packed buffer to the device and fills this struct with device pointers
+ * into that copy (see rx_decode_plan_build for the layout).
+ */
+typedef struct {
+    const int32_t *order;   /* device int32 [batch]: batch index of each plan row   */
+    const int32_t *nparts;  /* device int32 [batch]: partial results per request    */
+    const int32_t *items;   /* device int32 [n_items * 8]: work items               */
+    int32_t n_items;
+    int32_t max_parts;      /* largest nparts[b]                                     */
+} rx_decode_plan;
+
+typedef struct {
+    int32_t n_items;
+    int32_t max_parts;
+    int32_t n_segments;     /* shared segments found (groups of >= 2 requests)  */
+    int32_t kv_chunk;       /* positions per work item that the plan used       */
+    int64_t shared_tokens;  /* positions inside shared segments, counted once   */
+    int64_t tokens_read;    /* KV token rows the plan reads per kv head: shared
+                               segments once, everything else once per request */
+    int64_t buf_words;      /* int32 words of the packed buffer                 */
+} rx_decode_plan_info;
+
+/* Builds a decode plan.  Inputs (host): req_to_token (row stride rtt_stride),
+ * req_idx [batch], seq_len [batch] (> 0); num_q_heads, num_kv_heads;
+ * kv_chunk = positions per work item (multiple of 64, <= 4096; 0 picks one
+ * that gives about 1216 work items over all kv heads); min_shared =
+ * shortest shared segment worth grouping (>= 1).  Requests whose slot lists
+ * agree on positions [a, b) (same slot at every position, from position 0 on)
+ * form a segment; segments nest like the radix tree the slots came from.
+ * Packed output (host int32, capacity out_cap words): order [batch], nparts
+ * [batch], then items [n_items][8] = {first plan row, row count, pos_begin,
+ * pos_end, part index, is_final, 0, 0}.  RX_ERR_CAPACITY (info->buf_words
+ * set) if out_cap is too small. */
+int rx_decode_plan_build(const int32_t *req_to_token, int64_t rtt_stride, const int32_t *req_idx,
+                         const int32_t *seq_len, int32_t batch, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t kv_chunk, int32_t min_shared,
+                         int32_t *out_buf, int64_t out_cap, rx_decode_plan_info *info);
+
+/* Workspace bytes rx_attn_decode needs (0 when every request fits one work
+ * item).  With plan == NULL the split is chosen from batch and max_seq_len. */
+size_t rx_attn_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t max_seq_len,
+                                const rx_decode_plan *plan_or_null);
+
+/* Decode attention: one query per request b at position seq_len[b]-1 over
+ * positions 0 .. seq_len[b]-1 of req_to_token row req_idx[b] (its own new K/V
+ * must already be in the pool).
+ *   q, o: device bf16 [batch, num_q_heads, head_dim]; lse_or_null: device fp32
+ *   [batch, num_q_heads] or NULL; req_idx, seq_len: device int32 [batch];
+ *   max_seq_len: host bound on seq_len (sizes the grid without a plan);
+ *   plan_or_null: device plan from rx_decode_plan_build for this batch, or
+ *   NULL for one work split per request;
+ *   workspace: device, >= rx_attn_decode_workspace(...) bytes, 256-byte
+ *   aligned, contents ignored on entry (partial results of split work).
+ * Requires head_dim in {64, 128}, num_q_heads % num_kv_heads == 0 and
+ * 64 % (num_q_heads / num_kv_heads) == 0. */
+int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, float *lse_or_null,
+                   int32_t num_q_heads, const int32_t *req_idx, const int32_t *seq_len,
+                   const int32_t *req_to_token, int64_t rtt_stride, int32_t batch,
+                   int32_t max_seq_len, const rx_decode_plan *plan_or_null, void *workspace,
+                   size_t ws_bytes, float sm_scale, int32_t *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RX_H */

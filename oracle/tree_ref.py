@@ -37,7 +37,12 @@ Readings taken where the pages are silent:
     in the same call.  Nodes holding a given value always lie on one root
     path (the path of the call that set it, and splits keep both parts on
     it), so two leaves never tie and no tie-break is needed;
-  * freed slots are reported node by node, each node in token order.
+  * freed slots are reported node by node, each node in token order;
+  * locks: ``lock(tokens, +1)`` adds one to the lock count of every cached
+    token of the matched prefix (and touches the clock like a match);
+    ``lock(tokens, -1)`` takes one off again without touching the clock.  A
+    node with any locked token is never evicted.  Locks sit on tokens, so a
+    later split leaves each part exactly the locks of its own tokens.
 """
 from __future__ import annotations
 
@@ -45,9 +50,10 @@ from typing import Dict, List, Optional, Sequence, Tuple
 
 
 class _Tok:
-    __slots__ = ("token", "slot", "head", "last", "parent", "children")
+    __slots__ = ("token", "slot", "head", "last", "parent", "children", "lock")
 
     def __init__(self, token, slot, parent, head, last):
+        self.lock = 0
         self.token = token
         self.slot = slot
         self.head = head          # first token of a radix node
@@ -141,20 +147,60 @@ class RadixTreeRef:
             leaves = self._leaf_nodes()
             if not leaves:
                 break
-            head, last_tok = min(leaves, key=lambda hl: hl[0].last)
-            run, n = [], last_tok
-            while True:
-                run.append(n)
-                if n is head:
-                    break
-                n = n.parent
-            run.reverse()
+            runs = []
+            for head, last_tok in leaves:
+                run, n = [], last_tok
+                while True:
+                    run.append(n)
+                    if n is head:
+                        break
+                    n = n.parent
+                run.reverse()
+                if all(t.lock == 0 for t in run):
+                    runs.append((head.last, run))
+            if not runs:
+                break
+            _, run = min(runs, key=lambda lr: lr[0])
+            head = run[0]
             if cap is not None and len(freed) + len(run) > cap:
                 raise CapacityError(freed)
             del head.parent.children[head.token]
             freed.extend(t.slot for t in run)
             self.cached_tokens -= len(run)
         return freed
+
+    def lock(self, tokens: Sequence[int], delta: int) -> int:
+        """Lock (+1) or unlock (-1) the cached prefix of ``tokens``; returns
+        its length.  Unlocking a token whose count is zero raises ValueError
+        and changes nothing."""
+        assert delta in (1, -1)
+        if delta > 0:
+            self.clock += 1
+        path = self._walk(tokens)
+        if delta < 0 and any(t.lock == 0 for t in path):
+            raise ValueError("unlock without lock")
+        if delta > 0:
+            self._tick(path)
+        for t in path:
+            t.lock += delta
+        return len(path)
+
+    def evictable_tokens(self) -> int:
+        total, stack = 0, [self.root]
+        while stack:
+            n = stack.pop()
+            for c in n.children.values():
+                run, t = [c], c
+                while len(t.children) == 1:
+                    nxt = next(iter(t.children.values()))
+                    if nxt.head:
+                        break
+                    run.append(nxt)
+                    t = nxt
+                if all(x.lock == 0 for x in run):
+                    total += len(run)
+                stack.append(t)
+        return total
 
     # -- structure (for assertions) ----------------------------------------
     def nodes(self) -> List[Tuple[Tuple[int, ...], Tuple[int, ...]]]:

@@ -1,0 +1,396 @@
+"""Thin ctypes binding of librx (``include/rx.h``).
+
+Argument marshalling only: every function here checks the tensors it is
+given (device, dtype, contiguity), passes their data pointers and the current
+CUDA stream to the library function of the same name, and turns a non-zero
+status into ``RxError``.  No step of the path runs in Python, and there is no
+fallback: if ``_build/librx.so`` is missing, importing this module raises.
+
+Device tensors come from PyTorch (it owns device memory and streams); host
+arrays are numpy.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "librx.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"librx.so is not built ({LIB_PATH}); run __graft_entry__.build() or "
+                      "python -m prefix_shared_kv_radixattention_gb300.build")
+_lib = ctypes.CDLL(LIB_PATH)
+
+RX_OK = 0
+RX_ERR_INVALID = -1
+RX_ERR_CAPACITY = -2
+RX_ERR_NOMEM = -3
+RX_ERR_NOT_ENOUGH = -4
+RX_ERR_CUDA = -5
+RX_ERR_UNSUPPORTED = -6
+RX_DEV_BAD_SLOT = 1
+RX_DEV_BAD_LEN = 2
+
+
+class RxError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+class KVPool(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_slots", ctypes.c_int64),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+class DecodePlan(ctypes.Structure):
+    _fields_ = [("order", ctypes.c_void_p), ("nparts", ctypes.c_void_p), ("items", ctypes.c_void_p),
+                ("n_items", ctypes.c_int32), ("max_parts", ctypes.c_int32)]
+
+
+class DecodePlanInfo(ctypes.Structure):
+    _fields_ = [("n_items", ctypes.c_int32), ("max_parts", ctypes.c_int32),
+                ("n_segments", ctypes.c_int32), ("kv_chunk", ctypes.c_int32),
+                ("shared_tokens", ctypes.c_int64), ("tokens_read", ctypes.c_int64),
+                ("buf_words", ctypes.c_int64)]
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_PI64 = ctypes.POINTER(ctypes.c_int64)
+
+
+def _sig(name, res, *args):
+    f = getattr(_lib, name)
+    f.restype = res
+    f.argtypes = list(args)
+    return f
+
+
+_sig("rx_last_error", ctypes.c_char_p)
+_sig("rx_version", ctypes.c_int)
+_sig("rx_tree_create", ctypes.c_int, ctypes.POINTER(_P))
+_sig("rx_tree_destroy", None, _P)
+_sig("rx_match_prefix", ctypes.c_int, _P, _P, _I64, _P, _I64, _PI64)
+_sig("rx_insert", ctypes.c_int, _P, _P, _P, _I64, _PI64)
+_sig("rx_evict_lru", ctypes.c_int, _P, _I64, _P, _I64, _PI64)
+_sig("rx_lock_prefix", ctypes.c_int, _P, _P, _I64, _I32, _PI64)
+_sig("rx_tree_stats", ctypes.c_int, _P, _PI64, _PI64, _PI64)
+_sig("rx_tree_dump", ctypes.c_int, _P, _P, _I64, _PI64)
+_sig("rx_slot_alloc_create", ctypes.c_int, _P, _I64, _I64, ctypes.POINTER(_P))
+_sig("rx_slot_alloc_destroy", None, _P)
+_sig("rx_slot_alloc_take", ctypes.c_int, _P, _I64, _P)
+_sig("rx_slot_alloc_give", ctypes.c_int, _P, _P, _I64)
+_sig("rx_slot_alloc_free_count", _I64, _P)
+_sig("rx_admit", ctypes.c_int, _P, _P, _P, _I64, _P, _PI64, _PI64)
+_sig("rx_commit", ctypes.c_int, _P, _P, _P, _P, _I64, _I64)
+_sig("rx_kv_store", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I64, _P, _P)
+_sig("rx_attn_extend", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I32, _P, _P, _P, _P, _P,
+     _I64, _I32, _I32, ctypes.c_float, _P, _P)
+_sig("rx_decode_plan_build", ctypes.c_int, _P, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64,
+     ctypes.POINTER(DecodePlanInfo))
+_sig("rx_attn_decode_workspace", ctypes.c_size_t, _I32, _I32, _I32, _I32, _I32,
+     ctypes.POINTER(DecodePlan))
+_sig("rx_attn_decode", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I32, _P, _P, _P, _I64, _I32,
+     _I32, ctypes.POINTER(DecodePlan), _P, ctypes.c_size_t, ctypes.c_float, _P, _P)
+
+
+def library():
+    """The loaded ctypes.CDLL (for symbol checks)."""
+    return _lib
+
+
+def version() -> int:
+    return _lib.rx_version()
+
+
+def last_error() -> str:
+    return _lib.rx_last_error().decode()
+
+
+def _check(rc: int, allow=()) -> int:
+    if rc != RX_OK and rc not in allow:
+        raise RxError(rc, last_error())
+    return rc
+
+
+def _np(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ---------------------------------------------------------------------------
+# radix tree and slot free list (host)
+# ---------------------------------------------------------------------------
+
+
+class RadixTree:
+    """rx_tree: prefix match, insert, LRU eviction and locks over token ids."""
+
+    def __init__(self):
+        h = _P()
+        _check(_lib.rx_tree_create(ctypes.byref(h)))
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            _lib.rx_tree_destroy(h)
+            self._h = None
+
+    def match_prefix(self, tokens: Sequence[int]) -> Tuple[int, List[int]]:
+        t, tp = _np(tokens, np.int64)
+        out = np.empty(max(1, len(t)), np.int32)
+        k = ctypes.c_int64()
+        _check(_lib.rx_match_prefix(self._h, tp, len(t), out.ctypes.data_as(_P), len(t),
+                                    ctypes.byref(k)))
+        return k.value, out[:k.value].tolist()
+
+    def insert(self, tokens: Sequence[int], slots: Sequence[int]) -> int:
+        t, tp = _np(tokens, np.int64)
+        s, sp = _np(slots, np.int32)
+        assert len(t) == len(s)
+        k = ctypes.c_int64()
+        _check(_lib.rx_insert(self._h, tp, sp, len(t), ctypes.byref(k)))
+        return k.value
+
+    def evict(self, num_tokens: int, cap: Optional[int] = None) -> List[int]:
+        """Freed slots; raises RxError(RX_ERR_CAPACITY) if ``cap`` is too small."""
+        if cap is None:
+            _, _, ev = self.stats()
+            cap = max(ev, 1)
+        out = np.empty(max(1, cap), np.int32)
+        n = ctypes.c_int64()
+        rc = _lib.rx_evict_lru(self._h, int(num_tokens), out.ctypes.data_as(_P), cap, ctypes.byref(n))
+        _check(rc, allow=(RX_ERR_NOT_ENOUGH,))
+        return out[:n.value].tolist()
+
+    def lock(self, tokens: Sequence[int], delta: int) -> int:
+        t, tp = _np(tokens, np.int64)
+        k = ctypes.c_int64()
+        _check(_lib.rx_lock_prefix(self._h, tp, len(t), int(delta), ctypes.byref(k)))
+        return k.value
+
+    def stats(self) -> Tuple[int, int, int]:
+        a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(_lib.rx_tree_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+        return a.value, b.value, c.value
+
+    def dump(self) -> List[dict]:
+        need = ctypes.c_int64()
+        _check(_lib.rx_tree_dump(self._h, None, 0, ctypes.byref(need)), allow=(RX_ERR_CAPACITY,))
+        buf = np.empty(max(1, need.value), np.int64)
+        _check(_lib.rx_tree_dump(self._h, buf.ctypes.data_as(_P), len(buf), ctypes.byref(need)))
+        out, i = [], 0
+        while i < need.value:
+            nid, par, last, n = buf[i:i + 4].tolist()
+            i += 4
+            toks = buf[i:i + n].tolist()
+            slots = buf[i + n:i + 2 * n].tolist()
+            locks = buf[i + 2 * n:i + 3 * n].tolist()
+            i += 3 * n
+            out.append(dict(id=nid, parent=par, last=last, tokens=toks, slots=slots, locks=locks))
+        return out
+
+    def nodes(self) -> List[Tuple[Tuple[int, ...], Tuple[int, ...]]]:
+        """Every node as (token path before it, its own tokens), sorted."""
+        recs = self.dump()
+        path = {}
+        out = []
+        for r in recs:  # depth-first: parents come before children
+            before = () if r["parent"] < 0 else path[r["parent"]]
+            path[r["id"]] = before + tuple(r["tokens"])
+            out.append((before, tuple(r["tokens"])))
+        return sorted(out)
+
+
+class SlotAllocator:
+    """rx_slot_alloc: first-in first-out free list of pool slots."""
+
+    def __init__(self, free_order: Sequence[int], num_slots: int):
+        o, op = _np(free_order, np.int32)
+        h = _P()
+        _check(_lib.rx_slot_alloc_create(op, len(o), int(num_slots), ctypes.byref(h)))
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            _lib.rx_slot_alloc_destroy(h)
+            self._h = None
+
+    def take(self, n: int) -> np.ndarray:
+        out = np.empty(max(1, n), np.int32)
+        _check(_lib.rx_slot_alloc_take(self._h, int(n), out.ctypes.data_as(_P)))
+        return out[:n]
+
+    def give(self, slots: Sequence[int]) -> None:
+        s, sp = _np(slots, np.int32)
+        _check(_lib.rx_slot_alloc_give(self._h, sp, len(s)))
+
+    def free_count(self) -> int:
+        return _lib.rx_slot_alloc_free_count(self._h)
+
+
+def rx_admit(tree: RadixTree, alloc: SlotAllocator, tokens: Sequence[int]):
+    """(slot row int32 [n], prefix_len, evicted tokens)."""
+    t, tp = _np(tokens, np.int64)
+    row = np.empty(max(1, len(t)), np.int32)
+    k, ev = ctypes.c_int64(), ctypes.c_int64()
+    _check(_lib.rx_admit(tree._h, alloc._h, tp, len(t), row.ctypes.data_as(_P), ctypes.byref(k),
+                         ctypes.byref(ev)))
+    return row[:len(t)], k.value, ev.value
+
+
+def rx_commit(tree: RadixTree, alloc: SlotAllocator, tokens: Sequence[int], row: Sequence[int],
+              prefix_len: int) -> None:
+    t, tp = _np(tokens, np.int64)
+    r, rp = _np(row, np.int32)
+    _check(_lib.rx_commit(tree._h, alloc._h, tp, rp, len(t), int(prefix_len)))
+
+
+# ---------------------------------------------------------------------------
+# device entry points
+# ---------------------------------------------------------------------------
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev(t, dtype, name):
+    torch = _torch()
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_pool(k_pool, v_pool) -> KVPool:
+    torch = _torch()
+    _dev(k_pool, torch.bfloat16, "k_pool")
+    _dev(v_pool, torch.bfloat16, "v_pool")
+    if k_pool.shape != v_pool.shape or k_pool.dim() != 3:
+        raise ValueError("k_pool and v_pool must both be [num_slots, num_kv_heads, head_dim]")
+    S, hkv, d = k_pool.shape
+    return KVPool(k_pool.data_ptr(), v_pool.data_ptr(), S, hkv, d)
+
+
+def rx_kv_store(k_pool, v_pool, k_new, v_new, slots, dev_status=None, stream=None) -> None:
+    torch = _torch()
+    pool = make_pool(k_pool, v_pool)
+    _dev(k_new, torch.bfloat16, "k_new")
+    _dev(v_new, torch.bfloat16, "v_new")
+    _dev(slots, torch.int32, "slots")
+    _dev(dev_status, torch.int32, "dev_status")
+    n = slots.numel()
+    if k_new.numel() != n * pool.num_kv_heads * pool.head_dim or k_new.shape != v_new.shape:
+        raise ValueError("k_new/v_new must be [n, num_kv_heads, head_dim]")
+    _check(_lib.rx_kv_store(ctypes.byref(pool), _ptr(k_new), _ptr(v_new), _ptr(slots), n,
+                            _ptr(dev_status), _stream(stream)))
+
+
+def rx_attn_extend(k_pool, v_pool, q, o, lse, qo_indptr, req_idx, prefix_len, extend_len,
+                   req_to_token, max_extend_len: int, sm_scale: float, dev_status=None,
+                   stream=None) -> None:
+    torch = _torch()
+    pool = make_pool(k_pool, v_pool)
+    for t, n in ((q, "q"), (o, "o")):
+        _dev(t, torch.bfloat16, n)
+    _dev(lse, torch.float32, "lse")
+    for t, n in ((qo_indptr, "qo_indptr"), (req_idx, "req_idx"), (prefix_len, "prefix_len"),
+                 (extend_len, "extend_len"), (req_to_token, "req_to_token")):
+        _dev(t, torch.int32, n)
+    _dev(dev_status, torch.int32, "dev_status")
+    if q.dim() != 3 or q.shape != o.shape:
+        raise ValueError("q and o must be [tokens, num_q_heads, head_dim]")
+    _check(_lib.rx_attn_extend(ctypes.byref(pool), _ptr(q), _ptr(o), _ptr(lse), q.shape[1],
+                               _ptr(qo_indptr), _ptr(req_idx), _ptr(prefix_len), _ptr(extend_len),
+                               _ptr(req_to_token), req_to_token.shape[1], req_idx.numel(),
+                               int(max_extend_len), float(sm_scale), _ptr(dev_status),
+                               _stream(stream)))
+
+
+@dataclass
+class DevicePlan:
+    """A decode plan copied to the device; keeps its buffer alive."""
+
+    buf: object          # torch int32 tensor on the device
+    info: DecodePlanInfo
+    batch: int
+    struct: DecodePlan
+
+
+def rx_decode_plan_build(req_to_token_host, req_idx_host, seq_len_host, num_q_heads: int,
+                         num_kv_heads: int, kv_chunk: int = 0, min_shared: int = 16):
+    """Host plan: (packed int32 numpy buffer, DecodePlanInfo)."""
+    rtt, rp = _np(req_to_token_host, np.int32)
+    ri, rip = _np(req_idx_host, np.int32)
+    sl, slp = _np(seq_len_host, np.int32)
+    info = DecodePlanInfo()
+    rc = _lib.rx_decode_plan_build(rp, rtt.shape[1], rip, slp, len(ri), num_q_heads, num_kv_heads,
+                                   kv_chunk, min_shared, None, 0, ctypes.byref(info))
+    _check(rc, allow=(RX_ERR_CAPACITY,))
+    buf = np.empty(max(1, info.buf_words), np.int32)
+    _check(_lib.rx_decode_plan_build(rp, rtt.shape[1], rip, slp, len(ri), num_q_heads, num_kv_heads,
+                                     kv_chunk, min_shared, buf.ctypes.data_as(_P), len(buf),
+                                     ctypes.byref(info)))
+    return buf[:info.buf_words], info
+
+
+def plan_to_device(buf: np.ndarray, info: DecodePlanInfo, batch: int, device="cuda") -> DevicePlan:
+    torch = _torch()
+    d = torch.from_numpy(np.ascontiguousarray(buf)).to(device)
+    base = d.data_ptr()
+    st = DecodePlan(base, base + 4 * batch, base + 8 * batch, info.n_items, info.max_parts)
+    return DevicePlan(d, info, batch, st)
+
+
+def rx_attn_decode_workspace(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                             max_seq_len: int, plan: Optional[DevicePlan] = None) -> int:
+    pp = ctypes.byref(plan.struct) if plan is not None else None
+    return _lib.rx_attn_decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, pp)
+
+
+def rx_attn_decode(k_pool, v_pool, q, o, lse, req_idx, seq_len, req_to_token, max_seq_len: int,
+                   sm_scale: float, plan: Optional[DevicePlan] = None, workspace=None,
+                   dev_status=None, stream=None) -> None:
+    torch = _torch()
+    pool = make_pool(k_pool, v_pool)
+    _dev(q, torch.bfloat16, "q")
+    _dev(o, torch.bfloat16, "o")
+    _dev(lse, torch.float32, "lse")
+    for t, n in ((req_idx, "req_idx"), (seq_len, "seq_len"), (req_to_token, "req_to_token")):
+        _dev(t, torch.int32, n)
+    _dev(dev_status, torch.int32, "dev_status")
+    if workspace is not None:
+        _dev(workspace, workspace.dtype, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    pp = ctypes.byref(plan.struct) if plan is not None else None
+    _check(_lib.rx_attn_decode(ctypes.byref(pool), _ptr(q), _ptr(o), _ptr(lse), q.shape[1],
+                               _ptr(req_idx), _ptr(seq_len), _ptr(req_to_token),
+                               req_to_token.shape[1], req_idx.numel(), int(max_seq_len), pp,
+                               _ptr(workspace), ws_bytes, float(sm_scale), _ptr(dev_status),
+                               _stream(stream)))

@@ -1,0 +1,22 @@
+// rx_internal.h -- declarations shared by the translation units of librx.
+#pragma once
+
+#include <stdint.h>
+
+#define RX_ABI_VERSION 1
+
+// Longest position range one decode work item covers (the plan builder and
+// the no-plan split both stay at or below it).
+#define RX_MAX_KV_CHUNK 4096
+
+// Work items an automatic decode split aims for: about four waves of two
+// CTAs on each of 152 SMs.
+#define RX_DECODE_TARGET_ITEMS 1216
+
+// Sets the thread-local message returned by rx_last_error and returns code.
+int rx_set_error(int code, const char *fmt, ...);
+
+// Positions per decode work item when no plan is given, and the resulting
+// number of partial results per request.  Chosen from the batch shape only,
+// so rx_attn_decode_workspace and rx_attn_decode agree.
+int32_t rx_decode_default_chunk(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len);

@@ -157,13 +157,19 @@ def _empty_i32():
 
 
 def _finish(name, seed, rng, hq, hkv, d, num_slots, rows, cached_slots, new_slots,
-            ext, dec) -> Problem:
+            ext, dec, draw_values=True) -> Problem:
     """Draw values and assemble a Problem.
 
     rows: list of (token ids int64, slot ids int32) per req_to_token row.
     ext:  list of (row, prefix_len, extend_len).
     dec:  list of (row, seq_len).
+    With draw_values=False the value arrays have zero rows (structure only).
     """
+    if not draw_values:
+        def randn_bf16(_rng, shape):  # noqa: F811 - structure-only stand-in
+            return np.zeros((0,) + tuple(shape[1:]), dtype=np.uint16)
+    else:
+        randn_bf16 = globals()["randn_bf16"]
     stride = max(len(s) for _, s in rows)
     stride = (stride + 15) // 16 * 16
     rtt = np.full((len(rows), stride), -1, dtype=np.int32)
@@ -199,7 +205,8 @@ def _finish(name, seed, rng, hq, hkv, d, num_slots, rows, cached_slots, new_slot
 
 
 def tiny_extend(seed: int = 1001, hq: int = 4, hkv: int = 4, d: int = 64, batch: int = 4,
-                prefix: int = 64, extend: int = 16, num_slots: int = 512) -> Problem:
+                prefix: int = 64, extend: int = 16, num_slots: int = 512,
+                draw_values: bool = True) -> Problem:
     """Requests sharing one cached prefix, each extending it causally.
 
     Full size: 4 q heads = 4 kv heads, head_dim 64, 4 requests on one
@@ -217,11 +224,12 @@ def tiny_extend(seed: int = 1001, hq: int = 4, hkv: int = 4, d: int = 64, batch:
         rows.append((np.concatenate([shared_tok, new_tok[b]]), np.concatenate([shared_slots, s_new])))
     ext = [(b, prefix, extend) for b in range(batch)]
     return _finish("tiny_extend", seed, rng, hq, hkv, d, num_slots, rows, shared_slots,
-                   np.concatenate(new_slots), ext, [])
+                   np.concatenate(new_slots), ext, [], draw_values)
 
 
 def few_shot_decode(seed: int = 1002, hq: int = 32, hkv: int = 32, d: int = 128, batch: int = 64,
-                    shared: int = 1024, private: int = 256, num_slots: int = 2 * 1024 * 1024) -> Problem:
+                    shared: int = 1024, private: int = 256, num_slots: int = 2 * 1024 * 1024,
+                    draw_values: bool = True) -> Problem:
     """Few-shot batch: one shared example prefix, a private question each, one decode token.
 
     Full size: Llama-2-7B attention shape (32 = 32 heads, head_dim 128),
@@ -240,12 +248,13 @@ def few_shot_decode(seed: int = 1002, hq: int = 32, hkv: int = 32, d: int = 128,
                      np.concatenate([shared_slots, priv_slots[b], new_slots[b:b + 1]])))
     cached = np.concatenate([shared_slots] + priv_slots)
     dec = [(b, shared + private + 1) for b in range(batch)]
-    return _finish("few_shot_decode", seed, rng, hq, hkv, d, num_slots, rows, cached, new_slots, [], dec)
+    return _finish("few_shot_decode", seed, rng, hq, hkv, d, num_slots, rows, cached, new_slots, [], dec,
+                   draw_values)
 
 
 def cached_prefix_extend(seed: int = 1003, hq: int = 32, hkv: int = 8, d: int = 128,
                          n_prefix: int = 8, per_prefix: int = 4, prefix: int = 2048, extend: int = 512,
-                         num_slots: int = 1024 * 1024) -> Problem:
+                         num_slots: int = 1024 * 1024, draw_values: bool = True) -> Problem:
     """Requests extending cached prefixes (several requests per prefix).
 
     Full size: Llama-3-8B GQA (32 q / 8 kv heads, head_dim 128), 8 distinct
@@ -264,11 +273,12 @@ def cached_prefix_extend(seed: int = 1003, hq: int = 32, hkv: int = 8, d: int = 
         rows.append((np.concatenate([pre_tok[p], new_tok[b]]), np.concatenate([pre_slots[p], s_new])))
         ext.append((b, prefix, extend))
     return _finish("cached_prefix_extend", seed, rng, hq, hkv, d, num_slots, rows,
-                   np.concatenate(pre_slots), np.concatenate(new_slots), ext, [])
+                   np.concatenate(pre_slots), np.concatenate(new_slots), ext, [], draw_values)
 
 
 def tree_of_thought_decode(seed: int = 1004, hq: int = 32, hkv: int = 8, d: int = 128, depth: int = 4,
-                           fanout: int = 4, edge: int = 256, num_slots: int = 1024 * 1024) -> Problem:
+                           fanout: int = 4, edge: int = 256, num_slots: int = 1024 * 1024,
+                           draw_values: bool = True) -> Problem:
     """Branching program: a full tree of thoughts, one decode token per leaf.
 
     Full size: GQA 32/8, head_dim 128, depth 4, fanout 4, 256 tokens per edge
@@ -302,12 +312,13 @@ def tree_of_thought_decode(seed: int = 1004, hq: int = 32, hkv: int = 8, d: int 
         rows.append((toks, sl))
         dec.append((leaf, depth * edge + 1))
     return _finish("tree_of_thought_decode", seed, rng, hq, hkv, d, num_slots, rows,
-                   np.concatenate(edge_slots), new_slots, [], dec)
+                   np.concatenate(edge_slots), new_slots, [], dec, draw_values)
 
 
 def mixed_chat(seed: int = 1005, hq: int = 64, hkv: int = 8, d: int = 128, n_dec: int = 16,
                system: int = 8192, history: int = 24576, n_ext: int = 16, ext_prefix: int = 4096,
-               ext_new: int = 1024, num_slots: int = 1024 * 1024) -> Problem:
+               ext_new: int = 1024, num_slots: int = 1024 * 1024,
+               draw_values: bool = True) -> Problem:
     """Long multi-turn chat: decode rows on long shared-system-prompt contexts
     plus concurrent extend rows on their own cached prefixes.
 
@@ -338,7 +349,8 @@ def mixed_chat(seed: int = 1005, hq: int = 64, hkv: int = 8, d: int = 128, n_dec
         ext.append((n_dec + b, ext_prefix, ext_new))
     cached = np.concatenate([sys_slots] + hist_slots + epre_slots)
     new = np.concatenate([dec_new] + ext_new_slots)
-    return _finish("mixed_chat", seed, rng, hq, hkv, d, num_slots, rows, cached, new, ext, dec)
+    return _finish("mixed_chat", seed, rng, hq, hkv, d, num_slots, rows, cached, new, ext, dec,
+                   draw_values)
 
 
 def ragged(seed: int, hq: int, hkv: int, d: int, n_groups: int, per_group: int, shared_max: int,

@@ -1,0 +1,139 @@
+"""Helpers for the GPU parity tests: upload a Problem, run the C-ABI entry
+points, build the oracle's pools, compare.
+
+Tolerance (bf16 outputs): |gpu - oracle| <= 2e-2 + 1e-2 * |oracle| per
+element (max |err| <= 2e-2 absolute and 1e-2 relative, read as an allclose
+bound); lse within 1e-3 absolute (fp32 sums in the kernel, fp64 in the
+oracle).
+"""
+import numpy as np
+import torch
+
+import oracle
+from prefix_shared_kv_radixattention_gb300 import binding as rx
+from prefix_shared_kv_radixattention_gb300 import inputs
+
+ATOL, RTOL, LSE_ATOL = 2e-2, 1e-2, 1e-3
+FILL = 64.0  # unused pool rows hold this, so a wrong read shows
+
+
+def to_dev(a_u16: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a_u16).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def to_host_u16(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def i32(a) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+class Dev:
+    """A Problem on the device: pools with cached rows placed, index arrays."""
+
+    def __init__(self, prob: inputs.Problem, host_pools: bool = None, seed: int = 7):
+        self.prob = prob
+        S, hkv, d = prob.num_slots, prob.hkv, prob.d
+        if host_pools is None:
+            host_pools = S * hkv * d <= (1 << 24)
+        self.host_pools = host_pools
+        if host_pools:
+            rng = np.random.default_rng(seed)
+            kp = inputs.randn_bf16(rng, (S, hkv, d))
+            vp = inputs.randn_bf16(rng, (S, hkv, d))
+            kp[prob.cached_slots] = prob.cached_k
+            vp[prob.cached_slots] = prob.cached_v
+            self.kp_host, self.vp_host = kp, vp
+            self.k_pool, self.v_pool = to_dev(kp), to_dev(vp)
+        else:
+            self.k_pool = torch.full((S, hkv, d), FILL, dtype=torch.bfloat16, device="cuda")
+            self.v_pool = torch.full((S, hkv, d), FILL, dtype=torch.bfloat16, device="cuda")
+            idx = torch.from_numpy(prob.cached_slots.astype(np.int64)).cuda()
+            for pool, src in ((self.k_pool, prob.cached_k), (self.v_pool, prob.cached_v)):
+                for s in range(0, len(idx), 1 << 16):
+                    pool.index_copy_(0, idx[s:s + (1 << 16)], to_dev(src[s:s + (1 << 16)]))
+        self.rtt = i32(prob.req_to_token)
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    # -- the path ------------------------------------------------------------
+    def kv_store(self):
+        p = self.prob
+        rx.rx_kv_store(self.k_pool, self.v_pool, to_dev(p.new_k), to_dev(p.new_v), i32(p.new_slots),
+                       self.status)
+
+    def decode(self, plan: bool, kv_chunk: int = 0, min_shared: int = 16, with_lse: bool = True):
+        p = self.prob
+        B = len(p.dec_req_idx)
+        q = to_dev(p.q_dec)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, p.hq), dtype=torch.float32, device="cuda") if with_lse else None
+        dp = None
+        if plan:
+            buf, info = rx.rx_decode_plan_build(p.req_to_token, p.dec_req_idx, p.dec_seq_len, p.hq,
+                                                p.hkv, kv_chunk, min_shared)
+            dp = rx.plan_to_device(buf, info, B)
+        max_len = int(p.dec_seq_len.max())
+        ws_bytes = rx.rx_attn_decode_workspace(B, p.hq, p.hkv, p.d, max_len, dp)
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+        rx.rx_attn_decode(self.k_pool, self.v_pool, q, o, lse, i32(p.dec_req_idx), i32(p.dec_seq_len),
+                          self.rtt, max_len, p.sm_scale, dp, ws if ws_bytes else None, self.status)
+        torch.cuda.synchronize()
+        return o.float().cpu().numpy(), (lse.cpu().numpy() if with_lse else None)
+
+    def extend(self, with_lse: bool = True):
+        p = self.prob
+        q = to_dev(p.q_ext)
+        o = torch.empty_like(q)
+        lse = torch.empty((q.shape[0], p.hq), dtype=torch.float32, device="cuda") if with_lse else None
+        rx.rx_attn_extend(self.k_pool, self.v_pool, q, o, lse, i32(p.qo_indptr), i32(p.ext_req_idx),
+                          i32(p.ext_prefix_len), i32(p.ext_extend_len), self.rtt,
+                          int(p.ext_extend_len.max()), p.sm_scale, self.status)
+        torch.cuda.synchronize()
+        return o.float().cpu().numpy(), (lse.cpu().numpy() if with_lse else None)
+
+    def status_word(self) -> int:
+        return int(self.status.item())
+
+    # -- the oracle's view ---------------------------------------------------
+    def oracle_pools(self, rows=None):
+        """Host pools after the step's KV store, and the matching req_to_token.
+
+        Small pools: the full host pools plus the oracle's own kv_store.  Big
+        pools: a compact pool of the referenced rows only (pool rows renamed,
+        which the slot-permutation invariance makes exact), with the new rows
+        placed by the oracle's kv_store."""
+        p = self.prob
+        if self.host_pools:
+            kp, vp = self.kp_host.copy(), self.vp_host.copy()
+            oracle.kv_store(kp, vp, p.new_k, p.new_v, p.new_slots)
+            return kp, vp, p.req_to_token
+        slots = np.concatenate([p.cached_slots, p.new_slots])
+        uniq = np.unique(slots)
+        kp = np.zeros((len(uniq), p.hkv, p.d), np.uint16)
+        vp = np.zeros_like(kp)
+        pos_c = np.searchsorted(uniq, p.cached_slots)
+        kp[pos_c], vp[pos_c] = p.cached_k, p.cached_v
+        oracle.kv_store(kp, vp, p.new_k, p.new_v, np.searchsorted(uniq, p.new_slots).astype(np.int32))
+        rtt = p.req_to_token
+        loc = np.searchsorted(uniq, np.maximum(rtt, 0))
+        loc = np.minimum(loc, len(uniq) - 1)
+        hit = (rtt >= 0) & (uniq[loc] == rtt)
+        return kp, vp, np.where(hit, loc, -1).astype(np.int32)
+
+
+def compare(gpu, ref, what=""):
+    gpu = np.asarray(gpu, np.float64)
+    err = np.abs(gpu - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    assert not np.isnan(gpu).any(), f"{what}: NaN in GPU output"
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; "
+                           f"max abs err {err.max():.3e}")
+    return float(err.max())
+
+
+def compare_lse(gpu, ref, what=""):
+    err = np.abs(np.asarray(gpu, np.float64) - ref)
+    assert err.max() <= LSE_ATOL, f"{what}: lse max abs err {err.max():.3e}"
+    return float(err.max())

@@ -1,0 +1,258 @@
+"""GPU parity: the sm_103a kernels, called through the C ABI, against the fp64
+oracle on the same seeded inputs.
+
+Sizes span several 64-key tiles, several work items per request and ragged
+tails; the tolerance is stated in tests/_gpu.py.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from prefix_shared_kv_radixattention_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _gpu():
+    from tests import _gpu
+    return _gpu
+
+
+# ---------------------------------------------------------------------------
+# KV store
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("hkv,d", [(4, 64), (8, 128), (32, 128)])
+def test_kv_store_bit_exact(hkv, d):
+    g = _gpu()
+    prob = inputs.ragged(5, hq=hkv, hkv=hkv, d=d, n_groups=3, per_group=3, shared_max=40,
+                         private_max=30, extend_max=50, decode=False, num_slots=2000)
+    dev = g.Dev(prob)
+    dev.kv_store()
+    torch.cuda.synchronize()
+    kp, vp, _ = dev.oracle_pools()
+    assert np.array_equal(g.to_host_u16(dev.k_pool), kp)
+    assert np.array_equal(g.to_host_u16(dev.v_pool), vp)
+    assert dev.status_word() == 0
+
+
+def test_kv_store_bad_slot_flagged_not_written():
+    g = _gpu()
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.tiny_extend()
+    dev = g.Dev(prob)
+    before_k = g.to_host_u16(dev.k_pool)
+    slots = prob.new_slots.copy()
+    slots[3] = prob.num_slots + 7
+    slots[5] = -2
+    rx.rx_kv_store(dev.k_pool, dev.v_pool, g.to_dev(prob.new_k), g.to_dev(prob.new_v), g.i32(slots),
+                   dev.status)
+    torch.cuda.synchronize()
+    assert dev.status_word() & rx.RX_DEV_BAD_SLOT
+    after_k = g.to_host_u16(dev.k_pool)
+    ok = np.ones(len(slots), bool)
+    ok[[3, 5]] = False
+    assert np.array_equal(after_k[slots[ok]], prob.new_k[ok])
+    untouched = np.setdiff1d(np.arange(prob.num_slots), slots[ok])
+    assert np.array_equal(after_k[untouched], before_k[untouched])
+
+
+def test_kv_store_empty_is_noop():
+    g = _gpu()
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.tiny_extend()
+    dev = g.Dev(prob)
+    before = g.to_host_u16(dev.k_pool)
+    e = torch.empty((0, prob.hkv, prob.d), dtype=torch.bfloat16, device="cuda")
+    rx.rx_kv_store(dev.k_pool, dev.v_pool, e, e, torch.empty(0, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert np.array_equal(g.to_host_u16(dev.k_pool), before)
+
+
+# ---------------------------------------------------------------------------
+# extend
+# ---------------------------------------------------------------------------
+
+
+def _check_extend(prob, g=None):
+    g = g or _gpu()
+    dev = g.Dev(prob)
+    dev.kv_store()
+    o, lse = dev.extend()
+    kp, vp, rtt = dev.oracle_pools()
+    ro, rl = oracle.extend(prob.q_ext, kp, vp, rtt, prob.ext_req_idx, prob.ext_prefix_len,
+                           prob.ext_extend_len, prob.qo_indptr, prob.sm_scale)
+    g.compare(o, ro, prob.name)
+    g.compare_lse(lse, rl, prob.name)
+    assert dev.status_word() == 0
+    return o, lse
+
+
+def test_extend_tiny_full_config():
+    """The tiny-extend configuration at its full size, every output."""
+    _check_extend(inputs.tiny_extend())
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (8, 2, 64), (32, 8, 128), (16, 2, 128), (4, 1, 128)])
+def test_extend_ragged(hq, hkv, d):
+    prob = inputs.ragged(20 + hq + d, hq=hq, hkv=hkv, d=d, n_groups=3, per_group=2, shared_max=150,
+                         private_max=90, extend_max=140, decode=False, num_slots=3000)
+    _check_extend(prob)
+
+
+def test_extend_cached_prefix_reduced():
+    _check_extend(inputs.cached_prefix_extend(n_prefix=2, per_prefix=2, prefix=300, extend=150,
+                                              num_slots=4096))
+
+
+def test_extend_edge_cases():
+    # prefix 0 (plain causal), extend 1 (a single new token), long prefix
+    for P, E in ((0, 70), (0, 1), (5, 1), (333, 3), (64, 64), (1, 129)):
+        prob = inputs.tiny_extend(seed=P * 1000 + E, hq=8, hkv=2, d=128, batch=2, prefix=P, extend=E,
+                                  num_slots=1024)
+        _check_extend(prob)
+
+
+# ---------------------------------------------------------------------------
+# decode
+# ---------------------------------------------------------------------------
+
+
+def _check_decode(prob, plan, kv_chunk=0, min_shared=16, g=None):
+    g = g or _gpu()
+    dev = g.Dev(prob)
+    dev.kv_store()
+    o, lse = dev.decode(plan=plan, kv_chunk=kv_chunk, min_shared=min_shared)
+    kp, vp, rtt = dev.oracle_pools()
+    ro, rl = oracle.decode(prob.q_dec, kp, vp, rtt, prob.dec_req_idx, prob.dec_seq_len, prob.sm_scale)
+    g.compare(o, ro, f"{prob.name} plan={plan}")
+    g.compare_lse(lse, rl, f"{prob.name} plan={plan}")
+    assert dev.status_word() == 0
+    return o, lse
+
+
+@pytest.mark.parametrize("plan", [False, True])
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (32, 32, 128), (32, 8, 128), (64, 8, 128), (8, 1, 64)])
+def test_decode_ragged(plan, hq, hkv, d):
+    prob = inputs.ragged(40 + hq + d, hq=hq, hkv=hkv, d=d, n_groups=3, per_group=3, shared_max=400,
+                         private_max=300, extend_max=1, decode=True, num_slots=5000)
+    _check_decode(prob, plan, kv_chunk=128 if plan else 0, min_shared=8)
+
+
+@pytest.mark.parametrize("plan", [False, True])
+def test_decode_few_shot_reduced(plan):
+    _check_decode(inputs.few_shot_decode(batch=12, shared=300, private=77, num_slots=8192), plan)
+
+
+def test_decode_tree_of_thought_reduced():
+    prob = inputs.tree_of_thought_decode(depth=3, fanout=3, edge=70, num_slots=8192)
+    _check_decode(prob, plan=True, kv_chunk=64, min_shared=16)
+    _check_decode(prob, plan=True, kv_chunk=0, min_shared=16)
+    _check_decode(prob, plan=False)
+
+
+def test_decode_many_rows_per_segment():
+    """A segment shared by more requests than one work item holds (row blocks)."""
+    prob = inputs.few_shot_decode(hq=16, hkv=2, d=128, batch=40, shared=200, private=9,
+                                  num_slots=4096)
+    _check_decode(prob, plan=True, kv_chunk=64)
+
+
+def test_decode_single_token_context():
+    prob = inputs.few_shot_decode(hq=8, hkv=2, d=64, batch=5, shared=0, private=0, num_slots=64)
+    for plan in (False, True):
+        _check_decode(prob, plan)
+
+
+def test_decode_without_lse_output():
+    g = _gpu()
+    prob = inputs.few_shot_decode(hq=8, hkv=8, d=128, batch=6, shared=100, private=50, num_slots=1024)
+    dev = g.Dev(prob)
+    dev.kv_store()
+    o, _ = dev.decode(plan=True, with_lse=False)
+    kp, vp, rtt = dev.oracle_pools()
+    ro, _ = oracle.decode(prob.q_dec, kp, vp, rtt, prob.dec_req_idx, prob.dec_seq_len, prob.sm_scale)
+    g.compare(o, ro)
+
+
+def test_decode_bad_slot_is_flagged():
+    g = _gpu()
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.few_shot_decode(hq=8, hkv=8, d=128, batch=4, shared=40, private=20, num_slots=512)
+    prob.req_to_token = prob.req_to_token.copy()
+    prob.req_to_token[2, 45] = prob.num_slots + 100
+    dev = g.Dev(prob)
+    dev.kv_store()
+    o, _ = dev.decode(plan=False)
+    assert dev.status_word() & rx.RX_DEV_BAD_SLOT
+    assert np.isfinite(o).all()
+
+
+def test_decode_length_past_bound_is_flagged():
+    g = _gpu()
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.few_shot_decode(hq=8, hkv=8, d=64, batch=3, shared=400, private=200, num_slots=2048)
+    dev = g.Dev(prob)
+    dev.kv_store()
+    p = prob
+    q = g.to_dev(p.q_dec)
+    o = torch.zeros_like(q)
+    # claim max_seq_len far below the real lengths (601): the grid covers one
+    # 64-position chunk, so the rows are skipped and flagged
+    rx.rx_attn_decode(dev.k_pool, dev.v_pool, q, o, None, g.i32(p.dec_req_idx), g.i32(p.dec_seq_len),
+                      dev.rtt, 10, p.sm_scale, None, None, dev.status)
+    torch.cuda.synchronize()
+    assert dev.status_word() & rx.RX_DEV_BAD_LEN
+
+
+# ---------------------------------------------------------------------------
+# invariants on the GPU
+# ---------------------------------------------------------------------------
+
+
+def test_grouped_equals_ungrouped():
+    """Reading shared KV once per group gives the per-request result."""
+    g = _gpu()
+    prob = inputs.tree_of_thought_decode(depth=3, fanout=3, edge=90, num_slots=8192)
+    dev = g.Dev(prob)
+    dev.kv_store()
+    o1, l1 = dev.decode(plan=False)
+    o2, l2 = dev.decode(plan=True, kv_chunk=64, min_shared=1)
+    assert np.max(np.abs(o1 - o2)) <= 2 * g.ATOL
+    assert np.max(np.abs(l1 - l2)) <= 2 * g.LSE_ATOL
+
+
+def test_slot_permutation_bit_identical():
+    """Renaming pool rows (and req_to_token with them) changes no output bit."""
+    g = _gpu()
+    prob = inputs.few_shot_decode(hq=8, hkv=2, d=128, batch=6, shared=150, private=70, num_slots=2048)
+    dev = g.Dev(prob)
+    dev.kv_store()
+    o1, l1 = dev.decode(plan=False)
+    perm = np.random.default_rng(9).permutation(prob.num_slots).astype(np.int32)
+    prob2 = inputs.few_shot_decode(hq=8, hkv=2, d=128, batch=6, shared=150, private=70, num_slots=2048)
+    prob2.req_to_token = np.where(prob.req_to_token >= 0, perm[np.maximum(prob.req_to_token, 0)], -1)
+    prob2.cached_slots = perm[prob.cached_slots]
+    prob2.new_slots = perm[prob.new_slots]
+    dev2 = g.Dev(prob2)
+    dev2.kv_store()
+    o2, l2 = dev2.decode(plan=False)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_decode_equals_last_extend_row():
+    g = _gpu()
+    prob = inputs.tiny_extend(seed=77, hq=8, hkv=2, d=128, batch=3, prefix=100, extend=40,
+                              num_slots=1024)
+    dev = g.Dev(prob)
+    dev.kv_store()
+    oe, le = dev.extend()
+    last = prob.qo_indptr[1:] - 1
+    prob.q_dec = prob.q_ext[last]
+    prob.dec_req_idx = prob.ext_req_idx
+    prob.dec_seq_len = prob.ext_prefix_len + prob.ext_extend_len
+    od, ld = dev.decode(plan=False)
+    assert np.max(np.abs(od - oe[last])) <= 2 * g.ATOL

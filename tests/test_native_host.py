@@ -1,0 +1,375 @@
+"""Host side of librx on the CPU: ABI surface, radix tree, admission, plans.
+
+* the library loads and exports every function ``include/rx.h`` declares;
+* the C++ radix tree matches the oracle trie bit for bit (prefix lengths, slot
+  lists, freed-slot sequences, tree shape) on the nine-step walkthrough, on
+  seeded random operation sequences with locks and on hypothesis sequences;
+* rx_admit / rx_commit match the same steps composed from the oracle;
+* decode plans partition every request's context exactly once, group only
+  requests that really share slots, and find the radix structure of the
+  workload families;
+* error codes for bad arguments and short capacities.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle.tree_ref import RadixTreeRef
+from prefix_shared_kv_radixattention_gb300 import binding as rx
+from prefix_shared_kv_radixattention_gb300 import inputs
+from tests import _walkthrough
+from tests.test_tree_oracle import _apply, _random_ops
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "rx.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(rx_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_function():
+    names = declared_functions()
+    assert len(names) >= 20
+    lib = rx.library()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert rx.version() == 1
+
+
+# ---------------------------------------------------------------------------
+# radix tree
+# ---------------------------------------------------------------------------
+
+
+class _NativeAdapter:
+    def __init__(self):
+        self.t = rx.RadixTree()
+
+    def match_prefix(self, toks):
+        return self.t.match_prefix(toks)
+
+    def insert(self, toks, slots):
+        return self.t.insert(toks, slots)
+
+    def evict(self, n):
+        return self.t.evict(n)
+
+    def lock(self, toks, delta):
+        try:
+            return self.t.lock(toks, delta)
+        except rx.RxError as e:
+            if e.code == rx.RX_ERR_INVALID:
+                raise ValueError(str(e))
+            raise
+
+    def nodes(self):
+        return self.t.nodes()
+
+
+def test_walkthrough_native_matches_fixture():
+    spec = _walkthrough.load()
+    for step, ri, obs, exp in _walkthrough.run(_NativeAdapter(), spec):
+        if ri is None:
+            assert obs["nodes"] == exp["nodes"], f"step {step}"
+        else:
+            assert obs["matched"] == exp["matched"], f"step {step}"
+            assert obs["cached"] == len(exp["matched"]), f"step {step}"
+            assert obs["evicted_nodes"] == exp["evicted_nodes"], f"step {step}"
+
+
+def test_walkthrough_native_equals_oracle_slots():
+    spec = _walkthrough.load()
+    a = list(_walkthrough.run(RadixTreeRef(), spec))
+    b = list(_walkthrough.run(_NativeAdapter(), spec))
+    for (sa, ra, oa, _), (sb, rb, ob, _) in zip(a, b):
+        assert (sa, ra) == (sb, rb)
+        if ra is not None:
+            assert oa["freed"] == ob["freed"]
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_native_tree_vs_oracle_random(seed):
+    ref, nat = RadixTreeRef(), _NativeAdapter()
+    for op in _random_ops(seed, n_ops=80):
+        a, b = _apply(ref, op), _apply(nat, op)
+        if op[0] == "match":
+            assert a[0] == b[0] and list(a[1]) == list(b[1]), op
+        else:
+            assert a == b, op
+        assert ref.nodes() == nat.nodes(), op
+    c, n, e = nat.t.stats()
+    assert c == ref.cached_tokens and n == ref.num_nodes() and e == ref.evictable_tokens()
+
+
+def test_native_tree_vs_oracle_hypothesis():
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+    op = st.one_of(
+        st.tuples(st.just("insert"), st.lists(st.integers(0, 3), min_size=1, max_size=10)),
+        st.tuples(st.just("match"), st.lists(st.integers(0, 3), min_size=0, max_size=10)),
+        st.tuples(st.just("evict"), st.integers(0, 15)),
+        st.tuples(st.just("lock"), st.lists(st.integers(0, 3), min_size=0, max_size=10)),
+    )
+
+    @hyp.settings(max_examples=200, deadline=None)
+    @hyp.given(st.lists(op, max_size=50))
+    def check(ops):
+        ref, nat = RadixTreeRef(), _NativeAdapter()
+        nxt, held = 0, []
+        for o in ops:
+            if o[0] == "insert":
+                o = ("insert", o[1], list(range(nxt, nxt + len(o[1]))))
+                nxt += len(o[1])
+            elif o[0] == "lock":
+                if held and len(o[1]) % 2 == 1:
+                    o = ("unlock", held.pop(), -1)
+                else:
+                    k = ref.lock(o[1], 1)
+                    ref.lock(o[1][:k], -1)   # probe the length, undo
+                    held.append(o[1][:k])
+                    o = ("lock", o[1][:k], 1)
+            a, b = _apply(ref, o), _apply(nat, o)
+            if o[0] == "match":
+                assert a[0] == b[0] and list(a[1]) == list(b[1])
+            else:
+                assert a == b
+            assert ref.nodes() == nat.nodes()
+
+    check()
+
+
+def test_evict_capacity_and_not_enough():
+    t = rx.RadixTree()
+    t.insert([1, 2, 3], [10, 11, 12])
+    t.insert([4], [20])
+    with pytest.raises(rx.RxError) as e:
+        t.evict(4, cap=2)
+    assert e.value.code == rx.RX_ERR_CAPACITY
+    assert t.evict(100) == [10, 11, 12, 20]      # partial: NOT_ENOUGH reported as a list
+    assert t.stats() == (0, 0, 0)
+
+
+def test_locked_nodes_survive_eviction():
+    t = rx.RadixTree()
+    t.insert([1, 2, 3], [10, 11, 12])
+    t.insert([5, 6], [20, 21])
+    assert t.lock([1, 2, 3, 4], 1) == 3
+    assert t.evict(10) == [20, 21]
+    assert t.stats() == (3, 1, 0)
+    t.insert([7, 8], [30, 31])
+    with pytest.raises(rx.RxError) as e:
+        t.lock([7], -1)                       # never locked
+    assert e.value.code == rx.RX_ERR_INVALID
+    assert t.lock([1, 2], -1) == 2            # tokens 1, 2 unlocked; 3 still locked
+    assert t.evict(10) == [30, 31]            # the node [1 2 3] still holds a locked token
+    assert t.lock([1, 2, 3], 1) == 3 and t.lock([1, 2, 3], -1) == 3
+    assert t.lock([3], -1) == 0               # not a cached prefix: nothing to unlock
+    assert t.lock([1, 2, 3][:0], -1) == 0
+
+
+def test_match_capacity_error_code():
+    t = rx.RadixTree()
+    t.insert([1, 2, 3], [10, 11, 12])
+    import ctypes
+    toks = np.array([1, 2, 3], np.int64)
+    out = np.zeros(1, np.int32)
+    k = ctypes.c_int64()
+    rc = rx.library().rx_match_prefix(t._h, toks.ctypes.data_as(ctypes.c_void_p), 3,
+                                      out.ctypes.data_as(ctypes.c_void_p), 1, ctypes.byref(k))
+    assert rc == rx.RX_ERR_CAPACITY and k.value == 3
+    assert "capacity" in rx.last_error()
+
+
+def test_invalid_arguments():
+    lib = rx.library()
+    import ctypes
+    assert lib.rx_tree_create(None) == rx.RX_ERR_INVALID
+    assert lib.rx_insert(None, None, None, 0, None) == rx.RX_ERR_INVALID
+    assert lib.rx_kv_store(None, None, None, None, 0, None, None) == rx.RX_ERR_INVALID
+    assert lib.rx_attn_decode(None, None, None, None, 0, None, None, None, 0, 0, 0, None, None, 0,
+                              ctypes.c_float(1.0), None, None) == rx.RX_ERR_INVALID
+    assert lib.rx_attn_extend(None, None, None, None, 0, None, None, None, None, None, 0, 0, 0,
+                              ctypes.c_float(1.0), None, None) == rx.RX_ERR_INVALID
+    with pytest.raises(rx.RxError):
+        rx.SlotAllocator([0, 5], 3)
+    a = rx.SlotAllocator([0, 1, 2], 3)
+    with pytest.raises(rx.RxError) as e:
+        a.take(4)
+    assert e.value.code == rx.RX_ERR_NOT_ENOUGH and a.free_count() == 3
+
+
+# ---------------------------------------------------------------------------
+# admission
+# ---------------------------------------------------------------------------
+
+
+class OracleAdmission:
+    """rx_admit / rx_commit composed from the oracle trie and a FIFO list."""
+
+    def __init__(self, free):
+        self.t = RadixTreeRef()
+        self.free = list(free)
+
+    def admit(self, toks):
+        k, slots = self.t.match_prefix(toks)
+        self.t.lock(toks[:k], 1)
+        need = len(toks) - k
+        ev = 0
+        if len(self.free) < need:
+            got = self.t.evict(need - len(self.free))
+            ev = len(got)
+            self.free.extend(got)
+        if len(self.free) < need:
+            self.t.lock(toks[:k], -1)
+            return None, k, ev
+        new, self.free = self.free[:need], self.free[need:]
+        return list(slots) + new, k, ev
+
+    def commit(self, toks, row, k):
+        self.t.lock(toks[:k], -1)
+        c = self.t.insert(toks, row)
+        if c > k:
+            self.free.extend(row[k:c])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_admit_commit_vs_oracle(seed):
+    rng = np.random.default_rng(seed)
+    S = 60
+    free = rng.permutation(S).astype(np.int32)
+    nat_t, nat_a = rx.RadixTree(), rx.SlotAllocator(free, S)
+    ref = OracleAdmission(free.tolist())
+    pending = []
+    for step in range(40):
+        if pending and rng.random() < 0.5:
+            toks, row, k = pending.pop(rng.integers(len(pending)))
+            rx.rx_commit(nat_t, nat_a, toks, row, k)
+            ref.commit(toks, list(row), k)
+        else:
+            base = [int(x) for x in rng.integers(0, 3, size=rng.integers(1, 4))]
+            toks = base + [int(x) for x in rng.integers(0, 6, size=rng.integers(1, 12))]
+            exp_row, exp_k, exp_ev = ref.admit(toks)
+            try:
+                row, k, ev = rx.rx_admit(nat_t, nat_a, toks)
+            except rx.RxError as e:
+                assert e.code == rx.RX_ERR_NOT_ENOUGH and exp_row is None
+                continue
+            assert exp_row is not None and row.tolist() == exp_row and k == exp_k and ev == exp_ev
+            pending.append((toks, row, k))
+        assert nat_t.nodes() == ref.t.nodes()
+        assert nat_a.free_count() == len(ref.free)
+
+
+# ---------------------------------------------------------------------------
+# decode plans
+# ---------------------------------------------------------------------------
+
+
+def _plan(prob, kv_chunk=0, min_shared=16):
+    buf, info = rx.rx_decode_plan_build(prob.req_to_token, prob.dec_req_idx, prob.dec_seq_len,
+                                        prob.hq, prob.hkv, kv_chunk, min_shared)
+    B = len(prob.dec_req_idx)
+    order = buf[:B]
+    nparts = buf[B:2 * B]
+    items = buf[2 * B:].reshape(-1, 8)
+    return order, nparts, items, info
+
+
+def check_plan(prob, order, nparts, items, info):
+    B = len(prob.dec_req_idx)
+    G = prob.hq // prob.hkv
+    assert sorted(order.tolist()) == list(range(B))
+    cover = [np.zeros(int(L), np.int32) for L in prob.dec_seq_len]
+    parts = [[] for _ in range(B)]
+    reads = 0
+    for r0, nr, p0, p1, part, fin, z0, z1 in items.tolist():
+        assert 1 <= nr and nr * G <= 64 and p0 < p1 and z0 == z1 == 0
+        assert p1 - p0 <= info.kv_chunk
+        reqs = [int(order[r]) for r in range(r0, r0 + nr)]
+        rows = [prob.req_to_token[prob.dec_req_idx[b], p0:p1] for b in reqs]
+        for rr in rows[1:]:
+            assert np.array_equal(rr, rows[0]), "grouped requests must share slots"
+        for b in reqs:
+            cover[b][p0:p1] += 1
+            parts[b].append(part)
+            assert bool(fin) == (nparts[b] == 1)
+        reads += p1 - p0
+    assert reads * 1 >= info.tokens_read
+    for b in range(B):
+        assert np.all(cover[b] == 1), f"request {b} context not covered exactly once"
+        assert sorted(parts[b]) == list(range(int(nparts[b])))
+    assert info.max_parts == int(nparts.max())
+
+
+@pytest.mark.parametrize("seed", range(15))
+def test_plan_partitions_ragged(seed):
+    prob = inputs.ragged(100 + seed, hq=8, hkv=2, d=64, n_groups=3, per_group=int(2 + seed % 4),
+                         shared_max=300, private_max=200, extend_max=1, decode=True, num_slots=5000)
+    for kv_chunk, min_shared in ((64, 1), (128, 16), (0, 16), (4096, 64)):
+        order, nparts, items, info = _plan(prob, kv_chunk, min_shared)
+        check_plan(prob, order, nparts, items, info)
+
+
+def test_plan_structure_few_shot():
+    prob = inputs.few_shot_decode(draw_values=False)
+    order, nparts, items, info = _plan(prob)
+    check_plan(prob, order, nparts, items, info)
+    assert info.n_segments == 1 and info.shared_tokens == 1024
+    assert info.tokens_read == 1024 + 64 * 257 == prob.decode_unique_tokens()
+
+
+def test_plan_structure_tree_of_thought():
+    prob = inputs.tree_of_thought_decode(draw_values=False)
+    order, nparts, items, info = _plan(prob)
+    check_plan(prob, order, nparts, items, info)
+    assert info.n_segments == 4 + 16 + 64
+    assert info.shared_tokens == 84 * 256
+    assert info.tokens_read == prob.decode_unique_tokens() == 340 * 256 + 256
+
+
+def test_plan_structure_mixed_chat():
+    prob = inputs.mixed_chat(draw_values=False)
+    order, nparts, items, info = _plan(prob)
+    check_plan(prob, order, nparts, items, info)
+    assert info.n_segments == 1 and info.shared_tokens == 8192
+    assert info.tokens_read == prob.decode_unique_tokens()
+
+
+def test_plan_min_shared_folds_short_segments():
+    prob = inputs.tree_of_thought_decode(depth=3, fanout=3, edge=8, draw_values=False)
+    # edges of 8 tokens: level 1 spans [0, 8), level 2 [8, 16)
+    order, nparts, items, info = _plan(prob, 64, min_shared=8)
+    check_plan(prob, order, nparts, items, info)
+    assert info.n_segments == 3 + 9 and info.shared_tokens == 12 * 8
+    # level 1 is too short on its own and is folded into the level-2 segments
+    order, nparts, items, info = _plan(prob, 64, min_shared=9)
+    check_plan(prob, order, nparts, items, info)
+    assert info.n_segments == 9 and info.shared_tokens == 9 * 16
+    order, nparts, items, info = _plan(prob, 64, min_shared=17)
+    check_plan(prob, order, nparts, items, info)
+    assert info.n_segments == 0 and info.tokens_read == 27 * 25
+
+
+def test_plan_identical_requests():
+    prob = inputs.few_shot_decode(batch=3, shared=100, private=0, hq=4, hkv=4, d=64, num_slots=400,
+                                  draw_values=False)
+    rtt = prob.req_to_token.copy()
+    rtt[1] = rtt[0]
+    prob.req_to_token = rtt
+    order, nparts, items, info = _plan(prob, 64, 1)
+    check_plan(prob, order, nparts, items, info)
+
+
+def test_plan_invalid():
+    prob = inputs.few_shot_decode(batch=2, shared=10, private=5, hq=4, hkv=4, d=64, num_slots=100,
+                                  draw_values=False)
+    with pytest.raises(rx.RxError) as e:
+        rx.rx_decode_plan_build(prob.req_to_token, prob.dec_req_idx, prob.dec_seq_len, 4, 4, 100, 1)
+    assert e.value.code == rx.RX_ERR_INVALID
+    with pytest.raises(rx.RxError) as e:
+        rx.rx_decode_plan_build(prob.req_to_token, prob.dec_req_idx, prob.dec_seq_len, 128, 1, 64, 1)
+    assert e.value.code == rx.RX_ERR_UNSUPPORTED

@@ -66,6 +66,7 @@ class BruteTree:
 
     def __init__(self):
         self.slot = {}
+        self.locked = Counter()
         self.start = set()
         self.last = {}
         self.clock = 0
@@ -115,6 +116,19 @@ class BruteTree:
             self.last[p] = self.clock
         return k
 
+    def lock(self, toks, delta):
+        if delta > 0:
+            self.clock += 1
+        k = self._matched(toks)
+        ps = [tuple(toks[:i + 1]) for i in range(k)]
+        if delta < 0 and any(self.locked[p] == 0 for p in ps):
+            raise ValueError("unlock without lock")
+        if delta > 0:
+            self._touch(toks, k)
+        for p in ps:
+            self.locked[p] += delta
+        return k
+
     def evict(self, n):
         freed = []
         while len(freed) < n and self.slot:
@@ -123,7 +137,10 @@ class BruteTree:
             cands = {}
             for leaf in leaves:
                 s = self._node_start(leaf)
-                cands[s] = leaf
+                if all(self.locked[leaf[:L]] == 0 for L in range(len(s), len(leaf) + 1)):
+                    cands[s] = leaf
+            if not cands:
+                break
             s = min(cands, key=lambda q: self.last[q])
             leaf = cands[s]
             for L in range(len(s), len(leaf) + 1):
@@ -151,10 +168,17 @@ def _random_ops(seed, n_ops=60, alphabet=4, max_len=9):
     rng = random.Random(seed)
     next_slot = [0]
     ops = []
+    held = []
     for _ in range(n_ops):
-        kind = rng.choices(["insert", "match", "evict"], weights=[5, 3, 2])[0]
+        kind = rng.choices(["insert", "match", "evict", "lock", "unlock"], weights=[5, 3, 2, 1, 1])[0]
         toks = [rng.randrange(alphabet) for _ in range(rng.randrange(1, max_len))]
-        if kind == "evict":
+        if kind == "lock":
+            held.append(toks)
+            ops.append(("lock", toks, 1))
+        elif kind == "unlock":
+            if held:
+                ops.append(("unlock", held.pop(rng.randrange(len(held))), -1))
+        elif kind == "evict":
             ops.append(("evict", rng.randrange(1, 12)))
         elif kind == "match":
             ops.append(("match", toks))
@@ -166,6 +190,11 @@ def _random_ops(seed, n_ops=60, alphabet=4, max_len=9):
 
 
 def _apply(tree, op):
+    if op[0] in ("lock", "unlock"):
+        try:
+            return tree.lock(op[1], op[2])
+        except ValueError:
+            return "unlock-error"
     if op[0] == "insert":
         return tree.insert(op[1], op[2])
     if op[0] == "match":
