@@ -37,7 +37,8 @@
  *   - No exception, abort or device trap crosses this ABI.
  *   - "device" pointers are CUDA global memory on the current device; "host"
  *     pointers are ordinary process memory.  The caller owns every buffer;
- *     the library allocates no device memory.
+ *     the library allocates no device memory.  bf16 tensors (pools, q, o, new
+ *     K/V) must start on a 16-byte boundary (RX_ERR_INVALID otherwise).
  *   - GPU entry points are asynchronous on `stream` (a cudaStream_t passed as
  *     void*, NULL = legacy default stream) and return after validation and
  *     launch.  Errors found by kernels (an out-of-range slot id or length) are OR-ed as
@@ -68,8 +69,10 @@ extern "C" {
 #define RX_ERR_UNSUPPORTED (-6) /* shape the kernels are not built for         */
 
 #define RX_DEV_BAD_SLOT 1       /* a kernel met a slot id outside the pool     */
-#define RX_DEV_BAD_LEN 2        /* a device length exceeded its host bound or  
+#define RX_DEV_BAD_LEN 2        /* a device length exceeded its host bound or
                                    the req_to_token stride; rows left unwritten */
+#define RX_DEV_TIMEOUT 4        /* a pipeline wait gave up (never expected; the
+                                   kernel stopped early, outputs incomplete)   */
 
 /* Message for the last failed call on this thread ("" if none). */
 const char *rx_last_error(void);
@@ -254,8 +257,9 @@ typedef struct {
  * form a segment; segments nest like the radix tree the slots came from.
  * Packed output (host int32, capacity out_cap words): order [batch], nparts
  * [batch], then items [n_items][8] = {first plan row, row count, pos_begin,
- * pos_end, part index, is_final, 0, 0}.  RX_ERR_CAPACITY (info->buf_words
- * set) if out_cap is too small. */
+ * pos_end, part index, is_final, req_to_token row of the first request (its
+ * req_idx), batch index of the first request}.  RX_ERR_CAPACITY
+ * (info->buf_words set) if out_cap is too small. */
 int rx_decode_plan_build(const int32_t *req_to_token, int64_t rtt_stride, const int32_t *req_idx,
                          const int32_t *seq_len, int32_t batch, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t kv_chunk, int32_t min_shared,

@@ -1,37 +1,20 @@
-// rx_attn_rows.cu -- slot-gathered attention of up to 64 query rows per CTA
-// against one kv head, on the mma.sync tensor path, plus the log-sum-exp merge
-// of split results.  Serves decode (with or without a decode plan).
+// rx_attn_rows.cu -- extend attention on the mma.sync tensor path: up to 64
+// query rows (64 / G new tokens of one request times the G q-heads of one kv
+// head) per CTA against the slot-gathered keys 0 .. prefix + last token, each
+// row masked at its own causal bound j <= p.
 //
-// What is computed: for each query row (request b at position p, q-head h,
-// kv-head g = h / G) o = softmax(sm_scale * q K^T) V over the pool rows listed
-// in req_to_token[b][0..p] (north of the path: softmax(QK^T/sqrt(d) + causal
-// mask) V over per-request slot lists).  A CTA takes one work item: a set of
-// query rows that all read the same positions [p0, p1) of the same slot list,
-// i.e. the requests below one shared radix node ("SGLang: Efficient Execution
-// of Structured Language Model Programs", unite.ai, es, section "SGLang:
-// Modelo de programación y metodología": requests that share a prefix share
-// its KV), times the G q-heads of one kv head.  The shared KV is therefore
-// read from HBM once per group.
+// What is computed: o = softmax(sm_scale * q K^T + causal mask) V over the
+// pool rows listed in req_to_token[b][0..p] (kv-head g = h / G), the extend
+// pass of RadixAttention: new tokens attend to their cached prefix plus
+// themselves ("SGLang: Efficient Execution of Structured Language Model
+// Programs", unite.ai, es, section "Introducción a SGLang": KV of a shared
+// prefix is reused, not recomputed).
 //
-// Data path (HBM-bound; the contraction is small, so the legacy m16n8k16
-// tensor path is ample):
-//   - slot ids are prefetched one pipeline step ahead into registers;
-//   - K and V rows (head_dim * 2 bytes each) are gathered with 16-byte
-//     cp.async into a 3-stage shared-memory ring of 64-key tiles, stored with
-//     an XOR swizzle of the 16-byte chunks so ldmatrix reads are conflict-free;
-//   - S = Q K^T and O += P V on mma.sync with fp32 accumulators; online
-//     softmax in the exp2 domain with quad shuffles;
-//   - 4 warps split the rows (16 per warp) when a work item has many rows and
-//     split the keys of each tile when it has few; key-split partials are
-//     combined through shared memory at the end.
-// A work item that covers a row's whole context writes bf16 o directly;
-// otherwise it writes a normalised fp32 partial and its log2-sum-exp, and
-// merge_kernel combines the partials (o = sum_s w_s o_s / sum_s w_s with
-// w_s = 2^(lse_s - max lse)).
-//
-// The same kernel also runs extend rows (kExtend): 64 / G new tokens of one
-// request times the G q-heads, keys 0 .. prefix + last token, each row masked
-// at its own causal bound j <= p.
+// Data path: slot ids prefetched one pipeline step ahead into registers; K
+// and V rows gathered with 16-byte cp.async into a 3-stage shared-memory ring
+// of 64-key tiles (16-byte chunks XOR-swizzled for conflict-free ldmatrix);
+// S = Q K^T and O += P V on mma.sync m16n8k16 with fp32 accumulators; online
+// softmax in the exp2 domain.
 #include <math.h>
 
 #include "rx_common.cuh"
@@ -45,7 +28,7 @@ constexpr int kStages = 3;    // cp.async ring depth
 constexpr int kThreads = 128; // 4 warps
 constexpr int kMaxRows = 64;  // query rows per CTA
 
-enum Mode { kDecodeGrid = 0, kDecodePlan = 1, kExtend = 2 };
+enum Mode { kExtend = 2 };
 
 struct Params {
     const bf16 *q;
@@ -89,9 +72,7 @@ struct Work {
 template <int MODE>
 __device__ __forceinline__ int64_t qrow_of(const Params &p, const Work &w, int m)
 {
-    if (MODE == kDecodePlan) return __ldg(p.order + w.r0 + m / p.G);
-    if (MODE == kExtend) return w.qbase + m / p.G;
-    return w.b;
+    return w.qbase + m / p.G;
 }
 
 template <int D, int WM, int MODE>
@@ -370,17 +351,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_rows_kernel(const Params p)
     extern __shared__ __align__(128) unsigned char smem[];
     Work w;
     const int g = blockIdx.y;
-    if (MODE == kDecodePlan) {
-        const int32_t *it = p.items + 8 * (int64_t)blockIdx.x;
-        w.r0 = __ldg(it + 0);
-        w.M = __ldg(it + 1) * p.G;
-        w.p0 = __ldg(it + 2);
-        w.p1 = __ldg(it + 3);
-        w.part = __ldg(it + 4);
-        w.final_ = __ldg(it + 5) != 0;
-        w.b = 0;
-        w.slots = p.rtt + (int64_t)__ldg(p.req_idx + __ldg(p.order + w.r0)) * p.rtt_stride;
-    } else if (MODE == kExtend) {
+    {
         const int b = blockIdx.z;
         const int tb = kMaxRows / p.G;  // tokens per CTA
         const int E = __ldg(p.extend_len + b);
@@ -408,24 +379,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_rows_kernel(const Params p)
         w.qbase = (int64_t)__ldg(p.qo_indptr + b) + t0;
         w.cbase = P + t0;
         w.slots = p.rtt + (int64_t)__ldg(p.req_idx + b) * p.rtt_stride;
-    } else {
-        const int b = blockIdx.z;
-        const int64_t L = __ldg(p.seq_len + b);
-        if (L > (int64_t)gridDim.x * p.chunk || L > p.rtt_stride) {  // past max_seq_len
-            if (p.status && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
-                atomicOr(p.status, RX_DEV_BAD_LEN);
-            return;
-        }
-        const int64_t p0 = (int64_t)blockIdx.x * p.chunk;
-        if (p0 >= L) return;
-        w.b = b;
-        w.r0 = 0;
-        w.M = p.G;
-        w.p0 = p0;
-        w.p1 = min(L, p0 + (int64_t)p.chunk);
-        w.part = blockIdx.x;
-        w.final_ = L <= p.chunk;
-        w.slots = p.rtt + (int64_t)__ldg(p.req_idx + b) * p.rtt_stride;
     }
     if (w.M <= 0 || w.p1 <= w.p0) return;
     if (w.M <= 16)
@@ -434,50 +387,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_rows_kernel(const Params p)
         attn_rows_body<D, 2, MODE>(p, w, g, smem);
     else
         attn_rows_body<D, 4, MODE>(p, w, g, smem);
-}
-
-template <int D>
-__global__ void __launch_bounds__(128) merge_kernel(const Params p, int use_plan)
-{
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * 4 + warp;
-    if (row >= (int64_t)p.batch * p.hq) return;
-    const int b = (int)(row / p.hq);
-    const int np = use_plan ? __ldg(p.nparts + b)
-                            : (int)((__ldg(p.seq_len + b) + p.chunk - 1) / p.chunk);
-    if (np <= 1 || np > p.max_parts) return;  // > max_parts: flagged by the row kernel
-    const float *lp = p.ws_lse + row * p.max_parts;
-    float m = -INFINITY;
-    for (int i = lane; i < np; i += 32) m = fmaxf(m, lp[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    constexpr int PER = D / 32;
-    float acc[PER];
-#pragma unroll
-    for (int j = 0; j < PER; ++j) acc[j] = 0.f;
-    float wsum = 0.f;
-    for (int i = 0; i < np; ++i) {
-        const float wgt = rx::fast_exp2(lp[i] - m);
-        wsum += wgt;
-        const float *src = p.ws_o + (row * p.max_parts + i) * D + lane * PER;
-        if constexpr (PER == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(src);
-            acc[0] += wgt * v.x;
-            acc[1] += wgt * v.y;
-            acc[2] += wgt * v.z;
-            acc[3] += wgt * v.w;
-        } else {
-            const float2 v = *reinterpret_cast<const float2 *>(src);
-            acc[0] += wgt * v.x;
-            acc[1] += wgt * v.y;
-        }
-    }
-    const float inv = 1.f / wsum;
-    bf16 *dst = p.o + row * D + lane * PER;
-#pragma unroll
-    for (int j = 0; j < PER; j += 2)
-        *reinterpret_cast<uint32_t *>(dst + j) = rx::pack_bf16(acc[j] * inv, acc[j + 1] * inv);
-    if (p.lse && lane == 0) p.lse[row] = (m + log2f(wsum)) * rx::kLn2;
 }
 
 constexpr size_t smem_bytes(int D) { return (size_t)(kMaxRows + 2 * kStages * kBN) * D * 2; }
@@ -497,15 +406,6 @@ int launch_rows(const Params &p, dim3 grid, cudaStream_t st)
     return RX_OK;
 }
 
-template <int D>
-int launch_merge(const Params &p, int use_plan, cudaStream_t st)
-{
-    const int64_t rows = (int64_t)p.batch * p.hq;
-    merge_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(p, use_plan);
-    RX_CUDA_CHECK(cudaGetLastError());
-    return RX_OK;
-}
-
 int check_pool(const rx_kv_pool *pool, const char *fn)
 {
     if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0)
@@ -517,105 +417,6 @@ int check_pool(const rx_kv_pool *pool, const char *fn)
 }
 
 }  // namespace
-
-int32_t rx_decode_default_chunk(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len)
-{
-    const int64_t total = (int64_t)batch * num_kv_heads * (int64_t)max_seq_len;
-    int64_t c = (total + RX_DECODE_TARGET_ITEMS - 1) / RX_DECODE_TARGET_ITEMS;
-    c = (c + 63) / 64 * 64;
-    if (c < 64) c = 64;
-    if (c > RX_MAX_KV_CHUNK) c = RX_MAX_KV_CHUNK;
-    return (int32_t)c;
-}
-
-extern "C" size_t rx_attn_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                                           int32_t head_dim, int32_t max_seq_len,
-                                           const rx_decode_plan *plan)
-{
-    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seq_len <= 0)
-        return 0;
-    int64_t parts;
-    if (plan) {
-        parts = plan->max_parts;
-    } else {
-        const int64_t c = rx_decode_default_chunk(batch, num_kv_heads, max_seq_len);
-        parts = (max_seq_len + c - 1) / c;
-    }
-    if (parts <= 1) return 0;
-    const int64_t rows = (int64_t)batch * num_q_heads * parts;
-    const int64_t bytes = rows * (head_dim + 1) * 4;
-    return (size_t)((bytes + 255) / 256 * 256);
-}
-
-extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, float *lse,
-                              int32_t hq, const int32_t *req_idx, const int32_t *seq_len,
-                              const int32_t *rtt, int64_t rtt_stride, int32_t batch,
-                              int32_t max_seq_len, const rx_decode_plan *plan, void *workspace,
-                              size_t ws_bytes, float sm_scale, int32_t *dev_status, void *stream)
-{
-    int rc = check_pool(pool, "rx_attn_decode");
-    if (rc != RX_OK) return rc;
-    if (!q || !o || !req_idx || !seq_len || !rtt || rtt_stride <= 0 || batch < 0 || hq <= 0 ||
-        max_seq_len <= 0 || max_seq_len > rtt_stride || !(sm_scale > 0.f))
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: invalid argument");
-    if (hq % pool->num_kv_heads != 0 || 64 % (hq / pool->num_kv_heads) != 0)
-        return rx_set_error(RX_ERR_UNSUPPORTED,
-                            "rx_attn_decode: %d q heads over %d kv heads (need G | 64)", hq,
-                            pool->num_kv_heads);
-    if (plan && (!plan->order || !plan->nparts || !plan->items || plan->n_items < 0 ||
-                 plan->max_parts < 1))
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: invalid plan");
-    if (batch == 0) return RX_OK;
-    const int D = pool->head_dim;
-    Params p{};
-    p.q = (const bf16 *)q;
-    p.o = (bf16 *)o;
-    p.lse = lse;
-    p.k_pool = (const bf16 *)pool->k;
-    p.v_pool = (const bf16 *)pool->v;
-    p.num_slots = pool->num_slots;
-    p.hq = hq;
-    p.hkv = pool->num_kv_heads;
-    p.G = hq / pool->num_kv_heads;
-    p.req_idx = req_idx;
-    p.seq_len = seq_len;
-    p.rtt = rtt;
-    p.rtt_stride = rtt_stride;
-    p.batch = batch;
-    p.scale_log2 = sm_scale * rx::kLog2e;
-    p.status = dev_status;
-    dim3 grid;
-    if (plan) {
-        p.order = plan->order;
-        p.nparts = plan->nparts;
-        p.items = plan->items;
-        p.max_parts = plan->max_parts;
-        p.chunk = 0;
-        if (plan->n_items == 0) return RX_OK;
-        grid = dim3((unsigned)plan->n_items, (unsigned)p.hkv, 1);
-    } else {
-        p.chunk = rx_decode_default_chunk(batch, p.hkv, max_seq_len);
-        p.max_parts = (max_seq_len + p.chunk - 1) / p.chunk;
-        grid = dim3((unsigned)p.max_parts, (unsigned)p.hkv, (unsigned)batch);
-    }
-    const size_t need = rx_attn_decode_workspace(batch, hq, p.hkv, D, max_seq_len, plan);
-    if (need > 0) {
-        if (!workspace || ws_bytes < need)
-            return rx_set_error(RX_ERR_CAPACITY, "rx_attn_decode: workspace needs %zu bytes, got %zu",
-                                need, ws_bytes);
-        if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
-            return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: workspace must be 256-byte aligned");
-        p.ws_o = (float *)workspace;
-        p.ws_lse = p.ws_o + (int64_t)batch * hq * p.max_parts * D;
-    }
-    cudaStream_t st = (cudaStream_t)stream;
-    if (D == 128)
-        rc = plan ? launch_rows<128, kDecodePlan>(p, grid, st) : launch_rows<128, kDecodeGrid>(p, grid, st);
-    else
-        rc = plan ? launch_rows<64, kDecodePlan>(p, grid, st) : launch_rows<64, kDecodeGrid>(p, grid, st);
-    if (rc != RX_OK || need == 0) return rc;
-    return D == 128 ? launch_merge<128>(p, plan != nullptr, st) : launch_merge<64>(p, plan != nullptr, st);
-}
 
 extern "C" int rx_attn_extend(const rx_kv_pool *pool, const void *q, void *o, float *lse,
                               int32_t hq, const int32_t *qo_indptr, const int32_t *req_idx,
@@ -633,6 +434,9 @@ extern "C" int rx_attn_extend(const rx_kv_pool *pool, const void *q, void *o, fl
         return rx_set_error(RX_ERR_UNSUPPORTED,
                             "rx_attn_extend: %d q heads over %d kv heads (need G | 64)", hq,
                             pool->num_kv_heads);
+    if (rx_misaligned16(q) || rx_misaligned16(o) || rx_misaligned16(pool->k) ||
+        rx_misaligned16(pool->v) || (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_extend: q, o and the pools must be 16-byte aligned");
     if (batch == 0 || max_extend_len == 0) return RX_OK;
     const int D = pool->head_dim;
     Params p{};

@@ -1,0 +1,812 @@
+// rx_decode.cu -- decode attention over the token-slot pool: a persistent,
+// warp-specialised split-KV kernel plus the log-sum-exp merge of split
+// results.
+//
+// What is computed: for each request b (one query at position L_b - 1) and
+// q-head h, o = softmax(sm_scale * q K^T) V over the pool rows listed in
+// req_to_token[b][0 .. L_b-1], kv-head g = h / G.  Work is cut into items:
+// a set of query rows that read the same positions [p0, p1) of the same
+// slot list -- the requests below one shared radix node, times the G q-heads
+// of one kv head -- so the KV of a shared prefix is read from HBM once per
+// group ("SGLang: Efficient Execution of Structured Language Model Programs",
+// unite.ai, es, section "SGLang: Modelo de programación y metodología":
+// requests that share a prefix share its KV).  Items come from a host-built
+// decode plan, or, without one, from a fixed split of every request.
+//
+// The kernel is HBM-bound (about 4 flops per KV byte), so it is built to keep
+// bytes in flight:
+//   - one persistent CTA per SM walks a static round-robin share of the
+//     (item, kv head) list, longest items first;
+//   - a scheduler warp decodes the CTA's items 32 at a time (lane-parallel
+//     loads), publishes each as a descriptor in a 4-deep ring, and prefetches
+//     the slot ids of every 64-key stage with 4-byte cp.async into a 16-deep
+//     slot ring -- so no copy ever waits on a dependent index load;
+//   - three copier warps gather K and V rows (head_dim * 2 contiguous bytes
+//     per row and kv head, 16-byte cp.async, a third of every stage each)
+//     into a ring of 64-key stages, and the query rows into a double-buffered
+//     Q slot; every ring entry is an mbarrier that the copies themselves
+//     complete (cp.async.mbarrier.arrive), so the ring streams across item
+//     boundaries with no per-item fill or drain.  Several issuing warps are
+//     needed: measured on GB300, one warp issuing either 16-byte cp.async or
+//     256-byte bulk copies keeps only a few KB in flight (about 1 TB/s);
+//   - four consumer warps run S = Q K^T and O += P V on mma.sync m16n8k16
+//     (bf16 in, fp32 accumulators; the contraction is small, so the legacy
+//     tensor path is ample) with the online softmax in the exp2 domain; they
+//     split the rows 16 per warp when an item has many rows and split each
+//     stage's keys when it has few, combining key-split partials through
+//     shared memory;
+//   - rows sit at a padded stride of head_dim * 2 + 16 bytes, so the eight
+//     rows an ldmatrix reads fall in distinct banks; stage rows past an
+//     item's end are zero-filled by the copy and their scores masked.
+// An item that covers a row's whole context writes bf16 o directly;
+// otherwise it writes a normalised fp32 partial and its log2-sum-exp, and
+// merge_kernel combines them: o = sum_s w_s o_s / sum_s w_s with
+// w_s = 2^(lse_s - max lse).
+//
+// Every mbarrier wait is bounded; a wait that gives up sets RX_DEV_TIMEOUT,
+// raises a shared abort flag so the other warps stop too, and each copying
+// warp waits for its own copies before the CTA exits.
+#include <math.h>
+
+#include "rx_common.cuh"
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kBN = 64;                      // keys per stage
+constexpr int kCopiers = 7;                  // copier warps
+constexpr int kConsumers = 4;                // consumer warps
+constexpr int kThreads = 32 * (1 + kCopiers + kConsumers);  // scheduler, copiers, consumers
+constexpr int kConsumer0 = 32 * (1 + kCopiers);  // first consumer thread
+constexpr int kMaxRows = 64;                 // query rows per item
+constexpr int kNIT = 4;                      // item descriptor ring
+constexpr int kNSL = 16;                     // slot-id ring (stages)
+constexpr uint32_t kSpinLimit = 1u << 22;    // polls before a wait gives up
+
+// Item descriptor published by the scheduler warp.  M == 0 ends the stream.
+struct Desc {
+    int M, p0, p1, part, final_, g, rtt_row, pad;
+    int qrow[kMaxRows];                      // q/o row of each request of the item
+};
+
+template <int D>
+struct Layout {
+    static constexpr int NST = (D == 128) ? 4 : 8;      // K/V ring stages
+    static constexpr int RS = D + 8;                    // padded row stride (elements)
+    static constexpr int ROWB = D * 2;                  // bytes of one row
+    static constexpr int TILE = kBN * RS;               // elements of one K (or V) stage
+    static constexpr int QSLOT = kMaxRows * RS;         // elements of one Q slot
+    static constexpr int RED_FLOATS = 2 * 4 * 16 + 4 * 16 * D;  // m, l and O of 4 key splits
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + NST * TILE * 2;
+    static constexpr int OFF_Q = OFF_V + NST * TILE * 2;
+    static constexpr int OFF_RED = OFF_Q + 2 * QSLOT * 2;
+    static constexpr int OFF_SLOT = OFF_RED + RED_FLOATS * 4;
+    static constexpr int OFF_DESC = OFF_SLOT + kNSL * kBN * 4;
+    static constexpr int OFF_BAR = OFF_DESC + kNIT * (int)sizeof(Desc);
+    // barrier indices
+    static constexpr int B_FULL = 0, B_EMPTY = NST, B_QFULL = 2 * NST, B_QEMPTY = 2 * NST + 2,
+                         B_SLFULL = 2 * NST + 4, B_SLEMPTY = B_SLFULL + kNSL,
+                         B_ITFULL = B_SLEMPTY + kNSL, B_ITEMPTY = B_ITFULL + kNIT,
+                         N_BAR = B_ITEMPTY + kNIT;
+    static constexpr int OFF_ABORT = OFF_BAR + N_BAR * 8;
+    static constexpr int BYTES = OFF_ABORT + 16;
+};
+static_assert(Layout<128>::BYTES <= 227 * 1024, "shared memory budget");
+static_assert(Layout<64>::BYTES <= 227 * 1024, "shared memory budget");
+
+struct Params {
+    const bf16 *q;
+    bf16 *o;
+    float *lse;
+    const bf16 *k_pool;
+    const bf16 *v_pool;
+    int64_t num_slots;
+    int hq, hkv, G;
+    const int32_t *req_idx;
+    const int32_t *seq_len;
+    const int32_t *rtt;
+    int64_t rtt_stride;
+    const int32_t *order;   // plan
+    const int32_t *nparts;  // plan
+    const int32_t *items;   // plan
+    int batch;
+    int chunk;              // no plan: positions per item
+    int n_chunks;           // no plan: items per request
+    int total_work;         // items x kv heads
+    int max_parts;          // partial-result stride per row
+    float *ws_o;
+    float *ws_lse;
+    float scale_log2;
+    int32_t *status;
+};
+
+struct Item {
+    int M, p0, p1, part, final_, g, rtt_row, qrow0, r0;
+};
+
+// Decodes work index w (one per lane); false when the item is empty.
+template <bool PLAN>
+__device__ __forceinline__ bool get_item(const Params &p, int w, Item &it)
+{
+    it.g = w % p.hkv;
+    const int i = w / p.hkv;
+    if (PLAN) {
+        // scalar loads: the items array is only 4-byte aligned
+        const int32_t *v = p.items + 8 * (int64_t)i;
+        it.r0 = __ldg(v + 0);
+        it.M = __ldg(v + 1) * p.G;
+        it.p0 = __ldg(v + 2);
+        it.p1 = __ldg(v + 3);
+        it.part = __ldg(v + 4);
+        it.final_ = __ldg(v + 5);
+        it.rtt_row = __ldg(v + 6);
+        it.qrow0 = __ldg(v + 7);
+        return it.M > 0 && it.p1 > it.p0;
+    }
+    const int b = i / p.n_chunks, c = i % p.n_chunks;
+    const int64_t L = __ldg(p.seq_len + b);
+    if (L > (int64_t)p.n_chunks * p.chunk || L > p.rtt_stride) {  // past max_seq_len
+        if (c == 0 && it.g == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_LEN);
+        return false;
+    }
+    const int p0 = c * p.chunk;
+    if (p0 >= L) return false;
+    it.r0 = 0;
+    it.M = p.G;
+    it.p0 = p0;
+    it.p1 = (int)min(L, (int64_t)p0 + p.chunk);
+    it.part = c;
+    it.final_ = L <= p.chunk;
+    it.rtt_row = __ldg(p.req_idx + b);
+    it.qrow0 = b;
+    return true;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              int32_t *status)
+{
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (rx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+    }
+    *abort_flag = 1;
+    if (status) atomicOr(status, RX_DEV_TIMEOUT);
+    return false;
+}
+
+__device__ __forceinline__ int mpad_of(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
+
+__device__ __forceinline__ int shfl(int v, int src) { return __shfl_sync(0xffffffffu, v, src); }
+
+// ---------------------------------------------------------------------------
+// scheduler warp: descriptors and slot ids
+// ---------------------------------------------------------------------------
+
+template <int D, bool PLAN>
+__device__ void scheduler(const Params &p, unsigned char *smem)
+{
+    using L = Layout<D>;
+    Desc *descs = reinterpret_cast<Desc *>(smem + L::OFF_DESC);
+    int32_t *slotbuf = reinterpret_cast<int32_t *>(smem + L::OFF_SLOT);
+    const uint32_t bar = rx::smem_u32(smem + L::OFF_BAR);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
+    const int lane = threadIdx.x & 31;
+    uint32_t n_it = 0, n_tile = 0;
+    bool alive = true;
+    auto publish = [&](const Item &it, bool end) -> bool {
+        const uint32_t di = n_it % kNIT;
+        if (!wait_or_abort(bar + 8 * (L::B_ITEMPTY + di), ((n_it / kNIT) & 1) ^ 1, abort_flag, p.status))
+            return false;
+        Desc *d = descs + di;
+        if (lane == 0) {
+            d->M = end ? 0 : it.M;
+            d->p0 = it.p0;
+            d->p1 = it.p1;
+            d->part = it.part;
+            d->final_ = it.final_;
+            d->g = it.g;
+            d->rtt_row = it.rtt_row;
+            d->qrow[0] = it.qrow0;
+        }
+        if (!end && PLAN) {
+            const int nreq = it.M / p.G;
+            for (int i = 1 + lane; i < nreq; i += 32) d->qrow[i] = __ldg(p.order + it.r0 + i);
+        }
+        __syncwarp();
+        if (lane == 0) rx::mbar_arrive(bar + 8 * (L::B_ITFULL + di));
+        ++n_it;
+        return true;
+    };
+    for (int base = 0; alive && blockIdx.x + base * (int)gridDim.x < p.total_work; base += 32) {
+        const int wl = blockIdx.x + (base + lane) * (int)gridDim.x;
+        Item mine{};
+        const bool vl = wl < p.total_work && get_item<PLAN>(p, wl, mine);
+        for (int j = 0; j < 32; ++j) {
+            if (blockIdx.x + (base + j) * (int)gridDim.x >= p.total_work) break;
+            if (!__shfl_sync(0xffffffffu, vl, j)) continue;
+            Item it;
+            it.M = shfl(mine.M, j);
+            it.p0 = shfl(mine.p0, j);
+            it.p1 = shfl(mine.p1, j);
+            it.part = shfl(mine.part, j);
+            it.final_ = shfl(mine.final_, j);
+            it.g = shfl(mine.g, j);
+            it.rtt_row = shfl(mine.rtt_row, j);
+            it.qrow0 = shfl(mine.qrow0, j);
+            it.r0 = shfl(mine.r0, j);
+            if (!publish(it, false)) {
+                alive = false;
+                break;
+            }
+            const int32_t *row = p.rtt + (int64_t)it.rtt_row * p.rtt_stride;
+            const int ntiles = (it.p1 - it.p0 + kBN - 1) / kBN;
+            for (int t = 0; t < ntiles; ++t, ++n_tile) {
+                const uint32_t sb = n_tile % kNSL;
+                if (!wait_or_abort(bar + 8 * (L::B_SLEMPTY + sb), ((n_tile / kNSL) & 1) ^ 1, abort_flag,
+                                   p.status)) {
+                    alive = false;
+                    break;
+                }
+                int32_t *dst = slotbuf + sb * kBN;
+                const int pos = it.p0 + t * kBN + lane;
+                rx::cp_async_4(rx::smem_u32(dst + lane), row + (pos < it.p1 ? pos : 0), pos < it.p1 ? 4 : 0);
+                rx::cp_async_4(rx::smem_u32(dst + lane + 32), row + (pos + 32 < it.p1 ? pos + 32 : 0),
+                               pos + 32 < it.p1 ? 4 : 0);
+                rx::cp_async_mbar_arrive(bar + 8 * (L::B_SLFULL + sb));
+            }
+            if (!alive) break;
+        }
+    }
+    if (alive) publish(Item{}, true);
+    rx::cp_async_wait_all();
+}
+
+// ---------------------------------------------------------------------------
+// copier warp: Q rows and K/V stages
+// ---------------------------------------------------------------------------
+
+template <int D>
+__device__ void copier(const Params &p, unsigned char *smem)
+{
+    using L = Layout<D>;
+    constexpr int CPR = D / 8;                          // 16-byte chunks per row
+    constexpr int NCT = 32 * kCopiers;                  // copier threads
+    bf16 *Ks = reinterpret_cast<bf16 *>(smem + L::OFF_K);
+    bf16 *Vs = reinterpret_cast<bf16 *>(smem + L::OFF_V);
+    bf16 *Qs = reinterpret_cast<bf16 *>(smem + L::OFF_Q);
+    const Desc *descs = reinterpret_cast<const Desc *>(smem + L::OFF_DESC);
+    const int32_t *slotbuf = reinterpret_cast<const int32_t *>(smem + L::OFF_SLOT);
+    const uint32_t bar = rx::smem_u32(smem + L::OFF_BAR);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
+    const int cw = (threadIdx.x >> 5) - 1, lane = threadIdx.x & 31, ct = threadIdx.x - 32;
+    uint32_t n_it = 0, n_tile = 0, qi = 0;
+    for (;; ++n_it) {
+        const uint32_t di = n_it % kNIT;
+        if (!wait_or_abort(bar + 8 * (L::B_ITFULL + di), (n_it / kNIT) & 1, abort_flag, p.status)) break;
+        const Desc *d = descs + di;
+        const int M = d->M, p0 = d->p0, p1 = d->p1, g = d->g;
+        if (M == 0) break;
+        if (cw == 0) {  // query rows -> Q slot (rows past M zero-filled)
+            const uint32_t qs = qi & 1;
+            if (!wait_or_abort(bar + 8 * (L::B_QEMPTY + qs), ((qi >> 1) & 1) ^ 1, abort_flag, p.status))
+                break;
+            const int Mpad = mpad_of(M);
+            bf16 *qd = Qs + qs * L::QSLOT;
+            for (int idx = lane; idx < Mpad * CPR; idx += 32) {
+                const int m = idx / CPR, c = idx % CPR;
+                const uint32_t dst = rx::smem_u32(qd + m * L::RS + c * 8);
+                if (m < M) {
+                    const int64_t qr = d->qrow[m / p.G];
+                    rx::cp_async_16(dst, p.q + ((qr * p.hq + (int64_t)g * p.G + m % p.G) * D + c * 8), 16);
+                } else {
+                    rx::cp_async_16(dst, p.q, 0);
+                }
+            }
+            rx::cp_async_mbar_arrive(bar + 8 * (L::B_QFULL + qs));
+            ++qi;
+        }
+        __syncwarp();
+        if (lane == 0) rx::mbar_arrive(bar + 8 * (L::B_ITEMPTY + di));
+        // K/V stages: the copier threads stride over the stage's 16-byte chunks
+        const int ntiles = (p1 - p0 + kBN - 1) / kBN;
+        bool ok_all = true;
+        for (int t = 0; t < ntiles; ++t, ++n_tile) {
+            const uint32_t sb = n_tile % kNSL, s = n_tile % L::NST;
+            if (!wait_or_abort(bar + 8 * (L::B_SLFULL + sb), (n_tile / kNSL) & 1, abort_flag, p.status) ||
+                !wait_or_abort(bar + 8 * (L::B_EMPTY + s), ((n_tile / L::NST) & 1) ^ 1, abort_flag,
+                               p.status)) {
+                ok_all = false;
+                break;
+            }
+            const int base = p0 + t * kBN;
+            const int32_t *sl = slotbuf + sb * kBN;
+            bf16 *kd = Ks + s * L::TILE;
+            bf16 *vd = Vs + s * L::TILE;
+#pragma unroll 4
+            for (int idx = ct; idx < kBN * CPR; idx += NCT) {
+                const int r = idx / CPR, c = idx % CPR;
+                const int32_t slot = sl[r];
+                const bool inside = base + r < p1;
+                const bool ok = inside && slot >= 0 && (int64_t)slot < p.num_slots;
+                if (inside && !ok && c == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
+                const int64_t off = ok ? (((int64_t)slot * p.hkv + g) * D + c * 8) : 0;
+                const int dsto = r * L::RS + c * 8;
+                rx::cp_async_16(rx::smem_u32(kd + dsto), p.k_pool + off, ok ? 16 : 0);
+                rx::cp_async_16(rx::smem_u32(vd + dsto), p.v_pool + off, ok ? 16 : 0);
+            }
+            __syncwarp();
+            if (lane == 0) rx::mbar_arrive(bar + 8 * (L::B_SLEMPTY + sb));
+            rx::cp_async_mbar_arrive(bar + 8 * (L::B_FULL + s));
+        }
+        if (!ok_all) break;
+    }
+    rx::cp_async_wait_all();
+}
+
+// ---------------------------------------------------------------------------
+// consumer warps
+// ---------------------------------------------------------------------------
+
+template <int D, int WM>
+__device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uint32_t &n_tile,
+                        uint32_t &qi)
+{
+    using L = Layout<D>;
+    constexpr int WK = kConsumers / WM;   // warps along keys
+    constexpr int KW = kBN / WK;          // keys per warp per stage
+    constexpr int NT = KW / 8;            // S n-tiles per warp
+    constexpr int KT = KW / 16;           // PV k-steps per warp
+    constexpr int DT = D / 8;             // O n-tiles
+    constexpr int Mpad = WM * 16;
+    const bf16 *Ks = reinterpret_cast<const bf16 *>(smem + L::OFF_K);
+    const bf16 *Vs = reinterpret_cast<const bf16 *>(smem + L::OFF_V);
+    const bf16 *Qs = reinterpret_cast<const bf16 *>(smem + L::OFF_Q);
+    const uint32_t bar = rx::smem_u32(smem + L::OFF_BAR);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
+    const int cw = (threadIdx.x - kConsumer0) >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int wm = cw % WM, wk = cw / WM;
+    const int G = p.G;
+    const int M = d->M, p0 = d->p0, p1 = d->p1, g = d->g, part = d->part;
+    const bool fin = d->final_ != 0;
+
+    // Q fragments
+    const uint32_t qs = qi & 1;
+    if (!wait_or_abort(bar + 8 * (L::B_QFULL + qs), (qi >> 1) & 1, abort_flag, p.status)) return false;
+    uint32_t qf[D / 16][4];
+    {
+        const bf16 *qb = Qs + qs * L::QSLOT;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const int row = wm * 16 + (lane & 15);
+            const int ch = ks * 2 + (lane >> 4);
+            rx::ldmatrix_x4(rx::smem_u32(qb + row * L::RS + ch * 8), qf[ks][0], qf[ks][1], qf[ks][2],
+                            qf[ks][3]);
+        }
+    }
+    __syncwarp();
+    if (lane == 0) rx::mbar_arrive(bar + 8 * (L::B_QEMPTY + qs));
+    ++qi;
+
+    float m_r[2] = {-INFINITY, -INFINITY};
+    float l_r[2] = {0.f, 0.f};
+    float oacc[DT][4];
+#pragma unroll
+    for (int i = 0; i < DT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+
+    const int ntiles = (p1 - p0 + kBN - 1) / kBN;
+    for (int t = 0; t < ntiles; ++t, ++n_tile) {
+        const uint32_t s = n_tile % L::NST;
+        if (!wait_or_abort(bar + 8 * (L::B_FULL + s), (n_tile / L::NST) & 1, abort_flag, p.status))
+            return false;
+        const bf16 *kt = Ks + s * L::TILE;
+        const bf16 *vt = Vs + s * L::TILE;
+        float sc[NT][4];
+#pragma unroll
+        for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+                const int key = wk * KW + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+                const int ch = ks * 2 + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                rx::ldmatrix_x4(rx::smem_u32(kt + key * L::RS + ch * 8), b0, b1, b2, b3);
+                rx::mma_bf16_16816(sc[2 * np], qf[ks], b0, b1);
+                rx::mma_bf16_16816(sc[2 * np + 1], qf[ks], b2, b3);
+            }
+        }
+        const int kpos0 = p0 + t * kBN + wk * KW;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int pos = kpos0 + nt * 8 + tig * 2 + (j & 1);
+                sc[nt][j] = (pos < p1) ? sc[nt][j] * p.scale_log2 : -INFINITY;
+            }
+            mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+            mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m_r[0], mx0), mn1 = fmaxf(m_r[1], mx1);
+        const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
+        const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+        if (mn0 != m_r[0] || mn1 != m_r[1]) {
+            const float a0 = rx::fast_exp2(m_r[0] - mu0), a1 = rx::fast_exp2(m_r[1] - mu1);
+            l_r[0] *= a0;
+            l_r[1] *= a1;
+#pragma unroll
+            for (int i = 0; i < DT; ++i) {
+                oacc[i][0] *= a0;
+                oacc[i][1] *= a0;
+                oacc[i][2] *= a1;
+                oacc[i][3] *= a1;
+            }
+            m_r[0] = mn0;
+            m_r[1] = mn1;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            sc[nt][0] = rx::fast_exp2(sc[nt][0] - mu0);
+            sc[nt][1] = rx::fast_exp2(sc[nt][1] - mu0);
+            sc[nt][2] = rx::fast_exp2(sc[nt][2] - mu1);
+            sc[nt][3] = rx::fast_exp2(sc[nt][3] - mu1);
+            l_r[0] += sc[nt][0] + sc[nt][1];
+            l_r[1] += sc[nt][2] + sc[nt][3];
+        }
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+            uint32_t a[4];
+            a[0] = rx::pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
+            a[1] = rx::pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
+            a[2] = rx::pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+            a[3] = rx::pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+#pragma unroll
+            for (int dp = 0; dp < D / 16; ++dp) {
+                const int key = wk * KW + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                const int ch = dp * 2 + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                rx::ldmatrix_x4_trans(rx::smem_u32(vt + key * L::RS + ch * 8), b0, b1, b2, b3);
+                rx::mma_bf16_16816(oacc[2 * dp], a, b0, b1);
+                rx::mma_bf16_16816(oacc[2 * dp + 1], a, b2, b3);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) rx::mbar_arrive(bar + 8 * (L::B_EMPTY + s));
+    }
+
+    l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], 1);
+    l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], 2);
+    l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], 1);
+    l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], 2);
+
+    auto out_row = [&](int m) -> int64_t {
+        return (int64_t)d->qrow[m / G] * p.hq + (int64_t)g * G + m % G;
+    };
+    if constexpr (WK == 1) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int r = wm * 16 + gid + half * 8;
+            if (r >= M) continue;
+            const int64_t orow = out_row(r);
+            const float inv = 1.f / l_r[half];
+            if (fin) {
+                bf16 *dst = p.o + orow * D;
+#pragma unroll
+                for (int dt = 0; dt < DT; ++dt)
+                    *reinterpret_cast<uint32_t *>(dst + dt * 8 + tig * 2) =
+                        rx::pack_bf16(oacc[dt][2 * half] * inv, oacc[dt][2 * half + 1] * inv);
+                if (p.lse && tig == 0) p.lse[orow] = (m_r[half] + log2f(l_r[half])) * rx::kLn2;
+            } else {
+                const int64_t prow = orow * p.max_parts + part;
+                float *dst = p.ws_o + prow * D;
+#pragma unroll
+                for (int dt = 0; dt < DT; ++dt)
+                    *reinterpret_cast<float2 *>(dst + dt * 8 + tig * 2) =
+                        make_float2(oacc[dt][2 * half] * inv, oacc[dt][2 * half + 1] * inv);
+                if (tig == 0) p.ws_lse[prow] = m_r[half] + log2f(l_r[half]);
+            }
+        }
+    } else {
+        float *red_m = reinterpret_cast<float *>(smem + L::OFF_RED);
+        float *red_l = red_m + WK * Mpad;
+        float *red_o = red_l + WK * Mpad;  // [WK][Mpad][D]
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int r = wm * 16 + gid + half * 8;
+            if (tig == 0) {
+                red_m[wk * Mpad + r] = m_r[half];
+                red_l[wk * Mpad + r] = l_r[half];
+            }
+#pragma unroll
+            for (int dt = 0; dt < DT; ++dt)
+                *reinterpret_cast<float2 *>(red_o + (wk * Mpad + r) * D + dt * 8 + tig * 2) =
+                    make_float2(oacc[dt][2 * half], oacc[dt][2 * half + 1]);
+        }
+        rx::named_bar_sync(1, 32 * kConsumers);
+        const int ct = threadIdx.x - kConsumer0;
+        for (int e = ct; e < Mpad * D; e += 32 * kConsumers) {
+            const int r = e / D, c = e % D;
+            if (r >= M) continue;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < WK; ++k) mt = fmaxf(mt, red_m[k * Mpad + r]);
+            const float mu = (mt == -INFINITY) ? 0.f : mt;
+            float lt = 0.f, ot = 0.f;
+#pragma unroll
+            for (int k = 0; k < WK; ++k) {
+                const float f = rx::fast_exp2(red_m[k * Mpad + r] - mu);
+                lt += red_l[k * Mpad + r] * f;
+                ot += red_o[(k * Mpad + r) * D + c] * f;
+            }
+            const int64_t orow = out_row(r);
+            if (fin) {
+                p.o[orow * D + c] = __float2bfloat16_rn(ot / lt);
+                if (p.lse && c == 0) p.lse[orow] = (mt + log2f(lt)) * rx::kLn2;
+            } else {
+                const int64_t prow = orow * p.max_parts + part;
+                p.ws_o[prow * D + c] = ot / lt;
+                if (c == 0) p.ws_lse[prow] = mt + log2f(lt);
+            }
+        }
+        rx::named_bar_sync(1, 32 * kConsumers);  // the next item may overwrite the buffer
+    }
+    return true;
+}
+
+template <int D, bool PLAN>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p)
+{
+    using L = Layout<D>;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const uint32_t bar = rx::smem_u32(smem + L::OFF_BAR);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::NST; ++s) {
+            rx::mbar_init(bar + 8 * (L::B_FULL + s), 32 * kCopiers);  // copier lanes' copies
+            rx::mbar_init(bar + 8 * (L::B_EMPTY + s), kConsumers);
+        }
+        for (int q = 0; q < 2; ++q) {
+            rx::mbar_init(bar + 8 * (L::B_QFULL + q), 32);  // copier warp 0's lanes
+            rx::mbar_init(bar + 8 * (L::B_QEMPTY + q), kConsumers);
+        }
+        for (int s = 0; s < kNSL; ++s) {
+            rx::mbar_init(bar + 8 * (L::B_SLFULL + s), 32);       // scheduler lanes' copies
+            rx::mbar_init(bar + 8 * (L::B_SLEMPTY + s), kCopiers);
+        }
+        for (int i = 0; i < kNIT; ++i) {
+            rx::mbar_init(bar + 8 * (L::B_ITFULL + i), 1);        // scheduler
+            rx::mbar_init(bar + 8 * (L::B_ITEMPTY + i), kCopiers + kConsumers);
+        }
+        *reinterpret_cast<volatile int *>(smem + L::OFF_ABORT) = 0;
+        rx::fence_mbar_init();
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5;
+    if (warp == 0) {
+        scheduler<D, PLAN>(p, smem);
+        return;
+    }
+    if (warp <= kCopiers) {
+        copier<D>(p, smem);
+        return;
+    }
+    const Desc *descs = reinterpret_cast<const Desc *>(smem + L::OFF_DESC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
+    const int lane = threadIdx.x & 31;
+    uint32_t n_it = 0, n_tile = 0, qi = 0;
+    for (;; ++n_it) {
+        const uint32_t di = n_it % kNIT;
+        if (!wait_or_abort(bar + 8 * (L::B_ITFULL + di), (n_it / kNIT) & 1, abort_flag, p.status)) return;
+        const Desc *d = descs + di;
+        const int M = d->M;
+        if (M == 0) return;
+        bool ok;
+        if (M <= 16)
+            ok = consume<D, 1>(p, d, smem, n_tile, qi);
+        else if (M <= 32)
+            ok = consume<D, 2>(p, d, smem, n_tile, qi);
+        else
+            ok = consume<D, 4>(p, d, smem, n_tile, qi);
+        if (!ok) return;
+        __syncwarp();
+        if (lane == 0) rx::mbar_arrive(bar + 8 * (L::B_ITEMPTY + di));
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) merge_kernel(const Params p, int use_plan)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 4 + warp;
+    if (row >= (int64_t)p.batch * p.hq) return;
+    const int b = (int)(row / p.hq);
+    const int np = use_plan ? __ldg(p.nparts + b)
+                            : (int)((__ldg(p.seq_len + b) + p.chunk - 1) / p.chunk);
+    if (np <= 1 || np > p.max_parts) return;  // > max_parts: flagged by the decode kernel
+    const float *lp = p.ws_lse + row * p.max_parts;
+    float m = -INFINITY;
+    for (int i = lane; i < np; i += 32) m = fmaxf(m, lp[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    constexpr int PER = D / 32;
+    float acc[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+    float wsum = 0.f;
+    for (int i = 0; i < np; ++i) {
+        const float wgt = rx::fast_exp2(lp[i] - m);
+        wsum += wgt;
+        const float *src = p.ws_o + (row * p.max_parts + i) * D + lane * PER;
+        if constexpr (PER == 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(src);
+            acc[0] += wgt * v.x;
+            acc[1] += wgt * v.y;
+            acc[2] += wgt * v.z;
+            acc[3] += wgt * v.w;
+        } else {
+            const float2 v = *reinterpret_cast<const float2 *>(src);
+            acc[0] += wgt * v.x;
+            acc[1] += wgt * v.y;
+        }
+    }
+    const float inv = 1.f / wsum;
+    bf16 *dst = p.o + row * D + lane * PER;
+#pragma unroll
+    for (int j = 0; j < PER; j += 2)
+        *reinterpret_cast<uint32_t *>(dst + j) = rx::pack_bf16(acc[j] * inv, acc[j + 1] * inv);
+    if (p.lse && lane == 0) p.lse[row] = (m + log2f(wsum)) * rx::kLn2;
+}
+
+int num_sms()
+{
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            sms = 148;
+    }
+    return sms;
+}
+
+template <int D, bool PLAN>
+int launch_decode(const Params &p, cudaStream_t st)
+{
+    static bool configured = false;
+    if (!configured) {
+        RX_CUDA_CHECK(cudaFuncSetAttribute(decode_kernel<D, PLAN>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           Layout<D>::BYTES));
+        configured = true;
+    }
+    const int grid = p.total_work < num_sms() ? p.total_work : num_sms();
+    decode_kernel<D, PLAN><<<grid, kThreads, Layout<D>::BYTES, st>>>(p);
+    RX_CUDA_CHECK(cudaGetLastError());
+    return RX_OK;
+}
+
+template <int D>
+int launch_merge(const Params &p, int use_plan, cudaStream_t st)
+{
+    const int64_t rows = (int64_t)p.batch * p.hq;
+    merge_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(p, use_plan);
+    RX_CUDA_CHECK(cudaGetLastError());
+    return RX_OK;
+}
+
+}  // namespace
+
+int32_t rx_decode_default_chunk(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len)
+{
+    const int64_t total = (int64_t)batch * num_kv_heads * (int64_t)max_seq_len;
+    int64_t c = (total + RX_DECODE_TARGET_ITEMS - 1) / RX_DECODE_TARGET_ITEMS;
+    c = (c + 63) / 64 * 64;
+    if (c < 64) c = 64;
+    if (c > RX_MAX_KV_CHUNK) c = RX_MAX_KV_CHUNK;
+    return (int32_t)c;
+}
+
+extern "C" size_t rx_attn_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t head_dim, int32_t max_seq_len,
+                                           const rx_decode_plan *plan)
+{
+    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seq_len <= 0)
+        return 0;
+    int64_t parts;
+    if (plan) {
+        parts = plan->max_parts;
+    } else {
+        const int64_t c = rx_decode_default_chunk(batch, num_kv_heads, max_seq_len);
+        parts = (max_seq_len + c - 1) / c;
+    }
+    if (parts <= 1) return 0;
+    const int64_t rows = (int64_t)batch * num_q_heads * parts;
+    const int64_t bytes = rows * (head_dim + 1) * 4;
+    return (size_t)((bytes + 255) / 256 * 256);
+}
+
+extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, float *lse,
+                              int32_t hq, const int32_t *req_idx, const int32_t *seq_len,
+                              const int32_t *rtt, int64_t rtt_stride, int32_t batch,
+                              int32_t max_seq_len, const rx_decode_plan *plan, void *workspace,
+                              size_t ws_bytes, float sm_scale, int32_t *dev_status, void *stream)
+{
+    if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0)
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: invalid pool");
+    if (pool->head_dim != 64 && pool->head_dim != 128)
+        return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_decode: head_dim %d (supported: 64, 128)",
+                            pool->head_dim);
+    if (!q || !o || !req_idx || !seq_len || !rtt || rtt_stride <= 0 || rtt_stride > INT32_MAX ||
+        batch < 0 || hq <= 0 || max_seq_len <= 0 || max_seq_len > rtt_stride || !(sm_scale > 0.f))
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: invalid argument");
+    if (hq % pool->num_kv_heads != 0 || 64 % (hq / pool->num_kv_heads) != 0)
+        return rx_set_error(RX_ERR_UNSUPPORTED,
+                            "rx_attn_decode: %d q heads over %d kv heads (need G | 64)", hq,
+                            pool->num_kv_heads);
+    if (rx_misaligned16(q) || rx_misaligned16(o) || rx_misaligned16(pool->k) ||
+        rx_misaligned16(pool->v) || (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: q, o and the pools must be 16-byte aligned");
+    if (plan && (!plan->order || !plan->nparts || !plan->items || plan->n_items < 0 ||
+                 plan->max_parts < 1))
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: invalid plan");
+    if (batch == 0) return RX_OK;
+    const int D = pool->head_dim;
+    Params p{};
+    p.q = (const bf16 *)q;
+    p.o = (bf16 *)o;
+    p.lse = lse;
+    p.k_pool = (const bf16 *)pool->k;
+    p.v_pool = (const bf16 *)pool->v;
+    p.num_slots = pool->num_slots;
+    p.hq = hq;
+    p.hkv = pool->num_kv_heads;
+    p.G = hq / pool->num_kv_heads;
+    p.req_idx = req_idx;
+    p.seq_len = seq_len;
+    p.rtt = rtt;
+    p.rtt_stride = rtt_stride;
+    p.batch = batch;
+    p.scale_log2 = sm_scale * rx::kLog2e;
+    p.status = dev_status;
+    int64_t total;
+    if (plan) {
+        p.order = plan->order;
+        p.nparts = plan->nparts;
+        p.items = plan->items;
+        p.max_parts = plan->max_parts;
+        total = (int64_t)plan->n_items * p.hkv;
+    } else {
+        p.chunk = rx_decode_default_chunk(batch, p.hkv, max_seq_len);
+        p.n_chunks = (max_seq_len + p.chunk - 1) / p.chunk;
+        p.max_parts = p.n_chunks;
+        total = (int64_t)batch * p.n_chunks * p.hkv;
+    }
+    if (total > INT32_MAX)
+        return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_decode: %lld work items", (long long)total);
+    if (total == 0) return RX_OK;
+    p.total_work = (int)total;
+    const size_t need = rx_attn_decode_workspace(batch, hq, p.hkv, D, max_seq_len, plan);
+    if (need > 0) {
+        if (!workspace || ws_bytes < need)
+            return rx_set_error(RX_ERR_CAPACITY, "rx_attn_decode: workspace needs %zu bytes, got %zu",
+                                need, ws_bytes);
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+            return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: workspace must be 256-byte aligned");
+        p.ws_o = (float *)workspace;
+        p.ws_lse = p.ws_o + (int64_t)batch * hq * p.max_parts * D;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    int rc;
+    if (D == 128)
+        rc = plan ? launch_decode<128, true>(p, st) : launch_decode<128, false>(p, st);
+    else
+        rc = plan ? launch_decode<64, true>(p, st) : launch_decode<64, false>(p, st);
+    if (rc != RX_OK || need == 0) return rc;
+    return D == 128 ? launch_merge<128>(p, plan != nullptr, st) : launch_merge<64>(p, plan != nullptr, st);
+}

@@ -674,8 +674,9 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
                 int64_t nr = std::min(R, x.rb - r0 + 1);
                 bool fin = true;
                 for (int64_t r = r0; r < r0 + nr; ++r) fin = fin && nparts[(size_t)order[(size_t)r]] == 1;
+                const int32_t b0 = order[(size_t)r0];
                 items.push_back({{(int32_t)r0, (int32_t)nr, (int32_t)p0, (int32_t)p1,
-                                  (int32_t)(part_base[(size_t)k] + c), fin ? 1 : 0, 0, 0}});
+                                  (int32_t)(part_base[(size_t)k] + c), fin ? 1 : 0, req_idx[b0], b0}});
             }
         }
     }
@@ -684,8 +685,9 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
         for (int64_t c = 0; c * kv_chunk < L - s0; ++c) {
             int64_t p0 = s0 + c * kv_chunk, p1 = std::min(L, p0 + kv_chunk);
             bool fin = nparts[(size_t)order[(size_t)r]] == 1;
+            const int32_t b0 = order[(size_t)r];
             items.push_back({{(int32_t)r, 1, (int32_t)p0, (int32_t)p1,
-                              (int32_t)(priv_base[(size_t)r] + c), fin ? 1 : 0, 0, 0}});
+                              (int32_t)(priv_base[(size_t)r] + c), fin ? 1 : 0, req_idx[b0], b0}});
         }
     }
     // longest first, so that the tail of the grid holds the short items

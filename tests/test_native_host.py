@@ -286,8 +286,9 @@ def check_plan(prob, order, nparts, items, info):
     cover = [np.zeros(int(L), np.int32) for L in prob.dec_seq_len]
     parts = [[] for _ in range(B)]
     reads = 0
-    for r0, nr, p0, p1, part, fin, z0, z1 in items.tolist():
-        assert 1 <= nr and nr * G <= 64 and p0 < p1 and z0 == z1 == 0
+    for r0, nr, p0, p1, part, fin, row0, b0 in items.tolist():
+        assert 1 <= nr and nr * G <= 64 and p0 < p1
+        assert b0 == order[r0] and row0 == prob.dec_req_idx[b0]
         assert p1 - p0 <= info.kv_chunk
         reqs = [int(order[r]) for r in range(r0, r0 + nr)]
         rows = [prob.req_to_token[prob.dec_req_idx[b], p0:p1] for b in reqs]
