@@ -89,7 +89,7 @@ struct Layout {
     static constexpr int B_FULL = 0, B_EMPTY = NST, B_QFULL = 2 * NST, B_QEMPTY = 2 * NST + 2,
                          B_SLFULL = 2 * NST + 4, B_SLEMPTY = B_SLFULL + kNSL,
                          B_ITFULL = B_SLEMPTY + kNSL, B_ITEMPTY = B_ITFULL + kNIT,
-                         N_BAR = B_ITEMPTY + kNIT;
+                         B_RED = B_ITEMPTY + kNIT, N_BAR = B_RED + 1;
     static constexpr int OFF_ABORT = OFF_BAR + N_BAR * 8;
     static constexpr int BYTES = OFF_ABORT + 16;
 };
@@ -164,16 +164,24 @@ __device__ __forceinline__ bool get_item(const Params &p, int w, Item &it)
     return true;
 }
 
+// Bounded wait by a whole warp, with one answer for all its lanes (the warp
+// then runs warp-wide shuffles, ldmatrix and barriers).
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                               int32_t *status)
 {
+    bool ok = false;
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (rx::mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
+        if (rx::mbar_try_wait(bar, parity)) {
+            ok = true;
+            break;
+        }
+        if (*abort_flag) break;
     }
-    *abort_flag = 1;
-    if (status) atomicOr(status, RX_DEV_TIMEOUT);
-    return false;
+    if (!ok && !*abort_flag) {
+        *abort_flag = 1;
+        if (status) atomicOr(status, RX_DEV_TIMEOUT);
+    }
+    return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ int mpad_of(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : 64); }
@@ -351,7 +359,7 @@ __device__ void copier(const Params &p, unsigned char *smem)
 
 template <int D, int WM>
 __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uint32_t &n_tile,
-                        uint32_t &qi)
+                        uint32_t &qi, uint32_t &n_red)
 {
     using L = Layout<D>;
     constexpr int WK = kConsumers / WM;   // warps along keys
@@ -529,7 +537,11 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
                 *reinterpret_cast<float2 *>(red_o + (wk * Mpad + r) * D + dt * 8 + tig * 2) =
                     make_float2(oacc[dt][2 * half], oacc[dt][2 * half + 1]);
         }
-        rx::named_bar_sync(1, 32 * kConsumers);
+        // consumer-only barrier: one arrival per warp, bounded wait
+        __syncwarp();
+        if (lane == 0) rx::mbar_arrive(bar + 8 * L::B_RED);
+        if (!wait_or_abort(bar + 8 * L::B_RED, n_red & 1, abort_flag, p.status)) return false;
+        ++n_red;
         const int ct = threadIdx.x - kConsumer0;
         for (int e = ct; e < Mpad * D; e += 32 * kConsumers) {
             const int r = e / D, c = e % D;
@@ -555,7 +567,10 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
                 if (c == 0) p.ws_lse[prow] = mt + log2f(lt);
             }
         }
-        rx::named_bar_sync(1, 32 * kConsumers);  // the next item may overwrite the buffer
+        __syncwarp();  // the next item may overwrite the buffer once every warp is here
+        if (lane == 0) rx::mbar_arrive(bar + 8 * L::B_RED);
+        if (!wait_or_abort(bar + 8 * L::B_RED, n_red & 1, abort_flag, p.status)) return false;
+        ++n_red;
     }
     return true;
 }
@@ -583,6 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p)
             rx::mbar_init(bar + 8 * (L::B_ITFULL + i), 1);        // scheduler
             rx::mbar_init(bar + 8 * (L::B_ITEMPTY + i), kCopiers + kConsumers);
         }
+        rx::mbar_init(bar + 8 * L::B_RED, kConsumers);            // consumer-only barrier
         *reinterpret_cast<volatile int *>(smem + L::OFF_ABORT) = 0;
         rx::fence_mbar_init();
     }
@@ -599,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p)
     const Desc *descs = reinterpret_cast<const Desc *>(smem + L::OFF_DESC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
     const int lane = threadIdx.x & 31;
-    uint32_t n_it = 0, n_tile = 0, qi = 0;
+    uint32_t n_it = 0, n_tile = 0, qi = 0, n_red = 0;
     for (;; ++n_it) {
         const uint32_t di = n_it % kNIT;
         if (!wait_or_abort(bar + 8 * (L::B_ITFULL + di), (n_it / kNIT) & 1, abort_flag, p.status)) return;
@@ -608,11 +624,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p)
         if (M == 0) return;
         bool ok;
         if (M <= 16)
-            ok = consume<D, 1>(p, d, smem, n_tile, qi);
+            ok = consume<D, 1>(p, d, smem, n_tile, qi, n_red);
         else if (M <= 32)
-            ok = consume<D, 2>(p, d, smem, n_tile, qi);
+            ok = consume<D, 2>(p, d, smem, n_tile, qi, n_red);
         else
-            ok = consume<D, 4>(p, d, smem, n_tile, qi);
+            ok = consume<D, 4>(p, d, smem, n_tile, qi, n_red);
         if (!ok) return;
         __syncwarp();
         if (lane == 0) rx::mbar_arrive(bar + 8 * (L::B_ITEMPTY + di));

@@ -1,0 +1,521 @@
+// rx_extend.cu -- extend attention on the 5th-generation tensor cores
+// (tcgen05.mma, accumulators in TMEM).
+//
+// What is computed: the new tokens of a request attend to its cached prefix
+// plus themselves, causally -- the extend pass under RadixAttention, where a
+// request that shares a cached prefix reuses that prefix's KV instead of
+// recomputing it ("SGLang: Efficient Execution of Structured Language Model
+// Programs", unite.ai, es, section "Introducción a SGLang", RadixAttention
+// bullet).  For new token i of request b (absolute position p = P_b + i),
+// q-head h and kv-head g = h / G:
+//     o = softmax_j<=p( sm_scale * q . K[slot_j] ) V[slot_j],
+// slot_j = req_to_token[req_idx[b]][j].  Both products are real GEMMs, so
+// they run on tcgen05:
+//
+//   - a CTA owns 128 query rows: 128 / G new tokens of one request times the
+//     G q-heads of one kv head (rows token-major), so each gathered K/V tile
+//     serves all G heads;
+//   - three producer warps gather K and V rows through the slot list with
+//     16-byte cp.async straight into the 128-byte-swizzled K-major layout the
+//     tensor core reads (2 stages of 128 keys), then fence the generic writes
+//     into the async proxy and arrive on the stage's mbarrier;
+//   - one thread issues S = Q K^T (M = 128, N = 128 keys, K = head_dim) into
+//     one of two TMEM S buffers, and O += P V (N = head_dim, K = 128 keys, V
+//     read MN-major) into a TMEM O accumulator; tcgen05.commit signals each
+//     result on an mbarrier;
+//   - four softmax warps (one TMEM lane quadrant each, one row per thread)
+//     read S with tcgen05.ld, mask the causal bound on diagonal tiles, keep
+//     the running max in the exp2 domain, write P = 2^(s - m) as bf16 into a
+//     swizzled shared-memory tile (the A operand of the second GEMM) and
+//     rescale O in TMEM only when the row max grew by more than 2^8;
+//   - S is double-buffered, so Q K_{j+1}^T runs while the softmax of tile j
+//     does.
+// Every mbarrier wait is bounded: a wait that gives up sets RX_DEV_TIMEOUT
+// and raises an abort flag; every role then runs to the common exit, where
+// the MMA thread waits for its last tensor-core work and TMEM is freed.
+#include <math.h>
+
+#include "rx_common.cuh"
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kRows = 128;          // query rows per CTA (MMA M)
+constexpr int kBN = 128;            // keys per K/V tile (MMA N of S)
+constexpr int kStages = 2;          // K/V ring depth
+constexpr int kProducer0 = 128;     // first producer thread (warps 4-6)
+constexpr int kProducers = 96;
+constexpr int kMmaWarp = 7;
+constexpr int kThreads = 32 * 8;     // 8 warps: up to 255 registers per thread
+constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256, 256 + head_dim)
+constexpr float kRescale = 8.f;      // log2 units the running max may lag
+
+template <int D>
+struct XL {
+    static constexpr int NB = D / 64;            // 128-byte column blocks of one row
+    static constexpr int BLK = 128 * 128;        // bytes of one column block (128 rows)
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + NB * BLK;
+    static constexpr int OFF_V = OFF_K + kStages * NB * BLK;
+    static constexpr int OFF_P = OFF_V + kStages * NB * BLK;  // 128 rows x 128 keys: 2 blocks
+    static constexpr int OFF_SLOT = OFF_P + 2 * BLK;   // slot ids of the next two tiles
+    static constexpr int OFF_BAR = OFF_SLOT + 2 * kBN * 4;
+    static constexpr int B_KVFULL = 0, B_KVEMPTY = 2, B_SFULL = 4, B_SFREE = 6, B_PFULL = 8,
+                         B_ODONE = 9, B_FINAL = 10, N_BAR = 11;
+    static constexpr int OFF_TMEM = OFF_BAR + N_BAR * 8;
+    static constexpr int OFF_ABORT = OFF_TMEM + 8;
+    static constexpr int BYTES = OFF_ABORT + 8 + 1024;  // + room to align the base to 1024
+};
+static_assert(XL<128>::BYTES <= 227 * 1024, "shared memory budget");
+
+struct XParams {
+    const bf16 *q;
+    bf16 *o;
+    float *lse;
+    const bf16 *k_pool;
+    const bf16 *v_pool;
+    int64_t num_slots;
+    int hq, hkv, G;
+    const int32_t *qo_indptr;
+    const int32_t *req_idx;
+    const int32_t *prefix_len;
+    const int32_t *extend_len;
+    const int32_t *rtt;
+    int64_t rtt_stride;
+    float scale_log2;
+    int32_t *status;
+};
+
+struct Tile {
+    int M;             // valid query rows
+    int64_t qbase;     // packed token index of row group 0
+    int row0_pos;      // absolute position of row group 0
+    int kv_end;        // keys [0, kv_end)
+    int ntiles;
+    const int32_t *slots;
+    int g;
+};
+
+// Bounded wait of one thread; false when it gave up (or another role did).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              int32_t *status)
+{
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (rx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+    }
+    *abort_flag = 1;
+    if (status) atomicOr(status, RX_DEV_TIMEOUT);
+    return false;
+}
+// The same for a whole warp, with one answer for all its lanes (the warp-wide
+// tcgen05.ld / st that follow need every lane).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *status)
+{
+    return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag, status));
+}
+
+// byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile
+__device__ __forceinline__ uint32_t sw128(int r, int c)
+{
+    return (uint32_t)((c >> 3) * (128 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// ---------------------------------------------------------------------------
+// producer warps: Q once, then K/V tiles through the slot list
+// ---------------------------------------------------------------------------
+
+template <int D>
+__device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, uint32_t sbase)
+{
+    using L = XL<D>;
+    constexpr int CPR = D / 8;            // 16-byte chunks per row
+    const uint32_t bar = sbase + L::OFF_BAR;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
+    int32_t *sbuf = reinterpret_cast<int32_t *>(smem + L::OFF_SLOT);
+    const int pt = threadIdx.x - kProducer0;
+    const int G = p.G;
+
+    for (int idx = pt; idx < kRows * CPR; idx += kProducers) {
+        const int r = idx / CPR, c = idx % CPR;
+        const bool ok = r < T.M;
+        const bf16 *src = ok ? p.q + ((T.qbase + r / G) * p.hq + (int64_t)T.g * G + r % G) * D + c * 8 : p.q;
+        rx::cp_async_16(sbase + L::OFF_Q + sw128(r, c), src, ok ? 16 : 0);
+    }
+    // slot ids of tile j go to sbuf[j & 1] (the tile issued two steps back is done with it)
+    auto stage_slots = [&](int j) {
+        for (int k = pt; k < kBN; k += kProducers) {
+            const int pos = j * kBN + k;
+            sbuf[(j & 1) * kBN + k] = pos < T.kv_end ? __ldg(T.slots + pos) : -1;
+        }
+        rx::named_bar_sync(1, kProducers);
+    };
+    stage_slots(0);
+    bool alive = true;
+    for (int j = 0; j < T.ntiles; ++j) {
+        const int st = j % kStages;
+        if (j >= 1) {
+            // hand over tile j-1 before blocking on a stage: the MMA thread reaches
+            // the work that frees stage j only after it has tile j-1 (S_{j-1} is
+            // issued before O += P_{j-2} V_{j-2}), so the stage cannot free up
+            // before tile j-1 lands anyway
+            rx::cp_async_wait<0>();
+            rx::fence_proxy_async_smem();  // visible to the tensor core's reads
+            rx::mbar_arrive(bar + 8 * (L::B_KVFULL + (j - 1) % kStages));
+        }
+        if (j >= kStages) {
+            const bool ok = wait_or_abort(bar + 8 * (L::B_KVEMPTY + st), ((j / kStages) - 1) & 1,
+                                          abort_flag, p.status);
+            if (rx::named_bar_or(1, kProducers, !ok)) {  // every producer leaves together
+                alive = false;
+                break;
+            }
+        }
+        const uint32_t kd = sbase + L::OFF_K + st * L::NB * L::BLK;
+        const uint32_t vd = sbase + L::OFF_V + st * L::NB * L::BLK;
+        const int32_t *sl = sbuf + (j & 1) * kBN;
+#pragma unroll 4
+        for (int idx = pt; idx < kBN * CPR; idx += kProducers) {
+            const int r = idx / CPR, c = idx % CPR;
+            const int pos = j * kBN + r;
+            const int32_t s = sl[r];
+            const bool inside = pos < T.kv_end;
+            const bool ok = inside && s >= 0 && (int64_t)s < p.num_slots;
+            if (inside && !ok && c == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
+            const int64_t off = ok ? (((int64_t)s * p.hkv + T.g) * D + c * 8) : 0;
+            rx::cp_async_16(kd + sw128(r, c), p.k_pool + off, ok ? 16 : 0);
+            rx::cp_async_16(vd + sw128(r, c), p.v_pool + off, ok ? 16 : 0);
+        }
+        rx::cp_async_commit();
+        if (j + 1 < T.ntiles) stage_slots(j + 1);
+    }
+    rx::cp_async_wait<0>();
+    if (alive) {
+        rx::fence_proxy_async_smem();
+        rx::mbar_arrive(bar + 8 * (L::B_KVFULL + (T.ntiles - 1) % kStages));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// MMA thread
+// ---------------------------------------------------------------------------
+
+template <int D>
+__device__ void mma_issuer(const XParams &p, const Tile &T, unsigned char *smem, uint32_t sbase,
+                           uint32_t tmem)
+{
+    using L = XL<D>;
+    const uint32_t bar = sbase + L::OFF_BAR;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
+    constexpr uint32_t idesc_qk = rx::idesc_bf16(kRows, kBN, false, false);
+    constexpr uint32_t idesc_pv = rx::idesc_bf16(kRows, D, false, true);
+    const uint32_t tO = tmem + 256;
+    for (int j = 0; j <= T.ntiles; ++j) {
+        if (j < T.ntiles) {  // S_j = Q K_j^T
+            const int st = j % kStages, sb = j & 1;
+            if (!wait_or_abort(bar + 8 * (L::B_KVFULL + st), (j / kStages) & 1, abort_flag, p.status)) break;
+            if (j >= 2 && !wait_or_abort(bar + 8 * (L::B_SFREE + sb), ((j >> 1) - 1) & 1, abort_flag, p.status))
+                break;
+            rx::tc_fence_after();
+            const uint32_t kbase = sbase + L::OFF_K + st * L::NB * L::BLK;
+#pragma unroll
+            for (int kb = 0; kb < D / 16; ++kb) {
+                const uint32_t off = (kb >> 2) * L::BLK + (kb & 3) * 32;
+                rx::tc_mma(tmem + sb * 128, rx::sdesc_sw128(sbase + L::OFF_Q + off, 16, 1024),
+                           rx::sdesc_sw128(kbase + off, 16, 1024), idesc_qk, kb > 0);
+            }
+            rx::tc_commit(bar + 8 * (L::B_SFULL + sb));
+        }
+        if (j >= 1) {  // O += P_{j-1} V_{j-1}
+            const int jj = j - 1, st = jj % kStages;
+            if (!wait_or_abort(bar + 8 * L::B_PFULL, jj & 1, abort_flag, p.status)) break;
+            rx::tc_fence_after();
+            const uint32_t vbase = sbase + L::OFF_V + st * L::NB * L::BLK;
+#pragma unroll
+            for (int ks = 0; ks < kBN / 16; ++ks) {
+                const uint32_t aoff = (ks >> 2) * L::BLK + (ks & 3) * 32;
+                rx::tc_mma(tO, rx::sdesc_sw128(sbase + L::OFF_P + aoff, 16, 1024),
+                           rx::sdesc_sw128(vbase + ks * 16 * 128, L::BLK, 1024), idesc_pv,
+                           (jj > 0 || ks > 0) ? 1u : 0u);
+            }
+            rx::tc_commit(bar + 8 * L::B_ODONE);
+            rx::tc_commit(bar + 8 * (L::B_KVEMPTY + st));
+        }
+    }
+    // everything issued has finished before TMEM is released
+    rx::tc_commit(bar + 8 * L::B_FINAL);
+    wait_or_abort(bar + 8 * L::B_FINAL, 0, abort_flag, p.status);
+}
+
+// ---------------------------------------------------------------------------
+// softmax warps: one query row per thread
+// ---------------------------------------------------------------------------
+
+template <int D>
+__device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *smem, uint32_t sbase,
+                             uint32_t tmem)
+{
+    using L = XL<D>;
+    const uint32_t bar = sbase + L::OFF_BAR;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
+    const int row = threadIdx.x, warp = row >> 5;
+    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+    const uint32_t tO = tmem + 256 + lanes;
+    const int row_lim = T.row0_pos + row / p.G;   // keys at positions <= row_lim are visible
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    bool alive = true;
+    for (int j = 0; j < T.ntiles; ++j) {
+        const int sb = j & 1;
+        if (!warp_wait(bar + 8 * (L::B_SFULL + sb), (j >> 1) & 1, abort_flag, p.status)) {
+            alive = false;
+            break;
+        }
+        rx::tc_fence_after();
+        const uint32_t tS = tmem + sb * 128 + lanes;
+        const int kbase = j * kBN;
+        const bool need_mask = kbase + kBN - 1 > row_lim;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c4 = 0; c4 < kBN / 32; ++c4) {
+            uint32_t r[32];
+            rx::tmem_ld32(tS + c4 * 32, r);
+            rx::tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                if (!need_mask || kbase + c4 * 32 + k <= row_lim) mx = fmaxf(mx, u2f(r[k]));
+        }
+        const float m_new = fmaxf(m_used, mx * sl2);
+        const bool need = (m_used == -INFINITY) || (m_new > m_used + kRescale);
+        if (j > 0) {  // PV of tile j-1 done: the P tile is free and O is settled
+            if (!warp_wait(bar + 8 * L::B_ODONE, (j - 1) & 1, abort_flag, p.status)) {
+                alive = false;
+                break;
+            }
+            rx::tc_fence_after();
+        }
+        const float alpha = (need && m_used != -INFINITY) ? rx::fast_exp2(m_used - m_new) : 1.f;
+        if (j > 0 && __any_sync(0xffffffffu, need)) {  // rescale O rows in TMEM
+#pragma unroll
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+                uint32_t r[32];
+                rx::tmem_ld32(tO + c4 * 32, r);
+                rx::tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(u2f(r[k]) * alpha);
+                rx::tmem_st32(tO + c4 * 32, r);
+            }
+            rx::tmem_wait_st();
+        }
+        if (need) {
+            l *= alpha;
+            m_used = m_new;
+        }
+        const float mu = (m_used == -INFINITY) ? 0.f : m_used;
+        unsigned char *prow = smem + L::OFF_P;
+#pragma unroll
+        for (int c4 = 0; c4 < kBN / 32; ++c4) {
+            uint32_t r[32];
+            rx::tmem_ld32(tS + c4 * 32, r);
+            rx::tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // 8 keys -> one 16-byte chunk of the 256-byte P row
+                float e[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int key = c4 * 32 + q * 8 + k;
+                    const bool vis = !need_mask || kbase + key <= row_lim;
+                    e[k] = vis ? rx::fast_exp2(fmaf(u2f(r[q * 8 + k]), sl2, -mu)) : 0.f;
+                    l += e[k];
+                }
+                uint4 v;
+                v.x = rx::pack_bf16(e[0], e[1]);
+                v.y = rx::pack_bf16(e[2], e[3]);
+                v.z = rx::pack_bf16(e[4], e[5]);
+                v.w = rx::pack_bf16(e[6], e[7]);
+                *reinterpret_cast<uint4 *>(prow + sw128(row, c4 * 4 + q)) = v;
+            }
+        }
+        rx::tc_fence_before();
+        rx::fence_proxy_async_smem();
+        rx::mbar_arrive(bar + 8 * (L::B_SFREE + sb));
+        rx::mbar_arrive(bar + 8 * L::B_PFULL);
+    }
+    if (!alive) return;
+    if (!warp_wait(bar + 8 * L::B_ODONE, (T.ntiles - 1) & 1, abort_flag, p.status)) return;
+    rx::tc_fence_after();
+    const bool valid = row < T.M;
+    const int G = p.G;
+    const int64_t orow = (T.qbase + row / G) * p.hq + (int64_t)T.g * G + row % G;
+    const float inv = 1.f / l;
+#pragma unroll
+    for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t r[32];
+        rx::tmem_ld32(tO + c4 * 32, r);
+        rx::tmem_wait_ld();
+        if (valid) {
+            bf16 *dst = p.o + orow * D + c4 * 32;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 v;
+                v.x = rx::pack_bf16(u2f(r[8 * q + 0]) * inv, u2f(r[8 * q + 1]) * inv);
+                v.y = rx::pack_bf16(u2f(r[8 * q + 2]) * inv, u2f(r[8 * q + 3]) * inv);
+                v.z = rx::pack_bf16(u2f(r[8 * q + 4]) * inv, u2f(r[8 * q + 5]) * inv);
+                v.w = rx::pack_bf16(u2f(r[8 * q + 6]) * inv, u2f(r[8 * q + 7]) * inv);
+                *reinterpret_cast<uint4 *>(dst + 8 * q) = v;
+            }
+        }
+    }
+    if (valid && p.lse) p.lse[orow] = (m_used + log2f(l)) * rx::kLn2;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) extend_kernel(const XParams p)
+{
+    using L = XL<D>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw = rx::smem_u32(smem_raw);
+    unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned swizzle atoms
+    const uint32_t sbase = rx::smem_u32(smem);
+
+    // which rows: 128 / G tokens of request b times the G q-heads of kv head g
+    Tile T;
+    const int b = blockIdx.z;
+    T.g = blockIdx.y;
+    const int tb = kRows / p.G;
+    const int E = __ldg(p.extend_len + b);
+    if (E > (int)gridDim.x * tb) {  // past max_extend_len
+        if (p.status && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+            atomicOr(p.status, RX_DEV_BAD_LEN);
+        return;
+    }
+    const int t0 = ((int)gridDim.x - 1 - (int)blockIdx.x) * tb;  // longest rows first
+    if (t0 >= E) return;
+    const int ntok = min(tb, E - t0);
+    const int64_t P = __ldg(p.prefix_len + b);
+    if (P < 0 || P + E > p.rtt_stride) {
+        if (p.status && threadIdx.x == 0) atomicOr(p.status, RX_DEV_BAD_LEN);
+        return;
+    }
+    T.M = ntok * p.G;
+    T.qbase = (int64_t)__ldg(p.qo_indptr + b) + t0;
+    T.row0_pos = (int)(P + t0);
+    T.kv_end = (int)(P + t0 + ntok);
+    T.ntiles = (T.kv_end + kBN - 1) / kBN;
+    T.slots = p.rtt + (int64_t)__ldg(p.req_idx + b) * p.rtt_stride;
+
+    const uint32_t bar = sbase + L::OFF_BAR;
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        rx::mbar_init(bar + 8 * (L::B_KVFULL + 0), kProducers);
+        rx::mbar_init(bar + 8 * (L::B_KVFULL + 1), kProducers);
+        rx::mbar_init(bar + 8 * (L::B_KVEMPTY + 0), 1);
+        rx::mbar_init(bar + 8 * (L::B_KVEMPTY + 1), 1);
+        rx::mbar_init(bar + 8 * (L::B_SFULL + 0), 1);
+        rx::mbar_init(bar + 8 * (L::B_SFULL + 1), 1);
+        rx::mbar_init(bar + 8 * (L::B_SFREE + 0), 128);
+        rx::mbar_init(bar + 8 * (L::B_SFREE + 1), 128);
+        rx::mbar_init(bar + 8 * L::B_PFULL, 128);
+        rx::mbar_init(bar + 8 * L::B_ODONE, 1);
+        rx::mbar_init(bar + 8 * L::B_FINAL, 1);
+        *reinterpret_cast<volatile int *>(smem + L::OFF_ABORT) = 0;
+        rx::fence_mbar_init();
+    }
+    if (warp == kMmaWarp) rx::tmem_alloc(sbase + L::OFF_TMEM, kTmemCols);
+    rx::tc_fence_before();
+    __syncthreads();
+    rx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::OFF_TMEM);
+
+    if (warp < 4)
+        softmax_rows<D>(p, T, smem, sbase, tmem);
+    else if (warp < kMmaWarp)
+        producer<D>(p, T, smem, sbase);
+    else if ((threadIdx.x & 31) == 0)
+        mma_issuer<D>(p, T, smem, sbase, tmem);
+
+    rx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        rx::tc_fence_after();
+        rx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+int check_pool(const rx_kv_pool *pool)
+{
+    if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0)
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_extend: invalid pool");
+    if (pool->head_dim != 64 && pool->head_dim != 128)
+        return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_extend: head_dim %d (supported: 64, 128)",
+                            pool->head_dim);
+    return RX_OK;
+}
+
+template <int D>
+int launch_extend(const XParams &p, dim3 grid, cudaStream_t st)
+{
+    static bool configured = false;
+    if (!configured) {
+        RX_CUDA_CHECK(cudaFuncSetAttribute(extend_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           XL<D>::BYTES));
+        configured = true;
+    }
+    extend_kernel<D><<<grid, kThreads, XL<D>::BYTES, st>>>(p);
+    RX_CUDA_CHECK(cudaGetLastError());
+    return RX_OK;
+}
+
+}  // namespace
+
+extern "C" int rx_attn_extend(const rx_kv_pool *pool, const void *q, void *o, float *lse,
+                              int32_t hq, const int32_t *qo_indptr, const int32_t *req_idx,
+                              const int32_t *prefix_len, const int32_t *extend_len,
+                              const int32_t *rtt, int64_t rtt_stride, int32_t batch,
+                              int32_t max_extend_len, float sm_scale, int32_t *dev_status,
+                              void *stream)
+{
+    int rc = check_pool(pool);
+    if (rc != RX_OK) return rc;
+    if (!q || !o || !qo_indptr || !req_idx || !prefix_len || !extend_len || !rtt ||
+        rtt_stride <= 0 || rtt_stride > INT32_MAX || batch < 0 || hq <= 0 || max_extend_len < 0 ||
+        !(sm_scale > 0.f))
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_extend: invalid argument");
+    if (hq % pool->num_kv_heads != 0 || kRows % (hq / pool->num_kv_heads) != 0)
+        return rx_set_error(RX_ERR_UNSUPPORTED,
+                            "rx_attn_extend: %d q heads over %d kv heads (need G | 128)", hq,
+                            pool->num_kv_heads);
+    if (rx_misaligned16(q) || rx_misaligned16(o) || rx_misaligned16(pool->k) ||
+        rx_misaligned16(pool->v) || (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_extend: q, o and the pools must be 16-byte aligned");
+    if (batch == 0 || max_extend_len == 0) return RX_OK;
+    if (batch > 65535 || pool->num_kv_heads > 65535)
+        return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_extend: batch or kv heads above 65535");
+    XParams p{};
+    p.q = (const bf16 *)q;
+    p.o = (bf16 *)o;
+    p.lse = lse;
+    p.k_pool = (const bf16 *)pool->k;
+    p.v_pool = (const bf16 *)pool->v;
+    p.num_slots = pool->num_slots;
+    p.hq = hq;
+    p.hkv = pool->num_kv_heads;
+    p.G = hq / pool->num_kv_heads;
+    p.qo_indptr = qo_indptr;
+    p.req_idx = req_idx;
+    p.prefix_len = prefix_len;
+    p.extend_len = extend_len;
+    p.rtt = rtt;
+    p.rtt_stride = rtt_stride;
+    p.scale_log2 = sm_scale * rx::kLog2e;
+    p.status = dev_status;
+    const int tb = kRows / p.G;
+    dim3 grid((unsigned)((max_extend_len + tb - 1) / tb), (unsigned)p.hkv, (unsigned)batch);
+    cudaStream_t st = (cudaStream_t)stream;
+    return pool->head_dim == 128 ? launch_extend<128>(p, grid, st) : launch_extend<64>(p, grid, st);
+}
