@@ -289,6 +289,32 @@ int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, float *lse_or
                    int32_t max_seq_len, const rx_decode_plan *plan_or_null, void *workspace,
                    size_t ws_bytes, float sm_scale, int32_t *dev_status, void *stream);
 
+/* ---- decode without a caller workspace ----------------------------------
+ * The pages have no counterpart to this entry point; it exists for callers of
+ * this library that cannot give it device scratch memory -- for example an
+ * engine that commits all device memory at start-up (most of it to the KV
+ * pool) and allows no allocator calls while serving, or a host program that
+ * only lends its own buffers for inputs and outputs.
+ *
+ * Same arguments and results as rx_attn_decode, without workspace/ws_bytes:
+ * the partial results of split work go to a fixed device array of
+ * RX_DECODE_STATIC_SCRATCH_BYTES owned by the library (every GPU that loads
+ * the library holds one until the process exits).  The call allocates
+ * nothing.  Its first call with a given device current looks up that
+ * device's array address (cudaGetSymbolAddress) and keeps it; make that
+ * first call before any stream capture.  Every call shares the one array,
+ * so calls that overlap on the GPU (different streams, or different host
+ * threads without ordering) race; calls ordered on one stream are safe.
+ * Nothing needs clearing: whatever a call reads from the array it has
+ * written earlier in the same call.  Returns RX_ERR_CAPACITY when
+ * rx_attn_decode_workspace(...) for the batch exceeds the array. */
+#define RX_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
+int rx_attn_decode_static(const rx_kv_pool *pool, const void *q, void *o, float *lse,
+                          int32_t num_q_heads, const int32_t *req_idx, const int32_t *seq_len,
+                          const int32_t *req_to_token, int64_t rtt_stride, int32_t batch,
+                          int32_t max_seq_len, const rx_decode_plan *plan_or_null, float sm_scale,
+                          int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

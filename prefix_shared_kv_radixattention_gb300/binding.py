@@ -99,6 +99,9 @@ _sig("rx_attn_decode_workspace", ctypes.c_size_t, _I32, _I32, _I32, _I32, _I32,
      ctypes.POINTER(DecodePlan))
 _sig("rx_attn_decode", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I32, _P, _P, _P, _I64, _I32,
      _I32, ctypes.POINTER(DecodePlan), _P, ctypes.c_size_t, ctypes.c_float, _P, _P)
+_sig("rx_attn_decode_static", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I32, _P, _P, _P, _I64,
+     _I32, _I32, ctypes.POINTER(DecodePlan), ctypes.c_float, _P, _P)
+RX_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 def library():
@@ -394,3 +397,23 @@ def rx_attn_decode(k_pool, v_pool, q, o, lse, req_idx, seq_len, req_to_token, ma
                                req_to_token.shape[1], req_idx.numel(), int(max_seq_len), pp,
                                _ptr(workspace), ws_bytes, float(sm_scale), _ptr(dev_status),
                                _stream(stream)))
+
+
+def rx_attn_decode_static(k_pool, v_pool, q, o, lse, req_idx, seq_len, req_to_token, max_seq_len: int,
+                          sm_scale: float, plan: Optional[DevicePlan] = None, dev_status=None,
+                          stream=None) -> None:
+    """rx_attn_decode with the library's fixed scratch array instead of a
+    workspace (for callers that cannot allocate device memory; see rx.h)."""
+    torch = _torch()
+    pool = make_pool(k_pool, v_pool)
+    _dev(q, torch.bfloat16, "q")
+    _dev(o, torch.bfloat16, "o")
+    _dev(lse, torch.float32, "lse")
+    for t, n in ((req_idx, "req_idx"), (seq_len, "seq_len"), (req_to_token, "req_to_token")):
+        _dev(t, torch.int32, n)
+    _dev(dev_status, torch.int32, "dev_status")
+    pp = ctypes.byref(plan.struct) if plan is not None else None
+    _check(_lib.rx_attn_decode_static(ctypes.byref(pool), _ptr(q), _ptr(o), _ptr(lse), q.shape[1],
+                                      _ptr(req_idx), _ptr(seq_len), _ptr(req_to_token),
+                                      req_to_token.shape[1], req_idx.numel(), int(max_seq_len), pp,
+                                      float(sm_scale), _ptr(dev_status), _stream(stream)))

@@ -48,6 +48,8 @@
 // warp waits for its own copies before the CTA exits.
 #include <math.h>
 
+#include <mutex>
+
 #include "rx_common.cuh"
 
 namespace {
@@ -825,4 +827,65 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
         rc = plan ? launch_decode<64, true>(p, st) : launch_decode<64, false>(p, st);
     if (rc != RX_OK || need == 0) return rc;
     return D == 128 ? launch_merge<128>(p, plan != nullptr, st) : launch_merge<64>(p, plan != nullptr, st);
+}
+
+// ---------------------------------------------------------------------------
+// Decode without a caller workspace
+// ---------------------------------------------------------------------------
+//
+// Some callers cannot hand this library device scratch memory: an engine
+// whose device memory is all committed at start-up (most of it to the KV
+// pool) and that forbids allocator calls while serving, or a host program
+// that only lends its own buffers for inputs and outputs.  For them the
+// partial results of split work live in the fixed array below instead of a
+// workspace.  It is a file-scope device array, so every GPU that loads this
+// library holds RX_DECODE_STATIC_SCRATCH_BYTES of it until the process
+// exits.  In host code its name is only a stand-in for the symbol, never a
+// device address: the address is looked up once per device with
+// cudaGetSymbolAddress (on the first call made with that device current) and
+// kept.
+
+static __device__ __align__(256) unsigned char g_decode_scratch[RX_DECODE_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" int rx_attn_decode_static(const rx_kv_pool *pool, const void *q, void *o, float *lse,
+                                     int32_t num_q_heads, const int32_t *req_idx,
+                                     const int32_t *seq_len, const int32_t *req_to_token,
+                                     int64_t rtt_stride, int32_t batch, int32_t max_seq_len,
+                                     const rx_decode_plan *plan_or_null, float sm_scale,
+                                     int32_t *dev_status, void *stream)
+{
+    if (!pool || pool->num_kv_heads <= 0 || pool->head_dim <= 0)
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode_static: invalid pool");
+    const size_t need = rx_attn_decode_workspace(batch, num_q_heads, pool->num_kv_heads,
+                                                 pool->head_dim, max_seq_len, plan_or_null);
+    if (need > (size_t)RX_DECODE_STATIC_SCRATCH_BYTES)
+        return rx_set_error(RX_ERR_CAPACITY,
+                            "rx_attn_decode_static: this batch needs %zu bytes of partial results, "
+                            "above the fixed %u-byte scratch array; use rx_attn_decode with a workspace",
+                            need, (unsigned)RX_DECODE_STATIC_SCRATCH_BYTES);
+    void *scratch = nullptr;
+    if (need > 0) {
+        int dev = 0;
+        RX_CUDA_CHECK(cudaGetDevice(&dev));
+        if (dev < 0 || dev >= kMaxDevices)
+            return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_decode_static: device %d", dev);
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        if (!g_scratch_addr[dev]) {
+            void *addr = nullptr;
+            RX_CUDA_CHECK(cudaGetSymbolAddress(&addr, g_decode_scratch));
+            g_scratch_addr[dev] = addr;
+        }
+        scratch = g_scratch_addr[dev];
+    }
+    // Every entry read from the scratch array is written earlier in the same
+    // call, so nothing needs clearing between calls.
+    return rx_attn_decode(pool, q, o, lse, num_q_heads, req_idx, seq_len, req_to_token, rtt_stride,
+                          batch, max_seq_len, plan_or_null, scratch, need, sm_scale, dev_status,
+                          stream);
 }
