@@ -17,10 +17,13 @@
 //     serves all G heads;
 //   - three producer warps gather K and V rows through the slot list with
 //     16-byte cp.async straight into the 128-byte-swizzled K-major layout the
-//     tensor core reads (2 stages of 128 keys), then fence the generic writes
-//     into the async proxy and arrive on the stage's mbarrier;
-//   - one thread issues S = Q K^T (M = 128, N = 128 keys, K = head_dim) into
-//     one of two TMEM S buffers, and O += P V (N = head_dim, K = 128 keys, V
+//     tensor core reads, into a 5-stage ring of 64-key tiles; slot ids are
+//     prefetched four tiles ahead (4-byte cp.async into a small ring); each
+//     stage's mbarrier is completed by the copies themselves
+//     (cp.async.mbarrier.arrive), and the MMA thread fences the landed rows
+//     into the async proxy before the tensor core reads them;
+//   - one thread issues S = Q K^T (M = 128, N = 64 keys, K = head_dim) into
+//     one of two TMEM S buffers, and O += P V (N = head_dim, K = 64 keys, V
 //     read MN-major) into a TMEM O accumulator; tcgen05.commit signals each
 //     result on an mbarrier;
 //   - four softmax warps (one TMEM lane quadrant each, one row per thread)
@@ -28,8 +31,9 @@
 //     the running max in the exp2 domain, write P = 2^(s - m) as bf16 into a
 //     swizzled shared-memory tile (the A operand of the second GEMM) and
 //     rescale O in TMEM only when the row max grew by more than 2^8;
-//   - S is double-buffered, so Q K_{j+1}^T runs while the softmax of tile j
-//     does.
+//   - S and P are double-buffered, so Q K_{j+1}^T and O += P_j V_j run while
+//     the softmax warps work on the next tile; only the rare O rescale waits
+//     for the previous O += P V.
 // Every mbarrier wait is bounded: a wait that gives up sets RX_DEV_TIMEOUT
 // and raises an abort flag; every role then runs to the common exit, where
 // the MMA thread waits for its last tensor-core work and TMEM is freed.
@@ -42,33 +46,40 @@ namespace {
 using bf16 = __nv_bfloat16;
 
 constexpr int kRows = 128;          // query rows per CTA (MMA M)
-constexpr int kBN = 128;            // keys per K/V tile (MMA N of S)
-constexpr int kStages = 2;          // K/V ring depth
+constexpr int kBN = 64;             // keys per K/V tile (MMA N of S)
+constexpr int kStages = 5;          // K/V ring depth
+constexpr int kLag = kStages - 1;   // tiles in flight before one is handed over
+constexpr int kNSL = kLag + 1;       // slot-id ring (tiles)
 constexpr int kProducer0 = 128;     // first producer thread (warps 4-6)
 constexpr int kProducers = 96;
 constexpr int kMmaWarp = 7;
 constexpr int kThreads = 32 * 8;     // 8 warps: up to 255 registers per thread
 constexpr uint32_t kSpinLimit = 1u << 22;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256, 256 + head_dim)
+constexpr uint32_t kTmemCols = 256;  // S0 [0,64), S1 [64,128), O [128, 128 + head_dim)
+constexpr uint32_t kTmemO = 128;
 constexpr float kRescale = 8.f;      // log2 units the running max may lag
 
 template <int D>
 struct XL {
     static constexpr int NB = D / 64;            // 128-byte column blocks of one row
-    static constexpr int BLK = 128 * 128;        // bytes of one column block (128 rows)
+    static constexpr int QBLK = kRows * 128;     // bytes of one column block of Q (128 rows)
+    static constexpr int KBLK = kBN * 128;       // bytes of one column block of a K or V tile
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + NB * BLK;
-    static constexpr int OFF_V = OFF_K + kStages * NB * BLK;
-    static constexpr int OFF_P = OFF_V + kStages * NB * BLK;  // 128 rows x 128 keys: 2 blocks
-    static constexpr int OFF_SLOT = OFF_P + 2 * BLK;   // slot ids of the next two tiles
-    static constexpr int OFF_BAR = OFF_SLOT + 2 * kBN * 4;
-    static constexpr int B_KVFULL = 0, B_KVEMPTY = 2, B_SFULL = 4, B_SFREE = 6, B_PFULL = 8,
-                         B_ODONE = 9, B_FINAL = 10, N_BAR = 11;
+    static constexpr int OFF_K = OFF_Q + NB * QBLK;
+    static constexpr int OFF_V = OFF_K + kStages * NB * KBLK;
+    static constexpr int OFF_P = OFF_V + kStages * NB * KBLK;  // 2 x (128 rows x 64 keys)
+    static constexpr int OFF_SLOT = OFF_P + 2 * QBLK;           // slot-id ring
+    static constexpr int OFF_BAR = OFF_SLOT + kNSL * kBN * 4;
+    // per P buffer: p_full (softmax wrote it), pv_done (the MMA that read it finished)
+    static constexpr int B_KVFULL = 0, B_KVEMPTY = kStages, B_SFULL = 2 * kStages,
+                         B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2,
+                         B_FINAL = B_PVDONE + 2, N_BAR = B_FINAL + 1;
     static constexpr int OFF_TMEM = OFF_BAR + N_BAR * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 8;
     static constexpr int BYTES = OFF_ABORT + 8 + 1024;  // + room to align the base to 1024
 };
 static_assert(XL<128>::BYTES <= 227 * 1024, "shared memory budget");
+static_assert(XL<128>::OFF_BAR % 8 == 0 && XL<64>::OFF_BAR % 8 == 0, "mbarrier alignment");
 
 struct XParams {
     const bf16 *q;
@@ -118,10 +129,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag, status));
 }
 
-// byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile
-__device__ __forceinline__ uint32_t sw128(int r, int c)
+// byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major
+// tile whose 128-byte column blocks are blk bytes apart
+__device__ __forceinline__ uint32_t sw128(int r, int c, int blk)
 {
-    return (uint32_t)((c >> 3) * (128 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    return (uint32_t)((c >> 3) * blk + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
@@ -137,37 +149,41 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
     constexpr int CPR = D / 8;            // 16-byte chunks per row
     const uint32_t bar = sbase + L::OFF_BAR;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
-    int32_t *sbuf = reinterpret_cast<int32_t *>(smem + L::OFF_SLOT);
+    const int32_t *sbuf = reinterpret_cast<const int32_t *>(smem + L::OFF_SLOT);
     const int pt = threadIdx.x - kProducer0;
     const int G = p.G;
 
+    // slot ids of tile j -> slot ring entry j % kNSL (4-byte async copies)
+    auto fetch_slots = [&](int j) {
+        if (j < T.ntiles && pt < kBN) {
+            const int pos = j * kBN + pt;
+            rx::cp_async_4(sbase + L::OFF_SLOT + ((j % kNSL) * kBN + pt) * 4,
+                           T.slots + (pos < T.kv_end ? pos : 0), pos < T.kv_end ? 4 : 0);
+        }
+    };
+    // group "prologue": Q rows and the slot ids of the first kLag tiles
     for (int idx = pt; idx < kRows * CPR; idx += kProducers) {
         const int r = idx / CPR, c = idx % CPR;
         const bool ok = r < T.M;
         const bf16 *src = ok ? p.q + ((T.qbase + r / G) * p.hq + (int64_t)T.g * G + r % G) * D + c * 8 : p.q;
-        rx::cp_async_16(sbase + L::OFF_Q + sw128(r, c), src, ok ? 16 : 0);
+        rx::cp_async_16(sbase + L::OFF_Q + sw128(r, c, L::QBLK), src, ok ? 16 : 0);
     }
-    // slot ids of tile j go to sbuf[j & 1] (the tile issued two steps back is done with it)
-    auto stage_slots = [&](int j) {
-        for (int k = pt; k < kBN; k += kProducers) {
-            const int pos = j * kBN + k;
-            sbuf[(j & 1) * kBN + k] = pos < T.kv_end ? __ldg(T.slots + pos) : -1;
-        }
-        rx::named_bar_sync(1, kProducers);
-    };
-    stage_slots(0);
+    for (int j = 0; j < kLag; ++j) fetch_slots(j);
+    rx::cp_async_commit();
+
+    // one cp.async group per tile j: its K/V rows and the slot ids of tile
+    // j + kLag.  The stage's full barrier gets each producer thread's arrival
+    // as soon as that thread's copies have landed (cp.async.mbarrier.arrive),
+    // so handing a tile over never waits for the producer loop; the MMA
+    // thread fences the landed rows into the async proxy before reading them.
     bool alive = true;
     for (int j = 0; j < T.ntiles; ++j) {
         const int st = j % kStages;
-        if (j >= 1) {
-            // hand over tile j-1 before blocking on a stage: the MMA thread reaches
-            // the work that frees stage j only after it has tile j-1 (S_{j-1} is
-            // issued before O += P_{j-2} V_{j-2}), so the stage cannot free up
-            // before tile j-1 lands anyway
-            rx::cp_async_wait<0>();
-            rx::fence_proxy_async_smem();  // visible to the tensor core's reads
-            rx::mbar_arrive(bar + 8 * (L::B_KVFULL + (j - 1) % kStages));
-        }
+        if (j == 0)
+            rx::cp_async_wait<0>();                 // Q and the first slot ids
+        else if (j >= kLag)
+            rx::cp_async_wait<kLag - 1>();          // group of tile j - kLag: slot ids of tile j
+        rx::named_bar_sync(1, kProducers);          // every producer sees the slot ids
         if (j >= kStages) {
             const bool ok = wait_or_abort(bar + 8 * (L::B_KVEMPTY + st), ((j / kStages) - 1) & 1,
                                           abort_flag, p.status);
@@ -176,9 +192,9 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
                 break;
             }
         }
-        const uint32_t kd = sbase + L::OFF_K + st * L::NB * L::BLK;
-        const uint32_t vd = sbase + L::OFF_V + st * L::NB * L::BLK;
-        const int32_t *sl = sbuf + (j & 1) * kBN;
+        const uint32_t kd = sbase + L::OFF_K + st * L::NB * L::KBLK;
+        const uint32_t vd = sbase + L::OFF_V + st * L::NB * L::KBLK;
+        const int32_t *sl = sbuf + (j % kNSL) * kBN;
 #pragma unroll 4
         for (int idx = pt; idx < kBN * CPR; idx += kProducers) {
             const int r = idx / CPR, c = idx % CPR;
@@ -188,17 +204,16 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
             const bool ok = inside && s >= 0 && (int64_t)s < p.num_slots;
             if (inside && !ok && c == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
             const int64_t off = ok ? (((int64_t)s * p.hkv + T.g) * D + c * 8) : 0;
-            rx::cp_async_16(kd + sw128(r, c), p.k_pool + off, ok ? 16 : 0);
-            rx::cp_async_16(vd + sw128(r, c), p.v_pool + off, ok ? 16 : 0);
+            rx::cp_async_16(kd + sw128(r, c, L::KBLK), p.k_pool + off, ok ? 16 : 0);
+            rx::cp_async_16(vd + sw128(r, c, L::KBLK), p.v_pool + off, ok ? 16 : 0);
         }
+        rx::cp_async_mbar_arrive(bar + 8 * (L::B_KVFULL + st));
+        rx::named_bar_sync(1, kProducers);          // slot entry j % kNSL is read: refill allowed
+        fetch_slots(j + kLag);
         rx::cp_async_commit();
-        if (j + 1 < T.ntiles) stage_slots(j + 1);
     }
     rx::cp_async_wait<0>();
-    if (alive) {
-        rx::fence_proxy_async_smem();
-        rx::mbar_arrive(bar + 8 * (L::B_KVFULL + (T.ntiles - 1) % kStages));
-    }
+    (void)alive;
 }
 
 // ---------------------------------------------------------------------------
@@ -214,37 +229,61 @@ __device__ void mma_issuer(const XParams &p, const Tile &T, unsigned char *smem,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
     constexpr uint32_t idesc_qk = rx::idesc_bf16(kRows, kBN, false, false);
     constexpr uint32_t idesc_pv = rx::idesc_bf16(kRows, D, false, true);
-    const uint32_t tO = tmem + 256;
-    for (int j = 0; j <= T.ntiles; ++j) {
-        if (j < T.ntiles) {  // S_j = Q K_j^T
-            const int st = j % kStages, sb = j & 1;
-            if (!wait_or_abort(bar + 8 * (L::B_KVFULL + st), (j / kStages) & 1, abort_flag, p.status)) break;
-            if (j >= 2 && !wait_or_abort(bar + 8 * (L::B_SFREE + sb), ((j >> 1) - 1) & 1, abort_flag, p.status))
-                break;
-            rx::tc_fence_after();
-            const uint32_t kbase = sbase + L::OFF_K + st * L::NB * L::BLK;
+    const uint32_t tO = tmem + kTmemO;
+    // S_j = Q K_j^T and O += P_j V_j are independent apart from buffer reuse,
+    // so issue whichever is ready next: S_js when tile js has landed and its
+    // S buffer is free (at most two ahead of the O updates), else O += P_jp
+    // V_jp once the softmax has written P_jp.  O updates stay in order.
+    int js = 0, jp = 0;
+    uint32_t idle = 0;
+    while (jp < T.ntiles) {
+        bool did = false;
+        if (js < T.ntiles && js <= jp + 1) {
+            const int st = js % kStages, sb = js & 1;
+            if (rx::mbar_try_wait(bar + 8 * (L::B_KVFULL + st), (js / kStages) & 1) &&
+                (js < 2 || rx::mbar_try_wait(bar + 8 * (L::B_SFREE + sb), ((js >> 1) - 1) & 1))) {
+                rx::fence_proxy_async_smem();  // the landed K/V rows (and Q) -> async proxy
+                rx::tc_fence_after();
+                const uint32_t kbase = sbase + L::OFF_K + st * L::NB * L::KBLK;
 #pragma unroll
-            for (int kb = 0; kb < D / 16; ++kb) {
-                const uint32_t off = (kb >> 2) * L::BLK + (kb & 3) * 32;
-                rx::tc_mma(tmem + sb * 128, rx::sdesc_sw128(sbase + L::OFF_Q + off, 16, 1024),
-                           rx::sdesc_sw128(kbase + off, 16, 1024), idesc_qk, kb > 0);
+                for (int kb = 0; kb < D / 16; ++kb) {
+                    const uint32_t kofs = (kb & 3) * 32;
+                    rx::tc_mma(tmem + sb * kBN,
+                               rx::sdesc_sw128(sbase + L::OFF_Q + (kb >> 2) * L::QBLK + kofs, 16, 1024),
+                               rx::sdesc_sw128(kbase + (kb >> 2) * L::KBLK + kofs, 16, 1024), idesc_qk,
+                               kb > 0);
+                }
+                rx::tc_commit(bar + 8 * (L::B_SFULL + sb));
+                ++js;
+                did = true;
             }
-            rx::tc_commit(bar + 8 * (L::B_SFULL + sb));
         }
-        if (j >= 1) {  // O += P_{j-1} V_{j-1}
-            const int jj = j - 1, st = jj % kStages;
-            if (!wait_or_abort(bar + 8 * L::B_PFULL, jj & 1, abort_flag, p.status)) break;
-            rx::tc_fence_after();
-            const uint32_t vbase = sbase + L::OFF_V + st * L::NB * L::BLK;
+        if (!did && jp < js) {
+            const int st = jp % kStages, pb = jp & 1;
+            if (rx::mbar_try_wait(bar + 8 * (L::B_PFULL + pb), (jp >> 1) & 1)) {
+                rx::tc_fence_after();
+                const uint32_t vbase = sbase + L::OFF_V + st * L::NB * L::KBLK;
+                const uint32_t pbase = sbase + L::OFF_P + pb * L::QBLK;
 #pragma unroll
-            for (int ks = 0; ks < kBN / 16; ++ks) {
-                const uint32_t aoff = (ks >> 2) * L::BLK + (ks & 3) * 32;
-                rx::tc_mma(tO, rx::sdesc_sw128(sbase + L::OFF_P + aoff, 16, 1024),
-                           rx::sdesc_sw128(vbase + ks * 16 * 128, L::BLK, 1024), idesc_pv,
-                           (jj > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < kBN / 16; ++ks) {
+                    rx::tc_mma(tO, rx::sdesc_sw128(pbase + ks * 32, 16, 1024),
+                               rx::sdesc_sw128(vbase + ks * 16 * 128, L::KBLK, 1024), idesc_pv,
+                               (jp > 0 || ks > 0) ? 1u : 0u);
+                }
+                rx::tc_commit(bar + 8 * (L::B_PVDONE + pb));
+                rx::tc_commit(bar + 8 * (L::B_KVEMPTY + st));
+                ++jp;
+                did = true;
             }
-            rx::tc_commit(bar + 8 * L::B_ODONE);
-            rx::tc_commit(bar + 8 * (L::B_KVEMPTY + st));
+        }
+        if (did) {
+            idle = 0;
+        } else if (++idle > kSpinLimit || *abort_flag) {
+            if (!*abort_flag) {
+                *abort_flag = 1;
+                if (p.status) atomicOr(p.status, RX_DEV_TIMEOUT);
+            }
+            break;
         }
     }
     // everything issued has finished before TMEM is released
@@ -265,7 +304,7 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
     const int row = threadIdx.x, warp = row >> 5;
     const uint32_t lanes = (uint32_t)(warp * 32) << 16;
-    const uint32_t tO = tmem + 256 + lanes;
+    const uint32_t tO = tmem + kTmemO + lanes;
     const int row_lim = T.row0_pos + row / p.G;   // keys at positions <= row_lim are visible
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
@@ -277,30 +316,28 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
             break;
         }
         rx::tc_fence_after();
-        const uint32_t tS = tmem + sb * 128 + lanes;
+        const uint32_t tS = tmem + sb * kBN + lanes;
         const int kbase = j * kBN;
         const bool need_mask = kbase + kBN - 1 > row_lim;
+        uint32_t sv[kBN];  // this row's scores of the tile, loaded once
+        rx::tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        rx::tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        rx::tmem_wait_ld();
         float mx = -INFINITY;
 #pragma unroll
-        for (int c4 = 0; c4 < kBN / 32; ++c4) {
-            uint32_t r[32];
-            rx::tmem_ld32(tS + c4 * 32, r);
-            rx::tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-                if (!need_mask || kbase + c4 * 32 + k <= row_lim) mx = fmaxf(mx, u2f(r[k]));
-        }
+        for (int k = 0; k < kBN; ++k)
+            if (!need_mask || kbase + k <= row_lim) mx = fmaxf(mx, u2f(sv[k]));
         const float m_new = fmaxf(m_used, mx * sl2);
         const bool need = (m_used == -INFINITY) || (m_new > m_used + kRescale);
-        if (j > 0) {  // PV of tile j-1 done: the P tile is free and O is settled
-            if (!warp_wait(bar + 8 * L::B_ODONE, (j - 1) & 1, abort_flag, p.status)) {
+        const float alpha = (need && m_used != -INFINITY) ? rx::fast_exp2(m_used - m_new) : 1.f;
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+            // rescale O rows in TMEM once every O += P V so far has finished
+            if (!warp_wait(bar + 8 * (L::B_PVDONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag,
+                           p.status)) {
                 alive = false;
                 break;
             }
             rx::tc_fence_after();
-        }
-        const float alpha = (need && m_used != -INFINITY) ? rx::fast_exp2(m_used - m_new) : 1.f;
-        if (j > 0 && __any_sync(0xffffffffu, need)) {  // rescale O rows in TMEM
 #pragma unroll
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 uint32_t r[32];
@@ -316,38 +353,40 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
             l *= alpha;
             m_used = m_new;
         }
+        // P buffer j & 1 was last read by O += P_{j-2} V_{j-2}
+        if (j >= 2 && !warp_wait(bar + 8 * (L::B_PVDONE + (j & 1)), ((j >> 1) - 1) & 1, abort_flag,
+                                 p.status)) {
+            alive = false;
+            break;
+        }
         const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-        unsigned char *prow = smem + L::OFF_P;
+        unsigned char *prow = smem + L::OFF_P + (j & 1) * L::QBLK;
 #pragma unroll
-        for (int c4 = 0; c4 < kBN / 32; ++c4) {
-            uint32_t r[32];
-            rx::tmem_ld32(tS + c4 * 32, r);
-            rx::tmem_wait_ld();
+        for (int q = 0; q < kBN / 8; ++q) {  // 8 keys -> one 16-byte chunk of the P row
+            float e[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {  // 8 keys -> one 16-byte chunk of the 256-byte P row
-                float e[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int key = c4 * 32 + q * 8 + k;
-                    const bool vis = !need_mask || kbase + key <= row_lim;
-                    e[k] = vis ? rx::fast_exp2(fmaf(u2f(r[q * 8 + k]), sl2, -mu)) : 0.f;
-                    l += e[k];
-                }
-                uint4 v;
-                v.x = rx::pack_bf16(e[0], e[1]);
-                v.y = rx::pack_bf16(e[2], e[3]);
-                v.z = rx::pack_bf16(e[4], e[5]);
-                v.w = rx::pack_bf16(e[6], e[7]);
-                *reinterpret_cast<uint4 *>(prow + sw128(row, c4 * 4 + q)) = v;
+            for (int k = 0; k < 8; ++k) {
+                const int key = q * 8 + k;
+                const bool vis = !need_mask || kbase + key <= row_lim;
+                e[k] = vis ? rx::fast_exp2(fmaf(u2f(sv[key]), sl2, -mu)) : 0.f;
+                l += e[k];
             }
+            uint4 v;
+            v.x = rx::pack_bf16(e[0], e[1]);
+            v.y = rx::pack_bf16(e[2], e[3]);
+            v.z = rx::pack_bf16(e[4], e[5]);
+            v.w = rx::pack_bf16(e[6], e[7]);
+            *reinterpret_cast<uint4 *>(prow + sw128(row, q, L::QBLK)) = v;
         }
         rx::tc_fence_before();
         rx::fence_proxy_async_smem();
         rx::mbar_arrive(bar + 8 * (L::B_SFREE + sb));
-        rx::mbar_arrive(bar + 8 * L::B_PFULL);
+        rx::mbar_arrive(bar + 8 * (L::B_PFULL + (j & 1)));
     }
     if (!alive) return;
-    if (!warp_wait(bar + 8 * L::B_ODONE, (T.ntiles - 1) & 1, abort_flag, p.status)) return;
+    if (!warp_wait(bar + 8 * (L::B_PVDONE + ((T.ntiles - 1) & 1)), ((T.ntiles - 1) >> 1) & 1, abort_flag,
+                   p.status))
+        return;
     rx::tc_fence_after();
     const bool valid = row < T.M;
     const int G = p.G;
@@ -412,16 +451,18 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const XParams p)
     const uint32_t bar = sbase + L::OFF_BAR;
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        rx::mbar_init(bar + 8 * (L::B_KVFULL + 0), kProducers);
-        rx::mbar_init(bar + 8 * (L::B_KVFULL + 1), kProducers);
-        rx::mbar_init(bar + 8 * (L::B_KVEMPTY + 0), 1);
-        rx::mbar_init(bar + 8 * (L::B_KVEMPTY + 1), 1);
+        for (int i = 0; i < kStages; ++i) {
+            rx::mbar_init(bar + 8 * (L::B_KVFULL + i), kProducers);  // producer threads
+            rx::mbar_init(bar + 8 * (L::B_KVEMPTY + i), 1);          // MMA commit
+        }
         rx::mbar_init(bar + 8 * (L::B_SFULL + 0), 1);
         rx::mbar_init(bar + 8 * (L::B_SFULL + 1), 1);
         rx::mbar_init(bar + 8 * (L::B_SFREE + 0), 128);
         rx::mbar_init(bar + 8 * (L::B_SFREE + 1), 128);
-        rx::mbar_init(bar + 8 * L::B_PFULL, 128);
-        rx::mbar_init(bar + 8 * L::B_ODONE, 1);
+        for (int i = 0; i < 2; ++i) {
+            rx::mbar_init(bar + 8 * (L::B_PFULL + i), 128);   // softmax threads
+            rx::mbar_init(bar + 8 * (L::B_PVDONE + i), 1);    // MMA commit
+        }
         rx::mbar_init(bar + 8 * L::B_FINAL, 1);
         *reinterpret_cast<volatile int *>(smem + L::OFF_ABORT) = 0;
         rx::fence_mbar_init();
@@ -432,12 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const XParams p)
     rx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::OFF_TMEM);
 
-    if (warp < 4)
+    if (warp < 4) {
         softmax_rows<D>(p, T, smem, sbase, tmem);
-    else if (warp < kMmaWarp)
+    } else if (warp < kMmaWarp) {
         producer<D>(p, T, smem, sbase);
-    else if ((threadIdx.x & 31) == 0)
-        mma_issuer<D>(p, T, smem, sbase, tmem);
+    } else {
+        if ((threadIdx.x & 31) == 0) mma_issuer<D>(p, T, smem, sbase, tmem);
+        __syncwarp();  // the whole warp reaches the exit barrier together
+    }
 
     rx::tc_fence_before();
     __syncthreads();
