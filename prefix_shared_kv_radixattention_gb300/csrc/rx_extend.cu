@@ -12,28 +12,30 @@
 // slot_j = req_to_token[req_idx[b]][j].  Both products are real GEMMs, so
 // they run on tcgen05:
 //
-//   - a CTA owns 128 query rows: 128 / G new tokens of one request times the
-//     G q-heads of one kv head (rows token-major), so each gathered K/V tile
-//     serves all G heads;
+//   - a CTA owns 256 query rows: 256 / G new tokens of one request times the
+//     G q-heads of one kv head (rows token-major), as two 128-row tensor-core
+//     tiles that share every gathered K/V tile -- the gather through the slot
+//     list, not the tensor core, is the scarce resource, so each gathered
+//     byte feeds as many rows as TMEM holds accumulators for;
 //   - three producer warps gather K and V rows through the slot list with
 //     16-byte cp.async straight into the 128-byte-swizzled K-major layout the
-//     tensor core reads, into a 5-stage ring of 64-key tiles; slot ids are
-//     prefetched four tiles ahead (4-byte cp.async into a small ring); each
+//     tensor core reads, into a 3-stage ring of 64-key tiles; slot ids are
+//     prefetched two tiles ahead (4-byte cp.async into a small ring); each
 //     stage's mbarrier is completed by the copies themselves
 //     (cp.async.mbarrier.arrive), and the MMA thread fences the landed rows
 //     into the async proxy before the tensor core reads them;
-//   - one thread issues S = Q K^T (M = 128, N = 64 keys, K = head_dim) into
-//     one of two TMEM S buffers, and O += P V (N = head_dim, K = 64 keys, V
-//     read MN-major) into a TMEM O accumulator; tcgen05.commit signals each
-//     result on an mbarrier;
-//   - four softmax warps (one TMEM lane quadrant each, one row per thread)
-//     read S with tcgen05.ld, mask the causal bound on diagonal tiles, keep
-//     the running max in the exp2 domain, write P = 2^(s - m) as bf16 into a
-//     swizzled shared-memory tile (the A operand of the second GEMM) and
-//     rescale O in TMEM only when the row max grew by more than 2^8;
-//   - S and P are double-buffered, so Q K_{j+1}^T and O += P_j V_j run while
-//     the softmax warps work on the next tile; only the rare O rescale waits
-//     for the previous O += P V.
+//   - one thread issues, per Q tile, S = Q K^T (M = 128, N = 64 keys, K =
+//     head_dim) into one of two TMEM S buffers and O += P V (N = head_dim,
+//     K = 64 keys, V read MN-major) into a TMEM O accumulator, in whatever
+//     order their inputs become ready; tcgen05.commit signals each result on
+//     an mbarrier, and a K/V stage is released once both tiles' O += P V of
+//     it are done;
+//   - eight softmax warps (four per Q tile, one TMEM lane quadrant and one
+//     row per thread) load each row's 64 scores once with tcgen05.ld, mask
+//     the causal bound on diagonal tiles, keep the running max in the exp2
+//     domain, write P = 2^(s - m) as bf16 into a double-buffered swizzled
+//     shared-memory tile (the A operand of the second GEMM) and rescale O in
+//     TMEM only when the row max grew by more than 2^8.
 // Every mbarrier wait is bounded: a wait that gives up sets RX_DEV_TIMEOUT
 // and raises an abort flag; every role then runs to the common exit, where
 // the MMA thread waits for its last tensor-core work and TMEM is freed.
@@ -45,35 +47,37 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int kRows = 128;          // query rows per CTA (MMA M)
+constexpr int kQT = 2;              // Q tiles per CTA
+constexpr int kRows = 128;          // query rows per Q tile (MMA M)
+constexpr int kCtaRows = kQT * kRows;
 constexpr int kBN = 64;             // keys per K/V tile (MMA N of S)
-constexpr int kStages = 5;          // K/V ring depth
-constexpr int kLag = kStages - 1;   // tiles in flight before one is handed over
-constexpr int kNSL = kLag + 1;       // slot-id ring (tiles)
-constexpr int kProducer0 = 128;     // first producer thread (warps 4-6)
+constexpr int kStages = 3;          // K/V ring depth
+constexpr int kLag = kStages - 1;   // slot-id prefetch distance (tiles)
+constexpr int kNSL = kLag + 1;      // slot-id ring (tiles)
+constexpr int kProducer0 = 256;     // first producer thread (warps 8-10)
 constexpr int kProducers = 96;
-constexpr int kMmaWarp = 7;
-constexpr int kThreads = 32 * 8;     // 8 warps: up to 255 registers per thread
+constexpr int kMmaWarp = 11;
+constexpr int kThreads = 32 * 12;
 constexpr uint32_t kSpinLimit = 1u << 22;
-constexpr uint32_t kTmemCols = 256;  // S0 [0,64), S1 [64,128), O [128, 128 + head_dim)
-constexpr uint32_t kTmemO = 128;
+constexpr uint32_t kTmemCols = 512;  // per Q tile t: S0 [256t, +64), S1 [+64, +128), O [+128, +256)
 constexpr float kRescale = 8.f;      // log2 units the running max may lag
 
 template <int D>
 struct XL {
     static constexpr int NB = D / 64;            // 128-byte column blocks of one row
-    static constexpr int QBLK = kRows * 128;     // bytes of one column block of Q (128 rows)
+    static constexpr int QBLK = kRows * 128;     // bytes of one column block of a Q tile
     static constexpr int KBLK = kBN * 128;       // bytes of one column block of a K or V tile
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + NB * QBLK;
+    static constexpr int OFF_Q = 0;              // kQT tiles x NB blocks
+    static constexpr int OFF_K = OFF_Q + kQT * NB * QBLK;
     static constexpr int OFF_V = OFF_K + kStages * NB * KBLK;
-    static constexpr int OFF_P = OFF_V + kStages * NB * KBLK;  // 2 x (128 rows x 64 keys)
-    static constexpr int OFF_SLOT = OFF_P + 2 * QBLK;           // slot-id ring
+    static constexpr int OFF_P = OFF_V + kStages * NB * KBLK;  // [Q tile][2 buffers] x 128 x 64
+    static constexpr int OFF_SLOT = OFF_P + kQT * 2 * QBLK;    // slot-id ring
     static constexpr int OFF_BAR = OFF_SLOT + kNSL * kBN * 4;
-    // per P buffer: p_full (softmax wrote it), pv_done (the MMA that read it finished)
+    // per Q tile and buffer: s_full, s_free, p_full (softmax wrote P), pv_done
     static constexpr int B_KVFULL = 0, B_KVEMPTY = kStages, B_SFULL = 2 * kStages,
-                         B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2,
-                         B_FINAL = B_PVDONE + 2, N_BAR = B_FINAL + 1;
+                         B_SFREE = B_SFULL + 2 * kQT, B_PFULL = B_SFREE + 2 * kQT,
+                         B_PVDONE = B_PFULL + 2 * kQT, B_FINAL = B_PVDONE + 2 * kQT,
+                         N_BAR = B_FINAL + 1;
     static constexpr int OFF_TMEM = OFF_BAR + N_BAR * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 8;
     static constexpr int BYTES = OFF_ABORT + 8 + 1024;  // + room to align the base to 1024
@@ -100,7 +104,8 @@ struct XParams {
 };
 
 struct Tile {
-    int M;             // valid query rows
+    int M;             // valid query rows (<= 256)
+    int nqt;           // Q tiles with valid rows (1 or 2)
     int64_t qbase;     // packed token index of row group 0
     int row0_pos;      // absolute position of row group 0
     int kv_end;        // keys [0, kv_end)
@@ -162,11 +167,12 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
         }
     };
     // group "prologue": Q rows and the slot ids of the first kLag tiles
-    for (int idx = pt; idx < kRows * CPR; idx += kProducers) {
+    for (int idx = pt; idx < T.nqt * kRows * CPR; idx += kProducers) {
         const int r = idx / CPR, c = idx % CPR;
         const bool ok = r < T.M;
         const bf16 *src = ok ? p.q + ((T.qbase + r / G) * p.hq + (int64_t)T.g * G + r % G) * D + c * 8 : p.q;
-        rx::cp_async_16(sbase + L::OFF_Q + sw128(r, c, L::QBLK), src, ok ? 16 : 0);
+        rx::cp_async_16(sbase + L::OFF_Q + (r / kRows) * L::NB * L::QBLK + sw128(r % kRows, c, L::QBLK), src,
+                        ok ? 16 : 0);
     }
     for (int j = 0; j < kLag; ++j) fetch_slots(j);
     rx::cp_async_commit();
@@ -176,7 +182,6 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
     // as soon as that thread's copies have landed (cp.async.mbarrier.arrive),
     // so handing a tile over never waits for the producer loop; the MMA
     // thread fences the landed rows into the async proxy before reading them.
-    bool alive = true;
     for (int j = 0; j < T.ntiles; ++j) {
         const int st = j % kStages;
         if (j == 0)
@@ -187,10 +192,7 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
         if (j >= kStages) {
             const bool ok = wait_or_abort(bar + 8 * (L::B_KVEMPTY + st), ((j / kStages) - 1) & 1,
                                           abort_flag, p.status);
-            if (rx::named_bar_or(1, kProducers, !ok)) {  // every producer leaves together
-                alive = false;
-                break;
-            }
+            if (rx::named_bar_or(1, kProducers, !ok)) break;  // every producer leaves together
         }
         const uint32_t kd = sbase + L::OFF_K + st * L::NB * L::KBLK;
         const uint32_t vd = sbase + L::OFF_V + st * L::NB * L::KBLK;
@@ -213,7 +215,6 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
         rx::cp_async_commit();
     }
     rx::cp_async_wait<0>();
-    (void)alive;
 }
 
 // ---------------------------------------------------------------------------
@@ -229,50 +230,60 @@ __device__ void mma_issuer(const XParams &p, const Tile &T, unsigned char *smem,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
     constexpr uint32_t idesc_qk = rx::idesc_bf16(kRows, kBN, false, false);
     constexpr uint32_t idesc_pv = rx::idesc_bf16(kRows, D, false, true);
-    const uint32_t tO = tmem + kTmemO;
-    // S_j = Q K_j^T and O += P_j V_j are independent apart from buffer reuse,
-    // so issue whichever is ready next: S_js when tile js has landed and its
-    // S buffer is free (at most two ahead of the O updates), else O += P_jp
-    // V_jp once the softmax has written P_jp.  O updates stay in order.
-    int js = 0, jp = 0;
+    // S_j = Q K_j^T (for every Q tile) and O_t += P_t,j V_j are independent
+    // apart from buffer reuse, so issue whichever is ready: S_js once tile js
+    // has landed and both S buffers for it are free, O_t += P V once the
+    // softmax has written P_t; O updates of a tile stay in order, and a K/V
+    // stage is released after both tiles' O updates that read it.
+    int js = 0, jrel = 0;
+    int jp[kQT] = {0, 0};
     uint32_t idle = 0;
-    while (jp < T.ntiles) {
+    for (;;) {
+        const int jmin = (T.nqt == 2) ? min(jp[0], jp[1]) : jp[0];
+        if (jmin >= T.ntiles) break;
         bool did = false;
-        if (js < T.ntiles && js <= jp + 1) {
+        for (int t = 0; t < T.nqt; ++t) {
+            const int j = jp[t];
+            if (j >= js) continue;
+            const int pb = j & 1;
+            if (!rx::mbar_try_wait(bar + 8 * (L::B_PFULL + 2 * t + pb), (j >> 1) & 1)) continue;
+            rx::tc_fence_after();
+            const uint32_t vbase = sbase + L::OFF_V + (j % kStages) * L::NB * L::KBLK;
+            const uint32_t pbase = sbase + L::OFF_P + (2 * t + pb) * L::QBLK;
+#pragma unroll
+            for (int ks = 0; ks < kBN / 16; ++ks) {
+                rx::tc_mma(tmem + t * 256 + 128, rx::sdesc_sw128(pbase + ks * 32, 16, 1024),
+                           rx::sdesc_sw128(vbase + ks * 16 * 128, L::KBLK, 1024), idesc_pv,
+                           (j > 0 || ks > 0) ? 1u : 0u);
+            }
+            rx::tc_commit(bar + 8 * (L::B_PVDONE + 2 * t + pb));
+            jp[t] = j + 1;
+            did = true;
+        }
+        const int jdone = (T.nqt == 2) ? min(jp[0], jp[1]) : jp[0];
+        for (; jrel < jdone; ++jrel) rx::tc_commit(bar + 8 * (L::B_KVEMPTY + jrel % kStages));
+        if (js < T.ntiles) {
             const int st = js % kStages, sb = js & 1;
-            if (rx::mbar_try_wait(bar + 8 * (L::B_KVFULL + st), (js / kStages) & 1) &&
-                (js < 2 || rx::mbar_try_wait(bar + 8 * (L::B_SFREE + sb), ((js >> 1) - 1) & 1))) {
+            bool ready = rx::mbar_try_wait(bar + 8 * (L::B_KVFULL + st), (js / kStages) & 1);
+            for (int t = 0; t < T.nqt && ready; ++t)
+                ready = js < 2 ||
+                        rx::mbar_try_wait(bar + 8 * (L::B_SFREE + 2 * t + sb), ((js >> 1) - 1) & 1);
+            if (ready) {
                 rx::fence_proxy_async_smem();  // the landed K/V rows (and Q) -> async proxy
                 rx::tc_fence_after();
                 const uint32_t kbase = sbase + L::OFF_K + st * L::NB * L::KBLK;
+                for (int t = 0; t < T.nqt; ++t) {
+                    const uint32_t qbase = sbase + L::OFF_Q + t * L::NB * L::QBLK;
 #pragma unroll
-                for (int kb = 0; kb < D / 16; ++kb) {
-                    const uint32_t kofs = (kb & 3) * 32;
-                    rx::tc_mma(tmem + sb * kBN,
-                               rx::sdesc_sw128(sbase + L::OFF_Q + (kb >> 2) * L::QBLK + kofs, 16, 1024),
-                               rx::sdesc_sw128(kbase + (kb >> 2) * L::KBLK + kofs, 16, 1024), idesc_qk,
-                               kb > 0);
+                    for (int kb = 0; kb < D / 16; ++kb) {
+                        const uint32_t kofs = (kb >> 2) * L::QBLK + (kb & 3) * 32;
+                        const uint32_t bofs = (kb >> 2) * L::KBLK + (kb & 3) * 32;
+                        rx::tc_mma(tmem + t * 256 + sb * kBN, rx::sdesc_sw128(qbase + kofs, 16, 1024),
+                                   rx::sdesc_sw128(kbase + bofs, 16, 1024), idesc_qk, kb > 0);
+                    }
+                    rx::tc_commit(bar + 8 * (L::B_SFULL + 2 * t + sb));
                 }
-                rx::tc_commit(bar + 8 * (L::B_SFULL + sb));
                 ++js;
-                did = true;
-            }
-        }
-        if (!did && jp < js) {
-            const int st = jp % kStages, pb = jp & 1;
-            if (rx::mbar_try_wait(bar + 8 * (L::B_PFULL + pb), (jp >> 1) & 1)) {
-                rx::tc_fence_after();
-                const uint32_t vbase = sbase + L::OFF_V + st * L::NB * L::KBLK;
-                const uint32_t pbase = sbase + L::OFF_P + pb * L::QBLK;
-#pragma unroll
-                for (int ks = 0; ks < kBN / 16; ++ks) {
-                    rx::tc_mma(tO, rx::sdesc_sw128(pbase + ks * 32, 16, 1024),
-                               rx::sdesc_sw128(vbase + ks * 16 * 128, L::KBLK, 1024), idesc_pv,
-                               (jp > 0 || ks > 0) ? 1u : 0u);
-                }
-                rx::tc_commit(bar + 8 * (L::B_PVDONE + pb));
-                rx::tc_commit(bar + 8 * (L::B_KVEMPTY + st));
-                ++jp;
                 did = true;
             }
         }
@@ -300,28 +311,28 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
                              uint32_t tmem)
 {
     using L = XL<D>;
+    const int warp = threadIdx.x >> 5;
+    const int t = warp >> 2;                      // Q tile
+    if (t >= T.nqt) return;
     const uint32_t bar = sbase + L::OFF_BAR;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
-    const int row = threadIdx.x, warp = row >> 5;
-    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
-    const uint32_t tO = tmem + kTmemO + lanes;
+    const int rl = threadIdx.x & (kRows - 1);     // row in the Q tile = TMEM lane
+    const int row = t * kRows + rl;
+    const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tbase = tmem + t * 256 + lanes;
+    const uint32_t tO = tbase + 128;
     const int row_lim = T.row0_pos + row / p.G;   // keys at positions <= row_lim are visible
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
-    bool alive = true;
     for (int j = 0; j < T.ntiles; ++j) {
         const int sb = j & 1;
-        if (!warp_wait(bar + 8 * (L::B_SFULL + sb), (j >> 1) & 1, abort_flag, p.status)) {
-            alive = false;
-            break;
-        }
+        if (!warp_wait(bar + 8 * (L::B_SFULL + 2 * t + sb), (j >> 1) & 1, abort_flag, p.status)) return;
         rx::tc_fence_after();
-        const uint32_t tS = tmem + sb * kBN + lanes;
         const int kbase = j * kBN;
         const bool need_mask = kbase + kBN - 1 > row_lim;
         uint32_t sv[kBN];  // this row's scores of the tile, loaded once
-        rx::tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
-        rx::tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        rx::tmem_ld32(tbase + sb * kBN, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        rx::tmem_ld32(tbase + sb * kBN + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
         rx::tmem_wait_ld();
         float mx = -INFINITY;
 #pragma unroll
@@ -332,11 +343,9 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
         const float alpha = (need && m_used != -INFINITY) ? rx::fast_exp2(m_used - m_new) : 1.f;
         if (j > 0 && __any_sync(0xffffffffu, need)) {
             // rescale O rows in TMEM once every O += P V so far has finished
-            if (!warp_wait(bar + 8 * (L::B_PVDONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag,
-                           p.status)) {
-                alive = false;
-                break;
-            }
+            if (!warp_wait(bar + 8 * (L::B_PVDONE + 2 * t + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag,
+                           p.status))
+                return;
             rx::tc_fence_after();
 #pragma unroll
             for (int c4 = 0; c4 < D / 32; ++c4) {
@@ -353,14 +362,12 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
             l *= alpha;
             m_used = m_new;
         }
-        // P buffer j & 1 was last read by O += P_{j-2} V_{j-2}
-        if (j >= 2 && !warp_wait(bar + 8 * (L::B_PVDONE + (j & 1)), ((j >> 1) - 1) & 1, abort_flag,
-                                 p.status)) {
-            alive = false;
-            break;
-        }
+        // P buffer j & 1 of this Q tile was last read by O += P_{j-2} V_{j-2}
+        if (j >= 2 && !warp_wait(bar + 8 * (L::B_PVDONE + 2 * t + sb), ((j >> 1) - 1) & 1, abort_flag,
+                                 p.status))
+            return;
         const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-        unsigned char *prow = smem + L::OFF_P + (j & 1) * L::QBLK;
+        unsigned char *prow = smem + L::OFF_P + (2 * t + sb) * L::QBLK;
 #pragma unroll
         for (int q = 0; q < kBN / 8; ++q) {  // 8 keys -> one 16-byte chunk of the P row
             float e[8];
@@ -376,17 +383,15 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
             v.y = rx::pack_bf16(e[2], e[3]);
             v.z = rx::pack_bf16(e[4], e[5]);
             v.w = rx::pack_bf16(e[6], e[7]);
-            *reinterpret_cast<uint4 *>(prow + sw128(row, q, L::QBLK)) = v;
+            *reinterpret_cast<uint4 *>(prow + sw128(rl, q, L::QBLK)) = v;
         }
         rx::tc_fence_before();
         rx::fence_proxy_async_smem();
-        rx::mbar_arrive(bar + 8 * (L::B_SFREE + sb));
-        rx::mbar_arrive(bar + 8 * (L::B_PFULL + (j & 1)));
+        rx::mbar_arrive(bar + 8 * (L::B_SFREE + 2 * t + sb));
+        rx::mbar_arrive(bar + 8 * (L::B_PFULL + 2 * t + sb));
     }
-    if (!alive) return;
-    if (!warp_wait(bar + 8 * (L::B_PVDONE + ((T.ntiles - 1) & 1)), ((T.ntiles - 1) >> 1) & 1, abort_flag,
-                   p.status))
-        return;
+    const int jl = T.ntiles - 1;
+    if (!warp_wait(bar + 8 * (L::B_PVDONE + 2 * t + (jl & 1)), (jl >> 1) & 1, abort_flag, p.status)) return;
     rx::tc_fence_after();
     const bool valid = row < T.M;
     const int G = p.G;
@@ -422,11 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const XParams p)
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned swizzle atoms
     const uint32_t sbase = rx::smem_u32(smem);
 
-    // which rows: 128 / G tokens of request b times the G q-heads of kv head g
+    // which rows: 256 / G tokens of request b times the G q-heads of kv head g
     Tile T;
     const int b = blockIdx.z;
     T.g = blockIdx.y;
-    const int tb = kRows / p.G;
+    const int tb = kCtaRows / p.G;
     const int E = __ldg(p.extend_len + b);
     if (E > (int)gridDim.x * tb) {  // past max_extend_len
         if (p.status && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
@@ -442,6 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const XParams p)
         return;
     }
     T.M = ntok * p.G;
+    T.nqt = T.M > kRows ? 2 : 1;
     T.qbase = (int64_t)__ldg(p.qo_indptr + b) + t0;
     T.row0_pos = (int)(P + t0);
     T.kv_end = (int)(P + t0 + ntok);
@@ -455,12 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const XParams p)
             rx::mbar_init(bar + 8 * (L::B_KVFULL + i), kProducers);  // producer threads
             rx::mbar_init(bar + 8 * (L::B_KVEMPTY + i), 1);          // MMA commit
         }
-        rx::mbar_init(bar + 8 * (L::B_SFULL + 0), 1);
-        rx::mbar_init(bar + 8 * (L::B_SFULL + 1), 1);
-        rx::mbar_init(bar + 8 * (L::B_SFREE + 0), 128);
-        rx::mbar_init(bar + 8 * (L::B_SFREE + 1), 128);
-        for (int i = 0; i < 2; ++i) {
-            rx::mbar_init(bar + 8 * (L::B_PFULL + i), 128);   // softmax threads
+        for (int i = 0; i < 2 * kQT; ++i) {
+            rx::mbar_init(bar + 8 * (L::B_SFULL + i), 1);     // MMA commit
+            rx::mbar_init(bar + 8 * (L::B_SFREE + i), 128);   // softmax threads of the tile
+            rx::mbar_init(bar + 8 * (L::B_PFULL + i), 128);
             rx::mbar_init(bar + 8 * (L::B_PVDONE + i), 1);    // MMA commit
         }
         rx::mbar_init(bar + 8 * L::B_FINAL, 1);
@@ -473,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const XParams p)
     rx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::OFF_TMEM);
 
-    if (warp < 4) {
+    if (warp < 8) {
         softmax_rows<D>(p, T, smem, sbase, tmem);
     } else if (warp < kMmaWarp) {
         producer<D>(p, T, smem, sbase);
@@ -557,7 +561,7 @@ extern "C" int rx_attn_extend(const rx_kv_pool *pool, const void *q, void *o, fl
     p.rtt_stride = rtt_stride;
     p.scale_log2 = sm_scale * rx::kLog2e;
     p.status = dev_status;
-    const int tb = kRows / p.G;
+    const int tb = kCtaRows / p.G;
     dim3 grid((unsigned)((max_extend_len + tb - 1) / tb), (unsigned)p.hkv, (unsigned)batch);
     cudaStream_t st = (cudaStream_t)stream;
     return pool->head_dim == 128 ? launch_extend<128>(p, grid, st) : launch_extend<64>(p, grid, st);
