@@ -123,6 +123,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
         : "memory");
     return ok != 0;
 }
+// Non-blocking probe of a phase: unlike try_wait it never suspends the
+// thread, so a loop that polls several barriers reacts to whichever is ready.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 // Makes initialised mbarriers visible to the asynchronous (bulk copy) proxy.
 __device__ __forceinline__ void fence_mbar_init()
@@ -145,6 +158,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
             dst),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// Per-warpgroup register reallocation: every warp of a warpgroup executes the
+// same call; an increase waits until decreases elsewhere in the CTA have
+// released enough of the registers the CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
 }
 
 // ---- tcgen05 (5th-generation tensor cores, accumulators in TMEM) ------------

@@ -54,11 +54,18 @@ constexpr int kBN = 64;             // keys per K/V tile (MMA N of S)
 constexpr int kStages = 3;          // K/V ring depth
 constexpr int kLag = kStages - 1;   // slot-id prefetch distance (tiles)
 constexpr int kNSL = kLag + 1;      // slot-id ring (tiles)
-constexpr int kProducer0 = 256;     // first producer thread (warps 8-10)
-constexpr int kProducers = 96;
-constexpr int kMmaWarp = 11;
-constexpr int kThreads = 32 * 12;
+constexpr int kProducer0 = 256;     // producer threads: warps 8-14
+constexpr int kProducers = 224;
+constexpr int kMmaWarp = 15;
+constexpr int kThreads = 32 * 16;
+// registers: launched at 65536 / 512 = 128 a thread; the two softmax
+// warpgroups take 184, the producer / MMA warpgroups give back to 72
+// (2 x 128 x 184 + 2 x 128 x 72 = 65536)
+constexpr uint32_t kRegSoftmax = 184;
+constexpr uint32_t kRegOther = 72;
+static_assert(2 * 128 * kRegSoftmax + 2 * 128 * kRegOther == 65536, "register split");
 constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr uint32_t kIdleLimit = 1u << 27;  // polls of the MMA thread without progress
 constexpr uint32_t kTmemCols = 512;  // per Q tile t: S0 [256t, +64), S1 [+64, +128), O [+128, +256)
 constexpr float kRescale = 8.f;      // log2 units the running max may lag
 
@@ -73,8 +80,10 @@ struct XL {
     static constexpr int OFF_P = OFF_V + kStages * NB * KBLK;  // [Q tile][2 buffers] x 128 x 64
     static constexpr int OFF_SLOT = OFF_P + kQT * 2 * QBLK;    // slot-id ring
     static constexpr int OFF_BAR = OFF_SLOT + kNSL * kBN * 4;
-    // per Q tile and buffer: s_full, s_free, p_full (softmax wrote P), pv_done
-    static constexpr int B_KVFULL = 0, B_KVEMPTY = kStages, B_SFULL = 2 * kStages,
+    // per Q tile: q_full; per stage: kv_full, kv_empty; per Q tile and
+    // buffer: s_full, s_free, p_full (softmax wrote P), pv_done
+    static constexpr int B_QFULL = 0, B_KVFULL = kQT, B_KVEMPTY = B_KVFULL + kStages,
+                         B_SFULL = B_KVEMPTY + kStages,
                          B_SFREE = B_SFULL + 2 * kQT, B_PFULL = B_SFREE + 2 * kQT,
                          B_PVDONE = B_PFULL + 2 * kQT, B_FINAL = B_PVDONE + 2 * kQT,
                          N_BAR = B_FINAL + 1;
@@ -143,8 +152,17 @@ __device__ __forceinline__ uint32_t sw128(int r, int c, int blk)
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
+// Bounded wait that ignores the abort flag: used only to let copies already
+// issued finish landing before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int32_t *status)
+{
+    for (uint32_t i = 0; i < kSpinLimit; ++i)
+        if (rx::mbar_try_wait(bar, parity)) return;
+    if (status) atomicOr(status, RX_DEV_TIMEOUT);
+}
+
 // ---------------------------------------------------------------------------
-// producer warps: Q once, then K/V tiles through the slot list
+// producer warps: K and V tiles through the slot list
 // ---------------------------------------------------------------------------
 
 template <int D>
@@ -156,7 +174,6 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
     const int32_t *sbuf = reinterpret_cast<const int32_t *>(smem + L::OFF_SLOT);
     const int pt = threadIdx.x - kProducer0;
-    const int G = p.G;
 
     // slot ids of tile j -> slot ring entry j % kNSL (4-byte async copies)
     auto fetch_slots = [&](int j) {
@@ -166,14 +183,6 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
                            T.slots + (pos < T.kv_end ? pos : 0), pos < T.kv_end ? 4 : 0);
         }
     };
-    // group "prologue": Q rows and the slot ids of the first kLag tiles
-    for (int idx = pt; idx < T.nqt * kRows * CPR; idx += kProducers) {
-        const int r = idx / CPR, c = idx % CPR;
-        const bool ok = r < T.M;
-        const bf16 *src = ok ? p.q + ((T.qbase + r / G) * p.hq + (int64_t)T.g * G + r % G) * D + c * 8 : p.q;
-        rx::cp_async_16(sbase + L::OFF_Q + (r / kRows) * L::NB * L::QBLK + sw128(r % kRows, c, L::QBLK), src,
-                        ok ? 16 : 0);
-    }
     for (int j = 0; j < kLag; ++j) fetch_slots(j);
     rx::cp_async_commit();
 
@@ -184,9 +193,9 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
     // thread fences the landed rows into the async proxy before reading them.
     for (int j = 0; j < T.ntiles; ++j) {
         const int st = j % kStages;
-        if (j == 0)
-            rx::cp_async_wait<0>();                 // Q and the first slot ids
-        else if (j >= kLag)
+        if (j < kLag)
+            rx::cp_async_wait<0>();                 // the first slot ids
+        else
             rx::cp_async_wait<kLag - 1>();          // group of tile j - kLag: slot ids of tile j
         rx::named_bar_sync(1, kProducers);          // every producer sees the slot ids
         if (j >= kStages) {
@@ -197,7 +206,6 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
         const uint32_t kd = sbase + L::OFF_K + st * L::NB * L::KBLK;
         const uint32_t vd = sbase + L::OFF_V + st * L::NB * L::KBLK;
         const int32_t *sl = sbuf + (j % kNSL) * kBN;
-#pragma unroll 4
         for (int idx = pt; idx < kBN * CPR; idx += kProducers) {
             const int r = idx / CPR, c = idx % CPR;
             const int pos = j * kBN + r;
@@ -246,7 +254,7 @@ __device__ void mma_issuer(const XParams &p, const Tile &T, unsigned char *smem,
             const int j = jp[t];
             if (j >= js) continue;
             const int pb = j & 1;
-            if (!rx::mbar_try_wait(bar + 8 * (L::B_PFULL + 2 * t + pb), (j >> 1) & 1)) continue;
+            if (!rx::mbar_test_wait(bar + 8 * (L::B_PFULL + 2 * t + pb), (j >> 1) & 1)) continue;
             rx::tc_fence_after();
             const uint32_t vbase = sbase + L::OFF_V + (j % kStages) * L::NB * L::KBLK;
             const uint32_t pbase = sbase + L::OFF_P + (2 * t + pb) * L::QBLK;
@@ -264,12 +272,13 @@ __device__ void mma_issuer(const XParams &p, const Tile &T, unsigned char *smem,
         for (; jrel < jdone; ++jrel) rx::tc_commit(bar + 8 * (L::B_KVEMPTY + jrel % kStages));
         if (js < T.ntiles) {
             const int st = js % kStages, sb = js & 1;
-            bool ready = rx::mbar_try_wait(bar + 8 * (L::B_KVFULL + st), (js / kStages) & 1);
+            bool ready = rx::mbar_test_wait(bar + 8 * (L::B_KVFULL + st), (js / kStages) & 1);
             for (int t = 0; t < T.nqt && ready; ++t)
-                ready = js < 2 ||
-                        rx::mbar_try_wait(bar + 8 * (L::B_SFREE + 2 * t + sb), ((js >> 1) - 1) & 1);
+                ready = js == 0   ? rx::mbar_test_wait(bar + 8 * (L::B_QFULL + t), 0)
+                        : js < 2 ? true
+                                 : rx::mbar_test_wait(bar + 8 * (L::B_SFREE + 2 * t + sb), ((js >> 1) - 1) & 1);
             if (ready) {
-                rx::fence_proxy_async_smem();  // the landed K/V rows (and Q) -> async proxy
+                rx::fence_proxy_async_smem();  // K/V rows landed by cp.async -> async proxy
                 rx::tc_fence_after();
                 const uint32_t kbase = sbase + L::OFF_K + st * L::NB * L::KBLK;
                 for (int t = 0; t < T.nqt; ++t) {
@@ -289,7 +298,7 @@ __device__ void mma_issuer(const XParams &p, const Tile &T, unsigned char *smem,
         }
         if (did) {
             idle = 0;
-        } else if (++idle > kSpinLimit || *abort_flag) {
+        } else if (++idle > kIdleLimit || *abort_flag) {
             if (!*abort_flag) {
                 *abort_flag = 1;
                 if (p.status) atomicOr(p.status, RX_DEV_TIMEOUT);
@@ -299,7 +308,7 @@ __device__ void mma_issuer(const XParams &p, const Tile &T, unsigned char *smem,
     }
     // everything issued has finished before TMEM is released
     rx::tc_commit(bar + 8 * L::B_FINAL);
-    wait_or_abort(bar + 8 * L::B_FINAL, 0, abort_flag, p.status);
+    drain_wait(bar + 8 * L::B_FINAL, 0, p.status);
 }
 
 // ---------------------------------------------------------------------------
@@ -323,6 +332,25 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
     const uint32_t tO = tbase + 128;
     const int row_lim = T.row0_pos + row / p.G;   // keys at positions <= row_lim are visible
     const float sl2 = p.scale_log2;
+    {
+        // this tile's Q rows (CTA row r: token r / G, q head g G + r % G) with
+        // coalesced 16-byte copies by the tile's four warps, zeros past the
+        // last row; fenced into the async proxy before the tensor core reads
+        constexpr int CPR = D / 8;
+        const int G = p.G;
+        const uint32_t qd = sbase + L::OFF_Q + t * L::NB * L::QBLK;
+        for (int idx = rl; idx < kRows * CPR; idx += kRows) {
+            const int r = idx / CPR, c = idx % CPR;
+            const int qr = t * kRows + r;
+            const bool ok = qr < T.M;
+            const bf16 *src = ok ? p.q + ((T.qbase + qr / G) * p.hq + (int64_t)T.g * G + qr % G) * D + c * 8 : p.q;
+            rx::cp_async_16(qd + sw128(r, c, L::QBLK), src, ok ? 16 : 0);
+        }
+        rx::cp_async_commit();
+        rx::cp_async_wait<0>();
+        rx::fence_proxy_async_smem();
+        rx::mbar_arrive(bar + 8 * (L::B_QFULL + t));
+    }
     float m_used = -INFINITY, l = 0.f;
     for (int j = 0; j < T.ntiles; ++j) {
         const int sb = j & 1;
@@ -419,7 +447,7 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) extend_kernel(const XParams p)
+__global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_constant__ XParams p)
 {
     using L = XL<D>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -457,9 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const XParams p)
     const uint32_t bar = sbase + L::OFF_BAR;
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
+        for (int i = 0; i < kQT; ++i) rx::mbar_init(bar + 8 * (L::B_QFULL + i), 128);  // softmax threads
         for (int i = 0; i < kStages; ++i) {
-            rx::mbar_init(bar + 8 * (L::B_KVFULL + i), kProducers);  // producer threads
-            rx::mbar_init(bar + 8 * (L::B_KVEMPTY + i), 1);          // MMA commit
+            rx::mbar_init(bar + 8 * (L::B_KVFULL + i), kProducers);  // producer threads' copies
+            rx::mbar_init(bar + 8 * (L::B_KVEMPTY + i), 1);  // MMA commit
         }
         for (int i = 0; i < 2 * kQT; ++i) {
             rx::mbar_init(bar + 8 * (L::B_SFULL + i), 1);     // MMA commit
@@ -478,12 +507,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const XParams p)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::OFF_TMEM);
 
     if (warp < 8) {
+        rx::reg_alloc<kRegSoftmax>();  // warpgroups 0-1, one program point
         softmax_rows<D>(p, T, smem, sbase, tmem);
-    } else if (warp < kMmaWarp) {
-        producer<D>(p, T, smem, sbase);
     } else {
-        if ((threadIdx.x & 31) == 0) mma_issuer<D>(p, T, smem, sbase, tmem);
-        __syncwarp();  // the whole warp reaches the exit barrier together
+        rx::reg_dealloc<kRegOther>();  // warpgroups 2-3, one program point
+        if (warp < kMmaWarp) {
+            producer<D>(p, T, smem, sbase);
+        } else {
+            if ((threadIdx.x & 31) == 0) mma_issuer<D>(p, T, smem, sbase, tmem);
+            __syncwarp();  // the whole warp reaches the exit barrier together
+        }
     }
 
     rx::tc_fence_before();
