@@ -138,7 +138,7 @@ class ClockSampler:
 class GpuStep:
     """Device state of one workload and the step that runs the path on it."""
 
-    def __init__(self, prob: inputs.Problem, torch, rx):
+    def __init__(self, prob: inputs.Problem, torch, rx, extend_path: str = "gather"):
         self.torch, self.rx, self.prob = torch, rx, prob
         dev = "cuda"
         p = prob
@@ -180,6 +180,12 @@ class GpuStep:
             self.ext_P, self.ext_E = i32(p.ext_prefix_len), i32(p.ext_extend_len)
             self.max_E = int(p.ext_extend_len.max())
             self.launches += 1
+            self.ext_ws = None
+            if extend_path == "staged":
+                ctx = int((p.ext_prefix_len + p.ext_extend_len).sum())
+                nb = rx.rx_attn_extend_workspace(ctx, len(p.ext_req_idx), p.hkv, p.d)
+                self.ext_ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+                self.launches += 2  # packed-row offsets + row copy
 
     def kv_store(self):
         self.rx.rx_kv_store(self.k_pool, self.v_pool, self.k_new, self.v_new, self.slots, self.status)
@@ -194,7 +200,7 @@ class GpuStep:
         p = self.prob
         self.rx.rx_attn_extend(self.k_pool, self.v_pool, self.q_ext, self.o_ext, None, self.qo,
                                self.ext_req, self.ext_P, self.ext_E, self.rtt, self.max_E, p.sm_scale,
-                               self.status)
+                               self.status, workspace=self.ext_ws)
 
     def step(self, marks=None):
         """The whole path; ``marks`` (dict of event pairs) brackets the parts."""
@@ -227,7 +233,7 @@ def run_gpu(args, rank, world, local_rank):
         dist.init_process_group("nccl")
 
     prob = make_problem(args)
-    st = GpuStep(prob, torch, rx)
+    st = GpuStep(prob, torch, rx, args.extend_path)
     flush = torch.empty(L2_FLUSH_BYTES // 2, dtype=torch.bfloat16, device="cuda")
     torch.cuda.synchronize()
 
@@ -315,7 +321,7 @@ def run_gpu(args, rank, world, local_rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random slot permutation)",
-        "config": workload_config(prob, args.workload, world),
+        "config": workload_config(prob, args.workload, world, args.extend_path),
         "roofline": roof, "e2e": e2e, "gpu_launches": st.launches * args.steps,
         "clocks": clk.summary(), "parts": out, "wall_s_timed_loop": round(t_wall, 3),
     }
@@ -372,7 +378,7 @@ def make_problem(args):
     return inputs.FULL_SIZE[args.workload](**kw)
 
 
-def workload_config(prob, name, world):
+def workload_config(prob, name, world, extend_path="gather"):
     cfg = {"workload": name, "hq": prob.hq, "hkv": prob.hkv, "head_dim": prob.d,
            "pool_slots": prob.num_slots, "decode_requests": int(len(prob.dec_req_idx)),
            "extend_requests": int(len(prob.ext_req_idx)),
@@ -383,6 +389,7 @@ def workload_config(prob, name, world):
     if len(prob.ext_req_idx):
         cfg["extend_prefix"] = int(prob.ext_prefix_len.max())
         cfg["extend_new"] = int(prob.ext_extend_len.max())
+        cfg["extend_path"] = extend_path
     return cfg
 
 
@@ -494,7 +501,7 @@ def run_reference(args, rank, world):
             "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16, random slot permutation)",
-            "config": workload_config(prob, args.workload, world),
+            "config": workload_config(prob, args.workload, world, args.extend_path),
             "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -512,6 +519,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="override the pool size (profiling runs on a smaller device footprint)")
+    ap.add_argument("--extend-path", default="gather", choices=["staged", "gather"],
+                    help="extend gathering rows in the attention kernel (default) or through a staging workspace")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

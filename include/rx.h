@@ -204,7 +204,9 @@ int rx_kv_store(const rx_kv_pool *pool, const void *k_new, const void *v_new, co
  * extend_len[b] new ones whose K/V are already in the pool; the slot list is
  * req_to_token row req_idx[b], positions 0 .. prefix_len[b]+extend_len[b]-1.
  * New token i of request b sits at position prefix_len[b] + i and attends to
- * positions 0 .. prefix_len[b] + i.
+ * positions 0 .. prefix_len[b] + i (the extend pass over a reused prefix:
+ * "SGLang: Efficient Execution of Structured Language Model Programs",
+ * "Introducción a SGLang", RadixAttention bullet).
  *   q:  device bf16 [sum(extend_len), num_q_heads, head_dim], request b's
  *       tokens at rows qo_indptr[b] .. qo_indptr[b+1]-1;
  *   o:  device bf16, same shape as q;  lse_or_null: device fp32
@@ -213,14 +215,31 @@ int rx_kv_store(const rx_kv_pool *pool, const void *k_new, const void *v_new, co
  *       device int32 [batch]; req_to_token: device int32, row stride
  *       rtt_stride;
  *   max_extend_len: host bound on extend_len[b] (sizes the grid; larger
- *       device values are an error that leaves rows unwritten).
- * Requires head_dim == 128, num_q_heads % num_kv_heads == 0 and
+ *       device values are an error that leaves rows unwritten);
+ *   workspace, ws_bytes: NULL / 0, or device memory of at least
+ *       rx_attn_extend_workspace(...) bytes, 256-byte aligned, owned by the
+ *       caller and not used by anything else until the call's work on
+ *       `stream` is done.  With a workspace the call first copies every
+ *       request's context rows out of the pool into it, packed per request,
+ *       and the attention kernel then streams them with tiled TMA loads;
+ *       without one the attention kernel gathers rows through the slot list
+ *       itself.  Both give the same result.  Contexts that sum to more rows
+ *       than the workspace was sized for set RX_DEV_BAD_LEN and leave every
+ *       output row unwritten.
+ * Requires head_dim 64 or 128, num_q_heads % num_kv_heads == 0 and
  * 128 % (num_q_heads / num_kv_heads) == 0. */
 int rx_attn_extend(const rx_kv_pool *pool, const void *q, void *o, float *lse_or_null,
                    int32_t num_q_heads, const int32_t *qo_indptr, const int32_t *req_idx,
                    const int32_t *prefix_len, const int32_t *extend_len,
                    const int32_t *req_to_token, int64_t rtt_stride, int32_t batch,
-                   int32_t max_extend_len, float sm_scale, int32_t *dev_status, void *stream);
+                   int32_t max_extend_len, void *workspace, size_t ws_bytes, float sm_scale,
+                   int32_t *dev_status, void *stream);
+
+/* Workspace bytes for rx_attn_extend over `batch` requests whose contexts
+ * (prefix_len[b] + extend_len[b]) sum to at most total_ctx_tokens; 0 on an
+ * invalid argument (rx_last_error says which). */
+size_t rx_attn_extend_workspace(int64_t total_ctx_tokens, int32_t batch, int32_t num_kv_heads,
+                                int32_t head_dim);
 
 /* ---- decode -------------------------------------------------------------
  * Decode plan: which requests of the batch share which positions, so that a

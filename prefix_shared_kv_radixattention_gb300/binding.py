@@ -92,7 +92,8 @@ _sig("rx_admit", ctypes.c_int, _P, _P, _P, _I64, _P, _PI64, _PI64)
 _sig("rx_commit", ctypes.c_int, _P, _P, _P, _P, _I64, _I64)
 _sig("rx_kv_store", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I64, _P, _P)
 _sig("rx_attn_extend", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I32, _P, _P, _P, _P, _P,
-     _I64, _I32, _I32, ctypes.c_float, _P, _P)
+     _I64, _I32, _I32, _P, ctypes.c_size_t, ctypes.c_float, _P, _P)
+_sig("rx_attn_extend_workspace", ctypes.c_size_t, _I64, _I32, _I32, _I32)
 _sig("rx_decode_plan_build", ctypes.c_int, _P, _I64, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64,
      ctypes.POINTER(DecodePlanInfo))
 _sig("rx_attn_decode_workspace", ctypes.c_size_t, _I32, _I32, _I32, _I32, _I32,
@@ -315,9 +316,20 @@ def rx_kv_store(k_pool, v_pool, k_new, v_new, slots, dev_status=None, stream=Non
                             _ptr(dev_status), _stream(stream)))
 
 
+def rx_attn_extend_workspace(total_ctx_tokens: int, batch: int, num_kv_heads: int, head_dim: int) -> int:
+    """Workspace bytes for rx_attn_extend's staged path (contexts summing to at
+    most total_ctx_tokens tokens)."""
+    n = _lib.rx_attn_extend_workspace(int(total_ctx_tokens), int(batch), int(num_kv_heads), int(head_dim))
+    if n == 0:
+        raise RxError(last_error())
+    return int(n)
+
+
 def rx_attn_extend(k_pool, v_pool, q, o, lse, qo_indptr, req_idx, prefix_len, extend_len,
                    req_to_token, max_extend_len: int, sm_scale: float, dev_status=None,
-                   stream=None) -> None:
+                   stream=None, workspace=None) -> None:
+    """Extend attention; `workspace` (a device uint8 tensor of at least
+    rx_attn_extend_workspace(...) bytes) selects the staged path."""
     torch = _torch()
     pool = make_pool(k_pool, v_pool)
     for t, n in ((q, "q"), (o, "o")):
@@ -327,13 +339,15 @@ def rx_attn_extend(k_pool, v_pool, q, o, lse, qo_indptr, req_idx, prefix_len, ex
                  (extend_len, "extend_len"), (req_to_token, "req_to_token")):
         _dev(t, torch.int32, n)
     _dev(dev_status, torch.int32, "dev_status")
+    _dev(workspace, torch.uint8, "workspace")
     if q.dim() != 3 or q.shape != o.shape:
         raise ValueError("q and o must be [tokens, num_q_heads, head_dim]")
+    ws_bytes = 0 if workspace is None else workspace.numel()
     _check(_lib.rx_attn_extend(ctypes.byref(pool), _ptr(q), _ptr(o), _ptr(lse), q.shape[1],
                                _ptr(qo_indptr), _ptr(req_idx), _ptr(prefix_len), _ptr(extend_len),
                                _ptr(req_to_token), req_to_token.shape[1], req_idx.numel(),
-                               int(max_extend_len), float(sm_scale), _ptr(dev_status),
-                               _stream(stream)))
+                               int(max_extend_len), _ptr(workspace), ws_bytes, float(sm_scale),
+                               _ptr(dev_status), _stream(stream)))
 
 
 @dataclass

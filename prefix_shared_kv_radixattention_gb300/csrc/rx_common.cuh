@@ -160,6 +160,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// TMA tiled load of one box of a 3-D tensor map at coordinates (c0, c1, c2)
+// (c0 innermost) into dst, the map's swizzle applied; the bytes complete a
+// transaction on mbarrier bar.  Elements outside the map land as zeros.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int c0, int c1, int c2, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
 // Per-warpgroup register reallocation: every warp of a warpgroup executes the
 // same call; an increase waits until decreases elsewhere in the CTA have
 // released enough of the registers the CTA was launched with.

@@ -76,7 +76,6 @@ template <int D>
 struct Layout {
     static constexpr int NST = (D == 128) ? 4 : 8;      // K/V ring stages
     static constexpr int RS = D + 8;                    // padded row stride (elements)
-    static constexpr int ROWB = D * 2;                  // bytes of one row
     static constexpr int TILE = kBN * RS;               // elements of one K (or V) stage
     static constexpr int QSLOT = kMaxRows * RS;         // elements of one Q slot
     static constexpr int RED_FLOATS = 2 * 4 * 16 + 4 * 16 * D;  // m, l and O of 4 key splits

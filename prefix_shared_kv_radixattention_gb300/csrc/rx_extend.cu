@@ -39,7 +39,11 @@
 // Every mbarrier wait is bounded: a wait that gives up sets RX_DEV_TIMEOUT
 // and raises an abort flag; every role then runs to the common exit, where
 // the MMA thread waits for its last tensor-core work and TMEM is freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
+
+#include <mutex>
 
 #include "rx_common.cuh"
 
@@ -64,6 +68,12 @@ constexpr int kThreads = 32 * 16;
 constexpr uint32_t kRegSoftmax = 184;
 constexpr uint32_t kRegOther = 72;
 static_assert(2 * 128 * kRegSoftmax + 2 * 128 * kRegOther == 65536, "register split");
+// staged path (contexts copied into a workspace first): one TMA thread feeds
+// the ring, so the CTA is 8 softmax warps + a producer warp + the MMA warp
+constexpr int kStagedThreads = 32 * 10;
+constexpr int kStagedProducerWarp = 8;
+constexpr int kStagedMmaWarp = 9;
+constexpr int kStageBlock = 16;    // rows per copy unit of the staging kernel
 constexpr uint32_t kSpinLimit = 1u << 22;
 constexpr uint32_t kIdleLimit = 1u << 27;  // polls of the MMA thread without progress
 constexpr uint32_t kTmemCols = 512;  // per Q tile t: S0 [256t, +64), S1 [+64, +128), O [+128, +256)
@@ -94,7 +104,13 @@ struct XL {
 static_assert(XL<128>::BYTES <= 227 * 1024, "shared memory budget");
 static_assert(XL<128>::OFF_BAR % 8 == 0 && XL<64>::OFF_BAR % 8 == 0, "mbarrier alignment");
 
-struct XParams {
+struct XParams {  // 64-byte aligned through its tensor maps
+    // staged path: the packed context rows as [row][kv head][head_dim], box
+    // 64 x 1 x 64 (128-byte rows, 128-byte swizzle)
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
+    const int64_t *stage_offs;  // first packed row of request b; [batch] = rows used
+    int64_t stage_cap;          // rows the workspace holds
     const bf16 *q;
     bf16 *o;
     float *lse;
@@ -119,6 +135,7 @@ struct Tile {
     int row0_pos;      // absolute position of row group 0
     int kv_end;        // keys [0, kv_end)
     int ntiles;
+    int stage_row0;    // staged path: first packed row of this request
     const int32_t *slots;
     int g;
 };
@@ -225,11 +242,46 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
     rx::cp_async_wait<0>();
 }
 
+// Staged path: one thread streams tile j of the request's packed context with
+// four (D = 128) or two (D = 64) TMA box loads -- K and V, one box per
+// 128-byte column block, each box 64 rows of one kv head.  Every packed
+// region is a whole number of 64-row tiles with zeroed padding, so the boxes
+// never leave the request's region.
+template <int D>
+__device__ void tma_producer(const XParams &p, const Tile &T, unsigned char *smem, uint32_t sbase)
+{
+    using L = XL<D>;
+    const uint32_t bar = sbase + L::OFF_BAR;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
+    int issued = 0;
+    for (int j = 0; j < T.ntiles; ++j) {
+        const int st = j % kStages;
+        if (j >= kStages &&
+            !wait_or_abort(bar + 8 * (L::B_KVEMPTY + st), ((j / kStages) - 1) & 1, abort_flag, p.status))
+            break;
+        const uint32_t full = bar + 8 * (L::B_KVFULL + st);
+        rx::mbar_arrive_expect_tx(full, 2 * kBN * D * 2);
+        const uint32_t kd = sbase + L::OFF_K + st * L::NB * L::KBLK;
+        const uint32_t vd = sbase + L::OFF_V + st * L::NB * L::KBLK;
+        const int row = T.stage_row0 + j * kBN;
+#pragma unroll
+        for (int cb = 0; cb < L::NB; ++cb) {
+            rx::tma_load_3d(kd + cb * L::KBLK, &p.tm_k, cb * 64, T.g, row, full);
+            rx::tma_load_3d(vd + cb * L::KBLK, &p.tm_v, cb * 64, T.g, row, full);
+        }
+        issued = j + 1;
+    }
+    // no copy may still be landing when the CTA exits (normally every stage
+    // was consumed already; after an abort the last ones may not have been)
+    for (int jj = issued > kStages ? issued - kStages : 0; jj < issued; ++jj)
+        drain_wait(bar + 8 * (L::B_KVFULL + jj % kStages), (jj / kStages) & 1, p.status);
+}
+
 // ---------------------------------------------------------------------------
 // MMA thread
 // ---------------------------------------------------------------------------
 
-template <int D>
+template <int D, bool kStaged>
 __device__ void mma_issuer(const XParams &p, const Tile &T, unsigned char *smem, uint32_t sbase,
                            uint32_t tmem)
 {
@@ -278,7 +330,7 @@ __device__ void mma_issuer(const XParams &p, const Tile &T, unsigned char *smem,
                         : js < 2 ? true
                                  : rx::mbar_test_wait(bar + 8 * (L::B_SFREE + 2 * t + sb), ((js >> 1) - 1) & 1);
             if (ready) {
-                rx::fence_proxy_async_smem();  // K/V rows landed by cp.async -> async proxy
+                if (!kStaged) rx::fence_proxy_async_smem();  // K/V rows landed by cp.async -> async proxy
                 rx::tc_fence_after();
                 const uint32_t kbase = sbase + L::OFF_K + st * L::NB * L::KBLK;
                 for (int t = 0; t < T.nqt; ++t) {
@@ -446,8 +498,9 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
     if (valid && p.lse) p.lse[orow] = (m_used + log2f(l)) * rx::kLn2;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_constant__ XParams p)
+template <int D, bool kStaged>
+__global__ void __launch_bounds__(kStaged ? kStagedThreads : kThreads, 1)
+    extend_kernel(const __grid_constant__ XParams p)
 {
     using L = XL<D>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -474,6 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_consta
         if (p.status && threadIdx.x == 0) atomicOr(p.status, RX_DEV_BAD_LEN);
         return;
     }
+    if (kStaged) {
+        // contexts larger than the workspace: nothing was staged (flagged there)
+        if (p.stage_offs[gridDim.z] > p.stage_cap) return;
+        T.stage_row0 = (int)p.stage_offs[b];
+    }
     T.M = ntok * p.G;
     T.nqt = T.M > kRows ? 2 : 1;
     T.qbase = (int64_t)__ldg(p.qo_indptr + b) + t0;
@@ -484,10 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_consta
 
     const uint32_t bar = sbase + L::OFF_BAR;
     const int warp = threadIdx.x >> 5;
+    constexpr int mma_warp = kStaged ? kStagedMmaWarp : kMmaWarp;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kQT; ++i) rx::mbar_init(bar + 8 * (L::B_QFULL + i), 128);  // softmax threads
         for (int i = 0; i < kStages; ++i) {
-            rx::mbar_init(bar + 8 * (L::B_KVFULL + i), kProducers);  // producer threads' copies
+            // gather path: every producer thread's copies; staged: the TMA thread's
+            // arrival plus the boxes' bytes
+            rx::mbar_init(bar + 8 * (L::B_KVFULL + i), kStaged ? 1 : kProducers);
             rx::mbar_init(bar + 8 * (L::B_KVEMPTY + i), 1);  // MMA commit
         }
         for (int i = 0; i < 2 * kQT; ++i) {
@@ -500,30 +561,145 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_consta
         *reinterpret_cast<volatile int *>(smem + L::OFF_ABORT) = 0;
         rx::fence_mbar_init();
     }
-    if (warp == kMmaWarp) rx::tmem_alloc(sbase + L::OFF_TMEM, kTmemCols);
+    if (warp == mma_warp) rx::tmem_alloc(sbase + L::OFF_TMEM, kTmemCols);
     rx::tc_fence_before();
     __syncthreads();
     rx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::OFF_TMEM);
 
     if (warp < 8) {
-        rx::reg_alloc<kRegSoftmax>();  // warpgroups 0-1, one program point
+        if (!kStaged) rx::reg_alloc<kRegSoftmax>();  // warpgroups 0-1, one program point
         softmax_rows<D>(p, T, smem, sbase, tmem);
     } else {
-        rx::reg_dealloc<kRegOther>();  // warpgroups 2-3, one program point
-        if (warp < kMmaWarp) {
-            producer<D>(p, T, smem, sbase);
+        if (!kStaged) rx::reg_dealloc<kRegOther>();  // warpgroups 2-3, one program point
+        if (warp < mma_warp) {
+            if (!kStaged) {
+                producer<D>(p, T, smem, sbase);
+            } else if (warp == kStagedProducerWarp) {
+                if ((threadIdx.x & 31) == 0) tma_producer<D>(p, T, smem, sbase);
+                __syncwarp();
+            }
         } else {
-            if ((threadIdx.x & 31) == 0) mma_issuer<D>(p, T, smem, sbase, tmem);
+            if ((threadIdx.x & 31) == 0) mma_issuer<D, kStaged>(p, T, smem, sbase, tmem);
             __syncwarp();  // the whole warp reaches the exit barrier together
         }
     }
 
     rx::tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == mma_warp) {
         rx::tc_fence_after();
         rx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// staging: the contexts copied out of the pool, packed per request
+// ---------------------------------------------------------------------------
+
+// Packed rows of request b: its context (prefix + extend tokens) rounded up
+// to whole 64-row tiles; none for lengths the attention kernel rejects.
+__device__ __forceinline__ int64_t staged_rows(const int32_t *prefix_len, const int32_t *extend_len, int b,
+                                               int64_t rtt_stride)
+{
+    const int64_t P = __ldg(prefix_len + b), E = __ldg(extend_len + b);
+    if (P < 0 || E < 0 || P + E > rtt_stride) return 0;
+    return (P + E + kBN - 1) / kBN * kBN;
+}
+
+// offs[b] = first packed row of request b (exclusive prefix sum of the
+// packed row counts), offs[batch] = rows used; more than `cap` rows is
+// flagged, and then neither the copy nor the attention kernel does anything.
+__global__ void __launch_bounds__(1024) ctx_offsets_kernel(const int32_t *prefix_len, const int32_t *extend_len,
+                                                           int batch, int64_t rtt_stride, int64_t cap,
+                                                           int64_t *offs, int32_t *status)
+{
+    __shared__ int64_t warp_tot[32];
+    const int per = (batch + 1023) / 1024;
+    const int b0 = threadIdx.x * per;
+    int64_t local = 0;
+    for (int i = 0; i < per && b0 + i < batch; ++i) local += staged_rows(prefix_len, extend_len, b0 + i, rtt_stride);
+    // inclusive scan over the block: within each warp, then over warp totals
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t x = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t w = warp_tot[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, w, d);
+            if (lane >= d) w += y;
+        }
+        warp_tot[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    int64_t run = x - local + (warp > 0 ? warp_tot[warp - 1] : 0);  // exclusive
+    for (int i = 0; i < per && b0 + i < batch; ++i) {
+        offs[b0 + i] = run;
+        run += staged_rows(prefix_len, extend_len, b0 + i, rtt_stride);
+    }
+    if (threadIdx.x == 1023) {
+        const int64_t total = warp_tot[31];
+        offs[batch] = total;
+        if (total > cap && status) atomicOr(status, RX_DEV_BAD_LEN);
+    }
+}
+
+// Packed row offs[b] + pos = pool row req_to_token[req_idx[b]][pos] for K and
+// V (all kv heads: one contiguous row of the pool each), zeros from the end of
+// the context to the 64-row boundary and for slot ids outside the pool
+// (flagged).  One warp per block of kStageBlock rows; every request's region
+// is a multiple of 64 rows, so a block never straddles two requests.
+__global__ void __launch_bounds__(256) stage_rows_kernel(
+    const bf16 *__restrict__ k_pool, const bf16 *__restrict__ v_pool, int64_t num_slots,
+    const int32_t *__restrict__ rtt, int64_t rtt_stride, const int32_t *__restrict__ req_idx,
+    const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ extend_len, int batch,
+    const int64_t *__restrict__ offs, int64_t cap, bf16 *__restrict__ ks, bf16 *__restrict__ vs, int row_elems,
+    int32_t *status)
+{
+    const int64_t total = offs[batch];
+    if (total > cap) return;
+    const int lane = threadIdx.x & 31;
+    const int row_vecs = row_elems / 8;
+    const int64_t nblk = total / kStageBlock;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t blk = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; blk < nblk; blk += nwarps) {
+        const int64_t row0 = blk * kStageBlock;
+        int lo = 0, hi = batch - 1;  // last request whose region starts at or before row0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (offs[mid] <= row0) lo = mid; else hi = mid - 1;
+        }
+        const int b = lo;
+        const int64_t ctx = (int64_t)__ldg(prefix_len + b) + __ldg(extend_len + b);
+        const int64_t pos0 = row0 - offs[b];
+        int32_t my_slot = -1;
+        if (lane < kStageBlock && pos0 + lane < ctx) {
+            const int32_t sl = __ldg(rtt + (int64_t)__ldg(req_idx + b) * rtt_stride + pos0 + lane);
+            if (sl >= 0 && (int64_t)sl < num_slots) my_slot = sl;
+            else if (status) atomicOr(status, RX_DEV_BAD_SLOT);
+        }
+#pragma unroll 4
+        for (int r = 0; r < kStageBlock; ++r) {
+            const int32_t sl = __shfl_sync(0xffffffffu, my_slot, r);
+            const uint4 *ksrc = reinterpret_cast<const uint4 *>(k_pool + (int64_t)(sl < 0 ? 0 : sl) * row_elems);
+            const uint4 *vsrc = reinterpret_cast<const uint4 *>(v_pool + (int64_t)(sl < 0 ? 0 : sl) * row_elems);
+            uint4 *kdst = reinterpret_cast<uint4 *>(ks + (row0 + r) * row_elems);
+            uint4 *vdst = reinterpret_cast<uint4 *>(vs + (row0 + r) * row_elems);
+            for (int v = lane; v < row_vecs; v += 32) {
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                const uint4 kv = sl >= 0 ? __ldg(ksrc + v) : z;
+                const uint4 vv = sl >= 0 ? __ldg(vsrc + v) : z;
+                kdst[v] = kv;
+                vdst[v] = vv;
+            }
+        }
     }
 }
 
@@ -537,16 +713,78 @@ int check_pool(const rx_kv_pool *pool)
     return RX_OK;
 }
 
-template <int D>
+// Workspace of the staged path: int64 packed-row offsets [batch + 1], then the
+// packed K rows and the packed V rows, [cap][kv heads][head_dim] bf16 each,
+// every part 256-byte aligned.
+struct StageLayout {
+    size_t off_k, off_v, bytes;
+};
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+StageLayout stage_layout(int64_t cap, int32_t batch, int64_t row_bytes)
+{
+    StageLayout l;
+    l.off_k = align256((size_t)(batch + 1) * sizeof(int64_t));
+    const size_t region = align256((size_t)cap * (size_t)row_bytes);
+    l.off_v = l.off_k + region;
+    l.bytes = l.off_v + region;
+    return l;
+}
+// largest row count a workspace of ws_bytes holds (TMA row coordinates are int32)
+int64_t stage_cap_for(size_t ws_bytes, int32_t batch, int64_t row_bytes)
+{
+    const size_t head = align256((size_t)(batch + 1) * sizeof(int64_t));
+    if (ws_bytes <= head) return 0;
+    int64_t cap = (int64_t)((ws_bytes - head) / 2 / (size_t)row_bytes);
+    cap = cap < (int64_t)INT32_MAX - 2 * kBN ? cap : (int64_t)INT32_MAX - 2 * kBN;
+    while (cap > 0 && stage_layout(cap, batch, row_bytes).bytes > ws_bytes) --cap;
+    return cap;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); looked up once per process.
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Packed rows [cap][hkv][D] bf16 as a 3-D map whose box is 64 elements (128
+// bytes, the swizzle span) of one kv head over 64 consecutive rows.
+int encode_stage_map(CUtensorMap *m, void *base, int64_t cap, int hkv, int D)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
+    if (!fn) return rx_set_error(RX_ERR_CUDA, "rx_attn_extend: cuTensorMapEncodeTiled not available");
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)cap};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * sizeof(bf16), (cuuint64_t)hkv * D * sizeof(bf16)};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)kBN};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return rx_set_error(RX_ERR_CUDA, "rx_attn_extend: tensor map encode failed (%d)", (int)r);
+    return RX_OK;
+}
+
+template <int D, bool kStaged>
 int launch_extend(const XParams &p, dim3 grid, cudaStream_t st)
 {
     static bool configured = false;
     if (!configured) {
-        RX_CUDA_CHECK(cudaFuncSetAttribute(extend_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           XL<D>::BYTES));
+        RX_CUDA_CHECK(cudaFuncSetAttribute(extend_kernel<D, kStaged>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, XL<D>::BYTES));
         configured = true;
     }
-    extend_kernel<D><<<grid, kThreads, XL<D>::BYTES, st>>>(p);
+    extend_kernel<D, kStaged><<<grid, kStaged ? kStagedThreads : kThreads, XL<D>::BYTES, st>>>(p);
     RX_CUDA_CHECK(cudaGetLastError());
     return RX_OK;
 }
@@ -557,8 +795,8 @@ extern "C" int rx_attn_extend(const rx_kv_pool *pool, const void *q, void *o, fl
                               int32_t hq, const int32_t *qo_indptr, const int32_t *req_idx,
                               const int32_t *prefix_len, const int32_t *extend_len,
                               const int32_t *rtt, int64_t rtt_stride, int32_t batch,
-                              int32_t max_extend_len, float sm_scale, int32_t *dev_status,
-                              void *stream)
+                              int32_t max_extend_len, void *workspace, size_t ws_bytes, float sm_scale,
+                              int32_t *dev_status, void *stream)
 {
     int rc = check_pool(pool);
     if (rc != RX_OK) return rc;
@@ -573,6 +811,8 @@ extern "C" int rx_attn_extend(const rx_kv_pool *pool, const void *q, void *o, fl
     if (rx_misaligned16(q) || rx_misaligned16(o) || rx_misaligned16(pool->k) ||
         rx_misaligned16(pool->v) || (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
         return rx_set_error(RX_ERR_INVALID, "rx_attn_extend: q, o and the pools must be 16-byte aligned");
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_extend: workspace must be 256-byte aligned");
     if (batch == 0 || max_extend_len == 0) return RX_OK;
     if (batch > 65535 || pool->num_kv_heads > 65535)
         return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_extend: batch or kv heads above 65535");
@@ -597,5 +837,46 @@ extern "C" int rx_attn_extend(const rx_kv_pool *pool, const void *q, void *o, fl
     const int tb = kCtaRows / p.G;
     dim3 grid((unsigned)((max_extend_len + tb - 1) / tb), (unsigned)p.hkv, (unsigned)batch);
     cudaStream_t st = (cudaStream_t)stream;
-    return pool->head_dim == 128 ? launch_extend<128>(p, grid, st) : launch_extend<64>(p, grid, st);
+    const int D = pool->head_dim;
+    if (!workspace)
+        return D == 128 ? launch_extend<128, false>(p, grid, st) : launch_extend<64, false>(p, grid, st);
+
+    // staged path: offsets, packed copy of every context, then attention
+    const int64_t row_bytes = (int64_t)p.hkv * D * (int64_t)sizeof(bf16);
+    const int64_t cap = stage_cap_for(ws_bytes, batch, row_bytes);
+    if (cap < kBN) return rx_set_error(RX_ERR_CAPACITY, "rx_attn_extend: workspace of %zu bytes too small", ws_bytes);
+    const StageLayout lay = stage_layout(cap, batch, row_bytes);
+    int64_t *offs = static_cast<int64_t *>(workspace);
+    bf16 *ks = reinterpret_cast<bf16 *>(static_cast<char *>(workspace) + lay.off_k);
+    bf16 *vs = reinterpret_cast<bf16 *>(static_cast<char *>(workspace) + lay.off_v);
+    if ((rc = encode_stage_map(&p.tm_k, ks, cap, p.hkv, D)) != RX_OK) return rc;
+    if ((rc = encode_stage_map(&p.tm_v, vs, cap, p.hkv, D)) != RX_OK) return rc;
+    p.stage_offs = offs;
+    p.stage_cap = cap;
+    int dev = 0, sms = 0;
+    RX_CUDA_CHECK(cudaGetDevice(&dev));
+    RX_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    ctx_offsets_kernel<<<1, 1024, 0, st>>>(prefix_len, extend_len, batch, rtt_stride, cap, offs, dev_status);
+    RX_CUDA_CHECK(cudaGetLastError());
+    stage_rows_kernel<<<sms * 8, 256, 0, st>>>(p.k_pool, p.v_pool, p.num_slots, rtt, rtt_stride, req_idx,
+                                               prefix_len, extend_len, batch, offs, cap, ks, vs,
+                                               p.hkv * D, dev_status);
+    RX_CUDA_CHECK(cudaGetLastError());
+    return D == 128 ? launch_extend<128, true>(p, grid, st) : launch_extend<64, true>(p, grid, st);
+}
+
+extern "C" size_t rx_attn_extend_workspace(int64_t total_ctx_tokens, int32_t batch, int32_t num_kv_heads,
+                                           int32_t head_dim)
+{
+    if (total_ctx_tokens < 0 || batch <= 0 || batch > 65535 || num_kv_heads <= 0 ||
+        (head_dim != 64 && head_dim != 128)) {
+        rx_set_error(RX_ERR_INVALID, "rx_attn_extend_workspace: invalid argument");
+        return 0;
+    }
+    const int64_t cap = total_ctx_tokens + (int64_t)(kBN - 1) * batch;  // each context rounded up to 64 rows
+    if (cap > (int64_t)INT32_MAX - 2 * kBN) {
+        rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_extend_workspace: %lld context rows", (long long)cap);
+        return 0;
+    }
+    return stage_layout(cap < kBN ? kBN : cap, batch, (int64_t)num_kv_heads * head_dim * 2).bytes;
 }

@@ -81,14 +81,21 @@ class Dev:
         torch.cuda.synchronize()
         return o.float().cpu().numpy(), (lse.cpu().numpy() if with_lse else None)
 
-    def extend(self, with_lse: bool = True):
+    def extend(self, with_lse: bool = True, staged: bool = False, ws_rows=None):
+        """Extend through the C ABI; staged=True passes a workspace sized for
+        the problem's contexts (or for ws_rows context tokens)."""
         p = self.prob
         q = to_dev(p.q_ext)
         o = torch.empty_like(q)
         lse = torch.empty((q.shape[0], p.hq), dtype=torch.float32, device="cuda") if with_lse else None
+        ws = None
+        if staged:
+            rows = int((p.ext_prefix_len + p.ext_extend_len).sum()) if ws_rows is None else int(ws_rows)
+            nb = rx.rx_attn_extend_workspace(rows, len(p.ext_req_idx), p.hkv, p.d)
+            ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
         rx.rx_attn_extend(self.k_pool, self.v_pool, q, o, lse, i32(p.qo_indptr), i32(p.ext_req_idx),
                           i32(p.ext_prefix_len), i32(p.ext_extend_len), self.rtt,
-                          int(p.ext_extend_len.max()), p.sm_scale, self.status)
+                          int(p.ext_extend_len.max()), p.sm_scale, self.status, workspace=ws)
         torch.cuda.synchronize()
         return o.float().cpu().numpy(), (lse.cpu().numpy() if with_lse else None)
 

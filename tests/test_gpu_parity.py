@@ -77,11 +77,11 @@ def test_kv_store_empty_is_noop():
 # ---------------------------------------------------------------------------
 
 
-def _check_extend(prob, g=None):
+def _check_extend(prob, g=None, staged=False):
     g = g or _gpu()
     dev = g.Dev(prob)
     dev.kv_store()
-    o, lse = dev.extend()
+    o, lse = dev.extend(staged=staged)
     kp, vp, rtt = dev.oracle_pools()
     ro, rl = oracle.extend(prob.q_ext, kp, vp, rtt, prob.ext_req_idx, prob.ext_prefix_len,
                            prob.ext_extend_len, prob.qo_indptr, prob.sm_scale)
@@ -91,29 +91,68 @@ def _check_extend(prob, g=None):
     return o, lse
 
 
-def test_extend_tiny_full_config():
+@pytest.mark.parametrize("staged", [False, True])
+def test_extend_tiny_full_config(staged):
     """The tiny-extend configuration at its full size, every output."""
-    _check_extend(inputs.tiny_extend())
+    _check_extend(inputs.tiny_extend(), staged=staged)
 
 
+@pytest.mark.parametrize("staged", [False, True])
 @pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (8, 2, 64), (32, 8, 128), (16, 2, 128), (4, 1, 128)])
-def test_extend_ragged(hq, hkv, d):
+def test_extend_ragged(hq, hkv, d, staged):
     prob = inputs.ragged(20 + hq + d, hq=hq, hkv=hkv, d=d, n_groups=3, per_group=2, shared_max=150,
                          private_max=90, extend_max=140, decode=False, num_slots=3000)
-    _check_extend(prob)
+    _check_extend(prob, staged=staged)
 
 
-def test_extend_cached_prefix_reduced():
+@pytest.mark.parametrize("staged", [False, True])
+def test_extend_cached_prefix_reduced(staged):
     _check_extend(inputs.cached_prefix_extend(n_prefix=2, per_prefix=2, prefix=300, extend=150,
-                                              num_slots=4096))
+                                              num_slots=4096), staged=staged)
 
 
-def test_extend_edge_cases():
+@pytest.mark.parametrize("staged", [False, True])
+def test_extend_edge_cases(staged):
     # prefix 0 (plain causal), extend 1 (a single new token), long prefix
     for P, E in ((0, 70), (0, 1), (5, 1), (333, 3), (64, 64), (1, 129)):
         prob = inputs.tiny_extend(seed=P * 1000 + E, hq=8, hkv=2, d=128, batch=2, prefix=P, extend=E,
                                   num_slots=1024)
-        _check_extend(prob)
+        _check_extend(prob, staged=staged)
+
+
+def test_extend_staged_equals_gathered_bitwise():
+    """Staging the rows first changes where they are read from, not the arithmetic."""
+    g = _gpu()
+    prob = inputs.cached_prefix_extend(n_prefix=2, per_prefix=3, prefix=200, extend=130, num_slots=4096)
+    dev = g.Dev(prob)
+    dev.kv_store()
+    o1, l1 = dev.extend(staged=False)
+    o2, l2 = dev.extend(staged=True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    assert dev.status_word() == 0
+
+
+def test_extend_staged_workspace_too_small_is_flagged():
+    g = _gpu()
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.tiny_extend(seed=3, hq=8, hkv=2, d=128, batch=3, prefix=200, extend=40, num_slots=1024)
+    dev = g.Dev(prob)
+    dev.kv_store()
+    # sized for one request's context: the three need more rows than it holds
+    dev.extend(staged=True, ws_rows=240)
+    assert dev.status_word() & rx.RX_DEV_BAD_LEN
+
+
+def test_extend_staged_bad_slot_is_flagged():
+    g = _gpu()
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.tiny_extend(seed=4, hq=8, hkv=2, d=128, batch=2, prefix=100, extend=30, num_slots=1024)
+    dev = g.Dev(prob)
+    dev.kv_store()
+    dev.rtt[1, 17] = prob.num_slots + 5
+    o, _ = dev.extend(staged=True)
+    assert dev.status_word() & rx.RX_DEV_BAD_SLOT
+    assert np.isfinite(o).all()
 
 
 # ---------------------------------------------------------------------------

@@ -184,6 +184,17 @@ def test_match_capacity_error_code():
     assert "capacity" in rx.last_error()
 
 
+def test_extend_workspace_size():
+    """Offsets [batch+1] int64, then K and V areas of (total + 63 batch) rows of
+    num_kv_heads x head_dim bf16, each part rounded up to 256 bytes."""
+    def up(x):
+        return (x + 255) // 256 * 256
+    for total, batch, hkv, d in ((1000, 3, 8, 128), (0, 1, 4, 64), (81920, 32, 8, 128), (5, 7, 1, 64)):
+        rows = max(total + 63 * batch, 64)
+        want = up((batch + 1) * 8) + 2 * up(rows * hkv * d * 2)
+        assert rx.rx_attn_extend_workspace(total, batch, hkv, d) == want
+
+
 def test_invalid_arguments():
     lib = rx.library()
     import ctypes
@@ -193,7 +204,10 @@ def test_invalid_arguments():
     assert lib.rx_attn_decode(None, None, None, None, 0, None, None, None, 0, 0, 0, None, None, 0,
                               ctypes.c_float(1.0), None, None) == rx.RX_ERR_INVALID
     assert lib.rx_attn_extend(None, None, None, None, 0, None, None, None, None, None, 0, 0, 0,
-                              ctypes.c_float(1.0), None, None) == rx.RX_ERR_INVALID
+                              None, 0, ctypes.c_float(1.0), None, None) == rx.RX_ERR_INVALID
+    assert lib.rx_attn_extend_workspace(-1, 1, 8, 128) == 0
+    assert lib.rx_attn_extend_workspace(100, 0, 8, 128) == 0
+    assert lib.rx_attn_extend_workspace(100, 1, 8, 96) == 0
     with pytest.raises(rx.RxError):
         rx.SlotAllocator([0, 5], 3)
     a = rx.SlotAllocator([0, 1, 2], 3)
