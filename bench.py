@@ -138,7 +138,7 @@ class ClockSampler:
 class GpuStep:
     """Device state of one workload and the step that runs the path on it."""
 
-    def __init__(self, prob: inputs.Problem, torch, rx, extend_path: str = "gather"):
+    def __init__(self, prob: inputs.Problem, torch, rx, extend_path: str = "staged"):
         self.torch, self.rx, self.prob = torch, rx, prob
         dev = "cuda"
         p = prob
@@ -378,7 +378,7 @@ def make_problem(args):
     return inputs.FULL_SIZE[args.workload](**kw)
 
 
-def workload_config(prob, name, world, extend_path="gather"):
+def workload_config(prob, name, world, extend_path="staged"):
     cfg = {"workload": name, "hq": prob.hq, "hkv": prob.hkv, "head_dim": prob.d,
            "pool_slots": prob.num_slots, "decode_requests": int(len(prob.dec_req_idx)),
            "extend_requests": int(len(prob.ext_req_idx)),
@@ -519,8 +519,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="override the pool size (profiling runs on a smaller device footprint)")
-    ap.add_argument("--extend-path", default="gather", choices=["staged", "gather"],
-                    help="extend gathering rows in the attention kernel (default) or through a staging workspace")
+    ap.add_argument("--extend-path", default="staged", choices=["staged", "gather"],
+                    help="extend through a staging workspace (default) or gathering rows in the attention kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -75,7 +75,6 @@ constexpr int kStagedProducerWarp = 8;
 constexpr int kStagedMmaWarp = 9;
 constexpr int kStageBlock = 16;    // rows per copy unit of the staging kernel
 constexpr uint32_t kSpinLimit = 1u << 22;
-constexpr uint32_t kIdleLimit = 1u << 27;  // polls of the MMA thread without progress
 constexpr uint32_t kTmemCols = 512;  // per Q tile t: S0 [256t, +64), S1 [+64, +128), O [+128, +256)
 constexpr float kRescale = 8.f;      // log2 units the running max may lag
 
@@ -90,10 +89,12 @@ struct XL {
     static constexpr int OFF_P = OFF_V + kStages * NB * KBLK;  // [Q tile][2 buffers] x 128 x 64
     static constexpr int OFF_SLOT = OFF_P + kQT * 2 * QBLK;    // slot-id ring
     static constexpr int OFF_BAR = OFF_SLOT + kNSL * kBN * 4;
-    // per Q tile: q_full; per stage: kv_full, kv_empty; per Q tile and
-    // buffer: s_full, s_free, p_full (softmax wrote P), pv_done
-    static constexpr int B_QFULL = 0, B_KVFULL = kQT, B_KVEMPTY = B_KVFULL + kStages,
-                         B_SFULL = B_KVEMPTY + kStages,
+    // per Q tile: q_full; per stage: k_full, v_full, k_empty (S read it),
+    // v_empty (O += P V read it); per Q tile and buffer: s_full, s_free,
+    // p_full (softmax wrote P), pv_done
+    static constexpr int B_QFULL = 0, B_KFULL = kQT, B_VFULL = B_KFULL + kStages,
+                         B_KEMPTY = B_VFULL + kStages, B_VEMPTY = B_KEMPTY + kStages,
+                         B_SFULL = B_VEMPTY + kStages,
                          B_SFREE = B_SFULL + 2 * kQT, B_PFULL = B_SFREE + 2 * kQT,
                          B_PVDONE = B_PFULL + 2 * kQT, B_FINAL = B_PVDONE + 2 * kQT,
                          N_BAR = B_FINAL + 1;
@@ -144,6 +145,7 @@ struct Tile {
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                               int32_t *status)
 {
+    if (rx::mbar_test_wait(bar, parity)) return true;  // already flipped: no suspend
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         if (rx::mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
@@ -203,11 +205,13 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
     for (int j = 0; j < kLag; ++j) fetch_slots(j);
     rx::cp_async_commit();
 
-    // one cp.async group per tile j: its K/V rows and the slot ids of tile
-    // j + kLag.  The stage's full barrier gets each producer thread's arrival
-    // as soon as that thread's copies have landed (cp.async.mbarrier.arrive),
-    // so handing a tile over never waits for the producer loop; the MMA
-    // thread fences the landed rows into the async proxy before reading them.
+    // one cp.async group per tile j: its K and V rows and the slot ids of
+    // tile j + kLag.  K and V have their own stage barriers (a K stage frees
+    // as soon as S has read it, a V stage only after O += P V); each gets a
+    // producer thread's arrival as soon as that thread's copies have landed
+    // (cp.async.mbarrier.arrive), so handing a tile over never waits for the
+    // producer loop; the MMA thread fences the landed rows into the async
+    // proxy before reading them.
     for (int j = 0; j < T.ntiles; ++j) {
         const int st = j % kStages;
         if (j < kLag)
@@ -215,26 +219,34 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
         else
             rx::cp_async_wait<kLag - 1>();          // group of tile j - kLag: slot ids of tile j
         rx::named_bar_sync(1, kProducers);          // every producer sees the slot ids
-        if (j >= kStages) {
-            const bool ok = wait_or_abort(bar + 8 * (L::B_KVEMPTY + st), ((j / kStages) - 1) & 1,
-                                          abort_flag, p.status);
-            if (rx::named_bar_or(1, kProducers, !ok)) break;  // every producer leaves together
-        }
-        const uint32_t kd = sbase + L::OFF_K + st * L::NB * L::KBLK;
-        const uint32_t vd = sbase + L::OFF_V + st * L::NB * L::KBLK;
         const int32_t *sl = sbuf + (j % kNSL) * kBN;
-        for (int idx = pt; idx < kBN * CPR; idx += kProducers) {
-            const int r = idx / CPR, c = idx % CPR;
-            const int pos = j * kBN + r;
-            const int32_t s = sl[r];
-            const bool inside = pos < T.kv_end;
-            const bool ok = inside && s >= 0 && (int64_t)s < p.num_slots;
-            if (inside && !ok && c == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
-            const int64_t off = ok ? (((int64_t)s * p.hkv + T.g) * D + c * 8) : 0;
-            rx::cp_async_16(kd + sw128(r, c, L::KBLK), p.k_pool + off, ok ? 16 : 0);
-            rx::cp_async_16(vd + sw128(r, c, L::KBLK), p.v_pool + off, ok ? 16 : 0);
+        // one pass per matrix: K (w = 0) into its stage, then V (w = 1)
+        bool stop = false;
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            if (j >= kStages) {
+                const bool ok = wait_or_abort(bar + 8 * ((w ? L::B_VEMPTY : L::B_KEMPTY) + st),
+                                              ((j / kStages) - 1) & 1, abort_flag, p.status);
+                if (rx::named_bar_or(1, kProducers, !ok)) {  // every producer leaves together
+                    stop = true;
+                    break;
+                }
+            }
+            const uint32_t dst = sbase + (w ? L::OFF_V : L::OFF_K) + st * L::NB * L::KBLK;
+            const bf16 *pool = w ? p.v_pool : p.k_pool;
+            for (int idx = pt; idx < kBN * CPR; idx += kProducers) {
+                const int r = idx / CPR, c = idx % CPR;
+                const int pos = j * kBN + r;
+                const int32_t s = sl[r];
+                const bool inside = pos < T.kv_end;
+                const bool ok = inside && s >= 0 && (int64_t)s < p.num_slots;
+                if (w == 0 && inside && !ok && c == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
+                const int64_t off = ok ? (((int64_t)s * p.hkv + T.g) * D + c * 8) : 0;
+                rx::cp_async_16(dst + sw128(r, c, L::KBLK), pool + off, ok ? 16 : 0);
+            }
+            rx::cp_async_mbar_arrive(bar + 8 * ((w ? L::B_VFULL : L::B_KFULL) + st));
         }
-        rx::cp_async_mbar_arrive(bar + 8 * (L::B_KVFULL + st));
+        if (stop) break;
         rx::named_bar_sync(1, kProducers);          // slot entry j % kNSL is read: refill allowed
         fetch_slots(j + kLag);
         rx::cp_async_commit();
@@ -253,28 +265,33 @@ __device__ void tma_producer(const XParams &p, const Tile &T, unsigned char *sme
     using L = XL<D>;
     const uint32_t bar = sbase + L::OFF_BAR;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
-    int issued = 0;
+    int issued[2] = {0, 0};  // tiles of K, of V
     for (int j = 0; j < T.ntiles; ++j) {
         const int st = j % kStages;
-        if (j >= kStages &&
-            !wait_or_abort(bar + 8 * (L::B_KVEMPTY + st), ((j / kStages) - 1) & 1, abort_flag, p.status))
-            break;
-        const uint32_t full = bar + 8 * (L::B_KVFULL + st);
-        rx::mbar_arrive_expect_tx(full, 2 * kBN * D * 2);
-        const uint32_t kd = sbase + L::OFF_K + st * L::NB * L::KBLK;
-        const uint32_t vd = sbase + L::OFF_V + st * L::NB * L::KBLK;
         const int row = T.stage_row0 + j * kBN;
+        bool stop = false;
 #pragma unroll
-        for (int cb = 0; cb < L::NB; ++cb) {
-            rx::tma_load_3d(kd + cb * L::KBLK, &p.tm_k, cb * 64, T.g, row, full);
-            rx::tma_load_3d(vd + cb * L::KBLK, &p.tm_v, cb * 64, T.g, row, full);
+        for (int w = 0; w < 2; ++w) {  // K into its stage once S freed it, then V
+            if (j >= kStages && !wait_or_abort(bar + 8 * ((w ? L::B_VEMPTY : L::B_KEMPTY) + st),
+                                               ((j / kStages) - 1) & 1, abort_flag, p.status)) {
+                stop = true;
+                break;
+            }
+            const uint32_t full = bar + 8 * ((w ? L::B_VFULL : L::B_KFULL) + st);
+            rx::mbar_arrive_expect_tx(full, kBN * D * 2);
+            const uint32_t dst = sbase + (w ? L::OFF_V : L::OFF_K) + st * L::NB * L::KBLK;
+#pragma unroll
+            for (int cb = 0; cb < L::NB; ++cb)
+                rx::tma_load_3d(dst + cb * L::KBLK, w ? &p.tm_v : &p.tm_k, cb * 64, T.g, row, full);
+            issued[w] = j + 1;
         }
-        issued = j + 1;
+        if (stop) break;
     }
     // no copy may still be landing when the CTA exits (normally every stage
     // was consumed already; after an abort the last ones may not have been)
-    for (int jj = issued > kStages ? issued - kStages : 0; jj < issued; ++jj)
-        drain_wait(bar + 8 * (L::B_KVFULL + jj % kStages), (jj / kStages) & 1, p.status);
+    for (int w = 0; w < 2; ++w)
+        for (int jj = issued[w] > kStages ? issued[w] - kStages : 0; jj < issued[w]; ++jj)
+            drain_wait(bar + 8 * ((w ? L::B_VFULL : L::B_KFULL) + jj % kStages), (jj / kStages) & 1, p.status);
 }
 
 // ---------------------------------------------------------------------------
@@ -290,72 +307,67 @@ __device__ void mma_issuer(const XParams &p, const Tile &T, unsigned char *smem,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
     constexpr uint32_t idesc_qk = rx::idesc_bf16(kRows, kBN, false, false);
     constexpr uint32_t idesc_pv = rx::idesc_bf16(kRows, D, false, true);
-    // S_j = Q K_j^T (for every Q tile) and O_t += P_t,j V_j are independent
-    // apart from buffer reuse, so issue whichever is ready: S_js once tile js
-    // has landed and both S buffers for it are free, O_t += P V once the
-    // softmax has written P_t; O updates of a tile stay in order, and a K/V
-    // stage is released after both tiles' O updates that read it.
-    int js = 0, jrel = 0;
-    int jp[kQT] = {0, 0};
-    uint32_t idle = 0;
-    for (;;) {
-        const int jmin = (T.nqt == 2) ? min(jp[0], jp[1]) : jp[0];
-        if (jmin >= T.ntiles) break;
-        bool did = false;
+    auto wait = [&](int b, uint32_t parity) { return wait_or_abort(bar + 8 * b, parity, abort_flag, p.status); };
+    // shared-memory descriptors built once: every operand block is the
+    // region base plus a byte offset, i.e. the descriptor plus offset / 16
+    const uint64_t dq = rx::sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
+    const uint64_t dk = rx::sdesc_sw128(sbase + L::OFF_K, 16, 1024);
+    const uint64_t dv = rx::sdesc_sw128(sbase + L::OFF_V, L::KBLK, 1024);
+    const uint64_t dp = rx::sdesc_sw128(sbase + L::OFF_P, 16, 1024);
+
+    // S_j = Q K_j^T for every Q tile into S buffer j & 1; then K stage j is free
+    auto issue_s = [&](int j) -> bool {
+        const int st = j % kStages, sb = j & 1;
+        if (!wait(L::B_KFULL + st, (j / kStages) & 1)) return false;
+        for (int t = 0; t < T.nqt; ++t)
+            if (j == 0 && !wait(L::B_QFULL + t, 0)) return false;
+        // buffer sb was last read by the softmax of tile j - 2 (both Q tiles
+        // arrive on one barrier)
+        if (j >= 2 && !wait(L::B_SFREE + sb, ((j >> 1) - 1) & 1)) return false;
+        if (!kStaged) rx::fence_proxy_async_smem();  // K rows landed by cp.async -> async proxy
+        rx::tc_fence_after();
+        const uint64_t dks = dk + (uint64_t)((st * L::NB * L::KBLK) >> 4);
         for (int t = 0; t < T.nqt; ++t) {
-            const int j = jp[t];
-            if (j >= js) continue;
-            const int pb = j & 1;
-            if (!rx::mbar_test_wait(bar + 8 * (L::B_PFULL + 2 * t + pb), (j >> 1) & 1)) continue;
-            rx::tc_fence_after();
-            const uint32_t vbase = sbase + L::OFF_V + (j % kStages) * L::NB * L::KBLK;
-            const uint32_t pbase = sbase + L::OFF_P + (2 * t + pb) * L::QBLK;
+            const uint64_t dqt = dq + (uint64_t)((t * L::NB * L::QBLK) >> 4);
 #pragma unroll
-            for (int ks = 0; ks < kBN / 16; ++ks) {
-                rx::tc_mma(tmem + t * 256 + 128, rx::sdesc_sw128(pbase + ks * 32, 16, 1024),
-                           rx::sdesc_sw128(vbase + ks * 16 * 128, L::KBLK, 1024), idesc_pv,
-                           (j > 0 || ks > 0) ? 1u : 0u);
+            for (int kb = 0; kb < D / 16; ++kb) {
+                rx::tc_mma(tmem + t * 256 + sb * kBN, dqt + (uint64_t)(((kb >> 2) * L::QBLK + (kb & 3) * 32) >> 4),
+                           dks + (uint64_t)(((kb >> 2) * L::KBLK + (kb & 3) * 32) >> 4), idesc_qk, kb > 0);
             }
-            rx::tc_commit(bar + 8 * (L::B_PVDONE + 2 * t + pb));
-            jp[t] = j + 1;
-            did = true;
+            rx::tc_commit(bar + 8 * (L::B_SFULL + 2 * t + sb));
         }
-        const int jdone = (T.nqt == 2) ? min(jp[0], jp[1]) : jp[0];
-        for (; jrel < jdone; ++jrel) rx::tc_commit(bar + 8 * (L::B_KVEMPTY + jrel % kStages));
-        if (js < T.ntiles) {
-            const int st = js % kStages, sb = js & 1;
-            bool ready = rx::mbar_test_wait(bar + 8 * (L::B_KVFULL + st), (js / kStages) & 1);
-            for (int t = 0; t < T.nqt && ready; ++t)
-                ready = js == 0   ? rx::mbar_test_wait(bar + 8 * (L::B_QFULL + t), 0)
-                        : js < 2 ? true
-                                 : rx::mbar_test_wait(bar + 8 * (L::B_SFREE + 2 * t + sb), ((js >> 1) - 1) & 1);
-            if (ready) {
-                if (!kStaged) rx::fence_proxy_async_smem();  // K/V rows landed by cp.async -> async proxy
-                rx::tc_fence_after();
-                const uint32_t kbase = sbase + L::OFF_K + st * L::NB * L::KBLK;
-                for (int t = 0; t < T.nqt; ++t) {
-                    const uint32_t qbase = sbase + L::OFF_Q + t * L::NB * L::QBLK;
+        rx::tc_commit(bar + 8 * (L::B_KEMPTY + st));
+        return true;
+    };
+    // O_t += P_t,j V_j once the softmax of every Q tile has written P_t,j
+    // (one barrier for both tiles) and V_j has landed
+    auto issue_pv = [&](int j, int t) -> bool {
+        const int pb = j & 1;
+        if (t == 0) {
+            if (!wait(L::B_PFULL + pb, (j >> 1) & 1)) return false;
+            if (!wait(L::B_VFULL + j % kStages, (j / kStages) & 1)) return false;
+            if (!kStaged) rx::fence_proxy_async_smem();  // V rows landed by cp.async
+        }
+        rx::tc_fence_after();
+        const uint64_t dvs = dv + (uint64_t)(((j % kStages) * L::NB * L::KBLK) >> 4);
+        const uint64_t dps = dp + (uint64_t)(((2 * t + pb) * L::QBLK) >> 4);
 #pragma unroll
-                    for (int kb = 0; kb < D / 16; ++kb) {
-                        const uint32_t kofs = (kb >> 2) * L::QBLK + (kb & 3) * 32;
-                        const uint32_t bofs = (kb >> 2) * L::KBLK + (kb & 3) * 32;
-                        rx::tc_mma(tmem + t * 256 + sb * kBN, rx::sdesc_sw128(qbase + kofs, 16, 1024),
-                                   rx::sdesc_sw128(kbase + bofs, 16, 1024), idesc_qk, kb > 0);
-                    }
-                    rx::tc_commit(bar + 8 * (L::B_SFULL + 2 * t + sb));
-                }
-                ++js;
-                did = true;
-            }
-        }
-        if (did) {
-            idle = 0;
-        } else if (++idle > kIdleLimit || *abort_flag) {
-            if (!*abort_flag) {
-                *abort_flag = 1;
-                if (p.status) atomicOr(p.status, RX_DEV_TIMEOUT);
-            }
-            break;
+        for (int ks = 0; ks < kBN / 16; ++ks)
+            rx::tc_mma(tmem + t * 256 + 128, dps + (uint64_t)((ks * 32) >> 4), dvs + (uint64_t)((ks * 16 * 128) >> 4),
+                       idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+        rx::tc_commit(bar + 8 * (L::B_PVDONE + 2 * t + pb));
+        return true;
+    };
+    // a fixed order, each wait suspending the thread until its barrier
+    // flips: S_{j+1} goes ahead of O += P_j V_j so that the softmax of tile
+    // j + 1 can start while the tensor core finishes tile j
+    if (issue_s(0)) {
+        for (int j = 0; j < T.ntiles; ++j) {
+            if (j + 1 < T.ntiles && !issue_s(j + 1)) break;
+            bool ok = true;
+            for (int t = 0; t < T.nqt && ok; ++t) ok = issue_pv(j, t);
+            if (!ok) break;
+            rx::tc_commit(bar + 8 * (L::B_VEMPTY + j % kStages));
         }
     }
     // everything issued has finished before TMEM is released
@@ -414,11 +426,20 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
         rx::tmem_ld32(tbase + sb * kBN, *reinterpret_cast<uint32_t(*)[32]>(sv));
         rx::tmem_ld32(tbase + sb * kBN + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
         rx::tmem_wait_ld();
-        float mx = -INFINITY;
+        if (need_mask) {  // keys past the causal bound: -inf, so their weight is exactly 0
 #pragma unroll
-        for (int k = 0; k < kBN; ++k)
-            if (!need_mask || kbase + k <= row_lim) mx = fmaxf(mx, u2f(sv[k]));
-        const float m_new = fmaxf(m_used, mx * sl2);
+            for (int k = 0; k < kBN; ++k)
+                if (kbase + k > row_lim) sv[k] = __float_as_uint(-INFINITY);
+        }
+        // row max as a tree (max is exact, so the order does not matter)
+        float mt[kBN / 2];
+#pragma unroll
+        for (int k = 0; k < kBN / 2; ++k) mt[k] = fmaxf(u2f(sv[k]), u2f(sv[k + kBN / 2]));
+#pragma unroll
+        for (int w = kBN / 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) mt[k] = fmaxf(mt[k], mt[k + w]);
+        const float m_new = fmaxf(m_used, mt[0] * sl2);
         const bool need = (m_used == -INFINITY) || (m_new > m_used + kRescale);
         const float alpha = (need && m_used != -INFINITY) ? rx::fast_exp2(m_used - m_new) : 1.f;
         if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -446,29 +467,35 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
         if (j >= 2 && !warp_wait(bar + 8 * (L::B_PVDONE + 2 * t + sb), ((j >> 1) - 1) & 1, abort_flag,
                                  p.status))
             return;
+        // P = 2^(s sl2 - m): the scaling as packed pairs, 2^x on the MUFU, the
+        // row sum in four independent packed accumulators
         const float mu = (m_used == -INFINITY) ? 0.f : m_used;
+        const uint64_t scale2 = rx::f2(sl2, sl2), negm2 = rx::f2(-mu, -mu);
+        uint64_t acc[4] = {0, 0, 0, 0};
         unsigned char *prow = smem + L::OFF_P + (2 * t + sb) * L::QBLK;
 #pragma unroll
         for (int q = 0; q < kBN / 8; ++q) {  // 8 keys -> one 16-byte chunk of the P row
-            float e[8];
+            uint32_t pk[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int key = q * 8 + k;
-                const bool vis = !need_mask || kbase + key <= row_lim;
-                e[k] = vis ? rx::fast_exp2(fmaf(u2f(sv[key]), sl2, -mu)) : 0.f;
-                l += e[k];
+            for (int k = 0; k < 4; ++k) {
+                const int key = q * 8 + 2 * k;
+                float x0, x1;
+                rx::f2_split(rx::f2_fma(rx::f2(u2f(sv[key]), u2f(sv[key + 1])), scale2, negm2), x0, x1);
+                const float e0 = rx::fast_exp2(x0), e1 = rx::fast_exp2(x1);
+                acc[k] = rx::f2_add(acc[k], rx::f2(e0, e1));
+                pk[k] = rx::pack_bf16(e0, e1);
             }
-            uint4 v;
-            v.x = rx::pack_bf16(e[0], e[1]);
-            v.y = rx::pack_bf16(e[2], e[3]);
-            v.z = rx::pack_bf16(e[4], e[5]);
-            v.w = rx::pack_bf16(e[6], e[7]);
-            *reinterpret_cast<uint4 *>(prow + sw128(rl, q, L::QBLK)) = v;
+            *reinterpret_cast<uint4 *>(prow + sw128(rl, q, L::QBLK)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        {
+            float a0, a1;
+            rx::f2_split(rx::f2_add(rx::f2_add(acc[0], acc[1]), rx::f2_add(acc[2], acc[3])), a0, a1);
+            l += a0 + a1;
         }
         rx::tc_fence_before();
         rx::fence_proxy_async_smem();
-        rx::mbar_arrive(bar + 8 * (L::B_SFREE + 2 * t + sb));
-        rx::mbar_arrive(bar + 8 * (L::B_PFULL + 2 * t + sb));
+        rx::mbar_arrive(bar + 8 * (L::B_SFREE + sb));
+        rx::mbar_arrive(bar + 8 * (L::B_PFULL + sb));
     }
     const int jl = T.ntiles - 1;
     if (!warp_wait(bar + 8 * (L::B_PVDONE + 2 * t + (jl & 1)), (jl >> 1) & 1, abort_flag, p.status)) return;
@@ -548,13 +575,15 @@ __global__ void __launch_bounds__(kStaged ? kStagedThreads : kThreads, 1)
         for (int i = 0; i < kStages; ++i) {
             // gather path: every producer thread's copies; staged: the TMA thread's
             // arrival plus the boxes' bytes
-            rx::mbar_init(bar + 8 * (L::B_KVFULL + i), kStaged ? 1 : kProducers);
-            rx::mbar_init(bar + 8 * (L::B_KVEMPTY + i), 1);  // MMA commit
+            rx::mbar_init(bar + 8 * (L::B_KFULL + i), kStaged ? 1 : kProducers);
+            rx::mbar_init(bar + 8 * (L::B_VFULL + i), kStaged ? 1 : kProducers);
+            rx::mbar_init(bar + 8 * (L::B_KEMPTY + i), 1);  // MMA commits
+            rx::mbar_init(bar + 8 * (L::B_VEMPTY + i), 1);
         }
         for (int i = 0; i < 2 * kQT; ++i) {
             rx::mbar_init(bar + 8 * (L::B_SFULL + i), 1);     // MMA commit
-            rx::mbar_init(bar + 8 * (L::B_SFREE + i), 128);   // softmax threads of the tile
-            rx::mbar_init(bar + 8 * (L::B_PFULL + i), 128);
+            rx::mbar_init(bar + 8 * (L::B_SFREE + i), 128 * T.nqt);  // softmax threads of every Q tile (i < 2)
+            rx::mbar_init(bar + 8 * (L::B_PFULL + i), 128 * T.nqt);  // i < 2 used, as s_free
             rx::mbar_init(bar + 8 * (L::B_PVDONE + i), 1);    // MMA commit
         }
         rx::mbar_init(bar + 8 * L::B_FINAL, 1);
