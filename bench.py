@@ -265,15 +265,13 @@ def run_gpu(args, rank, world, local_rank):
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in steps_ev]
     part_ms = {k: [m[k][0].elapsed_time(m[k][1]) for m in marks] for k in parts}
-    tot_ms = float(sum(step_ms))
-    if dist:
-        t = torch.tensor([tot_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = max_over_ranks(sum(step_ms), dist, "cuda")
     ms_per_step = tot_ms / args.steps
 
     # end to end through the public API: pinned host inputs in, result out
-    e2e = run_e2e(st, torch, rx, args.steps, flush)
+    if dist:
+        dist.barrier()
+    e2e = run_e2e(st, torch, rx, args.steps, flush, dist, world)
 
     if dist:
         dist.destroy_process_group()
@@ -285,15 +283,15 @@ def run_gpu(args, rank, world, local_rank):
     kv_row = prob.kv_row_bytes
     out = {}
     if st.has_dec:
-        toks = B_dec * world * args.steps
-        value = toks / (tot_ms / 1e3)
+        value = job_throughput(B_dec, world, args.steps, tot_ms)
         metric, unit = "decode tok/s", "tok/s"
         dec_ms = statistics.mean(part_ms["decode"])
         uniq_bytes = st.plan_info.tokens_read * kv_row
         achieved = uniq_bytes / (dec_ms / 1e3) / 1e9
+        traffic, tsrc = profiled_traffic(args.workload, "decode")
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": None,
-                "kernel": "rx_attn_decode (attn_rows_kernel + merge_kernel)",
+                "frac": round(achieved / hbm, 4), "traffic": traffic, "traffic_source": tsrc,
+                "kernel": "rx_attn_decode (decode_kernel + merge_kernel)",
                 "algorithmic_bytes_per_launch": int(uniq_bytes), "launch_ms": round(dec_ms, 5),
                 "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)",
                 "frac_of_8000": round(achieved / 8000.0, 4)}
@@ -309,9 +307,12 @@ def run_gpu(args, rank, world, local_rank):
                          "flops": int(flops_ext), "frac_of_burst": tf / tflops}
         if not st.has_dec:
             metric, unit = "extend TFLOPS", "TFLOP/s"
-            value = flops_ext * world * args.steps / (tot_ms / 1e3) / 1e12
+            value = job_throughput(flops_ext, world, args.steps, tot_ms) / 1e12
+            traffic, tsrc = profiled_traffic(args.workload, args.extend_path)
             roof = {"bound": "tensor", "achieved": round(tf, 2), "peak": tflops, "unit": "TFLOP/s",
-                    "frac": round(tf / tflops, 4), "traffic": None, "kernel": "rx_attn_extend",
+                    "frac": round(tf / tflops, 4), "traffic": traffic, "traffic_source": tsrc,
+                    "kernel": "rx_attn_extend (" + ("offsets + staging copy + extend_kernel"
+                                                    if args.extend_path == "staged" else "extend_kernel") + ")",
                     "algorithmic_flops_per_launch": int(flops_ext), "launch_ms": round(ext_ms, 5),
                     "peak_source": f"{peak_src} bf16_tflops (burst)"}
     out["kv_store"] = {"ms": statistics.mean(part_ms["store"]),
@@ -330,7 +331,24 @@ def run_gpu(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(st, torch, rx, steps, flush):
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest of every rank's value: the slowest replica sets the job's
+    time.  A collective, so every rank calls it; `dist` None means one rank."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step: float, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job units per second: every rank's units over the slowest rank's
+    time (weak scaling: each rank carries the full per-GPU workload)."""
+    return units_per_rank_step * world * steps / (max_ms / 1e3)
+
+
+def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
     """Per step: pinned host -> device copies of the step's inputs, the path,
     device -> host copy of its outputs; timed with events on the stream."""
     p = st.prob
@@ -360,15 +378,29 @@ def run_e2e(st, torch, rx, steps, flush):
             h.copy_(d, non_blocking=True)
         ev[i][1].record()
     torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in ev) / n
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / n, dist, "cuda")
     h2d = sum(h.numel() * h.element_size() for h in h_in)
     d2h = sum(h.numel() * h.element_size() for h in h_out)
     if st.has_dec:
-        val, unit = len(p.dec_req_idx) / (ms / 1e3), "tok/s"
+        val, unit = job_throughput(len(p.dec_req_idx), world, 1, ms), "tok/s"
     else:
-        val, unit = p.extend_flops() / (ms / 1e3) / 1e12, "TFLOP/s"
+        val, unit = job_throughput(p.extend_flops(), world, 1, ms) / 1e12, "TFLOP/s"
     return {"value": round(val, 3), "unit": unit, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 5), "steps": n}
+
+
+# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
+# captures summarised in the named profile; an entry is removed whenever its
+# kernel changes, so that an old count is never reported for new code.
+PROFILED_TRAFFIC = {
+    ("few_shot_decode", "decode"): (293_437_440, "profiles/decode_kernel.few_shot_decode.md"),
+    ("cached_prefix_extend", "staged"): (584_500_736, "profiles/extend_kernel.cached_prefix_extend.md"),
+}
+
+
+def profiled_traffic(workload, part):
+    hit = PROFILED_TRAFFIC.get((workload, part))
+    return (hit[0], hit[1]) if hit else (None, None)
 
 
 def make_problem(args):

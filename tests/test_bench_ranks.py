@@ -1,0 +1,59 @@
+"""Multi-rank aggregation of bench.py, on CPU with the gloo backend.
+
+Every rank is a full replica of the per-GPU workload (the path has no
+exchange step); the job's time is the slowest rank's and its throughput is
+every rank's units over that time.  These run two real gloo ranks.
+"""
+import os
+import socket
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        # rank r took 10 + 5 r ms for its steps: the job took the slowest
+        ms = bench.max_over_ranks(10.0 + 5.0 * rank, dist, "cpu")
+        value = bench.job_throughput(64, world, 20, ms)
+        q.put((rank, ms, value))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_throughput_two_gloo_ranks():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert all(p.exitcode == 0 for p in procs)
+    got = sorted(q.get(timeout=5) for _ in range(world))
+    for rank, ms, value in got:
+        assert ms == 15.0                                  # the slower rank's time, on every rank
+        assert value == pytest.approx(64 * 2 * 20 / 0.015)  # both ranks' units over it
+
+
+def test_single_rank_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5) == 3.5
+    assert bench.job_throughput(10, 1, 4, 2.0) == pytest.approx(10 * 4 / 0.002)
