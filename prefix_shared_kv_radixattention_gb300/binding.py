@@ -50,14 +50,14 @@ class KVPool(ctypes.Structure):
 
 class DecodePlan(ctypes.Structure):
     _fields_ = [("order", ctypes.c_void_p), ("nparts", ctypes.c_void_p), ("items", ctypes.c_void_p),
-                ("n_items", ctypes.c_int32), ("max_parts", ctypes.c_int32)]
+                ("n_items", ctypes.c_int32), ("max_parts", ctypes.c_int32), ("n_wide", ctypes.c_int32)]
 
 
 class DecodePlanInfo(ctypes.Structure):
     _fields_ = [("n_items", ctypes.c_int32), ("max_parts", ctypes.c_int32),
                 ("n_segments", ctypes.c_int32), ("kv_chunk", ctypes.c_int32),
                 ("shared_tokens", ctypes.c_int64), ("tokens_read", ctypes.c_int64),
-                ("buf_words", ctypes.c_int64)]
+                ("buf_words", ctypes.c_int64), ("n_wide", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -381,7 +381,7 @@ def plan_to_device(buf: np.ndarray, info: DecodePlanInfo, batch: int, device="cu
     torch = _torch()
     d = torch.from_numpy(np.ascontiguousarray(buf)).to(device)
     base = d.data_ptr()
-    st = DecodePlan(base, base + 4 * batch, base + 8 * batch, info.n_items, info.max_parts)
+    st = DecodePlan(base, base + 4 * batch, base + 8 * batch, info.n_items, info.max_parts, info.n_wide)
     return DevicePlan(d, info, batch, st)
 
 

@@ -121,6 +121,7 @@ struct Params {
     float *ws_lse;
     float scale_log2;
     int32_t *status;
+    int wide0, n_wide;      // plan: single-request items for the wide kernel
 };
 
 struct Item {
@@ -692,6 +693,328 @@ int num_sms()
     return sms;
 }
 
+// ---------------------------------------------------------------------------
+// wide items: one request, every kv head at once
+// ---------------------------------------------------------------------------
+//
+// A plan item that holds a single request covers positions nobody else reads
+// (a private tail), with one query row per q head.  Its K (and V) rows for all
+// kv heads of a slot are contiguous in the pool (num_kv_heads * head_dim * 2
+// bytes: 8 KiB for 32 x 128), and on GB300 a random gather of whole slot rows
+// streams at HBM speed where a gather of 256-byte rows per kv head does not
+// (measured: 8 KiB rows 6.8 TB/s, 2 KiB rows 4.4 TB/s, 256-byte rows 2.9
+// TB/s).  So these items go to this kernel:
+//   - one producer warp moves whole slot rows, one bulk copy (TMA engine) per
+//     row, into a ring of stages whose full barrier counts the bytes;
+//   - eight consumer warps each own hq / 8 q heads, with q (pre-scaled into
+//     the exp2 domain) and the running o in registers, D / 32 values per
+//     lane; one query row per head makes the work a matrix-vector product,
+//     about one flop per byte, so it runs on the CUDA cores: per head and
+//     position a lane-split dot product, a warp all-reduce and an online
+//     softmax step.
+
+constexpr int kWideConsumers = 8;
+constexpr int kWideThreads = 32 * (1 + kWideConsumers);
+constexpr int kWideStages = 3;
+constexpr int kWideStageBytes = 32768;  // K bytes per stage (as many again for V)
+constexpr int kWideMaxPos = 32;         // positions per stage at most (one producer lane each)
+
+struct WideLayout {
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = kWideStages * kWideStageBytes;
+    static constexpr int OFF_OK = 2 * kWideStages * kWideStageBytes;  // int [stage][pos]: row valid
+    static constexpr int OFF_BAR = OFF_OK + kWideStages * kWideMaxPos * 4;
+    static constexpr int OFF_ABORT = OFF_BAR + 2 * kWideStages * 8;
+    static constexpr int BYTES = OFF_ABORT + 16 + 128;  // + room to align the base to 128
+};
+static_assert(WideLayout::OFF_BAR % 8 == 0, "mbarrier alignment");
+
+
+// bounded single-thread wait that ignores the abort flag: lets copies already
+// issued land before the CTA exits
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int32_t *status)
+{
+    for (uint32_t i = 0; i < kSpinLimit; ++i)
+        if (rx::mbar_try_wait(bar, parity)) return;
+    if (status) atomicOr(status, RX_DEV_TIMEOUT);
+}
+
+// E consecutive bf16 of shared memory as floats (E = 2 or 4: one 4- or
+// 8-byte load)
+template <int E>
+__device__ __forceinline__ void load_bf16(const unsigned char *src, float (&out)[E])
+{
+    if constexpr (E == 4) {
+        const uint2 r = *reinterpret_cast<const uint2 *>(src);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+        out[0] = a.x;
+        out[1] = a.y;
+        out[2] = b.x;
+        out[3] = b.y;
+    } else {
+        const uint32_t r = *reinterpret_cast<const uint32_t *>(src);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r));
+        out[0] = a.x;
+        out[1] = a.y;
+    }
+}
+
+template <int D, int LOG_NP, int HPW>
+__global__ void __launch_bounds__(kWideThreads, 1) decode_wide_kernel(const Params p)
+{
+    using WL = WideLayout;
+    constexpr int E = D / 32;  // values of a head row per lane
+    constexpr int NP = 1 << LOG_NP;  // positions per stage
+    extern __shared__ __align__(128) unsigned char wraw[];
+    const uint32_t raw = rx::smem_u32(wraw);
+    unsigned char *smem = wraw + (((raw + 127u) & ~127u) - raw);
+    const uint32_t sbase = rx::smem_u32(smem);
+    const uint32_t bar = sbase + WL::OFF_BAR;  // full: [0, S), empty: [S, 2S)
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + WL::OFF_ABORT);
+    int *okf = reinterpret_cast<int *>(smem + WL::OFF_OK);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int RB = p.hkv * D * 2;          // bytes of one slot row
+    const int64_t row_elems = (int64_t)p.hkv * D;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kWideStages; ++i) {
+            rx::mbar_init(bar + 8 * i, 1);                                  // producer + bytes
+            rx::mbar_init(bar + 8 * (kWideStages + i), kWideConsumers);     // consumer warps
+        }
+        *abort_flag = 0;
+        rx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // producer: stage j of the CTA's item sequence holds positions
+        // q0 .. q0 + NP - 1 of one item, one lane per position.  The slot ids
+        // of the next stage are loaded before waiting for a free stage, so
+        // their latency is not on the copy path.
+        struct Cursor {
+            int it, q0, p1;
+            const int32_t *slots;
+        };
+        auto open_item = [&](Cursor &c) {
+            if (c.it < p.n_wide) {
+                const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + c.it);
+                c.q0 = __ldg(v + 2);
+                c.p1 = __ldg(v + 3);
+                c.slots = p.rtt + (int64_t)__ldg(v + 6) * p.rtt_stride;
+            }
+        };
+        auto next_stage = [&](Cursor &c) {
+            c.q0 += NP;
+            if (c.q0 >= c.p1) {
+                c.it += gridDim.x;
+                open_item(c);
+            }
+        };
+        auto slot_of = [&](const Cursor &c) -> int32_t {
+            const int pos = c.q0 + lane;
+            return (c.it < p.n_wide && lane < NP && pos < c.p1) ? __ldg(c.slots + pos) : -1;
+        };
+        Cursor cur{(int)blockIdx.x, 0, 0, nullptr};
+        open_item(cur);
+        int32_t sl_cur = slot_of(cur);
+        int j = 0;
+        for (; cur.it < p.n_wide; ++j) {
+            Cursor nxt = cur;
+            next_stage(nxt);
+            const int32_t sl_nxt = slot_of(nxt);
+            const int st = j % kWideStages;
+            if (j >= kWideStages &&
+                !wait_or_abort(bar + 8 * (kWideStages + st), ((j / kWideStages) - 1) & 1, abort_flag, p.status))
+                break;
+            const bool inside = lane < NP && cur.q0 + lane < cur.p1;
+            const bool ok = inside && sl_cur >= 0 && (int64_t)sl_cur < p.num_slots;
+            if (inside && !ok && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
+            if (lane < NP) okf[st * kWideMaxPos + lane] = ok ? 1 : 0;
+            const int nok = __popc(__ballot_sync(0xffffffffu, ok));
+            __syncwarp();  // the flags are written before lane 0's arrive releases them
+            if (lane == 0) rx::mbar_arrive_expect_tx(bar + 8 * st, (uint32_t)(2 * nok * RB));
+            __syncwarp();
+            if (ok) {
+                const uint32_t off = (uint32_t)(st * kWideStageBytes + lane * RB);
+                rx::bulk_g2s(sbase + WL::OFF_K + off, p.k_pool + (int64_t)sl_cur * row_elems, (uint32_t)RB,
+                             bar + 8 * st);
+                rx::bulk_g2s(sbase + WL::OFF_V + off, p.v_pool + (int64_t)sl_cur * row_elems, (uint32_t)RB,
+                             bar + 8 * st);
+            }
+            cur = nxt;
+            sl_cur = sl_nxt;
+        }
+        // no copy may still be landing when the CTA exits
+        if (lane == 0)
+            for (int jj = j > kWideStages ? j - kWideStages : 0; jj < j; ++jj)
+                drain_wait(bar + 8 * (jj % kWideStages), (jj / kWideStages) & 1, p.status);
+        __syncwarp();
+    } else {
+        // consumers: warp cw owns q heads (= kv heads, G == 1) h0 .. h0 + HPW - 1
+        constexpr int HN = HPW * NP;                        // (head, position) pairs of a stage
+        constexpr int LOG_HN = LOG_NP + (HPW == 1 ? 0 : HPW == 2 ? 1 : HPW == 4 ? 2 : 3);
+        static_assert(HN <= 32 && (1 << LOG_HN) == HN, "one value per lane after the reduce-scatter");
+        const int cw = warp - 1;
+        const int h0 = cw * HPW;
+        // after the reduce-scatter, lane l holds pair x = l >> (5 - LOG_HN):
+        // head hx = x / NP, position ix = x % NP
+        const int x = lane >> (5 - LOG_HN);
+        const int hx = x >> LOG_NP, ix = x & (NP - 1);
+        int j = 0;
+        for (int it = blockIdx.x; it < p.n_wide; it += gridDim.x) {
+            const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + it);
+            const int p0 = __ldg(v + 2), p1 = __ldg(v + 3), part_idx = __ldg(v + 4);
+            const bool fin = __ldg(v + 5) != 0;
+            const int b = __ldg(v + 7);
+            float q[HPW][E], o[HPW][E], m[HPW], l[HPW];
+#pragma unroll
+            for (int hh = 0; hh < HPW; ++hh) {
+                const bf16 *qp = p.q + ((int64_t)b * p.hq + h0 + hh) * D + lane * E;
+                m[hh] = -INFINITY;
+                l[hh] = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    q[hh][e] = __bfloat162float(qp[e]) * p.scale_log2;
+                    o[hh][e] = 0.f;
+                }
+            }
+            for (int q0 = p0; q0 < p1; q0 += NP, ++j) {
+                const int st = j % kWideStages;
+                if (!wait_or_abort(bar + 8 * st, (j / kWideStages) & 1, abort_flag, p.status)) return;
+                const int n = min(NP, p1 - q0);
+                const unsigned char *ks = smem + WL::OFF_K + st * kWideStageBytes + h0 * D * 2 + lane * E * 2;
+                const unsigned char *vs = smem + WL::OFF_V + st * kWideStageBytes + h0 * D * 2 + lane * E * 2;
+                const int *okp = okf + st * kWideMaxPos;
+                // partial dot products over this lane's E dims, pair (hh, i) at hh * NP + i
+                float part[HN];
+#pragma unroll
+                for (int hh = 0; hh < HPW; ++hh)
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) {
+                        float kf[E];
+                        load_bf16<E>(ks + i * RB + hh * D * 2, kf);
+                        float acc = 0.f;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) acc = fmaf(q[hh][e], kf[e], acc);
+                        part[hh * NP + i] = acc;
+                    }
+                // reduce-scatter: halve the value list at each lane offset
+#pragma unroll
+                for (int s2 = 0, half = HN / 2; half >= 1; ++s2, half >>= 1) {
+                    const int off = 16 >> s2;
+                    const bool up = (lane & off) != 0;
+#pragma unroll
+                    for (int i = 0; i < half; ++i) {
+                        const float send = up ? part[i] : part[i + half];
+                        const float keep = up ? part[i + half] : part[i];
+                        part[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    }
+                }
+                float sc = part[0];
+#pragma unroll
+                for (int off = 16 >> LOG_HN; off >= 1; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
+                // a position past the item is out; a row with an invalid slot reads as zeros
+                const bool in = ix < n;
+                const bool okx = in && okp[ix] != 0;
+                sc = in ? (okx ? sc : 0.f) : -INFINITY;
+                // per head: max and sum over its NP positions (lane bits of ix)
+                float smax = sc;
+#pragma unroll
+                for (int bb = 0; bb < LOG_NP; ++bb)
+                    smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1 << (5 - LOG_HN + bb)));
+                float mh = m[0];
+#pragma unroll
+                for (int hh = 1; hh < HPW; ++hh) mh = hx == hh ? m[hh] : mh;
+                const float mn = fmaxf(mh, smax);
+                const float pw = rx::fast_exp2(sc - mn);  // 0 past the item
+                float ps = pw;
+#pragma unroll
+                for (int bb = 0; bb < LOG_NP; ++bb) ps += __shfl_xor_sync(0xffffffffu, ps, 1 << (5 - LOG_HN + bb));
+                const float al = rx::fast_exp2(mh - mn);  // 0 on the item's first stage
+                const float pv = okx ? pw : 0.f;          // weight of this lane's pair for V
+#pragma unroll
+                for (int hh = 0; hh < HPW; ++hh) {
+                    const int src = (hh << LOG_NP) << (5 - LOG_HN);
+                    const float a = __shfl_sync(0xffffffffu, al, src);
+                    m[hh] = __shfl_sync(0xffffffffu, mn, src);
+                    l[hh] = fmaf(l[hh], a, __shfl_sync(0xffffffffu, ps, src));
+#pragma unroll
+                    for (int e = 0; e < E; ++e) o[hh][e] *= a;
+                }
+#pragma unroll
+                for (int hh = 0; hh < HPW; ++hh)
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) {
+                        const float pi = __shfl_sync(0xffffffffu, pv, ((hh << LOG_NP) + i) << (5 - LOG_HN));
+                        // rows past the item or with an invalid slot were never
+                        // written in this stage: skip them (0 * stale NaN is NaN)
+                        if (i >= n || okp[i] == 0) continue;
+                        float vf[E];
+                        load_bf16<E>(vs + i * RB + hh * D * 2, vf);
+#pragma unroll
+                        for (int e = 0; e < E; ++e) o[hh][e] = fmaf(pi, vf[e], o[hh][e]);
+                    }
+                __syncwarp();
+                if (lane == 0) rx::mbar_arrive(bar + 8 * (kWideStages + st));
+            }
+            // results of the item for this warp's heads
+#pragma unroll
+            for (int hh = 0; hh < HPW; ++hh) {
+                const int64_t orow = (int64_t)b * p.hq + h0 + hh;
+                const float inv = 1.f / l[hh];
+                if (fin) {
+                    bf16 *dst = p.o + orow * D + lane * E;
+#pragma unroll
+                    for (int e = 0; e < E; e += 2)
+                        *reinterpret_cast<uint32_t *>(dst + e) = rx::pack_bf16(o[hh][e] * inv, o[hh][e + 1] * inv);
+                    if (p.lse && lane == 0) p.lse[orow] = (m[hh] + log2f(l[hh])) * rx::kLn2;
+                } else {
+                    const int64_t prow = orow * p.max_parts + part_idx;
+                    float *dst = p.ws_o + prow * D + lane * E;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) dst[e] = o[hh][e] * inv;
+                    if (lane == 0) p.ws_lse[prow] = m[hh] + log2f(l[hh]);
+                }
+            }
+        }
+    }
+}
+
+template <int D, int LOG_NP, int HPW>
+int launch_decode_wide_cfg(const Params &p, cudaStream_t st)
+{
+    static bool configured = false;
+    if (!configured) {
+        RX_CUDA_CHECK(cudaFuncSetAttribute(decode_wide_kernel<D, LOG_NP, HPW>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, WideLayout::BYTES));
+        configured = true;
+    }
+    const int grid = p.n_wide < num_sms() ? p.n_wide : num_sms();
+    decode_wide_kernel<D, LOG_NP, HPW><<<grid, kWideThreads, WideLayout::BYTES, st>>>(p);
+    RX_CUDA_CHECK(cudaGetLastError());
+    return RX_OK;
+}
+
+// Wide items need one q head per kv head and 8, 16, 32 or 64 heads: each of
+// the eight consumer warps then owns hq / 8 heads, and a stage holds
+// 2048 / D (head, position) pairs per warp -- one per lane or half-lane.
+bool wide_supported(int hq, int hkv, int D)
+{
+    return hq == hkv && (hq == 8 || hq == 16 || hq == 32 || hq == 64) && (D == 64 || D == 128);
+}
+
+template <int D>
+int launch_decode_wide(const Params &p, cudaStream_t st)
+{
+    constexpr int L0 = D == 128 ? 4 : 5;  // log2 positions per stage at 8 heads
+    switch (p.hq) {
+    case 8: return launch_decode_wide_cfg<D, L0, 1>(p, st);
+    case 16: return launch_decode_wide_cfg<D, L0 - 1, 2>(p, st);
+    case 32: return launch_decode_wide_cfg<D, L0 - 2, 4>(p, st);
+    default: return launch_decode_wide_cfg<D, L0 - 3, 8>(p, st);
+    }
+}
+
 template <int D, bool PLAN>
 int launch_decode(const Params &p, cudaStream_t st)
 {
@@ -770,7 +1093,7 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
         rx_misaligned16(pool->v) || (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
         return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: q, o and the pools must be 16-byte aligned");
     if (plan && (!plan->order || !plan->nparts || !plan->items || plan->n_items < 0 ||
-                 plan->max_parts < 1))
+                 plan->max_parts < 1 || plan->n_wide < 0 || plan->n_wide > plan->n_items))
         return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: invalid plan");
     if (batch == 0) return RX_OK;
     const int D = pool->head_dim;
@@ -797,7 +1120,12 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
         p.nparts = plan->nparts;
         p.items = plan->items;
         p.max_parts = plan->max_parts;
-        total = (int64_t)plan->n_items * p.hkv;
+        // the plan's last n_wide items hold one request each; they go to the
+        // wide kernel for the head counts it is built for (else to the
+        // per-head kernel with the rest)
+        p.n_wide = wide_supported(hq, p.hkv, D) ? plan->n_wide : 0;
+        p.wide0 = plan->n_items - p.n_wide;
+        total = (int64_t)p.wide0 * p.hkv;
     } else {
         p.chunk = rx_decode_default_chunk(batch, p.hkv, max_seq_len);
         p.n_chunks = (max_seq_len + p.chunk - 1) / p.chunk;
@@ -806,7 +1134,7 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
     }
     if (total > INT32_MAX)
         return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_decode: %lld work items", (long long)total);
-    if (total == 0) return RX_OK;
+    if (total == 0 && p.n_wide == 0) return RX_OK;
     p.total_work = (int)total;
     const size_t need = rx_attn_decode_workspace(batch, hq, p.hkv, D, max_seq_len, plan);
     if (need > 0) {
@@ -819,11 +1147,15 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
         p.ws_lse = p.ws_o + (int64_t)batch * hq * p.max_parts * D;
     }
     cudaStream_t st = (cudaStream_t)stream;
-    int rc;
-    if (D == 128)
-        rc = plan ? launch_decode<128, true>(p, st) : launch_decode<128, false>(p, st);
-    else
-        rc = plan ? launch_decode<64, true>(p, st) : launch_decode<64, false>(p, st);
+    int rc = RX_OK;
+    if (p.total_work > 0) {
+        if (D == 128)
+            rc = plan ? launch_decode<128, true>(p, st) : launch_decode<128, false>(p, st);
+        else
+            rc = plan ? launch_decode<64, true>(p, st) : launch_decode<64, false>(p, st);
+    }
+    if (rc == RX_OK && p.n_wide > 0)
+        rc = D == 128 ? launch_decode_wide<128>(p, st) : launch_decode_wide<64>(p, st);
     if (rc != RX_OK || need == 0) return rc;
     return D == 128 ? launch_merge<128>(p, plan != nullptr, st) : launch_merge<64>(p, plan != nullptr, st);
 }

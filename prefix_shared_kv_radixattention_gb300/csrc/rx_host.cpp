@@ -632,13 +632,37 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
     }
     reads = shared;
     for (int64_t r = 0; r < B; ++r) reads += seq_len[order[(size_t)r]] - priv_begin[(size_t)r];
-    if (kv_chunk == 0) {
-        // about RX_DECODE_TARGET_ITEMS work items over all kv heads
-        int64_t c = (reads * hkv + RX_DECODE_TARGET_ITEMS - 1) / RX_DECODE_TARGET_ITEMS;
+    const bool auto_chunk = kv_chunk == 0;
+    // One query row per kv head (G == 1): a request's own positions are read
+    // across all kv heads at once (whole contiguous slot rows), as
+    // single-request "wide" items; otherwise every item is per kv head.
+    const bool wide = G == 1;
+    if (auto_chunk) {
+        // about RX_DECODE_TARGET_ITEMS work items over all kv heads; with wide
+        // items, about RX_DECODE_TARGET_SHARED_ITEMS over the shared reads only
+        const int64_t n = wide ? shared * hkv : reads * hkv;
+        const int64_t target = wide ? RX_DECODE_TARGET_SHARED_ITEMS : RX_DECODE_TARGET_ITEMS;
+        int64_t c = (n + target - 1) / target;
         c = std::min<int64_t>(RX_MAX_KV_CHUNK, std::max<int64_t>(64, (c + 63) / 64 * 64));
         kv_chunk = (int32_t)c;
     }
     auto nchunks = [&](int64_t len) { return (len + kv_chunk - 1) / kv_chunk; };
+    // With wide items, a request's own (private) positions are cut by their
+    // own target count, RX_DECODE_TARGET_WIDE_ITEMS over the batch, into
+    // near-equal pieces of at most kv_chunk positions; otherwise into
+    // kv_chunk pieces.
+    int64_t priv_total = 0;
+    for (int64_t r = 0; r < B; ++r) priv_total += seq_len[order[(size_t)r]] - priv_begin[(size_t)r];
+    int64_t pchunk = kv_chunk;
+    if (auto_chunk && wide && priv_total > 0)
+        pchunk = std::min<int64_t>(kv_chunk, std::max<int64_t>(RX_DECODE_MIN_WIDE_CHUNK,
+                                   (priv_total + RX_DECODE_TARGET_WIDE_ITEMS - 1) / RX_DECODE_TARGET_WIDE_ITEMS));
+    auto npriv = [&](int64_t len) { return (len + pchunk - 1) / pchunk; };
+    // start of private piece c of n over len positions: near-equal pieces for
+    // wide items, whole kv_chunk pieces (64-key tiles) for per-head items
+    auto piece = [&](int64_t len, int64_t n, int64_t c) {
+        return wide ? len * c / n : std::min(len, c * (int64_t)kv_chunk);
+    };
     // part bases of segments and per-row private ranges
     std::vector<int64_t> part_base((size_t)n_iv, 0), base_after((size_t)n_iv, 0);
     for (int64_t k = n_iv - 1; k >= 0; --k) {
@@ -654,7 +678,7 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
     int64_t max_parts = 0;
     for (int64_t r = 0; r < B; ++r) {
         int64_t L = seq_len[order[(size_t)r]];
-        int64_t np = priv_base[(size_t)r] + nchunks(L - priv_begin[(size_t)r]);
+        int64_t np = priv_base[(size_t)r] + npriv(L - priv_begin[(size_t)r]);
         nparts[(size_t)order[(size_t)r]] = (int32_t)np;
         max_parts = std::max(max_parts, np);
     }
@@ -682,20 +706,28 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
     }
     for (int64_t r = 0; r < B; ++r) {
         int64_t L = seq_len[order[(size_t)r]], s0 = priv_begin[(size_t)r];
-        for (int64_t c = 0; c * kv_chunk < L - s0; ++c) {
-            int64_t p0 = s0 + c * kv_chunk, p1 = std::min(L, p0 + kv_chunk);
+        const int64_t n = npriv(L - s0);
+        for (int64_t c = 0; c < n; ++c) {
+            int64_t p0 = s0 + piece(L - s0, n, c), p1 = s0 + piece(L - s0, n, c + 1);
             bool fin = nparts[(size_t)order[(size_t)r]] == 1;
             const int32_t b0 = order[(size_t)r];
             items.push_back({{(int32_t)r, 1, (int32_t)p0, (int32_t)p1,
                               (int32_t)(priv_base[(size_t)r] + c), fin ? 1 : 0, req_idx[b0], b0}});
         }
     }
-    // longest first, so that the tail of the grid holds the short items
+    // items of several requests first, then single-request items (read
+    // across all kv heads at once); each group longest first, so that the
+    // tail of a grid holds the short items
     std::stable_sort(items.begin(), items.end(), [](const Item &a, const Item &b) {
+        const bool wa = a.v[1] == 1, wb = b.v[1] == 1;
+        if (wa != wb) return wb;
         int64_t la = (int64_t)a.v[3] - a.v[2], lb = (int64_t)b.v[3] - b.v[2];
         if (la != lb) return la > lb;
         return a.v[1] > b.v[1];
     });
+    int64_t n_wide = 0;
+    if (wide)
+        for (const Item &x : items) n_wide += x.v[1] == 1;
     if ((int64_t)items.size() > INT32_MAX / 8)
         return rx_set_error(RX_ERR_UNSUPPORTED, "rx_decode_plan_build: too many items");
     info->kv_chunk = kv_chunk;
@@ -705,6 +737,7 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
     info->shared_tokens = shared;
     info->tokens_read = reads;
     info->buf_words = 2 * B + 8 * (int64_t)items.size();
+    info->n_wide = (int32_t)n_wide;
     if (info->buf_words > out_cap)
         return rx_set_error(RX_ERR_CAPACITY, "rx_decode_plan_build: need %lld words",
                             (long long)info->buf_words);

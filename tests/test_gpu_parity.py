@@ -230,6 +230,21 @@ def test_decode_bad_slot_is_flagged():
     assert np.isfinite(o).all()
 
 
+def test_decode_bad_slot_in_wide_item_is_flagged():
+    """A bad slot id inside a single-request item (the all-heads path) is
+    flagged and read as a zero row, like the per-head path does."""
+    g = _gpu()
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.few_shot_decode(hq=8, hkv=8, d=128, batch=4, shared=40, private=90, num_slots=512)
+    prob.req_to_token = prob.req_to_token.copy()
+    prob.req_to_token[1, 70] = -3                      # inside request 1's private tail
+    dev = g.Dev(prob)
+    dev.kv_store()
+    o, _ = dev.decode(plan=True, kv_chunk=64)
+    assert dev.status_word() & rx.RX_DEV_BAD_SLOT
+    assert np.isfinite(o).all()
+
+
 def test_decode_length_past_bound_is_flagged():
     g = _gpu()
     from prefix_shared_kv_radixattention_gb300 import binding as rx

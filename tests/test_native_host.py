@@ -318,6 +318,16 @@ def check_plan(prob, order, nparts, items, info):
         assert np.all(cover[b] == 1), f"request {b} context not covered exactly once"
         assert sorted(parts[b]) == list(range(int(nparts[b])))
     assert info.max_parts == int(nparts.max())
+    # items of several requests first, then the single-request items, each
+    # group longest first; with one q head per kv head the single-request
+    # items are the n_wide "wide" ones, otherwise there are none
+    single = items[:, 1] == 1
+    n_single = int(single.sum())
+    assert np.all(single[len(items) - n_single:]) and not np.any(single[:len(items) - n_single])
+    assert int(info.n_wide) == (n_single if G == 1 else 0)
+    for grp in (items[~single], items[single]):
+        lens = grp[:, 3] - grp[:, 2]
+        assert np.all(lens[:-1] >= lens[1:])
 
 
 @pytest.mark.parametrize("seed", range(15))
