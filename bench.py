@@ -172,7 +172,10 @@ class GpuStep:
             self.plan = rx.plan_to_device(buf, info, B)
             ws = rx.rx_attn_decode_workspace(B, p.hq, p.hkv, p.d, self.max_len, self.plan)
             self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev) if ws else None
-            self.launches += 1 + (1 if info.max_parts > 1 else 0)
+            # per-head kernel (items of several requests), all-heads kernel
+            # (single-request items, one q head per kv head), merge of splits
+            n_wide = info.n_wide if (p.hq == p.hkv and p.hq in (8, 16, 32, 64)) else 0
+            self.launches += ((info.n_items - n_wide) > 0) + (n_wide > 0) + (info.max_parts > 1)
         if self.has_ext:
             self.q_ext = bf(p.q_ext)
             self.o_ext = torch.empty_like(self.q_ext)

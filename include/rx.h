@@ -291,8 +291,11 @@ int rx_decode_plan_build(const int32_t *req_to_token, int64_t rtt_stride, const 
                          int32_t num_kv_heads, int32_t kv_chunk, int32_t min_shared,
                          int32_t *out_buf, int64_t out_cap, rx_decode_plan_info *info);
 
-/* Workspace bytes rx_attn_decode needs (0 when every request fits one work
- * item).  With plan == NULL the split is chosen from batch and max_seq_len. */
+/* Workspace bytes rx_attn_decode needs: fp32 partial results when a request
+ * is split over several work items, plus 256 bytes for a work counter when
+ * the plan has single-request ("wide") items that run on the all-heads
+ * kernel; 0 when neither applies.  With plan == NULL the split is chosen
+ * from batch and max_seq_len. */
 size_t rx_attn_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                 int32_t head_dim, int32_t max_seq_len,
                                 const rx_decode_plan *plan_or_null);

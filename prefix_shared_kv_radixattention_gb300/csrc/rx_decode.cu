@@ -122,6 +122,7 @@ struct Params {
     float scale_log2;
     int32_t *status;
     int wide0, n_wide;      // plan: single-request items for the wide kernel
+    int *wide_counter;      // next wide item to hand out (zeroed before the launch)
 };
 
 struct Item {
@@ -723,7 +724,8 @@ struct WideLayout {
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = kWideStages * kWideStageBytes;
     static constexpr int OFF_OK = 2 * kWideStages * kWideStageBytes;  // int [stage][pos]: row valid
-    static constexpr int OFF_BAR = OFF_OK + kWideStages * kWideMaxPos * 4;
+    static constexpr int OFF_HDR = OFF_OK + kWideStages * kWideMaxPos * 4;  // int2 [stage]: item, first position
+    static constexpr int OFF_BAR = OFF_HDR + kWideStages * 8;
     static constexpr int OFF_ABORT = OFF_BAR + 2 * kWideStages * 8;
     static constexpr int BYTES = OFF_ABORT + 16 + 128;  // + room to align the base to 128
 };
@@ -787,13 +789,21 @@ __global__ void __launch_bounds__(kWideThreads, 1) decode_wide_kernel(const Para
     __syncthreads();
 
     if (warp == 0) {
-        // producer: stage j of the CTA's item sequence holds positions
-        // q0 .. q0 + NP - 1 of one item, one lane per position.  The slot ids
-        // of the next stage are loaded before waiting for a free stage, so
-        // their latency is not on the copy path.
+        // producer: stage j holds positions q0 .. q0 + NP - 1 of one item, one
+        // lane per position.  Items come from a global counter, first come
+        // first served, so a CTA that starts late (behind the per-head kernel
+        // running alongside) takes fewer of them.  Each stage's header names
+        // its item; a last header with item -1 tells the consumers to stop.
+        // The slot ids of the next stage are loaded before waiting for a free
+        // stage, so their latency is off the copy path.
         struct Cursor {
             int it, q0, p1;
             const int32_t *slots;
+        };
+        auto fetch = [&]() -> int {
+            int it = 0;
+            if (lane == 0) it = atomicAdd(p.wide_counter, 1);
+            return __shfl_sync(0xffffffffu, it, 0);
         };
         auto open_item = [&](Cursor &c) {
             if (c.it < p.n_wide) {
@@ -806,7 +816,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) decode_wide_kernel(const Para
         auto next_stage = [&](Cursor &c) {
             c.q0 += NP;
             if (c.q0 >= c.p1) {
-                c.it += gridDim.x;
+                c.it = fetch();
                 open_item(c);
             }
         };
@@ -814,24 +824,27 @@ __global__ void __launch_bounds__(kWideThreads, 1) decode_wide_kernel(const Para
             const int pos = c.q0 + lane;
             return (c.it < p.n_wide && lane < NP && pos < c.p1) ? __ldg(c.slots + pos) : -1;
         };
-        Cursor cur{(int)blockIdx.x, 0, 0, nullptr};
+        int2 *hdr = reinterpret_cast<int2 *>(smem + WL::OFF_HDR);
+        Cursor cur{fetch(), 0, 0, nullptr};
         open_item(cur);
         int32_t sl_cur = slot_of(cur);
         int j = 0;
-        for (; cur.it < p.n_wide; ++j) {
+        for (;; ++j) {
+            const bool end = cur.it >= p.n_wide;
             Cursor nxt = cur;
-            next_stage(nxt);
-            const int32_t sl_nxt = slot_of(nxt);
+            if (!end) next_stage(nxt);
+            const int32_t sl_nxt = end ? -1 : slot_of(nxt);
             const int st = j % kWideStages;
             if (j >= kWideStages &&
                 !wait_or_abort(bar + 8 * (kWideStages + st), ((j / kWideStages) - 1) & 1, abort_flag, p.status))
                 break;
-            const bool inside = lane < NP && cur.q0 + lane < cur.p1;
+            const bool inside = !end && lane < NP && cur.q0 + lane < cur.p1;
             const bool ok = inside && sl_cur >= 0 && (int64_t)sl_cur < p.num_slots;
             if (inside && !ok && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
             if (lane < NP) okf[st * kWideMaxPos + lane] = ok ? 1 : 0;
+            if (lane == 0) hdr[st] = make_int2(end ? -1 : cur.it, cur.q0);
             const int nok = __popc(__ballot_sync(0xffffffffu, ok));
-            __syncwarp();  // the flags are written before lane 0's arrive releases them
+            __syncwarp();  // flags and header are written before lane 0's arrive releases them
             if (lane == 0) rx::mbar_arrive_expect_tx(bar + 8 * st, (uint32_t)(2 * nok * RB));
             __syncwarp();
             if (ok) {
@@ -840,6 +853,10 @@ __global__ void __launch_bounds__(kWideThreads, 1) decode_wide_kernel(const Para
                              bar + 8 * st);
                 rx::bulk_g2s(sbase + WL::OFF_V + off, p.v_pool + (int64_t)sl_cur * row_elems, (uint32_t)RB,
                              bar + 8 * st);
+            }
+            if (end) {
+                ++j;
+                break;
             }
             cur = nxt;
             sl_cur = sl_nxt;
@@ -860,27 +877,58 @@ __global__ void __launch_bounds__(kWideThreads, 1) decode_wide_kernel(const Para
         // head hx = x / NP, position ix = x % NP
         const int x = lane >> (5 - LOG_HN);
         const int hx = x >> LOG_NP, ix = x & (NP - 1);
-        int j = 0;
-        for (int it = blockIdx.x; it < p.n_wide; it += gridDim.x) {
-            const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + it);
-            const int p0 = __ldg(v + 2), p1 = __ldg(v + 3), part_idx = __ldg(v + 4);
-            const bool fin = __ldg(v + 5) != 0;
-            const int b = __ldg(v + 7);
-            float q[HPW][E], o[HPW][E], m[HPW], l[HPW];
+        const int2 *hdr = reinterpret_cast<const int2 *>(smem + WL::OFF_HDR);
+        float q[HPW][E], o[HPW][E], m[HPW], l[HPW];
+        int cur = -1, p1 = 0, part_idx = 0, b = 0;
+        bool fin = false;
+        // the current item's results for this warp's heads
+        auto write_out = [&]() {
 #pragma unroll
             for (int hh = 0; hh < HPW; ++hh) {
-                const bf16 *qp = p.q + ((int64_t)b * p.hq + h0 + hh) * D + lane * E;
-                m[hh] = -INFINITY;
-                l[hh] = 0.f;
+                const int64_t orow = (int64_t)b * p.hq + h0 + hh;
+                const float inv = 1.f / l[hh];
+                if (fin) {
+                    bf16 *dst = p.o + orow * D + lane * E;
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    q[hh][e] = __bfloat162float(qp[e]) * p.scale_log2;
-                    o[hh][e] = 0.f;
+                    for (int e = 0; e < E; e += 2)
+                        *reinterpret_cast<uint32_t *>(dst + e) = rx::pack_bf16(o[hh][e] * inv, o[hh][e + 1] * inv);
+                    if (p.lse && lane == 0) p.lse[orow] = (m[hh] + log2f(l[hh])) * rx::kLn2;
+                } else {
+                    const int64_t prow = orow * p.max_parts + part_idx;
+                    float *dst = p.ws_o + prow * D + lane * E;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) dst[e] = o[hh][e] * inv;
+                    if (lane == 0) p.ws_lse[prow] = m[hh] + log2f(l[hh]);
                 }
             }
-            for (int q0 = p0; q0 < p1; q0 += NP, ++j) {
-                const int st = j % kWideStages;
-                if (!wait_or_abort(bar + 8 * st, (j / kWideStages) & 1, abort_flag, p.status)) return;
+        };
+        for (int j = 0;; ++j) {
+            const int st = j % kWideStages;
+            if (!wait_or_abort(bar + 8 * st, (j / kWideStages) & 1, abort_flag, p.status)) return;
+            const int2 h = hdr[st];
+            if (h.x != cur) {  // a new item starts (or, with -1, none is left)
+                if (cur >= 0) write_out();
+                if (h.x < 0) break;
+                cur = h.x;
+                const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + cur);
+                p1 = __ldg(v + 3);
+                part_idx = __ldg(v + 4);
+                fin = __ldg(v + 5) != 0;
+                b = __ldg(v + 7);
+#pragma unroll
+                for (int hh = 0; hh < HPW; ++hh) {
+                    const bf16 *qp = p.q + ((int64_t)b * p.hq + h0 + hh) * D + lane * E;
+                    m[hh] = -INFINITY;
+                    l[hh] = 0.f;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        q[hh][e] = __bfloat162float(qp[e]) * p.scale_log2;
+                        o[hh][e] = 0.f;
+                    }
+                }
+            }
+            {
+                const int q0 = h.y;
                 const int n = min(NP, p1 - q0);
                 const unsigned char *ks = smem + WL::OFF_K + st * kWideStageBytes + h0 * D * 2 + lane * E * 2;
                 const unsigned char *vs = smem + WL::OFF_V + st * kWideStageBytes + h0 * D * 2 + lane * E * 2;
@@ -957,25 +1005,6 @@ __global__ void __launch_bounds__(kWideThreads, 1) decode_wide_kernel(const Para
                 __syncwarp();
                 if (lane == 0) rx::mbar_arrive(bar + 8 * (kWideStages + st));
             }
-            // results of the item for this warp's heads
-#pragma unroll
-            for (int hh = 0; hh < HPW; ++hh) {
-                const int64_t orow = (int64_t)b * p.hq + h0 + hh;
-                const float inv = 1.f / l[hh];
-                if (fin) {
-                    bf16 *dst = p.o + orow * D + lane * E;
-#pragma unroll
-                    for (int e = 0; e < E; e += 2)
-                        *reinterpret_cast<uint32_t *>(dst + e) = rx::pack_bf16(o[hh][e] * inv, o[hh][e + 1] * inv);
-                    if (p.lse && lane == 0) p.lse[orow] = (m[hh] + log2f(l[hh])) * rx::kLn2;
-                } else {
-                    const int64_t prow = orow * p.max_parts + part_idx;
-                    float *dst = p.ws_o + prow * D + lane * E;
-#pragma unroll
-                    for (int e = 0; e < E; ++e) dst[e] = o[hh][e] * inv;
-                    if (lane == 0) p.ws_lse[prow] = m[hh] + log2f(l[hh]);
-                }
-            }
         }
     }
 }
@@ -1031,6 +1060,35 @@ int launch_decode(const Params &p, cudaStream_t st)
     return RX_OK;
 }
 
+// A second stream and two events per device for running the per-head and
+// the wide kernel side by side inside one rx_attn_decode call.  Created on
+// first use; the mutex keeps each call's record/wait pairs together when
+// several host threads call at once.
+struct ForkJoin {
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex &fork_mutex()
+{
+    static std::mutex m;
+    return m;
+}
+int fork_join_for_current_device(ForkJoin **out)
+{
+    static ForkJoin per_dev[64];
+    int dev = 0;
+    RX_CUDA_CHECK(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_decode: device %d", dev);
+    ForkJoin &f = per_dev[dev];
+    if (!f.side) {
+        RX_CUDA_CHECK(cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking));
+        RX_CUDA_CHECK(cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming));
+        RX_CUDA_CHECK(cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming));
+    }
+    *out = &f;
+    return RX_OK;
+}
+
 template <int D>
 int launch_merge(const Params &p, int use_plan, cudaStream_t st)
 {
@@ -1065,10 +1123,12 @@ extern "C" size_t rx_attn_decode_workspace(int32_t batch, int32_t num_q_heads, i
         const int64_t c = rx_decode_default_chunk(batch, num_kv_heads, max_seq_len);
         parts = (max_seq_len + c - 1) / c;
     }
-    if (parts <= 1) return 0;
-    const int64_t rows = (int64_t)batch * num_q_heads * parts;
-    const int64_t bytes = rows * (head_dim + 1) * 4;
-    return (size_t)((bytes + 255) / 256 * 256);
+    // partials (o and log2-sum-exp) when a request is split, then 256 bytes
+    // for the wide kernel's item counter when it runs
+    const int64_t rows = parts > 1 ? (int64_t)batch * num_q_heads * parts : 0;
+    const int64_t bytes = (rows * (head_dim + 1) * 4 + 255) / 256 * 256;
+    const bool wide = plan && plan->n_wide > 0 && wide_supported(num_q_heads, num_kv_heads, head_dim);
+    return (size_t)(bytes + (wide ? 256 : 0));
 }
 
 extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, float *lse,
@@ -1137,26 +1197,47 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
     if (total == 0 && p.n_wide == 0) return RX_OK;
     p.total_work = (int)total;
     const size_t need = rx_attn_decode_workspace(batch, hq, p.hkv, D, max_seq_len, plan);
+    const bool merge = p.max_parts > 1;
     if (need > 0) {
         if (!workspace || ws_bytes < need)
             return rx_set_error(RX_ERR_CAPACITY, "rx_attn_decode: workspace needs %zu bytes, got %zu",
                                 need, ws_bytes);
         if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
             return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: workspace must be 256-byte aligned");
-        p.ws_o = (float *)workspace;
-        p.ws_lse = p.ws_o + (int64_t)batch * hq * p.max_parts * D;
+        if (merge) {
+            p.ws_o = (float *)workspace;
+            p.ws_lse = p.ws_o + (int64_t)batch * hq * p.max_parts * D;
+        }
+        if (p.n_wide > 0) p.wide_counter = reinterpret_cast<int *>(static_cast<char *>(workspace) + need - 256);
     }
     cudaStream_t st = (cudaStream_t)stream;
     int rc = RX_OK;
-    if (p.total_work > 0) {
-        if (D == 128)
-            rc = plan ? launch_decode<128, true>(p, st) : launch_decode<128, false>(p, st);
-        else
-            rc = plan ? launch_decode<64, true>(p, st) : launch_decode<64, false>(p, st);
+    auto per_head = [&](cudaStream_t s) {
+        if (D == 128) return plan ? launch_decode<128, true>(p, s) : launch_decode<128, false>(p, s);
+        return plan ? launch_decode<64, true>(p, s) : launch_decode<64, false>(p, s);
+    };
+    if (p.n_wide == 0) {
+        if (p.total_work > 0) rc = per_head(st);
+    } else {
+        // the per-head items (shared segments) and the wide items run side by
+        // side: the per-head kernel on a second stream forked from and joined
+        // back into the caller's stream, the wide kernel on the caller's
+        RX_CUDA_CHECK(cudaMemsetAsync(p.wide_counter, 0, sizeof(int), st));
+        if (p.total_work > 0) {
+            std::lock_guard<std::mutex> g(fork_mutex());
+            ForkJoin *fj = nullptr;
+            if ((rc = fork_join_for_current_device(&fj)) != RX_OK) return rc;
+            RX_CUDA_CHECK(cudaEventRecord(fj->fork, st));
+            RX_CUDA_CHECK(cudaStreamWaitEvent(fj->side, fj->fork, 0));
+            rc = per_head(fj->side);
+            if (rc == RX_OK) rc = D == 128 ? launch_decode_wide<128>(p, st) : launch_decode_wide<64>(p, st);
+            RX_CUDA_CHECK(cudaEventRecord(fj->join, fj->side));
+            RX_CUDA_CHECK(cudaStreamWaitEvent(st, fj->join, 0));
+        } else {
+            rc = D == 128 ? launch_decode_wide<128>(p, st) : launch_decode_wide<64>(p, st);
+        }
     }
-    if (rc == RX_OK && p.n_wide > 0)
-        rc = D == 128 ? launch_decode_wide<128>(p, st) : launch_decode_wide<64>(p, st);
-    if (rc != RX_OK || need == 0) return rc;
+    if (rc != RX_OK || !merge) return rc;
     return D == 128 ? launch_merge<128>(p, plan != nullptr, st) : launch_merge<64>(p, plan != nullptr, st);
 }
 
