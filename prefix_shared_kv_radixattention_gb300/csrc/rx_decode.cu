@@ -21,8 +21,8 @@
 //     loads), publishes each as a descriptor in a 4-deep ring, and prefetches
 //     the slot ids of every 64-key stage with 4-byte cp.async into a 16-deep
 //     slot ring -- so no copy ever waits on a dependent index load;
-//   - three copier warps gather K and V rows (head_dim * 2 contiguous bytes
-//     per row and kv head, 16-byte cp.async, a third of every stage each)
+//   - seven copier warps gather K and V rows (head_dim * 2 contiguous bytes
+//     per row and kv head, 16-byte cp.async, a seventh of every stage each)
 //     into a ring of 64-key stages, and the query rows into a double-buffered
 //     Q slot; every ring entry is an mbarrier that the copies themselves
 //     complete (cp.async.mbarrier.arrive), so the ring streams across item
@@ -38,6 +38,9 @@
 //   - rows sit at a padded stride of head_dim * 2 + 16 bytes, so the eight
 //     rows an ldmatrix reads fall in distinct banks; stage rows past an
 //     item's end are zero-filled by the copy and their scores masked.
+// Single-request items of a plan with one q head per kv head go instead to
+// decode_wide_kernel (below), which reads whole slot rows across all kv heads
+// and runs alongside this kernel.
 // An item that covers a row's whole context writes bf16 o directly;
 // otherwise it writes a normalised fp32 partial and its log2-sum-exp, and
 // merge_kernel combines them: o = sum_s w_s o_s / sum_s w_s with
@@ -291,7 +294,7 @@ __device__ void copier(const Params &p, unsigned char *smem)
     const int32_t *slotbuf = reinterpret_cast<const int32_t *>(smem + L::OFF_SLOT);
     const uint32_t bar = rx::smem_u32(smem + L::OFF_BAR);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_ABORT);
-    const int cw = (threadIdx.x >> 5) - 1, lane = threadIdx.x & 31, ct = threadIdx.x - 32;
+    const int lane = threadIdx.x & 31, ct = threadIdx.x - 32;
     uint32_t n_it = 0, n_tile = 0, qi = 0;
     for (;; ++n_it) {
         const uint32_t di = n_it % kNIT;
@@ -299,13 +302,13 @@ __device__ void copier(const Params &p, unsigned char *smem)
         const Desc *d = descs + di;
         const int M = d->M, p0 = d->p0, p1 = d->p1, g = d->g;
         if (M == 0) break;
-        if (cw == 0) {  // query rows -> Q slot (rows past M zero-filled)
+        {  // query rows -> Q slot (rows past M zero-filled), by every copier thread
             const uint32_t qs = qi & 1;
             if (!wait_or_abort(bar + 8 * (L::B_QEMPTY + qs), ((qi >> 1) & 1) ^ 1, abort_flag, p.status))
                 break;
             const int Mpad = mpad_of(M);
             bf16 *qd = Qs + qs * L::QSLOT;
-            for (int idx = lane; idx < Mpad * CPR; idx += 32) {
+            for (int idx = ct; idx < Mpad * CPR; idx += NCT) {
                 const int m = idx / CPR, c = idx % CPR;
                 const uint32_t dst = rx::smem_u32(qd + m * L::RS + c * 8);
                 if (m < M) {
@@ -590,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p)
             rx::mbar_init(bar + 8 * (L::B_EMPTY + s), kConsumers);
         }
         for (int q = 0; q < 2; ++q) {
-            rx::mbar_init(bar + 8 * (L::B_QFULL + q), 32);  // copier warp 0's lanes
+            rx::mbar_init(bar + 8 * (L::B_QFULL + q), 32 * kCopiers);  // every copier lane's copies
             rx::mbar_init(bar + 8 * (L::B_QEMPTY + q), kConsumers);
         }
         for (int s = 0; s < kNSL; ++s) {
@@ -657,23 +660,33 @@ __global__ void __launch_bounds__(128) merge_kernel(const Params p, int use_plan
     float acc[PER];
 #pragma unroll
     for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+    // part weights computed lane-parallel (lane k: part base + k), then the
+    // parts' rows read eight at a time so their loads are in flight together
     float wsum = 0.f;
-    for (int i = 0; i < np; ++i) {
-        const float wgt = rx::fast_exp2(lp[i] - m);
-        wsum += wgt;
-        const float *src = p.ws_o + (row * p.max_parts + i) * D + lane * PER;
-        if constexpr (PER == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(src);
-            acc[0] += wgt * v.x;
-            acc[1] += wgt * v.y;
-            acc[2] += wgt * v.z;
-            acc[3] += wgt * v.w;
-        } else {
-            const float2 v = *reinterpret_cast<const float2 *>(src);
-            acc[0] += wgt * v.x;
-            acc[1] += wgt * v.y;
+    for (int base = 0; base < np; base += 32) {
+        const int cnt = min(32, np - base);
+        const float wl = lane < cnt ? rx::fast_exp2(lp[base + lane] - m) : 0.f;
+        wsum += wl;
+        const float *src0 = p.ws_o + (row * p.max_parts + base) * D + lane * PER;
+#pragma unroll 8
+        for (int k = 0; k < cnt; ++k) {
+            const float wgt = __shfl_sync(0xffffffffu, wl, k);
+            const float *src = src0 + (int64_t)k * D;
+            if constexpr (PER == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(src);
+                acc[0] = fmaf(wgt, v.x, acc[0]);
+                acc[1] = fmaf(wgt, v.y, acc[1]);
+                acc[2] = fmaf(wgt, v.z, acc[2]);
+                acc[3] = fmaf(wgt, v.w, acc[3]);
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(src);
+                acc[0] = fmaf(wgt, v.x, acc[0]);
+                acc[1] = fmaf(wgt, v.y, acc[1]);
+            }
         }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     const float inv = 1.f / wsum;
     bf16 *dst = p.o + row * D + lane * PER;
 #pragma unroll
