@@ -727,8 +727,6 @@ int num_sms()
 //     position a lane-split dot product, a warp all-reduce and an online
 //     softmax step.
 
-constexpr int kWideConsumers = 8;
-constexpr int kWideThreads = 32 * (1 + kWideConsumers);
 constexpr int kWideStages = 3;
 constexpr int kWideStageBytes = 32768;  // K bytes per stage (as many again for V)
 constexpr int kWideMaxPos = 32;         // positions per stage at most (one producer lane each)
@@ -775,8 +773,8 @@ __device__ __forceinline__ void load_bf16(const unsigned char *src, float (&out)
     }
 }
 
-template <int D, int LOG_NP, int HPW>
-__global__ void __launch_bounds__(kWideThreads, 1) decode_wide_kernel(const Params p)
+template <int D, int LOG_NP, int HPW, int CW>
+__global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Params p)
 {
     using WL = WideLayout;
     constexpr int E = D / 32;  // values of a head row per lane
@@ -794,7 +792,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) decode_wide_kernel(const Para
     if (threadIdx.x == 0) {
         for (int i = 0; i < kWideStages; ++i) {
             rx::mbar_init(bar + 8 * i, 1);                                  // producer + bytes
-            rx::mbar_init(bar + 8 * (kWideStages + i), kWideConsumers);     // consumer warps
+            rx::mbar_init(bar + 8 * (kWideStages + i), CW);                 // consumer warps
         }
         *abort_flag = 0;
         rx::fence_mbar_init();
@@ -1022,24 +1020,24 @@ __global__ void __launch_bounds__(kWideThreads, 1) decode_wide_kernel(const Para
     }
 }
 
-template <int D, int LOG_NP, int HPW>
+template <int D, int LOG_NP, int HPW, int CW>
 int launch_decode_wide_cfg(const Params &p, cudaStream_t st)
 {
     static bool configured = false;
     if (!configured) {
-        RX_CUDA_CHECK(cudaFuncSetAttribute(decode_wide_kernel<D, LOG_NP, HPW>,
+        RX_CUDA_CHECK(cudaFuncSetAttribute(decode_wide_kernel<D, LOG_NP, HPW, CW>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, WideLayout::BYTES));
         configured = true;
     }
     const int grid = p.n_wide < num_sms() ? p.n_wide : num_sms();
-    decode_wide_kernel<D, LOG_NP, HPW><<<grid, kWideThreads, WideLayout::BYTES, st>>>(p);
+    decode_wide_kernel<D, LOG_NP, HPW, CW><<<grid, 32 * (1 + CW), WideLayout::BYTES, st>>>(p);
     RX_CUDA_CHECK(cudaGetLastError());
     return RX_OK;
 }
 
-// Wide items need one q head per kv head and 8, 16, 32 or 64 heads: each of
-// the eight consumer warps then owns hq / 8 heads, and a stage holds
-// 2048 / D (head, position) pairs per warp -- one per lane or half-lane.
+// Wide items need one q head per kv head and 8, 16, 32 or 64 heads: the
+// consumer warps (16, or 8 for 8 heads) each own hq / 16 (or one) heads, and
+// a stage holds at most one (head, position) pair per lane for each of them.
 bool wide_supported(int hq, int hkv, int D)
 {
     return hq == hkv && (hq == 8 || hq == 16 || hq == 32 || hq == 64) && (D == 64 || D == 128);
@@ -1050,10 +1048,10 @@ int launch_decode_wide(const Params &p, cudaStream_t st)
 {
     constexpr int L0 = D == 128 ? 4 : 5;  // log2 positions per stage at 8 heads
     switch (p.hq) {
-    case 8: return launch_decode_wide_cfg<D, L0, 1>(p, st);
-    case 16: return launch_decode_wide_cfg<D, L0 - 1, 2>(p, st);
-    case 32: return launch_decode_wide_cfg<D, L0 - 2, 4>(p, st);
-    default: return launch_decode_wide_cfg<D, L0 - 3, 8>(p, st);
+    case 8: return launch_decode_wide_cfg<D, L0, 1, 8>(p, st);
+    case 16: return launch_decode_wide_cfg<D, L0 - 1, 1, 16>(p, st);
+    case 32: return launch_decode_wide_cfg<D, L0 - 2, 2, 16>(p, st);
+    default: return launch_decode_wide_cfg<D, L0 - 3, 4, 16>(p, st);
     }
 }
 
