@@ -736,11 +736,18 @@ struct WideLayout {
     static constexpr int OFF_V = kWideStages * kWideStageBytes;
     static constexpr int OFF_OK = 2 * kWideStages * kWideStageBytes;  // int [stage][pos]: row valid
     static constexpr int OFF_HDR = OFF_OK + kWideStages * kWideMaxPos * 4;  // int2 [stage]: item, first position
-    static constexpr int OFF_BAR = OFF_HDR + kWideStages * 8;
-    static constexpr int OFF_ABORT = OFF_BAR + 2 * kWideStages * 8;
+    static constexpr int OFF_Q = (OFF_HDR + kWideStages * 8 + 127) / 128 * 128;  // 2 x the item's query row
+    static constexpr int QBYTES = 16384;                                   // hq * D * 2 at most
+    static constexpr int OFF_BAR = OFF_Q + 2 * QBYTES;   // full [S], empty [S], q_empty [2]
+    static constexpr int OFF_ABORT = OFF_BAR + (2 * kWideStages + 2) * 8;
     static constexpr int BYTES = OFF_ABORT + 16 + 128;  // + room to align the base to 128
 };
 static_assert(WideLayout::OFF_BAR % 8 == 0, "mbarrier alignment");
+static_assert(WideLayout::BYTES <= 227 * 1024, "shared memory budget");
+// bulk copies land on 16-byte boundaries: stage rows (multiples of 128 bytes
+// from a stage base) and the q slots
+static_assert(WideLayout::OFF_V % 128 == 0 && WideLayout::OFF_Q % 128 == 0 && WideLayout::QBYTES % 128 == 0,
+              "bulk-copy destination alignment");
 
 
 // bounded single-thread wait that ignores the abort flag: lets copies already
@@ -794,6 +801,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
             rx::mbar_init(bar + 8 * i, 1);                                  // producer + bytes
             rx::mbar_init(bar + 8 * (kWideStages + i), CW);                 // consumer warps
         }
+        for (int i = 0; i < 2; ++i) rx::mbar_init(bar + 8 * (2 * kWideStages + i), CW);  // q slot read
         *abort_flag = 0;
         rx::fence_mbar_init();
     }
@@ -836,10 +844,12 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
             return (c.it < p.n_wide && lane < NP && pos < c.p1) ? __ldg(c.slots + pos) : -1;
         };
         int2 *hdr = reinterpret_cast<int2 *>(smem + WL::OFF_HDR);
+        const uint32_t qbytes = (uint32_t)(p.hq * D * 2);
         Cursor cur{fetch(), 0, 0, nullptr};
         open_item(cur);
         int32_t sl_cur = slot_of(cur);
-        int j = 0;
+        int j = 0, n_items = 0;   // items opened so far; item k uses q slot k & 1
+        bool first = true;        // the stage is its item's first
         for (;; ++j) {
             const bool end = cur.it >= p.n_wide;
             Cursor nxt = cur;
@@ -849,6 +859,13 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
             if (j >= kWideStages &&
                 !wait_or_abort(bar + 8 * (kWideStages + st), ((j / kWideStages) - 1) & 1, abort_flag, p.status))
                 break;
+            // an item's first stage also brings its query row into q slot k & 1,
+            // once the consumers have read item k - 2's out of it
+            const bool with_q = first && !end;
+            const int qb = n_items & 1;
+            if (with_q && n_items >= 2 &&
+                !wait_or_abort(bar + 8 * (2 * kWideStages + qb), ((n_items >> 1) - 1) & 1, abort_flag, p.status))
+                break;
             const bool inside = !end && lane < NP && cur.q0 + lane < cur.p1;
             const bool ok = inside && sl_cur >= 0 && (int64_t)sl_cur < p.num_slots;
             if (inside && !ok && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
@@ -856,8 +873,15 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
             if (lane == 0) hdr[st] = make_int2(end ? -1 : cur.it, cur.q0);
             const int nok = __popc(__ballot_sync(0xffffffffu, ok));
             __syncwarp();  // flags and header are written before lane 0's arrive releases them
-            if (lane == 0) rx::mbar_arrive_expect_tx(bar + 8 * st, (uint32_t)(2 * nok * RB));
+            if (lane == 0)
+                rx::mbar_arrive_expect_tx(bar + 8 * st, (uint32_t)(2 * nok * RB) + (with_q ? qbytes : 0u));
             __syncwarp();
+            if (with_q && lane == 0) {
+                const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + cur.it);
+                rx::bulk_g2s(sbase + WL::OFF_Q + qb * WL::QBYTES, p.q + (int64_t)__ldg(v + 7) * p.hq * D, qbytes,
+                             bar + 8 * st);
+            }
+            if (with_q) ++n_items;
             if (ok) {
                 const uint32_t off = (uint32_t)(st * kWideStageBytes + lane * RB);
                 rx::bulk_g2s(sbase + WL::OFF_K + off, p.k_pool + (int64_t)sl_cur * row_elems, (uint32_t)RB,
@@ -869,6 +893,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
                 ++j;
                 break;
             }
+            first = nxt.it != cur.it;
             cur = nxt;
             sl_cur = sl_nxt;
         }
@@ -890,7 +915,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
         const int hx = x >> LOG_NP, ix = x & (NP - 1);
         const int2 *hdr = reinterpret_cast<const int2 *>(smem + WL::OFF_HDR);
         float q[HPW][E], o[HPW][E], m[HPW], l[HPW];
-        int cur = -1, p1 = 0, part_idx = 0, b = 0;
+        int cur = -1, p1 = 0, part_idx = 0, b = 0, n_items = 0;
         bool fin = false;
         // the current item's results for this warp's heads
         auto write_out = [&]() {
@@ -926,24 +951,36 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
                 part_idx = __ldg(v + 4);
                 fin = __ldg(v + 5) != 0;
                 b = __ldg(v + 7);
+                // the query row came with this stage: read this warp's heads,
+                // then hand the q slot back
+                const int qb = n_items & 1;
+                const unsigned char *qs = smem + WL::OFF_Q + qb * WL::QBYTES + h0 * D * 2 + lane * E * 2;
 #pragma unroll
                 for (int hh = 0; hh < HPW; ++hh) {
-                    const bf16 *qp = p.q + ((int64_t)b * p.hq + h0 + hh) * D + lane * E;
+                    float qf[E];
+                    load_bf16<E>(qs + hh * D * 2, qf);
                     m[hh] = -INFINITY;
                     l[hh] = 0.f;
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
-                        q[hh][e] = __bfloat162float(qp[e]) * p.scale_log2;
+                        q[hh][e] = qf[e] * p.scale_log2;
                         o[hh][e] = 0.f;
                     }
                 }
+                __syncwarp();
+                if (lane == 0) rx::mbar_arrive(bar + 8 * (2 * kWideStages + qb));
+                ++n_items;
             }
             {
                 const int q0 = h.y;
                 const int n = min(NP, p1 - q0);
                 const unsigned char *ks = smem + WL::OFF_K + st * kWideStageBytes + h0 * D * 2 + lane * E * 2;
                 const unsigned char *vs = smem + WL::OFF_V + st * kWideStageBytes + h0 * D * 2 + lane * E * 2;
+                // bit i: position i of the stage holds a valid row
                 const int *okp = okf + st * kWideMaxPos;
+                uint32_t vmask = 0;
+#pragma unroll
+                for (int i = 0; i < NP; ++i) vmask |= (i < n && okp[i] != 0) ? (1u << i) : 0u;
                 // partial dot products over this lane's E dims, pair (hh, i) at hh * NP + i
                 float part[HN];
 #pragma unroll
@@ -974,7 +1011,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
                 for (int off = 16 >> LOG_HN; off >= 1; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
                 // a position past the item is out; a row with an invalid slot reads as zeros
                 const bool in = ix < n;
-                const bool okx = in && okp[ix] != 0;
+                const bool okx = (vmask >> ix) & 1u;
                 sc = in ? (okx ? sc : 0.f) : -INFINITY;
                 // per head: max and sum over its NP positions (lane bits of ix)
                 float smax = sc;
@@ -1007,7 +1044,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
                         const float pi = __shfl_sync(0xffffffffu, pv, ((hh << LOG_NP) + i) << (5 - LOG_HN));
                         // rows past the item or with an invalid slot were never
                         // written in this stage: skip them (0 * stale NaN is NaN)
-                        if (i >= n || okp[i] == 0) continue;
+                        if (!((vmask >> i) & 1u)) continue;
                         float vf[E];
                         load_bf16<E>(vs + i * RB + hh * D * 2, vf);
 #pragma unroll
