@@ -294,7 +294,7 @@ def run_gpu(args, rank, world, local_rank):
         traffic, tsrc = profiled_traffic(args.workload, "decode")
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": traffic, "traffic_source": tsrc,
-                "kernel": "rx_attn_decode (decode_kernel + merge_kernel)",
+                "kernel": "rx_attn_decode (decode_kernel + decode_wide_kernel + merge_kernel)",
                 "algorithmic_bytes_per_launch": int(uniq_bytes), "launch_ms": round(dec_ms, 5),
                 "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)",
                 "frac_of_8000": round(achieved / 8000.0, 4)}
@@ -396,6 +396,7 @@ def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
 # captures summarised in the named profile; an entry is removed whenever its
 # kernel changes, so that an old count is never reported for new code.
 PROFILED_TRAFFIC = {
+    ("few_shot_decode", "decode"): (299_800_000, "profiles/decode_kernel.few_shot_decode.md"),
     ("cached_prefix_extend", "staged"): (584_500_736, "profiles/extend_kernel.cached_prefix_extend.md"),
 }
 
