@@ -114,7 +114,41 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
     return r;
 }
 
+// 2^x for a pair, on the FMA pipe instead of the exp unit (Cody-Waite range
+// reduction): x = n + f with n = round(x) (read from the low mantissa bits of
+// x + 1.5 * 2^23) and f in [-1/2, 1/2]; 2^f from a cubic fitted to 2^f on
+// [-1/2, 1/2] by least squares at Chebyshev nodes (largest relative error
+// 7.5e-5 in fp32, below bf16's 2^-9); 2^n added to the exponent bits.
+// Inputs below -125, -inf included, give exactly 0; inputs must be < 127.
+__device__ __forceinline__ void poly_exp2_pair(float x0, float x1, float &e0, float &e1)
+{
+    constexpr float kRound = 12582912.f;  // 1.5 * 2^23
+    const uint64_t x = f2(fmaxf(x0, -127.f), fmaxf(x1, -127.f));
+    const uint64_t t = f2_add(x, f2(kRound, kRound));
+    const uint64_t r = f2_add(t, f2(-kRound, -kRound));              // round(x)
+    const uint64_t fr = f2_fma(r, f2(-1.f, -1.f), x);                // x - round(x)
+    uint64_t p = f2_fma(f2(0.055171623826026917f, 0.055171623826026917f), fr,
+                        f2(0.2426111251115799f, 0.2426111251115799f));
+    p = f2_fma(p, fr, f2(0.6932609677314758f, 0.6932609677314758f));
+    p = f2_fma(p, fr, f2(0.9999280571937561f, 0.9999280571937561f));
+    float t0, t1, p0, p1;
+    f2_split(t, t0, t1);
+    f2_split(p, p0, p1);
+    // low mantissa bits of t = round(x) + 2^22 (mod 2^23); shifting them into
+    // the exponent field and removing the 2^22 offset adds round(x) to it
+    const int n0 = (__float_as_int(t0) << 23), n1 = (__float_as_int(t1) << 23);
+    constexpr int kOff = (int)(0x400000u << 23);  // 2^22 << 23 (wraps to 0)
+    e0 = x0 < -125.f ? 0.f : __int_as_float(__float_as_int(p0) + n0 - kOff);
+    e1 = x1 < -125.f ? 0.f : __int_as_float(__float_as_int(p1) + n1 - kOff);
+}
+
 // ---- mbarrier (shared::cta) ------------------------------------------------
+
+// Time budget of every wait in the kernels, in SM cycles (clock64): about a
+// second at 2 GHz.  A wait is bounded by time, not by a number of polls,
+// since one mbarrier.try_wait may itself suspend the thread for a while.
+constexpr long long kWaitCycles = 1ll << 31;
+
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
@@ -197,20 +231,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
-// Per-warpgroup register reallocation: every warp of a warpgroup executes the
-// same call; an increase waits until decreases elsewhere in the CTA have
-// released enough of the registers the CTA was launched with.
-template <uint32_t N>
-__device__ __forceinline__ void reg_alloc()
-{
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void reg_dealloc()
-{
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
-}
-
 // ---- tcgen05 (5th-generation tensor cores, accumulators in TMEM) ------------
 
 // Allocates `ncols` TMEM columns (power of two >= 32) for this CTA; the base
@@ -258,6 +278,18 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// The same with the A operand in tensor memory: a_tmem addresses M lanes
+// (rows) by K / 2 columns, each 32-bit column holding two consecutive bf16
+// of a row (lower half first).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // The barrier gets one arrival when every tcgen05.mma issued so far by this

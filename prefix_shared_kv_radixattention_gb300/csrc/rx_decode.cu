@@ -67,7 +67,6 @@ constexpr int kConsumer0 = 32 * (1 + kCopiers);  // first consumer thread
 constexpr int kMaxRows = 64;                 // query rows per item
 constexpr int kNIT = 4;                      // item descriptor ring
 constexpr int kNSL = 16;                     // slot-id ring (stages)
-constexpr uint32_t kSpinLimit = 1u << 22;    // polls before a wait gives up
 
 // Item descriptor published by the scheduler warp.  M == 0 ends the stream.
 struct Desc {
@@ -176,13 +175,14 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
                                               int32_t *status)
 {
     bool ok = false;
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    const long long t0 = clock64();
+    do {
         if (rx::mbar_try_wait(bar, parity)) {
             ok = true;
             break;
         }
         if (*abort_flag) break;
-    }
+    } while (clock64() - t0 < rx::kWaitCycles);
     if (!ok && !*abort_flag) {
         *abort_flag = 1;
         if (status) atomicOr(status, RX_DEV_TIMEOUT);
@@ -754,8 +754,10 @@ static_assert(WideLayout::OFF_V % 128 == 0 && WideLayout::OFF_Q % 128 == 0 && Wi
 // issued land before the CTA exits
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int32_t *status)
 {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
+    const long long t0 = clock64();
+    do {
         if (rx::mbar_try_wait(bar, parity)) return;
+    } while (clock64() - t0 < rx::kWaitCycles);
     if (status) atomicOr(status, RX_DEV_TIMEOUT);
 }
 

@@ -44,6 +44,7 @@
 #include <math.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "rx_common.cuh"
 
@@ -54,28 +55,21 @@ using bf16 = __nv_bfloat16;
 constexpr int kQT = 2;              // Q tiles per CTA
 constexpr int kRows = 128;          // query rows per Q tile (MMA M)
 constexpr int kCtaRows = kQT * kRows;
-constexpr int kBN = 64;             // keys per K/V tile (MMA N of S)
-constexpr int kStages = 3;          // K/V ring depth
+constexpr int kBN = 128;            // keys per K/V tile (MMA N of S, MMA K of P V)
+constexpr int kStages = 2;          // K ring and V ring depth
 constexpr int kLag = kStages - 1;   // slot-id prefetch distance (tiles)
 constexpr int kNSL = kLag + 1;      // slot-id ring (tiles)
-constexpr int kProducer0 = 256;     // producer threads: warps 8-14
-constexpr int kProducers = 224;
-constexpr int kMmaWarp = 15;
-constexpr int kThreads = 32 * 16;
-// registers: launched at 65536 / 512 = 128 a thread; the two softmax
-// warpgroups take 184, the producer / MMA warpgroups give back to 72
-// (2 x 128 x 184 + 2 x 128 x 72 = 65536)
-constexpr uint32_t kRegSoftmax = 184;
-constexpr uint32_t kRegOther = 72;
-static_assert(2 * 128 * kRegSoftmax + 2 * 128 * kRegOther == 65536, "register split");
+constexpr int kProducer0 = 256;     // producer threads: warps 8-10
+constexpr int kProducers = 96;
+constexpr int kMmaWarp = 11;
+constexpr int kThreads = 32 * 12;   // no register reallocation: every warp keeps the launch count
 // staged path (contexts copied into a workspace first): one TMA thread feeds
 // the ring, so the CTA is 8 softmax warps + a producer warp + the MMA warp
 constexpr int kStagedThreads = 32 * 10;
 constexpr int kStagedProducerWarp = 8;
 constexpr int kStagedMmaWarp = 9;
 constexpr int kStageBlock = 16;    // rows per copy unit of the staging kernel
-constexpr uint32_t kSpinLimit = 1u << 22;
-constexpr uint32_t kTmemCols = 512;  // per Q tile t: S0 [256t, +64), S1 [+64, +128), O [+128, +256)
+constexpr uint32_t kTmemCols = 512;  // per Q tile t: S (then P as bf16) [256t, +128), O [256t + 128, +128)
 constexpr float kRescale = 8.f;      // log2 units the running max may lag
 
 template <int D>
@@ -86,18 +80,15 @@ struct XL {
     static constexpr int OFF_Q = 0;              // kQT tiles x NB blocks
     static constexpr int OFF_K = OFF_Q + kQT * NB * QBLK;
     static constexpr int OFF_V = OFF_K + kStages * NB * KBLK;
-    static constexpr int OFF_P = OFF_V + kStages * NB * KBLK;  // [Q tile][2 buffers] x 128 x 64
-    static constexpr int OFF_SLOT = OFF_P + kQT * 2 * QBLK;    // slot-id ring
+    static constexpr int OFF_SLOT = OFF_V + kStages * NB * KBLK;  // slot-id ring
     static constexpr int OFF_BAR = OFF_SLOT + kNSL * kBN * 4;
     // per Q tile: q_full; per stage: k_full, v_full, k_empty (S read it),
-    // v_empty (O += P V read it); per Q tile and buffer: s_full, s_free,
-    // p_full (softmax wrote P), pv_done
+    // v_empty (O += P V read it); per Q tile: s_full (S in TMEM), p_full
+    // (P written over S), pv_done (O += P V finished, S/P columns free)
     static constexpr int B_QFULL = 0, B_KFULL = kQT, B_VFULL = B_KFULL + kStages,
                          B_KEMPTY = B_VFULL + kStages, B_VEMPTY = B_KEMPTY + kStages,
-                         B_SFULL = B_VEMPTY + kStages,
-                         B_SFREE = B_SFULL + 2 * kQT, B_PFULL = B_SFREE + 2 * kQT,
-                         B_PVDONE = B_PFULL + 2 * kQT, B_FINAL = B_PVDONE + 2 * kQT,
-                         N_BAR = B_FINAL + 1;
+                         B_SFULL = B_VEMPTY + kStages, B_PFULL = B_SFULL + kQT,
+                         B_PVDONE = B_PFULL + kQT, B_FINAL = B_PVDONE + kQT, N_BAR = B_FINAL + 1;
     static constexpr int OFF_TMEM = OFF_BAR + N_BAR * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 8;
     static constexpr int BYTES = OFF_ABORT + 8 + 1024;  // + room to align the base to 1024
@@ -146,10 +137,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
                                               int32_t *status)
 {
     if (rx::mbar_test_wait(bar, parity)) return true;  // already flipped: no suspend
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    const long long t0 = clock64();
+    do {
         if (rx::mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-    }
+    } while (clock64() - t0 < rx::kWaitCycles);
     *abort_flag = 1;
     if (status) atomicOr(status, RX_DEV_TIMEOUT);
     return false;
@@ -175,8 +167,10 @@ __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 // issued finish landing before the CTA exits.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int32_t *status)
 {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
+    const long long t0 = clock64();
+    do {
         if (rx::mbar_try_wait(bar, parity)) return;
+    } while (clock64() - t0 < rx::kWaitCycles);
     if (status) atomicOr(status, RX_DEV_TIMEOUT);
 }
 
@@ -196,9 +190,10 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
 
     // slot ids of tile j -> slot ring entry j % kNSL (4-byte async copies)
     auto fetch_slots = [&](int j) {
-        if (j < T.ntiles && pt < kBN) {
-            const int pos = j * kBN + pt;
-            rx::cp_async_4(sbase + L::OFF_SLOT + ((j % kNSL) * kBN + pt) * 4,
+        if (j >= T.ntiles) return;
+        for (int r = pt; r < kBN; r += kProducers) {
+            const int pos = j * kBN + r;
+            rx::cp_async_4(sbase + L::OFF_SLOT + ((j % kNSL) * kBN + r) * 4,
                            T.slots + (pos < T.kv_end ? pos : 0), pos < T.kv_end ? 4 : 0);
         }
     };
@@ -313,63 +308,58 @@ __device__ void mma_issuer(const XParams &p, const Tile &T, unsigned char *smem,
     const uint64_t dq = rx::sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
     const uint64_t dk = rx::sdesc_sw128(sbase + L::OFF_K, 16, 1024);
     const uint64_t dv = rx::sdesc_sw128(sbase + L::OFF_V, L::KBLK, 1024);
-    const uint64_t dp = rx::sdesc_sw128(sbase + L::OFF_P, 16, 1024);
 
-    // S_j = Q K_j^T for every Q tile into S buffer j & 1; then K stage j is free
-    auto issue_s = [&](int j) -> bool {
-        const int st = j % kStages, sb = j & 1;
+    // Per Q tile t the work is a chain: S_t(j) = Q_t K_j^T into its TMEM
+    // columns, the softmax overwrites them with P_t(j) (bf16), O_t +=
+    // P_t(j) V_j reads P from TMEM, and only then may S_t(j + 1) reuse the
+    // columns.  The two tiles are staggered by half a step, so each tile's
+    // softmax overlaps tensor-core work of the other tile and the two
+    // softmaxes do not contend for the exp unit:
+    //   S_0(0) | P V_1(j - 1), S_1(j), P V_0(j), S_0(j + 1) | ... | P V_1(n - 1)
+    auto issue_s = [&](int t, int j) -> bool {
+        const int st = j % kStages;
         if (!wait(L::B_KFULL + st, (j / kStages) & 1)) return false;
-        for (int t = 0; t < T.nqt; ++t)
-            if (j == 0 && !wait(L::B_QFULL + t, 0)) return false;
-        // buffer sb was last read by the softmax of tile j - 2 (both Q tiles
-        // arrive on one barrier)
-        if (j >= 2 && !wait(L::B_SFREE + sb, ((j >> 1) - 1) & 1)) return false;
+        if (j == 0 ? !wait(L::B_QFULL + t, 0) : !wait(L::B_PVDONE + t, (j - 1) & 1)) return false;
         if (!kStaged) rx::fence_proxy_async_smem();  // K rows landed by cp.async -> async proxy
         rx::tc_fence_after();
         const uint64_t dks = dk + (uint64_t)((st * L::NB * L::KBLK) >> 4);
-        for (int t = 0; t < T.nqt; ++t) {
-            const uint64_t dqt = dq + (uint64_t)((t * L::NB * L::QBLK) >> 4);
+        const uint64_t dqt = dq + (uint64_t)((t * L::NB * L::QBLK) >> 4);
 #pragma unroll
-            for (int kb = 0; kb < D / 16; ++kb) {
-                rx::tc_mma(tmem + t * 256 + sb * kBN, dqt + (uint64_t)(((kb >> 2) * L::QBLK + (kb & 3) * 32) >> 4),
-                           dks + (uint64_t)(((kb >> 2) * L::KBLK + (kb & 3) * 32) >> 4), idesc_qk, kb > 0);
-            }
-            rx::tc_commit(bar + 8 * (L::B_SFULL + 2 * t + sb));
-        }
-        rx::tc_commit(bar + 8 * (L::B_KEMPTY + st));
+        for (int kb = 0; kb < D / 16; ++kb)
+            rx::tc_mma(tmem + t * 256, dqt + (uint64_t)(((kb >> 2) * L::QBLK + (kb & 3) * 32) >> 4),
+                       dks + (uint64_t)(((kb >> 2) * L::KBLK + (kb & 3) * 32) >> 4), idesc_qk, kb > 0);
+        rx::tc_commit(bar + 8 * (L::B_SFULL + t));
+        // the last tile to read K_j releases its stage
+        if (t == T.nqt - 1) rx::tc_commit(bar + 8 * (L::B_KEMPTY + st));
         return true;
     };
-    // O_t += P_t,j V_j once the softmax of every Q tile has written P_t,j
-    // (one barrier for both tiles) and V_j has landed
-    auto issue_pv = [&](int j, int t) -> bool {
-        const int pb = j & 1;
-        if (t == 0) {
-            if (!wait(L::B_PFULL + pb, (j >> 1) & 1)) return false;
-            if (!wait(L::B_VFULL + j % kStages, (j / kStages) & 1)) return false;
-            if (!kStaged) rx::fence_proxy_async_smem();  // V rows landed by cp.async
-        }
+    auto issue_pv = [&](int t, int j) -> bool {
+        const int st = j % kStages;
+        if (!wait(L::B_PFULL + t, j & 1)) return false;
+        if (!wait(L::B_VFULL + st, (j / kStages) & 1)) return false;
+        if (!kStaged) rx::fence_proxy_async_smem();  // V rows landed by cp.async
         rx::tc_fence_after();
-        const uint64_t dvs = dv + (uint64_t)(((j % kStages) * L::NB * L::KBLK) >> 4);
-        const uint64_t dps = dp + (uint64_t)(((2 * t + pb) * L::QBLK) >> 4);
+        const uint64_t dvs = dv + (uint64_t)((st * L::NB * L::KBLK) >> 4);
+        // A = P_t(j) in TMEM: 16 keys per MMA = 8 columns of bf16 pairs
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks)
-            rx::tc_mma(tmem + t * 256 + 128, dps + (uint64_t)((ks * 32) >> 4), dvs + (uint64_t)((ks * 16 * 128) >> 4),
-                       idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
-        rx::tc_commit(bar + 8 * (L::B_PVDONE + 2 * t + pb));
+            rx::tc_mma_ts(tmem + t * 256 + 128, tmem + t * 256 + ks * 8, dvs + (uint64_t)((ks * 16 * 128) >> 4),
+                          idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+        rx::tc_commit(bar + 8 * (L::B_PVDONE + t));
+        if (t == T.nqt - 1) rx::tc_commit(bar + 8 * (L::B_VEMPTY + st));
         return true;
     };
-    // a fixed order, each wait suspending the thread until its barrier
-    // flips: S_{j+1} goes ahead of O += P_j V_j so that the softmax of tile
-    // j + 1 can start while the tensor core finishes tile j
-    if (issue_s(0)) {
-        for (int j = 0; j < T.ntiles; ++j) {
-            if (j + 1 < T.ntiles && !issue_s(j + 1)) break;
-            bool ok = true;
-            for (int t = 0; t < T.nqt && ok; ++t) ok = issue_pv(j, t);
-            if (!ok) break;
-            rx::tc_commit(bar + 8 * (L::B_VEMPTY + j % kStages));
+    const bool two = T.nqt == 2;
+    bool ok = issue_s(0, 0);
+    for (int j = 0; j < T.ntiles && ok; ++j) {
+        if (two) {
+            if (j > 0 && !(ok = issue_pv(1, j - 1))) break;
+            if (!(ok = issue_s(1, j))) break;
         }
+        if (!(ok = issue_pv(0, j))) break;
+        if (j + 1 < T.ntiles && !(ok = issue_s(0, j + 1))) break;
     }
+    if (ok && two) issue_pv(1, T.ntiles - 1);
     // everything issued has finished before TMEM is released
     rx::tc_commit(bar + 8 * L::B_FINAL);
     drain_wait(bar + 8 * L::B_FINAL, 0, p.status);
@@ -416,38 +406,54 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
         rx::mbar_arrive(bar + 8 * (L::B_QFULL + t));
     }
     float m_used = -INFINITY, l = 0.f;
+    const uint32_t tS = tbase;  // S_t(j), then P_t(j) over its first kBN / 2 columns
     for (int j = 0; j < T.ntiles; ++j) {
-        const int sb = j & 1;
-        if (!warp_wait(bar + 8 * (L::B_SFULL + 2 * t + sb), (j >> 1) & 1, abort_flag, p.status)) return;
+        if (!warp_wait(bar + 8 * (L::B_SFULL + t), j & 1, abort_flag, p.status)) return;
         rx::tc_fence_after();
         const int kbase = j * kBN;
-        const bool need_mask = kbase + kBN - 1 > row_lim;
-        uint32_t sv[kBN];  // this row's scores of the tile, loaded once
-        rx::tmem_ld32(tbase + sb * kBN, *reinterpret_cast<uint32_t(*)[32]>(sv));
-        rx::tmem_ld32(tbase + sb * kBN + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-        rx::tmem_wait_ld();
-        if (need_mask) {  // keys past the causal bound: -inf, so their weight is exactly 0
+        // one answer per warp: the masked and unmasked passes below hold
+        // different warp-collective tcgen05.ld instructions, so all lanes of
+        // a warp must take the same one (the masked pass is exact for every row)
+        const bool need_mask = __any_sync(0xffffffffu, kbase + kBN - 1 > row_lim);
+        // pass 1: the row max over the tile's visible keys, 64 scores (two
+        // loads in flight) at a time; the causal test only on tiles that
+        // cross the row's bound
+        float mx = -INFINITY;
+        auto max_pass = [&](auto masked) {
 #pragma unroll
-            for (int k = 0; k < kBN; ++k)
-                if (kbase + k > row_lim) sv[k] = __float_as_uint(-INFINITY);
-        }
-        // row max as a tree (max is exact, so the order does not matter)
-        float mt[kBN / 2];
+            for (int hf = 0; hf < kBN / 64; ++hf) {
+                uint32_t sv[64];
+                rx::tmem_ld32(tS + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
+                rx::tmem_ld32(tS + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+                rx::tmem_wait_ld();
+                float mt[32];
 #pragma unroll
-        for (int k = 0; k < kBN / 2; ++k) mt[k] = fmaxf(u2f(sv[k]), u2f(sv[k + kBN / 2]));
+                for (int k = 0; k < 32; ++k) {
+                    float a = u2f(sv[k]), b2 = u2f(sv[k + 32]);
+                    if (decltype(masked)::value) {
+                        const int k0 = kbase + hf * 64 + k;
+                        a = k0 <= row_lim ? a : -INFINITY;
+                        b2 = k0 + 32 <= row_lim ? b2 : -INFINITY;
+                    }
+                    mt[k] = fmaxf(a, b2);
+                }
 #pragma unroll
-        for (int w = kBN / 4; w >= 1; w >>= 1)
+                for (int w = 16; w >= 1; w >>= 1)
 #pragma unroll
-            for (int k = 0; k < w; ++k) mt[k] = fmaxf(mt[k], mt[k + w]);
-        const float m_new = fmaxf(m_used, mt[0] * sl2);
+                    for (int k = 0; k < w; ++k) mt[k] = fmaxf(mt[k], mt[k + w]);
+                mx = fmaxf(mx, mt[0]);
+            }
+        };
+        if (need_mask)
+            max_pass(std::true_type{});
+        else
+            max_pass(std::false_type{});
+        const float m_new = fmaxf(m_used, mx * sl2);
         const bool need = (m_used == -INFINITY) || (m_new > m_used + kRescale);
         const float alpha = (need && m_used != -INFINITY) ? rx::fast_exp2(m_used - m_new) : 1.f;
         if (j > 0 && __any_sync(0xffffffffu, need)) {
-            // rescale O rows in TMEM once every O += P V so far has finished
-            if (!warp_wait(bar + 8 * (L::B_PVDONE + 2 * t + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag,
-                           p.status))
-                return;
-            rx::tc_fence_after();
+            // rescale the O rows in TMEM: O += P V of tile j - 1 finished
+            // before S_t(j) was issued, and the next one waits for p_full
 #pragma unroll
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 uint32_t r[32];
@@ -463,42 +469,60 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
             l *= alpha;
             m_used = m_new;
         }
-        // P buffer j & 1 of this Q tile was last read by O += P_{j-2} V_{j-2}
-        if (j >= 2 && !warp_wait(bar + 8 * (L::B_PVDONE + 2 * t + sb), ((j >> 1) - 1) & 1, abort_flag,
-                                 p.status))
-            return;
-        // P = 2^(s sl2 - m): the scaling as packed pairs, 2^x on the MUFU, the
-        // row sum in four independent packed accumulators
+        // pass 2: P = 2^(s sl2 - m) as bf16 pairs written back over the S
+        // columns already read (64 scores -> 32 columns at a time), the row
+        // sum in four packed accumulators.  Half of the exponentials go to
+        // the exp unit, half to a polynomial on the FMA pipe: the exp unit
+        // alone would take as long as all the tensor-core work.
         const float mu = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t scale2 = rx::f2(sl2, sl2), negm2 = rx::f2(-mu, -mu);
         uint64_t acc[4] = {0, 0, 0, 0};
-        unsigned char *prow = smem + L::OFF_P + (2 * t + sb) * L::QBLK;
+        auto exp_pass = [&](auto masked) {
 #pragma unroll
-        for (int q = 0; q < kBN / 8; ++q) {  // 8 keys -> one 16-byte chunk of the P row
-            uint32_t pk[4];
+            for (int c2 = 0; c2 < kBN / 64; ++c2) {
+                uint32_t sv[64];
+                rx::tmem_ld32(tS + c2 * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
+                rx::tmem_ld32(tS + c2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+                rx::tmem_wait_ld();
+                uint32_t pk[32];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int key = q * 8 + 2 * k;
-                float x0, x1;
-                rx::f2_split(rx::f2_fma(rx::f2(u2f(sv[key]), u2f(sv[key + 1])), scale2, negm2), x0, x1);
-                const float e0 = rx::fast_exp2(x0), e1 = rx::fast_exp2(x1);
-                acc[k] = rx::f2_add(acc[k], rx::f2(e0, e1));
-                pk[k] = rx::pack_bf16(e0, e1);
+                for (int k = 0; k < 32; ++k) {
+                    float s0 = u2f(sv[2 * k]), s1 = u2f(sv[2 * k + 1]);
+                    if (decltype(masked)::value) {
+                        const int key = kbase + c2 * 64 + 2 * k;
+                        s0 = key <= row_lim ? s0 : -INFINITY;
+                        s1 = key + 1 <= row_lim ? s1 : -INFINITY;
+                    }
+                    float x0, x1, e0, e1;
+                    rx::f2_split(rx::f2_fma(rx::f2(s0, s1), scale2, negm2), x0, x1);
+                    if (k & 1) {
+                        rx::poly_exp2_pair(x0, x1, e0, e1);
+                    } else {
+                        e0 = rx::fast_exp2(x0);
+                        e1 = rx::fast_exp2(x1);
+                    }
+                    acc[k & 3] = rx::f2_add(acc[k & 3], rx::f2(e0, e1));
+                    pk[k] = rx::pack_bf16(e0, e1);
+                }
+                // columns c2 * 32 .. c2 * 32 + 31 hold scores already loaded above
+                rx::tmem_st32(tS + c2 * 32, pk);
             }
-            *reinterpret_cast<uint4 *>(prow + sw128(rl, q, L::QBLK)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
+        };
+        if (need_mask)
+            exp_pass(std::true_type{});
+        else
+            exp_pass(std::false_type{});
+        rx::tmem_wait_st();
         {
             float a0, a1;
             rx::f2_split(rx::f2_add(rx::f2_add(acc[0], acc[1]), rx::f2_add(acc[2], acc[3])), a0, a1);
             l += a0 + a1;
         }
         rx::tc_fence_before();
-        rx::fence_proxy_async_smem();
-        rx::mbar_arrive(bar + 8 * (L::B_SFREE + sb));
-        rx::mbar_arrive(bar + 8 * (L::B_PFULL + sb));
+        rx::mbar_arrive(bar + 8 * (L::B_PFULL + t));
     }
     const int jl = T.ntiles - 1;
-    if (!warp_wait(bar + 8 * (L::B_PVDONE + 2 * t + (jl & 1)), (jl >> 1) & 1, abort_flag, p.status)) return;
+    if (!warp_wait(bar + 8 * (L::B_PVDONE + t), jl & 1, abort_flag, p.status)) return;
     rx::tc_fence_after();
     const bool valid = row < T.M;
     const int G = p.G;
@@ -580,10 +604,9 @@ __global__ void __launch_bounds__(kStaged ? kStagedThreads : kThreads, 1)
             rx::mbar_init(bar + 8 * (L::B_KEMPTY + i), 1);  // MMA commits
             rx::mbar_init(bar + 8 * (L::B_VEMPTY + i), 1);
         }
-        for (int i = 0; i < 2 * kQT; ++i) {
+        for (int i = 0; i < kQT; ++i) {
             rx::mbar_init(bar + 8 * (L::B_SFULL + i), 1);     // MMA commit
-            rx::mbar_init(bar + 8 * (L::B_SFREE + i), 128 * T.nqt);  // softmax threads of every Q tile (i < 2)
-            rx::mbar_init(bar + 8 * (L::B_PFULL + i), 128 * T.nqt);  // i < 2 used, as s_free
+            rx::mbar_init(bar + 8 * (L::B_PFULL + i), 128);   // the tile's softmax threads
             rx::mbar_init(bar + 8 * (L::B_PVDONE + i), 1);    // MMA commit
         }
         rx::mbar_init(bar + 8 * L::B_FINAL, 1);
@@ -597,10 +620,8 @@ __global__ void __launch_bounds__(kStaged ? kStagedThreads : kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::OFF_TMEM);
 
     if (warp < 8) {
-        if (!kStaged) rx::reg_alloc<kRegSoftmax>();  // warpgroups 0-1, one program point
         softmax_rows<D>(p, T, smem, sbase, tmem);
     } else {
-        if (!kStaged) rx::reg_dealloc<kRegOther>();  // warpgroups 2-3, one program point
         if (warp < mma_warp) {
             if (!kStaged) {
                 producer<D>(p, T, smem, sbase);
