@@ -14,31 +14,31 @@
 //
 //   - a CTA owns 256 query rows: 256 / G new tokens of one request times the
 //     G q-heads of one kv head (rows token-major), as two 128-row tensor-core
-//     tiles that share every gathered K/V tile -- the gather through the slot
-//     list, not the tensor core, is the scarce resource, so each gathered
-//     byte feeds as many rows as TMEM holds accumulators for;
-//   - three producer warps gather K and V rows through the slot list with
-//     16-byte cp.async straight into the 128-byte-swizzled K-major layout the
-//     tensor core reads, into a 3-stage ring of 64-key tiles; slot ids are
-//     prefetched two tiles ahead (4-byte cp.async into a small ring); each
-//     stage's mbarrier is completed by the copies themselves
-//     (cp.async.mbarrier.arrive), and the MMA thread fences the landed rows
-//     into the async proxy before the tensor core reads them;
-//   - one thread issues, per Q tile, S = Q K^T (M = 128, N = 64 keys, K =
-//     head_dim) into one of two TMEM S buffers and O += P V (N = head_dim,
-//     K = 64 keys, V read MN-major) into a TMEM O accumulator, in whatever
-//     order their inputs become ready; tcgen05.commit signals each result on
-//     an mbarrier, and a K/V stage is released once both tiles' O += P V of
-//     it are done;
+//     tiles that share every K/V tile of 128 keys;
+//   - K and V reach shared memory, in the 128-byte-swizzled layout the tensor
+//     core reads, by one of two producers: with a workspace, a staging kernel
+//     first packs each request's context rows and one thread streams them with
+//     tiled TMA loads; without one, three warps gather rows through the slot
+//     list with 16-byte cp.async (slot ids prefetched into a small ring).  K
+//     and V have rings of their own: a K stage frees as soon as S has read it;
+//   - per Q tile t, S_t = Q_t K^T (M = 128, N = 128 keys) lands in 128 TMEM
+//     columns; the softmax overwrites them with P_t as bf16 pairs, and O_t +=
+//     P_t V (A operand read from TMEM, V MN-major) accumulates in another 128
+//     columns -- P never touches shared memory.  S_t(j + 1) may reuse the
+//     columns only after O_t += P_t(j) V_j has read them, so the MMA thread
+//     staggers the two tiles by half a step (S_0, PV_1, S_1, PV_0, ...): each
+//     tile's softmax overlaps the other tile's tensor-core work;
 //   - eight softmax warps (four per Q tile, one TMEM lane quadrant and one
-//     row per thread) load each row's 64 scores once with tcgen05.ld, mask
-//     the causal bound on diagonal tiles, keep the running max in the exp2
-//     domain, write P = 2^(s - m) as bf16 into a double-buffered swizzled
-//     shared-memory tile (the A operand of the second GEMM) and rescale O in
-//     TMEM only when the row max grew by more than 2^8.
-// Every mbarrier wait is bounded: a wait that gives up sets RX_DEV_TIMEOUT
-// and raises an abort flag; every role then runs to the common exit, where
-// the MMA thread waits for its last tensor-core work and TMEM is freed.
+//     row per thread) read the row's scores 64 at a time (tcgen05.ld), take
+//     the row max, then write P = 2^(s - m) back over the scores, half of the
+//     exponentials on the exp unit and half by a polynomial on the FMA pipe;
+//     the causal test runs only on warps holding a row that crosses its
+//     bound, and O is rescaled in TMEM only when the row max grew by more
+//     than 2^8.
+// Every mbarrier wait is bounded in time: a wait that gives up sets
+// RX_DEV_TIMEOUT and raises an abort flag; every role then runs to the common
+// exit, where the MMA thread waits for its last tensor-core work and TMEM is
+// freed.  Warp-collective TMEM accesses always sit on warp-uniform paths.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -251,8 +251,8 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
 
 // Staged path: one thread streams tile j of the request's packed context with
 // four (D = 128) or two (D = 64) TMA box loads -- K and V, one box per
-// 128-byte column block, each box 64 rows of one kv head.  Every packed
-// region is a whole number of 64-row tiles with zeroed padding, so the boxes
+// 128-byte column block, each box kBN rows of one kv head.  Every packed
+// region is a whole number of kBN-row tiles with zeroed padding, so the boxes
 // never leave the request's region.
 template <int D>
 __device__ void tma_producer(const XParams &p, const Tile &T, unsigned char *smem, uint32_t sbase)
@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(kStaged ? kStagedThreads : kThreads, 1)
 // ---------------------------------------------------------------------------
 
 // Packed rows of request b: its context (prefix + extend tokens) rounded up
-// to whole 64-row tiles; none for lengths the attention kernel rejects.
+// to whole kBN-row tiles; none for lengths the attention kernel rejects.
 __device__ __forceinline__ int64_t staged_rows(const int32_t *prefix_len, const int32_t *extend_len, int b,
                                                int64_t rtt_stride)
 {
@@ -703,9 +703,9 @@ __global__ void __launch_bounds__(1024) ctx_offsets_kernel(const int32_t *prefix
 
 // Packed row offs[b] + pos = pool row req_to_token[req_idx[b]][pos] for K and
 // V (all kv heads: one contiguous row of the pool each), zeros from the end of
-// the context to the 64-row boundary and for slot ids outside the pool
+// the context to the kBN-row boundary and for slot ids outside the pool
 // (flagged).  One warp per block of kStageBlock rows; every request's region
-// is a multiple of 64 rows, so a block never straddles two requests.
+// is a multiple of kBN rows, so a block never straddles two requests.
 __global__ void __launch_bounds__(256) stage_rows_kernel(
     const bf16 *__restrict__ k_pool, const bf16 *__restrict__ v_pool, int64_t num_slots,
     const int32_t *__restrict__ rtt, int64_t rtt_stride, const int32_t *__restrict__ req_idx,
@@ -923,7 +923,7 @@ extern "C" size_t rx_attn_extend_workspace(int64_t total_ctx_tokens, int32_t bat
         rx_set_error(RX_ERR_INVALID, "rx_attn_extend_workspace: invalid argument");
         return 0;
     }
-    const int64_t cap = total_ctx_tokens + (int64_t)(kBN - 1) * batch;  // each context rounded up to 64 rows
+    const int64_t cap = total_ctx_tokens + (int64_t)(kBN - 1) * batch;  // each context rounded up to kBN rows
     if (cap > (int64_t)INT32_MAX - 2 * kBN) {
         rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_extend_workspace: %lld context rows", (long long)cap);
         return 0;
