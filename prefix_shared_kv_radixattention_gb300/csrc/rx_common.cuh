@@ -119,11 +119,11 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
 // x + 1.5 * 2^23) and f in [-1/2, 1/2]; 2^f from a cubic fitted to 2^f on
 // [-1/2, 1/2] by least squares at Chebyshev nodes (largest relative error
 // 7.5e-5 in fp32, below bf16's 2^-9); 2^n added to the exponent bits.
-// Inputs below -125, -inf included, give exactly 0; inputs must be < 127.
+// Inputs are finite and below 127; inputs below -125 give 2^-125 (not 0).
 __device__ __forceinline__ void poly_exp2_pair(float x0, float x1, float &e0, float &e1)
 {
     constexpr float kRound = 12582912.f;  // 1.5 * 2^23
-    const uint64_t x = f2(fmaxf(x0, -127.f), fmaxf(x1, -127.f));
+    const uint64_t x = f2(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
     const uint64_t t = f2_add(x, f2(kRound, kRound));
     const uint64_t r = f2_add(t, f2(-kRound, -kRound));              // round(x)
     const uint64_t fr = f2_fma(r, f2(-1.f, -1.f), x);                // x - round(x)
@@ -134,12 +134,19 @@ __device__ __forceinline__ void poly_exp2_pair(float x0, float x1, float &e0, fl
     float t0, t1, p0, p1;
     f2_split(t, t0, t1);
     f2_split(p, p0, p1);
-    // low mantissa bits of t = round(x) + 2^22 (mod 2^23); shifting them into
-    // the exponent field and removing the 2^22 offset adds round(x) to it
-    const int n0 = (__float_as_int(t0) << 23), n1 = (__float_as_int(t1) << 23);
-    constexpr int kOff = (int)(0x400000u << 23);  // 2^22 << 23 (wraps to 0)
-    e0 = x0 < -125.f ? 0.f : __int_as_float(__float_as_int(p0) + n0 - kOff);
-    e1 = x1 < -125.f ? 0.f : __int_as_float(__float_as_int(p1) + n1 - kOff);
+    // the low mantissa bits of t hold round(x) + 2^22; times 2^23 (mod 2^32)
+    // that is round(x) in the exponent field (the 2^22 and the exponent of t
+    // overflow away), added to p's bits in one integer multiply-add
+    // (unsigned: the overflow is the point)
+    e0 = __uint_as_float(__float_as_uint(t0) * (1u << 23) + __float_as_uint(p0));
+    e1 = __uint_as_float(__float_as_uint(t1) * (1u << 23) + __float_as_uint(p1));
+}
+// Largest of three (one instruction).
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // ---- mbarrier (shared::cta) ------------------------------------------------

@@ -420,29 +420,32 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
         // cross the row's bound
         float mx = -INFINITY;
         auto max_pass = [&](auto masked) {
+            float mt0 = -INFINITY;
 #pragma unroll
             for (int hf = 0; hf < kBN / 64; ++hf) {
                 uint32_t sv[64];
                 rx::tmem_ld32(tS + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
                 rx::tmem_ld32(tS + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
                 rx::tmem_wait_ld();
-                float mt[32];
+                if (decltype(masked)::value) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    float a = u2f(sv[k]), b2 = u2f(sv[k + 32]);
-                    if (decltype(masked)::value) {
-                        const int k0 = kbase + hf * 64 + k;
-                        a = k0 <= row_lim ? a : -INFINITY;
-                        b2 = k0 + 32 <= row_lim ? b2 : -INFINITY;
-                    }
-                    mt[k] = fmaxf(a, b2);
+                    for (int k = 0; k < 64; ++k)
+                        if (kbase + hf * 64 + k > row_lim) sv[k] = __float_as_uint(-INFINITY);
                 }
+                // 64 -> 22 -> 8 -> 3 -> 1 with three-input max
+                float m22[22], m8[8], m3[3];
 #pragma unroll
-                for (int w = 16; w >= 1; w >>= 1)
+                for (int k = 0; k < 21; ++k) m22[k] = rx::fmax3(u2f(sv[3 * k]), u2f(sv[3 * k + 1]), u2f(sv[3 * k + 2]));
+                m22[21] = u2f(sv[63]);
 #pragma unroll
-                    for (int k = 0; k < w; ++k) mt[k] = fmaxf(mt[k], mt[k + w]);
-                mx = fmaxf(mx, mt[0]);
+                for (int k = 0; k < 7; ++k) m8[k] = rx::fmax3(m22[3 * k], m22[3 * k + 1], m22[3 * k + 2]);
+                m8[7] = m22[21];
+                m3[0] = rx::fmax3(m8[0], m8[1], m8[2]);
+                m3[1] = rx::fmax3(m8[3], m8[4], m8[5]);
+                m3[2] = fmaxf(m8[6], m8[7]);
+                mt0 = rx::fmax3(mt0, rx::fmax3(m3[0], m3[1], m3[2]), -INFINITY);
             }
+            mx = mt0;
         };
         if (need_mask)
             max_pass(std::true_type{});
@@ -495,9 +498,9 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
                     }
                     float x0, x1, e0, e1;
                     rx::f2_split(rx::f2_fma(rx::f2(s0, s1), scale2, negm2), x0, x1);
-                    if (k & 1) {
+                    if (!decltype(masked)::value && (k & 1)) {  // finite inputs only
                         rx::poly_exp2_pair(x0, x1, e0, e1);
-                    } else {
+                    } else {  // the exp unit maps -inf to exactly 0
                         e0 = rx::fast_exp2(x0);
                         e1 = rx::fast_exp2(x1);
                     }
