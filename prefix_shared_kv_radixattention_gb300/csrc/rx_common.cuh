@@ -114,33 +114,6 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
     return r;
 }
 
-// 2^x for a pair, on the FMA pipe instead of the exp unit (Cody-Waite range
-// reduction): x = n + f with n = round(x) (read from the low mantissa bits of
-// x + 1.5 * 2^23) and f in [-1/2, 1/2]; 2^f from a cubic fitted to 2^f on
-// [-1/2, 1/2] by least squares at Chebyshev nodes (largest relative error
-// 7.5e-5 in fp32, below bf16's 2^-9); 2^n added to the exponent bits.
-// Inputs are finite and below 127; inputs below -125 give 2^-125 (not 0).
-__device__ __forceinline__ void poly_exp2_pair(float x0, float x1, float &e0, float &e1)
-{
-    constexpr float kRound = 12582912.f;  // 1.5 * 2^23
-    const uint64_t x = f2(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
-    const uint64_t t = f2_add(x, f2(kRound, kRound));
-    const uint64_t r = f2_add(t, f2(-kRound, -kRound));              // round(x)
-    const uint64_t fr = f2_fma(r, f2(-1.f, -1.f), x);                // x - round(x)
-    uint64_t p = f2_fma(f2(0.055171623826026917f, 0.055171623826026917f), fr,
-                        f2(0.2426111251115799f, 0.2426111251115799f));
-    p = f2_fma(p, fr, f2(0.6932609677314758f, 0.6932609677314758f));
-    p = f2_fma(p, fr, f2(0.9999280571937561f, 0.9999280571937561f));
-    float t0, t1, p0, p1;
-    f2_split(t, t0, t1);
-    f2_split(p, p0, p1);
-    // the low mantissa bits of t hold round(x) + 2^22; times 2^23 (mod 2^32)
-    // that is round(x) in the exponent field (the 2^22 and the exponent of t
-    // overflow away), added to p's bits in one integer multiply-add
-    // (unsigned: the overflow is the point)
-    e0 = __uint_as_float(__float_as_uint(t0) * (1u << 23) + __float_as_uint(p0));
-    e1 = __uint_as_float(__float_as_uint(t1) * (1u << 23) + __float_as_uint(p1));
-}
 // Largest of three (one instruction).
 __device__ __forceinline__ float fmax3(float a, float b, float c)
 {

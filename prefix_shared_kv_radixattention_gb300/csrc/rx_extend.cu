@@ -30,8 +30,8 @@
 //     tile's softmax overlaps the other tile's tensor-core work;
 //   - eight softmax warps (four per Q tile, one TMEM lane quadrant and one
 //     row per thread) read the row's scores 64 at a time (tcgen05.ld), take
-//     the row max, then write P = 2^(s - m) back over the scores, half of the
-//     exponentials on the exp unit and half by a polynomial on the FMA pipe;
+//     the row max (three-input max), then write P = 2^(s - m) back over the
+//     scores;
 //     the causal test runs only on warps holding a row that crosses its
 //     bound, and O is rescaled in TMEM only when the row max grew by more
 //     than 2^8.
@@ -474,9 +474,9 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
         }
         // pass 2: P = 2^(s sl2 - m) as bf16 pairs written back over the S
         // columns already read (64 scores -> 32 columns at a time), the row
-        // sum in four packed accumulators.  Half of the exponentials go to
-        // the exp unit, half to a polynomial on the FMA pipe: the exp unit
-        // alone would take as long as all the tensor-core work.
+        // sum in four packed accumulators.  (Measured: moving a share of the
+        // exponentials to a polynomial on the FMA pipe is slower here, since
+        // the softmax is bound by issue and the ALU pipe, not the exp unit.)
         const float mu = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t scale2 = rx::f2(sl2, sl2), negm2 = rx::f2(-mu, -mu);
         uint64_t acc[4] = {0, 0, 0, 0};
@@ -496,14 +496,9 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
                         s0 = key <= row_lim ? s0 : -INFINITY;
                         s1 = key + 1 <= row_lim ? s1 : -INFINITY;
                     }
-                    float x0, x1, e0, e1;
+                    float x0, x1;
                     rx::f2_split(rx::f2_fma(rx::f2(s0, s1), scale2, negm2), x0, x1);
-                    if (!decltype(masked)::value && (k & 1)) {  // finite inputs only
-                        rx::poly_exp2_pair(x0, x1, e0, e1);
-                    } else {  // the exp unit maps -inf to exactly 0
-                        e0 = rx::fast_exp2(x0);
-                        e1 = rx::fast_exp2(x1);
-                    }
+                    const float e0 = rx::fast_exp2(x0), e1 = rx::fast_exp2(x1);  // -inf -> 0
                     acc[k & 3] = rx::f2_add(acc[k & 3], rx::f2(e0, e1));
                     pk[k] = rx::pack_bf16(e0, e1);
                 }
