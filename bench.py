@@ -266,6 +266,8 @@ def run_gpu(args, rank, world, local_rank):
         t_wall = time.perf_counter() - t_wall
     if dist:
         dist.barrier()
+    if int(st.status.item()) != 0:
+        raise RuntimeError(f"device status {int(st.status.item())} after the timed steps")
     step_ms = [a.elapsed_time(b) for a, b in steps_ev]
     part_ms = {k: [m[k][0].elapsed_time(m[k][1]) for m in marks] for k in parts}
     tot_ms = max_over_ranks(sum(step_ms), dist, "cuda")
@@ -275,6 +277,8 @@ def run_gpu(args, rank, world, local_rank):
     if dist:
         dist.barrier()
     e2e = run_e2e(st, torch, rx, args.steps, flush, dist, world)
+    if int(st.status.item()) != 0:
+        raise RuntimeError(f"device status {int(st.status.item())} after the end-to-end steps")
 
     if dist:
         dist.destroy_process_group()
@@ -396,7 +400,6 @@ def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
 # captures summarised in the named profile; an entry is removed whenever its
 # kernel changes, so that an old count is never reported for new code.
 PROFILED_TRAFFIC = {
-    ("few_shot_decode", "decode"): (299_800_000, "profiles/decode_kernel.few_shot_decode.md"),
     ("cached_prefix_extend", "staged"): (584_200_000, "profiles/extend_kernel.cached_prefix_extend.md"),
 }
 

@@ -944,7 +944,9 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
             const int st = j % kWideStages;
             if (!wait_or_abort(bar + 8 * st, (j / kWideStages) & 1, abort_flag, p.status)) return;
             const int2 h = hdr[st];
-            if (h.x != cur) {  // a new item starts (or, with -1, none is left)
+            // a new item starts, or (item -1) none is left -- possibly before
+            // this CTA got any, when the other CTAs drained the queue first
+            if (h.x != cur || h.x < 0) {
                 if (cur >= 0) write_out();
                 if (h.x < 0) break;
                 cur = h.x;

@@ -245,6 +245,22 @@ def test_decode_bad_slot_in_wide_item_is_flagged():
     assert np.isfinite(o).all()
 
 
+def test_decode_wide_ctas_that_find_the_queue_empty():
+    """All-heads CTAs that start after the other CTAs have taken every
+    single-request item end cleanly.  A 4096-position shared segment read as
+    one chunk (three row blocks x eight kv heads: 24 per-head CTAs) holds 24
+    SMs far longer than the 160 short private tails take on the rest, so the
+    all-heads CTAs that wait for those SMs find the work queue empty."""
+    g = _gpu()
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.few_shot_decode(hq=8, hkv=8, d=128, batch=160, shared=4096, private=20, num_slots=8192)
+    buf, info = rx.rx_decode_plan_build(prob.req_to_token, prob.dec_req_idx, prob.dec_seq_len, prob.hq,
+                                        prob.hkv, 4096, 16)
+    assert info.n_wide == 160 and info.n_items - info.n_wide == 3
+    for _ in range(3):
+        _check_decode(prob, plan=True, kv_chunk=4096, g=g)
+
+
 def test_decode_length_past_bound_is_flagged():
     g = _gpu()
     from prefix_shared_kv_radixattention_gb300 import binding as rx
