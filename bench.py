@@ -400,6 +400,7 @@ def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
 # captures summarised in the named profile; an entry is removed whenever its
 # kernel changes, so that an old count is never reported for new code.
 PROFILED_TRAFFIC = {
+    ("few_shot_decode", "decode"): (299_800_000, "profiles/decode_kernel.few_shot_decode.md"),
     ("cached_prefix_extend", "staged"): (584_200_000, "profiles/extend_kernel.cached_prefix_extend.md"),
 }
 
