@@ -647,15 +647,15 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
         kv_chunk = (int32_t)c;
     }
     auto nchunks = [&](int64_t len) { return (len + kv_chunk - 1) / kv_chunk; };
-    // With wide items, a request's own (private) positions are cut by their
-    // own target count, RX_DECODE_TARGET_WIDE_ITEMS over the batch, into
-    // near-equal pieces of at most kv_chunk positions; otherwise into
-    // kv_chunk pieces.
+    // With wide items, a request's own (private) positions are cut into
+    // near-equal pieces: with automatic chunking, of about priv_total /
+    // RX_DECODE_TARGET_WIDE_ITEMS positions (16 .. RX_MAX_KV_CHUNK), else of
+    // at most kv_chunk.  Otherwise they are cut into kv_chunk pieces.
     int64_t priv_total = 0;
     for (int64_t r = 0; r < B; ++r) priv_total += seq_len[order[(size_t)r]] - priv_begin[(size_t)r];
     int64_t pchunk = kv_chunk;
     if (auto_chunk && wide && priv_total > 0)
-        pchunk = std::min<int64_t>(kv_chunk, std::max<int64_t>(RX_DECODE_MIN_WIDE_CHUNK,
+        pchunk = std::min<int64_t>(RX_MAX_KV_CHUNK, std::max<int64_t>(RX_DECODE_MIN_WIDE_CHUNK,
                                    (priv_total + RX_DECODE_TARGET_WIDE_ITEMS - 1) / RX_DECODE_TARGET_WIDE_ITEMS));
     auto npriv = [&](int64_t len) { return (len + pchunk - 1) / pchunk; };
     // start of private piece c of n over len positions: near-equal pieces for
