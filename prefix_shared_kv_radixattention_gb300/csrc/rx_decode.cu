@@ -761,12 +761,24 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int32_
     if (status) atomicOr(status, RX_DEV_TIMEOUT);
 }
 
-// E consecutive bf16 of shared memory as floats (E = 2 or 4: one 4- or
-// 8-byte load)
+// E consecutive bf16 of shared memory as floats (E = 2, 4, 8 or 16: one 4-,
+// 8- or 16-byte load, or two 16-byte loads)
 template <int E>
 __device__ __forceinline__ void load_bf16(const unsigned char *src, float (&out)[E])
 {
-    if constexpr (E == 4) {
+    if constexpr (E == 8 || E == 16) {
+#pragma unroll
+        for (int c = 0; c < E / 8; ++c) {
+            const uint4 r = *reinterpret_cast<const uint4 *>(src + 16 * c);
+            const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[k]));
+                out[8 * c + 2 * k] = f.x;
+                out[8 * c + 2 * k + 1] = f.y;
+            }
+        }
+    } else if constexpr (E == 4) {
         const uint2 r = *reinterpret_cast<const uint2 *>(src);
         const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
         const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
@@ -786,7 +798,6 @@ template <int D, int LOG_NP, int HPW, int CW>
 __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Params p)
 {
     using WL = WideLayout;
-    constexpr int E = D / 32;  // values of a head row per lane
     constexpr int NP = 1 << LOG_NP;  // positions per stage
     extern __shared__ __align__(128) unsigned char wraw[];
     const uint32_t raw = rx::smem_u32(wraw);
@@ -815,10 +826,14 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
         // first served, so a CTA that starts late (behind the per-head kernel
         // running alongside) takes fewer of them.  Each stage's header names
         // its item; a last header with item -1 tells the consumers to stop.
-        // The slot ids of the next stage are loaded before waiting for a free
-        // stage, so their latency is off the copy path.
+        // Under load a global load takes microseconds, so nothing on the copy
+        // path waits for one: a cursor runs three stages ahead of the stage
+        // being issued, and its loads (at an item boundary: the claim, the
+        // item's fields, then slot ids) are made before the wait for a free
+        // stage.  Claims stay only a few stages ahead of their first copy, so
+        // the queue still hands the last items to the CTAs that free up first.
         struct Cursor {
-            int it, q0, p1;
+            int it, q0, p1, b;
             const int32_t *slots;
         };
         auto fetch = [&]() -> int {
@@ -826,20 +841,20 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
             if (lane == 0) it = atomicAdd(p.wide_counter, 1);
             return __shfl_sync(0xffffffffu, it, 0);
         };
-        auto open_item = [&](Cursor &c) {
-            if (c.it < p.n_wide) {
-                const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + c.it);
+        auto open_item = [&](Cursor &c, int it) {
+            c.it = it;
+            if (it < p.n_wide) {
+                const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + it);
                 c.q0 = __ldg(v + 2);
                 c.p1 = __ldg(v + 3);
+                c.b = __ldg(v + 7);
                 c.slots = p.rtt + (int64_t)__ldg(v + 6) * p.rtt_stride;
             }
         };
-        auto next_stage = [&](Cursor &c) {
+        auto advance = [&](Cursor &c) {
+            if (c.it >= p.n_wide) return;  // past the end: stays there
             c.q0 += NP;
-            if (c.q0 >= c.p1) {
-                c.it = fetch();
-                open_item(c);
-            }
+            if (c.q0 >= c.p1) open_item(c, fetch());
         };
         auto slot_of = [&](const Cursor &c) -> int32_t {
             const int pos = c.q0 + lane;
@@ -847,57 +862,69 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
         };
         int2 *hdr = reinterpret_cast<int2 *>(smem + WL::OFF_HDR);
         const uint32_t qbytes = (uint32_t)(p.hq * D * 2);
-        Cursor cur{fetch(), 0, 0, nullptr};
-        open_item(cur);
-        int32_t sl_cur = slot_of(cur);
+        Cursor c0{}, c1, c2, c3;
+        open_item(c0, fetch());
+        int32_t s0 = slot_of(c0);
+        c1 = c0;
+        advance(c1);
+        int32_t s1 = slot_of(c1);
+        c2 = c1;
+        advance(c2);
+        int32_t s2 = slot_of(c2);
+        c3 = c2;
+        advance(c3);
+        int32_t s3 = slot_of(c3);
         int j = 0, n_items = 0;   // items opened so far; item k uses q slot k & 1
-        bool first = true;        // the stage is its item's first
+        int prev_it = -1;
         for (;; ++j) {
-            const bool end = cur.it >= p.n_wide;
-            Cursor nxt = cur;
-            if (!end) next_stage(nxt);
-            const int32_t sl_nxt = end ? -1 : slot_of(nxt);
+            const bool end = c0.it >= p.n_wide;
             const int st = j % kWideStages;
             if (j >= kWideStages &&
                 !wait_or_abort(bar + 8 * (kWideStages + st), ((j / kWideStages) - 1) & 1, abort_flag, p.status))
                 break;
             // an item's first stage also brings its query row into q slot k & 1,
             // once the consumers have read item k - 2's out of it
-            const bool with_q = first && !end;
+            const bool with_q = !end && c0.it != prev_it;
             const int qb = n_items & 1;
             if (with_q && n_items >= 2 &&
                 !wait_or_abort(bar + 8 * (2 * kWideStages + qb), ((n_items >> 1) - 1) & 1, abort_flag, p.status))
                 break;
-            const bool inside = !end && lane < NP && cur.q0 + lane < cur.p1;
-            const bool ok = inside && sl_cur >= 0 && (int64_t)sl_cur < p.num_slots;
+            const bool inside = !end && lane < NP && c0.q0 + lane < c0.p1;
+            const bool ok = inside && s0 >= 0 && (int64_t)s0 < p.num_slots;
             if (inside && !ok && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
             if (lane < NP) okf[st * kWideMaxPos + lane] = ok ? 1 : 0;
-            if (lane == 0) hdr[st] = make_int2(end ? -1 : cur.it, cur.q0);
+            if (lane == 0) hdr[st] = make_int2(end ? -1 : c0.it, c0.q0);
             const int nok = __popc(__ballot_sync(0xffffffffu, ok));
             __syncwarp();  // flags and header are written before lane 0's arrive releases them
             if (lane == 0)
                 rx::mbar_arrive_expect_tx(bar + 8 * st, (uint32_t)(2 * nok * RB) + (with_q ? qbytes : 0u));
             __syncwarp();
-            if (with_q && lane == 0) {
-                const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + cur.it);
-                rx::bulk_g2s(sbase + WL::OFF_Q + qb * WL::QBYTES, p.q + (int64_t)__ldg(v + 7) * p.hq * D, qbytes,
+            if (with_q && lane == 0)
+                rx::bulk_g2s(sbase + WL::OFF_Q + qb * WL::QBYTES, p.q + (int64_t)c0.b * p.hq * D, qbytes,
                              bar + 8 * st);
-            }
             if (with_q) ++n_items;
             if (ok) {
                 const uint32_t off = (uint32_t)(st * kWideStageBytes + lane * RB);
-                rx::bulk_g2s(sbase + WL::OFF_K + off, p.k_pool + (int64_t)sl_cur * row_elems, (uint32_t)RB,
+                rx::bulk_g2s(sbase + WL::OFF_K + off, p.k_pool + (int64_t)s0 * row_elems, (uint32_t)RB,
                              bar + 8 * st);
-                rx::bulk_g2s(sbase + WL::OFF_V + off, p.v_pool + (int64_t)sl_cur * row_elems, (uint32_t)RB,
+                rx::bulk_g2s(sbase + WL::OFF_V + off, p.v_pool + (int64_t)s0 * row_elems, (uint32_t)RB,
                              bar + 8 * st);
             }
             if (end) {
                 ++j;
                 break;
             }
-            first = nxt.it != cur.it;
-            cur = nxt;
-            sl_cur = sl_nxt;
+            prev_it = c0.it;
+            // shift the lookahead; the new far cursor's loads are in flight
+            // while the next stage waits to be free
+            c0 = c1;
+            s0 = s1;
+            c1 = c2;
+            s1 = s2;
+            c2 = c3;
+            s2 = s3;
+            advance(c3);
+            s3 = slot_of(c3);
         }
         // no copy may still be landing when the CTA exits
         if (lane == 0)
@@ -905,39 +932,53 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
                 drain_wait(bar + 8 * (jj % kWideStages), (jj / kWideStages) & 1, p.status);
         __syncwarp();
     } else {
-        // consumers: warp cw owns q heads (= kv heads, G == 1) h0 .. h0 + HPW - 1
-        constexpr int HN = HPW * NP;                        // (head, position) pairs of a stage
-        constexpr int LOG_HN = LOG_NP + (HPW == 1 ? 0 : HPW == 2 ? 1 : HPW == 4 ? 2 : 3);
-        static_assert(HN <= 32 && (1 << LOG_HN) == HN, "one value per lane after the reduce-scatter");
+        // consumers: warp cw owns q heads (= kv heads, G == 1) h0 .. h0 + HPW - 1.
+        // A stage is taken in sub-stages of NPS positions: eight (head,
+        // position) pairs, four lanes each.  Lane l serves pair x = l / 4
+        // (head hh = x / NPS, position pi = x % NPS) and quarter qd = l % 4 of
+        // its dot product, DQ dims; the quarters meet in two shuffles, and max
+        // and sum over a head's positions take LOG_NPS shuffles each, so the
+        // chain of dependent shuffles per sub-stage stays short.  For P.V the
+        // 32 / HPW lanes of a head each own DO consecutive output dims.
+        constexpr int LOG_HPW = HPW == 1 ? 0 : HPW == 2 ? 1 : 2;
+        constexpr int LOG_NPS = LOG_NP + LOG_HPW <= 3 ? LOG_NP : 3 - LOG_HPW;
+        constexpr int NPS = 1 << LOG_NPS;
+        static_assert(HPW * NPS == 8 && NP % NPS == 0, "eight (head, position) pairs per sub-stage");
+        constexpr int DQ = D / 4;          // dims of a lane's quarter of a dot product
+        constexpr int NCH = DQ / 8;        // its 16-byte chunks (4 at d 128, 2 at d 64)
+        constexpr int DO = D * HPW / 32;   // output dims per lane
+        static_assert(NCH == 2 || NCH == 4, "quarter of 2 or 4 chunks");
         const int cw = warp - 1;
         const int h0 = cw * HPW;
-        // after the reduce-scatter, lane l holds pair x = l >> (5 - LOG_HN):
-        // head hx = x / NP, position ix = x % NP
-        const int x = lane >> (5 - LOG_HN);
-        const int hx = x >> LOG_NP, ix = x & (NP - 1);
+        const int x = lane >> 2, qd = lane & 3;
+        const int hh = x >> LOG_NPS, pi = x & (NPS - 1);
+        const int hl = lane & (32 / HPW - 1);  // lane within its head's lanes
+        const int head = h0 + hh;
+        // chunk c of a quarter is read at rotated position cc(c), so that the
+        // eight lanes of each 16-byte load phase hit distinct bank groups
+        auto chunk_at = [&](int c) -> int {
+            return NCH == 4 ? ((c + (qd >> 1) + 2 * (x & 1)) & 3) : ((c + (x & 1)) & 1);
+        };
         const int2 *hdr = reinterpret_cast<const int2 *>(smem + WL::OFF_HDR);
-        float q[HPW][E], o[HPW][E], m[HPW], l[HPW];
+        float q[NCH][8], o[DO], m = -INFINITY, l = 0.f;
         int cur = -1, p1 = 0, part_idx = 0, b = 0, n_items = 0;
         bool fin = false;
-        // the current item's results for this warp's heads
+        // the current item's result for this lane's head
         auto write_out = [&]() {
+            const int64_t orow = (int64_t)b * p.hq + head;
+            const float inv = 1.f / l;
+            if (fin) {
+                bf16 *dst = p.o + orow * D + hl * DO;
 #pragma unroll
-            for (int hh = 0; hh < HPW; ++hh) {
-                const int64_t orow = (int64_t)b * p.hq + h0 + hh;
-                const float inv = 1.f / l[hh];
-                if (fin) {
-                    bf16 *dst = p.o + orow * D + lane * E;
+                for (int e = 0; e < DO; e += 2)
+                    *reinterpret_cast<uint32_t *>(dst + e) = rx::pack_bf16(o[e] * inv, o[e + 1] * inv);
+                if (p.lse && hl == 0) p.lse[orow] = (m + log2f(l)) * rx::kLn2;
+            } else {
+                const int64_t prow = orow * p.max_parts + part_idx;
+                float *dst = p.ws_o + prow * D + hl * DO;
 #pragma unroll
-                    for (int e = 0; e < E; e += 2)
-                        *reinterpret_cast<uint32_t *>(dst + e) = rx::pack_bf16(o[hh][e] * inv, o[hh][e + 1] * inv);
-                    if (p.lse && lane == 0) p.lse[orow] = (m[hh] + log2f(l[hh])) * rx::kLn2;
-                } else {
-                    const int64_t prow = orow * p.max_parts + part_idx;
-                    float *dst = p.ws_o + prow * D + lane * E;
-#pragma unroll
-                    for (int e = 0; e < E; ++e) dst[e] = o[hh][e] * inv;
-                    if (lane == 0) p.ws_lse[prow] = m[hh] + log2f(l[hh]);
-                }
+                for (int e = 0; e < DO; ++e) dst[e] = o[e] * inv;
+                if (hl == 0) p.ws_lse[prow] = m + log2f(l);
             }
         };
         for (int j = 0;; ++j) {
@@ -955,108 +996,79 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
                 part_idx = __ldg(v + 4);
                 fin = __ldg(v + 5) != 0;
                 b = __ldg(v + 7);
-                // the query row came with this stage: read this warp's heads,
-                // then hand the q slot back
+                // the query row came with this stage: read this lane's quarter
+                // of its head (in the rotated chunk order), then hand the q
+                // slot back
                 const int qb = n_items & 1;
-                const unsigned char *qs = smem + WL::OFF_Q + qb * WL::QBYTES + h0 * D * 2 + lane * E * 2;
+                const unsigned char *qs = smem + WL::OFF_Q + qb * WL::QBYTES + head * D * 2 + qd * DQ * 2;
 #pragma unroll
-                for (int hh = 0; hh < HPW; ++hh) {
-                    float qf[E];
-                    load_bf16<E>(qs + hh * D * 2, qf);
-                    m[hh] = -INFINITY;
-                    l[hh] = 0.f;
+                for (int c = 0; c < NCH; ++c) {
+                    load_bf16<8>(qs + 16 * chunk_at(c), q[c]);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        q[hh][e] = qf[e] * p.scale_log2;
-                        o[hh][e] = 0.f;
-                    }
+                    for (int e = 0; e < 8; ++e) q[c][e] *= p.scale_log2;
                 }
+#pragma unroll
+                for (int e = 0; e < DO; ++e) o[e] = 0.f;
+                m = -INFINITY;
+                l = 0.f;
                 __syncwarp();
                 if (lane == 0) rx::mbar_arrive(bar + 8 * (2 * kWideStages + qb));
                 ++n_items;
             }
-            {
-                const int q0 = h.y;
-                const int n = min(NP, p1 - q0);
-                const unsigned char *ks = smem + WL::OFF_K + st * kWideStageBytes + h0 * D * 2 + lane * E * 2;
-                const unsigned char *vs = smem + WL::OFF_V + st * kWideStageBytes + h0 * D * 2 + lane * E * 2;
-                // bit i: position i of the stage holds a valid row
-                const int *okp = okf + st * kWideMaxPos;
+            const int n = min(NP, p1 - h.y);  // positions of the item in this stage
+            const int *okp = okf + st * kWideMaxPos;
+            for (int sub = 0; sub * NPS < n; ++sub) {
+                const int ns = min(NPS, n - sub * NPS);
+                const unsigned char *kst = smem + WL::OFF_K + st * kWideStageBytes + sub * NPS * RB;
+                const unsigned char *vst = smem + WL::OFF_V + st * kWideStageBytes + sub * NPS * RB;
+                // bit i: position i of the sub-stage holds a valid row
                 uint32_t vmask = 0;
 #pragma unroll
-                for (int i = 0; i < NP; ++i) vmask |= (i < n && okp[i] != 0) ? (1u << i) : 0u;
-                // partial dot products over this lane's E dims, pair (hh, i) at hh * NP + i
-                float part[HN];
+                for (int i = 0; i < NPS; ++i) vmask |= (i < ns && okp[sub * NPS + i] != 0) ? (1u << i) : 0u;
+                // this lane's quarter of the dot product of its pair
+                const unsigned char *kr = kst + pi * RB + head * D * 2 + qd * DQ * 2;
+                float sc = 0.f;
 #pragma unroll
-                for (int hh = 0; hh < HPW; ++hh)
+                for (int c = 0; c < NCH; ++c) {
+                    float kf[8];
+                    load_bf16<8>(kr + 16 * chunk_at(c), kf);
 #pragma unroll
-                    for (int i = 0; i < NP; ++i) {
-                        float kf[E];
-                        load_bf16<E>(ks + i * RB + hh * D * 2, kf);
-                        float acc = 0.f;
-#pragma unroll
-                        for (int e = 0; e < E; ++e) acc = fmaf(q[hh][e], kf[e], acc);
-                        part[hh * NP + i] = acc;
-                    }
-                // reduce-scatter: halve the value list at each lane offset
-#pragma unroll
-                for (int s2 = 0, half = HN / 2; half >= 1; ++s2, half >>= 1) {
-                    const int off = 16 >> s2;
-                    const bool up = (lane & off) != 0;
-#pragma unroll
-                    for (int i = 0; i < half; ++i) {
-                        const float send = up ? part[i] : part[i + half];
-                        const float keep = up ? part[i + half] : part[i];
-                        part[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                    }
+                    for (int e = 0; e < 8; ++e) sc = fmaf(q[c][e], kf[e], sc);
                 }
-                float sc = part[0];
-#pragma unroll
-                for (int off = 16 >> LOG_HN; off >= 1; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
+                sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+                sc += __shfl_xor_sync(0xffffffffu, sc, 2);
                 // a position past the item is out; a row with an invalid slot reads as zeros
-                const bool in = ix < n;
-                const bool okx = (vmask >> ix) & 1u;
-                sc = in ? (okx ? sc : 0.f) : -INFINITY;
-                // per head: max and sum over its NP positions (lane bits of ix)
+                const bool okx = (vmask >> pi) & 1u;
+                sc = pi < ns ? (okx ? sc : 0.f) : -INFINITY;
                 float smax = sc;
 #pragma unroll
-                for (int bb = 0; bb < LOG_NP; ++bb)
-                    smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1 << (5 - LOG_HN + bb)));
-                float mh = m[0];
-#pragma unroll
-                for (int hh = 1; hh < HPW; ++hh) mh = hx == hh ? m[hh] : mh;
-                const float mn = fmaxf(mh, smax);
+                for (int k = 0; k < LOG_NPS; ++k) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 4 << k));
+                const float mn = fmaxf(m, smax);
                 const float pw = rx::fast_exp2(sc - mn);  // 0 past the item
                 float ps = pw;
 #pragma unroll
-                for (int bb = 0; bb < LOG_NP; ++bb) ps += __shfl_xor_sync(0xffffffffu, ps, 1 << (5 - LOG_HN + bb));
-                const float al = rx::fast_exp2(mh - mn);  // 0 on the item's first stage
-                const float pv = okx ? pw : 0.f;          // weight of this lane's pair for V
+                for (int k = 0; k < LOG_NPS; ++k) ps += __shfl_xor_sync(0xffffffffu, ps, 4 << k);
+                const float al = rx::fast_exp2(m - mn);   // 0 on the item's first sub-stage
+                m = mn;
+                l = fmaf(l, al, ps);
 #pragma unroll
-                for (int hh = 0; hh < HPW; ++hh) {
-                    const int src = (hh << LOG_NP) << (5 - LOG_HN);
-                    const float a = __shfl_sync(0xffffffffu, al, src);
-                    m[hh] = __shfl_sync(0xffffffffu, mn, src);
-                    l[hh] = fmaf(l[hh], a, __shfl_sync(0xffffffffu, ps, src));
+                for (int e = 0; e < DO; ++e) o[e] *= al;
+                const float pv = okx ? pw : 0.f;  // weight of this lane's pair for V
+                const unsigned char *vr = vst + head * D * 2 + hl * DO * 2;
 #pragma unroll
-                    for (int e = 0; e < E; ++e) o[hh][e] *= a;
+                for (int i = 0; i < NPS; ++i) {
+                    const float w = __shfl_sync(0xffffffffu, pv, ((hh << LOG_NPS) + i) << 2);
+                    // rows past the item or with an invalid slot were never
+                    // written in this stage: skip them (0 * stale NaN is NaN)
+                    if (!((vmask >> i) & 1u)) continue;
+                    float vf[DO];
+                    load_bf16<DO>(vr + i * RB, vf);
+#pragma unroll
+                    for (int e = 0; e < DO; ++e) o[e] = fmaf(w, vf[e], o[e]);
                 }
-#pragma unroll
-                for (int hh = 0; hh < HPW; ++hh)
-#pragma unroll
-                    for (int i = 0; i < NP; ++i) {
-                        const float pi = __shfl_sync(0xffffffffu, pv, ((hh << LOG_NP) + i) << (5 - LOG_HN));
-                        // rows past the item or with an invalid slot were never
-                        // written in this stage: skip them (0 * stale NaN is NaN)
-                        if (!((vmask >> i) & 1u)) continue;
-                        float vf[E];
-                        load_bf16<E>(vs + i * RB + hh * D * 2, vf);
-#pragma unroll
-                        for (int e = 0; e < E; ++e) o[hh][e] = fmaf(pi, vf[e], o[hh][e]);
-                    }
-                __syncwarp();
-                if (lane == 0) rx::mbar_arrive(bar + 8 * (kWideStages + st));
             }
+            __syncwarp();
+            if (lane == 0) rx::mbar_arrive(bar + 8 * (kWideStages + st));
         }
     }
 }
