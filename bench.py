@@ -173,8 +173,12 @@ class GpuStep:
             ws = rx.rx_attn_decode_workspace(B, p.hq, p.hkv, p.d, self.max_len, self.plan)
             self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev) if ws else None
             # per-head kernel (items of several requests), all-heads kernel
-            # (single-request items, one q head per kv head), merge of splits
-            n_wide = info.n_wide if (p.hq == p.hkv and p.hq in (8, 16, 32, 64)) else 0
+            # (single-request items: one q head per kv head, or 8 kv heads
+            # with 2 to 16 q heads each), merge of splits
+            G = p.hq // p.hkv
+            all_heads = (G == 1 and p.hq in (8, 16, 32, 64)) or \
+                (p.hkv == 8 and G in (2, 4, 8, 16) and p.hq * p.d * 2 <= 16384)
+            n_wide = info.n_wide if all_heads else 0
             self.launches += ((info.n_items - n_wide) > 0) + (n_wide > 0) + (info.max_parts > 1)
         if self.has_ext:
             self.q_ext = bf(p.q_ext)

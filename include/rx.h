@@ -269,7 +269,8 @@ typedef struct {
     int64_t buf_words;      /* int32 words of the packed buffer                 */
     int32_t n_wide;         /* items at the end of the list that hold a single
                                request, read across all kv heads at once; set
-                               when there is one q head per kv head          */
+                               for one q head per kv head, or for 8 kv heads
+                               with 2, 4, 8 or 16 q heads each                */
 } rx_decode_plan_info;
 
 /* Builds a decode plan.  Inputs (host): req_to_token (row stride rtt_stride),

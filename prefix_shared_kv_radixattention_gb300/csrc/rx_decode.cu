@@ -107,6 +107,7 @@ struct Params {
     const bf16 *v_pool;
     int64_t num_slots;
     int hq, hkv, G;
+    int head_dim;
     const int32_t *req_idx;
     const int32_t *seq_len;
     const int32_t *rtt;
@@ -731,24 +732,31 @@ constexpr int kWideStages = 3;
 constexpr int kWideStageBytes = 32768;  // K bytes per stage (as many again for V)
 constexpr int kWideMaxPos = 32;         // positions per stage at most (one producer lane each)
 
-struct WideLayout {
+// Shared-memory layout of an all-heads kernel: STAGES ring entries of K
+// (and as many of V) rows at ROW_STRIDE bytes, per-stage row flags and
+// headers, NQ query-row slots, then the barriers: full [STAGES], empty
+// [STAGES], q_empty [NQ].
+template <int STAGES_, int STAGE_BYTES_, int NQ_>
+struct WideLayoutT {
+    static constexpr int STAGES = STAGES_, STAGE_BYTES = STAGE_BYTES_, NQ = NQ_;
     static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = kWideStages * kWideStageBytes;
-    static constexpr int OFF_OK = 2 * kWideStages * kWideStageBytes;  // int [stage][pos]: row valid
-    static constexpr int OFF_HDR = OFF_OK + kWideStages * kWideMaxPos * 4;  // int2 [stage]: item, first position
-    static constexpr int OFF_Q = (OFF_HDR + kWideStages * 8 + 127) / 128 * 128;  // 2 x the item's query row
-    static constexpr int QBYTES = 16384;                                   // hq * D * 2 at most
-    static constexpr int OFF_BAR = OFF_Q + 2 * QBYTES;   // full [S], empty [S], q_empty [2]
-    static constexpr int OFF_ABORT = OFF_BAR + (2 * kWideStages + 2) * 8;
+    static constexpr int OFF_V = STAGES * STAGE_BYTES;
+    static constexpr int OFF_OK = 2 * STAGES * STAGE_BYTES;               // int [stage][pos]: row valid
+    static constexpr int OFF_HDR = OFF_OK + STAGES * kWideMaxPos * 4;     // int2 [stage]: item, first position
+    static constexpr int OFF_Q = (OFF_HDR + STAGES * 8 + 127) / 128 * 128;  // NQ x the item's query row
+    static constexpr int QBYTES = 16384;                                  // hq * D * 2 at most
+    static constexpr int OFF_BAR = OFF_Q + NQ * QBYTES;
+    static constexpr int OFF_ABORT = OFF_BAR + (2 * STAGES + NQ) * 8;
     static constexpr int BYTES = OFF_ABORT + 16 + 128;  // + room to align the base to 128
+    static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
+    static_assert(BYTES <= 227 * 1024, "shared memory budget");
+    // bulk copies land on 16-byte boundaries: stage bases, rows (16-byte
+    // multiples from a stage base) and the q slots
+    static_assert(STAGE_BYTES % 128 == 0 && OFF_V % 128 == 0 && OFF_Q % 128 == 0 && QBYTES % 128 == 0,
+                  "bulk-copy destination alignment");
 };
-static_assert(WideLayout::OFF_BAR % 8 == 0, "mbarrier alignment");
-static_assert(WideLayout::BYTES <= 227 * 1024, "shared memory budget");
-// bulk copies land on 16-byte boundaries: stage rows (multiples of 128 bytes
-// from a stage base) and the q slots
-static_assert(WideLayout::OFF_V % 128 == 0 && WideLayout::OFF_Q % 128 == 0 && WideLayout::QBYTES % 128 == 0,
-              "bulk-copy destination alignment");
-
+// one q head per kv head: slot rows packed (32 KB of K a stage), two q slots
+using WideLayout = WideLayoutT<kWideStages, kWideStageBytes, 2>;
 
 // bounded single-thread wait that ignores the abort flag: lets copies already
 // issued land before the CTA exits
@@ -794,6 +802,129 @@ __device__ __forceinline__ void load_bf16(const unsigned char *src, float (&out)
     }
 }
 
+// Producer warp of an all-heads kernel (layout WL, NP positions a stage,
+// one lane per position).  Items come from a global counter, first come
+// first served, so a CTA that starts late (behind the per-head kernel
+// running alongside) takes fewer of them.  Each stage's header names its
+// item; a last header with item -1 tells the consumers to stop.  A stage's
+// rows sit row_stride bytes apart (row bytes RB = hkv * head_dim * 2).
+template <class WL, int NP>
+__device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sbase, volatile int *abort_flag,
+                              int row_stride)
+{
+    const uint32_t bar = sbase + WL::OFF_BAR;
+    int *okf = reinterpret_cast<int *>(smem + WL::OFF_OK);
+    const int lane = threadIdx.x & 31;
+    const int RB = p.hkv * p.head_dim * 2;
+    const int64_t row_elems = (int64_t)p.hkv * p.head_dim;
+    // Under load a global load takes microseconds, so nothing on the copy
+    // path waits for one: a cursor runs three stages ahead of the stage
+    // being issued, and its loads (at an item boundary: the claim, the
+    // item's fields, then slot ids) are made before the wait for a free
+    // stage.  Claims stay only a few stages ahead of their first copy, so
+    // the queue still hands the last items to the CTAs that free up first.
+    struct Cursor {
+        int it, q0, p1, b;
+        const int32_t *slots;
+    };
+    auto fetch = [&]() -> int {
+        int it = 0;
+        if (lane == 0) it = atomicAdd(p.wide_counter, 1);
+        return __shfl_sync(0xffffffffu, it, 0);
+    };
+    auto open_item = [&](Cursor &c, int it) {
+        c.it = it;
+        if (it < p.n_wide) {
+            const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + it);
+            c.q0 = __ldg(v + 2);
+            c.p1 = __ldg(v + 3);
+            c.b = __ldg(v + 7);
+            c.slots = p.rtt + (int64_t)__ldg(v + 6) * p.rtt_stride;
+        }
+    };
+    auto advance = [&](Cursor &c) {
+        if (c.it >= p.n_wide) return;  // past the end: stays there
+        c.q0 += NP;
+        if (c.q0 >= c.p1) open_item(c, fetch());
+    };
+    auto slot_of = [&](const Cursor &c) -> int32_t {
+        const int pos = c.q0 + lane;
+        return (c.it < p.n_wide && lane < NP && pos < c.p1) ? __ldg(c.slots + pos) : -1;
+    };
+    int2 *hdr = reinterpret_cast<int2 *>(smem + WL::OFF_HDR);
+    const uint32_t qbytes = (uint32_t)(p.hq * p.head_dim * 2);
+    Cursor c0{}, c1, c2, c3;
+    open_item(c0, fetch());
+    int32_t s0 = slot_of(c0);
+    c1 = c0;
+    advance(c1);
+    int32_t s1 = slot_of(c1);
+    c2 = c1;
+    advance(c2);
+    int32_t s2 = slot_of(c2);
+    c3 = c2;
+    advance(c3);
+    int32_t s3 = slot_of(c3);
+    int j = 0, n_items = 0;   // items opened so far; item k uses q slot k % NQ
+    int prev_it = -1;
+    for (;; ++j) {
+        const bool end = c0.it >= p.n_wide;
+        const int st = j % WL::STAGES;
+        if (j >= WL::STAGES &&
+            !wait_or_abort(bar + 8 * (WL::STAGES + st), ((j / WL::STAGES) - 1) & 1, abort_flag, p.status))
+            break;
+        // an item's first stage also brings its query row into q slot
+        // k % NQ, once the consumers have read item k - NQ's out of it
+        const bool with_q = !end && c0.it != prev_it;
+        const int qb = n_items % WL::NQ;
+        if (with_q && n_items >= WL::NQ &&
+            !wait_or_abort(bar + 8 * (2 * WL::STAGES + qb), ((n_items / WL::NQ) - 1) & 1, abort_flag,
+                           p.status))
+            break;
+        const bool inside = !end && lane < NP && c0.q0 + lane < c0.p1;
+        const bool ok = inside && s0 >= 0 && (int64_t)s0 < p.num_slots;
+        if (inside && !ok && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
+        if (lane < NP) okf[st * kWideMaxPos + lane] = ok ? 1 : 0;
+        if (lane == 0) hdr[st] = make_int2(end ? -1 : c0.it, c0.q0);
+        const int nok = __popc(__ballot_sync(0xffffffffu, ok));
+        __syncwarp();  // flags and header are written before lane 0's arrive releases them
+        if (lane == 0)
+            rx::mbar_arrive_expect_tx(bar + 8 * st, (uint32_t)(2 * nok * RB) + (with_q ? qbytes : 0u));
+        __syncwarp();
+        if (with_q && lane == 0)
+            rx::bulk_g2s(sbase + WL::OFF_Q + qb * WL::QBYTES, p.q + (int64_t)c0.b * p.hq * p.head_dim, qbytes,
+                         bar + 8 * st);
+        if (with_q) ++n_items;
+        if (ok) {
+            const uint32_t off = (uint32_t)(st * WL::STAGE_BYTES + lane * row_stride);
+            rx::bulk_g2s(sbase + WL::OFF_K + off, p.k_pool + (int64_t)s0 * row_elems, (uint32_t)RB,
+                         bar + 8 * st);
+            rx::bulk_g2s(sbase + WL::OFF_V + off, p.v_pool + (int64_t)s0 * row_elems, (uint32_t)RB,
+                         bar + 8 * st);
+        }
+        if (end) {
+            ++j;
+            break;
+        }
+        prev_it = c0.it;
+        // shift the lookahead; the new far cursor's loads are in flight
+        // while the next stage waits to be free
+        c0 = c1;
+        s0 = s1;
+        c1 = c2;
+        s1 = s2;
+        c2 = c3;
+        s2 = s3;
+        advance(c3);
+        s3 = slot_of(c3);
+    }
+    // no copy may still be landing when the CTA exits
+    if (lane == 0)
+        for (int jj = j > WL::STAGES ? j - WL::STAGES : 0; jj < j; ++jj)
+            drain_wait(bar + 8 * (jj % WL::STAGES), (jj / WL::STAGES) & 1, p.status);
+    __syncwarp();
+}
+
 template <int D, int LOG_NP, int HPW, int CW>
 __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Params p)
 {
@@ -808,7 +939,6 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
     int *okf = reinterpret_cast<int *>(smem + WL::OFF_OK);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int RB = p.hkv * D * 2;          // bytes of one slot row
-    const int64_t row_elems = (int64_t)p.hkv * D;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kWideStages; ++i) {
             rx::mbar_init(bar + 8 * i, 1);                                  // producer + bytes
@@ -821,116 +951,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
     __syncthreads();
 
     if (warp == 0) {
-        // producer: stage j holds positions q0 .. q0 + NP - 1 of one item, one
-        // lane per position.  Items come from a global counter, first come
-        // first served, so a CTA that starts late (behind the per-head kernel
-        // running alongside) takes fewer of them.  Each stage's header names
-        // its item; a last header with item -1 tells the consumers to stop.
-        // Under load a global load takes microseconds, so nothing on the copy
-        // path waits for one: a cursor runs three stages ahead of the stage
-        // being issued, and its loads (at an item boundary: the claim, the
-        // item's fields, then slot ids) are made before the wait for a free
-        // stage.  Claims stay only a few stages ahead of their first copy, so
-        // the queue still hands the last items to the CTAs that free up first.
-        struct Cursor {
-            int it, q0, p1, b;
-            const int32_t *slots;
-        };
-        auto fetch = [&]() -> int {
-            int it = 0;
-            if (lane == 0) it = atomicAdd(p.wide_counter, 1);
-            return __shfl_sync(0xffffffffu, it, 0);
-        };
-        auto open_item = [&](Cursor &c, int it) {
-            c.it = it;
-            if (it < p.n_wide) {
-                const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + it);
-                c.q0 = __ldg(v + 2);
-                c.p1 = __ldg(v + 3);
-                c.b = __ldg(v + 7);
-                c.slots = p.rtt + (int64_t)__ldg(v + 6) * p.rtt_stride;
-            }
-        };
-        auto advance = [&](Cursor &c) {
-            if (c.it >= p.n_wide) return;  // past the end: stays there
-            c.q0 += NP;
-            if (c.q0 >= c.p1) open_item(c, fetch());
-        };
-        auto slot_of = [&](const Cursor &c) -> int32_t {
-            const int pos = c.q0 + lane;
-            return (c.it < p.n_wide && lane < NP && pos < c.p1) ? __ldg(c.slots + pos) : -1;
-        };
-        int2 *hdr = reinterpret_cast<int2 *>(smem + WL::OFF_HDR);
-        const uint32_t qbytes = (uint32_t)(p.hq * D * 2);
-        Cursor c0{}, c1, c2, c3;
-        open_item(c0, fetch());
-        int32_t s0 = slot_of(c0);
-        c1 = c0;
-        advance(c1);
-        int32_t s1 = slot_of(c1);
-        c2 = c1;
-        advance(c2);
-        int32_t s2 = slot_of(c2);
-        c3 = c2;
-        advance(c3);
-        int32_t s3 = slot_of(c3);
-        int j = 0, n_items = 0;   // items opened so far; item k uses q slot k & 1
-        int prev_it = -1;
-        for (;; ++j) {
-            const bool end = c0.it >= p.n_wide;
-            const int st = j % kWideStages;
-            if (j >= kWideStages &&
-                !wait_or_abort(bar + 8 * (kWideStages + st), ((j / kWideStages) - 1) & 1, abort_flag, p.status))
-                break;
-            // an item's first stage also brings its query row into q slot k & 1,
-            // once the consumers have read item k - 2's out of it
-            const bool with_q = !end && c0.it != prev_it;
-            const int qb = n_items & 1;
-            if (with_q && n_items >= 2 &&
-                !wait_or_abort(bar + 8 * (2 * kWideStages + qb), ((n_items >> 1) - 1) & 1, abort_flag, p.status))
-                break;
-            const bool inside = !end && lane < NP && c0.q0 + lane < c0.p1;
-            const bool ok = inside && s0 >= 0 && (int64_t)s0 < p.num_slots;
-            if (inside && !ok && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
-            if (lane < NP) okf[st * kWideMaxPos + lane] = ok ? 1 : 0;
-            if (lane == 0) hdr[st] = make_int2(end ? -1 : c0.it, c0.q0);
-            const int nok = __popc(__ballot_sync(0xffffffffu, ok));
-            __syncwarp();  // flags and header are written before lane 0's arrive releases them
-            if (lane == 0)
-                rx::mbar_arrive_expect_tx(bar + 8 * st, (uint32_t)(2 * nok * RB) + (with_q ? qbytes : 0u));
-            __syncwarp();
-            if (with_q && lane == 0)
-                rx::bulk_g2s(sbase + WL::OFF_Q + qb * WL::QBYTES, p.q + (int64_t)c0.b * p.hq * D, qbytes,
-                             bar + 8 * st);
-            if (with_q) ++n_items;
-            if (ok) {
-                const uint32_t off = (uint32_t)(st * kWideStageBytes + lane * RB);
-                rx::bulk_g2s(sbase + WL::OFF_K + off, p.k_pool + (int64_t)s0 * row_elems, (uint32_t)RB,
-                             bar + 8 * st);
-                rx::bulk_g2s(sbase + WL::OFF_V + off, p.v_pool + (int64_t)s0 * row_elems, (uint32_t)RB,
-                             bar + 8 * st);
-            }
-            if (end) {
-                ++j;
-                break;
-            }
-            prev_it = c0.it;
-            // shift the lookahead; the new far cursor's loads are in flight
-            // while the next stage waits to be free
-            c0 = c1;
-            s0 = s1;
-            c1 = c2;
-            s1 = s2;
-            c2 = c3;
-            s2 = s3;
-            advance(c3);
-            s3 = slot_of(c3);
-        }
-        // no copy may still be landing when the CTA exits
-        if (lane == 0)
-            for (int jj = j > kWideStages ? j - kWideStages : 0; jj < j; ++jj)
-                drain_wait(bar + 8 * (jj % kWideStages), (jj / kWideStages) & 1, p.status);
-        __syncwarp();
+        wide_producer<WL, NP>(p, smem, sbase, abort_flag, RB);
     } else {
         // consumers: warp cw owns q heads (= kv heads, G == 1) h0 .. h0 + HPW - 1.
         // A stage is taken in sub-stages of NPS positions: eight (head,
@@ -1073,6 +1094,245 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
     }
 }
 
+// ---------------------------------------------------------------------------
+// single-request items with several q heads per kv head
+// ---------------------------------------------------------------------------
+//
+// With G = hq / hkv > 1 a kv head's K row meets G query rows, so the work per
+// byte is G times that of G == 1 and belongs on the tensor cores.  This
+// kernel keeps the all-heads data path (whole slot rows, 2 KiB at 8 x 128,
+// one bulk copy each, from the same producer) and gives each of the eight kv
+// heads one consumer warp that runs mma.sync m16n8k16 on them: the G query
+// rows of the kv head, padded to 16, against 16 positions a stage.
+//   - rows sit at a stride of 2048 + 16 bytes, so the eight rows an ldmatrix
+//     reads fall in distinct banks;
+//   - bulk copies cannot zero-fill, so V rows of positions past the item or
+//     with an invalid slot id are zeroed in the mma operands instead (a
+//     probability of 0 times a stale NaN would still be NaN); their scores
+//     are -inf past the item and 0 for an invalid slot (a zero K row).
+
+constexpr int kGqaNP = 16;                         // positions per stage
+constexpr int kGqaRowStride = 2048 + 16;           // slot row (8 kv heads x 128 x 2 at most) + pad
+using GqaLayout = WideLayoutT<3, kGqaNP * kGqaRowStride, 1>;
+constexpr int kGqaWarps = 8;                       // one consumer warp per kv head
+
+template <int D>
+__global__ void __launch_bounds__(32 * (1 + kGqaWarps), 1) decode_gqa_kernel(const Params p)
+{
+    using WL = GqaLayout;
+    constexpr int KS = D / 16;   // k-steps of S = Q K^T
+    constexpr int DT = D / 8;    // n-tiles of O
+    extern __shared__ __align__(128) unsigned char graw[];
+    const uint32_t raw = rx::smem_u32(graw);
+    unsigned char *smem = graw + (((raw + 127u) & ~127u) - raw);
+    const uint32_t sbase = rx::smem_u32(smem);
+    const uint32_t bar = sbase + WL::OFF_BAR;  // full: [0, S), empty: [S, 2S), q_empty: [2S]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + WL::OFF_ABORT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < WL::STAGES; ++i) {
+            rx::mbar_init(bar + 8 * i, 1);                          // producer + bytes
+            rx::mbar_init(bar + 8 * (WL::STAGES + i), kGqaWarps);   // consumer warps
+        }
+        rx::mbar_init(bar + 8 * (2 * WL::STAGES), kGqaWarps);       // q slot read
+        *abort_flag = 0;
+        rx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        wide_producer<WL, kGqaNP>(p, smem, sbase, abort_flag, kGqaRowStride);
+        return;
+    }
+    // consumer warp: kv head g, q heads g * G .. g * G + G - 1 as rows 0 .. G - 1
+    const int g = warp - 1;
+    const int G = p.G;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int2 *hdr = reinterpret_cast<const int2 *>(smem + WL::OFF_HDR);
+    const int *okf = reinterpret_cast<const int *>(smem + WL::OFF_OK);
+    uint32_t qf[KS][4];
+    float oacc[DT][4], m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+    int cur = -1, p1 = 0, part_idx = 0, b = 0;
+    bool fin = false;
+    auto write_out = [&]() {
+        float l0 = l_r[0], l1 = l_r[1];
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        const float ls[2] = {l0, l1};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int r = gid + half * 8;
+            if (r >= G) continue;
+            const int64_t orow = (int64_t)b * p.hq + (int64_t)g * G + r;
+            const float inv = 1.f / ls[half];
+            if (fin) {
+                bf16 *dst = p.o + orow * D;
+#pragma unroll
+                for (int dt = 0; dt < DT; ++dt)
+                    *reinterpret_cast<uint32_t *>(dst + dt * 8 + tig * 2) =
+                        rx::pack_bf16(oacc[dt][2 * half] * inv, oacc[dt][2 * half + 1] * inv);
+                if (p.lse && tig == 0) p.lse[orow] = (m_r[half] + log2f(ls[half])) * rx::kLn2;
+            } else {
+                const int64_t prow = orow * p.max_parts + part_idx;
+                float *dst = p.ws_o + prow * D;
+#pragma unroll
+                for (int dt = 0; dt < DT; ++dt)
+                    *reinterpret_cast<float2 *>(dst + dt * 8 + tig * 2) =
+                        make_float2(oacc[dt][2 * half] * inv, oacc[dt][2 * half + 1] * inv);
+                if (tig == 0) p.ws_lse[prow] = m_r[half] + log2f(ls[half]);
+            }
+        }
+    };
+    for (int j = 0;; ++j) {
+        const int st = j % WL::STAGES;
+        if (!wait_or_abort(bar + 8 * st, (j / WL::STAGES) & 1, abort_flag, p.status)) return;
+        const int2 h = hdr[st];
+        // a new item starts, or (item -1) none is left -- possibly before
+        // this CTA got any, when the other CTAs drained the queue first
+        if (h.x != cur || h.x < 0) {
+            if (cur >= 0) write_out();
+            if (h.x < 0) break;
+            cur = h.x;
+            const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + cur);
+            p1 = __ldg(v + 3);
+            part_idx = __ldg(v + 4);
+            fin = __ldg(v + 5) != 0;
+            b = __ldg(v + 7);
+            // the query rows came with this stage: A fragments of rows
+            // 0 .. G - 1 (rows past G read row 0 and are zeroed), then hand
+            // the q slot back
+            const unsigned char *qs = smem + WL::OFF_Q + (size_t)g * G * D * 2;
+            const int qrow = (lane & 15) < G ? (lane & 15) : 0;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int ch = ks * 2 + (lane >> 4);
+                rx::ldmatrix_x4(rx::smem_u32(qs + qrow * D * 2 + ch * 16), qf[ks][0], qf[ks][1], qf[ks][2],
+                                qf[ks][3]);
+                if (gid >= G) qf[ks][0] = qf[ks][2] = 0u;
+                if (gid + 8 >= G) qf[ks][1] = qf[ks][3] = 0u;
+            }
+            __syncwarp();
+            if (lane == 0) rx::mbar_arrive(bar + 8 * (2 * WL::STAGES));
+            m_r[0] = m_r[1] = -INFINITY;
+            l_r[0] = l_r[1] = 0.f;
+#pragma unroll
+            for (int dt = 0; dt < DT; ++dt) oacc[dt][0] = oacc[dt][1] = oacc[dt][2] = oacc[dt][3] = 0.f;
+        }
+        const int n = min(kGqaNP, p1 - h.y);  // positions of the item in this stage
+        const int *okp = okf + st * kWideMaxPos;
+        uint32_t vmask = 0;  // bit i: position i holds a valid row
+#pragma unroll
+        for (int i = 0; i < kGqaNP; ++i) vmask |= (i < n && okp[i] != 0) ? (1u << i) : 0u;
+        const unsigned char *kt = smem + WL::OFF_K + st * WL::STAGE_BYTES + g * D * 2;
+        const unsigned char *vt = smem + WL::OFF_V + st * WL::STAGE_BYTES + g * D * 2;
+        // S = Q K^T over the stage's 16 positions (two n-tiles)
+        float sc[2][4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+        {
+            const int key = (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int ch = ks * 2 + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                rx::ldmatrix_x4(rx::smem_u32(kt + key * kGqaRowStride + ch * 16), b0, b1, b2, b3);
+                rx::mma_bf16_16816(sc[0], qf[ks], b0, b1);
+                rx::mma_bf16_16816(sc[1], qf[ks], b2, b3);
+            }
+        }
+        // scale into the exp2 domain; -inf past the item, 0 for an invalid slot
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int pos = nt * 8 + tig * 2 + (jj & 1);
+                const float x = pos < n ? (((vmask >> pos) & 1u) ? sc[nt][jj] * p.scale_log2 : 0.f) : -INFINITY;
+                sc[nt][jj] = x;
+                if (jj < 2) mx0 = fmaxf(mx0, x);
+                else mx1 = fmaxf(mx1, x);
+            }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m_r[0], mx0), mn1 = fmaxf(m_r[1], mx1);  // finite: n >= 1
+        const float a0 = rx::fast_exp2(m_r[0] - mn0), a1 = rx::fast_exp2(m_r[1] - mn1);
+        m_r[0] = mn0;
+        m_r[1] = mn1;
+        l_r[0] *= a0;
+        l_r[1] *= a1;
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+            oacc[dt][0] *= a0;
+            oacc[dt][1] *= a0;
+            oacc[dt][2] *= a1;
+            oacc[dt][3] *= a1;
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            sc[nt][0] = rx::fast_exp2(sc[nt][0] - mn0);
+            sc[nt][1] = rx::fast_exp2(sc[nt][1] - mn0);
+            sc[nt][2] = rx::fast_exp2(sc[nt][2] - mn1);
+            sc[nt][3] = rx::fast_exp2(sc[nt][3] - mn1);
+            l_r[0] += sc[nt][0] + sc[nt][1];
+            l_r[1] += sc[nt][2] + sc[nt][3];
+        }
+        uint32_t a[4];
+        a[0] = rx::pack_bf16(sc[0][0], sc[0][1]);
+        a[1] = rx::pack_bf16(sc[0][2], sc[0][3]);
+        a[2] = rx::pack_bf16(sc[1][0], sc[1][1]);
+        a[3] = rx::pack_bf16(sc[1][2], sc[1][3]);
+        // V rows of positions tig*2, tig*2+1 (b0, b2) and tig*2+8, +9 (b1, b3):
+        // zero the ones that were never written in this stage
+        const uint32_t vz0 = (((vmask >> (tig * 2)) & 1u) ? 0x0000ffffu : 0u) |
+                             (((vmask >> (tig * 2 + 1)) & 1u) ? 0xffff0000u : 0u);
+        const uint32_t vz1 = (((vmask >> (tig * 2 + 8)) & 1u) ? 0x0000ffffu : 0u) |
+                             (((vmask >> (tig * 2 + 9)) & 1u) ? 0xffff0000u : 0u);
+        {
+            const int key = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+            for (int dp = 0; dp < D / 16; ++dp) {
+                const int ch = dp * 2 + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                rx::ldmatrix_x4_trans(rx::smem_u32(vt + key * kGqaRowStride + ch * 16), b0, b1, b2, b3);
+                b0 &= vz0;
+                b1 &= vz1;
+                b2 &= vz0;
+                b3 &= vz1;
+                rx::mma_bf16_16816(oacc[2 * dp], a, b0, b1);
+                rx::mma_bf16_16816(oacc[2 * dp + 1], a, b2, b3);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) rx::mbar_arrive(bar + 8 * (WL::STAGES + st));
+    }
+}
+
+// Single-request items with G > 1 go to decode_gqa_kernel for 8 kv heads and
+// G = 2, 4, 8 or 16 (the q rows of a kv head fit one m16 tile) when a query
+// row fits the q slot.
+bool gqa_supported(int hq, int hkv, int D)
+{
+    return rx_gqa_heads(hq, hkv) && (D == 64 || D == 128) && hq * D * 2 <= GqaLayout::QBYTES;
+}
+
+template <int D>
+int launch_decode_gqa(const Params &p, cudaStream_t st)
+{
+    static bool configured = false;
+    if (!configured) {
+        RX_CUDA_CHECK(cudaFuncSetAttribute(decode_gqa_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           GqaLayout::BYTES));
+        configured = true;
+    }
+    const int grid = p.n_wide < num_sms() ? p.n_wide : num_sms();
+    decode_gqa_kernel<D><<<grid, 32 * (1 + kGqaWarps), GqaLayout::BYTES, st>>>(p);
+    RX_CUDA_CHECK(cudaGetLastError());
+    return RX_OK;
+}
+
 template <int D, int LOG_NP, int HPW, int CW>
 int launch_decode_wide_cfg(const Params &p, cudaStream_t st)
 {
@@ -1106,6 +1366,13 @@ int launch_decode_wide(const Params &p, cudaStream_t st)
     case 32: return launch_decode_wide_cfg<D, L0 - 2, 2, 16>(p, st);
     default: return launch_decode_wide_cfg<D, L0 - 3, 4, 16>(p, st);
     }
+}
+
+// the all-heads kernel for the plan's single-request items
+int launch_all_heads(const Params &p, int D, cudaStream_t st)
+{
+    if (p.G == 1) return D == 128 ? launch_decode_wide<128>(p, st) : launch_decode_wide<64>(p, st);
+    return D == 128 ? launch_decode_gqa<128>(p, st) : launch_decode_gqa<64>(p, st);
 }
 
 template <int D, bool PLAN>
@@ -1191,7 +1458,8 @@ extern "C" size_t rx_attn_decode_workspace(int32_t batch, int32_t num_q_heads, i
     // for the wide kernel's item counter when it runs
     const int64_t rows = parts > 1 ? (int64_t)batch * num_q_heads * parts : 0;
     const int64_t bytes = (rows * (head_dim + 1) * 4 + 255) / 256 * 256;
-    const bool wide = plan && plan->n_wide > 0 && wide_supported(num_q_heads, num_kv_heads, head_dim);
+    const bool wide = plan && plan->n_wide > 0 && (wide_supported(num_q_heads, num_kv_heads, head_dim) ||
+                                                   gqa_supported(num_q_heads, num_kv_heads, head_dim));
     return (size_t)(bytes + (wide ? 256 : 0));
 }
 
@@ -1231,6 +1499,7 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
     p.hq = hq;
     p.hkv = pool->num_kv_heads;
     p.G = hq / pool->num_kv_heads;
+    p.head_dim = D;
     p.req_idx = req_idx;
     p.seq_len = seq_len;
     p.rtt = rtt;
@@ -1247,7 +1516,7 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
         // the plan's last n_wide items hold one request each; they go to the
         // wide kernel for the head counts it is built for (else to the
         // per-head kernel with the rest)
-        p.n_wide = wide_supported(hq, p.hkv, D) ? plan->n_wide : 0;
+        p.n_wide = (wide_supported(hq, p.hkv, D) || gqa_supported(hq, p.hkv, D)) ? plan->n_wide : 0;
         p.wide0 = plan->n_items - p.n_wide;
         total = (int64_t)p.wide0 * p.hkv;
     } else {
@@ -1294,11 +1563,11 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
             RX_CUDA_CHECK(cudaEventRecord(fj->fork, st));
             RX_CUDA_CHECK(cudaStreamWaitEvent(fj->side, fj->fork, 0));
             rc = per_head(fj->side);
-            if (rc == RX_OK) rc = D == 128 ? launch_decode_wide<128>(p, st) : launch_decode_wide<64>(p, st);
+            if (rc == RX_OK) rc = launch_all_heads(p, D, st);
             RX_CUDA_CHECK(cudaEventRecord(fj->join, fj->side));
             RX_CUDA_CHECK(cudaStreamWaitEvent(st, fj->join, 0));
         } else {
-            rc = D == 128 ? launch_decode_wide<128>(p, st) : launch_decode_wide<64>(p, st);
+            rc = launch_all_heads(p, D, st);
         }
     }
     if (rc != RX_OK || !merge) return rc;

@@ -633,10 +633,11 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
     reads = shared;
     for (int64_t r = 0; r < B; ++r) reads += seq_len[order[(size_t)r]] - priv_begin[(size_t)r];
     const bool auto_chunk = kv_chunk == 0;
-    // One query row per kv head (G == 1): a request's own positions are read
-    // across all kv heads at once (whole contiguous slot rows), as
+    // With one q head per kv head, or with the head counts the
+    // several-q-heads all-heads kernel takes, a request's own positions are
+    // read across all kv heads at once (whole contiguous slot rows), as
     // single-request "wide" items; otherwise every item is per kv head.
-    const bool wide = G == 1;
+    const bool wide = G == 1 || rx_gqa_heads(hq, hkv);
     if (auto_chunk) {
         // about RX_DECODE_TARGET_ITEMS work items over all kv heads; with wide
         // items, about RX_DECODE_TARGET_SHARED_ITEMS over the shared reads only

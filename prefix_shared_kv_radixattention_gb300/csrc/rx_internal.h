@@ -21,6 +21,15 @@
 #define RX_DECODE_MIN_WIDE_CHUNK 16
 #define RX_DECODE_TARGET_SHARED_ITEMS 152
 
+// Head counts whose single-request decode items have an all-heads kernel
+// with several q heads per kv head: 8 kv heads, G = 2, 4, 8 or 16.
+static inline bool rx_gqa_heads(int32_t hq, int32_t hkv)
+{
+    if (hkv != 8 || hq % hkv != 0) return false;
+    const int32_t G = hq / hkv;
+    return G == 2 || G == 4 || G == 8 || G == 16;
+}
+
 // Sets the thread-local message returned by rx_last_error and returns code.
 int rx_set_error(int code, const char *fmt, ...);
 

@@ -174,7 +174,8 @@ def _check_decode(prob, plan, kv_chunk=0, min_shared=16, g=None):
 
 
 @pytest.mark.parametrize("plan", [False, True])
-@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (32, 32, 128), (32, 8, 128), (64, 8, 128), (8, 1, 64)])
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (32, 32, 128), (32, 8, 128), (64, 8, 128), (8, 1, 64),
+                                      (16, 8, 64), (64, 8, 64)])
 def test_decode_ragged(plan, hq, hkv, d):
     prob = inputs.ragged(40 + hq + d, hq=hq, hkv=hkv, d=d, n_groups=3, per_group=3, shared_max=400,
                          private_max=300, extend_max=1, decode=True, num_slots=5000)
@@ -230,12 +231,19 @@ def test_decode_bad_slot_is_flagged():
     assert np.isfinite(o).all()
 
 
-def test_decode_bad_slot_in_wide_item_is_flagged():
-    """A bad slot id inside a single-request item (the all-heads path) is
-    flagged and read as a zero row, like the per-head path does."""
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 8)])
+def test_decode_bad_slot_in_wide_item_is_flagged(hq, hkv):
+    """A bad slot id inside a single-request item (the all-heads kernels, one
+    and four q heads per kv head) is flagged and read as a zero row, like the
+    per-head path does: the other rows match the oracle with that row's K
+    and V set to zero."""
     g = _gpu()
     from prefix_shared_kv_radixattention_gb300 import binding as rx
-    prob = inputs.few_shot_decode(hq=8, hkv=8, d=128, batch=4, shared=40, private=90, num_slots=512)
+    prob = inputs.few_shot_decode(hq=hq, hkv=hkv, d=128, batch=4, shared=40, private=90, num_slots=512)
+    buf, info = rx.rx_decode_plan_build(prob.req_to_token, prob.dec_req_idx, prob.dec_seq_len, prob.hq,
+                                        prob.hkv, 64, 16)
+    assert info.n_wide > 0
+    good_slot = int(prob.req_to_token[1, 70])
     prob.req_to_token = prob.req_to_token.copy()
     prob.req_to_token[1, 70] = -3                      # inside request 1's private tail
     dev = g.Dev(prob)
@@ -243,9 +251,19 @@ def test_decode_bad_slot_in_wide_item_is_flagged():
     o, _ = dev.decode(plan=True, kv_chunk=64)
     assert dev.status_word() & rx.RX_DEV_BAD_SLOT
     assert np.isfinite(o).all()
+    # the oracle with the bad position reading a zero row
+    kp, vp, rtt = dev.oracle_pools()
+    kp, vp = kp.copy(), vp.copy()
+    rtt = rtt.copy()
+    rtt[1, 70] = good_slot
+    kp[good_slot] = 0
+    vp[good_slot] = 0
+    ro, _ = oracle.decode(prob.q_dec, kp, vp, rtt, prob.dec_req_idx, prob.dec_seq_len, prob.sm_scale)
+    g.compare(o, ro, "bad slot as a zero row")
 
 
-def test_decode_wide_ctas_that_find_the_queue_empty():
+@pytest.mark.parametrize("hq", [8, 32])
+def test_decode_wide_ctas_that_find_the_queue_empty(hq):
     """All-heads CTAs that start after the other CTAs have taken every
     single-request item end cleanly.  A 4096-position shared segment read as
     one chunk (three row blocks x eight kv heads: 24 per-head CTAs) holds 24
@@ -253,10 +271,11 @@ def test_decode_wide_ctas_that_find_the_queue_empty():
     all-heads CTAs that wait for those SMs find the work queue empty."""
     g = _gpu()
     from prefix_shared_kv_radixattention_gb300 import binding as rx
-    prob = inputs.few_shot_decode(hq=8, hkv=8, d=128, batch=160, shared=4096, private=20, num_slots=8192)
+    prob = inputs.few_shot_decode(hq=hq, hkv=8, d=128, batch=160, shared=4096, private=20, num_slots=8192)
     buf, info = rx.rx_decode_plan_build(prob.req_to_token, prob.dec_req_idx, prob.dec_seq_len, prob.hq,
                                         prob.hkv, 4096, 16)
-    assert info.n_wide == 160 and info.n_items - info.n_wide == 3
+    # row blocks of 64 query rows: 64 requests at G = 1, 16 at G = 4
+    assert info.n_wide == 160 and info.n_items - info.n_wide == (3 if hq == 8 else 10)
     for _ in range(3):
         _check_decode(prob, plan=True, kv_chunk=4096, g=g)
 

@@ -294,6 +294,13 @@ def _plan(prob, kv_chunk=0, min_shared=16):
     return order, nparts, items, info
 
 
+def _plan_wide(prob):
+    """Head counts for which the plan makes all-heads single-request items:
+    one q head per kv head, or 8 kv heads with G = 2, 4, 8 or 16."""
+    G = prob.hq // prob.hkv
+    return G == 1 or (prob.hkv == 8 and G in (2, 4, 8, 16))
+
+
 def check_plan(prob, order, nparts, items, info, auto=False):
     B = len(prob.dec_req_idx)
     G = prob.hq // prob.hkv
@@ -306,7 +313,7 @@ def check_plan(prob, order, nparts, items, info, auto=False):
         assert b0 == order[r0] and row0 == prob.dec_req_idx[b0]
         # single-request items of an automatic plan for the all-heads kernel
         # follow their own length target (at most 4096 positions)
-        wide_auto = nr == 1 and G == 1 and auto
+        wide_auto = nr == 1 and _plan_wide(prob) and auto
         assert p1 - p0 <= (4096 if wide_auto else info.kv_chunk)
         reqs = [int(order[r]) for r in range(r0, r0 + nr)]
         rows = [prob.req_to_token[prob.dec_req_idx[b], p0:p1] for b in reqs]
@@ -323,12 +330,12 @@ def check_plan(prob, order, nparts, items, info, auto=False):
         assert sorted(parts[b]) == list(range(int(nparts[b])))
     assert info.max_parts == int(nparts.max())
     # items of several requests first, then the single-request items, each
-    # group longest first; with one q head per kv head the single-request
-    # items are the n_wide "wide" ones, otherwise there are none
+    # group longest first; for the head counts with an all-heads kernel the
+    # single-request items are the n_wide "wide" ones, otherwise there are none
     single = items[:, 1] == 1
     n_single = int(single.sum())
     assert np.all(single[len(items) - n_single:]) and not np.any(single[:len(items) - n_single])
-    assert int(info.n_wide) == (n_single if G == 1 else 0)
+    assert int(info.n_wide) == (n_single if _plan_wide(prob) else 0)
     for grp in (items[~single], items[single]):
         lens = grp[:, 3] - grp[:, 2]
         assert np.all(lens[:-1] >= lens[1:])
