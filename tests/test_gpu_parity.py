@@ -187,6 +187,16 @@ def test_decode_few_shot_reduced(plan):
     _check_decode(inputs.few_shot_decode(batch=12, shared=300, private=77, num_slots=8192), plan)
 
 
+@pytest.mark.parametrize("hq", [8, 32])
+@pytest.mark.parametrize("shared,private", [(300, 200), (700, 600)])
+def test_decode_split_rows_merged(hq, shared, private):
+    """Rows split into few (9) and many (21) parts, written by the per-head
+    and the all-heads kernels (one and four q heads per kv head), combine to
+    the oracle's result."""
+    prob = inputs.few_shot_decode(hq=hq, hkv=8, d=128, batch=6, shared=shared, private=private, num_slots=8192)
+    _check_decode(prob, plan=True, kv_chunk=64)
+
+
 def test_decode_tree_of_thought_reduced():
     prob = inputs.tree_of_thought_decode(depth=3, fanout=3, edge=70, num_slots=8192)
     _check_decode(prob, plan=True, kv_chunk=64, min_shared=16)
