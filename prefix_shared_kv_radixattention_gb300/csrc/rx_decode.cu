@@ -733,20 +733,23 @@ constexpr int kWideStageBytes = 32768;  // K bytes per stage (as many again for 
 constexpr int kWideMaxPos = 32;         // positions per stage at most (one producer lane each)
 
 // Shared-memory layout of an all-heads kernel: STAGES ring entries of K
-// (and as many of V) rows at ROW_STRIDE bytes, per-stage row flags and
-// headers, NQ query-row slots, then the barriers: full [STAGES], empty
-// [STAGES], q_empty [NQ].
+// (and as many of V) rows, per-stage row flags, slot ids and headers, NQ
+// query-row slots, then the barriers: full [STAGES], empty [STAGES], q_empty
+// [NQ], desc [STAGES] (a stage's slot ids are written: the copy warps may
+// start).
 template <int STAGES_, int STAGE_BYTES_, int NQ_>
 struct WideLayoutT {
     static constexpr int STAGES = STAGES_, STAGE_BYTES = STAGE_BYTES_, NQ = NQ_;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = STAGES * STAGE_BYTES;
     static constexpr int OFF_OK = 2 * STAGES * STAGE_BYTES;               // int [stage][pos]: row valid
-    static constexpr int OFF_HDR = OFF_OK + STAGES * kWideMaxPos * 4;     // int2 [stage]: item, first position
+    static constexpr int OFF_SLOT = OFF_OK + STAGES * kWideMaxPos * 4;    // int [stage][pos]: slot id or -1
+    static constexpr int OFF_HDR = OFF_SLOT + STAGES * kWideMaxPos * 4;   // int2 [stage]: item, first position
     static constexpr int OFF_Q = (OFF_HDR + STAGES * 8 + 127) / 128 * 128;  // NQ x the item's query row
     static constexpr int QBYTES = 16384;                                  // hq * D * 2 at most
     static constexpr int OFF_BAR = OFF_Q + NQ * QBYTES;
-    static constexpr int OFF_ABORT = OFF_BAR + (2 * STAGES + NQ) * 8;
+    static constexpr int OFF_ABORT = OFF_BAR + (3 * STAGES + NQ) * 8;
+    static constexpr int B_DESC = 2 * STAGES + NQ;  // first desc barrier
     static constexpr int BYTES = OFF_ABORT + 16 + 128;  // + room to align the base to 128
     static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
     static_assert(BYTES <= 227 * 1024, "shared memory budget");
@@ -808,12 +811,13 @@ __device__ __forceinline__ void load_bf16(const unsigned char *src, float (&out)
 // running alongside) takes fewer of them.  Each stage's header names its
 // item; a last header with item -1 tells the consumers to stop.  A stage's
 // rows sit row_stride bytes apart (row bytes RB = hkv * head_dim * 2).
-template <class WL, int NP>
+template <class WL, int NP, int NH>
 __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sbase, volatile int *abort_flag,
                               int row_stride)
 {
     const uint32_t bar = sbase + WL::OFF_BAR;
     int *okf = reinterpret_cast<int *>(smem + WL::OFF_OK);
+    int *slotf = reinterpret_cast<int *>(smem + WL::OFF_SLOT);
     const int lane = threadIdx.x & 31;
     const int RB = p.hkv * p.head_dim * 2;
     const int64_t row_elems = (int64_t)p.hkv * p.head_dim;
@@ -884,7 +888,10 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
         const bool inside = !end && lane < NP && c0.q0 + lane < c0.p1;
         const bool ok = inside && s0 >= 0 && (int64_t)s0 < p.num_slots;
         if (inside && !ok && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
-        if (lane < NP) okf[st * kWideMaxPos + lane] = ok ? 1 : 0;
+        if (lane < NP) {
+            okf[st * kWideMaxPos + lane] = ok ? 1 : 0;
+            slotf[st * kWideMaxPos + lane] = ok ? s0 : -1;
+        }
         if (lane == 0) hdr[st] = make_int2(end ? -1 : c0.it, c0.q0);
         const int nok = __popc(__ballot_sync(0xffffffffu, ok));
         __syncwarp();  // flags and header are written before lane 0's arrive releases them
@@ -895,7 +902,11 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
             rx::bulk_g2s(sbase + WL::OFF_Q + qb * WL::QBYTES, p.q + (int64_t)c0.b * p.hq * p.head_dim, qbytes,
                          bar + 8 * st);
         if (with_q) ++n_items;
-        if (ok) {
+        if constexpr (NH > 0) {
+            // the copy warps issue this stage's row copies (issuing bulk
+            // copies costs each warp tens of nanoseconds apiece)
+            if (lane == 0) rx::mbar_arrive(bar + 8 * (WL::B_DESC + st));
+        } else if (ok) {
             const uint32_t off = (uint32_t)(st * WL::STAGE_BYTES + lane * row_stride);
             rx::bulk_g2s(sbase + WL::OFF_K + off, p.k_pool + (int64_t)s0 * row_elems, (uint32_t)RB,
                          bar + 8 * st);
@@ -925,8 +936,38 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
     __syncwarp();
 }
 
+// Copy warp h of NH of an all-heads kernel: for every stage the producer
+// described, issues the K and V row copies of positions h, h + NH, ... (one
+// lane each) onto the stage's full barrier.  It stops at the stage whose
+// header holds no item; the producer's drain covers its copies.
+template <class WL, int NP, int NH>
+__device__ void wide_copier(const Params &p, unsigned char *smem, uint32_t sbase, volatile int *abort_flag,
+                            int row_stride, int h)
+{
+    const uint32_t bar = sbase + WL::OFF_BAR;
+    const int *slotf = reinterpret_cast<const int *>(smem + WL::OFF_SLOT);
+    const int2 *hdr = reinterpret_cast<const int2 *>(smem + WL::OFF_HDR);
+    const int lane = threadIdx.x & 31;
+    const uint32_t RB = (uint32_t)(p.hkv * p.head_dim * 2);
+    const int64_t row_elems = (int64_t)p.hkv * p.head_dim;
+    const int pos = lane * NH + h;
+    for (int j = 0;; ++j) {
+        const int st = j % WL::STAGES;
+        if (!wait_or_abort(bar + 8 * (WL::B_DESC + st), (j / WL::STAGES) & 1, abort_flag, p.status)) return;
+        if (hdr[st].x < 0) return;
+        const int s = pos < NP ? slotf[st * kWideMaxPos + pos] : -1;
+        if (s >= 0) {
+            const uint32_t off = (uint32_t)(st * WL::STAGE_BYTES + pos * row_stride);
+            rx::bulk_g2s(sbase + WL::OFF_K + off, p.k_pool + (int64_t)s * row_elems, RB, bar + 8 * st);
+            rx::bulk_g2s(sbase + WL::OFF_V + off, p.v_pool + (int64_t)s * row_elems, RB, bar + 8 * st);
+        }
+    }
+}
+
+constexpr int kWideCopyWarps = 2;  // copy warps of the one-q-head-per-kv-head kernel
+
 template <int D, int LOG_NP, int HPW, int CW>
-__global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Params p)
+__global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide_kernel(const Params p)
 {
     using WL = WideLayout;
     constexpr int NP = 1 << LOG_NP;  // positions per stage
@@ -945,13 +986,16 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
             rx::mbar_init(bar + 8 * (kWideStages + i), CW);                 // consumer warps
         }
         for (int i = 0; i < 2; ++i) rx::mbar_init(bar + 8 * (2 * kWideStages + i), CW);  // q slot read
+        for (int i = 0; i < kWideStages; ++i) rx::mbar_init(bar + 8 * (WL::B_DESC + i), 1);  // producer
         *abort_flag = 0;
         rx::fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == 0) {
-        wide_producer<WL, NP>(p, smem, sbase, abort_flag, RB);
+        wide_producer<WL, NP, kWideCopyWarps>(p, smem, sbase, abort_flag, RB);
+    } else if (warp <= kWideCopyWarps) {
+        wide_copier<WL, NP, kWideCopyWarps>(p, smem, sbase, abort_flag, RB, warp - 1);
     } else {
         // consumers: warp cw owns q heads (= kv heads, G == 1) h0 .. h0 + HPW - 1.
         // A stage is taken in sub-stages of NPS positions: eight (head,
@@ -969,7 +1013,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1) decode_wide_kernel(const Par
         constexpr int NCH = DQ / 8;        // its 16-byte chunks (4 at d 128, 2 at d 64)
         constexpr int DO = D * HPW / 32;   // output dims per lane
         static_assert(NCH == 2 || NCH == 4, "quarter of 2 or 4 chunks");
-        const int cw = warp - 1;
+        const int cw = warp - 1 - kWideCopyWarps;
         const int h0 = cw * HPW;
         const int x = lane >> 2, qd = lane & 3;
         const int hh = x >> LOG_NPS, pi = x & (NPS - 1);
@@ -1115,9 +1159,10 @@ constexpr int kGqaNP = 16;                         // positions per stage
 constexpr int kGqaRowStride = 2048 + 16;           // slot row (8 kv heads x 128 x 2 at most) + pad
 using GqaLayout = WideLayoutT<3, kGqaNP * kGqaRowStride, 1>;
 constexpr int kGqaWarps = 8;                       // one consumer warp per kv head
+constexpr int kGqaCopyWarps = 2;                   // copy warps: 32 row copies a stage
 
 template <int D>
-__global__ void __launch_bounds__(32 * (1 + kGqaWarps), 1) decode_gqa_kernel(const Params p)
+__global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decode_gqa_kernel(const Params p)
 {
     using WL = GqaLayout;
     constexpr int KS = D / 16;   // k-steps of S = Q K^T
@@ -1135,16 +1180,21 @@ __global__ void __launch_bounds__(32 * (1 + kGqaWarps), 1) decode_gqa_kernel(con
             rx::mbar_init(bar + 8 * (WL::STAGES + i), kGqaWarps);   // consumer warps
         }
         rx::mbar_init(bar + 8 * (2 * WL::STAGES), kGqaWarps);       // q slot read
+        for (int i = 0; i < WL::STAGES; ++i) rx::mbar_init(bar + 8 * (WL::B_DESC + i), 1);  // producer
         *abort_flag = 0;
         rx::fence_mbar_init();
     }
     __syncthreads();
     if (warp == 0) {
-        wide_producer<WL, kGqaNP>(p, smem, sbase, abort_flag, kGqaRowStride);
+        wide_producer<WL, kGqaNP, kGqaCopyWarps>(p, smem, sbase, abort_flag, kGqaRowStride);
+        return;
+    }
+    if (warp <= kGqaCopyWarps) {
+        wide_copier<WL, kGqaNP, kGqaCopyWarps>(p, smem, sbase, abort_flag, kGqaRowStride, warp - 1);
         return;
     }
     // consumer warp: kv head g, q heads g * G .. g * G + G - 1 as rows 0 .. G - 1
-    const int g = warp - 1;
+    const int g = warp - 1 - kGqaCopyWarps;
     const int G = p.G;
     const int gid = lane >> 2, tig = lane & 3;
     const int2 *hdr = reinterpret_cast<const int2 *>(smem + WL::OFF_HDR);
@@ -1328,7 +1378,7 @@ int launch_decode_gqa(const Params &p, cudaStream_t st)
         configured = true;
     }
     const int grid = p.n_wide < num_sms() ? p.n_wide : num_sms();
-    decode_gqa_kernel<D><<<grid, 32 * (1 + kGqaWarps), GqaLayout::BYTES, st>>>(p);
+    decode_gqa_kernel<D><<<grid, 32 * (1 + kGqaCopyWarps + kGqaWarps), GqaLayout::BYTES, st>>>(p);
     RX_CUDA_CHECK(cudaGetLastError());
     return RX_OK;
 }
@@ -1343,7 +1393,7 @@ int launch_decode_wide_cfg(const Params &p, cudaStream_t st)
         configured = true;
     }
     const int grid = p.n_wide < num_sms() ? p.n_wide : num_sms();
-    decode_wide_kernel<D, LOG_NP, HPW, CW><<<grid, 32 * (1 + CW), WideLayout::BYTES, st>>>(p);
+    decode_wide_kernel<D, LOG_NP, HPW, CW><<<grid, 32 * (1 + kWideCopyWarps + CW), WideLayout::BYTES, st>>>(p);
     RX_CUDA_CHECK(cudaGetLastError());
     return RX_OK;
 }
