@@ -209,25 +209,35 @@ class GpuStep:
                                self.ext_req, self.ext_P, self.ext_E, self.rtt, self.max_E, p.sm_scale,
                                self.status, workspace=self.ext_ws)
 
+    def parts(self):
+        return [("store", self.kv_store)] + ([("extend", self.extend)] if self.has_ext else []) + \
+            ([("decode", self.decode)] if self.has_dec else [])
+
+    def capture(self):
+        """Captures each part of the step (after warm-up) as a CUDA graph;
+        replaying one runs the same kernels as the call, without the launch
+        gaps between them."""
+        torch = self.torch
+        self.graphs = {}
+        for name, fn in self.parts():
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            self.graphs[name] = g
+        torch.cuda.synchronize()
+
     def step(self, marks=None):
         """The whole path; ``marks`` (dict of event pairs) brackets the parts."""
-        if marks:
-            marks["store"][0].record()
-        self.kv_store()
-        if marks:
-            marks["store"][1].record()
-        if self.has_ext:
+        graphs = getattr(self, "graphs", None)
+        for name, fn in self.parts():
             if marks:
-                marks["extend"][0].record()
-            self.extend()
+                marks[name][0].record()
+            if graphs:
+                graphs[name].replay()
+            else:
+                fn()
             if marks:
-                marks["extend"][1].record()
-        if self.has_dec:
-            if marks:
-                marks["decode"][0].record()
-            self.decode()
-            if marks:
-                marks["decode"][1].record()
+                marks[name][1].record()
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -250,6 +260,12 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if int(st.status.item()) != 0:
         raise RuntimeError(f"device status {int(st.status.item())} after warm-up")
+    if args.graph:
+        st.capture()
+        for _ in range(args.warmup):
+            flush.zero_()
+            st.step()
+        torch.cuda.synchronize()
 
     E = torch.cuda.Event
     parts = ["store"] + (["extend"] if st.has_ext else []) + (["decode"] if st.has_dec else [])
@@ -333,7 +349,7 @@ def run_gpu(args, rank, world, local_rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random slot permutation)",
-        "config": workload_config(prob, args.workload, world, args.extend_path),
+        "config": workload_config(prob, args.workload, world, args.extend_path, getattr(args, "graph", False)),
         "roofline": roof, "e2e": e2e, "gpu_launches": st.launches * args.steps,
         "clocks": clk.summary(), "parts": out, "wall_s_timed_loop": round(t_wall, 3),
     }
@@ -421,12 +437,13 @@ def make_problem(args):
     return inputs.FULL_SIZE[args.workload](**kw)
 
 
-def workload_config(prob, name, world, extend_path="staged"):
+def workload_config(prob, name, world, extend_path="staged", graph=False):
     cfg = {"workload": name, "hq": prob.hq, "hkv": prob.hkv, "head_dim": prob.d,
            "pool_slots": prob.num_slots, "decode_requests": int(len(prob.dec_req_idx)),
            "extend_requests": int(len(prob.ext_req_idx)),
            "l2": "256 MiB buffer written between timed steps",
-           "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+           "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+           "launch": "CUDA graph per part" if graph else "direct calls"}
     if len(prob.dec_req_idx):
         cfg["decode_context"] = int(prob.dec_seq_len.max())
     if len(prob.ext_req_idx):
@@ -544,7 +561,7 @@ def run_reference(args, rank, world):
             "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16, random slot permutation)",
-            "config": workload_config(prob, args.workload, world, args.extend_path),
+            "config": workload_config(prob, args.workload, world, args.extend_path, getattr(args, "graph", False)),
             "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -562,6 +579,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="override the pool size (profiling runs on a smaller device footprint)")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each part of the timed step as a CUDA graph of the same calls")
     ap.add_argument("--extend-path", default="staged", choices=["staged", "gather"],
                     help="extend through a staging workspace (default) or gathering rows in the attention kernel")
     args = ap.parse_args()
