@@ -415,59 +415,36 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
         // different warp-collective tcgen05.ld instructions, so all lanes of
         // a warp must take the same one (the masked pass is exact for every row)
         const bool need_mask = __any_sync(0xffffffffu, kbase + kBN - 1 > row_lim);
-        // pass 1: the row max over the tile's visible keys, 64 scores (two
-        // loads in flight) at a time; the causal test only on tiles that
-        // cross the row's bound
-        float mx = -INFINITY;
-        auto max_pass = [&](auto masked) {
-            float mt0 = -INFINITY;
+        // the tile's kBN scores of this row, loaded once (four loads in
+        // flight) and kept in registers for the max and the exponentials;
+        // the causal test only on tiles that cross the row's bound
+        uint32_t sv[kBN];
 #pragma unroll
-            for (int hf = 0; hf < kBN / 64; ++hf) {
-                uint32_t sv[64];
-                rx::tmem_ld32(tS + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
-                rx::tmem_ld32(tS + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-                rx::tmem_wait_ld();
-                if (decltype(masked)::value) {
+        for (int c = 0; c < kBN / 32; ++c)
+            rx::tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
+        rx::tmem_wait_ld();
+        if (need_mask) {
 #pragma unroll
-                    for (int k = 0; k < 64; ++k)
-                        if (kbase + hf * 64 + k > row_lim) sv[k] = __float_as_uint(-INFINITY);
-                }
-                // 64 -> 22 -> 8 -> 3 -> 1 with three-input max
-                float m22[22], m8[8], m3[3];
+            for (int k = 0; k < kBN; ++k)
+                if (kbase + k > row_lim) sv[k] = __float_as_uint(-INFINITY);
+        }
+        // the row max: four running three-input maxima (few live registers
+        // next to the kBN scores)
+        float mx;
+        {
+            float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-                for (int k = 0; k < 21; ++k) m22[k] = rx::fmax3(u2f(sv[3 * k]), u2f(sv[3 * k + 1]), u2f(sv[3 * k + 2]));
-                m22[21] = u2f(sv[63]);
-#pragma unroll
-                for (int k = 0; k < 7; ++k) m8[k] = rx::fmax3(m22[3 * k], m22[3 * k + 1], m22[3 * k + 2]);
-                m8[7] = m22[21];
-                m3[0] = rx::fmax3(m8[0], m8[1], m8[2]);
-                m3[1] = rx::fmax3(m8[3], m8[4], m8[5]);
-                m3[2] = fmaxf(m8[6], m8[7]);
-                mt0 = rx::fmax3(mt0, rx::fmax3(m3[0], m3[1], m3[2]), -INFINITY);
+            for (int k = 0; k < kBN / 8; ++k) {
+                a0 = rx::fmax3(a0, u2f(sv[8 * k]), u2f(sv[8 * k + 1]));
+                a1 = rx::fmax3(a1, u2f(sv[8 * k + 2]), u2f(sv[8 * k + 3]));
+                a2 = rx::fmax3(a2, u2f(sv[8 * k + 4]), u2f(sv[8 * k + 5]));
+                a3 = rx::fmax3(a3, u2f(sv[8 * k + 6]), u2f(sv[8 * k + 7]));
             }
-            mx = mt0;
-        };
-        if (need_mask)
-            max_pass(std::true_type{});
-        else
-            max_pass(std::false_type{});
+            mx = rx::fmax3(fmaxf(a0, a1), a2, a3);
+        }
         const float m_new = fmaxf(m_used, mx * sl2);
         const bool need = (m_used == -INFINITY) || (m_new > m_used + kRescale);
         const float alpha = (need && m_used != -INFINITY) ? rx::fast_exp2(m_used - m_new) : 1.f;
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-            // rescale the O rows in TMEM: O += P V of tile j - 1 finished
-            // before S_t(j) was issued, and the next one waits for p_full
-#pragma unroll
-            for (int c4 = 0; c4 < D / 32; ++c4) {
-                uint32_t r[32];
-                rx::tmem_ld32(tO + c4 * 32, r);
-                rx::tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(u2f(r[k]) * alpha);
-                rx::tmem_st32(tO + c4 * 32, r);
-            }
-            rx::tmem_wait_st();
-        }
         if (need) {
             l *= alpha;
             m_used = m_new;
@@ -480,36 +457,37 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
         const float mu = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t scale2 = rx::f2(sl2, sl2), negm2 = rx::f2(-mu, -mu);
         uint64_t acc[4] = {0, 0, 0, 0};
-        auto exp_pass = [&](auto masked) {
 #pragma unroll
-            for (int c2 = 0; c2 < kBN / 64; ++c2) {
-                uint32_t sv[64];
-                rx::tmem_ld32(tS + c2 * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
-                rx::tmem_ld32(tS + c2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-                rx::tmem_wait_ld();
-                uint32_t pk[32];
+        for (int c2 = 0; c2 < kBN / 64; ++c2) {
+            uint32_t pk[32];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    float s0 = u2f(sv[2 * k]), s1 = u2f(sv[2 * k + 1]);
-                    if (decltype(masked)::value) {
-                        const int key = kbase + c2 * 64 + 2 * k;
-                        s0 = key <= row_lim ? s0 : -INFINITY;
-                        s1 = key + 1 <= row_lim ? s1 : -INFINITY;
-                    }
-                    float x0, x1;
-                    rx::f2_split(rx::f2_fma(rx::f2(s0, s1), scale2, negm2), x0, x1);
-                    const float e0 = rx::fast_exp2(x0), e1 = rx::fast_exp2(x1);  // -inf -> 0
-                    acc[k & 3] = rx::f2_add(acc[k & 3], rx::f2(e0, e1));
-                    pk[k] = rx::pack_bf16(e0, e1);
-                }
-                // columns c2 * 32 .. c2 * 32 + 31 hold scores already loaded above
-                rx::tmem_st32(tS + c2 * 32, pk);
+            for (int k = 0; k < 32; ++k) {
+                float x0, x1;
+                rx::f2_split(rx::f2_fma(rx::f2(u2f(sv[c2 * 64 + 2 * k]), u2f(sv[c2 * 64 + 2 * k + 1])), scale2, negm2),
+                             x0, x1);
+                const float e0 = rx::fast_exp2(x0), e1 = rx::fast_exp2(x1);  // -inf -> 0
+                acc[k & 3] = rx::f2_add(acc[k & 3], rx::f2(e0, e1));
+                pk[k] = rx::pack_bf16(e0, e1);
             }
-        };
-        if (need_mask)
-            exp_pass(std::true_type{});
-        else
-            exp_pass(std::false_type{});
+            // P over the first kBN / 2 columns: every score is in registers
+            rx::tmem_st32(tS + c2 * 32, pk);
+        }
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+            // rescale the O rows in TMEM (after the exponentials, when the
+            // scores no longer hold registers): O += P V of tile j - 1
+            // finished before S_t(j) was issued, and the next one waits for
+            // p_full
+#pragma unroll
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+                uint32_t r[32];
+                rx::tmem_ld32(tO + c4 * 32, r);
+                rx::tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(u2f(r[k]) * alpha);
+                rx::tmem_st32(tO + c4 * 32, r);
+            }
+            rx::tmem_wait_st();
+        }
         rx::tmem_wait_st();
         {
             float a0, a1;
