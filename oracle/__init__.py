@@ -15,6 +15,8 @@ Contents
                                ``attention``
   * ``merge_partials``      -- log-sum-exp combination of partial results
   * ``tree_ref.RadixTreeRef`` -- per-token trie with LRU eviction
+  * ``tree_ref.schedule`` / ``tree_ref.optimal_hit_rate`` -- cache-aware
+                               request order and the optimal cache hit rate
 
 Every function here is pinned in ``tests/test_oracle_pins.py`` and
 ``tests/test_tree_oracle.py``; none is "parity unpinned".

@@ -114,6 +114,11 @@ class RadixTreeRef:
         self._tick(path)
         return len(path), [t.slot for t in path]
 
+    def prefix_len(self, tokens: Sequence[int]) -> int:
+        """Longest cached prefix length of ``tokens``, as a probe: the clock
+        does not move and no node counts as used."""
+        return len(self._walk(tokens))
+
     def insert(self, tokens: Sequence[int], slots: Sequence[int]) -> int:
         """Cache ``tokens`` with ``slots``; returns how many leading tokens
         were already cached (those keep the tree's slots)."""
@@ -233,3 +238,44 @@ class RadixTreeRef:
             for t, c in n.children.items():
                 stack.append((c, acc + (t,)))
         return sorted(out)
+
+
+# ---------------------------------------------------------------------------
+# cache-aware scheduling
+# ---------------------------------------------------------------------------
+# "SGLang: Evaluación y resultados": the cache-aware scheduling reaches about
+# 96 % of the optimal cache hit rate on average.  The pages name no policy;
+# the plain reading: waiting requests with the longest cached prefix run
+# first, ties in arrival order.  The hit rate is the share of prompt tokens
+# found cached at admission; the optimum computes every distinct prefix token
+# exactly once (an unbounded cache, one request at a time).
+
+SCHED_FCFS = 0  # arrival order
+SCHED_LPM = 1   # longest cached prefix first
+
+
+def schedule(tree: RadixTreeRef, requests: Sequence[Sequence[int]], policy: int) -> Tuple[List[int], List[int]]:
+    """(order to run the waiting requests in, their cached prefix lengths)."""
+    lens = [tree.prefix_len(r) for r in requests]
+    order = list(range(len(requests)))
+    if policy == SCHED_LPM:
+        order.sort(key=lambda i: (-lens[i], i))
+    return order, lens
+
+
+def optimal_hit_rate(requests: Sequence[Sequence[int]]) -> float:
+    """1 - (distinct prefix tokens) / (prompt tokens): a token is computed
+    once per distinct prefix ending in it, i.e. once per node of the
+    per-token trie of all requests."""
+    root: dict = {}
+    distinct = total = 0
+    for r in requests:
+        node = root
+        for t in r:
+            total += 1
+            nxt = node.get(t)
+            if nxt is None:
+                nxt = node[t] = {}
+                distinct += 1
+            node = nxt
+    return 0.0 if total == 0 else 1.0 - distinct / total

@@ -33,6 +33,8 @@ RX_ERR_NOMEM = -3
 RX_ERR_NOT_ENOUGH = -4
 RX_ERR_CUDA = -5
 RX_ERR_UNSUPPORTED = -6
+RX_SCHED_FCFS = 0
+RX_SCHED_LPM = 1
 RX_DEV_BAD_SLOT = 1
 RX_DEV_BAD_LEN = 2
 
@@ -90,6 +92,8 @@ _sig("rx_slot_alloc_give", ctypes.c_int, _P, _P, _I64)
 _sig("rx_slot_alloc_free_count", _I64, _P)
 _sig("rx_admit", ctypes.c_int, _P, _P, _P, _I64, _P, _PI64, _PI64)
 _sig("rx_commit", ctypes.c_int, _P, _P, _P, _P, _I64, _I64)
+_sig("rx_prefix_len", ctypes.c_int, _P, _P, _I64, _PI64)
+_sig("rx_schedule", ctypes.c_int, _P, _P, _P, _I32, _I32, _P, _P)
 _sig("rx_kv_store", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I64, _P, _P)
 _sig("rx_attn_extend", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I32, _P, _P, _P, _P, _P,
      _I64, _I32, _I32, _P, ctypes.c_size_t, ctypes.c_float, _P, _P)
@@ -181,6 +185,13 @@ class RadixTree:
         _check(_lib.rx_lock_prefix(self._h, tp, len(t), int(delta), ctypes.byref(k)))
         return k.value
 
+    def prefix_len(self, tokens: Sequence[int]) -> int:
+        """Cached prefix length, without touching the LRU clock."""
+        t, tp = _np(tokens, np.int64)
+        k = ctypes.c_int64()
+        _check(_lib.rx_prefix_len(self._h, tp, len(t), ctypes.byref(k)))
+        return k.value
+
     def stats(self) -> Tuple[int, int, int]:
         a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
         _check(_lib.rx_tree_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
@@ -257,6 +268,21 @@ def rx_commit(tree: RadixTree, alloc: SlotAllocator, tokens: Sequence[int], row:
     t, tp = _np(tokens, np.int64)
     r, rp = _np(row, np.int32)
     _check(_lib.rx_commit(tree._h, alloc._h, tp, rp, len(t), int(prefix_len)))
+
+
+def rx_schedule(tree: RadixTree, requests: Sequence[Sequence[int]], policy: int):
+    """(order int32 [n], cached prefix lengths int64 [n]) for waiting requests."""
+    n = len(requests)
+    offs = np.zeros(n + 1, np.int64)
+    for i, r in enumerate(requests):
+        offs[i + 1] = offs[i] + len(r)
+    toks = np.concatenate([np.asarray(r, np.int64) for r in requests]) if n else np.zeros(0, np.int64)
+    toks = np.ascontiguousarray(toks, np.int64)
+    order = np.empty(max(1, n), np.int32)
+    plen = np.empty(max(1, n), np.int64)
+    _check(_lib.rx_schedule(tree._h, toks.ctypes.data_as(_P), offs.ctypes.data_as(_P), n, int(policy),
+                            order.ctypes.data_as(_P), plen.ctypes.data_as(_P)))
+    return order[:n], plen[:n]
 
 
 # ---------------------------------------------------------------------------

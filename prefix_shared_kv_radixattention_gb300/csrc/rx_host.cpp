@@ -304,6 +304,46 @@ extern "C" int rx_match_prefix(rx_tree *tree, const int64_t *tokens, int64_t n, 
     RX_CATCH
 }
 
+extern "C" int rx_prefix_len(rx_tree *tree, const int64_t *tokens, int64_t n, int64_t *out_len)
+{
+    if (!tree || n < 0 || (n > 0 && !tokens) || !out_len)
+        return rx_set_error(RX_ERR_INVALID, "rx_prefix_len: invalid argument");
+    RX_TRY
+    *out_len = tree->walk(tokens, n).matched;
+    return RX_OK;
+    RX_CATCH
+}
+
+// Cache-aware scheduling ("SGLang: Evaluación y resultados"): probe every
+// waiting request's cached prefix, then order them -- arrival order, or
+// longest cached prefix first with ties in arrival order (a stable sort).
+extern "C" int rx_schedule(rx_tree *tree, const int64_t *tokens, const int64_t *offsets, int32_t n_req,
+                           int32_t policy, int32_t *out_order, int64_t *out_prefix_len)
+{
+    if (!tree || n_req < 0 || (policy != RX_SCHED_FCFS && policy != RX_SCHED_LPM))
+        return rx_set_error(RX_ERR_INVALID, "rx_schedule: invalid argument");
+    if (n_req == 0) return RX_OK;
+    if (!offsets || !out_order || !out_prefix_len || offsets[0] != 0)
+        return rx_set_error(RX_ERR_INVALID, "rx_schedule: invalid argument");
+    for (int32_t i = 0; i < n_req; ++i)
+        if (offsets[i + 1] < offsets[i])
+            return rx_set_error(RX_ERR_INVALID, "rx_schedule: offsets decrease at request %d", i);
+    if (offsets[n_req] > 0 && !tokens) return rx_set_error(RX_ERR_INVALID, "rx_schedule: null tokens");
+    RX_TRY
+    std::vector<int64_t> len((size_t)n_req);
+    for (int32_t i = 0; i < n_req; ++i)
+        len[(size_t)i] = tree->walk(tokens + offsets[i], offsets[i + 1] - offsets[i]).matched;
+    std::vector<int32_t> order((size_t)n_req);
+    for (int32_t i = 0; i < n_req; ++i) order[(size_t)i] = i;
+    if (policy == RX_SCHED_LPM)
+        std::stable_sort(order.begin(), order.end(),
+                         [&](int32_t a, int32_t b) { return len[(size_t)a] > len[(size_t)b]; });
+    std::memcpy(out_order, order.data(), sizeof(int32_t) * (size_t)n_req);
+    std::memcpy(out_prefix_len, len.data(), sizeof(int64_t) * (size_t)n_req);
+    return RX_OK;
+    RX_CATCH
+}
+
 extern "C" int rx_insert(rx_tree *tree, const int64_t *tokens, const int32_t *slots, int64_t n,
                          int64_t *out_already_cached)
 {

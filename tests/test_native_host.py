@@ -20,6 +20,7 @@ from oracle.tree_ref import RadixTreeRef
 from prefix_shared_kv_radixattention_gb300 import binding as rx
 from prefix_shared_kv_radixattention_gb300 import inputs
 from tests import _walkthrough
+from tests.serving_sim import OracleAdmission
 from tests.test_tree_oracle import _apply, _random_ops
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "rx.h")
@@ -220,35 +221,6 @@ def test_invalid_arguments():
 # ---------------------------------------------------------------------------
 # admission
 # ---------------------------------------------------------------------------
-
-
-class OracleAdmission:
-    """rx_admit / rx_commit composed from the oracle trie and a FIFO list."""
-
-    def __init__(self, free):
-        self.t = RadixTreeRef()
-        self.free = list(free)
-
-    def admit(self, toks):
-        k, slots = self.t.match_prefix(toks)
-        self.t.lock(toks[:k], 1)
-        need = len(toks) - k
-        ev = 0
-        if len(self.free) < need:
-            got = self.t.evict(need - len(self.free))
-            ev = len(got)
-            self.free.extend(got)
-        if len(self.free) < need:
-            self.t.lock(toks[:k], -1)
-            return None, k, ev
-        new, self.free = self.free[:need], self.free[need:]
-        return list(slots) + new, k, ev
-
-    def commit(self, toks, row, k):
-        self.t.lock(toks[:k], -1)
-        c = self.t.insert(toks, row)
-        if c > k:
-            self.free.extend(row[k:c])
 
 
 @pytest.mark.parametrize("seed", range(12))
