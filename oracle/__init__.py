@@ -14,6 +14,7 @@ Contents
   * ``extend`` / ``decode`` -- the two query layouts of the path, mapped onto
                                ``attention``
   * ``merge_partials``      -- log-sum-exp combination of partial results
+  * ``rope`` / ``rope_f64``  -- rotary position embedding (rotate-half form)
   * ``tree_ref.RadixTreeRef`` -- per-token trie with LRU eviction
   * ``tree_ref.schedule`` / ``tree_ref.optimal_hit_rate`` -- cache-aware
                                request order and the optimal cache hit rate
@@ -104,6 +105,34 @@ def kv_store(k_pool: np.ndarray, v_pool: np.ndarray, k_new: np.ndarray, v_new: n
                              _ptr(slots), len(slots))
     if rc != 0:
         raise ValueError(f"oracle_kv_store: status {rc}")
+
+
+# ---------------------------------------------------------------------------
+# Rotary position embedding (not from the pages, which do not reach inside
+# the model: the position encoding the Llama-family models whose attention
+# shapes the workloads use apply to q and k before attention)
+# ---------------------------------------------------------------------------
+
+
+def rope_f64(x: np.ndarray, pos, base: float) -> np.ndarray:
+    """Rotate-half rotary embedding of x [n, heads, d] (fp64) at positions
+    pos [n]: for c < d/2, with theta_c = base^(-2c/d) and a = pos * theta_c,
+        x'[c]       = x[c] cos a - x[c + d/2] sin a
+        x'[c + d/2] = x[c + d/2] cos a + x[c] sin a."""
+    x = np.asarray(x, np.float64)
+    n, h, d = x.shape
+    half = d // 2
+    theta = float(base) ** (-2.0 * np.arange(half, dtype=np.float64) / d)
+    a = np.asarray(pos, np.float64).reshape(n, 1, 1) * theta.reshape(1, 1, half)
+    c, s = np.cos(a), np.sin(a)
+    lo, hi = x[..., :half], x[..., half:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
+
+
+def rope(x_bf16: np.ndarray, pos, base: float) -> np.ndarray:
+    """rope_f64 of bf16 bits (uint16 [n, heads, d]), widened exactly."""
+    bits = np.ascontiguousarray(x_bf16, dtype=np.uint16).astype(np.uint32) << 16
+    return rope_f64(bits.view(np.float32).astype(np.float64), pos, base)
 
 
 # ---------------------------------------------------------------------------

@@ -387,3 +387,56 @@ def test_pins_catch_mutant(name):
         assert any(caught), f"mutant {name} survived every pin"
     finally:
         shutil.rmtree(tmp)
+
+
+# ---------------------------------------------------------------------------
+# rotary position embedding
+# ---------------------------------------------------------------------------
+
+
+def test_rope_position_zero_is_identity():
+    x = np.random.default_rng(1).standard_normal((3, 2, 8))
+    assert np.array_equal(oracle.rope_f64(x, [0, 0, 0], 10000.0), x)
+
+
+def test_rope_worked_example():
+    """d = 4, base 100: pairs (0, 2) and (1, 3) turn by theta_0 = 1 and
+    theta_1 = 100^(-1/2) = 0.1 radians per position.  At position 1 the unit
+    vector e0 goes to (cos 1, 0, sin 1, 0) and e1 to (0, cos 0.1, 0, sin 0.1);
+    at position 2, e2 goes to (-sin 2, 0, cos 2, 0)."""
+    e = np.eye(4).reshape(4, 1, 4)
+    out = oracle.rope_f64(e, [1, 1, 2, 0], 100.0)
+    assert np.allclose(out[0, 0], [np.cos(1), 0, np.sin(1), 0], atol=1e-15)
+    assert np.allclose(out[1, 0], [0, np.cos(0.1), 0, np.sin(0.1)], atol=1e-15)
+    assert np.allclose(out[2, 0], [-np.sin(2), 0, np.cos(2), 0], atol=1e-15)
+    assert np.allclose(out[3, 0], [0, 0, 0, 1], atol=1e-15)
+
+
+def test_rope_keeps_pair_norms_and_composes():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((5, 3, 16))
+    pos = np.array([0, 7, 100, 4095, 32768])
+    y = oracle.rope_f64(x, pos, 10000.0)
+    half = 8
+    assert np.allclose(x[..., :half] ** 2 + x[..., half:] ** 2, y[..., :half] ** 2 + y[..., half:] ** 2)
+    # rotations compose: turning by a then by b is turning by a + b
+    z = oracle.rope_f64(oracle.rope_f64(x, pos, 10000.0), [3, 3, 3, 3, 3], 10000.0)
+    assert np.allclose(z, oracle.rope_f64(x, pos + 3, 10000.0), atol=1e-9)
+
+
+def test_rope_scores_depend_on_relative_position():
+    """q at position p and k at position p - r give the same score for every
+    p: the property that makes the embedding relative."""
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((1, 1, 32))
+    k = rng.standard_normal((1, 1, 32))
+    r = 5
+    scores = [float(np.sum(oracle.rope_f64(q, [p], 500000.0) * oracle.rope_f64(k, [p - r], 500000.0)))
+              for p in (5, 40, 1000, 30000)]
+    assert np.allclose(scores, scores[0], rtol=0, atol=1e-9)
+
+
+def test_rope_from_bf16_bits():
+    x = np.array([[[0x3F80, 0x0000, 0x4000, 0xBF80]]], np.uint16)  # 1, 0, 2, -1
+    out = oracle.rope(x, [0], 10000.0)
+    assert np.array_equal(out, np.array([[[1.0, 0.0, 2.0, -1.0]]]))
