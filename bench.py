@@ -138,7 +138,7 @@ class ClockSampler:
 class GpuStep:
     """Device state of one workload and the step that runs the path on it."""
 
-    def __init__(self, prob: inputs.Problem, torch, rx, extend_path: str = "staged"):
+    def __init__(self, prob: inputs.Problem, torch, rx, extend_path: str = "staged", rope_base: float = 0.0):
         self.torch, self.rx, self.prob = torch, rx, prob
         dev = "cuda"
         p = prob
@@ -193,9 +193,36 @@ class GpuStep:
                 nb = rx.rx_attn_extend_workspace(ctx, len(p.ext_req_idx), p.hkv, p.d)
                 self.ext_ws = torch.empty(nb, dtype=torch.uint8, device=dev)
                 self.launches += 2  # packed-row offsets + row copy
+        # rotary position embedding (optional): K rotated on its way into the
+        # pool, the step's q rows rotated in place
+        self.rope_base = rope_base
+        if rope_base:
+            pos_of = {}
+            for r in range(p.req_to_token.shape[0]):
+                for j, sl in enumerate(p.req_to_token[r]):
+                    if sl >= 0:
+                        pos_of[int(sl)] = j
+            self.pos_new = i32(np.array([pos_of[int(sl)] for sl in p.new_slots], np.int32))
+            if self.has_ext:
+                self.pos_ext = i32(np.concatenate([np.arange(P, P + E, dtype=np.int32) for P, E in
+                                                   zip(p.ext_prefix_len, p.ext_extend_len)]))
+                self.launches += 1
+            if self.has_dec:
+                self.pos_dec = i32(p.dec_seq_len - 1)
+                self.launches += 1
 
     def kv_store(self):
-        self.rx.rx_kv_store(self.k_pool, self.v_pool, self.k_new, self.v_new, self.slots, self.status)
+        if self.rope_base:
+            self.rx.rx_kv_store_rope(self.k_pool, self.v_pool, self.k_new, self.v_new, self.slots, self.pos_new,
+                                     self.rope_base, self.status)
+        else:
+            self.rx.rx_kv_store(self.k_pool, self.v_pool, self.k_new, self.v_new, self.slots, self.status)
+
+    def rope_q(self):
+        if self.has_ext:
+            self.rx.rx_rope(self.q_ext, self.pos_ext, self.rope_base)
+        if self.has_dec:
+            self.rx.rx_rope(self.q_dec, self.pos_dec, self.rope_base)
 
     def decode(self):
         p = self.prob
@@ -210,8 +237,8 @@ class GpuStep:
                                self.status, workspace=self.ext_ws)
 
     def parts(self):
-        return [("store", self.kv_store)] + ([("extend", self.extend)] if self.has_ext else []) + \
-            ([("decode", self.decode)] if self.has_dec else [])
+        return [("store", self.kv_store)] + ([("rope_q", self.rope_q)] if self.rope_base else []) + \
+            ([("extend", self.extend)] if self.has_ext else []) + ([("decode", self.decode)] if self.has_dec else [])
 
     def capture(self):
         """Captures each part of the step (after warm-up) as a CUDA graph;
@@ -250,7 +277,7 @@ def run_gpu(args, rank, world, local_rank):
         dist.init_process_group("nccl")
 
     prob = make_problem(args)
-    st = GpuStep(prob, torch, rx, args.extend_path)
+    st = GpuStep(prob, torch, rx, args.extend_path, args.rope)
     flush = torch.empty(L2_FLUSH_BYTES // 2, dtype=torch.bfloat16, device="cuda")
     torch.cuda.synchronize()
 
@@ -268,7 +295,7 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize()
 
     E = torch.cuda.Event
-    parts = ["store"] + (["extend"] if st.has_ext else []) + (["decode"] if st.has_dec else [])
+    parts = [name for name, _ in st.parts()]
     marks = [{k: (E(enable_timing=True), E(enable_timing=True)) for k in parts}
              for _ in range(args.steps)]
     steps_ev = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(args.steps)]
@@ -344,12 +371,20 @@ def run_gpu(args, rank, world, local_rank):
                     "peak_source": f"{peak_src} bf16_tflops (burst)"}
     out["kv_store"] = {"ms": statistics.mean(part_ms["store"]),
                        "gbs": 2 * len(prob.new_slots) * kv_row / (statistics.mean(part_ms["store"]) / 1e3) / 1e9}
+    if st.rope_base:
+        # K rotated inside the store (above); q rows rotated in place: read and
+        # write of every q row
+        q_bytes = 2 * (prob.q_ext.size + prob.q_dec.size) * 2
+        rq = statistics.mean(part_ms["rope_q"])
+        out["kv_store"]["rope_base"] = st.rope_base
+        out["rope_q"] = {"ms": rq, "gbs": q_bytes / (rq / 1e3) / 1e9}
     line = {
         "metric": f"prefix-shared attn: {metric}", "value": round(value, 3), "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random slot permutation)",
-        "config": workload_config(prob, args.workload, world, args.extend_path, getattr(args, "graph", False)),
+        "config": workload_config(prob, args.workload, world, args.extend_path, getattr(args, "graph", False),
+                                  getattr(args, "rope", 0.0)),
         "roofline": roof, "e2e": e2e, "gpu_launches": st.launches * args.steps,
         "clocks": clk.summary(), "parts": out, "wall_s_timed_loop": round(t_wall, 3),
     }
@@ -438,7 +473,7 @@ def make_problem(args):
     return inputs.FULL_SIZE[args.workload](**kw)
 
 
-def workload_config(prob, name, world, extend_path="staged", graph=False):
+def workload_config(prob, name, world, extend_path="staged", graph=False, rope=0.0):
     cfg = {"workload": name, "hq": prob.hq, "hkv": prob.hkv, "head_dim": prob.d,
            "pool_slots": prob.num_slots, "decode_requests": int(len(prob.dec_req_idx)),
            "extend_requests": int(len(prob.ext_req_idx)),
@@ -451,6 +486,8 @@ def workload_config(prob, name, world, extend_path="staged", graph=False):
         cfg["extend_prefix"] = int(prob.ext_prefix_len.max())
         cfg["extend_new"] = int(prob.ext_extend_len.max())
         cfg["extend_path"] = extend_path
+    if rope:
+        cfg["rope_base"] = rope
     return cfg
 
 
@@ -562,7 +599,8 @@ def run_reference(args, rank, world):
             "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16, random slot permutation)",
-            "config": workload_config(prob, args.workload, world, args.extend_path, getattr(args, "graph", False)),
+            "config": workload_config(prob, args.workload, world, args.extend_path, getattr(args, "graph", False),
+                                  getattr(args, "rope", 0.0)),
             "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -580,6 +618,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="override the pool size (profiling runs on a smaller device footprint)")
+    ap.add_argument("--rope", type=float, default=0.0, metavar="BASE",
+                    help="add rotary position embedding to the step (K fused into the store, q in place)")
     ap.add_argument("--graph", action="store_true",
                     help="replay each part of the timed step as a CUDA graph of the same calls")
     ap.add_argument("--extend-path", default="staged", choices=["staged", "gather"],

@@ -208,7 +208,11 @@ int rx_prefix_len(rx_tree *tree, const int64_t *tokens, int64_t n, int64_t *out_
 int rx_schedule(rx_tree *tree, const int64_t *tokens, const int64_t *offsets, int32_t n_req, int32_t policy,
                 int32_t *out_order, int64_t *out_prefix_len);
 
-/* ---- KV pool (device) ---------------------------------------------------- */
+/* ---- KV pool (device) ----------------------------------------------------
+ * One layer's K and V.  A model's pools for L layers may share one
+ * allocation each, [L, num_slots, num_kv_heads, head_dim]: layer l's pool is
+ * k = base_k + l * num_slots * num_kv_heads * head_dim elements (v alike),
+ * and the same slot ids and req_to_token rows serve every layer. */
 typedef struct {
     void *k;              /* device bf16 [num_slots, num_kv_heads, head_dim] */
     void *v;              /* device bf16, same shape                         */
@@ -225,6 +229,29 @@ typedef struct {
  * "Introducción a SGLang", RadixAttention bullet. */
 int rx_kv_store(const rx_kv_pool *pool, const void *k_new, const void *v_new, const int32_t *slots,
                 int64_t n, int32_t *dev_status, void *stream);
+
+/* ---- rotary position embedding (device) --------------------------------
+ * Not from the pages, which do not reach inside the model: the position
+ * encoding that the Llama-family models whose attention shapes the workloads
+ * take apply to q and k before attention, in its rotate-half form.  For a
+ * token at position p, every head, and c < head_dim / 2, with
+ * theta_c = base^(-2c / head_dim) and a = p * theta_c:
+ *     x'[c]                = x[c] cos a - x[c + head_dim/2] sin a
+ *     x'[c + head_dim / 2] = x[c + head_dim/2] cos a + x[c] sin a
+ * Angles are formed in double precision (theta_c tabulated on the host, a
+ * reduced modulo 2 pi), the rotation in fp32, results rounded to bf16.
+ * head_dim 64 or 128; base > 1 (10000 and 500000 are usual). */
+
+/* In place on x: device bf16 [n, heads, head_dim], 16-byte aligned; pos:
+ * device int32 [n], the tokens' positions. */
+int rx_rope(void *x, const int32_t *pos, int64_t n, int32_t heads, int32_t head_dim, double base,
+            void *stream);
+
+/* rx_kv_store with K rotated on the way into the pool: K[slots[i]] =
+ * rope(k_new[i], pos[i]) as rx_rope computes it, V[slots[i]] = v_new[i].
+ * Same buffers and errors as rx_kv_store, plus pos: device int32 [n]. */
+int rx_kv_store_rope(const rx_kv_pool *pool, const void *k_new, const void *v_new, const int32_t *slots,
+                     const int32_t *pos, int64_t n, double base, int32_t *dev_status, void *stream);
 
 /* Extend attention.  Request b (b < batch) has prefix_len[b] cached tokens and
  * extend_len[b] new ones whose K/V are already in the pool; the slot list is

@@ -95,6 +95,8 @@ _sig("rx_commit", ctypes.c_int, _P, _P, _P, _P, _I64, _I64)
 _sig("rx_prefix_len", ctypes.c_int, _P, _P, _I64, _PI64)
 _sig("rx_schedule", ctypes.c_int, _P, _P, _P, _I32, _I32, _P, _P)
 _sig("rx_kv_store", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I64, _P, _P)
+_sig("rx_rope", ctypes.c_int, _P, _P, _I64, _I32, _I32, ctypes.c_double, _P)
+_sig("rx_kv_store_rope", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _P, _I64, ctypes.c_double, _P, _P)
 _sig("rx_attn_extend", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I32, _P, _P, _P, _P, _P,
      _I64, _I32, _I32, _P, ctypes.c_size_t, ctypes.c_float, _P, _P)
 _sig("rx_attn_extend_workspace", ctypes.c_size_t, _I64, _I32, _I32, _I32)
@@ -340,6 +342,32 @@ def rx_kv_store(k_pool, v_pool, k_new, v_new, slots, dev_status=None, stream=Non
         raise ValueError("k_new/v_new must be [n, num_kv_heads, head_dim]")
     _check(_lib.rx_kv_store(ctypes.byref(pool), _ptr(k_new), _ptr(v_new), _ptr(slots), n,
                             _ptr(dev_status), _stream(stream)))
+
+
+def rx_rope(x, pos, base: float, stream=None) -> None:
+    """In place on x (bf16 [n, heads, head_dim]) at positions pos (int32 [n])."""
+    torch = _torch()
+    _dev(x, torch.bfloat16, "x")
+    _dev(pos, torch.int32, "pos")
+    if x.dim() != 3 or pos.numel() != x.shape[0]:
+        raise ValueError("x must be [n, heads, head_dim] and pos [n]")
+    _check(_lib.rx_rope(_ptr(x), _ptr(pos), x.shape[0], x.shape[1], x.shape[2], float(base), _stream(stream)))
+
+
+def rx_kv_store_rope(k_pool, v_pool, k_new, v_new, slots, pos, base: float, dev_status=None,
+                     stream=None) -> None:
+    torch = _torch()
+    pool = make_pool(k_pool, v_pool)
+    _dev(k_new, torch.bfloat16, "k_new")
+    _dev(v_new, torch.bfloat16, "v_new")
+    _dev(slots, torch.int32, "slots")
+    _dev(pos, torch.int32, "pos")
+    _dev(dev_status, torch.int32, "dev_status")
+    n = slots.numel()
+    if k_new.numel() != n * pool.num_kv_heads * pool.head_dim or k_new.shape != v_new.shape or pos.numel() != n:
+        raise ValueError("k_new/v_new must be [n, num_kv_heads, head_dim] and pos [n]")
+    _check(_lib.rx_kv_store_rope(ctypes.byref(pool), _ptr(k_new), _ptr(v_new), _ptr(slots), _ptr(pos), n,
+                                 float(base), _ptr(dev_status), _stream(stream)))
 
 
 def rx_attn_extend_workspace(total_ctx_tokens: int, batch: int, num_kv_heads: int, head_dim: int) -> int:

@@ -210,6 +210,12 @@ def test_invalid_arguments():
     assert lib.rx_attn_extend_workspace(-1, 1, 8, 128) == 0
     assert lib.rx_attn_extend_workspace(100, 0, 8, 128) == 0
     assert lib.rx_attn_extend_workspace(100, 1, 8, 96) == 0
+    base = ctypes.c_double(10000.0)
+    assert lib.rx_rope(None, None, 0, 4, 96, base, None) == rx.RX_ERR_UNSUPPORTED
+    assert lib.rx_rope(None, None, 0, 4, 64, ctypes.c_double(1.0), None) == rx.RX_ERR_UNSUPPORTED
+    assert lib.rx_rope(None, None, 5, 4, 64, base, None) == rx.RX_ERR_INVALID
+    assert lib.rx_rope(None, None, 0, 4, 64, base, None) == rx.RX_OK  # nothing to do
+    assert lib.rx_kv_store_rope(None, None, None, None, None, 0, base, None, None) == rx.RX_ERR_INVALID
     with pytest.raises(rx.RxError):
         rx.SlotAllocator([0, 5], 3)
     a = rx.SlotAllocator([0, 1, 2], 3)
