@@ -208,6 +208,20 @@ int rx_prefix_len(rx_tree *tree, const int64_t *tokens, int64_t n, int64_t *out_
 int rx_schedule(rx_tree *tree, const int64_t *tokens, const int64_t *offsets, int32_t n_req, int32_t policy,
                 int32_t *out_order, int64_t *out_prefix_len);
 
+/* ---- multimodal keys (host) ---------------------------------------------
+ * Source: "SGLang: Efficient Execution of Structured Language Model
+ * Programs" (unite.ai, es), "SGLang: Evaluación y resultados", multimodal
+ * results: RadixAttention computes the hash of each input image and uses it
+ * as the key in the radix tree, so requests about the same image reuse the
+ * KV of its tokens.  rx_image_keys gives the keys of the n_tokens positions an
+ * image occupies in a request's key sequence: key i (0-based) is output i + 1
+ * of the SplitMix64 generator seeded with the 64-bit FNV-1a hash of the
+ * image's bytes, with the top bit set -- negative as int64, so no image key
+ * equals a text token id (those are >= 0).  Identical bytes give identical
+ * keys; other bytes give other keys except with probability about
+ * n_tokens^2 / 2^63.  out_keys: host int64 [n_tokens]. */
+int rx_image_keys(const uint8_t *data, int64_t nbytes, int64_t n_tokens, int64_t *out_keys);
+
 /* ---- KV pool (device) ----------------------------------------------------
  * One layer's K and V.  A model's pools for L layers may share one
  * allocation each, [L, num_slots, num_kv_heads, head_dim]: layer l's pool is

@@ -18,6 +18,7 @@ Contents
   * ``tree_ref.RadixTreeRef`` -- per-token trie with LRU eviction
   * ``tree_ref.schedule`` / ``tree_ref.optimal_hit_rate`` -- cache-aware
                                request order and the optimal cache hit rate
+  * ``keys.image_keys``       -- radix-tree keys of an image's tokens
 
 Every function here is pinned in ``tests/test_oracle_pins.py`` and
 ``tests/test_tree_oracle.py``; none is "parity unpinned".

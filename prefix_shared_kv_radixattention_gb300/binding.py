@@ -93,6 +93,7 @@ _sig("rx_slot_alloc_free_count", _I64, _P)
 _sig("rx_admit", ctypes.c_int, _P, _P, _P, _I64, _P, _PI64, _PI64)
 _sig("rx_commit", ctypes.c_int, _P, _P, _P, _P, _I64, _I64)
 _sig("rx_prefix_len", ctypes.c_int, _P, _P, _I64, _PI64)
+_sig("rx_image_keys", ctypes.c_int, _P, _I64, _I64, _P)
 _sig("rx_schedule", ctypes.c_int, _P, _P, _P, _I32, _I32, _P, _P)
 _sig("rx_kv_store", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I64, _P, _P)
 _sig("rx_rope", ctypes.c_int, _P, _P, _I64, _I32, _I32, ctypes.c_double, _P)
@@ -270,6 +271,15 @@ def rx_commit(tree: RadixTree, alloc: SlotAllocator, tokens: Sequence[int], row:
     t, tp = _np(tokens, np.int64)
     r, rp = _np(row, np.int32)
     _check(_lib.rx_commit(tree._h, alloc._h, tp, rp, len(t), int(prefix_len)))
+
+
+def rx_image_keys(data: bytes, n_tokens: int) -> np.ndarray:
+    """int64 keys of the n_tokens positions an image (its raw bytes) occupies."""
+    buf = np.frombuffer(bytes(data), dtype=np.uint8)
+    out = np.empty(max(1, n_tokens), np.int64)
+    _check(_lib.rx_image_keys(buf.ctypes.data_as(_P) if len(buf) else None, len(buf), int(n_tokens),
+                              out.ctypes.data_as(_P)))
+    return out[:n_tokens]
 
 
 def rx_schedule(tree: RadixTree, requests: Sequence[Sequence[int]], policy: int):

@@ -344,6 +344,33 @@ extern "C" int rx_schedule(rx_tree *tree, const int64_t *tokens, const int64_t *
     RX_CATCH
 }
 
+// Image keys ("SGLang: Evaluación y resultados": an image's hash is its key
+// in the radix tree): the FNV-1a 64-bit hash of the bytes (offset basis
+// 0xcbf29ce484222325, prime 0x100000001b3) seeds a SplitMix64 generator
+// (increment 0x9e3779b97f4a7c15, its published finaliser); output i + 1 with
+// the top bit set is the key of image token i.
+extern "C" int rx_image_keys(const uint8_t *data, int64_t nbytes, int64_t n_tokens, int64_t *out_keys)
+{
+    if (nbytes < 0 || n_tokens < 0 || (nbytes > 0 && !data) || (n_tokens > 0 && !out_keys))
+        return rx_set_error(RX_ERR_INVALID, "rx_image_keys: invalid argument");
+    uint64_t h = 0xcbf29ce484222325ull;
+    for (int64_t i = 0; i < nbytes; ++i) {
+        h ^= (uint64_t)data[i];
+        h *= 0x100000001b3ull;
+    }
+    uint64_t state = h;
+    for (int64_t i = 0; i < n_tokens; ++i) {
+        state += 0x9e3779b97f4a7c15ull;
+        uint64_t z = state;
+        z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+        z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+        z ^= z >> 31;
+        z |= 0x8000000000000000ull;
+        std::memcpy(out_keys + i, &z, sizeof(z));
+    }
+    return RX_OK;
+}
+
 extern "C" int rx_insert(rx_tree *tree, const int64_t *tokens, const int32_t *slots, int64_t n,
                          int64_t *out_already_cached)
 {
