@@ -5,9 +5,10 @@
 A step is one pass of the whole path over one batch of synthetic input: the
 KV store of the step's new tokens, then the attention the workload needs
 (decode with its decode plan, and/or extend).  Inputs are resident in HBM
-before timing starts; a 256 MiB buffer is written between timed steps so that
-no KV survives in L2 (129 MB); each step is timed with CUDA events on the
-launching stream.  The decode plan is built once, before timing, from the
+before timing starts; between timed steps a 256 MiB buffer is written, so that
+no KV survives in L2 (129 MB), and a second 256 MiB buffer is read, so that the
+lines the write left dirty are written back before the step rather than
+inside it; each step is timed with CUDA events on the launching stream.  The decode plan is built once, before timing, from the
 host copy of req_to_token (the sharing structure is fixed for the batch).
 
 Workloads (default: few_shot_decode, the configuration the headline metric
@@ -278,11 +279,11 @@ def run_gpu(args, rank, world, local_rank):
 
     prob = make_problem(args)
     st = GpuStep(prob, torch, rx, args.extend_path, args.rope)
-    flush = torch.empty(L2_FLUSH_BYTES // 2, dtype=torch.bfloat16, device="cuda")
+    flush = L2Flush(torch)
     torch.cuda.synchronize()
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         st.step()
     torch.cuda.synchronize()
     if int(st.status.item()) != 0:
@@ -290,7 +291,7 @@ def run_gpu(args, rank, world, local_rank):
     if args.graph:
         st.capture()
         for _ in range(args.warmup):
-            flush.zero_()
+            flush()
             st.step()
         torch.cuda.synchronize()
 
@@ -305,7 +306,7 @@ def run_gpu(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         t_wall = time.perf_counter()
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             steps_ev[i][0].record()
             st.step(marks[i])
             steps_ev[i][1].record()
@@ -404,6 +405,23 @@ def max_over_ranks(value: float, dist=None, device="cpu") -> float:
     return float(t.item())
 
 
+class L2Flush:
+    """Run between timed steps: writes a buffer twice the size of L2 (no input
+    of the step stays cached), then reads another one of the same size, which
+    evicts the dirty lines of the write (the step would otherwise pay for
+    writing them back) and leaves L2 holding clean lines of no use to it."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 2, dtype=torch.bfloat16, device="cuda")
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.acc = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.w.zero_()
+        self.torch.sum(self.r, dim=0, out=self.acc)
+
+
 def job_throughput(units_per_rank_step: float, world: int, steps: int, max_ms: float) -> float:
     """Whole-job units per second: every rank's units over the slowest rank's
     time (weak scaling: each rank carries the full per-GPU workload)."""
@@ -431,7 +449,7 @@ def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
     E = torch.cuda.Event
     ev = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(n)]
     for i in range(n):
-        flush.zero_()
+        flush()
         ev[i][0].record()
         for h, d in zip(h_in, d_in):
             d.copy_(h, non_blocking=True)
@@ -477,7 +495,8 @@ def workload_config(prob, name, world, extend_path="staged", graph=False, rope=0
     cfg = {"workload": name, "hq": prob.hq, "hkv": prob.hkv, "head_dim": prob.d,
            "pool_slots": prob.num_slots, "decode_requests": int(len(prob.dec_req_idx)),
            "extend_requests": int(len(prob.ext_req_idx)),
-           "l2": "256 MiB buffer written between timed steps",
+           "l2": "between timed steps: 256 MiB written (evicts the step's inputs), then 256 MiB read "
+                 "(evicts the write's dirty lines)",
            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
            "launch": "CUDA graph per part" if graph else "direct calls"}
     if len(prob.dec_req_idx):

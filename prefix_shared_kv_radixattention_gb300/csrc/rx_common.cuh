@@ -81,6 +81,28 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Programmatic dependent launch (PTX griddepcontrol).  A kernel launched with
+// programmatic stream serialization may start once every CTA of the kernel
+// before it on the stream has executed launch_dependents (or exited); it
+// must then call pdl_wait before it reads what that kernel writes.  pdl_wait
+// returns once the grids this one depends on have completed and their
+// writes are visible; for a kernel launched the ordinary way it returns at
+// once.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+// Held by every thread of a dependent kernel that does not wait up front:
+// the thread waits for the grids before it on its way out, so this grid
+// completes only after them and a kernel that waits on it waits on them too.
+struct PdlWaitOnExit {
+    __device__ ~PdlWaitOnExit() { pdl_wait(); }
+};
+
 // 2^x with the hardware approximation (ex2.approx); -inf -> 0.
 __device__ __forceinline__ float fast_exp2(float x)
 {

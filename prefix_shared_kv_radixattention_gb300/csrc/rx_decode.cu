@@ -588,6 +588,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p)
     using L = Layout<D>;
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t bar = rx::smem_u32(smem + L::OFF_BAR);
+    // the kernels after this one in the call do not wait for it to start
+    // (the all-heads kernel) or wait for it in their own code (the merge)
+    rx::pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < L::NST; ++s) {
             rx::mbar_init(bar + 8 * (L::B_FULL + s), 32 * kCopiers);  // copier lanes' copies
@@ -647,11 +650,15 @@ __global__ void __launch_bounds__(128) merge_kernel(const Params p, int use_plan
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 4 + warp;
-    if (row >= (int64_t)p.batch * p.hq) return;
-    const int b = (int)(row / p.hq);
-    const int np = use_plan ? __ldg(p.nparts + b)
-                            : (int)((__ldg(p.seq_len + b) + p.chunk - 1) / p.chunk);
-    if (np <= 1 || np > p.max_parts) return;  // > max_parts: flagged by the decode kernel
+    const bool live = row < (int64_t)p.batch * p.hq;
+    int np = 0;
+    if (live) {  // the plan and the lengths are inputs: read before the wait
+        const int b = (int)(row / p.hq);
+        np = use_plan ? __ldg(p.nparts + b) : (int)((__ldg(p.seq_len + b) + p.chunk - 1) / p.chunk);
+    }
+    // the partials are written by the decode kernels just before this one
+    rx::pdl_wait();
+    if (!live || np <= 1 || np > p.max_parts) return;  // > max_parts: flagged by the decode kernel
     const float *lp = p.ws_lse + row * p.max_parts;
     float m = -INFINITY;
     for (int i = lane; i < np; i += 32) m = fmaxf(m, lp[i]);
@@ -980,6 +987,10 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
     int *okf = reinterpret_cast<int *>(smem + WL::OFF_OK);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int RB = p.hkv * D * 2;          // bytes of one slot row
+    // runs beside the per-head kernel (it reads none of that kernel's
+    // results) and ends after it; the merge may be launched at once
+    rx::PdlWaitOnExit ends_after_per_head;
+    rx::pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int i = 0; i < kWideStages; ++i) {
             rx::mbar_init(bar + 8 * i, 1);                                  // producer + bytes
@@ -1174,6 +1185,8 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
     const uint32_t bar = sbase + WL::OFF_BAR;  // full: [0, S), empty: [S, 2S), q_empty: [2S]
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + WL::OFF_ABORT);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    rx::PdlWaitOnExit ends_after_per_head;  // as in the one-q-head kernel
+    rx::pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int i = 0; i < WL::STAGES; ++i) {
             rx::mbar_init(bar + 8 * i, 1);                          // producer + bytes
@@ -1368,8 +1381,31 @@ bool gqa_supported(int hq, int hkv, int D)
     return rx_gqa_heads(hq, hkv) && (D == 64 || D == 128) && hq * D * 2 <= GqaLayout::QBYTES;
 }
 
+// Launches `kernel` on `st`.  With `dependent`, it is launched as a
+// programmatic dependent of the kernel enqueued just before it on `st`: it
+// may start while that kernel runs, and orders itself with pdl_wait (see
+// rx_common.cuh).  One stream carries the whole call, so its kernels need no
+// events between them.
+template <typename... KArgs, typename... Args>
+int launch_on(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+              bool dependent, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    RX_CUDA_CHECK(cudaLaunchKernelEx(&cfg, kernel, args...));
+    return RX_OK;
+}
+
 template <int D>
-int launch_decode_gqa(const Params &p, cudaStream_t st)
+int launch_decode_gqa(const Params &p, cudaStream_t st, bool dependent)
 {
     static bool configured = false;
     if (!configured) {
@@ -1378,13 +1414,12 @@ int launch_decode_gqa(const Params &p, cudaStream_t st)
         configured = true;
     }
     const int grid = p.n_wide < num_sms() ? p.n_wide : num_sms();
-    decode_gqa_kernel<D><<<grid, 32 * (1 + kGqaCopyWarps + kGqaWarps), GqaLayout::BYTES, st>>>(p);
-    RX_CUDA_CHECK(cudaGetLastError());
-    return RX_OK;
+    return launch_on(decode_gqa_kernel<D>, grid, 32 * (1 + kGqaCopyWarps + kGqaWarps), GqaLayout::BYTES, st,
+                     dependent, p);
 }
 
 template <int D, int LOG_NP, int HPW, int CW>
-int launch_decode_wide_cfg(const Params &p, cudaStream_t st)
+int launch_decode_wide_cfg(const Params &p, cudaStream_t st, bool dependent)
 {
     static bool configured = false;
     if (!configured) {
@@ -1393,9 +1428,8 @@ int launch_decode_wide_cfg(const Params &p, cudaStream_t st)
         configured = true;
     }
     const int grid = p.n_wide < num_sms() ? p.n_wide : num_sms();
-    decode_wide_kernel<D, LOG_NP, HPW, CW><<<grid, 32 * (1 + kWideCopyWarps + CW), WideLayout::BYTES, st>>>(p);
-    RX_CUDA_CHECK(cudaGetLastError());
-    return RX_OK;
+    return launch_on(decode_wide_kernel<D, LOG_NP, HPW, CW>, grid, 32 * (1 + kWideCopyWarps + CW),
+                     WideLayout::BYTES, st, dependent, p);
 }
 
 // Wide items need one q head per kv head and 8, 16, 32 or 64 heads: the
@@ -1407,22 +1441,23 @@ bool wide_supported(int hq, int hkv, int D)
 }
 
 template <int D>
-int launch_decode_wide(const Params &p, cudaStream_t st)
+int launch_decode_wide(const Params &p, cudaStream_t st, bool dependent)
 {
     constexpr int L0 = D == 128 ? 4 : 5;  // log2 positions per stage at 8 heads
     switch (p.hq) {
-    case 8: return launch_decode_wide_cfg<D, L0, 1, 8>(p, st);
-    case 16: return launch_decode_wide_cfg<D, L0 - 1, 1, 16>(p, st);
-    case 32: return launch_decode_wide_cfg<D, L0 - 2, 2, 16>(p, st);
-    default: return launch_decode_wide_cfg<D, L0 - 3, 4, 16>(p, st);
+    case 8: return launch_decode_wide_cfg<D, L0, 1, 8>(p, st, dependent);
+    case 16: return launch_decode_wide_cfg<D, L0 - 1, 1, 16>(p, st, dependent);
+    case 32: return launch_decode_wide_cfg<D, L0 - 2, 2, 16>(p, st, dependent);
+    default: return launch_decode_wide_cfg<D, L0 - 3, 4, 16>(p, st, dependent);
     }
 }
 
 // the all-heads kernel for the plan's single-request items
-int launch_all_heads(const Params &p, int D, cudaStream_t st)
+int launch_all_heads(const Params &p, int D, cudaStream_t st, bool dependent)
 {
-    if (p.G == 1) return D == 128 ? launch_decode_wide<128>(p, st) : launch_decode_wide<64>(p, st);
-    return D == 128 ? launch_decode_gqa<128>(p, st) : launch_decode_gqa<64>(p, st);
+    if (p.G == 1)
+        return D == 128 ? launch_decode_wide<128>(p, st, dependent) : launch_decode_wide<64>(p, st, dependent);
+    return D == 128 ? launch_decode_gqa<128>(p, st, dependent) : launch_decode_gqa<64>(p, st, dependent);
 }
 
 template <int D, bool PLAN>
@@ -1436,47 +1471,14 @@ int launch_decode(const Params &p, cudaStream_t st)
         configured = true;
     }
     const int grid = p.total_work < num_sms() ? p.total_work : num_sms();
-    decode_kernel<D, PLAN><<<grid, kThreads, Layout<D>::BYTES, st>>>(p);
-    RX_CUDA_CHECK(cudaGetLastError());
-    return RX_OK;
-}
-
-// A second stream and two events per device for running the per-head and
-// the wide kernel side by side inside one rx_attn_decode call.  Created on
-// first use; the mutex keeps each call's record/wait pairs together when
-// several host threads call at once.
-struct ForkJoin {
-    cudaStream_t side = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-std::mutex &fork_mutex()
-{
-    static std::mutex m;
-    return m;
-}
-int fork_join_for_current_device(ForkJoin **out)
-{
-    static ForkJoin per_dev[64];
-    int dev = 0;
-    RX_CUDA_CHECK(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 64) return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_decode: device %d", dev);
-    ForkJoin &f = per_dev[dev];
-    if (!f.side) {
-        RX_CUDA_CHECK(cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking));
-        RX_CUDA_CHECK(cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming));
-        RX_CUDA_CHECK(cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming));
-    }
-    *out = &f;
-    return RX_OK;
+    return launch_on(decode_kernel<D, PLAN>, grid, kThreads, Layout<D>::BYTES, st, false, p);
 }
 
 template <int D>
 int launch_merge(const Params &p, int use_plan, cudaStream_t st)
 {
     const int64_t rows = (int64_t)p.batch * p.hq;
-    merge_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(p, use_plan);
-    RX_CUDA_CHECK(cudaGetLastError());
-    return RX_OK;
+    return launch_on(merge_kernel<D>, (unsigned)((rows + 3) / 4), 128, 0, st, true, p, use_plan);
 }
 
 }  // namespace
@@ -1599,27 +1601,15 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
         if (D == 128) return plan ? launch_decode<128, true>(p, s) : launch_decode<128, false>(p, s);
         return plan ? launch_decode<64, true>(p, s) : launch_decode<64, false>(p, s);
     };
-    if (p.n_wide == 0) {
-        if (p.total_work > 0) rc = per_head(st);
-    } else {
-        // the per-head items (shared segments) and the wide items run side by
-        // side: the per-head kernel on a second stream forked from and joined
-        // back into the caller's stream, the wide kernel on the caller's
-        RX_CUDA_CHECK(cudaMemsetAsync(p.wide_counter, 0, sizeof(int), st));
-        if (p.total_work > 0) {
-            std::lock_guard<std::mutex> g(fork_mutex());
-            ForkJoin *fj = nullptr;
-            if ((rc = fork_join_for_current_device(&fj)) != RX_OK) return rc;
-            RX_CUDA_CHECK(cudaEventRecord(fj->fork, st));
-            RX_CUDA_CHECK(cudaStreamWaitEvent(fj->side, fj->fork, 0));
-            rc = per_head(fj->side);
-            if (rc == RX_OK) rc = launch_all_heads(p, D, st);
-            RX_CUDA_CHECK(cudaEventRecord(fj->join, fj->side));
-            RX_CUDA_CHECK(cudaStreamWaitEvent(st, fj->join, 0));
-        } else {
-            rc = launch_all_heads(p, D, st);
-        }
-    }
+    // One stream, up to three kernels.  The per-head items (shared segments)
+    // and the single-request items run side by side: the all-heads kernel is
+    // a programmatic dependent of the per-head kernel, which lets it start at
+    // once; it reads nothing the per-head kernel writes and ends after it.
+    // The merge is a dependent of the last of them and waits for it (and so
+    // for both) before it reads their partial results.
+    if (p.n_wide > 0) RX_CUDA_CHECK(cudaMemsetAsync(p.wide_counter, 0, sizeof(int), st));
+    if (p.total_work > 0) rc = per_head(st);
+    if (rc == RX_OK && p.n_wide > 0) rc = launch_all_heads(p, D, st, p.total_work > 0);
     if (rc != RX_OK || !merge) return rc;
     return D == 128 ? launch_merge<128>(p, plan != nullptr, st) : launch_merge<64>(p, plan != nullptr, st);
 }
