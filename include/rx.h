@@ -321,7 +321,7 @@ typedef struct {
     const int32_t *items;   /* device int32 [n_items * 8]: work items               */
     int32_t n_items;
     int32_t max_parts;      /* largest nparts[b]                                     */
-    int32_t n_wide;         /* the last n_wide items hold one request each (from
+    int32_t n_wide;         /* the last n_wide items are all-heads items (from
                                rx_decode_plan_info.n_wide; 0 is always valid)   */
 } rx_decode_plan;
 
@@ -334,10 +334,15 @@ typedef struct {
     int64_t tokens_read;    /* KV token rows the plan reads per kv head: shared
                                segments once, everything else once per request */
     int64_t buf_words;      /* int32 words of the packed buffer                 */
-    int32_t n_wide;         /* items at the end of the list that hold a single
-                               request, read across all kv heads at once; set
-                               for one q head per kv head, or for 8 kv heads
-                               with 2, 4, 8 or 16 q heads each                */
+    int32_t n_wide;         /* all-heads items at the end of the list, read
+                               across all kv heads at once (whole slot rows).
+                               With one q head per kv head: the items that
+                               hold a single request.  With 8 kv heads and
+                               G = 2, 4, 8 or 16 q heads each: those, and the
+                               items of shared segments cut into groups of up
+                               to 16 / G requests (16 query rows per kv head)
+                               when a chunk makes at most 16 such groups.
+                               Otherwise 0.                                   */
 } rx_decode_plan_info;
 
 /* Builds a decode plan.  Inputs (host): req_to_token (row stride rtt_stride),
@@ -350,10 +355,12 @@ typedef struct {
  * Packed output (host int32, capacity out_cap words): order [batch], nparts
  * [batch], then items [n_items][8] = {first plan row, row count, pos_begin,
  * pos_end, part index, is_final, req_to_token row of the first request (its
- * req_idx), batch index of the first request}.  Items holding several
- * requests come first, then the info->n_wide items that hold one request;
- * each group is ordered longest first.  RX_ERR_CAPACITY (info->buf_words set)
- * if out_cap is too small. */
+ * req_idx), batch index of the first request}.  Per-head items come first,
+ * then the info->n_wide all-heads items; within each part, items holding
+ * several requests come before single-request ones, each ordered longest
+ * first.  RX_ERR_CAPACITY (info->buf_words set) if out_cap is too small.
+ * rx_attn_decode flags RX_DEV_BAD_LEN for an all-heads item with more
+ * requests than its kernel takes (and reads it as its first request). */
 int rx_decode_plan_build(const int32_t *req_to_token, int64_t rtt_stride, const int32_t *req_idx,
                          const int32_t *seq_len, int32_t batch, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t kv_chunk, int32_t min_shared,

@@ -744,7 +744,7 @@ constexpr int kWideMaxPos = 32;         // positions per stage at most (one prod
 // query-row slots, then the barriers: full [STAGES], empty [STAGES], q_empty
 // [NQ], desc [STAGES] (a stage's slot ids are written: the copy warps may
 // start).
-template <int STAGES_, int STAGE_BYTES_, int NQ_>
+template <int STAGES_, int STAGE_BYTES_, int NQ_, int QBYTES_>
 struct WideLayoutT {
     static constexpr int STAGES = STAGES_, STAGE_BYTES = STAGE_BYTES_, NQ = NQ_;
     static constexpr int OFF_K = 0;
@@ -752,8 +752,8 @@ struct WideLayoutT {
     static constexpr int OFF_OK = 2 * STAGES * STAGE_BYTES;               // int [stage][pos]: row valid
     static constexpr int OFF_SLOT = OFF_OK + STAGES * kWideMaxPos * 4;    // int [stage][pos]: slot id or -1
     static constexpr int OFF_HDR = OFF_SLOT + STAGES * kWideMaxPos * 4;   // int2 [stage]: item, first position
-    static constexpr int OFF_Q = (OFF_HDR + STAGES * 8 + 127) / 128 * 128;  // NQ x the item's query row
-    static constexpr int QBYTES = 16384;                                  // hq * D * 2 at most
+    static constexpr int OFF_Q = (OFF_HDR + STAGES * 8 + 127) / 128 * 128;  // NQ x the item's query rows
+    static constexpr int QBYTES = QBYTES_;                                // bytes of one q slot
     static constexpr int OFF_BAR = OFF_Q + NQ * QBYTES;
     static constexpr int OFF_ABORT = OFF_BAR + (3 * STAGES + NQ) * 8;
     static constexpr int B_DESC = 2 * STAGES + NQ;  // first desc barrier
@@ -766,7 +766,8 @@ struct WideLayoutT {
                   "bulk-copy destination alignment");
 };
 // one q head per kv head: slot rows packed (32 KB of K a stage), two q slots
-using WideLayout = WideLayoutT<kWideStages, kWideStageBytes, 2>;
+// of one request's query row (hq * D * 2 bytes, 16 KB at most)
+using WideLayout = WideLayoutT<kWideStages, kWideStageBytes, 2, 16384>;
 
 // bounded single-thread wait that ignores the abort flag: lets copies already
 // issued land before the CTA exits
@@ -813,12 +814,13 @@ __device__ __forceinline__ void load_bf16(const unsigned char *src, float (&out)
 }
 
 // Producer warp of an all-heads kernel (layout WL, NP positions a stage,
-// one lane per position).  Items come from a global counter, first come
+// one lane per position; GROUPS: items may hold up to 16 / G requests,
+// else one).  Items come from a global counter, first come
 // first served, so a CTA that starts late (behind the per-head kernel
 // running alongside) takes fewer of them.  Each stage's header names its
 // item; a last header with item -1 tells the consumers to stop.  A stage's
 // rows sit row_stride bytes apart (row bytes RB = hkv * head_dim * 2).
-template <class WL, int NP, int NH>
+template <class WL, int NP, int NH, bool GROUPS>
 __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sbase, volatile int *abort_flag,
                               int row_stride)
 {
@@ -835,7 +837,7 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
     // stage.  Claims stay only a few stages ahead of their first copy, so
     // the queue still hands the last items to the CTAs that free up first.
     struct Cursor {
-        int it, q0, p1, b;
+        int it, q0, p1, nr, qb;   // qb: batch index of the item's request `lane`
         const int32_t *slots;
     };
     auto fetch = [&]() -> int {
@@ -849,8 +851,16 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
             const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + it);
             c.q0 = __ldg(v + 2);
             c.p1 = __ldg(v + 3);
-            c.b = __ldg(v + 7);
             c.slots = p.rtt + (int64_t)__ldg(v + 6) * p.rtt_stride;
+            int nr = __ldg(v + 1);
+            // a malformed item (more requests than the kernel's rows, or
+            // none) is flagged and read as its first request alone
+            if (nr < 1 || (GROUPS ? nr * p.G > 16 : nr != 1)) {
+                if (lane == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_LEN);
+                nr = 1;
+            }
+            c.nr = nr;
+            c.qb = lane == 0 ? __ldg(v + 7) : (lane < nr ? __ldg(p.order + __ldg(v) + lane) : 0);
         }
     };
     auto advance = [&](Cursor &c) {
@@ -903,11 +913,13 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
         const int nok = __popc(__ballot_sync(0xffffffffu, ok));
         __syncwarp();  // flags and header are written before lane 0's arrive releases them
         if (lane == 0)
-            rx::mbar_arrive_expect_tx(bar + 8 * st, (uint32_t)(2 * nok * RB) + (with_q ? qbytes : 0u));
+            rx::mbar_arrive_expect_tx(bar + 8 * st,
+                                      (uint32_t)(2 * nok * RB) + (with_q ? (uint32_t)c0.nr * qbytes : 0u));
         __syncwarp();
-        if (with_q && lane == 0)
-            rx::bulk_g2s(sbase + WL::OFF_Q + qb * WL::QBYTES, p.q + (int64_t)c0.b * p.hq * p.head_dim, qbytes,
-                         bar + 8 * st);
+        // the query rows of the item's requests, one after another in the slot
+        if (with_q && lane < c0.nr)
+            rx::bulk_g2s(sbase + WL::OFF_Q + qb * WL::QBYTES + lane * qbytes,
+                         p.q + (int64_t)c0.qb * p.hq * p.head_dim, qbytes, bar + 8 * st);
         if (with_q) ++n_items;
         if constexpr (NH > 0) {
             // the copy warps issue this stage's row copies (issuing bulk
@@ -1004,7 +1016,7 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
     __syncthreads();
 
     if (warp == 0) {
-        wide_producer<WL, NP, kWideCopyWarps>(p, smem, sbase, abort_flag, RB);
+        wide_producer<WL, NP, kWideCopyWarps, false>(p, smem, sbase, abort_flag, RB);
     } else if (warp <= kWideCopyWarps) {
         wide_copier<WL, NP, kWideCopyWarps>(p, smem, sbase, abort_flag, RB, warp - 1);
     } else {
@@ -1168,7 +1180,9 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
 
 constexpr int kGqaNP = 16;                         // positions per stage
 constexpr int kGqaRowStride = 2048 + 16;           // slot row (8 kv heads x 128 x 2 at most) + pad
-using GqaLayout = WideLayoutT<3, kGqaNP * kGqaRowStride, 1>;
+// one q slot: the query rows of an item's requests (up to 16 / G of them,
+// 16 * 8 * D * 2 bytes at most)
+using GqaLayout = WideLayoutT<3, kGqaNP * kGqaRowStride, 1, 32768>;
 constexpr int kGqaWarps = 8;                       // one consumer warp per kv head
 constexpr int kGqaCopyWarps = 2;                   // copy warps: 32 row copies a stage
 
@@ -1199,14 +1213,15 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
     }
     __syncthreads();
     if (warp == 0) {
-        wide_producer<WL, kGqaNP, kGqaCopyWarps>(p, smem, sbase, abort_flag, kGqaRowStride);
+        wide_producer<WL, kGqaNP, kGqaCopyWarps, true>(p, smem, sbase, abort_flag, kGqaRowStride);
         return;
     }
     if (warp <= kGqaCopyWarps) {
         wide_copier<WL, kGqaNP, kGqaCopyWarps>(p, smem, sbase, abort_flag, kGqaRowStride, warp - 1);
         return;
     }
-    // consumer warp: kv head g, q heads g * G .. g * G + G - 1 as rows 0 .. G - 1
+    // consumer warp: kv head g.  Row m = i * G + j of its m16 tile is q head
+    // g * G + j of the item's request i (M = requests x G rows, 16 at most).
     const int g = warp - 1 - kGqaCopyWarps;
     const int G = p.G;
     const int gid = lane >> 2, tig = lane & 3;
@@ -1214,7 +1229,8 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
     const int *okf = reinterpret_cast<const int *>(smem + WL::OFF_OK);
     uint32_t qf[KS][4];
     float oacc[DT][4], m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
-    int cur = -1, p1 = 0, part_idx = 0, b = 0;
+    int cur = -1, p1 = 0, part_idx = 0, M = 0;
+    int ob[2] = {0, 0};  // batch index of this thread's output rows gid, gid + 8
     bool fin = false;
     auto write_out = [&]() {
         float l0 = l_r[0], l1 = l_r[1];
@@ -1226,8 +1242,8 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int r = gid + half * 8;
-            if (r >= G) continue;
-            const int64_t orow = (int64_t)b * p.hq + (int64_t)g * G + r;
+            if (r >= M) continue;
+            const int64_t orow = (int64_t)ob[half] * p.hq + (int64_t)g * G + r % G;
             const float inv = 1.f / ls[half];
             if (fin) {
                 bf16 *dst = p.o + orow * D;
@@ -1258,22 +1274,33 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
             if (h.x < 0) break;
             cur = h.x;
             const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + cur);
+            const int r0 = __ldg(v + 0);
+            int nr = __ldg(v + 1);
+            if (nr < 1 || nr * G > 16) nr = 1;  // flagged by the producer, which copied one row
+            M = nr * G;
             p1 = __ldg(v + 3);
             part_idx = __ldg(v + 4);
             fin = __ldg(v + 5) != 0;
-            b = __ldg(v + 7);
+            const int b0 = __ldg(v + 7);
+            // batch indices of the two output rows: loaded now, used when
+            // the item's last stage is done
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int i = (gid + half * 8) / G;
+                ob[half] = (i == 0 || i >= nr) ? b0 : __ldg(p.order + r0 + i);
+            }
             // the query rows came with this stage: A fragments of rows
-            // 0 .. G - 1 (rows past G read row 0 and are zeroed), then hand
+            // 0 .. M - 1 (rows past M read row 0 and are zeroed), then hand
             // the q slot back
-            const unsigned char *qs = smem + WL::OFF_Q + (size_t)g * G * D * 2;
-            const int qrow = (lane & 15) < G ? (lane & 15) : 0;
+            const int qm = (lane & 15) < M ? (lane & 15) : 0;
+            const unsigned char *qs =
+                smem + WL::OFF_Q + (size_t)(qm / G) * p.hq * D * 2 + (size_t)(g * G + qm % G) * D * 2;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 const int ch = ks * 2 + (lane >> 4);
-                rx::ldmatrix_x4(rx::smem_u32(qs + qrow * D * 2 + ch * 16), qf[ks][0], qf[ks][1], qf[ks][2],
-                                qf[ks][3]);
-                if (gid >= G) qf[ks][0] = qf[ks][2] = 0u;
-                if (gid + 8 >= G) qf[ks][1] = qf[ks][3] = 0u;
+                rx::ldmatrix_x4(rx::smem_u32(qs + ch * 16), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+                if (gid >= M) qf[ks][0] = qf[ks][2] = 0u;
+                if (gid + 8 >= M) qf[ks][1] = qf[ks][3] = 0u;
             }
             __syncwarp();
             if (lane == 0) rx::mbar_arrive(bar + 8 * (2 * WL::STAGES));
@@ -1373,12 +1400,13 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
     }
 }
 
-// Single-request items with G > 1 go to decode_gqa_kernel for 8 kv heads and
-// G = 2, 4, 8 or 16 (the q rows of a kv head fit one m16 tile) when a query
-// row fits the q slot.
+// All-heads items with G > 1 (one request, or a group of up to 16 / G
+// requests) go to decode_gqa_kernel for 8 kv heads and G = 2, 4, 8 or 16: a
+// kv head's 16 query rows fit one m16 tile, and a group's query rows the q
+// slot.
 bool gqa_supported(int hq, int hkv, int D)
 {
-    return rx_gqa_heads(hq, hkv) && (D == 64 || D == 128) && hq * D * 2 <= GqaLayout::QBYTES;
+    return rx_gqa_heads(hq, hkv) && (D == 64 || D == 128) && 16 * hkv * D * 2 <= GqaLayout::QBYTES;
 }
 
 // Launches `kernel` on `st`.  With `dependent`, it is launched as a

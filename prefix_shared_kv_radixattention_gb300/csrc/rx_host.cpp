@@ -750,25 +750,34 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
         nparts[(size_t)order[(size_t)r]] = (int32_t)np;
         max_parts = std::max(max_parts, np);
     }
-    // work items
+    // work items; `all` marks the ones for an all-heads kernel
     struct Item {
         int32_t v[8];
+        bool all;
     };
     std::vector<Item> items;
-    const int64_t R = 64 / G;  // requests per item (64 query rows)
+    const int64_t R = 64 / G;  // requests per per-head item (64 query rows)
+    // groups of up to 16 / G requests (16 query rows per kv head) for the
+    // several-q-heads all-heads kernel
+    const bool groups = G > 1 && rx_gqa_heads(hq, hkv);
+    const int64_t RG = 16 / G;
     for (int64_t k = 0; k < n_iv; ++k) {
         if (!is_seg[(size_t)k]) continue;
         const Interval &x = iv[(size_t)k];
+        const int64_t nreq = x.rb - x.lb + 1;
+        const bool grouped = groups && (nreq + RG - 1) / RG <= RX_DECODE_MAX_GROUPS;
+        const int64_t step = grouped ? RG : R;
         int64_t s0 = seg_start[(size_t)k], s1 = x.lcp;
         for (int64_t c = 0; c * kv_chunk < s1 - s0; ++c) {
             int64_t p0 = s0 + c * kv_chunk, p1 = std::min(s1, p0 + kv_chunk);
-            for (int64_t r0 = x.lb; r0 <= x.rb; r0 += R) {
-                int64_t nr = std::min(R, x.rb - r0 + 1);
+            for (int64_t r0 = x.lb; r0 <= x.rb; r0 += step) {
+                int64_t nr = std::min(step, x.rb - r0 + 1);
                 bool fin = true;
                 for (int64_t r = r0; r < r0 + nr; ++r) fin = fin && nparts[(size_t)order[(size_t)r]] == 1;
                 const int32_t b0 = order[(size_t)r0];
                 items.push_back({{(int32_t)r0, (int32_t)nr, (int32_t)p0, (int32_t)p1,
-                                  (int32_t)(part_base[(size_t)k] + c), fin ? 1 : 0, req_idx[b0], b0}});
+                                  (int32_t)(part_base[(size_t)k] + c), fin ? 1 : 0, req_idx[b0], b0},
+                                 grouped});
             }
         }
     }
@@ -780,22 +789,24 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
             bool fin = nparts[(size_t)order[(size_t)r]] == 1;
             const int32_t b0 = order[(size_t)r];
             items.push_back({{(int32_t)r, 1, (int32_t)p0, (int32_t)p1,
-                              (int32_t)(priv_base[(size_t)r] + c), fin ? 1 : 0, req_idx[b0], b0}});
+                              (int32_t)(priv_base[(size_t)r] + c), fin ? 1 : 0, req_idx[b0], b0},
+                             wide});
         }
     }
-    // items of several requests first, then single-request items (read
-    // across all kv heads at once); each group longest first, so that the
-    // tail of a grid holds the short items
+    // per-head items first, then the all-heads items (read across all kv
+    // heads at once); within each, items of several requests before
+    // single-request ones, and each of those longest first, so that the tail
+    // of a grid holds the short items
     std::stable_sort(items.begin(), items.end(), [](const Item &a, const Item &b) {
-        const bool wa = a.v[1] == 1, wb = b.v[1] == 1;
-        if (wa != wb) return wb;
+        if (a.all != b.all) return b.all;
+        const bool sa = a.v[1] == 1, sb = b.v[1] == 1;
+        if (sa != sb) return sb;
         int64_t la = (int64_t)a.v[3] - a.v[2], lb = (int64_t)b.v[3] - b.v[2];
         if (la != lb) return la > lb;
         return a.v[1] > b.v[1];
     });
     int64_t n_wide = 0;
-    if (wide)
-        for (const Item &x : items) n_wide += x.v[1] == 1;
+    for (const Item &x : items) n_wide += x.all;
     if ((int64_t)items.size() > INT32_MAX / 8)
         return rx_set_error(RX_ERR_UNSUPPORTED, "rx_decode_plan_build: too many items");
     info->kv_chunk = kv_chunk;

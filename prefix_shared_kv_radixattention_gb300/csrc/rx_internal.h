@@ -20,6 +20,16 @@
 #define RX_DECODE_TARGET_WIDE_ITEMS 304
 #define RX_DECODE_MIN_WIDE_CHUNK 16
 #define RX_DECODE_TARGET_SHARED_ITEMS 152
+// With 8 kv heads and G q heads each (G >= 2), the all-heads kernel also
+// takes items of up to 16 / G requests that share their positions (16 query
+// rows per kv head).  A shared chunk whose requests make at most this many
+// such groups goes to it, one item per group (read as whole slot rows; the
+// groups of one chunk are claimed together, so all but the first mostly hit
+// L2); a chunk shared more widely stays with the per-head kernel.  Measured
+// on tree-of-thought decode (1, 4 and 16 groups per segment): limits of 4,
+// 8 and 16 give 0.093, 0.093 and 0.088 ms; on the long-chat decode (8
+// groups) 8 beats 4 by 1.5 %.
+#define RX_DECODE_MAX_GROUPS 16
 
 // Head counts whose single-request decode items have an all-heads kernel
 // with several q heads per kv head: 8 kv heads, G = 2, 4, 8 or 16.

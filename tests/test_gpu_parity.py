@@ -272,6 +272,37 @@ def test_decode_bad_slot_in_wide_item_is_flagged(hq, hkv):
     g.compare(o, ro, "bad slot as a zero row")
 
 
+@pytest.mark.parametrize("hq", [16, 32, 64])
+def test_decode_bad_slot_in_group_item_is_flagged(hq):
+    """A bad slot id inside a shared segment read by a group item (several
+    requests on the all-heads kernel with G = 2, 4, 8) is flagged and read as
+    a zero row for every request of the group.  The id is planted in every
+    request's list, so the segment stays shared."""
+    g = _gpu()
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.few_shot_decode(hq=hq, hkv=8, d=128, batch=5, shared=60, private=30, num_slots=1024)
+    prob.req_to_token = prob.req_to_token.copy()
+    good_slot = int(prob.req_to_token[0, 33])
+    prob.req_to_token[:, 33] = prob.num_slots + 7
+    buf, info = rx.rx_decode_plan_build(prob.req_to_token, prob.dec_req_idx, prob.dec_seq_len, prob.hq,
+                                        prob.hkv, 64, 16)
+    items = buf[2 * len(prob.dec_req_idx):].reshape(-1, 8)
+    tail = items[len(items) - info.n_wide:]
+    assert np.any(tail[:, 1] > 1) and len(items) == info.n_wide   # groups only, no per-head item
+    dev = g.Dev(prob)
+    dev.kv_store()
+    o, _ = dev.decode(plan=True, kv_chunk=64)
+    assert dev.status_word() & rx.RX_DEV_BAD_SLOT
+    assert np.isfinite(o).all()
+    kp, vp, rtt = dev.oracle_pools()
+    kp, vp, rtt = kp.copy(), vp.copy(), rtt.copy()
+    rtt[:, 33] = good_slot
+    kp[good_slot] = 0
+    vp[good_slot] = 0
+    ro, _ = oracle.decode(prob.q_dec, kp, vp, rtt, prob.dec_req_idx, prob.dec_seq_len, prob.sm_scale)
+    g.compare(o, ro, "bad slot in a group item as a zero row")
+
+
 @pytest.mark.parametrize("hq", [8, 32])
 def test_decode_wide_ctas_that_find_the_queue_empty(hq):
     """All-heads CTAs that start after the other CTAs have taken every

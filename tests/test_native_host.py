@@ -307,16 +307,25 @@ def check_plan(prob, order, nparts, items, info, auto=False):
         assert np.all(cover[b] == 1), f"request {b} context not covered exactly once"
         assert sorted(parts[b]) == list(range(int(nparts[b])))
     assert info.max_parts == int(nparts.max())
-    # items of several requests first, then the single-request items, each
-    # group longest first; for the head counts with an all-heads kernel the
-    # single-request items are the n_wide "wide" ones, otherwise there are none
-    single = items[:, 1] == 1
-    n_single = int(single.sum())
-    assert np.all(single[len(items) - n_single:]) and not np.any(single[:len(items) - n_single])
-    assert int(info.n_wide) == (n_single if _plan_wide(prob) else 0)
-    for grp in (items[~single], items[single]):
-        lens = grp[:, 3] - grp[:, 2]
-        assert np.all(lens[:-1] >= lens[1:])
+    # per-head items first, then the n_wide all-heads ones: for the head
+    # counts with an all-heads kernel every single-request item, and with
+    # G > 1 also groups of up to 16 / G requests (16 query rows per kv head);
+    # otherwise none.  Within each part, items of several requests come
+    # before single-request ones, each of those longest first.
+    n_wide = int(info.n_wide)
+    head, tail = items[:len(items) - n_wide], items[len(items) - n_wide:]
+    if not _plan_wide(prob):
+        assert n_wide == 0
+    else:
+        assert not np.any(head[:, 1] == 1)
+        assert np.all(tail[:, 1] * G <= 16) if G > 1 else np.all(tail[:, 1] == 1)
+    for part in (head, tail):
+        single = part[:, 1] == 1
+        k = int(single.sum())
+        assert np.all(single[len(part) - k:]) and not np.any(single[:len(part) - k])
+        for grp in (part[~single], part[single]):
+            lens = grp[:, 3] - grp[:, 2]
+            assert np.all(lens[:-1] >= lens[1:])
 
 
 @pytest.mark.parametrize("seed", range(15))
@@ -343,6 +352,13 @@ def test_plan_structure_tree_of_thought():
     assert info.n_segments == 4 + 16 + 64
     assert info.shared_tokens == 84 * 256
     assert info.tokens_read == prob.decode_unique_tokens() == 340 * 256 + 256
+    # G = 4: groups of 4 requests.  Every segment goes to the all-heads
+    # kernel: the 64 level-3 ones (4 requests: one group), the 16 level-2 ones
+    # (16 requests: four groups) and the 4 level-1 ones (64 requests: sixteen
+    # groups, the most one chunk is cut into); no per-head items remain.
+    groups = items[items[:, 1] > 1]
+    assert len(groups) == 64 + 16 * 4 + 4 * 16 and np.all(groups[:, 1] == 4)
+    assert int(info.n_wide) == len(items)
 
 
 def test_plan_structure_mixed_chat():
