@@ -645,6 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p)
     }
 }
 
+constexpr int kMergeFew = 12;  // parts up to which a row's partials are loaded in one go
+
 template <int D>
 __global__ void __launch_bounds__(128) merge_kernel(const Params p, int use_plan)
 {
@@ -660,36 +662,71 @@ __global__ void __launch_bounds__(128) merge_kernel(const Params p, int use_plan
     rx::pdl_wait();
     if (!live || np <= 1 || np > p.max_parts) return;  // > max_parts: flagged by the decode kernel
     const float *lp = p.ws_lse + row * p.max_parts;
-    float m = -INFINITY;
-    for (int i = lane; i < np; i += 32) m = fmaxf(m, lp[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     constexpr int PER = D / 32;
     float acc[PER];
 #pragma unroll
     for (int j = 0; j < PER; ++j) acc[j] = 0.f;
-    // part weights computed lane-parallel (lane k: part base + k), then the
-    // parts' rows read eight at a time so their loads are in flight together
-    float wsum = 0.f;
-    for (int base = 0; base < np; base += 32) {
-        const int cnt = min(32, np - base);
-        const float wl = lane < cnt ? rx::fast_exp2(lp[base + lane] - m) : 0.f;
-        wsum += wl;
-        const float *src0 = p.ws_o + (row * p.max_parts + base) * D + lane * PER;
-#pragma unroll 8
-        for (int k = 0; k < cnt; ++k) {
+    float m = -INFINITY, wsum = 0.f;
+    if (np <= kMergeFew) {
+        // few parts: their rows and log2-sum-exps are loaded together (one
+        // round trip to L2), then weighted
+        const float *src0 = p.ws_o + row * p.max_parts * D + lane * PER;
+        float v[kMergeFew][PER];
+#pragma unroll
+        for (int k = 0; k < kMergeFew; ++k) {
+            if (k < np) {
+                if constexpr (PER == 4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(src0 + (int64_t)k * D);
+                    v[k][0] = t.x;
+                    v[k][1] = t.y;
+                    v[k][2] = t.z;
+                    v[k][3] = t.w;
+                } else {
+                    const float2 t = *reinterpret_cast<const float2 *>(src0 + (int64_t)k * D);
+                    v[k][0] = t.x;
+                    v[k][1] = t.y;
+                }
+            }
+        }
+        const float ll = lane < np ? lp[lane] : -INFINITY;
+        m = ll;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float wl = lane < np ? rx::fast_exp2(ll - m) : 0.f;
+        wsum = wl;
+#pragma unroll
+        for (int k = 0; k < kMergeFew; ++k) {
             const float wgt = __shfl_sync(0xffffffffu, wl, k);
-            const float *src = src0 + (int64_t)k * D;
-            if constexpr (PER == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(src);
-                acc[0] = fmaf(wgt, v.x, acc[0]);
-                acc[1] = fmaf(wgt, v.y, acc[1]);
-                acc[2] = fmaf(wgt, v.z, acc[2]);
-                acc[3] = fmaf(wgt, v.w, acc[3]);
-            } else {
-                const float2 v = *reinterpret_cast<const float2 *>(src);
-                acc[0] = fmaf(wgt, v.x, acc[0]);
-                acc[1] = fmaf(wgt, v.y, acc[1]);
+            if (k < np)
+#pragma unroll
+                for (int j = 0; j < PER; ++j) acc[j] = fmaf(wgt, v[k][j], acc[j]);
+        }
+    } else {
+        for (int i = lane; i < np; i += 32) m = fmaxf(m, lp[i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        // part weights computed lane-parallel (lane k: part base + k), then the
+        // parts' rows read eight at a time so their loads are in flight together
+        for (int base = 0; base < np; base += 32) {
+            const int cnt = min(32, np - base);
+            const float wl = lane < cnt ? rx::fast_exp2(lp[base + lane] - m) : 0.f;
+            wsum += wl;
+            const float *src0 = p.ws_o + (row * p.max_parts + base) * D + lane * PER;
+#pragma unroll 8
+            for (int k = 0; k < cnt; ++k) {
+                const float wgt = __shfl_sync(0xffffffffu, wl, k);
+                const float *src = src0 + (int64_t)k * D;
+                if constexpr (PER == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src);
+                    acc[0] = fmaf(wgt, v.x, acc[0]);
+                    acc[1] = fmaf(wgt, v.y, acc[1]);
+                    acc[2] = fmaf(wgt, v.z, acc[2]);
+                    acc[3] = fmaf(wgt, v.w, acc[3]);
+                } else {
+                    const float2 v = *reinterpret_cast<const float2 *>(src);
+                    acc[0] = fmaf(wgt, v.x, acc[0]);
+                    acc[1] = fmaf(wgt, v.y, acc[1]);
+                }
             }
         }
     }

@@ -707,9 +707,12 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
     const bool wide = G == 1 || rx_gqa_heads(hq, hkv);
     if (auto_chunk) {
         // about RX_DECODE_TARGET_ITEMS work items over all kv heads; with wide
-        // items, about RX_DECODE_TARGET_SHARED_ITEMS over the shared reads only
+        // items, about RX_DECODE_TARGET_SHARED_ITEMS per-head items over the
+        // shared reads only, or RX_DECODE_TARGET_GROUP_CHUNKS (kv head, chunk)
+        // pairs when the shared chunks go to the all-heads kernel in groups
         const int64_t n = wide ? shared * hkv : reads * hkv;
-        const int64_t target = wide ? RX_DECODE_TARGET_SHARED_ITEMS : RX_DECODE_TARGET_ITEMS;
+        const int64_t target = !wide ? RX_DECODE_TARGET_ITEMS
+                               : G > 1 ? RX_DECODE_TARGET_GROUP_CHUNKS : RX_DECODE_TARGET_SHARED_ITEMS;
         int64_t c = (n + target - 1) / target;
         c = std::min<int64_t>(RX_MAX_KV_CHUNK, std::max<int64_t>(64, (c + 63) / 64 * 64));
         kv_chunk = (int32_t)c;

@@ -14,12 +14,17 @@
 #define RX_DECODE_TARGET_ITEMS 1216
 // automatic plans with single-request ("wide") items: pieces of the private
 // positions over the whole batch (two per SM of a 152-SM GPU, handed out
-// first come first served) and their shortest length, and (kv head, shared
-// chunk) items for the per-head kernel (one wave).  Measured on few-shot
-// decode: 304 / 152 beats 608 / 304 by 7 %.
+// first come first served) and their shortest length; (kv head, shared
+// chunk) items for the per-head kernel, which runs beside the all-heads
+// kernel (half an SM wave: each item pays a fixed start-up, so fewer,
+// longer ones take less SM time); and, when shared chunks go to the
+// all-heads kernel in request groups, the chunk size that gives about one
+// wave of (kv head, chunk) pairs.  Measured on few-shot decode: 304 / 152
+// beats 608 / 304 by 7 %, and 76 per-head items beat 152 by 6 %.
 #define RX_DECODE_TARGET_WIDE_ITEMS 304
 #define RX_DECODE_MIN_WIDE_CHUNK 16
-#define RX_DECODE_TARGET_SHARED_ITEMS 152
+#define RX_DECODE_TARGET_SHARED_ITEMS 76
+#define RX_DECODE_TARGET_GROUP_CHUNKS 152
 // With 8 kv heads and G q heads each (G >= 2), the all-heads kernel also
 // takes items of up to 16 / G requests that share their positions (16 query
 // rows per kv head).  A shared chunk whose requests make at most this many
