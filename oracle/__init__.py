@@ -19,9 +19,13 @@ Contents
   * ``tree_ref.schedule`` / ``tree_ref.optimal_hit_rate`` -- cache-aware
                                request order and the optimal cache hit rate
   * ``keys.image_keys``       -- radix-tree keys of an image's tokens
+  * ``fsm.compress`` / ``fsm.step`` -- the compressed finite-state machine of
+                               constrained decoding: jumps over fixed tokens,
+                               and a masked-argmax decoding step with them
 
-Every function here is pinned in ``tests/test_oracle_pins.py`` and
-``tests/test_tree_oracle.py``; none is "parity unpinned".
+Every function here is pinned in ``tests/test_oracle_pins.py``,
+``tests/test_tree_oracle.py``, ``tests/test_image_keys.py`` and
+``tests/test_fsm_oracle.py``; none is "parity unpinned".
 """
 from __future__ import annotations
 
