@@ -73,6 +73,10 @@ extern "C" {
                                    the req_to_token stride; rows left unwritten */
 #define RX_DEV_TIMEOUT 4        /* a pipeline wait gave up (never expected; the
                                    kernel stopped early, outputs incomplete)   */
+#define RX_DEV_FSM_DONE 8       /* rx_fsm_step: a request's state allows no
+                                   token (its constrained text is complete)    */
+#define RX_DEV_BAD_STATE 16     /* rx_fsm_step: a state id outside the machine,
+                                   or a mask bit with no matching edge          */
 
 /* Message for the last failed call on this thread ("" if none). */
 const char *rx_last_error(void);
@@ -418,6 +422,77 @@ int rx_attn_decode_static(const rx_kv_pool *pool, const void *q, void *o, float 
                           const int32_t *req_to_token, int64_t rtt_stride, int32_t batch,
                           int32_t max_seq_len, const rx_decode_plan *plan_or_null, float sm_scale,
                           int32_t *dev_status, void *stream);
+
+/* ---- compressed finite-state machine (constrained decoding) -------------
+ * Source: "SGLang: Efficient Execution of Structured Language Model
+ * Programs" (unite.ai, es), "Introducción a SGLang", compressed-FSM bullet.
+ * Systems that follow an output constraint look only at the next token, so
+ * they decode one token per step; the runtime instead builds a compressed
+ * finite-state machine of the constraint and decodes a path of several
+ * tokens in one step wherever the constraint fixes them.
+ *
+ * The constraint is a deterministic automaton over token ids (how it is
+ * derived from a regular expression and a tokenizer is outside this
+ * library): states 0 .. n_states-1, and for state s the edges
+ * e in [row_ptr[s], row_ptr[s+1]) with token tok[e] (strictly increasing
+ * within a state, < vocab) leading to state nxt[e].  A state without edges
+ * is terminal.  A state with exactly one edge fixes the next token.
+ *
+ * rx_fsm_compress (host): the jump of every state s -- the tokens fixed along
+ * the path of single-edge states from s, and the state where it stops (the
+ * first state with zero or several edges, a state the path already passed,
+ * or after max_jump tokens) -- packed as jump_len [S], jump_off [S] (int64,
+ * state order), jump_end [S] and jump_tok [sum of jump_len]; and the
+ * allowed-token mask: bit t % 32 of word t / 32 of row s is set when state s
+ * has an edge with token t, uint32 [S][ceil(vocab / 32)].  Any output may be
+ * NULL; info (required) gets the sizes, so a first call with NULL outputs
+ * sizes jump_tok.  RX_ERR_INVALID (nothing written) for arrays that break
+ * the rules above; RX_ERR_CAPACITY when out_jump_tok is given and
+ * jump_tok_cap < info->jump_tokens. */
+typedef struct {
+    int64_t n_edges;
+    int64_t jump_tokens;   /* tokens over all jumps                        */
+    int32_t n_singular;    /* states with exactly one edge                 */
+    int32_t n_looped;      /* states whose jump stopped on a repeated state */
+    int32_t longest_jump;
+} rx_fsm_info;
+
+int rx_fsm_compress(int32_t n_states, int32_t vocab, const int64_t *row_ptr, const int32_t *tok,
+                    const int32_t *nxt, int32_t max_jump, uint32_t *out_mask, int32_t *out_jump_len,
+                    int64_t *out_jump_off, int32_t *out_jump_end, int32_t *out_jump_tok,
+                    int64_t jump_tok_cap, rx_fsm_info *info);
+
+/* The compressed machine on the device: copies of the automaton's arrays and
+ * of rx_fsm_compress's outputs (for the same max_jump), owned by the caller. */
+typedef struct {
+    const int64_t *row_ptr;
+    const int32_t *tok;
+    const int32_t *nxt;
+    const uint32_t *mask;
+    const int32_t *jump_len;
+    const int64_t *jump_off;
+    const int32_t *jump_end;
+    const int32_t *jump_tok;
+    int32_t n_states, vocab, max_jump;
+} rx_fsm;
+
+/* One constrained decoding step for `batch` requests (device, asynchronous
+ * on `stream`).  For request b in state s = state[b]:
+ *   t  = argmax over the tokens s allows of logits[b][t] (NaN counts as
+ *        -inf; equal values go to the smallest id),
+ *   s1 = the state edge (s, t) leads to,
+ * then out_tokens[b][0] = t, out_tokens[b][1 .. 1+L) = the jump of s1
+ * (L = jump_len[s1] <= max_jump), out_count[b] = 1 + L and
+ * state[b] = jump_end[s1].  A terminal state sets RX_DEV_FSM_DONE, a state
+ * id out of range (or a mask bit without its edge) RX_DEV_BAD_STATE; such a
+ * request gets out_count[b] = 0 and keeps its state.
+ *   logits: device fp32 rows of logits_stride floats (>= vocab, a multiple
+ *   of 4, rows 16-byte aligned); state: device int32 [batch], updated in
+ *   place; out_tokens: device int32 [batch][1 + max_jump]; out_count: device
+ *   int32 [batch].  Rows are read once, as 16-byte vectors. */
+int rx_fsm_step(const rx_fsm *fsm, const float *logits, int64_t logits_stride, int32_t batch,
+                int32_t *state, int32_t *out_tokens, int32_t *out_count, int32_t *dev_status,
+                void *stream);
 
 #ifdef __cplusplus
 }

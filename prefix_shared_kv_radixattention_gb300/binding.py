@@ -37,6 +37,9 @@ RX_SCHED_FCFS = 0
 RX_SCHED_LPM = 1
 RX_DEV_BAD_SLOT = 1
 RX_DEV_BAD_LEN = 2
+RX_DEV_TIMEOUT = 4
+RX_DEV_FSM_DONE = 8
+RX_DEV_BAD_STATE = 16
 
 
 class RxError(RuntimeError):
@@ -94,6 +97,22 @@ _sig("rx_admit", ctypes.c_int, _P, _P, _P, _I64, _P, _PI64, _PI64)
 _sig("rx_commit", ctypes.c_int, _P, _P, _P, _P, _I64, _I64)
 _sig("rx_prefix_len", ctypes.c_int, _P, _P, _I64, _PI64)
 _sig("rx_image_keys", ctypes.c_int, _P, _I64, _I64, _P)
+
+
+class FsmInfo(ctypes.Structure):
+    _fields_ = [("n_edges", ctypes.c_int64), ("jump_tokens", ctypes.c_int64), ("n_singular", ctypes.c_int32),
+                ("n_looped", ctypes.c_int32), ("longest_jump", ctypes.c_int32)]
+
+
+class FsmStruct(ctypes.Structure):
+    _fields_ = [("row_ptr", _P), ("tok", _P), ("nxt", _P), ("mask", _P), ("jump_len", _P), ("jump_off", _P),
+                ("jump_end", _P), ("jump_tok", _P), ("n_states", ctypes.c_int32), ("vocab", ctypes.c_int32),
+                ("max_jump", ctypes.c_int32)]
+
+
+_sig("rx_fsm_compress", ctypes.c_int, _I32, _I32, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _I64,
+     ctypes.POINTER(FsmInfo))
+_sig("rx_fsm_step", ctypes.c_int, ctypes.POINTER(FsmStruct), _P, _I64, _I32, _P, _P, _P, _P, _P)
 _sig("rx_schedule", ctypes.c_int, _P, _P, _P, _I32, _I32, _P, _P)
 _sig("rx_kv_store", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I64, _P, _P)
 _sig("rx_rope", ctypes.c_int, _P, _P, _I64, _I32, _I32, ctypes.c_double, _P)
@@ -495,3 +514,77 @@ def rx_attn_decode_static(k_pool, v_pool, q, o, lse, req_idx, seq_len, req_to_to
                                       _ptr(req_idx), _ptr(seq_len), _ptr(req_to_token),
                                       req_to_token.shape[1], req_idx.numel(), int(max_seq_len), pp,
                                       float(sm_scale), _ptr(dev_status), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# compressed finite-state machine (constrained decoding)
+# ---------------------------------------------------------------------------
+
+
+def rx_fsm_compress(n_states: int, vocab: int, row_ptr, tok, nxt, max_jump: int):
+    """Host compression of a token automaton (CSR).  Returns (mask uint32
+    [S, ceil(V/32)], jump_len int32 [S], jump_off int64 [S], jump_end int32
+    [S], jump_tok int32 [total], info)."""
+    rp, rpp = _np(row_ptr, np.int64)
+    t, tp = _np(tok, np.int32)
+    n, np_ = _np(nxt, np.int32)
+    info = FsmInfo()
+    _check(_lib.rx_fsm_compress(int(n_states), int(vocab), rpp, tp if len(t) else None, np_ if len(n) else None,
+                                int(max_jump), None, None, None, None, None, 0, ctypes.byref(info)))
+    W = (int(vocab) + 31) // 32
+    mask = np.empty((int(n_states), W), np.uint32)
+    jl = np.empty(int(n_states), np.int32)
+    jo = np.empty(int(n_states), np.int64)
+    je = np.empty(int(n_states), np.int32)
+    jt = np.empty(max(1, int(info.jump_tokens)), np.int32)
+    _check(_lib.rx_fsm_compress(int(n_states), int(vocab), rpp, tp if len(t) else None, np_ if len(n) else None,
+                                int(max_jump), mask.ctypes.data_as(_P), jl.ctypes.data_as(_P),
+                                jo.ctypes.data_as(_P), je.ctypes.data_as(_P), jt.ctypes.data_as(_P), len(jt),
+                                ctypes.byref(info)))
+    return mask, jl, jo, je, jt[:int(info.jump_tokens)], info
+
+
+class Fsm:
+    """A compressed machine resident on the current CUDA device: the
+    automaton and its compression (rx_fsm_compress), as torch tensors."""
+
+    def __init__(self, n_states: int, vocab: int, row_ptr, tok, nxt, max_jump: int):
+        torch = _torch()
+        mask, jl, jo, je, jt, info = rx_fsm_compress(n_states, vocab, row_ptr, tok, nxt, max_jump)
+        self.info = info
+        self.n_states, self.vocab, self.max_jump = int(n_states), int(vocab), int(max_jump)
+
+        def dev(a, dt):
+            a = np.ascontiguousarray(a, dtype=dt)
+            if a.size == 0:
+                a = np.zeros(1, dt)
+            return torch.from_numpy(a).cuda()
+
+        self.row_ptr = dev(row_ptr, np.int64)
+        self.tok = dev(tok, np.int32)
+        self.nxt = dev(nxt, np.int32)
+        self.mask = torch.from_numpy(mask.view(np.int32)).cuda()
+        self.jump_len, self.jump_off = dev(jl, np.int32), dev(jo, np.int64)
+        self.jump_end, self.jump_tok = dev(je, np.int32), dev(jt, np.int32)
+        self.struct = FsmStruct(self.row_ptr.data_ptr(), self.tok.data_ptr(), self.nxt.data_ptr(),
+                                self.mask.data_ptr(), self.jump_len.data_ptr(), self.jump_off.data_ptr(),
+                                self.jump_end.data_ptr(), self.jump_tok.data_ptr(), self.n_states, self.vocab,
+                                self.max_jump)
+
+
+def rx_fsm_step(fsm: Fsm, logits, state, out_tokens, out_count, dev_status=None, stream=None) -> None:
+    """One constrained decoding step: logits fp32 [B, >= V] (rows 16-byte
+    aligned), state int32 [B] (updated), out_tokens int32 [B, 1 + max_jump],
+    out_count int32 [B]."""
+    torch = _torch()
+    _dev(logits, torch.float32, "logits")
+    _dev(state, torch.int32, "state")
+    _dev(out_tokens, torch.int32, "out_tokens")
+    _dev(out_count, torch.int32, "out_count")
+    _dev(dev_status, torch.int32, "dev_status")
+    B = state.numel()
+    if logits.dim() != 2 or logits.shape[0] != B or out_tokens.shape != (B, 1 + fsm.max_jump) or \
+            out_count.numel() != B:
+        raise ValueError("rx_fsm_step: logits [B, V], out_tokens [B, 1 + max_jump], out_count [B]")
+    _check(_lib.rx_fsm_step(ctypes.byref(fsm.struct), _ptr(logits), logits.shape[1], B, _ptr(state),
+                            _ptr(out_tokens), _ptr(out_count), _ptr(dev_status), _stream(stream)))

@@ -45,16 +45,6 @@ int rx_set_error(int code, const char *fmt, ...)
 extern "C" const char *rx_last_error(void) { return g_last_error.c_str(); }
 extern "C" int rx_version(void) { return RX_ABI_VERSION; }
 
-#define RX_TRY try {
-#define RX_CATCH                                                            \
-    }                                                                       \
-    catch (const std::bad_alloc &) {                                        \
-        return rx_set_error(RX_ERR_NOMEM, "%s: host allocation failed", __func__); \
-    }                                                                       \
-    catch (...) {                                                           \
-        return rx_set_error(RX_ERR_INVALID, "%s: unexpected exception", __func__); \
-    }
-
 // ---------------------------------------------------------------------------
 // radix tree
 // ---------------------------------------------------------------------------

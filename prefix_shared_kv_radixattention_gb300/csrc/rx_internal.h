@@ -48,6 +48,21 @@ static inline bool rx_gqa_heads(int32_t hq, int32_t hkv)
 // Sets the thread-local message returned by rx_last_error and returns code.
 int rx_set_error(int code, const char *fmt, ...);
 
+// Host entry points that allocate wrap their body in RX_TRY ... RX_CATCH so
+// that no exception crosses the C ABI.
+#ifdef __cplusplus
+#include <new>
+#define RX_TRY try {
+#define RX_CATCH                                                                   \
+    }                                                                              \
+    catch (const std::bad_alloc &) {                                               \
+        return rx_set_error(RX_ERR_NOMEM, "%s: host allocation failed", __func__); \
+    }                                                                              \
+    catch (...) {                                                                  \
+        return rx_set_error(RX_ERR_INVALID, "%s: unexpected exception", __func__); \
+    }
+#endif
+
 // Positions per decode work item when no plan is given, and the resulting
 // number of partial results per request.  Chosen from the batch shape only,
 // so rx_attn_decode_workspace and rx_attn_decode agree.
