@@ -18,6 +18,9 @@ is quoted on):
   cached_prefix_extend    32 x (2048 cached + 512 new), GQA 32/8
   mixed_chat              16 decode x 32k + 16 extend x (4096 + 1024), 64/8
   tiny_extend             4 x (64 cached + 16 new), 4 heads, head_dim 64
+  constrained_decode      one compressed-FSM decoding step (masked argmax and
+                          jump) for 256 requests over a 128,256-id vocabulary
+                          under a JSON-object constraint
 
 One JSON line is printed by rank 0.  Under torchrun every rank runs the same
 workload on its own GPU (independent replicas, no collective on the data
@@ -588,6 +591,180 @@ def cpu_baseline(prob, name, budget_s=15.0):
                       f"(fp64), repeated {reps} times", "seconds": round(tot, 3)}
 
 
+# ---------------------------------------------------------------------------
+# constrained decoding (compressed finite-state machine)
+# ---------------------------------------------------------------------------
+
+FSM_WORKLOAD = "constrained_decode"
+FSM_SHAPE = {"vocab": 128256, "batch": 256, "n_fields": 8, "max_jump": 16}
+
+
+def fsm_problem():
+    from prefix_shared_kv_radixattention_gb300 import fsm_inputs
+    a = fsm_inputs.json_automaton(vocab=FSM_SHAPE["vocab"], n_fields=FSM_SHAPE["n_fields"])
+    state, logits = fsm_inputs.step_inputs(a, FSM_SHAPE["batch"])
+    return a, state, logits
+
+
+def fsm_config(a, world):
+    return {"workload": FSM_WORKLOAD, "vocab": a.vocab, "batch": FSM_SHAPE["batch"], "states": a.n_states,
+            "edges": int(len(a.tok)), "max_jump": FSM_SHAPE["max_jump"], "constraint": a.schema_text,
+            "l2": "between timed steps: 256 MiB written (evicts the step's inputs), then 256 MiB read "
+                  "(evicts the write's dirty lines)",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU", "launch": "direct calls"}
+
+
+def fsm_oracle_sample(a, jumps, ends, state, logits, n):
+    """The oracle's step over the first n requests; (seconds, requests)."""
+    from oracle import fsm as ofsm
+    t0 = time.perf_counter()
+    ofsm.step(logits[:n], state[:n], a.row_ptr, a.tok, a.nxt, jumps, ends)
+    return time.perf_counter() - t0, n
+
+
+def run_gpu_fsm(args, rank, world, local_rank):
+    import torch
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    a, state0, logits = fsm_problem()
+    B, V, J = FSM_SHAPE["batch"], a.vocab, FSM_SHAPE["max_jump"]
+    m = rx.Fsm(a.n_states, a.vocab, a.row_ptr, a.tok, a.nxt, J)
+    lg = torch.from_numpy(logits).cuda()
+    st0 = torch.from_numpy(state0).cuda()
+    st = st0.clone()
+    out = torch.zeros((B, 1 + J), dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(B, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flush = L2Flush(torch)
+    E = torch.cuda.Event
+
+    def step(marks=None):
+        st.copy_(st0)                   # every step starts from the batch's states
+        if marks:
+            marks[0].record()
+        rx.rx_fsm_step(m, lg, st, out, cnt, status)
+        if marks:
+            marks[1].record()
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after warm-up")
+    marks = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(args.steps)]
+    steps_ev = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush()
+            steps_ev[i][0].record()
+            step(marks[i])
+            steps_ev[i][1].record()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after the timed steps")
+    tot_ms = max_over_ranks(sum(a_.elapsed_time(b_) for a_, b_ in steps_ev), dist, "cuda")
+    k_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in marks)
+    emitted = cnt.cpu().numpy()
+    # end to end: pinned host logits and states in, tokens and counts out
+    h_lg = torch.from_numpy(logits).pin_memory()
+    h_st = torch.from_numpy(state0).pin_memory()
+    h_out = torch.empty((B, 1 + J), dtype=torch.int32, pin_memory=True)
+    h_cnt = torch.empty(B, dtype=torch.int32, pin_memory=True)
+    n = max(3, min(args.steps, 200))
+    ev = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(n)]
+    if dist:
+        dist.barrier()
+    for i in range(n):
+        flush()
+        ev[i][0].record()
+        lg.copy_(h_lg, non_blocking=True)
+        st.copy_(h_st, non_blocking=True)
+        rx.rx_fsm_step(m, lg, st, out, cnt, status)
+        h_out.copy_(out, non_blocking=True)
+        h_cnt.copy_(cnt, non_blocking=True)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(a_.elapsed_time(b_) for a_, b_ in ev), dist, "cuda")
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after the end-to-end steps")
+    if dist:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    hbm, _, _, peak_src = measured_peaks()
+    W = (V + 31) // 32
+    algo = B * (V * 4 + W * 4)          # each request's logits row and its state's mask row
+    achieved = algo / (k_ms / 1e3) / 1e9
+    traffic, tsrc = profiled_traffic(FSM_WORKLOAD, "fsm")
+    line = {
+        "metric": "constrained decode: requests/s", "value": round(job_throughput(B, world, args.steps, tot_ms), 3),
+        "unit": "req/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded JSON-object constraint, N(0,1) fp32 logits)",
+        "config": fsm_config(a, world),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": traffic, "traffic_source": tsrc,
+                     "kernel": "rx_fsm_step (fsm_step_kernel)", "algorithmic_bytes_per_launch": int(algo),
+                     "launch_ms": round(k_ms, 5), "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"},
+        "e2e": {"value": round(job_throughput(B, world, n, e2e_ms), 3), "unit": "req/s",
+                "h2d_bytes_per_step": int(logits.nbytes + state0.nbytes),
+                "d2h_bytes_per_step": int(out.numel() * 4 + cnt.numel() * 4), "ms_per_step": round(e2e_ms / n, 5),
+                "steps": n},
+        "gpu_launches": args.steps, "clocks": clk.summary(),
+        "parts": {"fsm_step": {"ms": k_ms, "tokens_per_step": float(emitted.mean()),
+                               "jump_tokens_per_step": float(emitted.mean() - 1.0)}},
+        "wall_s_timed_loop": round(t_wall, 3),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        from oracle import fsm as ofsm
+        jumps, ends, _ = ofsm.compress(a.n_states, a.row_ptr, a.tok, a.nxt, J)
+        tot, work, reps = 0.0, 0, 0
+        while tot < args.cpu_seconds and reps < 1000:
+            sec, nr = fsm_oracle_sample(a, jumps, ends, state0, logits, B)
+            tot, work, reps = tot + sec, work + nr, reps + 1
+        line["cpu_baseline"] = {"value": round(work / tot, 3), "unit": "req/s", "cores": 1, "kind": "oracle",
+                                "sample": f"the oracle's step over all {B} requests, repeated {reps} times",
+                                "seconds": round(tot, 3)}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_fsm(args, rank, world):
+    if rank != 0:
+        return
+    from oracle import fsm as ofsm
+    a, state0, logits = fsm_problem()
+    B, J = FSM_SHAPE["batch"], FSM_SHAPE["max_jump"]
+    jumps, ends, _ = ofsm.compress(a.n_states, a.row_ptr, a.tok, a.nxt, J)
+    secs = []
+    for i in range(args.warmup + args.steps):
+        s, _ = fsm_oracle_sample(a, jumps, ends, state0, logits, B)
+        if i >= args.warmup:
+            secs.append(s)
+    tot = sum(secs)
+    value = B * args.steps / tot
+    line = {"impl": "reference", "metric": "constrained decode: requests/s", "value": round(value, 3),
+            "unit": "req/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 (argmax), int", "data": "synthetic (seeded JSON-object constraint)",
+            "config": fsm_config(a, world),
+            "cpu_baseline": {"value": round(value, 3), "unit": "req/s", "cores": 1, "kind": "oracle",
+                             "sample": f"the oracle's step over all {B} requests per step"},
+            "e2e": {"value": round(value, 3), "unit": "req/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -634,7 +811,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="few_shot_decode", choices=sorted(inputs.FULL_SIZE))
+    ap.add_argument("--workload", default="few_shot_decode", choices=sorted(inputs.FULL_SIZE) + [FSM_WORKLOAD])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -652,7 +829,12 @@ def main():
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
-    if args.impl == "reference":
+    if args.workload == FSM_WORKLOAD:
+        if args.impl == "reference":
+            run_reference_fsm(args, rank, world)
+        else:
+            run_gpu_fsm(args, rank, world, local_rank)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_gpu(args, rank, world, local_rank)

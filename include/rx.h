@@ -442,9 +442,14 @@ int rx_attn_decode_static(const rx_kv_pool *pool, const void *q, void *o, float 
  * the path of single-edge states from s, and the state where it stops (the
  * first state with zero or several edges, a state the path already passed,
  * or after max_jump tokens) -- packed as jump_len [S], jump_off [S] (int64,
- * state order), jump_end [S] and jump_tok [sum of jump_len]; and the
+ * state order), jump_end [S] and jump_tok [sum of jump_len]; the
  * allowed-token mask: bit t % 32 of word t / 32 of row s is set when state s
- * has an edge with token t, uint32 [S][ceil(vocab / 32)].  Any output may be
+ * has an edge with token t, uint32 [S][W] with W = ceil(vocab / 128) * 4
+ * (rows padded to 16 bytes with zero words); and its word ranks:
+ * rank[s][w] = the number of edges of state s with a token below 32 w,
+ * int32 [S][W] (so that the edge of an allowed token t
+ * is row_ptr[s] + rank[s][t / 32] + the set bits of its mask word below
+ * t % 32, found without a search).  Any output may be
  * NULL; info (required) gets the sizes, so a first call with NULL outputs
  * sizes jump_tok.  RX_ERR_INVALID (nothing written) for arrays that break
  * the rules above; RX_ERR_CAPACITY when out_jump_tok is given and
@@ -458,9 +463,9 @@ typedef struct {
 } rx_fsm_info;
 
 int rx_fsm_compress(int32_t n_states, int32_t vocab, const int64_t *row_ptr, const int32_t *tok,
-                    const int32_t *nxt, int32_t max_jump, uint32_t *out_mask, int32_t *out_jump_len,
-                    int64_t *out_jump_off, int32_t *out_jump_end, int32_t *out_jump_tok,
-                    int64_t jump_tok_cap, rx_fsm_info *info);
+                    const int32_t *nxt, int32_t max_jump, uint32_t *out_mask, int32_t *out_rank,
+                    int32_t *out_jump_len, int64_t *out_jump_off, int32_t *out_jump_end,
+                    int32_t *out_jump_tok, int64_t jump_tok_cap, rx_fsm_info *info);
 
 /* The compressed machine on the device: copies of the automaton's arrays and
  * of rx_fsm_compress's outputs (for the same max_jump), owned by the caller. */
@@ -469,6 +474,7 @@ typedef struct {
     const int32_t *tok;
     const int32_t *nxt;
     const uint32_t *mask;
+    const int32_t *rank;
     const int32_t *jump_len;
     const int64_t *jump_off;
     const int32_t *jump_end;
@@ -487,7 +493,8 @@ typedef struct {
  * id out of range (or a mask bit without its edge) RX_DEV_BAD_STATE; such a
  * request gets out_count[b] = 0 and keeps its state.
  *   logits: device fp32 rows of logits_stride floats (>= vocab, a multiple
- *   of 4, rows 16-byte aligned); state: device int32 [batch], updated in
+ *   of 4, rows 16-byte aligned); fsm->mask 16-byte aligned; state: device
+ *   int32 [batch], updated in
  *   place; out_tokens: device int32 [batch][1 + max_jump]; out_count: device
  *   int32 [batch].  Rows are read once, as 16-byte vectors. */
 int rx_fsm_step(const rx_fsm *fsm, const float *logits, int64_t logits_stride, int32_t batch,

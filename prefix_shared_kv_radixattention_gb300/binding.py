@@ -105,12 +105,12 @@ class FsmInfo(ctypes.Structure):
 
 
 class FsmStruct(ctypes.Structure):
-    _fields_ = [("row_ptr", _P), ("tok", _P), ("nxt", _P), ("mask", _P), ("jump_len", _P), ("jump_off", _P),
-                ("jump_end", _P), ("jump_tok", _P), ("n_states", ctypes.c_int32), ("vocab", ctypes.c_int32),
-                ("max_jump", ctypes.c_int32)]
+    _fields_ = [("row_ptr", _P), ("tok", _P), ("nxt", _P), ("mask", _P), ("rank", _P), ("jump_len", _P),
+                ("jump_off", _P), ("jump_end", _P), ("jump_tok", _P), ("n_states", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("max_jump", ctypes.c_int32)]
 
 
-_sig("rx_fsm_compress", ctypes.c_int, _I32, _I32, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _I64,
+_sig("rx_fsm_compress", ctypes.c_int, _I32, _I32, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _I64,
      ctypes.POINTER(FsmInfo))
 _sig("rx_fsm_step", ctypes.c_int, ctypes.POINTER(FsmStruct), _P, _I64, _I32, _P, _P, _P, _P, _P)
 _sig("rx_schedule", ctypes.c_int, _P, _P, _P, _I32, _I32, _P, _P)
@@ -523,25 +523,26 @@ def rx_attn_decode_static(k_pool, v_pool, q, o, lse, req_idx, seq_len, req_to_to
 
 def rx_fsm_compress(n_states: int, vocab: int, row_ptr, tok, nxt, max_jump: int):
     """Host compression of a token automaton (CSR).  Returns (mask uint32
-    [S, ceil(V/32)], jump_len int32 [S], jump_off int64 [S], jump_end int32
-    [S], jump_tok int32 [total], info)."""
+    [S, W], rank int32 [S, W] with W = ceil(V / 128) * 4, jump_len int32 [S],
+    jump_off int64 [S], jump_end int32 [S], jump_tok int32 [total], info)."""
     rp, rpp = _np(row_ptr, np.int64)
     t, tp = _np(tok, np.int32)
     n, np_ = _np(nxt, np.int32)
     info = FsmInfo()
     _check(_lib.rx_fsm_compress(int(n_states), int(vocab), rpp, tp if len(t) else None, np_ if len(n) else None,
-                                int(max_jump), None, None, None, None, None, 0, ctypes.byref(info)))
-    W = (int(vocab) + 31) // 32
+                                int(max_jump), None, None, None, None, None, None, 0, ctypes.byref(info)))
+    W = (int(vocab) + 127) // 128 * 4   # mask words per state, rows padded to 16 bytes
     mask = np.empty((int(n_states), W), np.uint32)
+    rank = np.empty((int(n_states), W), np.int32)
     jl = np.empty(int(n_states), np.int32)
     jo = np.empty(int(n_states), np.int64)
     je = np.empty(int(n_states), np.int32)
     jt = np.empty(max(1, int(info.jump_tokens)), np.int32)
     _check(_lib.rx_fsm_compress(int(n_states), int(vocab), rpp, tp if len(t) else None, np_ if len(n) else None,
-                                int(max_jump), mask.ctypes.data_as(_P), jl.ctypes.data_as(_P),
-                                jo.ctypes.data_as(_P), je.ctypes.data_as(_P), jt.ctypes.data_as(_P), len(jt),
-                                ctypes.byref(info)))
-    return mask, jl, jo, je, jt[:int(info.jump_tokens)], info
+                                int(max_jump), mask.ctypes.data_as(_P), rank.ctypes.data_as(_P),
+                                jl.ctypes.data_as(_P), jo.ctypes.data_as(_P), je.ctypes.data_as(_P),
+                                jt.ctypes.data_as(_P), len(jt), ctypes.byref(info)))
+    return mask, rank, jl, jo, je, jt[:int(info.jump_tokens)], info
 
 
 class Fsm:
@@ -550,7 +551,7 @@ class Fsm:
 
     def __init__(self, n_states: int, vocab: int, row_ptr, tok, nxt, max_jump: int):
         torch = _torch()
-        mask, jl, jo, je, jt, info = rx_fsm_compress(n_states, vocab, row_ptr, tok, nxt, max_jump)
+        mask, rank, jl, jo, je, jt, info = rx_fsm_compress(n_states, vocab, row_ptr, tok, nxt, max_jump)
         self.info = info
         self.n_states, self.vocab, self.max_jump = int(n_states), int(vocab), int(max_jump)
 
@@ -564,10 +565,12 @@ class Fsm:
         self.tok = dev(tok, np.int32)
         self.nxt = dev(nxt, np.int32)
         self.mask = torch.from_numpy(mask.view(np.int32)).cuda()
+        self.rank = torch.from_numpy(rank).cuda()
         self.jump_len, self.jump_off = dev(jl, np.int32), dev(jo, np.int64)
         self.jump_end, self.jump_tok = dev(je, np.int32), dev(jt, np.int32)
         self.struct = FsmStruct(self.row_ptr.data_ptr(), self.tok.data_ptr(), self.nxt.data_ptr(),
-                                self.mask.data_ptr(), self.jump_len.data_ptr(), self.jump_off.data_ptr(),
+                                self.mask.data_ptr(), self.rank.data_ptr(), self.jump_len.data_ptr(),
+                                self.jump_off.data_ptr(),
                                 self.jump_end.data_ptr(), self.jump_tok.data_ptr(), self.n_states, self.vocab,
                                 self.max_jump)
 

@@ -34,12 +34,19 @@ def random_automaton(rng, n_states, vocab, p_single=0.3, loops=True):
 
 
 def _compare(S, V, row_ptr, tok, nxt, max_jump):
-    mask, jl, jo, je, jt, info = rx.rx_fsm_compress(S, V, row_ptr, tok, nxt, max_jump)
+    mask, rank, jl, jo, je, jt, info = rx.rx_fsm_compress(S, V, row_ptr, tok, nxt, max_jump)
     jumps, ends, looped = ref.compress(S, row_ptr, tok, nxt, max_jump)
     length, offset, end, toks = ref.jump_table(jumps, ends)
     assert jl.tolist() == length.tolist() and jo.tolist() == offset.tolist()
     assert je.tolist() == end.tolist() and jt.tolist() == toks.tolist()
-    assert np.array_equal(mask, ref.allowed_mask(S, V, row_ptr, tok))
+    W = (V + 127) // 128 * 4          # rows padded to 16 bytes
+    assert mask.shape == (S, W)
+    assert np.array_equal(mask[:, :(V + 31) // 32], ref.allowed_mask(S, V, row_ptr, tok))
+    assert not mask[:, (V + 31) // 32:].any()
+    # word ranks: edges of the state with a token below 32 w
+    for s in range(S):
+        t = np.asarray(tok[row_ptr[s]:row_ptr[s + 1]])
+        assert rank[s].tolist() == [int(np.sum(t < 32 * w)) for w in range(W)]
     assert info.n_edges == len(tok) and info.jump_tokens == len(toks)
     assert info.n_singular == int(np.sum(np.diff(row_ptr) == 1))
     assert info.n_looped == sum(looped) and info.longest_jump == (max(length) if S else 0)
@@ -76,7 +83,7 @@ def test_compress_rejects_bad_automata():
         t = np.asarray(tok, np.int32)
         n = np.asarray(nxt, np.int32)
         return lib.rx_fsm_compress(S, V, rp.ctypes.data_as(P), t.ctypes.data_as(P), n.ctypes.data_as(P),
-                                   max_jump, None, None, None, None,
+                                   max_jump, None, None, None, None, None,
                                    None if jt is None else jt.ctypes.data_as(P), cap, ctypes.byref(info))
 
     assert call(2, 4, [0, 2, 2], [1, 3], [1, 0]) == rx.RX_OK
