@@ -482,6 +482,7 @@ PROFILED_TRAFFIC = {
     ("few_shot_decode", "decode"): (298_800_000, "profiles/decode_kernel.few_shot_decode.md"),
     ("tree_of_thought_decode", "decode"): (401_500_000, "profiles/decode_kernel.tree_of_thought_decode.md"),
     ("cached_prefix_extend", "staged"): (585_800_000, "profiles/extend_kernel.cached_prefix_extend.md"),
+    ("constrained_decode", "fsm"): (132_000_000, "profiles/fsm_step_kernel.constrained_decode.md"),
 }
 
 
