@@ -482,7 +482,7 @@ PROFILED_TRAFFIC = {
     ("few_shot_decode", "decode"): (298_800_000, "profiles/decode_kernel.few_shot_decode.md"),
     ("tree_of_thought_decode", "decode"): (401_500_000, "profiles/decode_kernel.tree_of_thought_decode.md"),
     ("cached_prefix_extend", "staged"): (585_800_000, "profiles/extend_kernel.cached_prefix_extend.md"),
-    ("constrained_decode", "fsm"): (132_000_000, "profiles/fsm_step_kernel.constrained_decode.md"),
+    ("constrained_decode", "fsm"): (132_300_000, "profiles/fsm_scan_kernel.constrained_decode.md"),
 }
 
 
@@ -640,6 +640,7 @@ def run_gpu_fsm(args, rank, world, local_rank):
     out = torch.zeros((B, 1 + J), dtype=torch.int32, device="cuda")
     cnt = torch.zeros(B, dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = rx.fsm_workspace(B)
     flush = L2Flush(torch)
     E = torch.cuda.Event
 
@@ -647,7 +648,7 @@ def run_gpu_fsm(args, rank, world, local_rank):
         st.copy_(st0)                   # every step starts from the batch's states
         if marks:
             marks[0].record()
-        rx.rx_fsm_step(m, lg, st, out, cnt, status)
+        rx.rx_fsm_step(m, lg, st, out, cnt, ws, status)
         if marks:
             marks[1].record()
 
@@ -692,7 +693,7 @@ def run_gpu_fsm(args, rank, world, local_rank):
         ev[i][0].record()
         lg.copy_(h_lg, non_blocking=True)
         st.copy_(h_st, non_blocking=True)
-        rx.rx_fsm_step(m, lg, st, out, cnt, status)
+        rx.rx_fsm_step(m, lg, st, out, cnt, ws, status)
         h_out.copy_(out, non_blocking=True)
         h_cnt.copy_(cnt, non_blocking=True)
         ev[i][1].record()
@@ -717,13 +718,14 @@ def run_gpu_fsm(args, rank, world, local_rank):
         "config": fsm_config(a, world),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": traffic, "traffic_source": tsrc,
-                     "kernel": "rx_fsm_step (fsm_step_kernel)", "algorithmic_bytes_per_launch": int(algo),
+                     "kernel": "rx_fsm_step (fsm_scan_kernel + fsm_finish_kernel)",
+                     "algorithmic_bytes_per_launch": int(algo),
                      "launch_ms": round(k_ms, 5), "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"},
         "e2e": {"value": round(job_throughput(B, world, n, e2e_ms), 3), "unit": "req/s",
                 "h2d_bytes_per_step": int(logits.nbytes + state0.nbytes),
                 "d2h_bytes_per_step": int(out.numel() * 4 + cnt.numel() * 4), "ms_per_step": round(e2e_ms / n, 5),
                 "steps": n},
-        "gpu_launches": args.steps, "clocks": clk.summary(),
+        "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
         "parts": {"fsm_step": {"ms": k_ms, "tokens_per_step": float(emitted.mean()),
                                "jump_tokens_per_step": float(emitted.mean() - 1.0)}},
         "wall_s_timed_loop": round(t_wall, 3),

@@ -493,13 +493,16 @@ typedef struct {
  * id out of range (or a mask bit without its edge) RX_DEV_BAD_STATE; such a
  * request gets out_count[b] = 0 and keeps its state.
  *   logits: device fp32 rows of logits_stride floats (>= vocab, a multiple
- *   of 4, rows 16-byte aligned); fsm->mask 16-byte aligned; state: device
- *   int32 [batch], updated in
+ *   of 4, rows 16-byte aligned); state: device int32 [batch], updated in
  *   place; out_tokens: device int32 [batch][1 + max_jump]; out_count: device
- *   int32 [batch].  Rows are read once, as 16-byte vectors. */
+ *   int32 [batch]; workspace: device uint64 [batch], 8-byte aligned, all
+ *   zero before the first call -- every call leaves it zero (the per-request
+ *   best candidate while the call runs).  Rows are read once, as 16-byte
+ *   vectors.  Two kernels on `stream`: the scan, then the finish as its
+ *   programmatic dependent. */
 int rx_fsm_step(const rx_fsm *fsm, const float *logits, int64_t logits_stride, int32_t batch,
-                int32_t *state, int32_t *out_tokens, int32_t *out_count, int32_t *dev_status,
-                void *stream);
+                int32_t *state, int32_t *out_tokens, int32_t *out_count, uint64_t *workspace,
+                int32_t *dev_status, void *stream);
 
 #ifdef __cplusplus
 }

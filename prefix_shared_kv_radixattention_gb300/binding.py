@@ -112,7 +112,7 @@ class FsmStruct(ctypes.Structure):
 
 _sig("rx_fsm_compress", ctypes.c_int, _I32, _I32, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _I64,
      ctypes.POINTER(FsmInfo))
-_sig("rx_fsm_step", ctypes.c_int, ctypes.POINTER(FsmStruct), _P, _I64, _I32, _P, _P, _P, _P, _P)
+_sig("rx_fsm_step", ctypes.c_int, ctypes.POINTER(FsmStruct), _P, _I64, _I32, _P, _P, _P, _P, _P, _P)
 _sig("rx_schedule", ctypes.c_int, _P, _P, _P, _I32, _I32, _P, _P)
 _sig("rx_kv_store", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I64, _P, _P)
 _sig("rx_rope", ctypes.c_int, _P, _P, _I64, _I32, _I32, ctypes.c_double, _P)
@@ -575,11 +575,22 @@ class Fsm:
                                 self.max_jump)
 
 
-def rx_fsm_step(fsm: Fsm, logits, state, out_tokens, out_count, dev_status=None, stream=None) -> None:
+def fsm_workspace(batch: int):
+    """The zeroed device workspace rx_fsm_step needs for `batch` requests
+    (every call leaves it zero, so it can be kept and reused)."""
+    torch = _torch()
+    return torch.zeros(max(1, int(batch)), dtype=torch.int64, device="cuda")
+
+
+def rx_fsm_step(fsm: Fsm, logits, state, out_tokens, out_count, workspace, dev_status=None,
+                stream=None) -> None:
     """One constrained decoding step: logits fp32 [B, >= V] (rows 16-byte
     aligned), state int32 [B] (updated), out_tokens int32 [B, 1 + max_jump],
-    out_count int32 [B]."""
+    out_count int32 [B], workspace from fsm_workspace(B)."""
     torch = _torch()
+    _dev(workspace, torch.int64, "workspace")
+    if workspace.numel() < state.numel():
+        raise ValueError("rx_fsm_step: workspace smaller than the batch")
     _dev(logits, torch.float32, "logits")
     _dev(state, torch.int32, "state")
     _dev(out_tokens, torch.int32, "out_tokens")
@@ -590,4 +601,5 @@ def rx_fsm_step(fsm: Fsm, logits, state, out_tokens, out_count, dev_status=None,
             out_count.numel() != B:
         raise ValueError("rx_fsm_step: logits [B, V], out_tokens [B, 1 + max_jump], out_count [B]")
     _check(_lib.rx_fsm_step(ctypes.byref(fsm.struct), _ptr(logits), logits.shape[1], B, _ptr(state),
-                            _ptr(out_tokens), _ptr(out_count), _ptr(dev_status), _stream(stream)))
+                            _ptr(out_tokens), _ptr(out_count), _ptr(workspace), _ptr(dev_status),
+                            _stream(stream)))

@@ -18,15 +18,15 @@
 //     follows that edge, and emits the jump of the state it reaches in the
 //     same step (rx_fsm_step, on the device).
 //
-// The step is a streaming pass over each request's logits row (HBM-bound):
-// a cluster of C CTAs shares a row and each CTA takes one slice.  In a CTA
-// one thread streams the slice into a ring of shared-memory stages with bulk
-// copies (cp.async.bulk onto mbarriers: 96 KB in flight per CTA, no
-// registers held) together with the matching words of the request state's
-// allowed-token mask, and fifteen warps scan each landed stage from shared
-// memory alone.  The CTAs' best (value, id) pairs meet
-// in CTA 0 through distributed shared memory, and one warp of CTA 0 follows
-// the edge and writes the jump.
+// The step is a streaming pass over each request's logits row (HBM-bound),
+// in two kernels on one stream.  The scan kernel's CTAs (one resident wave)
+// walk (request, 16384-id tile) pairs with 16-byte loads of logits and of
+// the 32-bit allowed-token mask words of the request's state, and fold each
+// tile's allowed candidates into the request's best (value, id) key with a
+// 64-bit atomicMax.  The finish kernel, a programmatic dependent of the scan,
+// gives each request a warp that follows the chosen edge without a search
+// (a per-word prefix count of the state's edges), writes the jump, and sets
+// the request's key back to zero for the next call.
 #include <algorithm>
 #include <climits>
 #include <cmath>
@@ -37,19 +37,11 @@
 
 namespace {
 
-constexpr int kFsmThreads = 512;                  // warp 0 copies, warps 1 .. 15 scan
-constexpr int kFsmScanWarps = kFsmThreads / 32 - 1;
-constexpr int kFsmScanThreads = 32 * kFsmScanWarps;
-constexpr int kFsmMaxCluster = 8;
-constexpr int kFsmStages = 3;                     // ring of logits stages per CTA
-constexpr int kFsmStageIds = 8192;                // 32 KB of fp32 logits a stage
-constexpr int kFsmGroups = kFsmStageIds / 4;      // 16-byte groups of four ids a stage
-constexpr int kFsmCopyBytes = 8192;               // largest single bulk copy
-constexpr int kFsmGroupsPerThread = (kFsmGroups + kFsmScanThreads - 1) / kFsmScanThreads;
-constexpr int kFsmOffMask = kFsmStages * kFsmStageIds * 4;         // mask words [S][ids / 32]
-constexpr int kFsmOffBar = kFsmOffMask + kFsmStages * (kFsmStageIds / 32) * 4;  // full [S], empty [S]
-constexpr int kFsmOffAbort = kFsmOffBar + 2 * kFsmStages * 8;
-constexpr int kFsmSmem = kFsmOffAbort + 16 + 128;  // + room to align the base to 128
+constexpr int kScanThreads = 512;
+constexpr int kTileIds = 16384;          // ids of one scan tile (64 KB of fp32 logits)
+constexpr int kScanUnroll = 4;           // 16-byte groups each thread has in flight
+constexpr int kScanCtasPerSm = 3;        // resident scan CTAs per SM (registers allow three)
+constexpr int kFinishThreads = 256;      // one warp per request
 
 struct FsmParams {
     const int64_t *row_ptr;
@@ -66,258 +58,102 @@ struct FsmParams {
     int32_t *state;
     int32_t *out_tokens;
     int32_t *out_count;
+    unsigned long long *best;
     int32_t *status;
-    int32_t n_states, vocab, max_jump, words, chunk;
+    int32_t n_states, vocab, max_jump, words, batch, tiles_per_row;
 };
 
-// candidate (v, i) beats (bv, bi): larger value, or equal value and smaller id
-__device__ __forceinline__ bool beats(float v, int i, float bv, int bi)
+// Order-preserving key of a candidate (value v, id i): a larger value, then
+// a smaller id, gives a larger key.  NaN counts as -inf and -0 as +0 (equal
+// values tie); every candidate's key is above 0, which means "none".
+__device__ __forceinline__ unsigned long long key_of(float v, int i)
 {
-    return v > bv || (v == bv && i < bi);
+    if (v != v) v = -INFINITY;
+    if (v == 0.f) v = 0.f;
+    uint32_t u = __float_as_uint(v);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i);
 }
 
-__device__ __forceinline__ void take(float v, int i, float &bv, int &bi)
+// Scan: CTAs walk (request, tile) pairs and fold each tile's allowed
+// candidates into the request's best key with a 64-bit atomicMax, one per
+// warp and tile.  16-byte loads of logits and of the state's mask words,
+// four groups in flight per thread.
+__global__ void __launch_bounds__(kScanThreads, kScanCtasPerSm) fsm_scan_kernel(const FsmParams p)
 {
-    v = (v != v) ? -INFINITY : v;  // NaN counts as -inf
-    if (beats(v, i, bv, bi)) {
-        bv = v;
-        bi = i;
-    }
-}
-
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n"
-                 "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-// value at the same shared-memory offset in CTA `rank` of this cluster
-__device__ __forceinline__ uint32_t dsmem_ld_u32(const void *local, uint32_t rank)
-{
-    uint32_t addr = rx::smem_u32(local), remote, v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(addr), "r"(rank));
-    asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(remote) : "memory");
-    return v;
-}
-
-// bounded wait of one thread (the copying lane); false on timeout or abort
-__device__ __forceinline__ bool fsm_wait1(uint32_t bar, uint32_t parity, volatile int *abort_flag, int32_t *status)
-{
-    const long long t0 = clock64();
-    do {
-        if (rx::mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-    } while (clock64() - t0 < rx::kWaitCycles);
-    if (!*abort_flag) {
-        *abort_flag = 1;
-        if (status) atomicOr(status, RX_DEV_TIMEOUT);
-    }
-    return false;
-}
-
-// bounded wait of a whole warp; false (for every lane) on timeout or abort
-__device__ __forceinline__ bool fsm_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                              int32_t *status)
-{
-    bool ok = false;
-    const long long t0 = clock64();
-    do {
-        if (rx::mbar_try_wait(bar, parity)) {
-            ok = true;
-            break;
-        }
-        if (*abort_flag) break;
-    } while (clock64() - t0 < rx::kWaitCycles);
-    if (!ok && !*abort_flag) {
-        *abort_flag = 1;
-        if (status) atomicOr(status, RX_DEV_TIMEOUT);
-    }
-    return __all_sync(0xffffffffu, ok);
-}
-
-__global__ void __launch_bounds__(kFsmThreads) fsm_step_kernel(const FsmParams p)
-{
-    extern __shared__ __align__(128) unsigned char fraw[];
-    __shared__ float wv[kFsmThreads / 32];
-    __shared__ int wi[kFsmThreads / 32];
-    __shared__ float cta_v;
-    __shared__ int cta_i;
-    const uint32_t raw = rx::smem_u32(fraw);
-    unsigned char *smem = fraw + (((raw + 127u) & ~127u) - raw);
-    const float *buf = reinterpret_cast<const float *>(smem);
-    const uint32_t *mbuf = reinterpret_cast<const uint32_t *>(smem + kFsmOffMask);
-    const uint32_t bar = rx::smem_u32(smem + kFsmOffBar);  // full [S], empty [S]
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kFsmOffAbort);
-    const uint32_t rank = cluster_rank();
-    uint32_t nrank;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(nrank));
-    const int b = (int)(blockIdx.x / nrank);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kFsmStages; ++i) {
-            rx::mbar_init(bar + 8 * i, 1);                                 // the copying lane + bytes
-            rx::mbar_init(bar + 8 * (kFsmStages + i), kFsmScanWarps);      // scanning warps
-        }
-        *abort_flag = 0;
-        rx::fence_mbar_init();
-    }
-    __syncthreads();
-    const int s = __ldg(p.state + b);
-    const bool good = s >= 0 && s < p.n_states;
-    const int lo = (int)rank * p.chunk;
-    const int hi = min(p.vocab, lo + p.chunk);
-    const int n_stages = (good && hi > lo) ? (hi - lo + kFsmStageIds - 1) / kFsmStageIds : 0;
-    // requests start their rows at different stages (taken round the row):
-    // the rows' streams then do not walk the same offsets in step
-    const int rot = n_stages ? b % n_stages : 0;
-    auto stage_at = [&](int j) { return j + rot < n_stages ? j + rot : j + rot - n_stages; };
-
-    float bv = -INFINITY;
-    int bi = INT_MAX;
-    if (warp == 0) {
-        if (lane == 0) {
-            // whole 16-byte groups: a row holds at least vocab rounded up to
-            // four ids, and ids past vocab have no mask bit; mask rows are
-            // padded to 16 bytes, and a stage starts on a 128-id boundary
-            const float *row = p.logits + (int64_t)b * p.stride;
-            const uint32_t *mrow = p.mask + (int64_t)s * p.words;
-            int j = 0;
-            for (; j < n_stages; ++j) {
-                const int st = j % kFsmStages;
-                if (j >= kFsmStages &&
-                    !fsm_wait1(bar + 8 * (kFsmStages + st), ((j / kFsmStages) - 1) & 1, abort_flag, p.status))
-                    break;
-                const int i0 = lo + stage_at(j) * kFsmStageIds;
-                const int cnt = min(kFsmStageIds, hi - i0);
-                const uint32_t bytes = (uint32_t)((cnt + 3) / 4) * 16u;
-                const uint32_t mbytes = (uint32_t)((cnt + 127) / 128) * 16u;
-                rx::mbar_arrive_expect_tx(bar + 8 * st, bytes + mbytes);
-                // the stage in copies of at most 8 KB, so that it streams in
-                // as several requests at once
-                for (uint32_t c = 0; c < bytes; c += kFsmCopyBytes)
-                    rx::bulk_g2s(rx::smem_u32(buf + st * kFsmStageIds) + c,
-                                 reinterpret_cast<const unsigned char *>(row + i0) + c,
-                                 min((uint32_t)kFsmCopyBytes, bytes - c), bar + 8 * st);
-                rx::bulk_g2s(rx::smem_u32(mbuf + st * (kFsmStageIds / 32)), mrow + i0 / 32, mbytes, bar + 8 * st);
-            }
-            // no copy may still be landing when the CTA exits
-            for (int jj = j > kFsmStages ? j - kFsmStages : 0; jj < j; ++jj) {
-                const long long t0 = clock64();
-                while (!rx::mbar_try_wait(bar + 8 * (jj % kFsmStages), (jj / kFsmStages) & 1))
-                    if (clock64() - t0 >= rx::kWaitCycles) {
-                        if (p.status) atomicOr(p.status, RX_DEV_TIMEOUT);
-                        break;
-                    }
-            }
-        }
-        __syncwarp();
-    } else {
-        const int ct = (int)threadIdx.x - 32;
-        for (int j = 0; j < n_stages; ++j) {
-            const int st = j % kFsmStages;
-            const int i0 = lo + stage_at(j) * kFsmStageIds;       // a multiple of 128: groups sit in mask words
-            const int ng = (min(kFsmStageIds, hi - i0) + 3) / 4;
-            if (!fsm_wait_warp(bar + 8 * st, (j / kFsmStages) & 1, abort_flag, p.status)) break;
-            const float4 *sb = reinterpret_cast<const float4 *>(buf + st * kFsmStageIds);
-            const uint32_t *sm = mbuf + st * (kFsmStageIds / 32);
-            uint32_t mb[kFsmGroupsPerThread];
+    rx::pdl_launch_dependents();  // the finish kernel may launch now and wait on the device
+    const int lane = threadIdx.x & 31;
+    const int total = p.batch * p.tiles_per_row;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        const int b = tile / p.tiles_per_row;
+        const int lo = (tile - b * p.tiles_per_row) * kTileIds;
+        const int hi = min(p.vocab, lo + kTileIds);
+        const int s = __ldg(p.state + b);
+        if (s < 0 || s >= p.n_states) continue;  // flagged by the finish kernel
+        const float4 *row = reinterpret_cast<const float4 *>(p.logits + (int64_t)b * p.stride);
+        const uint32_t *mrow = p.mask + (int64_t)s * p.words;
+        // whole 16-byte groups: a row holds at least vocab rounded up to four
+        // ids, and ids past vocab have no mask bit; a tile starts on a word
+        const int g1 = (hi + 3) / 4;
+        unsigned long long best = 0;
+        for (int g = lo / 4 + (int)threadIdx.x; g < g1; g += kScanThreads * kScanUnroll) {
+            float4 x[kScanUnroll];
+            uint32_t m[kScanUnroll];
 #pragma unroll
-            for (int u = 0; u < kFsmGroupsPerThread; ++u) {
-                const int g = ct + u * kFsmScanThreads;
-                mb[u] = g < ng ? (sm[g >> 3] >> ((4 * g) & 31)) & 0xFu : 0u;
+            for (int u = 0; u < kScanUnroll; ++u) {
+                const int gg = g + u * kScanThreads;
+                m[u] = 0u;
+                if (gg < g1) {
+                    m[u] = (__ldg(mrow + (gg >> 3)) >> ((4 * gg) & 31)) & 0xFu;
+                    x[u] = __ldg(row + gg);
+                }
             }
 #pragma unroll
-            for (int u = 0; u < kFsmGroupsPerThread; ++u) {
-                if (!mb[u]) continue;
-                const int g = ct + u * kFsmScanThreads;
-                const float4 x = sb[g];
-                const int i = i0 + 4 * g;
-                if (mb[u] & 1u) take(x.x, i, bv, bi);
-                if (mb[u] & 2u) take(x.y, i + 1, bv, bi);
-                if (mb[u] & 4u) take(x.z, i + 2, bv, bi);
-                if (mb[u] & 8u) take(x.w, i + 3, bv, bi);
+            for (int u = 0; u < kScanUnroll; ++u) {
+                if (!m[u]) continue;
+                const int i = 4 * (g + u * kScanThreads);
+                if (m[u] & 1u) best = max(best, key_of(x[u].x, i));
+                if (m[u] & 2u) best = max(best, key_of(x[u].y, i + 1));
+                if (m[u] & 4u) best = max(best, key_of(x[u].z, i + 2));
+                if (m[u] & 8u) best = max(best, key_of(x[u].w, i + 3));
             }
-            __syncwarp();
-            if (lane == 0) rx::mbar_arrive(bar + 8 * (kFsmStages + st));
         }
-    }
-    // warp, then CTA
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (beats(ov, oi, bv, bi)) {
-            bv = ov;
-            bi = oi;
-        }
+        for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+        if (lane == 0 && best) atomicMax(p.best + b, best);
     }
+}
+
+// Finish: one warp per request follows the chosen edge and writes the jump,
+// then re-arms the request's key for the next call.
+__global__ void __launch_bounds__(kFinishThreads) fsm_finish_kernel(const FsmParams p)
+{
+    const int b = (int)((blockIdx.x * (unsigned)kFinishThreads + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    // the state is an input (the scan does not write it): read before the wait
+    const int s = b < p.batch ? __ldg(p.state + b) : 0;
+    rx::pdl_wait();  // the scan kernel's keys are complete and visible
+    if (b >= p.batch) return;
+    unsigned long long key = 0;
     if (lane == 0) {
-        wv[warp] = bv;
-        wi[warp] = bi;
+        key = p.best[b];
+        p.best[b] = 0ull;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int w = 1; w < kFsmThreads / 32; ++w)
-            if (beats(wv[w], wi[w], bv, bi)) {
-                bv = wv[w];
-                bi = wi[w];
-            }
-        cta_v = bv;
-        cta_i = bi;
-    }
-    // the cluster's CTAs meet in CTA 0 (both barriers are reached by every
-    // thread of every CTA; the second keeps each CTA's shared memory alive
-    // until CTA 0 has read it)
-    cluster_sync();
-    if (rank == 0 && warp == 0) {
-        float v = -INFINITY;
-        int i = INT_MAX;
-        if (lane < (int)nrank) {
-            v = __uint_as_float(dsmem_ld_u32(&cta_v, (uint32_t)lane));
-            i = (int)dsmem_ld_u32(&cta_i, (uint32_t)lane);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-            if (beats(ov, oi, v, i)) {
-                v = ov;
-                i = oi;
-            }
-        }
-        bv = v;
-        bi = i;
-    }
-    cluster_sync();
-    if (rank != 0 || warp != 0) return;
-
-    // follow the chosen edge, then the jump of the state it reaches
-    int32_t *out = p.out_tokens + (int64_t)b * (1 + p.max_jump);
-    if (!good) {
+    key = __shfl_sync(0xffffffffu, key, 0);
+    const bool good = s >= 0 && s < p.n_states;
+    if (!good || key == 0ull) {  // a bad state, or no token allowed (the text is complete)
         if (lane == 0) {
             p.out_count[b] = 0;
-            if (p.status) atomicOr(p.status, RX_DEV_BAD_STATE);
+            if (p.status) atomicOr(p.status, good ? RX_DEV_FSM_DONE : RX_DEV_BAD_STATE);
         }
         return;
     }
-    if (bi == INT_MAX) {  // no token allowed: the constrained text is complete
-        if (lane == 0) {
-            p.out_count[b] = 0;
-            if (p.status) atomicOr(p.status, RX_DEV_FSM_DONE);
-        }
-        return;
-    }
+    const int bi = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
     int s1 = -1, jl = 0;
     int64_t off = 0;
-    if (lane == 0) {
+    if (lane == 0 && bi >= 0 && bi < p.vocab) {
         // the chosen token's edge: the state's edges below its mask word,
-        // plus the allowed ids below it within the word (three independent
-        // loads, then the edge)
+        // plus the allowed ids below it within the word (no search)
         const int64_t wrd = (int64_t)s * p.words + (bi >> 5);
         const int64_t e = __ldg(p.row_ptr + s) + __ldg(p.rank + wrd) +
                           __popc(__ldg(p.mask + wrd) & ((1u << (bi & 31)) - 1u));
@@ -340,6 +176,7 @@ __global__ void __launch_bounds__(kFsmThreads) fsm_step_kernel(const FsmParams p
         }
         return;
     }
+    int32_t *out = p.out_tokens + (int64_t)b * (1 + p.max_jump);
     for (int k = lane; k < jl; k += 32) out[1 + k] = __ldg(p.jump_tok + off + k);
     if (lane == 0) {
         out[0] = bi;
@@ -449,17 +286,18 @@ extern "C" int rx_fsm_compress(int32_t n_states, int32_t vocab, const int64_t *r
 }
 
 extern "C" int rx_fsm_step(const rx_fsm *fsm, const float *logits, int64_t logits_stride, int32_t batch,
-                           int32_t *state, int32_t *out_tokens, int32_t *out_count, int32_t *dev_status,
-                           void *stream)
+                           int32_t *state, int32_t *out_tokens, int32_t *out_count, uint64_t *workspace,
+                           int32_t *dev_status, void *stream)
 {
     if (!fsm || batch < 0 || fsm->n_states < 1 || fsm->vocab < 1 || fsm->max_jump < 0)
         return rx_set_error(RX_ERR_INVALID, "rx_fsm_step: invalid argument");
     if (batch == 0) return RX_OK;
-    if (!logits || !state || !out_tokens || !out_count || !fsm->row_ptr || !fsm->tok || !fsm->nxt ||
-        !fsm->mask || !fsm->rank || !fsm->jump_len || !fsm->jump_off || !fsm->jump_end || !fsm->jump_tok)
+    if (!logits || !state || !out_tokens || !out_count || !workspace || !fsm->row_ptr || !fsm->tok ||
+        !fsm->nxt || !fsm->mask || !fsm->rank || !fsm->jump_len || !fsm->jump_off || !fsm->jump_end ||
+        !fsm->jump_tok)
         return rx_set_error(RX_ERR_INVALID, "rx_fsm_step: null pointer");
-    if ((reinterpret_cast<uintptr_t>(fsm->mask) & 15) != 0)
-        return rx_set_error(RX_ERR_INVALID, "rx_fsm_step: the mask must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 7) != 0)
+        return rx_set_error(RX_ERR_INVALID, "rx_fsm_step: the workspace must be 8-byte aligned");
     if (logits_stride < fsm->vocab || logits_stride % 4 != 0 ||
         (reinterpret_cast<uintptr_t>(logits) & 15) != 0)
         return rx_set_error(RX_ERR_INVALID,
@@ -480,37 +318,33 @@ extern "C" int rx_fsm_step(const rx_fsm *fsm, const float *logits, int64_t logit
     p.state = state;
     p.out_tokens = out_tokens;
     p.out_count = out_count;
+    p.best = reinterpret_cast<unsigned long long *>(workspace);
     p.status = dev_status;
     p.n_states = fsm->n_states;
     p.vocab = fsm->vocab;
     p.max_jump = fsm->max_jump;
     p.words = (fsm->vocab + 127) / 128 * 4;
-    // CTAs per request: as many as keep the grid to one wave of two
-    // 512-thread CTAs per SM (registers allow two), at most a portable
-    // cluster of 8, and slices of at least 2048 ids
-    const int want = 2 * fsm_num_sms() / batch;
-    const int by_size = std::max(1, fsm->vocab / 2048);
-    const int C = std::max(1, std::min(std::min(want, by_size), kFsmMaxCluster));
-    p.chunk = (int)(((int64_t)fsm->vocab + C - 1) / C);
-    p.chunk = (p.chunk + 127) / 128 * 128;  // slices start on a mask word
-    if ((int64_t)batch * C > INT32_MAX) return rx_set_error(RX_ERR_UNSUPPORTED, "rx_fsm_step: batch too large");
-    static bool configured = false;
-    if (!configured) {
-        RX_CUDA_CHECK(cudaFuncSetAttribute(fsm_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFsmSmem));
-        configured = true;
-    }
+    p.batch = batch;
+    p.tiles_per_row = (fsm->vocab + kTileIds - 1) / kTileIds;
+    const int64_t tiles = (int64_t)batch * p.tiles_per_row;
+    if (tiles > INT32_MAX) return rx_set_error(RX_ERR_UNSUPPORTED, "rx_fsm_step: batch too large");
+    cudaStream_t st = (cudaStream_t)stream;
+    // scan: one resident wave of CTAs walking the (request, tile) pairs
+    const int64_t resident = (int64_t)kScanCtasPerSm * fsm_num_sms();
+    const unsigned grid = (unsigned)std::min<int64_t>(tiles, resident);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(batch * C));
-    cfg.blockDim = dim3(kFsmThreads);
-    cfg.dynamicSmemBytes = kFsmSmem;
-    cfg.stream = (cudaStream_t)stream;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kScanThreads);
+    cfg.stream = st;
+    RX_CUDA_CHECK(cudaLaunchKernelEx(&cfg, fsm_scan_kernel, p));
+    // finish: a programmatic dependent of the scan, waiting on the device
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)(((int64_t)batch * 32 + kFinishThreads - 1) / kFinishThreads));
+    cfg.blockDim = dim3(kFinishThreads);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    RX_CUDA_CHECK(cudaLaunchKernelEx(&cfg, fsm_step_kernel, p));
+    RX_CUDA_CHECK(cudaLaunchKernelEx(&cfg, fsm_finish_kernel, p));
     return RX_OK;
 }

@@ -103,10 +103,10 @@ def test_step_argument_checks_without_a_gpu():
     """Host-side checks run before any CUDA call: a null machine, a negative
     batch; an empty batch is a no-op."""
     lib = rx.library()
-    assert lib.rx_fsm_step(None, None, 8, 1, None, None, None, None, None) == rx.RX_ERR_INVALID
+    assert lib.rx_fsm_step(None, None, 8, 1, None, None, None, None, None, None) == rx.RX_ERR_INVALID
     st = rx.FsmStruct()
     st.n_states, st.vocab, st.max_jump = 2, 8, 4
-    assert lib.rx_fsm_step(ctypes.byref(st), None, 8, -1, None, None, None, None, None) == rx.RX_ERR_INVALID
-    assert lib.rx_fsm_step(ctypes.byref(st), None, 8, 0, None, None, None, None, None) == rx.RX_OK
+    assert lib.rx_fsm_step(ctypes.byref(st), None, 8, -1, None, None, None, None, None, None) == rx.RX_ERR_INVALID
+    assert lib.rx_fsm_step(ctypes.byref(st), None, 8, 0, None, None, None, None, None, None) == rx.RX_OK
     # a null pointer with a non-empty batch
-    assert lib.rx_fsm_step(ctypes.byref(st), None, 8, 1, None, None, None, None, None) == rx.RX_ERR_INVALID
+    assert lib.rx_fsm_step(ctypes.byref(st), None, 8, 1, None, None, None, None, None, None) == rx.RX_ERR_INVALID

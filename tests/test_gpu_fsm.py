@@ -33,8 +33,10 @@ def _run(S, V, row_ptr, tok, nxt, max_jump, state, logits, stride=None):
     out = torch.full((B, 1 + max_jump), -7, dtype=torch.int32, device="cuda")
     cnt = torch.full((B,), -7, dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rx.rx_fsm_step(m, lg, st, out, cnt, status)
+    ws = rx.fsm_workspace(B)
+    rx.rx_fsm_step(m, lg, st, out, cnt, ws, status)
     torch.cuda.synchronize()
+    assert not ws.any()   # left zero for the next call
     o, c, s2 = out.cpu().numpy(), cnt.cpu().numpy(), st.cpu().numpy()
     got = [o[b, :c[b]].tolist() for b in range(B)]
     jumps, ends, _ = ref.compress(S, row_ptr, tok, nxt, max_jump)
@@ -89,7 +91,7 @@ def test_terminal_and_bad_states_are_flagged():
     out = torch.zeros((5, 17), dtype=torch.int32, device="cuda")
     cnt = torch.full((5,), -1, dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rx.rx_fsm_step(m, lg, s_dev, out, cnt, status)
+    rx.rx_fsm_step(m, lg, s_dev, out, cnt, rx.fsm_workspace(5), status)
     torch.cuda.synchronize()
     c, s2 = cnt.cpu().numpy(), s_dev.cpu().numpy()
     assert c.tolist() == [0, 2, 0, 3, 0]
@@ -126,9 +128,10 @@ def test_decoding_loop_matches_oracle():
     cnt = torch.zeros(B, dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     texts = [list(jumps[a.start]) for _ in range(B)]
+    ws = rx.fsm_workspace(B)   # reused: every call leaves it zero
     for k in range(steps):
         lg = torch.from_numpy(rows[k]).cuda()
-        rx.rx_fsm_step(m, lg, st, out, cnt, status)
+        rx.rx_fsm_step(m, lg, st, out, cnt, ws, status)
         o, c = out.cpu().numpy(), cnt.cpu().numpy()
         for b in range(B):
             texts[b].extend(o[b, :c[b]].tolist())
