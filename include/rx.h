@@ -248,6 +248,34 @@ typedef struct {
 int rx_kv_store(const rx_kv_pool *pool, const void *k_new, const void *v_new, const int32_t *slots,
                 int64_t n, int32_t *dev_status, void *stream);
 
+/* ---- FP8 key/value pools (device) ---------------------------------------
+ * Not from the pages, which do not speak of reduced-precision KV: a pool of
+ * OCP FP8 E4M3 codes ("fn": bias 7, subnormals m/8 * 2^-6, no infinities,
+ * largest finite 448), one byte per value in the [S, Hkv, d] layout, with
+ * one fp32 scale per pool.  The value a code stands for is E4M3(code) *
+ * scale, half the bytes of a bf16 pool.
+ *
+ * rx_kv_store_fp8: for each i < n, K[slots[i]] = E4M3(k_new[i] / k_scale)
+ * and the same for V, where the division is a correctly rounded fp32
+ * division of the bf16 value, the code is the nearest (ties to the even
+ * mantissa), magnitudes past 448 saturate to 448 and NaN stays NaN.
+ * k_new, v_new: device bf16 [n, Hkv, d], 16-byte aligned; pools 8-byte
+ * aligned; Hkv * d a multiple of 8.  A slot id outside the pool sets
+ * RX_DEV_BAD_SLOT and its row is not written.  (The attention kernels
+ * read bf16 pools; reading FP8 pools is not built yet.) */
+typedef struct {
+    void *k;          /* device uint8 [num_slots, num_kv_heads, head_dim] */
+    void *v;
+    int64_t num_slots;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    float k_scale;    /* > 0 */
+    float v_scale;    /* > 0 */
+} rx_kv_pool_fp8;
+
+int rx_kv_store_fp8(const rx_kv_pool_fp8 *pool, const void *k_new, const void *v_new, const int32_t *slots,
+                    int64_t n, int32_t *dev_status, void *stream);
+
 /* ---- rotary position embedding (device) --------------------------------
  * Not from the pages, which do not reach inside the model: the position
  * encoding that the Llama-family models whose attention shapes the workloads

@@ -19,13 +19,16 @@ Contents
   * ``tree_ref.schedule`` / ``tree_ref.optimal_hit_rate`` -- cache-aware
                                request order and the optimal cache hit rate
   * ``keys.image_keys``       -- radix-tree keys of an image's tokens
+  * ``fp8.encode`` / ``fp8.quantize_rows`` -- E4M3 codes of FP8 key/value
+                               pools (nearest, ties to even, saturating)
   * ``fsm.compress`` / ``fsm.step`` -- the compressed finite-state machine of
                                constrained decoding: jumps over fixed tokens,
                                and a masked-argmax decoding step with them
 
 Every function here is pinned in ``tests/test_oracle_pins.py``,
-``tests/test_tree_oracle.py``, ``tests/test_image_keys.py`` and
-``tests/test_fsm_oracle.py``; none is "parity unpinned".
+``tests/test_tree_oracle.py``, ``tests/test_image_keys.py``,
+``tests/test_fsm_oracle.py`` and ``tests/test_fp8_oracle.py``; none is
+"parity unpinned".
 """
 from __future__ import annotations
 

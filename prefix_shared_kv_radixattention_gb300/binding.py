@@ -99,6 +99,14 @@ _sig("rx_prefix_len", ctypes.c_int, _P, _P, _I64, _PI64)
 _sig("rx_image_keys", ctypes.c_int, _P, _I64, _I64, _P)
 
 
+class KVPoolFp8(ctypes.Structure):
+    _fields_ = [("k", _P), ("v", _P), ("num_slots", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+
+
+_sig("rx_kv_store_fp8", ctypes.c_int, ctypes.POINTER(KVPoolFp8), _P, _P, _P, _I64, _P, _P)
+
+
 class FsmInfo(ctypes.Structure):
     _fields_ = [("n_edges", ctypes.c_int64), ("jump_tokens", ctypes.c_int64), ("n_singular", ctypes.c_int32),
                 ("n_looped", ctypes.c_int32), ("longest_jump", ctypes.c_int32)]
@@ -603,3 +611,29 @@ def rx_fsm_step(fsm: Fsm, logits, state, out_tokens, out_count, workspace, dev_s
     _check(_lib.rx_fsm_step(ctypes.byref(fsm.struct), _ptr(logits), logits.shape[1], B, _ptr(state),
                             _ptr(out_tokens), _ptr(out_count), _ptr(workspace), _ptr(dev_status),
                             _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# FP8 key/value pools
+# ---------------------------------------------------------------------------
+
+
+def rx_kv_store_fp8(k_pool, v_pool, k_scale: float, v_scale: float, k_new, v_new, slots, dev_status=None,
+                    stream=None) -> None:
+    """Store bf16 rows into uint8 E4M3 pools [S, Hkv, d] with per-pool scales."""
+    torch = _torch()
+    _dev(k_pool, torch.uint8, "k_pool")
+    _dev(v_pool, torch.uint8, "v_pool")
+    _dev(k_new, torch.bfloat16, "k_new")
+    _dev(v_new, torch.bfloat16, "v_new")
+    _dev(slots, torch.int32, "slots")
+    _dev(dev_status, torch.int32, "dev_status")
+    if k_pool.shape != v_pool.shape or k_pool.dim() != 3:
+        raise ValueError("k_pool and v_pool must both be [num_slots, num_kv_heads, head_dim]")
+    S, hkv, d = k_pool.shape
+    n = slots.numel()
+    if k_new.shape != (n, hkv, d) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [n, num_kv_heads, head_dim]")
+    pool = KVPoolFp8(k_pool.data_ptr(), v_pool.data_ptr(), S, hkv, d, float(k_scale), float(v_scale))
+    _check(_lib.rx_kv_store_fp8(ctypes.byref(pool), _ptr(k_new), _ptr(v_new), _ptr(slots), n,
+                                _ptr(dev_status), _stream(stream)))

@@ -38,6 +38,48 @@ __global__ void __launch_bounds__(256) kv_store_kernel(const uint4 *__restrict__
     }
 }
 
+// FP8 store: each thread takes 8 bf16 values (16 bytes) of a new row, divides
+// them by the pool's scale (correctly rounded fp32 division) and writes their
+// E4M3 codes (8 bytes): round to nearest even, magnitudes past 448 saturate.
+__global__ void __launch_bounds__(256) kv_store_fp8_kernel(const uint4 *__restrict__ k_new,
+                                                           const uint4 *__restrict__ v_new,
+                                                           const int32_t *__restrict__ slots,
+                                                           int64_t n_rows, int64_t chunks_per_row,
+                                                           uint2 *__restrict__ k_pool, uint2 *__restrict__ v_pool,
+                                                           int64_t num_slots, float k_scale, float v_scale,
+                                                           int32_t *status)
+{
+    const int64_t total = n_rows * chunks_per_row;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * total; i += step) {
+        const bool is_v = i >= total;
+        const int64_t j = is_v ? i - total : i;
+        const int64_t row = j / chunks_per_row;
+        const int64_t c = j - row * chunks_per_row;
+        const int32_t s = __ldg(slots + row);
+        if (s < 0 || (int64_t)s >= num_slots) {
+            if (status && c == 0 && !is_v) atomicOr(status, RX_DEV_BAD_SLOT);
+            continue;
+        }
+        const uint4 val = is_v ? __ldg(v_new + j) : __ldg(k_new + j);
+        const float scale = is_v ? v_scale : k_scale;
+        const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+        uint32_t codes[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint16_t pair[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[2 * h + q]));
+                const float lo = __fdiv_rn(f.x, scale), hi = __fdiv_rn(f.y, scale);
+                asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(pair[q]) : "f"(hi), "f"(lo));
+            }
+            codes[h] = (uint32_t)pair[0] | ((uint32_t)pair[1] << 16);
+        }
+        (is_v ? v_pool : k_pool)[(int64_t)s * chunks_per_row + c] = make_uint2(codes[0], codes[1]);
+    }
+}
+
 int num_sms()
 {
     static int sms = 0;
@@ -75,6 +117,34 @@ extern "C" int rx_kv_store(const rx_kv_pool *pool, const void *k_new, const void
     kv_store_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
         (const uint4 *)k_new, (const uint4 *)v_new, slots, n, cpr, (uint4 *)pool->k,
         (uint4 *)pool->v, pool->num_slots, dev_status);
+    RX_CUDA_CHECK(cudaGetLastError());
+    return RX_OK;
+}
+
+extern "C" int rx_kv_store_fp8(const rx_kv_pool_fp8 *pool, const void *k_new, const void *v_new,
+                               const int32_t *slots, int64_t n, int32_t *dev_status, void *stream)
+{
+    if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0 ||
+        pool->head_dim <= 0 || n < 0 || (n > 0 && (!k_new || !v_new || !slots)) ||
+        !(pool->k_scale > 0.f) || !(pool->v_scale > 0.f))
+        return rx_set_error(RX_ERR_INVALID, "rx_kv_store_fp8: invalid argument");
+    const int64_t row_elems = (int64_t)pool->num_kv_heads * pool->head_dim;
+    if (row_elems % 8 != 0)
+        return rx_set_error(RX_ERR_UNSUPPORTED, "rx_kv_store_fp8: a row of %lld values is not a multiple of 8",
+                            (long long)row_elems);
+    auto misaligned = [](const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
+    if (misaligned(pool->k, 8) || misaligned(pool->v, 8) || misaligned(k_new, 16) || misaligned(v_new, 16))
+        return rx_set_error(RX_ERR_INVALID, "rx_kv_store_fp8: pools must be 8-byte and new rows 16-byte aligned");
+    if (n == 0) return RX_OK;
+    const int64_t cpr = row_elems / 8;
+    const int64_t work = 2 * n * cpr;
+    const int threads = 256;
+    int64_t blocks = (work + threads - 1) / threads;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    kv_store_fp8_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+        (const uint4 *)k_new, (const uint4 *)v_new, slots, n, cpr, (uint2 *)pool->k, (uint2 *)pool->v,
+        pool->num_slots, pool->k_scale, pool->v_scale, dev_status);
     RX_CUDA_CHECK(cudaGetLastError());
     return RX_OK;
 }
