@@ -142,7 +142,8 @@ class ClockSampler:
 class GpuStep:
     """Device state of one workload and the step that runs the path on it."""
 
-    def __init__(self, prob: inputs.Problem, torch, rx, extend_path: str = "staged", rope_base: float = 0.0):
+    def __init__(self, prob: inputs.Problem, torch, rx, extend_path: str = "staged", rope_base: float = 0.0,
+                 kv_fp8: bool = False):
         self.torch, self.rx, self.prob = torch, rx, prob
         dev = "cuda"
         p = prob
@@ -200,6 +201,12 @@ class GpuStep:
                 nb = rx.rx_attn_extend_workspace(ctx, len(p.ext_req_idx), p.hkv, p.d)
                 self.ext_ws = torch.empty(nb, dtype=torch.uint8, device=dev)
                 self.launches += 2  # packed-row offsets + row copy
+        # FP8 pools (optional): the step's rows also stored as E4M3 codes
+        self.kv_fp8 = kv_fp8
+        if kv_fp8:
+            self.k8 = torch.zeros((p.num_slots, p.hkv, p.d), dtype=torch.uint8, device=dev)
+            self.v8 = torch.zeros_like(self.k8)
+            self.launches += 1
         # rotary position embedding (optional): K rotated on its way into the
         # pool, the step's q rows rotated in place
         self.rope_base = rope_base
@@ -243,8 +250,12 @@ class GpuStep:
                                self.ext_req, self.ext_P, self.ext_E, self.rtt, self.max_E, p.sm_scale,
                                self.status, workspace=self.ext_ws)
 
+    def store_fp8(self):
+        self.rx.rx_kv_store_fp8(self.k8, self.v8, 1.0, 1.0, self.k_new, self.v_new, self.slots, self.status)
+
     def parts(self):
-        return [("store", self.kv_store)] + ([("rope_q", self.rope_q)] if self.rope_base else []) + \
+        return [("store", self.kv_store)] + ([("store_fp8", self.store_fp8)] if self.kv_fp8 else []) + \
+            ([("rope_q", self.rope_q)] if self.rope_base else []) + \
             ([("extend", self.extend)] if self.has_ext else []) + ([("decode", self.decode)] if self.has_dec else [])
 
     def capture(self):
@@ -284,7 +295,7 @@ def run_gpu(args, rank, world, local_rank):
         dist.init_process_group("nccl")
 
     prob = make_problem(args)
-    st = GpuStep(prob, torch, rx, args.extend_path, args.rope)
+    st = GpuStep(prob, torch, rx, args.extend_path, args.rope, getattr(args, "kv_fp8", False))
     flush = L2Flush(torch)
     torch.cuda.synchronize()
 
@@ -378,6 +389,10 @@ def run_gpu(args, rank, world, local_rank):
                     "peak_source": f"{peak_src} bf16_tflops (burst)"}
     out["kv_store"] = {"ms": statistics.mean(part_ms["store"]),
                        "gbs": 2 * len(prob.new_slots) * kv_row / (statistics.mean(part_ms["store"]) / 1e3) / 1e9}
+    if st.kv_fp8:
+        f8 = statistics.mean(part_ms["store_fp8"])
+        n_vals = len(prob.new_slots) * prob.hkv * prob.d
+        out["kv_store_fp8"] = {"ms": f8, "gbs": 2 * n_vals * (2 + 1) / (f8 / 1e3) / 1e9}
     if st.rope_base:
         # K rotated inside the store (above); q rows rotated in place: read and
         # write of every q row
@@ -395,6 +410,8 @@ def run_gpu(args, rank, world, local_rank):
         "roofline": roof, "e2e": e2e, "gpu_launches": st.launches * args.steps,
         "clocks": clk.summary(), "parts": out, "wall_s_timed_loop": round(t_wall, 3),
     }
+    if st.kv_fp8:
+        line["config"]["kv_fp8"] = "extra part: the step's K/V rows also stored as E4M3 codes (scale 1)"
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(prob, args.workload, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -820,6 +837,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="override the pool size (profiling runs on a smaller device footprint)")
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="also store the step's K/V rows into FP8 (E4M3) pools (an extra part of the step)")
     ap.add_argument("--rope", type=float, default=0.0, metavar="BASE",
                     help="add rotary position embedding to the step (K fused into the store, q in place)")
     ap.add_argument("--graph", action="store_true",
