@@ -22,6 +22,15 @@
  *   - a host radix tree (rx_match_prefix / rx_insert / rx_evict_lru) and a
  *     slot free list, which only produce slot ids and prefix lengths.
  *
+ * Around that path:
+ *   - cache-aware scheduling over the tree (rx_prefix_len, rx_schedule);
+ *   - radix keys for an image's tokens (rx_image_keys);
+ *   - the rotary position embedding, in place and fused into the scatter
+ *     (rx_rope, rx_kv_store_rope);
+ *   - FP8 (E4M3) pools and their scatter (rx_kv_store_fp8);
+ *   - the compressed finite-state machine of constrained decoding
+ *     (rx_fsm_compress on the host, rx_fsm_step on the device).
+ *
  * Attention definition (all attention entry points).  For a query row of
  * request b at absolute position p, q-head h, with G = num_q_heads /
  * num_kv_heads and kv-head g = h / G:
