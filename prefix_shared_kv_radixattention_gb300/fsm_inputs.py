@@ -176,6 +176,30 @@ def json_automaton(seed: int = 3001, vocab: int = 128256, n_fields: int = 8) -> 
                           strings, shown)
 
 
+def trim(a: TokenAutomaton) -> TokenAutomaton:
+    """The automaton without its dead ends: edges into states from which
+    the terminal state cannot be reached are dropped (a token that leads
+    nowhere but a dead end is then not allowed).  ``json_automaton`` keeps
+    them, as a plain character walk gives them; a request that reaches one
+    is flagged as having no token left."""
+    S = a.n_states
+    # states that reach the terminal: backwards over the edges
+    src = np.repeat(np.arange(S), np.diff(a.row_ptr))
+    live = np.zeros(S, bool)
+    live[a.terminal] = True
+    changed = True
+    while changed:
+        new = live.copy()
+        np.logical_or.at(new, src, live[a.nxt])
+        changed = bool((new != live).any())
+        live = new
+    keep = live[a.nxt]
+    counts = np.bincount(src[keep], minlength=S)
+    row_ptr = np.zeros(S + 1, np.int64)
+    row_ptr[1:] = np.cumsum(counts)
+    return dataclasses.replace(a, row_ptr=row_ptr, tok=a.tok[keep].copy(), nxt=a.nxt[keep].copy())
+
+
 def reachable_states(a: TokenAutomaton) -> np.ndarray:
     """States reachable from the start along token edges (breadth first)."""
     seen = np.zeros(a.n_states, bool)

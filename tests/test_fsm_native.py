@@ -110,3 +110,30 @@ def test_step_argument_checks_without_a_gpu():
     assert lib.rx_fsm_step(ctypes.byref(st), None, 8, 0, None, None, None, None, None, None) == rx.RX_OK
     # a null pointer with a non-empty batch
     assert lib.rx_fsm_step(ctypes.byref(st), None, 8, 1, None, None, None, None, None, None) == rx.RX_ERR_INVALID
+
+
+def test_json_decoding_emits_schema_text_and_saves_steps():
+    """End to end on the synthetic JSON constraint (oracle only): with logits
+    that favour short values, decoding with jumps reaches the terminal state,
+    the text it emits matches the schema's regular expression, and it takes
+    fewer model steps than tokens (the fixed keys and separators come as
+    jumps)."""
+    import re
+    a = fsm_inputs.trim(fsm_inputs.json_automaton(vocab=6000, n_fields=6))
+    ref.validate(a.n_states, a.vocab, a.row_ptr, a.tok, a.nxt)
+    # trimmed: every reachable state but the terminal one has an edge
+    assert all(a.row_ptr[s + 1] > a.row_ptr[s] for s in fsm_inputs.reachable_states(a) if s != a.terminal)
+    jumps, ends, _ = ref.compress(a.n_states, a.row_ptr, a.tok, a.nxt, 16)
+    rng = np.random.default_rng(3)
+    rows = rng.standard_normal((400, a.vocab)).astype(np.float32)
+    # prefer closing pieces and end-of-sequence once they are allowed
+    closers = [t for t, w in enumerate(a.strings) if w in ("", ', "', '", "', "}", '"}')]
+    rows[:, closers] += 6.0
+    toks, state, used = ref.decode_with_jumps(a.start, a.row_ptr, a.tok, a.nxt, jumps, ends, rows)
+    assert state == a.terminal and toks[-1] == 0           # ended by end-of-sequence
+    text = "".join(a.strings[t] for t in toks)
+    parts = []
+    for i in range(6):
+        parts.append(("{" if i == 0 else ", ") + f'"K{i}": ' + ("[0-9]+" if i % 2 == 0 else '"[a-z ]*"'))
+    assert re.fullmatch("".join(parts) + "}", text), text
+    assert used < len(toks)
