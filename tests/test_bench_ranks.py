@@ -57,3 +57,22 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.job_throughput(10, 1, 4, 2.0) == pytest.approx(10 * 4 / 0.002)
+
+
+def test_reference_arm_json_line_constrained_decode():
+    """The reference arm (the oracle on the host) prints one JSON line with
+    the contract's keys for the constrained-decoding workload."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--workload", "constrained_decode",
+                        "--impl", "reference", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["value"] > 0 and line["config"]["workload"] == "constrained_decode"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
