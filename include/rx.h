@@ -388,8 +388,11 @@ typedef struct {
 
 /* Builds a decode plan.  Inputs (host): req_to_token (row stride rtt_stride),
  * req_idx [batch], seq_len [batch] (> 0); num_q_heads, num_kv_heads;
- * kv_chunk = positions per work item (multiple of 64, <= 4096; 0 picks one
- * that gives about 1216 work items over all kv heads); min_shared =
+ * kv_chunk = positions per work item (multiple of 64, <= 4096; 0 picks one:
+ * about 1216 work items over all kv heads; with all-heads items, shared
+ * chunks for about 76 per-head items -- or 152 (chunk, kv head) pairs when
+ * they go to the all-heads kernel in request groups -- and private pieces
+ * of about 1/304 of the batch's private positions); min_shared =
  * shortest shared segment worth grouping (>= 1).  Requests whose slot lists
  * agree on positions [a, b) (same slot at every position, from position 0 on)
  * form a segment; segments nest like the radix tree the slots came from.
