@@ -497,7 +497,7 @@ def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
 # kernel changes, so that an old count is never reported for new code.
 PROFILED_TRAFFIC = {
     ("few_shot_decode", "decode"): (298_800_000, "profiles/decode_kernel.few_shot_decode.md"),
-    ("tree_of_thought_decode", "decode"): (401_500_000, "profiles/decode_kernel.tree_of_thought_decode.md"),
+    ("tree_of_thought_decode", "decode"): (401_500_000, "profiles/decode_gqa_kernel.tree_of_thought_decode.md"),
     ("cached_prefix_extend", "staged"): (585_800_000, "profiles/extend_kernel.cached_prefix_extend.md"),
     ("constrained_decode", "fsm"): (132_300_000, "profiles/fsm_scan_kernel.constrained_decode.md"),
 }
