@@ -403,3 +403,23 @@ def test_plan_invalid():
     with pytest.raises(rx.RxError) as e:
         rx.rx_decode_plan_build(prob.req_to_token, prob.dec_req_idx, prob.dec_seq_len, 128, 1, 64, 1)
     assert e.value.code == rx.RX_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("hq,batch,all_heads", [(32, 64, True), (32, 68, False), (64, 32, True), (64, 34, False)])
+def test_plan_group_limit(hq, batch, all_heads):
+    """With 8 kv heads, a shared segment whose requests make at most 16
+    groups of 16 / G requests goes to the all-heads kernel, one item per
+    group; one more group sends it to the per-head kernel, in items of
+    64 / G requests."""
+    G = hq // 8
+    prob = inputs.few_shot_decode(hq=hq, hkv=8, d=128, batch=batch, shared=128, private=8, num_slots=8192,
+                                  draw_values=False)
+    order, nparts, items, info = _plan(prob, 128, 16)
+    check_plan(prob, order, nparts, items, info)
+    shared = items[items[:, 2] == 0]                 # the items of the shared prefix (positions 0 ..)
+    if all_heads:
+        assert np.all(shared[:, 1] <= 16 // G) and len(shared) == -(-batch // (16 // G))
+        assert info.n_items == info.n_wide
+    else:
+        assert np.all(shared[:, 1] <= 64 // G) and len(shared) == -(-batch // (64 // G))
+        assert info.n_items - info.n_wide == len(shared)
