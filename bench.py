@@ -508,11 +508,30 @@ def profiled_traffic(workload, part):
     return (hit[0], hit[1]) if hit else (None, None)
 
 
-def make_problem(args):
+TREE_WORKLOADS = ("mixed_chat",)
+WORKLOADS = sorted(list(inputs.FULL_SIZE) + list(TREE_WORKLOADS))
+
+
+def make_problem(args, admit_with="library"):
+    """The workload's batch.  The long multi-turn chat batch is admitted into
+    its full pool through a radix cache: the library's (``admit_with`` =
+    "library") or, for the reference arm, the oracle's trie ("oracle"); both
+    hand out the same slot lists (a CPU test checks it bit for bit)."""
     kw = {}
     if args.pool_slots:
         kw["num_slots"] = args.pool_slots
-    return inputs.FULL_SIZE[args.workload](**kw)
+    if args.workload not in TREE_WORKLOADS:
+        return inputs.FULL_SIZE[args.workload](**kw)
+    scn = inputs.mixed_chat_scenario(**kw)
+    if admit_with == "oracle":
+        from oracle import tree_ref
+        _, out = tree_ref.replay(scn.free_order, scn.prefill, scn.batch)
+        rows, ks = [np.asarray(r, np.int32) for r, _, _ in out], [k for _, k, _ in out]
+    else:
+        from prefix_shared_kv_radixattention_gb300 import admission
+        adm = admission.replay(scn)
+        rows, ks = adm.rows, adm.prefix_lens
+    return inputs.problem_from_admission(scn, rows, ks)
 
 
 def workload_config(prob, name, world, extend_path="staged", graph=False, rope=0.0):
@@ -788,7 +807,7 @@ def run_reference_fsm(args, rank, world):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    prob = make_problem(args)
+    prob = make_problem(args, admit_with="oracle")
     threads = cores()
     pools = _oracle_pools(prob)
     has_dec = len(prob.dec_req_idx) > 0
@@ -831,7 +850,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="few_shot_decode", choices=sorted(inputs.FULL_SIZE) + [FSM_WORKLOAD])
+    ap.add_argument("--workload", default="few_shot_decode", choices=WORKLOADS + [FSM_WORKLOAD])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

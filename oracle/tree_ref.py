@@ -241,6 +241,76 @@ class RadixTreeRef:
 
 
 # ---------------------------------------------------------------------------
+# admission into a token-slot pool
+# ---------------------------------------------------------------------------
+# "Introducción a SGLang", RadixAttention bullet (the cache of finished calls
+# is reused by later calls that share a prefix) and the nine-step walkthrough
+# of "SGLang: Modelo de programación y metodología" (steps 5, 8 and 9: under
+# memory pressure, least-recently-used nodes are evicted to make room, and a
+# request's own matched prefix is kept).  The composition, step by step:
+#   admit(tokens):  match the cached prefix (a use: clock and path), lock it
+#                   (+1), and when the free list holds fewer slots than the
+#                   uncached tokens, evict least-recently-used unlocked leaves
+#                   for the difference and append the freed slots to the free
+#                   list's tail; then take the fresh slots from its head.  If
+#                   the pool still cannot hold the request, unlock and refuse.
+#   commit(tokens): unlock the admitted prefix, insert the whole sequence with
+#                   its slot list, and return to the free list the fresh slots
+#                   of tokens that another request cached in the meantime.
+
+
+class Admission:
+    """A radix cache over a pool whose free slots start as ``free_order``."""
+
+    def __init__(self, free_order: Sequence[int]):
+        from collections import deque
+        self.tree = RadixTreeRef()
+        self.free = deque(int(x) for x in free_order)
+        self.freed: List[int] = []      # every evicted slot, in eviction order
+
+    def admit(self, tokens: Sequence[int]):
+        """(slot list, cached prefix length, tokens evicted); the slot list is
+        None when the pool cannot hold the request."""
+        k, slots = self.tree.match_prefix(tokens)
+        self.tree.lock(tokens[:k], 1)
+        need = len(tokens) - k
+        ev = 0
+        if len(self.free) < need:
+            got = self.tree.evict(need - len(self.free))
+            ev = len(got)
+            self.freed.extend(got)
+            self.free.extend(got)
+        if len(self.free) < need:
+            self.tree.lock(tokens[:k], -1)
+            return None, k, ev
+        fresh = [self.free.popleft() for _ in range(need)]
+        return list(slots) + fresh, k, ev
+
+    def commit(self, tokens: Sequence[int], row: Sequence[int], k: int) -> None:
+        self.tree.lock(tokens[:k], -1)
+        c = self.tree.insert(tokens, row)
+        if c > k:
+            self.free.extend(int(x) for x in row[k:c])
+
+
+def replay(free_order: Sequence[int], prefill: Sequence[Sequence[int]], batch: Sequence[Sequence[int]]):
+    """Admit and commit every prefill sequence in order, then admit every
+    batch request in order (not committed).  Returns the Admission and, per
+    batch request, (slot list, cached prefix length, tokens evicted)."""
+    adm = Admission(free_order)
+    for toks in prefill:
+        toks = [int(t) for t in toks]
+        row, k, _ = adm.admit(toks)
+        if row is None:
+            raise ValueError("a prefill sequence does not fit the pool")
+        adm.commit(toks, row, k)
+    out = []
+    for toks in batch:
+        out.append(adm.admit([int(t) for t in toks]))
+    return adm, out
+
+
+# ---------------------------------------------------------------------------
 # cache-aware scheduling
 # ---------------------------------------------------------------------------
 # "SGLang: Evaluación y resultados": the cache-aware scheduling reaches about

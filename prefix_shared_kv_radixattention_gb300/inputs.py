@@ -20,6 +20,10 @@ Recipe (shared by every family):
   * slot ids: a seeded random permutation of ``[0, num_slots)``, handed out
     in order of first use (shared prefix tokens first, then each request's
     private tokens in request order, then the step's new tokens).
+  * the long multi-turn chat instead comes as a ``Scenario``: token
+    sequences and a free list only; its slot lists are whatever the radix
+    cache hands out when the scenario's admissions are replayed through it
+    (``problem_from_admission`` then draws the values).
 """
 from __future__ import annotations
 
@@ -315,42 +319,142 @@ def tree_of_thought_decode(seed: int = 1004, hq: int = 32, hkv: int = 8, d: int 
                    np.concatenate(edge_slots), new_slots, [], dec, draw_values)
 
 
-def mixed_chat(seed: int = 1005, hq: int = 64, hkv: int = 8, d: int = 128, n_dec: int = 16,
-               system: int = 8192, history: int = 24576, n_ext: int = 16, ext_prefix: int = 4096,
-               ext_new: int = 1024, num_slots: int = 1024 * 1024,
-               draw_values: bool = True) -> Problem:
-    """Long multi-turn chat: decode rows on long shared-system-prompt contexts
-    plus concurrent extend rows on their own cached prefixes.
+@dataclasses.dataclass
+class Scenario:
+    """A batch whose slot lists come out of the radix cache, as data only.
 
-    Full size: Llama-70B attention shape (64 q / 8 kv heads, head_dim 128);
-    16 decode requests of 8192 shared + 24576 private + 1 new tokens, 16
-    extend requests of 1024 new tokens on distinct 4096-token cached
-    prefixes, 1M-slot pool.
+    The pool starts empty with ``free_order`` as its free list.  Every
+    ``prefill`` sequence is admitted (prefix match, fresh slots) and then
+    committed (inserted into the cache), in order; then every ``batch``
+    request is admitted, in order, and not committed: its row of
+    ``req_to_token`` is the admitted slot list.  The first ``n_dec`` batch
+    requests decode one token (all but their last token must be cached); the
+    others extend their cached prefix by their remaining tokens.  Replaying
+    the admissions is the radix cache's job (the library's tree, or the
+    oracle's); this object only says what is admitted and in which order.
+    """
+
+    name: str
+    seed: int
+    hq: int
+    hkv: int
+    d: int
+    num_slots: int
+    free_order: np.ndarray            # int32 [num_slots]
+    prefill: List[np.ndarray]         # int64 token sequences, admitted then committed
+    batch: List[np.ndarray]           # int64 token sequences of the step's requests
+    n_dec: int
+    notes: dict = dataclasses.field(default_factory=dict)
+
+
+def _cold_families(rng: np.random.Generator, volume: int, lo: int, exact: bool) -> List[np.ndarray]:
+    """Cold conversations that take ``volume`` fresh slots (at least, or
+    exactly with ``exact``): families of a system prompt of 256 .. 2048
+    tokens shared by 1 .. 6 continuations of 512 .. 8192 tokens each.
+    Returned in admission order (a family's sequences one after another);
+    token ids come from ranges starting at ``lo``, disjoint per family."""
+    seqs, used, fam = [], 0, 0
+    while used < volume:
+        base = lo + fam * 1_000_000
+        sys_tok = _tokens(rng, int(rng.integers(256, 2049)), base)
+        n_kids = int(rng.integers(1, 7))
+        for k in range(n_kids):
+            fresh_sys = len(sys_tok) if k == 0 else 0
+            n = int(rng.integers(512, 8193))
+            left = volume - used
+            if exact and fresh_sys + n >= left:
+                if left - fresh_sys < 1:         # the shared part alone would not fit
+                    break
+                n = left - fresh_sys
+            seqs.append(np.concatenate([sys_tok, _tokens(rng, n, base + 100_000 + 10_000 * k)]))
+            used += fresh_sys + n
+            if used >= volume:
+                break
+        fam += 1
+        if exact and volume - used > 0 and volume - used < 257:
+            # too little room for another family's system prompt: lengthen
+            # the last continuation instead (its tokens are fresh)
+            extra = volume - used
+            tail = seqs[-1]
+            seqs[-1] = np.concatenate([tail, _tokens(rng, extra, lo + 900_000_000 + fam)])
+            used += extra
+    return seqs
+
+
+def mixed_chat_scenario(seed: int = 1005, hq: int = 64, hkv: int = 8, d: int = 128, n_dec: int = 16,
+                        system: int = 8192, history: int = 24576, n_ext: int = 16, ext_prefix: int = 4096,
+                        ext_new: int = 1024, num_slots: int = 1024 * 1024, cold_before: int = 131072,
+                        fill: bool = True) -> Scenario:
+    """Long multi-turn chat under a full pool: the admissions of one mixed batch.
+
+    Full size: Llama-70B attention shape (64 q / 8 kv heads, head_dim 128).
+      * warm cache: an 8192-token system prompt followed by 16 chat
+        histories of 24576 tokens each (16 sessions on one system prompt),
+        and 16 distinct 4096-token documents;
+      * cold cache: seeded conversations (``_cold_families``), ``cold_before``
+        tokens of them cached before the warm part and the rest after it, so
+        that the 1M-slot pool is exactly full (``fill``);
+      * the batch: 16 decode requests (a session's history plus one new
+        token, 32769 tokens) and 16 extend requests (a document plus 1024 new
+        tokens); admitting their 16 + 16 x 1024 fresh slots into the full
+        pool evicts least-recently-used cold conversations.
+    The free list is a seeded random permutation of the pool's slots.
     """
     rng = np.random.default_rng(seed)
     sys_tok = _tokens(rng, system, 1_000_000)
     hist_tok = [_tokens(rng, history + 1, 10_000_000 + 100_000 * b) for b in range(n_dec)]
     epre_tok = [_tokens(rng, ext_prefix, 100_000_000 + 10_000 * b) for b in range(n_ext)]
     enew_tok = [_tokens(rng, ext_new, 200_000_000 + 10_000 * b) for b in range(n_ext)]
-    src = _SlotSource(rng, num_slots)
-    sys_slots = src.take(system)
-    hist_slots = [src.take(history) for _ in range(n_dec)]
-    epre_slots = [src.take(ext_prefix) for _ in range(n_ext)]
-    dec_new = src.take(n_dec)
-    ext_new_slots = [src.take(ext_new) for _ in range(n_ext)]
-    rows, dec, ext = [], [], []
-    for b in range(n_dec):
-        rows.append((np.concatenate([sys_tok, hist_tok[b]]),
-                     np.concatenate([sys_slots, hist_slots[b], dec_new[b:b + 1]])))
-        dec.append((b, system + history + 1))
-    for b in range(n_ext):
-        rows.append((np.concatenate([epre_tok[b], enew_tok[b]]),
-                     np.concatenate([epre_slots[b], ext_new_slots[b]])))
-        ext.append((n_dec + b, ext_prefix, ext_new))
-    cached = np.concatenate([sys_slots] + hist_slots + epre_slots)
-    new = np.concatenate([dec_new] + ext_new_slots)
-    return _finish("mixed_chat", seed, rng, hq, hkv, d, num_slots, rows, cached, new, ext, dec,
-                   draw_values)
+    free_order = rng.permutation(num_slots).astype(np.int32)
+    warm = [np.concatenate([sys_tok, hist_tok[b][:history]]) for b in range(n_dec)] + list(epre_tok)
+    warm_slots = system + n_dec * history + n_ext * ext_prefix
+    batch_new = n_dec + n_ext * ext_new
+    if warm_slots + batch_new > num_slots:
+        raise ValueError("the batch does not fit the pool")
+    cold_after = num_slots - warm_slots - cold_before if fill else 0
+    if fill and (cold_before < batch_new or cold_after < 0):
+        raise ValueError("cold_before must cover the batch's fresh slots and fit the pool")
+    before = _cold_families(rng, cold_before, 3_000_000_000, exact=True) if cold_before else []
+    after = _cold_families(rng, cold_after, 5_000_000_000, exact=True) if cold_after else []
+    batch = [np.concatenate([sys_tok, hist_tok[b]]) for b in range(n_dec)] + \
+            [np.concatenate([epre_tok[b], enew_tok[b]]) for b in range(n_ext)]
+    notes = {"warm_tokens": warm_slots, "cold_before": cold_before, "cold_after": cold_after,
+             "batch_fresh_slots": batch_new, "cold_sequences": len(before) + len(after)}
+    return Scenario(name="mixed_chat", seed=seed, hq=hq, hkv=hkv, d=d, num_slots=num_slots,
+                    free_order=free_order, prefill=before + warm + after, batch=batch, n_dec=n_dec,
+                    notes=notes)
+
+
+def problem_from_admission(scn: Scenario, rows: List[np.ndarray], prefix_lens: List[int],
+                           draw_values: bool = True) -> Problem:
+    """The Problem of a scenario's batch, given the slot list and cached
+    prefix length each batch request was admitted with.  Values are drawn
+    from a generator seeded by (seed, 1): cached K/V for the distinct cached
+    slots in order of first appearance, new K/V for the fresh slots in batch
+    order, then the extend queries and the decode queries."""
+    if len(rows) != len(scn.batch) or len(prefix_lens) != len(scn.batch):
+        raise ValueError("one admitted row and prefix length per batch request")
+    seen, cached, new, ext, dec, out_rows = set(), [], [], [], [], []
+    for i, (toks, row, k) in enumerate(zip(scn.batch, rows, prefix_lens)):
+        row = np.asarray(row, np.int32)
+        k = int(k)
+        if len(row) != len(toks) or not 0 <= k <= len(toks):
+            raise ValueError(f"batch request {i}: bad admitted row")
+        for s in row[:k].tolist():
+            if s not in seen:
+                seen.add(s)
+                cached.append(s)
+        new.append(row[k:])
+        out_rows.append((toks, row))
+        if i < scn.n_dec:
+            if len(toks) - k != 1:
+                raise ValueError(f"decode request {i}: {len(toks) - k} uncached tokens, expected 1")
+            dec.append((i, len(toks)))
+        else:
+            ext.append((i, k, len(toks) - k))
+    rng = np.random.default_rng([scn.seed, 1])
+    return _finish(scn.name, scn.seed, rng, scn.hq, scn.hkv, scn.d, scn.num_slots, out_rows,
+                   np.array(cached, np.int32), np.concatenate(new).astype(np.int32), ext, dec, draw_values)
 
 
 def ragged(seed: int, hq: int, hkv: int, d: int, n_groups: int, per_group: int, shared_max: int,
@@ -392,7 +496,6 @@ FULL_SIZE = {
     "few_shot_decode": few_shot_decode,
     "cached_prefix_extend": cached_prefix_extend,
     "tree_of_thought_decode": tree_of_thought_decode,
-    "mixed_chat": mixed_chat,
 }
 
 

@@ -26,36 +26,16 @@ from typing import List, Sequence
 
 import numpy as np
 
-from oracle.tree_ref import SCHED_FCFS, SCHED_LPM, RadixTreeRef, optimal_hit_rate, schedule
+from oracle.tree_ref import SCHED_FCFS, SCHED_LPM, Admission, optimal_hit_rate, schedule
 
 
-class OracleAdmission:
-    """rx_admit / rx_commit composed from the oracle trie and a FIFO list."""
+class OracleAdmission(Admission):
+    """rx_admit / rx_commit composed from the oracle trie and a FIFO free
+    list (``oracle.tree_ref.Admission``); ``t`` is its trie."""
 
-    def __init__(self, free):
-        self.t = RadixTreeRef()
-        self.free = list(free)
-
-    def admit(self, toks):
-        k, slots = self.t.match_prefix(toks)
-        self.t.lock(toks[:k], 1)
-        need = len(toks) - k
-        ev = 0
-        if len(self.free) < need:
-            got = self.t.evict(need - len(self.free))
-            ev = len(got)
-            self.free.extend(got)
-        if len(self.free) < need:
-            self.t.lock(toks[:k], -1)
-            return None, k, ev
-        new, self.free = self.free[:need], self.free[need:]
-        return list(slots) + new, k, ev
-
-    def commit(self, toks, row, k):
-        self.t.lock(toks[:k], -1)
-        c = self.t.insert(toks, row)
-        if c > k:
-            self.free.extend(row[k:c])
+    @property
+    def t(self):
+        return self.tree
 
 
 class _Native:

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
-from prefix_shared_kv_radixattention_gb300 import inputs
+from prefix_shared_kv_radixattention_gb300 import admission, inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -89,9 +89,11 @@ def test_extend_full_size_cached_prefix(staged):
 
 
 def test_mixed_chat_full_size():
-    """Long-context decode (32k, 8k shared) and extend rows of one batch."""
+    """Long-context decode (32k, 8k shared) and extend rows of one batch,
+    with the slot lists the radix cache handed out when the batch was
+    admitted into the full 1M-slot pool (LRU eviction included)."""
     g = _gpu()
-    prob = inputs.mixed_chat()
+    prob = admission.mixed_chat()
     dev = g.Dev(prob)
     dev.kv_store()
     o_e, lse_e = dev.extend(staged=True)

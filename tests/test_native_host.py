@@ -17,6 +17,7 @@ import numpy as np
 import pytest
 
 from oracle.tree_ref import RadixTreeRef
+from prefix_shared_kv_radixattention_gb300 import admission
 from prefix_shared_kv_radixattention_gb300 import binding as rx
 from prefix_shared_kv_radixattention_gb300 import inputs
 from tests import _walkthrough
@@ -362,7 +363,7 @@ def test_plan_structure_tree_of_thought():
 
 
 def test_plan_structure_mixed_chat():
-    prob = inputs.mixed_chat(draw_values=False)
+    prob = admission.mixed_chat(draw_values=False)
     order, nparts, items, info = _plan(prob)
     check_plan(prob, order, nparts, items, info, auto=True)
     assert info.n_segments == 1 and info.shared_tokens == 8192
