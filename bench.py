@@ -8,23 +8,31 @@ KV store of the step's new tokens, then the attention the workload needs
 before timing starts; between timed steps a 256 MiB buffer is written, so that
 no KV survives in L2 (129 MB), and a second 256 MiB buffer is read, so that the
 lines the write left dirty are written back before the step rather than
-inside it; each step is timed with CUDA events on the launching stream.  The decode plan is built once, before timing, from the
-host copy of req_to_token (the sharing structure is fixed for the batch).
+inside it; each step is timed with CUDA events on the launching stream.  The
+decode plan is built once per batch, before timing, from the host copy of
+req_to_token (its time is reported); it stays valid for the batch's later
+decode steps, since each request's last piece follows its length on the
+device.
 
-Workloads (default: few_shot_decode, the configuration the headline metric
-is quoted on):
+Workloads (default: mixed_chat, the largest configuration that fits one GPU):
+  mixed_chat              16 decode x 32k + 16 extend x (4096 + 1024), 64/8,
+                          admitted through the radix cache into a full
+                          1M-slot pool (LRU eviction of cold conversations)
   few_shot_decode         64 x (1024 shared + 256 private + 1), MHA 32x128, 2M slots
   tree_of_thought_decode  256 leaves of a depth-4 fanout-4 tree, GQA 32/8
   cached_prefix_extend    32 x (2048 cached + 512 new), GQA 32/8
-  mixed_chat              16 decode x 32k + 16 extend x (4096 + 1024), 64/8
   tiny_extend             4 x (64 cached + 16 new), 4 heads, head_dim 64
   constrained_decode      one compressed-FSM decoding step (masked argmax and
                           jump) for 256 requests over a 128,256-id vocabulary
                           under a JSON-object constraint
 
-One JSON line is printed by rank 0.  Under torchrun every rank runs the same
-workload on its own GPU (independent replicas, no collective on the data
-path); value = work of all ranks / the slowest rank's time.
+One JSON line is printed by rank 0: "roofline" describes the step's dominant
+part (the longer of extend and decode), "rooflines" every part.  "e2e" runs
+the same step through the public API one synchronized step at a time, with
+the step's inputs copied in from pinned host memory and its outputs copied
+back.  Under torchrun every rank runs the same workload on its own GPU
+(independent replicas, no collective on the data path); value = work of all
+ranks / the slowest rank's time.
 
 --impl reference times the fp64 oracle (the plain CPU definition) on the host
 cores, on a bounded sample of the same workload, in the same units.
@@ -172,7 +180,9 @@ class GpuStep:
             self.o_dec = torch.empty_like(self.q_dec)
             self.dec_req, self.dec_len = i32(p.dec_req_idx), i32(p.dec_seq_len)
             self.max_len = int(p.dec_seq_len.max())
+            t0 = time.perf_counter()
             buf, info = rx.rx_decode_plan_build(p.req_to_token, p.dec_req_idx, p.dec_seq_len, p.hq, p.hkv)
+            self.plan_build_ms = (time.perf_counter() - t0) * 1e3
             self.plan_info = info
             self.plan = rx.plan_to_device(buf, info, B)
             ws = rx.rx_attn_decode_workspace(B, p.hq, p.hkv, p.d, self.max_len, self.plan)
@@ -353,51 +363,54 @@ def run_gpu(args, rank, world, local_rank):
     B_dec = len(prob.dec_req_idx)
     flops_ext = prob.extend_flops()
     kv_row = prob.kv_row_bytes
-    out = {}
+    out, roofs = {}, {}
+    ms_of = {k: statistics.mean(v) for k, v in part_ms.items()}
     if st.has_dec:
-        value = job_throughput(B_dec, world, args.steps, tot_ms)
-        metric, unit = "decode tok/s", "tok/s"
-        dec_ms = statistics.mean(part_ms["decode"])
+        dec_ms = ms_of["decode"]
         uniq_bytes = st.plan_info.tokens_read * kv_row
         achieved = uniq_bytes / (dec_ms / 1e3) / 1e9
         traffic, tsrc = profiled_traffic(args.workload, "decode")
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": traffic, "traffic_source": tsrc,
-                "kernel": "rx_attn_decode (" + " + ".join(st.decode_kernels) + ")",
-                "algorithmic_bytes_per_launch": int(uniq_bytes), "launch_ms": round(dec_ms, 5),
-                "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)",
-                "frac_of_8000": round(achieved / 8000.0, 4)}
+        roofs["decode"] = {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": traffic, "traffic_source": tsrc,
+            "kernel": "rx_attn_decode (" + " + ".join(st.decode_kernels) + ")",
+            "algorithmic_bytes_per_launch": int(uniq_bytes), "launch_ms": round(dec_ms, 5),
+            "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)", "frac_of_8000": round(achieved / 8000.0, 4)}
         out["decode"] = {"tok_s": B_dec / (dec_ms / 1e3), "hbm_gbs_unique": achieved,
                          "unique_kv_bytes": int(uniq_bytes),
                          "dense_kv_bytes": int(prob.decode_dense_tokens() * kv_row),
                          "ms": dec_ms, "segments": st.plan_info.n_segments,
-                         "work_items": st.plan_info.n_items, "kv_chunk": st.plan_info.kv_chunk}
+                         "work_items": st.plan_info.n_items, "kv_chunk": st.plan_info.kv_chunk,
+                         "plan_build_ms_once_per_batch": round(st.plan_build_ms, 3)}
     if st.has_ext:
-        ext_ms = statistics.mean(part_ms["extend"])
+        ext_ms = ms_of["extend"]
         tf = flops_ext / (ext_ms / 1e3) / 1e12
+        traffic, tsrc = profiled_traffic(args.workload, args.extend_path)
+        roofs["extend"] = {
+            "bound": "tensor", "achieved": round(tf, 2), "peak": tflops, "unit": "TFLOP/s",
+            "frac": round(tf / tflops, 4), "traffic": traffic, "traffic_source": tsrc,
+            "kernel": "rx_attn_extend (" + ("offsets + staging copy + extend_kernel"
+                                            if args.extend_path == "staged" else "extend_kernel") + ")",
+            "algorithmic_flops_per_launch": int(flops_ext), "launch_ms": round(ext_ms, 5),
+            "peak_source": f"{peak_src} bf16_tflops (burst)",
+            "frac_of_sustained": round(tf / tflops_sus, 4) if tflops_sus else None}
         out["extend"] = {"tflops": tf, "ms": ext_ms, "tok_s": float(np.sum(prob.ext_extend_len)) / (ext_ms / 1e3),
                          "flops": int(flops_ext), "frac_of_burst": tf / tflops}
-        if not st.has_dec:
-            metric, unit = "extend TFLOPS", "TFLOP/s"
-            value = job_throughput(flops_ext, world, args.steps, tot_ms) / 1e12
-            traffic, tsrc = profiled_traffic(args.workload, args.extend_path)
-            roof = {"bound": "tensor", "achieved": round(tf, 2), "peak": tflops, "unit": "TFLOP/s",
-                    "frac": round(tf / tflops, 4), "traffic": traffic, "traffic_source": tsrc,
-                    "kernel": "rx_attn_extend (" + ("offsets + staging copy + extend_kernel"
-                                                    if args.extend_path == "staged" else "extend_kernel") + ")",
-                    "algorithmic_flops_per_launch": int(flops_ext), "launch_ms": round(ext_ms, 5),
-                    "peak_source": f"{peak_src} bf16_tflops (burst)"}
-    out["kv_store"] = {"ms": statistics.mean(part_ms["store"]),
-                       "gbs": 2 * len(prob.new_slots) * kv_row / (statistics.mean(part_ms["store"]) / 1e3) / 1e9}
+    metric, unit, per_step = step_metric(prob)
+    value = job_throughput(per_step, world, args.steps, tot_ms)
+    # the dominant part of the step (the longer of extend and decode) is the
+    # kernel the line's roofline describes; both are in "rooflines"
+    dominant = max(roofs, key=lambda k: roofs[k]["launch_ms"])
+    out["kv_store"] = {"ms": ms_of["store"], "gbs": 2 * len(prob.new_slots) * kv_row / (ms_of["store"] / 1e3) / 1e9}
     if st.kv_fp8:
-        f8 = statistics.mean(part_ms["store_fp8"])
+        f8 = ms_of["store_fp8"]
         n_vals = len(prob.new_slots) * prob.hkv * prob.d
         out["kv_store_fp8"] = {"ms": f8, "gbs": 2 * n_vals * (2 + 1) / (f8 / 1e3) / 1e9}
     if st.rope_base:
         # K rotated inside the store (above); q rows rotated in place: read and
         # write of every q row
         q_bytes = 2 * (prob.q_ext.size + prob.q_dec.size) * 2
-        rq = statistics.mean(part_ms["rope_q"])
+        rq = ms_of["rope_q"]
         out["kv_store"]["rope_base"] = st.rope_base
         out["rope_q"] = {"ms": rq, "gbs": q_bytes / (rq / 1e3) / 1e9}
     line = {
@@ -407,7 +420,8 @@ def run_gpu(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random slot permutation)",
         "config": workload_config(prob, args.workload, world, args.extend_path, getattr(args, "graph", False),
                                   getattr(args, "rope", 0.0)),
-        "roofline": roof, "e2e": e2e, "gpu_launches": st.launches * args.steps,
+        "roofline": dict(roofs[dominant], part=dominant), "rooflines": roofs, "e2e": e2e,
+        "gpu_launches": st.launches * args.steps,
         "clocks": clk.summary(), "parts": out, "wall_s_timed_loop": round(t_wall, 3),
     }
     if st.kv_fp8:
@@ -415,6 +429,18 @@ def run_gpu(args, rank, world, local_rank):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(prob, args.workload, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
+
+
+def step_metric(prob):
+    """(metric, unit, units per step) of a workload's step: decode tokens
+    for decode batches, TFLOP for extend batches, and for a mixed batch the
+    tokens it carries (one per decode request plus every extend token)."""
+    n_dec, n_ext = len(prob.dec_req_idx), int(np.sum(prob.ext_extend_len))
+    if n_dec and n_ext:
+        return "tok/s (decode + extend tokens of the mixed step)", "tok/s", float(n_dec + n_ext)
+    if n_dec:
+        return "decode tok/s", "tok/s", float(n_dec)
+    return "extend TFLOPS", "TFLOP/s", prob.extend_flops() / 1e12
 
 
 def max_over_ranks(value: float, dist=None, device="cpu") -> float:
@@ -452,10 +478,16 @@ def job_throughput(units_per_rank_step: float, world: int, steps: int, max_ms: f
 
 
 def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
-    """Per step: pinned host -> device copies of the step's inputs, the path,
-    device -> host copy of its outputs; timed with events on the stream."""
+    """The step as a caller runs it through the public API, one step at a
+    time: the step's inputs copied in from pinned host memory (new K/V rows
+    and their slots, the queries, the decode lengths), the path, its outputs
+    copied back, and a synchronize -- a serving loop reads every step's
+    output before it can form the next step.  Host wall time per step, L2
+    flushed (untimed) before each one.  The decode plan is not rebuilt per
+    step: it was built once for the batch (its time is reported beside),
+    and each request's last piece follows its length on the device, so the
+    same plan serves the batch's later decode steps."""
     p = st.prob
-    s = torch.cuda.current_stream()
     h_in = [st.k_new.cpu().pin_memory(), st.v_new.cpu().pin_memory(), st.slots.cpu().pin_memory()]
     d_in = [st.k_new, st.v_new, st.slots]
     outs = []
@@ -464,42 +496,46 @@ def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
         d_in.append(st.q_ext)
         outs.append(st.o_ext)
     if st.has_dec:
-        h_in.append(st.q_dec.cpu().pin_memory())
-        d_in.append(st.q_dec)
+        h_in += [st.q_dec.cpu().pin_memory(), st.dec_len.cpu().pin_memory()]
+        d_in += [st.q_dec, st.dec_len]
         outs.append(st.o_dec)
     h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
     n = max(3, min(steps, 200))
-    E = torch.cuda.Event
-    ev = [(E(enable_timing=True), E(enable_timing=True)) for _ in range(n)]
+    secs = []
     for i in range(n):
         flush()
-        ev[i][0].record()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
         for h, d in zip(h_in, d_in):
             d.copy_(h, non_blocking=True)
         st.step()
         for h, d in zip(h_out, outs):
             h.copy_(d, non_blocking=True)
-        ev[i][1].record()
-    torch.cuda.synchronize()
-    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / n, dist, "cuda")
+        torch.cuda.synchronize()
+        secs.append(time.perf_counter() - t0)
+    ms = max_over_ranks(sum(secs) / n * 1e3, dist, "cuda")
     h2d = sum(h.numel() * h.element_size() for h in h_in)
     d2h = sum(h.numel() * h.element_size() for h in h_out)
+    _, unit, per_step = step_metric(p)
+    out = {"value": round(job_throughput(per_step, world, 1, ms), 3), "unit": unit,
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 5),
+           "steps": n, "timing": "host wall clock per step, synchronized every step"}
     if st.has_dec:
-        val, unit = job_throughput(len(p.dec_req_idx), world, 1, ms), "tok/s"
-    else:
-        val, unit = job_throughput(p.extend_flops(), world, 1, ms) / 1e12, "TFLOP/s"
-    return {"value": round(val, 3), "unit": unit, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 5), "steps": n}
+        out["decode_plan"] = {"built": "once per batch, reused by every later decode step",
+                              "build_ms": round(st.plan_build_ms, 3)}
+    return out
 
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
-# captures summarised in the named profile; an entry is removed whenever its
-# kernel changes, so that an old count is never reported for new code.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# a part's main kernel, from one ncu capture of that kernel alone; each entry
+# says which capture.  An entry is removed whenever its kernel changes, so
+# that an old count is never reported for new code.
 PROFILED_TRAFFIC = {
-    ("few_shot_decode", "decode"): (298_800_000, "profiles/decode_kernel.few_shot_decode.md"),
-    ("tree_of_thought_decode", "decode"): (401_500_000, "profiles/decode_gqa_kernel.tree_of_thought_decode.md"),
-    ("cached_prefix_extend", "staged"): (585_800_000, "profiles/extend_kernel.cached_prefix_extend.md"),
-    ("constrained_decode", "fsm"): (132_300_000, "profiles/fsm_scan_kernel.constrained_decode.md"),
+    ("cached_prefix_extend", "staged"): (
+        585_800_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend (1M-slot pool): "
+                     "extend_kernel alone, without the staging copy"),
+    ("constrained_decode", "fsm"): (
+        132_300_000, "ncu launch list of constrained_decode: fsm_scan_kernel + fsm_finish_kernel"),
 }
 
 
@@ -559,73 +595,160 @@ def workload_config(prob, name, world, extend_path="staged", graph=False, rope=0
 
 
 def _oracle_pools(prob):
+    """Compact host pools for the oracle: the cached rows in the order they
+    were drawn, then the step's new rows placed by the oracle's own
+    kv_store, and req_to_token renamed to those rows (pool rows renamed
+    consistently give the same attention)."""
     import oracle
-    slots = np.concatenate([prob.cached_slots, prob.new_slots])
-    uniq = np.unique(slots)
-    kp = np.zeros((len(uniq), prob.hkv, prob.d), np.uint16)
+    S = prob.num_slots
+    row_of = np.full(S, -1, np.int64)
+    nc = len(prob.cached_slots)
+    row_of[prob.cached_slots] = np.arange(nc)
+    fresh = prob.new_slots[row_of[prob.new_slots] < 0]
+    row_of[fresh] = nc + np.arange(len(fresh))
+    kp = np.zeros((nc + len(fresh), prob.hkv, prob.d), np.uint16)
     vp = np.zeros_like(kp)
-    pos = np.searchsorted(uniq, prob.cached_slots)
-    kp[pos], vp[pos] = prob.cached_k, prob.cached_v
-    oracle.kv_store(kp, vp, prob.new_k, prob.new_v, np.searchsorted(uniq, prob.new_slots).astype(np.int32))
+    kp[:nc], vp[:nc] = prob.cached_k, prob.cached_v
+    oracle.kv_store(kp, vp, prob.new_k, prob.new_v, row_of[prob.new_slots].astype(np.int32))
     rtt = prob.req_to_token
-    loc = np.minimum(np.searchsorted(uniq, np.maximum(rtt, 0)), len(uniq) - 1)
-    rtt_c = np.where((rtt >= 0) & (uniq[loc] == rtt), loc, -1).astype(np.int32)
+    ok = (rtt >= 0) & (rtt < S)
+    rtt_c = np.where(ok, row_of[np.where(ok, rtt, 0)], -1).astype(np.int32)
     return kp, vp, rtt_c
 
 
-def oracle_sample(prob, pools, rows_dec, rows_ext_tokens, threads):
-    """One bounded oracle pass: the first rows_dec decode rows and the last
-    rows_ext_tokens extend tokens of each extend request.  Returns
-    (seconds, decode rows done, extend flops done)."""
-    import oracle
+def head_pools(prob, pools):
+    """The oracle's pools cut to kv head 0 (each kv head's attention costs
+    the same, so the sample runs one and the rate counts the others)."""
     kp, vp, rtt = pools
-    flops = 0
-    nd = 0
-    t0 = time.perf_counter()
+    return np.ascontiguousarray(kp[:, :1]), np.ascontiguousarray(vp[:, :1]), rtt
+
+
+def oracle_sample(prob, hp, rows_dec, ext_tokens, threads):
+    """One bounded oracle pass on kv head 0 (its G q heads): the first
+    rows_dec decode rows, and ext_tokens extend tokens of each extend
+    request, evenly spaced over its new tokens (its last token included).
+    Returns (decode seconds, rows, extend seconds, tokens, extend flops)."""
+    import oracle
+    kp, vp, rtt = hp
+    G = prob.hq // prob.hkv
+    sd = se = 0.0
+    nd = ne = flops = 0
     if len(prob.dec_req_idx) and rows_dec:
         nd = min(rows_dec, len(prob.dec_req_idx))
-        oracle.decode(prob.q_dec[:nd], kp, vp, rtt, prob.dec_req_idx[:nd], prob.dec_seq_len[:nd],
-                      prob.sm_scale, n_threads=threads)
-    if len(prob.ext_req_idx) and rows_ext_tokens:
+        q = np.ascontiguousarray(prob.q_dec[:nd, :G])
+        t0 = time.perf_counter()
+        oracle.decode(q, kp, vp, rtt, prob.dec_req_idx[:nd], prob.dec_seq_len[:nd], prob.sm_scale,
+                      n_threads=threads)
+        sd = time.perf_counter() - t0
+    if len(prob.ext_req_idx) and ext_tokens:
         q_rows, kend, qi = [], [], []
         for b in range(len(prob.ext_req_idx)):
             E, P = int(prob.ext_extend_len[b]), int(prob.ext_prefix_len[b])
-            for i in range(max(0, E - rows_ext_tokens), E):
+            k = min(E, ext_tokens)
+            for i in sorted({E - 1 - (j * E) // k for j in range(k)}):
                 qi.append(int(prob.qo_indptr[b]) + i)
                 q_rows.append(int(prob.ext_req_idx[b]))
                 kend.append(P + i + 1)
         kend = np.array(kend, np.int32)
-        oracle.attention(prob.q_ext[qi], kp, vp, rtt, np.array(q_rows, np.int32), np.zeros_like(kend),
-                         kend, prob.sm_scale, n_threads=threads)
-        flops = int(4 * prob.d * prob.hq * kend.astype(np.int64).sum())
-    return time.perf_counter() - t0, nd, flops
+        q = np.ascontiguousarray(prob.q_ext[qi][:, :G])
+        t0 = time.perf_counter()
+        oracle.attention(q, kp, vp, rtt, np.array(q_rows, np.int32), np.zeros_like(kend), kend, prob.sm_scale,
+                         n_threads=threads)
+        se = time.perf_counter() - t0
+        ne = len(kend)
+        flops = int(4 * prob.d * G * kend.astype(np.int64).sum())
+    return sd, nd, se, ne, flops
+
+
+def _sample_shape(prob, frac, threads=1):
+    """(decode rows, extend tokens per request) for a fraction of the step;
+    at least one decode row per thread (the oracle spreads rows, not a
+    row's keys, over its threads)."""
+    nd = len(prob.dec_req_idx)
+    emax = int(prob.ext_extend_len.max()) if len(prob.ext_req_idx) else 0
+    rows = min(nd, max(threads, int(np.ceil(nd * frac)))) if nd else 0
+    toks = min(emax, max(1, int(np.ceil(emax * frac)))) if emax else 0
+    return rows, toks
+
+
+class OracleRate:
+    """Accumulates oracle samples; the rate is the step's own mix of decode
+    rows and extend tokens (or its flops), at the measured time per decode
+    row and per extend token, over all kv heads."""
+
+    def __init__(self, prob):
+        self.prob = prob
+        self.sd = self.se = 0.0
+        self.nd = self.ne = self.flops = 0
+
+    def add(self, sample):
+        sd, nd, se, ne, fl = sample
+        self.sd, self.nd, self.se, self.ne, self.flops = (self.sd + sd, self.nd + nd, self.se + se,
+                                                          self.ne + ne, self.flops + fl)
+
+    def seconds(self):
+        return self.sd + self.se
+
+    def value(self):
+        p = self.prob
+        _, unit, per_step = step_metric(p)
+        if unit == "TFLOP/s":
+            return self.flops / self.se / 1e12          # head 0's flops over head 0's time
+        t_row = self.sd / self.nd * p.hkv if self.nd else 0.0
+        t_tok = self.se / self.ne * p.hkv if self.ne else 0.0
+        n_dec, n_ext = len(p.dec_req_idx), int(np.sum(p.ext_extend_len))
+        return per_step / (n_dec * t_row + n_ext * t_tok)
+
+
+def _describe(prob, name, rows, toks):
+    parts = []
+    if rows:
+        parts.append(f"{rows} of {len(prob.dec_req_idx)} decode rows")
+    if toks:
+        parts.append(f"{toks} of each extend request's {int(prob.ext_extend_len.max())} new tokens "
+                     f"(evenly spaced, last included) over {len(prob.ext_req_idx)} requests")
+    return (" + ".join(parts) + f" of {name}, on kv head 0 of {prob.hkv} (fp64); the rate weighs "
+            "decode rows and extend tokens as the step does and counts every kv head")
+
+
+def calibrated_sample(prob, hp, threads, seconds):
+    """The fraction of a step whose oracle pass takes about `seconds`."""
+    frac = 1.0 / 1024
+    while True:
+        rows, toks = _sample_shape(prob, frac, threads)
+        sd, _, se, _, _ = oracle_sample(prob, hp, rows, toks, threads)
+        sec = sd + se
+        if sec >= seconds / 8 or frac >= 1.0:
+            return min(1.0, frac * max(1.0, seconds / max(sec, 1e-4)))
+        frac = min(1.0, frac * 4)
+
+
+def cpu_rate(prob, name, hp, threads, budget_s):
+    """The oracle as it stands on `threads` host cores, repeated over a
+    bounded sample of the step until about budget_s seconds of CPU work."""
+    frac = calibrated_sample(prob, hp, threads, budget_s / 3)
+    rows, toks = _sample_shape(prob, frac, threads)
+    acc, reps = OracleRate(prob), 0
+    while acc.seconds() < budget_s and reps < 10000:
+        acc.add(oracle_sample(prob, hp, rows, toks, threads))
+        reps += 1
+    _, unit, _ = step_metric(prob)
+    return {"value": round(acc.value(), 6), "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": _describe(prob, name, rows, toks) + f"; repeated {reps} times",
+            "seconds": round(acc.seconds(), 3)}
+
+
+SINGLE_CORE_WORKLOADS = ("tiny_extend", "few_shot_decode", "tree_of_thought_decode")
 
 
 def cpu_baseline(prob, name, budget_s=15.0):
-    """The oracle as it stands, on all host cores, repeated over a bounded
-    sample until about budget_s seconds of CPU work are done."""
-    threads = cores()
-    pools = _oracle_pools(prob)
-    has_dec = len(prob.dec_req_idx) > 0
-    tot, work, reps = 0.0, 0, 0
-    if has_dec:
-        rows = len(prob.dec_req_idx)
-        sec, _, _ = oracle_sample(prob, pools, 1, 0, threads)
-        rows = int(max(1, min(rows, budget_s / max(sec, 1e-4))))
-        while tot < budget_s and reps < 10000:
-            sec, nd, _ = oracle_sample(prob, pools, rows, 0, threads)
-            tot, work, reps = tot + sec, work + nd, reps + 1
-        return {"value": round(work / tot, 3), "unit": "tok/s", "cores": threads, "kind": "oracle",
-                "sample": f"{rows} of {len(prob.dec_req_idx)} decode rows of {name} (all heads, fp64), "
-                          f"repeated {reps} times", "seconds": round(tot, 3)}
-    sec, _, _ = oracle_sample(prob, pools, 0, 1, threads)
-    toks = int(max(1, min(int(prob.ext_extend_len.min()), budget_s / max(sec, 1e-4))))
-    while tot < budget_s and reps < 10000:
-        sec, _, fl = oracle_sample(prob, pools, 0, toks, threads)
-        tot, work, reps = tot + sec, work + fl, reps + 1
-    return {"value": round(work / tot / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"last {toks} extend tokens of each of {len(prob.ext_req_idx)} requests of {name} "
-                      f"(fp64), repeated {reps} times", "seconds": round(tot, 3)}
+    """The oracle on all host cores; for the small and decode configurations
+    also on one core."""
+    hp = head_pools(prob, _oracle_pools(prob))
+    out = cpu_rate(prob, name, hp, cores(), budget_s)
+    if name in SINGLE_CORE_WORKLOADS:
+        out["single_core"] = cpu_rate(prob, name, hp, 1, budget_s / 2)
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -809,38 +932,28 @@ def run_reference(args, rank, world):
         return
     prob = make_problem(args, admit_with="oracle")
     threads = cores()
-    pools = _oracle_pools(prob)
-    has_dec = len(prob.dec_req_idx) > 0
-    # a step = a bounded sample of the workload, sized to a few seconds
-    sec1, _, _ = oracle_sample(prob, pools, 1 if has_dec else 0, 0 if has_dec else 1, threads)
-    budget = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
-    n = int(max(1, budget / max(sec1, 1e-4)))
-    secs, work = [], []
+    hp = head_pools(prob, _oracle_pools(prob))
+    # a step = a bounded sample of the workload, sized so that the whole run
+    # takes about --cpu-seconds
+    budget = max(0.05, args.cpu_seconds / max(1, args.steps + args.warmup))
+    frac = calibrated_sample(prob, hp, threads, budget)
+    rows, toks = _sample_shape(prob, frac, threads)
+    acc = OracleRate(prob)
     for i in range(args.warmup + args.steps):
-        if has_dec:
-            s, nd, _ = oracle_sample(prob, pools, min(n, len(prob.dec_req_idx)), 0, threads)
-            w = nd
-        else:
-            s, _, fl = oracle_sample(prob, pools, 0, min(n, int(prob.ext_extend_len.min())), threads)
-            w = fl
+        sample = oracle_sample(prob, hp, rows, toks, threads)
         if i >= args.warmup:
-            secs.append(s)
-            work.append(w)
-    tot = sum(secs)
-    if has_dec:
-        value, unit, metric = sum(work) / tot, "tok/s", "decode tok/s"
-        sample = f"{work[0]} of {len(prob.dec_req_idx)} decode rows per step, all heads, fp64"
-    else:
-        value, unit, metric = sum(work) / tot / 1e12, "TFLOP/s", "extend TFLOPS"
-        sample = f"last {min(n, int(prob.ext_extend_len.min()))} extend tokens per request per step, fp64"
+            acc.add(sample)
+    metric, unit, _ = step_metric(prob)
+    value = acc.value()
     line = {"impl": "reference", "metric": f"prefix-shared attn: {metric}", "value": round(value, 6),
             "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16, random slot permutation)",
+            "ms_per_step": round(acc.seconds() / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16, random slot permutation)",
             "config": workload_config(prob, args.workload, world, args.extend_path, getattr(args, "graph", False),
-                                  getattr(args, "rope", 0.0)),
+                                      getattr(args, "rope", 0.0)),
             "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
-                             "sample": sample},
+                             "sample": _describe(prob, args.workload, rows, toks) + "; one sample per step"},
             "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -848,9 +961,9 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="few_shot_decode", choices=WORKLOADS + [FSM_WORKLOAD])
+    ap.add_argument("--workload", default="mixed_chat", choices=WORKLOADS + [FSM_WORKLOAD])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -350,12 +350,30 @@ size_t rx_attn_extend_workspace(int64_t total_ctx_tokens, int32_t batch, int32_t
                                 int32_t head_dim);
 
 /* ---- decode -------------------------------------------------------------
+ * Source: "SGLang: Efficient Execution of Structured Language Model
+ * Programs" (unite.ai, es), "Introducción a SGLang", RadixAttention bullet:
+ * later calls reuse the KV cache of the prefixes they share.  Reading a
+ * shared prefix's KV from HBM once for all the requests below it, by way of
+ * a plan that groups those requests, is this library's design, not the
+ * pages'.
+ *
  * Decode plan: which requests of the batch share which positions, so that a
  * shared segment's KV is read once for all of them.  Built on the host by
  * rx_decode_plan_build from the host copy of req_to_token; the caller copies
  * the packed buffer to the device and fills this struct with device pointers
  * into that copy (see rx_decode_plan_build for the layout).
+ *
+ * A plan outlives the step it was built for.  A request's last position is
+ * never part of a shared segment, so every request ends in a piece of its
+ * own, and that piece's pos_end is RX_PLAN_OPEN_END: the kernels end it at
+ * the request's seq_len when the plan is used.  The same plan therefore
+ * serves every later decode step of the batch -- each request one token
+ * longer, its earlier slot ids unchanged -- with no host work; rebuild it
+ * when the batch's requests change.  (Later steps reuse the split of the
+ * first: a request's last piece grows by one position per step.)
  */
+#define RX_PLAN_OPEN_END (-1)
+
 typedef struct {
     const int32_t *order;   /* device int32 [batch]: batch index of each plan row   */
     const int32_t *nparts;  /* device int32 [batch]: partial results per request    */
@@ -453,9 +471,15 @@ int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, float *lse_or
  * first call before any stream capture.  Every call shares the one array,
  * so calls that overlap on the GPU (different streams, or different host
  * threads without ordering) race; calls ordered on one stream are safe.
- * Nothing needs clearing: whatever a call reads from the array it has
- * written earlier in the same call.  Returns RX_ERR_CAPACITY when
- * rx_attn_decode_workspace(...) for the batch exceeds the array. */
+ * Nothing needs clearing by the caller: every partial result a call reads
+ * from the array it has written earlier in the same call, and the call
+ * zeroes the one counter it keeps there before its kernels start.  A device
+ * reset (cudaDeviceReset, or anything else that destroys the device's
+ * primary context) makes the kept address stale: do not call this entry
+ * point on that device afterwards.  The arguments are checked as
+ * rx_attn_decode checks them (RX_ERR_INVALID / RX_ERR_UNSUPPORTED), then
+ * RX_ERR_CAPACITY is returned when rx_attn_decode_workspace(...) for the
+ * batch exceeds the array. */
 #define RX_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
 int rx_attn_decode_static(const rx_kv_pool *pool, const void *q, void *o, float *lse,
                           int32_t num_q_heads, const int32_t *req_idx, const int32_t *seq_len,
@@ -543,6 +567,27 @@ typedef struct {
 int rx_fsm_step(const rx_fsm *fsm, const float *logits, int64_t logits_stride, int32_t batch,
                 int32_t *state, int32_t *out_tokens, int32_t *out_count, uint64_t *workspace,
                 int32_t *dev_status, void *stream);
+
+/* ---- failure paths, for tests -------------------------------------------
+ * Not from the pages.  Two switches that let a test drive the library's
+ * error paths without a failing allocator or a stuck GPU.
+ *
+ * rx_test_fail_alloc: the n-th next radix-tree node allocation (counting
+ * from 1, over every tree in the process) fails as a failing host allocator
+ * would; the call that needed it returns RX_ERR_NOMEM and leaves the tree
+ * and the free list exactly as they were.  n = 0 switches it off;
+ * RX_ERR_INVALID for n < 0.
+ *
+ * rx_decode_set_wait_limit: the bound, in SM clock cycles, on each pipeline
+ * wait of the decode kernels launched from then on (process-wide);
+ * cycles <= 0 restores the default of 2^31 cycles (about one second).  A
+ * wait that runs out ORs RX_DEV_TIMEOUT into the call's status word and
+ * stops its CTA: the other warps leave at their next wait, and the copies
+ * already in flight are waited for (with the default bound) before the CTA
+ * exits, so the context stays usable.  The outputs of that call are then
+ * incomplete. */
+int rx_test_fail_alloc(int64_t n);
+int rx_decode_set_wait_limit(int64_t cycles);
 
 #ifdef __cplusplus
 }

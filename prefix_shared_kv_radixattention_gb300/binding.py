@@ -40,6 +40,7 @@ RX_DEV_BAD_LEN = 2
 RX_DEV_TIMEOUT = 4
 RX_DEV_FSM_DONE = 8
 RX_DEV_BAD_STATE = 16
+RX_PLAN_OPEN_END = -1
 
 
 class RxError(RuntimeError):
@@ -137,6 +138,18 @@ _sig("rx_attn_decode", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I32, _
 _sig("rx_attn_decode_static", ctypes.c_int, ctypes.POINTER(KVPool), _P, _P, _P, _I32, _P, _P, _P, _I64,
      _I32, _I32, ctypes.POINTER(DecodePlan), ctypes.c_float, _P, _P)
 RX_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
+_sig("rx_test_fail_alloc", ctypes.c_int, _I64)
+_sig("rx_decode_set_wait_limit", ctypes.c_int, _I64)
+
+
+def rx_test_fail_alloc(n: int) -> None:
+    """The n-th next radix-tree node allocation fails (0: off); see rx.h."""
+    _check(_lib.rx_test_fail_alloc(int(n)))
+
+
+def rx_decode_set_wait_limit(cycles: int) -> None:
+    """Bound on each decode pipeline wait, in SM cycles (<= 0: the default)."""
+    _check(_lib.rx_decode_set_wait_limit(int(cycles)))
 
 
 def library():
@@ -458,13 +471,16 @@ def rx_decode_plan_build(req_to_token_host, req_idx_host, seq_len_host, num_q_he
     ri, rip = _np(req_idx_host, np.int32)
     sl, slp = _np(seq_len_host, np.int32)
     info = DecodePlanInfo()
+    # one call with room for the usual plan sizes; a second one only when the
+    # library reports that more words are needed
+    buf = np.empty(2 * len(ri) + 8 * max(8192, 64 * len(ri)), np.int32)
     rc = _lib.rx_decode_plan_build(rp, rtt.shape[1], rip, slp, len(ri), num_q_heads, num_kv_heads,
-                                   kv_chunk, min_shared, None, 0, ctypes.byref(info))
-    _check(rc, allow=(RX_ERR_CAPACITY,))
-    buf = np.empty(max(1, info.buf_words), np.int32)
-    _check(_lib.rx_decode_plan_build(rp, rtt.shape[1], rip, slp, len(ri), num_q_heads, num_kv_heads,
-                                     kv_chunk, min_shared, buf.ctypes.data_as(_P), len(buf),
-                                     ctypes.byref(info)))
+                                   kv_chunk, min_shared, buf.ctypes.data_as(_P), len(buf), ctypes.byref(info))
+    if rc == RX_ERR_CAPACITY:
+        buf = np.empty(max(1, info.buf_words), np.int32)
+        rc = _lib.rx_decode_plan_build(rp, rtt.shape[1], rip, slp, len(ri), num_q_heads, num_kv_heads,
+                                       kv_chunk, min_shared, buf.ctypes.data_as(_P), len(buf), ctypes.byref(info))
+    _check(rc)
     return buf[:info.buf_words], info
 
 

@@ -53,6 +53,8 @@
 
 #include <mutex>
 
+#include <atomic>
+
 #include "rx_common.cuh"
 
 namespace {
@@ -126,11 +128,25 @@ struct Params {
     int32_t *status;
     int wide0, n_wide;      // plan: single-request items for the wide kernel
     int *wide_counter;      // next wide item to hand out (zeroed before the launch)
+    long long wait_cycles;  // bound on each pipeline wait (rx_decode_set_wait_limit)
 };
 
 struct Item {
     int M, p0, p1, part, final_, g, rtt_row, qrow0, r0;
 };
+
+// End of a plan item whose pos_end is RX_PLAN_OPEN_END: the length of its
+// request (batch index b) now.  A length past the slot-list stride, or not
+// past the item's start, is an error: flagged (by `report` lanes), and the
+// item is read as its first position alone, so that nothing outside the
+// buffers is touched and no row is left without keys.
+__device__ __forceinline__ int open_end(const Params &p, int b, int p0, bool report)
+{
+    const int64_t L = __ldg(p.seq_len + b);
+    if (L > p0 && L <= p.rtt_stride) return (int)L;
+    if (report && p.status) atomicOr(p.status, RX_DEV_BAD_LEN);
+    return p0 + 1;
+}
 
 // Decodes work index w (one per lane); false when the item is empty.
 template <bool PLAN>
@@ -149,6 +165,7 @@ __device__ __forceinline__ bool get_item(const Params &p, int w, Item &it)
         it.final_ = __ldg(v + 5);
         it.rtt_row = __ldg(v + 6);
         it.qrow0 = __ldg(v + 7);
+        if (it.p1 == RX_PLAN_OPEN_END) it.p1 = open_end(p, it.qrow0, it.p0, it.g == 0);
         return it.M > 0 && it.p1 > it.p0;
     }
     const int b = i / p.n_chunks, c = i % p.n_chunks;
@@ -173,17 +190,22 @@ __device__ __forceinline__ bool get_item(const Params &p, int w, Item &it)
 // Bounded wait by a whole warp, with one answer for all its lanes (the warp
 // then runs warp-wide shuffles, ldmatrix and barriers).
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                              int32_t *status)
+                                              int32_t *status, long long limit)
 {
-    bool ok = false;
-    const long long t0 = clock64();
-    do {
-        if (rx::mbar_try_wait(bar, parity)) {
-            ok = true;
-            break;
+    // already complete: no suspend; otherwise blocking tries while the
+    // limit lasts (the clock is read before each try, since one try may
+    // itself suspend for longer than a small limit)
+    bool ok = rx::mbar_test_wait(bar, parity);
+    if (!ok) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < limit) {
+            if (rx::mbar_try_wait(bar, parity)) {
+                ok = true;
+                break;
+            }
+            if (*abort_flag) break;
         }
-        if (*abort_flag) break;
-    } while (clock64() - t0 < rx::kWaitCycles);
+    }
     if (!ok && !*abort_flag) {
         *abort_flag = 1;
         if (status) atomicOr(status, RX_DEV_TIMEOUT);
@@ -212,7 +234,7 @@ __device__ void scheduler(const Params &p, unsigned char *smem)
     bool alive = true;
     auto publish = [&](const Item &it, bool end) -> bool {
         const uint32_t di = n_it % kNIT;
-        if (!wait_or_abort(bar + 8 * (L::B_ITEMPTY + di), ((n_it / kNIT) & 1) ^ 1, abort_flag, p.status))
+        if (!wait_or_abort(bar + 8 * (L::B_ITEMPTY + di), ((n_it / kNIT) & 1) ^ 1, abort_flag, p.status, p.wait_cycles))
             return false;
         Desc *d = descs + di;
         if (lane == 0) {
@@ -260,7 +282,7 @@ __device__ void scheduler(const Params &p, unsigned char *smem)
             for (int t = 0; t < ntiles; ++t, ++n_tile) {
                 const uint32_t sb = n_tile % kNSL;
                 if (!wait_or_abort(bar + 8 * (L::B_SLEMPTY + sb), ((n_tile / kNSL) & 1) ^ 1, abort_flag,
-                                   p.status)) {
+                                   p.status, p.wait_cycles)) {
                     alive = false;
                     break;
                 }
@@ -299,13 +321,13 @@ __device__ void copier(const Params &p, unsigned char *smem)
     uint32_t n_it = 0, n_tile = 0, qi = 0;
     for (;; ++n_it) {
         const uint32_t di = n_it % kNIT;
-        if (!wait_or_abort(bar + 8 * (L::B_ITFULL + di), (n_it / kNIT) & 1, abort_flag, p.status)) break;
+        if (!wait_or_abort(bar + 8 * (L::B_ITFULL + di), (n_it / kNIT) & 1, abort_flag, p.status, p.wait_cycles)) break;
         const Desc *d = descs + di;
         const int M = d->M, p0 = d->p0, p1 = d->p1, g = d->g;
         if (M == 0) break;
         {  // query rows -> Q slot (rows past M zero-filled), by every copier thread
             const uint32_t qs = qi & 1;
-            if (!wait_or_abort(bar + 8 * (L::B_QEMPTY + qs), ((qi >> 1) & 1) ^ 1, abort_flag, p.status))
+            if (!wait_or_abort(bar + 8 * (L::B_QEMPTY + qs), ((qi >> 1) & 1) ^ 1, abort_flag, p.status, p.wait_cycles))
                 break;
             const int Mpad = mpad_of(M);
             bf16 *qd = Qs + qs * L::QSLOT;
@@ -329,9 +351,9 @@ __device__ void copier(const Params &p, unsigned char *smem)
         bool ok_all = true;
         for (int t = 0; t < ntiles; ++t, ++n_tile) {
             const uint32_t sb = n_tile % kNSL, s = n_tile % L::NST;
-            if (!wait_or_abort(bar + 8 * (L::B_SLFULL + sb), (n_tile / kNSL) & 1, abort_flag, p.status) ||
+            if (!wait_or_abort(bar + 8 * (L::B_SLFULL + sb), (n_tile / kNSL) & 1, abort_flag, p.status, p.wait_cycles) ||
                 !wait_or_abort(bar + 8 * (L::B_EMPTY + s), ((n_tile / L::NST) & 1) ^ 1, abort_flag,
-                               p.status)) {
+                               p.status, p.wait_cycles)) {
                 ok_all = false;
                 break;
             }
@@ -389,7 +411,7 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
 
     // Q fragments
     const uint32_t qs = qi & 1;
-    if (!wait_or_abort(bar + 8 * (L::B_QFULL + qs), (qi >> 1) & 1, abort_flag, p.status)) return false;
+    if (!wait_or_abort(bar + 8 * (L::B_QFULL + qs), (qi >> 1) & 1, abort_flag, p.status, p.wait_cycles)) return false;
     uint32_t qf[D / 16][4];
     {
         const bf16 *qb = Qs + qs * L::QSLOT;
@@ -414,7 +436,7 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
     const int ntiles = (p1 - p0 + kBN - 1) / kBN;
     for (int t = 0; t < ntiles; ++t, ++n_tile) {
         const uint32_t s = n_tile % L::NST;
-        if (!wait_or_abort(bar + 8 * (L::B_FULL + s), (n_tile / L::NST) & 1, abort_flag, p.status))
+        if (!wait_or_abort(bar + 8 * (L::B_FULL + s), (n_tile / L::NST) & 1, abort_flag, p.status, p.wait_cycles))
             return false;
         const bf16 *kt = Ks + s * L::TILE;
         const bf16 *vt = Vs + s * L::TILE;
@@ -547,7 +569,7 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
         // consumer-only barrier: one arrival per warp, bounded wait
         __syncwarp();
         if (lane == 0) rx::mbar_arrive(bar + 8 * L::B_RED);
-        if (!wait_or_abort(bar + 8 * L::B_RED, n_red & 1, abort_flag, p.status)) return false;
+        if (!wait_or_abort(bar + 8 * L::B_RED, n_red & 1, abort_flag, p.status, p.wait_cycles)) return false;
         ++n_red;
         const int ct = threadIdx.x - kConsumer0;
         for (int e = ct; e < Mpad * D; e += 32 * kConsumers) {
@@ -576,7 +598,7 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
         }
         __syncwarp();  // the next item may overwrite the buffer once every warp is here
         if (lane == 0) rx::mbar_arrive(bar + 8 * L::B_RED);
-        if (!wait_or_abort(bar + 8 * L::B_RED, n_red & 1, abort_flag, p.status)) return false;
+        if (!wait_or_abort(bar + 8 * L::B_RED, n_red & 1, abort_flag, p.status, p.wait_cycles)) return false;
         ++n_red;
     }
     return true;
@@ -628,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p)
     uint32_t n_it = 0, n_tile = 0, qi = 0, n_red = 0;
     for (;; ++n_it) {
         const uint32_t di = n_it % kNIT;
-        if (!wait_or_abort(bar + 8 * (L::B_ITFULL + di), (n_it / kNIT) & 1, abort_flag, p.status)) return;
+        if (!wait_or_abort(bar + 8 * (L::B_ITFULL + di), (n_it / kNIT) & 1, abort_flag, p.status, p.wait_cycles)) return;
         const Desc *d = descs + di;
         const int M = d->M;
         if (M == 0) return;
@@ -788,8 +810,9 @@ struct WideLayoutT {
     static constexpr int OFF_V = STAGES * STAGE_BYTES;
     static constexpr int OFF_OK = 2 * STAGES * STAGE_BYTES;               // int [stage][pos]: row valid
     static constexpr int OFF_SLOT = OFF_OK + STAGES * kWideMaxPos * 4;    // int [stage][pos]: slot id or -1
-    static constexpr int OFF_HDR = OFF_SLOT + STAGES * kWideMaxPos * 4;   // int2 [stage]: item, first position
-    static constexpr int OFF_Q = (OFF_HDR + STAGES * 8 + 127) / 128 * 128;  // NQ x the item's query rows
+    static constexpr int OFF_HDR = OFF_SLOT + STAGES * kWideMaxPos * 4;   // int4 [stage]: item, first
+                                                                          // position, item end, 0
+    static constexpr int OFF_Q = (OFF_HDR + STAGES * 16 + 127) / 128 * 128;  // NQ x the item's query rows
     static constexpr int QBYTES = QBYTES_;                                // bytes of one q slot
     static constexpr int OFF_BAR = OFF_Q + NQ * QBYTES;
     static constexpr int OFF_ABORT = OFF_BAR + (3 * STAGES + NQ) * 8;
@@ -888,6 +911,7 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
             const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + it);
             c.q0 = __ldg(v + 2);
             c.p1 = __ldg(v + 3);
+            if (c.p1 == RX_PLAN_OPEN_END) c.p1 = open_end(p, __ldg(v + 7), c.q0, lane == 0);
             c.slots = p.rtt + (int64_t)__ldg(v + 6) * p.rtt_stride;
             int nr = __ldg(v + 1);
             // a malformed item (more requests than the kernel's rows, or
@@ -909,7 +933,7 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
         const int pos = c.q0 + lane;
         return (c.it < p.n_wide && lane < NP && pos < c.p1) ? __ldg(c.slots + pos) : -1;
     };
-    int2 *hdr = reinterpret_cast<int2 *>(smem + WL::OFF_HDR);
+    int4 *hdr = reinterpret_cast<int4 *>(smem + WL::OFF_HDR);
     const uint32_t qbytes = (uint32_t)(p.hq * p.head_dim * 2);
     Cursor c0{}, c1, c2, c3;
     open_item(c0, fetch());
@@ -929,7 +953,7 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
         const bool end = c0.it >= p.n_wide;
         const int st = j % WL::STAGES;
         if (j >= WL::STAGES &&
-            !wait_or_abort(bar + 8 * (WL::STAGES + st), ((j / WL::STAGES) - 1) & 1, abort_flag, p.status))
+            !wait_or_abort(bar + 8 * (WL::STAGES + st), ((j / WL::STAGES) - 1) & 1, abort_flag, p.status, p.wait_cycles))
             break;
         // an item's first stage also brings its query row into q slot
         // k % NQ, once the consumers have read item k - NQ's out of it
@@ -937,7 +961,7 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
         const int qb = n_items % WL::NQ;
         if (with_q && n_items >= WL::NQ &&
             !wait_or_abort(bar + 8 * (2 * WL::STAGES + qb), ((n_items / WL::NQ) - 1) & 1, abort_flag,
-                           p.status))
+                           p.status, p.wait_cycles))
             break;
         const bool inside = !end && lane < NP && c0.q0 + lane < c0.p1;
         const bool ok = inside && s0 >= 0 && (int64_t)s0 < p.num_slots;
@@ -946,7 +970,7 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
             okf[st * kWideMaxPos + lane] = ok ? 1 : 0;
             slotf[st * kWideMaxPos + lane] = ok ? s0 : -1;
         }
-        if (lane == 0) hdr[st] = make_int2(end ? -1 : c0.it, c0.q0);
+        if (lane == 0) hdr[st] = make_int4(end ? -1 : c0.it, c0.q0, c0.p1, 0);
         const int nok = __popc(__ballot_sync(0xffffffffu, ok));
         __syncwarp();  // flags and header are written before lane 0's arrive releases them
         if (lane == 0)
@@ -1002,14 +1026,14 @@ __device__ void wide_copier(const Params &p, unsigned char *smem, uint32_t sbase
 {
     const uint32_t bar = sbase + WL::OFF_BAR;
     const int *slotf = reinterpret_cast<const int *>(smem + WL::OFF_SLOT);
-    const int2 *hdr = reinterpret_cast<const int2 *>(smem + WL::OFF_HDR);
+    const int4 *hdr = reinterpret_cast<const int4 *>(smem + WL::OFF_HDR);
     const int lane = threadIdx.x & 31;
     const uint32_t RB = (uint32_t)(p.hkv * p.head_dim * 2);
     const int64_t row_elems = (int64_t)p.hkv * p.head_dim;
     const int pos = lane * NH + h;
     for (int j = 0;; ++j) {
         const int st = j % WL::STAGES;
-        if (!wait_or_abort(bar + 8 * (WL::B_DESC + st), (j / WL::STAGES) & 1, abort_flag, p.status)) return;
+        if (!wait_or_abort(bar + 8 * (WL::B_DESC + st), (j / WL::STAGES) & 1, abort_flag, p.status, p.wait_cycles)) return;
         if (hdr[st].x < 0) return;
         const int s = pos < NP ? slotf[st * kWideMaxPos + pos] : -1;
         if (s >= 0) {
@@ -1084,7 +1108,7 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
         auto chunk_at = [&](int c) -> int {
             return NCH == 4 ? ((c + (qd >> 1) + 2 * (x & 1)) & 3) : ((c + (x & 1)) & 1);
         };
-        const int2 *hdr = reinterpret_cast<const int2 *>(smem + WL::OFF_HDR);
+        const int4 *hdr = reinterpret_cast<const int4 *>(smem + WL::OFF_HDR);
         float q[NCH][8], o[DO], m = -INFINITY, l = 0.f;
         int cur = -1, p1 = 0, part_idx = 0, b = 0, n_items = 0;
         bool fin = false;
@@ -1108,8 +1132,8 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
         };
         for (int j = 0;; ++j) {
             const int st = j % kWideStages;
-            if (!wait_or_abort(bar + 8 * st, (j / kWideStages) & 1, abort_flag, p.status)) return;
-            const int2 h = hdr[st];
+            if (!wait_or_abort(bar + 8 * st, (j / kWideStages) & 1, abort_flag, p.status, p.wait_cycles)) return;
+            const int4 h = hdr[st];
             // a new item starts, or (item -1) none is left -- possibly before
             // this CTA got any, when the other CTAs drained the queue first
             if (h.x != cur || h.x < 0) {
@@ -1117,7 +1141,7 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
                 if (h.x < 0) break;
                 cur = h.x;
                 const int32_t *v = p.items + 8 * (int64_t)(p.wide0 + cur);
-                p1 = __ldg(v + 3);
+                p1 = h.z;   // the item's end as the producer resolved it
                 part_idx = __ldg(v + 4);
                 fin = __ldg(v + 5) != 0;
                 b = __ldg(v + 7);
@@ -1262,7 +1286,7 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
     const int g = warp - 1 - kGqaCopyWarps;
     const int G = p.G;
     const int gid = lane >> 2, tig = lane & 3;
-    const int2 *hdr = reinterpret_cast<const int2 *>(smem + WL::OFF_HDR);
+    const int4 *hdr = reinterpret_cast<const int4 *>(smem + WL::OFF_HDR);
     const int *okf = reinterpret_cast<const int *>(smem + WL::OFF_OK);
     uint32_t qf[KS][4];
     float oacc[DT][4], m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
@@ -1302,8 +1326,8 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
     };
     for (int j = 0;; ++j) {
         const int st = j % WL::STAGES;
-        if (!wait_or_abort(bar + 8 * st, (j / WL::STAGES) & 1, abort_flag, p.status)) return;
-        const int2 h = hdr[st];
+        if (!wait_or_abort(bar + 8 * st, (j / WL::STAGES) & 1, abort_flag, p.status, p.wait_cycles)) return;
+        const int4 h = hdr[st];
         // a new item starts, or (item -1) none is left -- possibly before
         // this CTA got any, when the other CTAs drained the queue first
         if (h.x != cur || h.x < 0) {
@@ -1315,7 +1339,7 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
             int nr = __ldg(v + 1);
             if (nr < 1 || nr * G > 16) nr = 1;  // flagged by the producer, which copied one row
             M = nr * G;
-            p1 = __ldg(v + 3);
+            p1 = h.z;   // the item's end as the producer resolved it
             part_idx = __ldg(v + 4);
             fin = __ldg(v + 5) != 0;
             const int b0 = __ldg(v + 7);
@@ -1580,30 +1604,50 @@ extern "C" size_t rx_attn_decode_workspace(int32_t batch, int32_t num_q_heads, i
     return (size_t)(bytes + (wide ? 256 : 0));
 }
 
+// Bound on each pipeline wait of the decode kernels (0: rx::kWaitCycles).
+static std::atomic<long long> g_decode_wait_cycles{0};
+
+extern "C" int rx_decode_set_wait_limit(int64_t cycles)
+{
+    g_decode_wait_cycles.store(cycles > 0 ? (long long)cycles : 0);
+    return RX_OK;
+}
+
+// Argument checks shared by rx_attn_decode and rx_attn_decode_static (`who`
+// names the entry point in the message).
+static int check_decode_args(const char *who, const rx_kv_pool *pool, const void *q, const void *o, const float *lse,
+                      int32_t hq, const int32_t *req_idx, const int32_t *seq_len, const int32_t *rtt,
+                      int64_t rtt_stride, int32_t batch, int32_t max_seq_len, const rx_decode_plan *plan,
+                      float sm_scale)
+{
+    if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0)
+        return rx_set_error(RX_ERR_INVALID, "%s: invalid pool", who);
+    if (pool->head_dim != 64 && pool->head_dim != 128)
+        return rx_set_error(RX_ERR_UNSUPPORTED, "%s: head_dim %d (supported: 64, 128)", who, pool->head_dim);
+    if (!q || !o || !req_idx || !seq_len || !rtt || rtt_stride <= 0 || rtt_stride > INT32_MAX ||
+        batch < 0 || hq <= 0 || max_seq_len <= 0 || max_seq_len > rtt_stride || !(sm_scale > 0.f))
+        return rx_set_error(RX_ERR_INVALID, "%s: invalid argument", who);
+    if (hq % pool->num_kv_heads != 0 || 64 % (hq / pool->num_kv_heads) != 0)
+        return rx_set_error(RX_ERR_UNSUPPORTED, "%s: %d q heads over %d kv heads (need G | 64)", who, hq,
+                            pool->num_kv_heads);
+    if (rx_misaligned16(q) || rx_misaligned16(o) || rx_misaligned16(pool->k) ||
+        rx_misaligned16(pool->v) || (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
+        return rx_set_error(RX_ERR_INVALID, "%s: q, o and the pools must be 16-byte aligned", who);
+    if (plan && (!plan->order || !plan->nparts || !plan->items || plan->n_items < 0 ||
+                 plan->max_parts < 1 || plan->n_wide < 0 || plan->n_wide > plan->n_items))
+        return rx_set_error(RX_ERR_INVALID, "%s: invalid plan", who);
+    return RX_OK;
+}
+
 extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, float *lse,
                               int32_t hq, const int32_t *req_idx, const int32_t *seq_len,
                               const int32_t *rtt, int64_t rtt_stride, int32_t batch,
                               int32_t max_seq_len, const rx_decode_plan *plan, void *workspace,
                               size_t ws_bytes, float sm_scale, int32_t *dev_status, void *stream)
 {
-    if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0)
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: invalid pool");
-    if (pool->head_dim != 64 && pool->head_dim != 128)
-        return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_decode: head_dim %d (supported: 64, 128)",
-                            pool->head_dim);
-    if (!q || !o || !req_idx || !seq_len || !rtt || rtt_stride <= 0 || rtt_stride > INT32_MAX ||
-        batch < 0 || hq <= 0 || max_seq_len <= 0 || max_seq_len > rtt_stride || !(sm_scale > 0.f))
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: invalid argument");
-    if (hq % pool->num_kv_heads != 0 || 64 % (hq / pool->num_kv_heads) != 0)
-        return rx_set_error(RX_ERR_UNSUPPORTED,
-                            "rx_attn_decode: %d q heads over %d kv heads (need G | 64)", hq,
-                            pool->num_kv_heads);
-    if (rx_misaligned16(q) || rx_misaligned16(o) || rx_misaligned16(pool->k) ||
-        rx_misaligned16(pool->v) || (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: q, o and the pools must be 16-byte aligned");
-    if (plan && (!plan->order || !plan->nparts || !plan->items || plan->n_items < 0 ||
-                 plan->max_parts < 1 || plan->n_wide < 0 || plan->n_wide > plan->n_items))
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: invalid plan");
+    const int chk = check_decode_args("rx_attn_decode", pool, q, o, lse, hq, req_idx, seq_len, rtt, rtt_stride,
+                                      batch, max_seq_len, plan, sm_scale);
+    if (chk != RX_OK) return chk;
     if (batch == 0) return RX_OK;
     const int D = pool->head_dim;
     Params p{};
@@ -1624,6 +1668,8 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
     p.batch = batch;
     p.scale_log2 = sm_scale * rx::kLog2e;
     p.status = dev_status;
+    const long long limit = g_decode_wait_cycles.load();
+    p.wait_cycles = limit > 0 ? limit : rx::kWaitCycles;
     int64_t total;
     if (plan) {
         p.order = plan->order;
@@ -1693,7 +1739,9 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
 // exits.  In host code its name is only a stand-in for the symbol, never a
 // device address: the address is looked up once per device with
 // cudaGetSymbolAddress (on the first call made with that device current) and
-// kept.
+// kept.  A device reset (cudaDeviceReset, or anything else that destroys the
+// device's primary context) unloads the module and makes the kept address
+// stale: this entry point must not be called on that device afterwards.
 
 static __device__ __align__(256) unsigned char g_decode_scratch[RX_DECODE_STATIC_SCRATCH_BYTES];
 
@@ -1710,8 +1758,12 @@ extern "C" int rx_attn_decode_static(const rx_kv_pool *pool, const void *q, void
                                      const rx_decode_plan *plan_or_null, float sm_scale,
                                      int32_t *dev_status, void *stream)
 {
-    if (!pool || pool->num_kv_heads <= 0 || pool->head_dim <= 0)
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode_static: invalid pool");
+    // the same checks as rx_attn_decode first, so that a malformed call is
+    // reported as such rather than as a batch too big for the array
+    const int chk = check_decode_args("rx_attn_decode_static", pool, q, o, lse, num_q_heads, req_idx, seq_len,
+                                      req_to_token, rtt_stride, batch, max_seq_len, plan_or_null, sm_scale);
+    if (chk != RX_OK) return chk;
+    if (batch == 0) return RX_OK;
     const size_t need = rx_attn_decode_workspace(batch, num_q_heads, pool->num_kv_heads,
                                                  pool->head_dim, max_seq_len, plan_or_null);
     if (need > (size_t)RX_DECODE_STATIC_SCRATCH_BYTES)
@@ -1733,8 +1785,9 @@ extern "C" int rx_attn_decode_static(const rx_kv_pool *pool, const void *q, void
         }
         scratch = g_scratch_addr[dev];
     }
-    // Every entry read from the scratch array is written earlier in the same
-    // call, so nothing needs clearing between calls.
+    // Every partial read from the scratch array is written earlier in the
+    // same call, and rx_attn_decode zeroes the work counter it keeps at the
+    // array's end before each launch, so nothing carries over between calls.
     return rx_attn_decode(pool, q, o, lse, num_q_heads, req_idx, seq_len, req_to_token, rtt_stride,
                           batch, max_seq_len, plan_or_null, scratch, need, sm_scale, dev_status,
                           stream);

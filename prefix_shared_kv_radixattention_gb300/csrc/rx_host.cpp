@@ -10,11 +10,13 @@
 // nodes are evicted).  Node boundaries are kept as inserts made them; nodes
 // are never merged.
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <deque>
 #include <map>
+#include <memory>
 #include <new>
 #include <set>
 #include <string>
@@ -43,6 +45,31 @@ int rx_set_error(int code, const char *fmt, ...)
 }
 
 extern "C" const char *rx_last_error(void) { return g_last_error.c_str(); }
+
+// Allocation-failure hook for tests: the n-th next radix-tree node
+// allocation (counting from 1) throws std::bad_alloc, as a failing host
+// allocator would; 0 disables it.
+static std::atomic<int64_t> g_fail_alloc_in{0};
+
+extern "C" int rx_test_fail_alloc(int64_t n)
+{
+    if (n < 0) return rx_set_error(RX_ERR_INVALID, "rx_test_fail_alloc: n < 0");
+    g_fail_alloc_in.store(n);
+    return RX_OK;
+}
+
+// Counts one host allocation against the hook; throws when it is the one
+// the hook names.
+static void count_alloc()
+{
+    int64_t left = g_fail_alloc_in.load();
+    while (left > 0) {
+        if (g_fail_alloc_in.compare_exchange_weak(left, left - 1)) {
+            if (left == 1) throw std::bad_alloc();
+            return;
+        }
+    }
+}
 extern "C" int rx_version(void) { return RX_ABI_VERSION; }
 
 // ---------------------------------------------------------------------------
@@ -111,9 +138,17 @@ struct rx_tree {
         }
     }
 
-    Node *new_node(Node *parent)
+    // A node, allocated but not yet part of the tree: operations allocate
+    // every node they need before they change anything, so that a failed
+    // allocation leaves the tree as it was.
+    static Node *raw_node()
     {
-        Node *n = new Node();
+        count_alloc();
+        return new Node();
+    }
+
+    Node *adopt(Node *n, Node *parent)
+    {
         n->id = next_id++;
         n->parent = parent;
         by_id[n->id] = n;
@@ -150,10 +185,11 @@ struct rx_tree {
         }
     }
 
-    // Split n after its first k tokens; n keeps the upper part.
-    Node *split(Node *n, int64_t k)
+    // Split n after its first k tokens; n keeps the upper part, the lower
+    // part goes to `lo` (a node from raw_node).
+    Node *split(Node *n, int64_t k, Node *lo)
     {
-        Node *lo = new_node(n);
+        adopt(lo, n);
         lo->tok.assign(n->tok.begin() + k, n->tok.end());
         lo->slot.assign(n->slot.begin() + k, n->slot.end());
         lo->lock.assign(n->lock.begin() + k, n->lock.end());
@@ -202,20 +238,28 @@ struct rx_tree {
         return true;
     }
 
+    // RX_OK when every cached token of the prefix of t[0..n) holds a lock.
+    int check_unlock(const int64_t *t, int64_t n)
+    {
+        Walk w = walk(t, n);
+        for (size_t i = 0; i < w.nodes.size(); ++i) {
+            Node *x = w.nodes[i];
+            int64_t m = (i + 1 == w.nodes.size()) ? w.in_last : (int64_t)x->tok.size();
+            for (int64_t j = 0; j < m; ++j)
+                if (x->lock[j] <= 0)
+                    return rx_set_error(RX_ERR_INVALID, "rx_lock_prefix: unlocking a token that is not locked");
+        }
+        return RX_OK;
+    }
+
     int lock(const int64_t *t, int64_t n, int32_t delta, int64_t *len)
     {
+        if (delta < 0) {
+            const int rc = check_unlock(t, n);
+            if (rc != RX_OK) return rc;
+        }
         if (delta > 0) ++clock;
         Walk w = walk(t, n);
-        if (delta < 0) {
-            for (size_t i = 0; i < w.nodes.size(); ++i) {
-                Node *x = w.nodes[i];
-                int64_t m = (i + 1 == w.nodes.size()) ? w.in_last : (int64_t)x->tok.size();
-                for (int64_t j = 0; j < m; ++j)
-                    if (x->lock[j] <= 0)
-                        return rx_set_error(RX_ERR_INVALID,
-                                            "rx_lock_prefix: unlocking a token that is not locked");
-            }
-        }
         for (size_t i = 0; i < w.nodes.size(); ++i) {
             Node *x = w.nodes[i];
             int64_t m = (i + 1 == w.nodes.size()) ? w.in_last : (int64_t)x->tok.size();
@@ -234,17 +278,21 @@ struct rx_tree {
 
     int64_t insert(const int64_t *t, const int32_t *s, int64_t n)
     {
-        ++clock;
         Walk w = walk(t, n);
+        const bool grow = w.matched < n;
+        const bool cut = grow && !w.nodes.empty() && w.in_last < (int64_t)w.nodes.back()->tok.size();
+        // the nodes this insert needs, before anything changes
+        std::unique_ptr<Node> lo(cut ? raw_node() : nullptr);
+        std::unique_ptr<Node> fresh(grow ? raw_node() : nullptr);
+        ++clock;
         Node *attach = &root;
         if (!w.nodes.empty()) {
             attach = w.nodes.back();
-            if (w.matched < n && w.in_last < (int64_t)attach->tok.size())
-                split(attach, w.in_last);  // diverges strictly inside: split
+            if (cut) split(attach, w.in_last, lo.release());  // diverges strictly inside: split
         }
         tick(w);
-        if (w.matched < n) {
-            Node *leaf = new_node(attach);
+        if (grow) {
+            Node *leaf = adopt(fresh.release(), attach);
             leaf->tok.assign(t + w.matched, t + n);
             leaf->slot.assign(s + w.matched, s + n);
             leaf->lock.assign((size_t)(n - w.matched), 0);
@@ -262,6 +310,7 @@ extern "C" int rx_tree_create(rx_tree **out)
 {
     if (!out) return rx_set_error(RX_ERR_INVALID, "rx_tree_create: null out");
     RX_TRY
+    count_alloc();
     *out = new rx_tree();
     return RX_OK;
     RX_CATCH
@@ -561,9 +610,13 @@ extern "C" int rx_commit(rx_tree *tree, rx_slot_alloc *alloc, const int64_t *tok
         (n > 0 && (!tokens || !row)))
         return rx_set_error(RX_ERR_INVALID, "rx_commit: invalid argument");
     RX_TRY
-    int rc = tree->lock(tokens, prefix_len, -1, nullptr);
+    // check the unlock, insert (a failed allocation there changes nothing),
+    // then unlock; the order of the insert and the unlock does not change
+    // the resulting tree
+    int rc = tree->check_unlock(tokens, prefix_len);
     if (rc != RX_OK) return rc;
     int64_t cached = tree->insert(tokens, row, n);
+    tree->lock(tokens, prefix_len, -1, nullptr);
     if (cached > prefix_len) alloc->q.insert(alloc->q.end(), row + prefix_len, row + cached);
     return RX_OK;
     RX_CATCH
@@ -613,13 +666,24 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
     auto row = [&](int64_t b) { return rtt + (int64_t)req_idx[b] * stride; };
     std::vector<int32_t> order((size_t)B);
     for (int64_t i = 0; i < B; ++i) order[(size_t)i] = (int32_t)i;
+    // Any order in which rows with a common prefix sit next to each other
+    // will do; the byte-wise order of the slot lists is one (a common prefix
+    // of k slots is a common prefix of 4k bytes), and memcmp finds the first
+    // difference of two long shared prefixes quickly.
     std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
-        return std::lexicographical_compare(row(a), row(a) + seq_len[a], row(b), row(b) + seq_len[b]);
+        const int64_t la = seq_len[a], lb = seq_len[b];
+        const int c = std::memcmp(row(a), row(b), sizeof(int32_t) * (size_t)std::min(la, lb));
+        return c < 0 || (c == 0 && la < lb);
     });
+    // Common prefix of neighbours, at most one short of the shorter request:
+    // a request's last position always stays its own, so that every request
+    // ends in a private piece that can follow its length (RX_PLAN_OPEN_END).
     std::vector<int64_t> lcp((size_t)(B > 1 ? B - 1 : 0));
     for (int64_t i = 0; i + 1 < B; ++i) {
         const int32_t *x = row(order[(size_t)i]), *y = row(order[(size_t)i + 1]);
-        int64_t m = std::min(seq_len[order[(size_t)i]], seq_len[order[(size_t)i + 1]]), k = 0;
+        const int64_t m = std::min(seq_len[order[(size_t)i]], seq_len[order[(size_t)i + 1]]) - 1;
+        int64_t k = 0;
+        while (k + 16 <= m && std::memcmp(x + k, y + k, 64) == 0) k += 16;
         while (k < m && x[k] == y[k]) ++k;
         lcp[(size_t)i] = k;
     }
@@ -781,6 +845,9 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
             int64_t p0 = s0 + piece(L - s0, n, c), p1 = s0 + piece(L - s0, n, c + 1);
             bool fin = nparts[(size_t)order[(size_t)r]] == 1;
             const int32_t b0 = order[(size_t)r];
+            // the request's last piece ends wherever its length is when the
+            // plan is used
+            if (c + 1 == n) p1 = RX_PLAN_OPEN_END;
             items.push_back({{(int32_t)r, 1, (int32_t)p0, (int32_t)p1,
                               (int32_t)(priv_base[(size_t)r] + c), fin ? 1 : 0, req_idx[b0], b0},
                              wide});
@@ -790,11 +857,14 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
     // heads at once); within each, items of several requests before
     // single-request ones, and each of those longest first, so that the tail
     // of a grid holds the short items
-    std::stable_sort(items.begin(), items.end(), [](const Item &a, const Item &b) {
+    auto item_end = [&](const Item &x) -> int64_t {
+        return x.v[3] == RX_PLAN_OPEN_END ? (int64_t)seq_len[x.v[7]] : (int64_t)x.v[3];
+    };
+    std::stable_sort(items.begin(), items.end(), [&](const Item &a, const Item &b) {
         if (a.all != b.all) return b.all;
         const bool sa = a.v[1] == 1, sb = b.v[1] == 1;
         if (sa != sb) return sb;
-        int64_t la = (int64_t)a.v[3] - a.v[2], lb = (int64_t)b.v[3] - b.v[2];
+        int64_t la = item_end(a) - a.v[2], lb = item_end(b) - b.v[2];
         if (la != lb) return la > lb;
         return a.v[1] > b.v[1];
     });

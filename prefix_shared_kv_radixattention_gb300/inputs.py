@@ -38,10 +38,15 @@ import numpy as np
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:
-    """float32 -> bf16 bits (uint16), round to nearest, ties to even."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    bias = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
-    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+    """float32 -> bf16 bits (uint16), round to nearest, ties to even: add
+    0x7FFF plus the lowest kept bit to the float's bits, keep the top half."""
+    u = np.array(x, dtype=np.float32, copy=True).view(np.uint32)
+    lsb = u >> np.uint32(16)
+    lsb &= np.uint32(1)
+    u += lsb
+    u += np.uint32(0x7FFF)
+    u >>= np.uint32(16)
+    return u.astype(np.uint16)
 
 
 def bf16_to_f32(h: np.ndarray) -> np.ndarray:

@@ -1,9 +1,10 @@
 """Helpers for the GPU parity tests: upload a Problem, run the C-ABI entry
 points, build the oracle's pools, compare.
 
-Tolerance (bf16 outputs): |gpu - oracle| <= 2e-2 + 1e-2 * |oracle| per
-element (max |err| <= 2e-2 absolute and 1e-2 relative, read as an allclose
-bound); lse within 1e-3 absolute (fp32 sums in the kernel, fp64 in the
+Tolerance (bf16 outputs): both readings of "max |err| <= 2e-2 absolute and
+1e-2 relative" hold -- the allclose bound |gpu - oracle| <= 2e-2 + 1e-2 *
+|oracle| per element, and the stricter max |gpu - oracle| <= 2e-2 over every
+element; lse within 1e-3 absolute (fp32 sums in the kernel, fp64 in the
 oracle).
 """
 import numpy as np
@@ -62,7 +63,11 @@ class Dev:
         rx.rx_kv_store(self.k_pool, self.v_pool, to_dev(p.new_k), to_dev(p.new_v), i32(p.new_slots),
                        self.status)
 
-    def decode(self, plan: bool, kv_chunk: int = 0, min_shared: int = 16, with_lse: bool = True):
+    def decode(self, plan: bool, kv_chunk: int = 0, min_shared: int = 16, with_lse: bool = True,
+               plan_seq_len=None, seq_len=None):
+        """Decode through the C ABI.  plan_seq_len: the lengths the plan is
+        built for (default: the problem's); seq_len: the lengths the device
+        call sees (default: the problem's)."""
         p = self.prob
         B = len(p.dec_req_idx)
         q = to_dev(p.q_dec)
@@ -70,13 +75,15 @@ class Dev:
         lse = torch.empty((B, p.hq), dtype=torch.float32, device="cuda") if with_lse else None
         dp = None
         if plan:
-            buf, info = rx.rx_decode_plan_build(p.req_to_token, p.dec_req_idx, p.dec_seq_len, p.hq,
+            lens = p.dec_seq_len if plan_seq_len is None else np.asarray(plan_seq_len, np.int32)
+            buf, info = rx.rx_decode_plan_build(p.req_to_token, p.dec_req_idx, lens, p.hq,
                                                 p.hkv, kv_chunk, min_shared)
             dp = rx.plan_to_device(buf, info, B)
-        max_len = int(p.dec_seq_len.max())
+        dev_len = p.dec_seq_len if seq_len is None else np.asarray(seq_len, np.int32)
+        max_len = min(int(dev_len.max()), p.rtt_stride)
         ws_bytes = rx.rx_attn_decode_workspace(B, p.hq, p.hkv, p.d, max_len, dp)
         ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
-        rx.rx_attn_decode(self.k_pool, self.v_pool, q, o, lse, i32(p.dec_req_idx), i32(p.dec_seq_len),
+        rx.rx_attn_decode(self.k_pool, self.v_pool, q, o, lse, i32(p.dec_req_idx), i32(dev_len),
                           self.rtt, max_len, p.sm_scale, dp, ws if ws_bytes else None, self.status)
         torch.cuda.synchronize()
         return o.float().cpu().numpy(), (lse.cpu().numpy() if with_lse else None)
@@ -107,26 +114,28 @@ class Dev:
         """Host pools after the step's KV store, and the matching req_to_token.
 
         Small pools: the full host pools plus the oracle's own kv_store.  Big
-        pools: a compact pool of the referenced rows only (pool rows renamed,
-        which the slot-permutation invariance makes exact), with the new rows
-        placed by the oracle's kv_store."""
+        pools: a compact pool of the cached rows (in the order they were
+        drawn) and the new rows, placed by the oracle's kv_store, with
+        req_to_token renamed to those rows (the slot-permutation invariance
+        makes the renaming exact)."""
         p = self.prob
         if self.host_pools:
             kp, vp = self.kp_host.copy(), self.vp_host.copy()
             oracle.kv_store(kp, vp, p.new_k, p.new_v, p.new_slots)
             return kp, vp, p.req_to_token
-        slots = np.concatenate([p.cached_slots, p.new_slots])
-        uniq = np.unique(slots)
-        kp = np.zeros((len(uniq), p.hkv, p.d), np.uint16)
+        S = p.num_slots
+        row_of = np.full(S, -1, np.int64)
+        nc = len(p.cached_slots)
+        row_of[p.cached_slots] = np.arange(nc)
+        fresh = p.new_slots[row_of[p.new_slots] < 0]
+        row_of[fresh] = nc + np.arange(len(fresh))
+        kp = np.zeros((nc + len(fresh), p.hkv, p.d), np.uint16)
         vp = np.zeros_like(kp)
-        pos_c = np.searchsorted(uniq, p.cached_slots)
-        kp[pos_c], vp[pos_c] = p.cached_k, p.cached_v
-        oracle.kv_store(kp, vp, p.new_k, p.new_v, np.searchsorted(uniq, p.new_slots).astype(np.int32))
+        kp[:nc], vp[:nc] = p.cached_k, p.cached_v
+        oracle.kv_store(kp, vp, p.new_k, p.new_v, row_of[p.new_slots].astype(np.int32))
         rtt = p.req_to_token
-        loc = np.searchsorted(uniq, np.maximum(rtt, 0))
-        loc = np.minimum(loc, len(uniq) - 1)
-        hit = (rtt >= 0) & (uniq[loc] == rtt)
-        return kp, vp, np.where(hit, loc, -1).astype(np.int32)
+        ok = (rtt >= 0) & (rtt < S)
+        return kp, vp, np.where(ok, row_of[np.where(ok, rtt, 0)], -1).astype(np.int32)
 
 
 def compare(gpu, ref, what=""):
@@ -137,6 +146,7 @@ def compare(gpu, ref, what=""):
     assert not np.isnan(gpu).any(), f"{what}: NaN in GPU output"
     assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; "
                            f"max abs err {err.max():.3e}")
+    assert err.max() <= ATOL, f"{what}: max abs err {err.max():.3e} above {ATOL}"
     return float(err.max())
 
 

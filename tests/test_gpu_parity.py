@@ -217,6 +217,73 @@ def test_decode_single_token_context():
         _check_decode(prob, plan)
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(32, 32, 128), (32, 8, 128), (64, 8, 128), (8, 2, 64), (4, 4, 64)])
+def test_decode_plan_serves_later_steps(hq, hkv, d):
+    """A plan built when every request was k tokens shorter serves the later
+    step unchanged: each request's last piece ends at its length on the
+    device (RX_PLAN_OPEN_END).  All-heads kernels (one and several q heads
+    per kv head) and the per-head kernel (two kv heads) alike."""
+    g = _gpu()
+    prob = inputs.few_shot_decode(hq=hq, hkv=hkv, d=d, batch=9, shared=200, private=90, num_slots=8192)
+    dev = g.Dev(prob)
+    dev.kv_store()
+    kp, vp, rtt = dev.oracle_pools()
+    ro, rl = oracle.decode(prob.q_dec, kp, vp, rtt, prob.dec_req_idx, prob.dec_seq_len, prob.sm_scale)
+    for k in (1, 5, 40):
+        for chunk in (0, 64):
+            o, lse = dev.decode(plan=True, kv_chunk=chunk, plan_seq_len=prob.dec_seq_len - k)
+            g.compare(o, ro, f"plan built {k} tokens earlier, chunk {chunk}")
+            g.compare_lse(lse, rl, f"plan built {k} tokens earlier, chunk {chunk}")
+    assert dev.status_word() == 0
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 32), (32, 8), (8, 2)])
+def test_decode_open_end_past_the_slot_lists_is_flagged(hq, hkv):
+    """A device length past the slot lists' stride, or one that no longer
+    reaches a request's last piece, is flagged (RX_DEV_BAD_LEN); the outputs
+    stay finite and nothing outside the buffers is read."""
+    g = _gpu()
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.few_shot_decode(hq=hq, hkv=hkv, d=128, batch=5, shared=64, private=40, num_slots=2048)
+    dev = g.Dev(prob)
+    dev.kv_store()
+    for bad in (prob.rtt_stride + 3, 10):
+        lens = prob.dec_seq_len.copy()
+        lens[2] = bad
+        dev.status.zero_()
+        o, _ = dev.decode(plan=True, kv_chunk=64, seq_len=lens)
+        assert dev.status_word() & rx.RX_DEV_BAD_LEN, bad
+        assert np.isfinite(o).all()
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 32), (32, 8), (8, 2)])
+def test_decode_wait_that_runs_out_is_reported(hq, hkv):
+    """With the decode kernels' wait limit cut to a few cycles, their first
+    pipeline wait that is not already satisfied runs out: the call's status
+    word gets RX_DEV_TIMEOUT, the kernels leave cleanly (copies in flight are
+    waited for), and the context stays usable -- the next call with the
+    default limit matches the oracle.  No GPU fault is involved: the waits
+    are bounded by construction and simply give up early."""
+    g = _gpu()
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.few_shot_decode(hq=hq, hkv=hkv, d=128, batch=6, shared=300, private=200, num_slots=4096)
+    dev = g.Dev(prob)
+    dev.kv_store()
+    try:
+        rx.rx_decode_set_wait_limit(8)
+        dev.decode(plan=True, kv_chunk=64)
+        assert dev.status_word() & rx.RX_DEV_TIMEOUT
+    finally:
+        rx.rx_decode_set_wait_limit(0)
+    dev.status.zero_()
+    o, lse = dev.decode(plan=True, kv_chunk=64)
+    assert dev.status_word() == 0
+    kp, vp, rtt = dev.oracle_pools()
+    ro, rl = oracle.decode(prob.q_dec, kp, vp, rtt, prob.dec_req_idx, prob.dec_seq_len, prob.sm_scale)
+    g.compare(o, ro, "after a timed-out call")
+    g.compare_lse(lse, rl, "after a timed-out call")
+
+
 def test_decode_without_lse_output():
     g = _gpu()
     prob = inputs.few_shot_decode(hq=8, hkv=8, d=128, batch=6, shared=100, private=50, num_slots=1024)

@@ -286,8 +286,14 @@ def check_plan(prob, order, nparts, items, info, auto=False):
     assert sorted(order.tolist()) == list(range(B))
     cover = [np.zeros(int(L), np.int32) for L in prob.dec_seq_len]
     parts = [[] for _ in range(B)]
+    open_end = [0] * B
     reads = 0
     for r0, nr, p0, p1, part, fin, row0, b0 in items.tolist():
+        if p1 == rx.RX_PLAN_OPEN_END:
+            # a request's own last piece ends at its length when the plan is used
+            assert nr == 1
+            p1 = int(prob.dec_seq_len[b0])
+            open_end[b0] += 1
         assert 1 <= nr and nr * G <= 64 and p0 < p1
         assert b0 == order[r0] and row0 == prob.dec_req_idx[b0]
         # single-request items of an automatic plan for the all-heads kernel
@@ -304,6 +310,7 @@ def check_plan(prob, order, nparts, items, info, auto=False):
             assert bool(fin) == (nparts[b] == 1)
         reads += p1 - p0
     assert reads * 1 >= info.tokens_read
+    assert open_end == [1] * B, "every request ends in one open-ended piece of its own"
     for b in range(B):
         assert np.all(cover[b] == 1), f"request {b} context not covered exactly once"
         assert sorted(parts[b]) == list(range(int(nparts[b])))
@@ -314,6 +321,9 @@ def check_plan(prob, order, nparts, items, info, auto=False):
     # otherwise none.  Within each part, items of several requests come
     # before single-request ones, each of those longest first.
     n_wide = int(info.n_wide)
+    items = items.copy()
+    is_open = items[:, 3] == rx.RX_PLAN_OPEN_END
+    items[is_open, 3] = prob.dec_seq_len[items[is_open, 7]]
     head, tail = items[:len(items) - n_wide], items[len(items) - n_wide:]
     if not _plan_wide(prob):
         assert n_wide == 0

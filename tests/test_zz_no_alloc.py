@@ -59,18 +59,51 @@ def _static(rx, g, dev, plan, prob):
 
 
 def test_static_scratch_matches_workspace_two_calls():
+    """The static array and a workspace give bit-identical results (the same
+    kernels run on the same plan; only where the partials live differs).
+    The second call in a row is a smaller batch with other shapes than the
+    first, so a partial read from the wrong offset, or one left over from
+    the first call's data, would show.  Both also match the oracle."""
+    import oracle
     cases = [
+        (inputs.tree_of_thought_decode(seed=72, depth=3, fanout=3, edge=90, num_slots=8192), 64),
         (inputs.few_shot_decode(seed=71, hq=8, hkv=2, d=128, batch=10, shared=300, private=150,
                                 num_slots=8192), 64),
-        (inputs.tree_of_thought_decode(seed=72, depth=3, fanout=3, edge=90, num_slots=8192), 64),
     ]
+    sizes = []
     for prob, kv_chunk in cases:   # two calls in a row on the shared array
         rx, g, dev, plan = _setup(prob, kv_chunk)
+        sizes.append(rx.rx_attn_decode_workspace(len(prob.dec_req_idx), prob.hq, prob.hkv, prob.d,
+                                                 int(prob.dec_seq_len.max()), plan))
         o_ws, l_ws = _with_workspace(rx, g, dev, plan, prob)
         o_st, l_st = _static(rx, g, dev, plan, prob)
-        assert np.max(np.abs(o_st - o_ws)) <= g.ATOL + g.RTOL * np.max(np.abs(o_ws))
-        assert np.max(np.abs(l_st - l_ws)) <= g.LSE_ATOL
+        assert np.array_equal(o_st, o_ws), "static scratch and workspace outputs differ"
+        assert np.array_equal(l_st, l_ws), "static scratch and workspace log-sum-exps differ"
         assert dev.status_word() == 0
+        kp, vp, rtt = dev.oracle_pools()
+        ro, rl = oracle.decode(prob.q_dec, kp, vp, rtt, prob.dec_req_idx, prob.dec_seq_len, prob.sm_scale)
+        g.compare(o_st, ro, f"{prob.name} static scratch")
+        g.compare_lse(l_st, rl, f"{prob.name} static scratch")
+    assert sizes[1] < sizes[0], "the second call must use less of the array than the first"
+
+
+def test_static_scratch_checks_arguments_before_capacity():
+    """A malformed plan is reported as invalid, not as a batch too big for
+    the array."""
+    import ctypes
+    prob = inputs.few_shot_decode(seed=73, hq=8, hkv=8, d=128, batch=4, shared=100, private=70, num_slots=1024)
+    rx, g, dev, plan = _setup(prob, 64)
+    bad = rx.DecodePlan.from_buffer_copy(plan.struct)
+    bad.max_parts = 0
+    q = g.to_dev(prob.q_dec)
+    o = torch.empty_like(q)
+    with pytest.raises(rx.RxError) as e:
+        rx._check(rx._lib.rx_attn_decode_static(
+            ctypes.byref(rx.make_pool(dev.k_pool, dev.v_pool)), rx._ptr(q), rx._ptr(o), None, prob.hq,
+            rx._ptr(g.i32(prob.dec_req_idx)), rx._ptr(g.i32(prob.dec_seq_len)), rx._ptr(dev.rtt),
+            dev.rtt.shape[1], len(prob.dec_req_idx), int(prob.dec_seq_len.max()), ctypes.byref(bad),
+            ctypes.c_float(prob.sm_scale), None, rx._stream(None)))
+    assert e.value.code == rx.RX_ERR_INVALID
 
 
 def test_static_scratch_refuses_oversized_batch():
