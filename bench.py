@@ -531,6 +531,12 @@ def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
 # says which capture.  An entry is removed whenever its kernel changes, so
 # that an old count is never reported for new code.
 PROFILED_TRAFFIC = {
+    ("mixed_chat", "staged"): (
+        846_600_000, "ncu --set full -k extend_kernel -c 1 on mixed_chat (600,000-slot pool; the kernel "
+                     "reads the same staged rows, Q and O at any pool size): extend_kernel alone"),
+    ("mixed_chat", "decode"): (
+        1_665_600_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat (600,000-slot pool; "
+                       "same rows): decode_gqa_kernel alone, without the merge"),
     ("cached_prefix_extend", "staged"): (
         585_800_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend (1M-slot pool): "
                      "extend_kernel alone, without the staging copy"),
