@@ -214,9 +214,16 @@ class GpuStep:
         # FP8 pools (optional): the step's rows also stored as E4M3 codes
         self.kv_fp8 = kv_fp8
         if kv_fp8:
+            # E4M3 pools (scale 1): the cached rows quantized at set-up, the
+            # step's rows stored by rx_kv_store_fp8 in the timed step; decode
+            # reads them (rx_attn_decode_fp8), extend keeps the bf16 pools
             self.k8 = torch.zeros((p.num_slots, p.hkv, p.d), dtype=torch.uint8, device=dev)
             self.v8 = torch.zeros_like(self.k8)
-            self.launches += 1
+            for s0 in range(0, len(idx), 1 << 16):
+                sl = idx[s0:s0 + (1 << 16)].to(torch.int32)
+                rx.rx_kv_store_fp8(self.k8, self.v8, 1.0, 1.0, self.k_pool[sl.long()], self.v_pool[sl.long()], sl,
+                                   self.status)
+            self.launches += 1  # the step's FP8 store
         # rotary position embedding (optional): K rotated on its way into the
         # pool, the step's q rows rotated in place
         self.rope_base = rope_base
@@ -250,6 +257,11 @@ class GpuStep:
 
     def decode(self):
         p = self.prob
+        if self.kv_fp8:
+            self.rx.rx_attn_decode_fp8(self.k8, self.v8, 1.0, 1.0, self.q_dec, self.o_dec, None, self.dec_req,
+                                       self.dec_len, self.rtt, self.max_len, p.sm_scale, self.plan, self.ws,
+                                       self.status)
+            return
         self.rx.rx_attn_decode(self.k_pool, self.v_pool, self.q_dec, self.o_dec, None, self.dec_req,
                                self.dec_len, self.rtt, self.max_len, p.sm_scale, self.plan, self.ws,
                                self.status)
@@ -367,13 +379,14 @@ def run_gpu(args, rank, world, local_rank):
     ms_of = {k: statistics.mean(v) for k, v in part_ms.items()}
     if st.has_dec:
         dec_ms = ms_of["decode"]
-        uniq_bytes = st.plan_info.tokens_read * kv_row
+        uniq_bytes = st.plan_info.tokens_read * (kv_row // 2 if st.kv_fp8 else kv_row)
         achieved = uniq_bytes / (dec_ms / 1e3) / 1e9
         traffic, tsrc = profiled_traffic(args.workload, "decode")
         roofs["decode"] = {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "traffic": traffic, "traffic_source": tsrc,
-            "kernel": "rx_attn_decode (" + " + ".join(st.decode_kernels) + ")",
+            "kernel": ("rx_attn_decode_fp8 (decode_gqa_kernel<F8> + merge_kernel)" if st.kv_fp8 else
+                       "rx_attn_decode (" + " + ".join(st.decode_kernels) + ")"),
             "algorithmic_bytes_per_launch": int(uniq_bytes), "launch_ms": round(dec_ms, 5),
             "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)", "frac_of_8000": round(achieved / 8000.0, 4)}
         out["decode"] = {"tok_s": B_dec / (dec_ms / 1e3), "hbm_gbs_unique": achieved,
@@ -425,7 +438,8 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk.summary(), "parts": out, "wall_s_timed_loop": round(t_wall, 3),
     }
     if st.kv_fp8:
-        line["config"]["kv_fp8"] = "extra part: the step's K/V rows also stored as E4M3 codes (scale 1)"
+        line["config"]["kv_fp8"] = ("decode reads E4M3 pools (scale 1; cached rows quantized at set-up), and the "
+                                    "step also stores its K/V rows as codes (extra part); extend reads bf16 pools")
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(prob, args.workload, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -976,7 +990,7 @@ def main():
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="override the pool size (profiling runs on a smaller device footprint)")
     ap.add_argument("--kv-fp8", action="store_true",
-                    help="also store the step's K/V rows into FP8 (E4M3) pools (an extra part of the step)")
+                    help="decode over FP8 (E4M3) pools; the step also stores its K/V rows as codes")
     ap.add_argument("--rope", type=float, default=0.0, metavar="BASE",
                     help="add rotary position embedding to the step (K fused into the store, q in place)")
     ap.add_argument("--graph", action="store_true",

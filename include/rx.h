@@ -236,16 +236,22 @@ int rx_schedule(rx_tree *tree, const int64_t *tokens, const int64_t *offsets, in
 int rx_image_keys(const uint8_t *data, int64_t nbytes, int64_t n_tokens, int64_t *out_keys);
 
 /* ---- KV pool (device) ----------------------------------------------------
- * One layer's K and V.  A model's pools for L layers may share one
- * allocation each, [L, num_slots, num_kv_heads, head_dim]: layer l's pool is
- * k = base_k + l * num_slots * num_kv_heads * head_dim elements (v alike),
- * and the same slot ids and req_to_token rows serve every layer. */
+ * K and V of one layer, or of a model's L layers in one allocation each.
+ * With num_layers L > 1, k and v point to [L, num_slots, num_kv_heads,
+ * head_dim] arrays and a call reads or writes layer `layer` only: the
+ * layer's rows start layer * num_slots * num_kv_heads * head_dim elements
+ * after k (v alike).  A slot id names the same token in every layer, so one
+ * radix tree, one slot list per request and one decode plan serve all
+ * layers.  num_layers 0 or 1 is a one-layer pool (layer must be 0); a layer
+ * outside [0, L) is RX_ERR_INVALID. */
 typedef struct {
-    void *k;              /* device bf16 [num_slots, num_kv_heads, head_dim] */
-    void *v;              /* device bf16, same shape                         */
+    void *k;              /* device bf16 [num_layers,] num_slots, num_kv_heads, head_dim */
+    void *v;              /* device bf16, same shape                                     */
     int64_t num_slots;
     int32_t num_kv_heads;
-    int32_t head_dim;     /* 64 or 128                                       */
+    int32_t head_dim;     /* 64 or 128                                                   */
+    int32_t num_layers;   /* 0 or 1: one layer; L > 1: k and v hold L layers             */
+    int32_t layer;        /* the layer this call reads or writes                         */
 } rx_kv_pool;
 
 /* KV slot scatter: K[slots[i]] = k_new[i], V[slots[i]] = v_new[i] for i < n.
@@ -270,20 +276,23 @@ int rx_kv_store(const rx_kv_pool *pool, const void *k_new, const void *v_new, co
  * mantissa), magnitudes past 448 saturate to 448 and NaN stays NaN.
  * k_new, v_new: device bf16 [n, Hkv, d], 16-byte aligned; pools 8-byte
  * aligned; Hkv * d a multiple of 8.  A slot id outside the pool sets
- * RX_DEV_BAD_SLOT and its row is not written.  (The attention kernels
- * read bf16 pools; reading FP8 pools is not built yet.) */
+ * RX_DEV_BAD_SLOT and its row is not written.  rx_attn_decode_fp8 reads
+ * such pools; extend reads bf16 pools. */
 typedef struct {
-    void *k;          /* device uint8 [num_slots, num_kv_heads, head_dim] */
+    void *k;          /* device uint8 [num_layers,] num_slots, num_kv_heads, head_dim */
     void *v;
     int64_t num_slots;
     int32_t num_kv_heads;
     int32_t head_dim;
     float k_scale;    /* > 0 */
     float v_scale;    /* > 0 */
+    int32_t num_layers;   /* as in rx_kv_pool */
+    int32_t layer;
 } rx_kv_pool_fp8;
 
 int rx_kv_store_fp8(const rx_kv_pool_fp8 *pool, const void *k_new, const void *v_new, const int32_t *slots,
                     int64_t n, int32_t *dev_status, void *stream);
+
 
 /* ---- rotary position embedding (device) --------------------------------
  * Not from the pages, which do not reach inside the model: the position
@@ -486,6 +495,27 @@ int rx_attn_decode_static(const rx_kv_pool *pool, const void *q, void *o, float 
                           const int32_t *req_to_token, int64_t rtt_stride, int32_t batch,
                           int32_t max_seq_len, const rx_decode_plan *plan_or_null, float sm_scale,
                           int32_t *dev_status, void *stream);
+
+/* ---- decode over FP8 pools ------------------------------------------------ */
+
+/* Decode attention over FP8 pools: rx_attn_decode's definition applied to the
+ * values E4M3(code) * scale of each pool, with the same arguments (q, o and
+ * lse as there).  A plan is required, and all its items must go to the
+ * all-heads kernel (rx_decode_plan_info.n_wide == n_items, which the plan
+ * builder gives for these head counts unless a shared segment's requests
+ * make more than 16 groups); so is a workspace of
+ * rx_attn_decode_workspace(...) bytes.  Supported: 8 kv heads with 2, 4, 8
+ * or 16 q heads each, head_dim 64 or 128 (RX_ERR_UNSUPPORTED otherwise).
+ * The products run in f16 with fp32 sums: codes widen to f16 exactly, q is
+ * converted to f16 (exact for |q| within f16's range, which q must respect;
+ * values below 2^-14 round to f16 subnormals), and the softmax weights are
+ * rounded to f16 rather than bf16.  K's scale multiplies the scores, V's the
+ * output.  Each slot row read is num_kv_heads * head_dim bytes, half a bf16
+ * pool's. */
+int rx_attn_decode_fp8(const rx_kv_pool_fp8 *pool, const void *q, void *o, float *lse, int32_t num_q_heads,
+                       const int32_t *req_idx, const int32_t *seq_len, const int32_t *req_to_token,
+                       int64_t rtt_stride, int32_t batch, int32_t max_seq_len, const rx_decode_plan *plan,
+                       void *workspace, size_t ws_bytes, float sm_scale, int32_t *dev_status, void *stream);
 
 /* ---- compressed finite-state machine (constrained decoding) -------------
  * Source: "SGLang: Efficient Execution of Structured Language Model

@@ -15,7 +15,8 @@ The reading taken is the plain one:
   E4M3(x / scale), rounded to the nearest code with ties to the even
   mantissa, magnitudes past 448 saturate to 448, and NaN stays NaN;
 * attention over an FP8 pool is the fp64 definition applied to
-  decode(code) * scale.
+  decode(code) * scale (``attention``: the bf16-pool oracle on the decoded
+  codes, with each pool's scale taken out of its sums).
 
 Pinned in ``tests/test_fp8_oracle.py``.
 """
@@ -84,3 +85,33 @@ def quantize_rows(x, scale: float) -> np.ndarray:
 def dequantize(codes, scale: float) -> np.ndarray:
     """The values attention reads from an FP8 pool: decode(code) * scale."""
     return decode(codes) * float(scale)
+
+
+def bf16_bits(codes) -> np.ndarray:
+    """decode(code) as bf16 bits: every E4M3 value (subnormals included) has
+    at most 4 significant bits and an exponent inside bf16's range, so the
+    float32 of it has 16 zero low bits and the top half is exact."""
+    f = decode(codes).astype(np.float32)
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def attention(q, k_codes, v_codes, k_scale: float, v_scale: float, rtt, q_row, kbeg, kend, sm_scale,
+              n_threads=None):
+    """fp64 attention over FP8 pools: the definition applied to
+    decode(code) * scale.  Each pool's scale comes out of its sums:
+        s_j = sm_scale * q . (decode(k_j) k_scale) = (sm_scale k_scale) q . decode(k_j),
+        o   = sum_j w_j decode(v_j) v_scale / sum_j w_j = v_scale (sum_j w_j decode(v_j) / sum_j w_j),
+    so the attention of the decoded codes (exact bf16 values) with the score
+    scale sm_scale * k_scale, times v_scale, is that definition.
+    Returns (o fp64, lse fp64)."""
+    from . import attention as attention_bf16
+    o, lse = attention_bf16(q, bf16_bits(k_codes), bf16_bits(v_codes), rtt, q_row, kbeg, kend,
+                            float(sm_scale) * float(k_scale), n_threads)
+    return o * float(v_scale), lse
+
+
+def decode_rows(q, k_codes, v_codes, k_scale, v_scale, rtt, req_idx, seq_len, sm_scale, n_threads=None):
+    """Decode rows over FP8 pools: one query per request at position L_b - 1."""
+    n = len(req_idx)
+    return attention(q, k_codes, v_codes, k_scale, v_scale, rtt, np.asarray(req_idx, np.int32),
+                     np.zeros(n, np.int32), np.asarray(seq_len, np.int32), sm_scale, n_threads)

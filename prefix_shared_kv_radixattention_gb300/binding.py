@@ -51,7 +51,8 @@ class RxError(RuntimeError):
 
 class KVPool(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_slots", ctypes.c_int64),
-                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("num_layers", ctypes.c_int32), ("layer", ctypes.c_int32)]
 
 
 class DecodePlan(ctypes.Structure):
@@ -102,10 +103,13 @@ _sig("rx_image_keys", ctypes.c_int, _P, _I64, _I64, _P)
 
 class KVPoolFp8(ctypes.Structure):
     _fields_ = [("k", _P), ("v", _P), ("num_slots", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+                ("head_dim", ctypes.c_int32), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
+                ("num_layers", ctypes.c_int32), ("layer", ctypes.c_int32)]
 
 
 _sig("rx_kv_store_fp8", ctypes.c_int, ctypes.POINTER(KVPoolFp8), _P, _P, _P, _I64, _P, _P)
+_sig("rx_attn_decode_fp8", ctypes.c_int, ctypes.POINTER(KVPoolFp8), _P, _P, _P, _I32, _P, _P, _P, _I64, _I32,
+     _I32, _P, _P, ctypes.c_size_t, ctypes.c_float, _P, _P)
 
 
 class FsmInfo(ctypes.Structure):
@@ -370,19 +374,31 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def make_pool(k_pool, v_pool) -> KVPool:
+def _pool_dims(k_pool, v_pool, layer: int):
+    """(num_slots, kv heads, head_dim, num_layers) of a one-layer pool
+    [S, Hkv, d] or a layered one [L, S, Hkv, d]."""
+    if k_pool.shape != v_pool.shape or k_pool.dim() not in (3, 4):
+        raise ValueError("k_pool and v_pool must both be [num_slots, num_kv_heads, head_dim] or "
+                         "[num_layers, num_slots, num_kv_heads, head_dim]")
+    if k_pool.dim() == 3:
+        return (*k_pool.shape, 0)
+    L, S, hkv, d = k_pool.shape
+    return S, hkv, d, L
+
+
+def make_pool(k_pool, v_pool, layer: int = 0) -> KVPool:
+    """The C pool of k_pool / v_pool: one layer [S, Hkv, d], or layer `layer`
+    of a layered pool [L, S, Hkv, d]."""
     torch = _torch()
     _dev(k_pool, torch.bfloat16, "k_pool")
     _dev(v_pool, torch.bfloat16, "v_pool")
-    if k_pool.shape != v_pool.shape or k_pool.dim() != 3:
-        raise ValueError("k_pool and v_pool must both be [num_slots, num_kv_heads, head_dim]")
-    S, hkv, d = k_pool.shape
-    return KVPool(k_pool.data_ptr(), v_pool.data_ptr(), S, hkv, d)
+    S, hkv, d, L = _pool_dims(k_pool, v_pool, layer)
+    return KVPool(k_pool.data_ptr(), v_pool.data_ptr(), S, hkv, d, L, int(layer))
 
 
-def rx_kv_store(k_pool, v_pool, k_new, v_new, slots, dev_status=None, stream=None) -> None:
+def rx_kv_store(k_pool, v_pool, k_new, v_new, slots, dev_status=None, stream=None, layer: int = 0) -> None:
     torch = _torch()
-    pool = make_pool(k_pool, v_pool)
+    pool = make_pool(k_pool, v_pool, layer)
     _dev(k_new, torch.bfloat16, "k_new")
     _dev(v_new, torch.bfloat16, "v_new")
     _dev(slots, torch.int32, "slots")
@@ -405,9 +421,9 @@ def rx_rope(x, pos, base: float, stream=None) -> None:
 
 
 def rx_kv_store_rope(k_pool, v_pool, k_new, v_new, slots, pos, base: float, dev_status=None,
-                     stream=None) -> None:
+                     stream=None, layer: int = 0) -> None:
     torch = _torch()
-    pool = make_pool(k_pool, v_pool)
+    pool = make_pool(k_pool, v_pool, layer)
     _dev(k_new, torch.bfloat16, "k_new")
     _dev(v_new, torch.bfloat16, "v_new")
     _dev(slots, torch.int32, "slots")
@@ -431,11 +447,11 @@ def rx_attn_extend_workspace(total_ctx_tokens: int, batch: int, num_kv_heads: in
 
 def rx_attn_extend(k_pool, v_pool, q, o, lse, qo_indptr, req_idx, prefix_len, extend_len,
                    req_to_token, max_extend_len: int, sm_scale: float, dev_status=None,
-                   stream=None, workspace=None) -> None:
+                   stream=None, workspace=None, layer: int = 0) -> None:
     """Extend attention; `workspace` (a device uint8 tensor of at least
     rx_attn_extend_workspace(...) bytes) selects the staged path."""
     torch = _torch()
-    pool = make_pool(k_pool, v_pool)
+    pool = make_pool(k_pool, v_pool, layer)
     for t, n in ((q, "q"), (o, "o")):
         _dev(t, torch.bfloat16, n)
     _dev(lse, torch.float32, "lse")
@@ -500,9 +516,9 @@ def rx_attn_decode_workspace(batch: int, num_q_heads: int, num_kv_heads: int, he
 
 def rx_attn_decode(k_pool, v_pool, q, o, lse, req_idx, seq_len, req_to_token, max_seq_len: int,
                    sm_scale: float, plan: Optional[DevicePlan] = None, workspace=None,
-                   dev_status=None, stream=None) -> None:
+                   dev_status=None, stream=None, layer: int = 0) -> None:
     torch = _torch()
-    pool = make_pool(k_pool, v_pool)
+    pool = make_pool(k_pool, v_pool, layer)
     _dev(q, torch.bfloat16, "q")
     _dev(o, torch.bfloat16, "o")
     _dev(lse, torch.float32, "lse")
@@ -522,11 +538,11 @@ def rx_attn_decode(k_pool, v_pool, q, o, lse, req_idx, seq_len, req_to_token, ma
 
 def rx_attn_decode_static(k_pool, v_pool, q, o, lse, req_idx, seq_len, req_to_token, max_seq_len: int,
                           sm_scale: float, plan: Optional[DevicePlan] = None, dev_status=None,
-                          stream=None) -> None:
+                          stream=None, layer: int = 0) -> None:
     """rx_attn_decode with the library's fixed scratch array instead of a
     workspace (for callers that cannot allocate device memory; see rx.h)."""
     torch = _torch()
-    pool = make_pool(k_pool, v_pool)
+    pool = make_pool(k_pool, v_pool, layer)
     _dev(q, torch.bfloat16, "q")
     _dev(o, torch.bfloat16, "o")
     _dev(lse, torch.float32, "lse")
@@ -635,8 +651,8 @@ def rx_fsm_step(fsm: Fsm, logits, state, out_tokens, out_count, workspace, dev_s
 
 
 def rx_kv_store_fp8(k_pool, v_pool, k_scale: float, v_scale: float, k_new, v_new, slots, dev_status=None,
-                    stream=None) -> None:
-    """Store bf16 rows into uint8 E4M3 pools [S, Hkv, d] with per-pool scales."""
+                    stream=None, layer: int = 0) -> None:
+    """Store bf16 rows into uint8 E4M3 pools ([L,] S, Hkv, d) with per-pool scales."""
     torch = _torch()
     _dev(k_pool, torch.uint8, "k_pool")
     _dev(v_pool, torch.uint8, "v_pool")
@@ -644,12 +660,38 @@ def rx_kv_store_fp8(k_pool, v_pool, k_scale: float, v_scale: float, k_new, v_new
     _dev(v_new, torch.bfloat16, "v_new")
     _dev(slots, torch.int32, "slots")
     _dev(dev_status, torch.int32, "dev_status")
-    if k_pool.shape != v_pool.shape or k_pool.dim() != 3:
-        raise ValueError("k_pool and v_pool must both be [num_slots, num_kv_heads, head_dim]")
-    S, hkv, d = k_pool.shape
+    S, hkv, d, L = _pool_dims(k_pool, v_pool, layer)
     n = slots.numel()
     if k_new.shape != (n, hkv, d) or v_new.shape != k_new.shape:
         raise ValueError("k_new/v_new must be [n, num_kv_heads, head_dim]")
-    pool = KVPoolFp8(k_pool.data_ptr(), v_pool.data_ptr(), S, hkv, d, float(k_scale), float(v_scale))
+    pool = KVPoolFp8(k_pool.data_ptr(), v_pool.data_ptr(), S, hkv, d, float(k_scale), float(v_scale), L,
+                     int(layer))
     _check(_lib.rx_kv_store_fp8(ctypes.byref(pool), _ptr(k_new), _ptr(v_new), _ptr(slots), n,
                                 _ptr(dev_status), _stream(stream)))
+
+
+def rx_attn_decode_fp8(k_pool, v_pool, k_scale: float, v_scale: float, q, o, lse, req_idx, seq_len, req_to_token,
+                       max_seq_len: int, sm_scale: float, plan: DevicePlan, workspace, dev_status=None, stream=None,
+                       layer: int = 0) -> None:
+    """Decode attention over uint8 E4M3 pools ([L,] S, Hkv, d) with per-pool
+    scales; a decode plan whose items all go to the all-heads kernel, and a
+    workspace of rx_attn_decode_workspace(...) bytes, are required."""
+    torch = _torch()
+    _dev(k_pool, torch.uint8, "k_pool")
+    _dev(v_pool, torch.uint8, "v_pool")
+    _dev(q, torch.bfloat16, "q")
+    _dev(o, torch.bfloat16, "o")
+    _dev(lse, torch.float32, "lse")
+    for t, n in ((req_idx, "req_idx"), (seq_len, "seq_len"), (req_to_token, "req_to_token")):
+        _dev(t, torch.int32, n)
+    _dev(dev_status, torch.int32, "dev_status")
+    if workspace is not None:
+        _dev(workspace, workspace.dtype, "workspace")
+    S, hkv, d, L = _pool_dims(k_pool, v_pool, layer)
+    pool = KVPoolFp8(k_pool.data_ptr(), v_pool.data_ptr(), S, hkv, d, float(k_scale), float(v_scale), L, int(layer))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    pp = ctypes.byref(plan.struct) if plan is not None else None
+    _check(_lib.rx_attn_decode_fp8(ctypes.byref(pool), _ptr(q), _ptr(o), _ptr(lse), q.shape[1], _ptr(req_idx),
+                                   _ptr(seq_len), _ptr(req_to_token), req_to_token.shape[1], req_idx.numel(),
+                                   int(max_seq_len), pp, _ptr(workspace), ws_bytes, float(sm_scale),
+                                   _ptr(dev_status), _stream(stream)))

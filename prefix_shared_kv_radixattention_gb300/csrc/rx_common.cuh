@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -72,6 +73,32 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         "{%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D += A * B for one m16n8k16 f16 tile with fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two FP8 E4M3 codes (low byte first) -> packed f16x2, exact (every E4M3
+// value, subnormals included, is an f16 value; NaN stays NaN).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes)
+{
+    uint32_t r;
+    asm volatile("{\n .reg .b16 c;\n mov.b16 c, %1;\n cvt.rn.f16x2.e4m3x2 %0, c;\n}\n" : "=r"(r) : "h"(codes));
+    return r;
+}
+
+// Two floats -> packed f16x2 (round to nearest even), low half = lo.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi)
+{
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
 }
 
 // Two floats -> packed bf16x2 (round to nearest even), low half = lo.

@@ -54,6 +54,7 @@
 #include <mutex>
 
 #include <atomic>
+#include <type_traits>
 
 #include "rx_common.cuh"
 
@@ -129,6 +130,12 @@ struct Params {
     int wide0, n_wide;      // plan: single-request items for the wide kernel
     int *wide_counter;      // next wide item to hand out (zeroed before the launch)
     long long wait_cycles;  // bound on each pipeline wait (rx_decode_set_wait_limit)
+    // the pools as bytes, for the all-heads kernels' whole-row copies: bf16
+    // pools (row_bytes = hkv * d * 2) or FP8 code pools (hkv * d)
+    const unsigned char *kb;
+    const unsigned char *vb;
+    int64_t row_bytes;
+    float v_scale;          // FP8 pools: scale of V (K's is folded into scale_log2); 1 otherwise
 };
 
 struct Item {
@@ -888,8 +895,7 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
     int *okf = reinterpret_cast<int *>(smem + WL::OFF_OK);
     int *slotf = reinterpret_cast<int *>(smem + WL::OFF_SLOT);
     const int lane = threadIdx.x & 31;
-    const int RB = p.hkv * p.head_dim * 2;
-    const int64_t row_elems = (int64_t)p.hkv * p.head_dim;
+    const int RB = (int)p.row_bytes;
     // Under load a global load takes microseconds, so nothing on the copy
     // path waits for one: a cursor runs three stages ahead of the stage
     // being issued, and its loads (at an item boundary: the claim, the
@@ -988,10 +994,8 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
             if (lane == 0) rx::mbar_arrive(bar + 8 * (WL::B_DESC + st));
         } else if (ok) {
             const uint32_t off = (uint32_t)(st * WL::STAGE_BYTES + lane * row_stride);
-            rx::bulk_g2s(sbase + WL::OFF_K + off, p.k_pool + (int64_t)s0 * row_elems, (uint32_t)RB,
-                         bar + 8 * st);
-            rx::bulk_g2s(sbase + WL::OFF_V + off, p.v_pool + (int64_t)s0 * row_elems, (uint32_t)RB,
-                         bar + 8 * st);
+            rx::bulk_g2s(sbase + WL::OFF_K + off, p.kb + (int64_t)s0 * p.row_bytes, (uint32_t)RB, bar + 8 * st);
+            rx::bulk_g2s(sbase + WL::OFF_V + off, p.vb + (int64_t)s0 * p.row_bytes, (uint32_t)RB, bar + 8 * st);
         }
         if (end) {
             ++j;
@@ -1028,8 +1032,7 @@ __device__ void wide_copier(const Params &p, unsigned char *smem, uint32_t sbase
     const int *slotf = reinterpret_cast<const int *>(smem + WL::OFF_SLOT);
     const int4 *hdr = reinterpret_cast<const int4 *>(smem + WL::OFF_HDR);
     const int lane = threadIdx.x & 31;
-    const uint32_t RB = (uint32_t)(p.hkv * p.head_dim * 2);
-    const int64_t row_elems = (int64_t)p.hkv * p.head_dim;
+    const uint32_t RB = (uint32_t)p.row_bytes;
     const int pos = lane * NH + h;
     for (int j = 0;; ++j) {
         const int st = j % WL::STAGES;
@@ -1038,8 +1041,8 @@ __device__ void wide_copier(const Params &p, unsigned char *smem, uint32_t sbase
         const int s = pos < NP ? slotf[st * kWideMaxPos + pos] : -1;
         if (s >= 0) {
             const uint32_t off = (uint32_t)(st * WL::STAGE_BYTES + pos * row_stride);
-            rx::bulk_g2s(sbase + WL::OFF_K + off, p.k_pool + (int64_t)s * row_elems, RB, bar + 8 * st);
-            rx::bulk_g2s(sbase + WL::OFF_V + off, p.v_pool + (int64_t)s * row_elems, RB, bar + 8 * st);
+            rx::bulk_g2s(sbase + WL::OFF_K + off, p.kb + (int64_t)s * p.row_bytes, RB, bar + 8 * st);
+            rx::bulk_g2s(sbase + WL::OFF_V + off, p.vb + (int64_t)s * p.row_bytes, RB, bar + 8 * st);
         }
     }
 }
@@ -1246,11 +1249,36 @@ constexpr int kGqaRowStride = 2048 + 16;           // slot row (8 kv heads x 128
 using GqaLayout = WideLayoutT<3, kGqaNP * kGqaRowStride, 1, 32768>;
 constexpr int kGqaWarps = 8;                       // one consumer warp per kv head
 constexpr int kGqaCopyWarps = 2;                   // copy warps: 32 row copies a stage
-
+// FP8 (E4M3) pools: slot rows of one byte a value (1 KiB at 8 x 128), the
+// same q slot, and per consumer warp an f16 copy of its kv head's V rows of
+// the stage (16 rows of D halves + a 16-byte pad, for conflict-free
+// ldmatrix), placed after the layout
+constexpr int kGqaRowStride8 = 1024 + 16;
+using GqaLayout8 = WideLayoutT<3, kGqaNP * kGqaRowStride8, 1, 32768>;
+__host__ __device__ constexpr int gqa8_scratch_off() { return (GqaLayout8::OFF_ABORT + 16 + 127) / 128 * 128; }
 template <int D>
+__host__ __device__ constexpr int gqa8_scratch_rs() { return D * 2 + 16; }
+template <int D>
+__host__ __device__ constexpr int gqa8_bytes()
+{
+    return gqa8_scratch_off() + kGqaWarps * kGqaNP * gqa8_scratch_rs<D>() + 128;
+}
+static_assert(gqa8_bytes<128>() <= 227 * 1024, "shared memory budget");
+
+// F8: the pools hold E4M3 codes (rx_attn_decode_fp8).  The MMAs then run on
+// f16 operands: codes widen to f16 exactly, q converts exactly within f16's
+// range, and P rounds to f16.  K fragments are built straight from the code
+// rows: with the 16 dims of a k-step permuted so that lane group tig takes
+// dims 4 tig .. 4 tig + 3 (a dot product does not depend on the order of
+// its terms; q's fragments use the same order), one 4-byte load gives both
+// B registers.  V rows are widened into the warp's f16 scratch first, then
+// read with ldmatrix.trans as on the bf16 path.  K's scale is in
+// scale_log2, V's multiplies the output.
+template <int D, bool F8>
 __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decode_gqa_kernel(const Params p)
 {
-    using WL = GqaLayout;
+    using WL = std::conditional_t<F8, GqaLayout8, GqaLayout>;
+    constexpr int RS = F8 ? kGqaRowStride8 : kGqaRowStride;  // slot row stride in a stage
     constexpr int KS = D / 16;   // k-steps of S = Q K^T
     constexpr int DT = D / 8;    // n-tiles of O
     extern __shared__ __align__(128) unsigned char graw[];
@@ -1274,11 +1302,11 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
     }
     __syncthreads();
     if (warp == 0) {
-        wide_producer<WL, kGqaNP, kGqaCopyWarps, true>(p, smem, sbase, abort_flag, kGqaRowStride);
+        wide_producer<WL, kGqaNP, kGqaCopyWarps, true>(p, smem, sbase, abort_flag, RS);
         return;
     }
     if (warp <= kGqaCopyWarps) {
-        wide_copier<WL, kGqaNP, kGqaCopyWarps>(p, smem, sbase, abort_flag, kGqaRowStride, warp - 1);
+        wide_copier<WL, kGqaNP, kGqaCopyWarps>(p, smem, sbase, abort_flag, RS, warp - 1);
         return;
     }
     // consumer warp: kv head g.  Row m = i * G + j of its m16 tile is q head
@@ -1305,7 +1333,7 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
             const int r = gid + half * 8;
             if (r >= M) continue;
             const int64_t orow = (int64_t)ob[half] * p.hq + (int64_t)g * G + r % G;
-            const float inv = 1.f / ls[half];
+            const float inv = F8 ? p.v_scale / ls[half] : 1.f / ls[half];
             if (fin) {
                 bf16 *dst = p.o + orow * D;
 #pragma unroll
@@ -1353,15 +1381,35 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
             // the query rows came with this stage: A fragments of rows
             // 0 .. M - 1 (rows past M read row 0 and are zeroed), then hand
             // the q slot back
-            const int qm = (lane & 15) < M ? (lane & 15) : 0;
-            const unsigned char *qs =
-                smem + WL::OFF_Q + (size_t)(qm / G) * p.hq * D * 2 + (size_t)(g * G + qm % G) * D * 2;
+            if constexpr (F8) {
+                // rows gid and gid + 8, dims 4 tig .. 4 tig + 3 of every
+                // k-step (the permuted order), bf16 -> f16
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const int ch = ks * 2 + (lane >> 4);
-                rx::ldmatrix_x4(rx::smem_u32(qs + ch * 16), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
-                if (gid >= M) qf[ks][0] = qf[ks][2] = 0u;
-                if (gid + 8 >= M) qf[ks][1] = qf[ks][3] = 0u;
+                for (int half = 0; half < 2; ++half) {
+                    const int r = gid + half * 8;
+                    const int qm = r < M ? r : 0;
+                    const unsigned char *qs =
+                        smem + WL::OFF_Q + (size_t)(qm / G) * p.hq * D * 2 + (size_t)(g * G + qm % G) * D * 2;
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const uint2 w = *reinterpret_cast<const uint2 *>(qs + (ks * 16 + 4 * tig) * 2);
+                        const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.x));
+                        const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.y));
+                        qf[ks][half] = r < M ? rx::pack_f16(x01.x, x01.y) : 0u;
+                        qf[ks][half + 2] = r < M ? rx::pack_f16(x23.x, x23.y) : 0u;
+                    }
+                }
+            } else {
+                const int qm = (lane & 15) < M ? (lane & 15) : 0;
+                const unsigned char *qs =
+                    smem + WL::OFF_Q + (size_t)(qm / G) * p.hq * D * 2 + (size_t)(g * G + qm % G) * D * 2;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int ch = ks * 2 + (lane >> 4);
+                    rx::ldmatrix_x4(rx::smem_u32(qs + ch * 16), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+                    if (gid >= M) qf[ks][0] = qf[ks][2] = 0u;
+                    if (gid + 8 >= M) qf[ks][1] = qf[ks][3] = 0u;
+                }
             }
             __syncwarp();
             if (lane == 0) rx::mbar_arrive(bar + 8 * (2 * WL::STAGES));
@@ -1375,13 +1423,24 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
         uint32_t vmask = 0;  // bit i: position i holds a valid row
 #pragma unroll
         for (int i = 0; i < kGqaNP; ++i) vmask |= (i < n && okp[i] != 0) ? (1u << i) : 0u;
-        const unsigned char *kt = smem + WL::OFF_K + st * WL::STAGE_BYTES + g * D * 2;
-        const unsigned char *vt = smem + WL::OFF_V + st * WL::STAGE_BYTES + g * D * 2;
+        constexpr int EB = F8 ? 1 : 2;  // bytes a value in the pools
+        const unsigned char *kt = smem + WL::OFF_K + st * WL::STAGE_BYTES + g * D * EB;
+        const unsigned char *vt = smem + WL::OFF_V + st * WL::STAGE_BYTES + g * D * EB;
         // S = Q K^T over the stage's 16 positions (two n-tiles)
         float sc[2][4];
 #pragma unroll
         for (int i = 0; i < 2; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-        {
+        if constexpr (F8) {
+            // B of n-tile nt: position nt * 8 + gid, dims 4 tig .. 4 tig + 3
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint32_t c4 = *reinterpret_cast<const uint32_t *>(kt + (nt * 8 + gid) * RS + ks * 16 + 4 * tig);
+                    rx::mma_f16_16816(sc[nt], qf[ks], rx::e4m3x2_to_f16x2((uint16_t)(c4 & 0xffffu)),
+                                      rx::e4m3x2_to_f16x2((uint16_t)(c4 >> 16)));
+                }
+        } else {
             const int key = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
@@ -1431,17 +1490,59 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
             l_r[1] += sc[nt][2] + sc[nt][3];
         }
         uint32_t a[4];
-        a[0] = rx::pack_bf16(sc[0][0], sc[0][1]);
-        a[1] = rx::pack_bf16(sc[0][2], sc[0][3]);
-        a[2] = rx::pack_bf16(sc[1][0], sc[1][1]);
-        a[3] = rx::pack_bf16(sc[1][2], sc[1][3]);
+        if constexpr (F8) {
+            a[0] = rx::pack_f16(sc[0][0], sc[0][1]);
+            a[1] = rx::pack_f16(sc[0][2], sc[0][3]);
+            a[2] = rx::pack_f16(sc[1][0], sc[1][1]);
+            a[3] = rx::pack_f16(sc[1][2], sc[1][3]);
+        } else {
+            a[0] = rx::pack_bf16(sc[0][0], sc[0][1]);
+            a[1] = rx::pack_bf16(sc[0][2], sc[0][3]);
+            a[2] = rx::pack_bf16(sc[1][0], sc[1][1]);
+            a[3] = rx::pack_bf16(sc[1][2], sc[1][3]);
+        }
         // V rows of positions tig*2, tig*2+1 (b0, b2) and tig*2+8, +9 (b1, b3):
         // zero the ones that were never written in this stage
         const uint32_t vz0 = (((vmask >> (tig * 2)) & 1u) ? 0x0000ffffu : 0u) |
                              (((vmask >> (tig * 2 + 1)) & 1u) ? 0xffff0000u : 0u);
         const uint32_t vz1 = (((vmask >> (tig * 2 + 8)) & 1u) ? 0x0000ffffu : 0u) |
                              (((vmask >> (tig * 2 + 9)) & 1u) ? 0xffff0000u : 0u);
-        {
+        if constexpr (F8) {
+            // widen this kv head's 16 V rows into the warp's f16 scratch:
+            // lane l takes half l & 1 of row l / 2 (D / 2 codes)
+            unsigned char *scr = smem + gqa8_scratch_off() + (warp - 1 - kGqaCopyWarps) * kGqaNP * gqa8_scratch_rs<D>();
+            {
+                const int r = lane >> 1, c0 = (lane & 1) * (D / 2);
+#pragma unroll
+                for (int c = 0; c < D / 2; c += 16) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(vt + r * RS + c0 + c);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                    uint32_t h[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        h[2 * k] = rx::e4m3x2_to_f16x2((uint16_t)(ws[k] & 0xffffu));
+                        h[2 * k + 1] = rx::e4m3x2_to_f16x2((uint16_t)(ws[k] >> 16));
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(scr + r * gqa8_scratch_rs<D>() + (c0 + c) * 2);
+                    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+                }
+            }
+            __syncwarp();
+            const int key = (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+            for (int dp = 0; dp < D / 16; ++dp) {
+                const int ch = dp * 2 + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                rx::ldmatrix_x4_trans(rx::smem_u32(scr + key * gqa8_scratch_rs<D>() + ch * 16), b0, b1, b2, b3);
+                b0 &= vz0;
+                b1 &= vz1;
+                b2 &= vz0;
+                b3 &= vz1;
+                rx::mma_f16_16816(oacc[2 * dp], a, b0, b1);
+                rx::mma_f16_16816(oacc[2 * dp + 1], a, b2, b3);
+            }
+        } else {
             const int key = (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
             for (int dp = 0; dp < D / 16; ++dp) {
@@ -1493,18 +1594,18 @@ int launch_on(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t sm
     return RX_OK;
 }
 
-template <int D>
+template <int D, bool F8 = false>
 int launch_decode_gqa(const Params &p, cudaStream_t st, bool dependent)
 {
+    constexpr int bytes = F8 ? gqa8_bytes<D>() : GqaLayout::BYTES;
     static bool configured = false;
     if (!configured) {
-        RX_CUDA_CHECK(cudaFuncSetAttribute(decode_gqa_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           GqaLayout::BYTES));
+        RX_CUDA_CHECK(cudaFuncSetAttribute(decode_gqa_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           bytes));
         configured = true;
     }
     const int grid = p.n_wide < num_sms() ? p.n_wide : num_sms();
-    return launch_on(decode_gqa_kernel<D>, grid, 32 * (1 + kGqaCopyWarps + kGqaWarps), GqaLayout::BYTES, st,
-                     dependent, p);
+    return launch_on(decode_gqa_kernel<D, F8>, grid, 32 * (1 + kGqaCopyWarps + kGqaWarps), bytes, st, dependent, p);
 }
 
 template <int D, int LOG_NP, int HPW, int CW>
@@ -1639,12 +1740,15 @@ static int check_decode_args(const char *who, const rx_kv_pool *pool, const void
     return RX_OK;
 }
 
-extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, float *lse,
+extern "C" int rx_attn_decode(const rx_kv_pool *pool_in, const void *q, void *o, float *lse,
                               int32_t hq, const int32_t *req_idx, const int32_t *seq_len,
                               const int32_t *rtt, int64_t rtt_stride, int32_t batch,
                               int32_t max_seq_len, const rx_decode_plan *plan, void *workspace,
                               size_t ws_bytes, float sm_scale, int32_t *dev_status, void *stream)
 {
+    rx_kv_pool layer_view;
+    if (const int rc = rx_pool_layer(pool_in, &layer_view, 0, "rx_attn_decode")) return rc;
+    const rx_kv_pool *pool = pool_in ? &layer_view : nullptr;
     const int chk = check_decode_args("rx_attn_decode", pool, q, o, lse, hq, req_idx, seq_len, rtt, rtt_stride,
                                       batch, max_seq_len, plan, sm_scale);
     if (chk != RX_OK) return chk;
@@ -1656,6 +1760,10 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
     p.lse = lse;
     p.k_pool = (const bf16 *)pool->k;
     p.v_pool = (const bf16 *)pool->v;
+    p.kb = (const unsigned char *)pool->k;
+    p.vb = (const unsigned char *)pool->v;
+    p.row_bytes = (int64_t)pool->num_kv_heads * pool->head_dim * 2;
+    p.v_scale = 1.f;
     p.num_slots = pool->num_slots;
     p.hq = hq;
     p.hkv = pool->num_kv_heads;
@@ -1726,6 +1834,96 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, fl
 }
 
 // ---------------------------------------------------------------------------
+// Decode over FP8 (E4M3) pools
+// ---------------------------------------------------------------------------
+//
+// The all-heads GQA kernel reads whole slot rows of codes (half the bytes of
+// a bf16 pool) and widens them to f16 on the way to the tensor cores; the
+// plan's items are the same as for a bf16 pool of the same head counts, and
+// split rows merge as usual.  K's scale joins the score scale, V's the
+// output.
+
+extern "C" int rx_attn_decode_fp8(const rx_kv_pool_fp8 *pool_in, const void *q, void *o, float *lse,
+                                  int32_t hq, const int32_t *req_idx, const int32_t *seq_len,
+                                  const int32_t *rtt, int64_t rtt_stride, int32_t batch, int32_t max_seq_len,
+                                  const rx_decode_plan *plan, void *workspace, size_t ws_bytes, float sm_scale,
+                                  int32_t *dev_status, void *stream)
+{
+    rx_kv_pool_fp8 layer_view;
+    if (const int rc = rx_pool_layer(pool_in, &layer_view, 1, "rx_attn_decode_fp8")) return rc;
+    const rx_kv_pool_fp8 *pool = pool_in ? &layer_view : nullptr;
+    if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0 ||
+        !(pool->k_scale > 0.f) || !(pool->v_scale > 0.f))
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode_fp8: invalid pool");
+    const int D = pool->head_dim;
+    if ((D != 64 && D != 128) || !rx_gqa_heads(hq, pool->num_kv_heads))
+        return rx_set_error(RX_ERR_UNSUPPORTED,
+                            "rx_attn_decode_fp8: %d q heads over %d kv heads, head_dim %d (supported: 8 kv heads "
+                            "with 2, 4, 8 or 16 q heads each, head_dim 64 or 128)",
+                            hq, pool->num_kv_heads, D);
+    if (!q || !o || !req_idx || !seq_len || !rtt || rtt_stride <= 0 || rtt_stride > INT32_MAX || batch < 0 ||
+        max_seq_len <= 0 || max_seq_len > rtt_stride || !(sm_scale > 0.f))
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode_fp8: invalid argument");
+    if (rx_misaligned16(q) || rx_misaligned16(o) || rx_misaligned16(pool->k) || rx_misaligned16(pool->v) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode_fp8: q, o and the pools must be 16-byte aligned");
+    if (!plan || !plan->order || !plan->nparts || !plan->items || plan->n_items < 0 || plan->max_parts < 1 ||
+        plan->n_wide < 0 || plan->n_wide > plan->n_items)
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode_fp8: a valid decode plan is required");
+    if (plan->n_wide != plan->n_items)
+        return rx_set_error(RX_ERR_UNSUPPORTED,
+                            "rx_attn_decode_fp8: the plan has %d items for the per-head kernel; over FP8 pools "
+                            "every item must go to the all-heads kernel (shared segments in at most %d groups)",
+                            plan->n_items - plan->n_wide, RX_DECODE_MAX_GROUPS);
+    if (batch == 0 || plan->n_items == 0) return RX_OK;
+    Params p{};
+    p.q = (const bf16 *)q;
+    p.o = (bf16 *)o;
+    p.lse = lse;
+    p.kb = (const unsigned char *)pool->k;
+    p.vb = (const unsigned char *)pool->v;
+    p.row_bytes = (int64_t)pool->num_kv_heads * D;
+    p.v_scale = pool->v_scale;
+    p.num_slots = pool->num_slots;
+    p.hq = hq;
+    p.hkv = pool->num_kv_heads;
+    p.G = hq / pool->num_kv_heads;
+    p.head_dim = D;
+    p.req_idx = req_idx;
+    p.seq_len = seq_len;
+    p.rtt = rtt;
+    p.rtt_stride = rtt_stride;
+    p.batch = batch;
+    p.scale_log2 = sm_scale * pool->k_scale * rx::kLog2e;
+    p.status = dev_status;
+    const long long limit = g_decode_wait_cycles.load();
+    p.wait_cycles = limit > 0 ? limit : rx::kWaitCycles;
+    p.order = plan->order;
+    p.nparts = plan->nparts;
+    p.items = plan->items;
+    p.max_parts = plan->max_parts;
+    p.n_wide = plan->n_wide;
+    p.wide0 = 0;
+    const size_t need = rx_attn_decode_workspace(batch, hq, p.hkv, D, max_seq_len, plan);
+    if (!workspace || ws_bytes < need)
+        return rx_set_error(RX_ERR_CAPACITY, "rx_attn_decode_fp8: workspace needs %zu bytes, got %zu", need,
+                            ws_bytes);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode_fp8: workspace must be 256-byte aligned");
+    const bool merge = p.max_parts > 1;
+    if (merge) {
+        p.ws_o = (float *)workspace;
+        p.ws_lse = p.ws_o + (int64_t)batch * hq * p.max_parts * D;
+    }
+    p.wide_counter = reinterpret_cast<int *>(static_cast<char *>(workspace) + need - 256);
+    cudaStream_t st = (cudaStream_t)stream;
+    RX_CUDA_CHECK(cudaMemsetAsync(p.wide_counter, 0, sizeof(int), st));
+    int rc = D == 128 ? launch_decode_gqa<128, true>(p, st, false) : launch_decode_gqa<64, true>(p, st, false);
+    if (rc != RX_OK || !merge) return rc;
+    return D == 128 ? launch_merge<128>(p, 1, st) : launch_merge<64>(p, 1, st);
+}
+
+// ---------------------------------------------------------------------------
 // Decode without a caller workspace
 // ---------------------------------------------------------------------------
 //
@@ -1751,13 +1949,16 @@ std::mutex g_scratch_mu;
 void *g_scratch_addr[kMaxDevices] = {};
 }  // namespace
 
-extern "C" int rx_attn_decode_static(const rx_kv_pool *pool, const void *q, void *o, float *lse,
+extern "C" int rx_attn_decode_static(const rx_kv_pool *pool_in, const void *q, void *o, float *lse,
                                      int32_t num_q_heads, const int32_t *req_idx,
                                      const int32_t *seq_len, const int32_t *req_to_token,
                                      int64_t rtt_stride, int32_t batch, int32_t max_seq_len,
                                      const rx_decode_plan *plan_or_null, float sm_scale,
                                      int32_t *dev_status, void *stream)
 {
+    rx_kv_pool layer_view;
+    if (const int rc = rx_pool_layer(pool_in, &layer_view, 0, "rx_attn_decode_static")) return rc;
+    const rx_kv_pool *pool = pool_in ? &layer_view : nullptr;
     // the same checks as rx_attn_decode first, so that a malformed call is
     // reported as such rather than as a batch too big for the array
     const int chk = check_decode_args("rx_attn_decode_static", pool, q, o, lse, num_q_heads, req_idx, seq_len,

@@ -817,13 +817,16 @@ int launch_extend(const XParams &p, dim3 grid, cudaStream_t st)
 
 }  // namespace
 
-extern "C" int rx_attn_extend(const rx_kv_pool *pool, const void *q, void *o, float *lse,
+extern "C" int rx_attn_extend(const rx_kv_pool *pool_in, const void *q, void *o, float *lse,
                               int32_t hq, const int32_t *qo_indptr, const int32_t *req_idx,
                               const int32_t *prefix_len, const int32_t *extend_len,
                               const int32_t *rtt, int64_t rtt_stride, int32_t batch,
                               int32_t max_extend_len, void *workspace, size_t ws_bytes, float sm_scale,
                               int32_t *dev_status, void *stream)
 {
+    rx_kv_pool layer_view;
+    if (const int rc = rx_pool_layer(pool_in, &layer_view, 0, "rx_attn_extend")) return rc;
+    const rx_kv_pool *pool = pool_in ? &layer_view : nullptr;
     int rc = check_pool(pool);
     if (rc != RX_OK) return rc;
     if (!q || !o || !qo_indptr || !req_idx || !prefix_len || !extend_len || !rtt ||

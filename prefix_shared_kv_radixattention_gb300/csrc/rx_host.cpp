@@ -72,6 +72,33 @@ static void count_alloc()
 }
 extern "C" int rx_version(void) { return RX_ABI_VERSION; }
 
+// Layered pools: one layer's rows are num_slots * num_kv_heads * head_dim
+// elements (bf16, or one byte for FP8 codes) after the previous layer's.
+template <class Pool>
+static int pool_layer(const Pool *in, Pool *out, int64_t elem_bytes, const char *who)
+{
+    *out = *in;
+    const int32_t L = in->num_layers;
+    if (L < 0 || in->layer < 0 || in->layer >= (L > 1 ? L : 1))
+        return rx_set_error(RX_ERR_INVALID, "%s: layer %d of a pool of %d layers", who, in->layer, L);
+    if (in->layer > 0) {
+        const int64_t off = (int64_t)in->layer * in->num_slots * in->num_kv_heads * in->head_dim * elem_bytes;
+        out->k = static_cast<char *>(in->k) + off;
+        out->v = static_cast<char *>(in->v) + off;
+    }
+    out->num_layers = 0;
+    out->layer = 0;
+    return RX_OK;
+}
+
+int rx_pool_layer(const void *in, void *out, int fp8, const char *who)
+{
+    if (!in) return RX_OK;
+    if (fp8)
+        return pool_layer(static_cast<const rx_kv_pool_fp8 *>(in), static_cast<rx_kv_pool_fp8 *>(out), 1, who);
+    return pool_layer(static_cast<const rx_kv_pool *>(in), static_cast<rx_kv_pool *>(out), 2, who);
+}
+
 // ---------------------------------------------------------------------------
 // radix tree
 // ---------------------------------------------------------------------------

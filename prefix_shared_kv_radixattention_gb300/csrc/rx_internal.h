@@ -3,7 +3,7 @@
 
 #include <stdint.h>
 
-#define RX_ABI_VERSION 1
+#define RX_ABI_VERSION 2
 
 // Longest position range one decode work item covers (the plan builder and
 // the no-plan split both stay at or below it).
@@ -47,6 +47,12 @@ static inline bool rx_gqa_heads(int32_t hq, int32_t hkv)
 
 // Sets the thread-local message returned by rx_last_error and returns code.
 int rx_set_error(int code, const char *fmt, ...);
+
+// The one-layer view of a pool: for a layered pool, k and v advanced to the
+// call's layer (num_layers and layer of the result are 0).  RX_ERR_INVALID
+// (message naming `who`) for a layer outside the pool.  A null `in` is
+// passed through for the caller's own checks.
+int rx_pool_layer(const void *in, void *out, int fp8, const char *who);
 
 // Host entry points that allocate wrap their body in RX_TRY ... RX_CATCH so
 // that no exception crosses the C ABI.

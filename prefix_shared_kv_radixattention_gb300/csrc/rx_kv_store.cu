@@ -94,9 +94,12 @@ int num_sms()
 
 }  // namespace
 
-extern "C" int rx_kv_store(const rx_kv_pool *pool, const void *k_new, const void *v_new,
+extern "C" int rx_kv_store(const rx_kv_pool *pool_in, const void *k_new, const void *v_new,
                            const int32_t *slots, int64_t n, int32_t *dev_status, void *stream)
 {
+    rx_kv_pool layer_view;
+    if (const int rc = rx_pool_layer(pool_in, &layer_view, 0, "rx_kv_store")) return rc;
+    const rx_kv_pool *pool = pool_in ? &layer_view : nullptr;
     if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0 ||
         pool->head_dim <= 0 || n < 0 || (n > 0 && (!k_new || !v_new || !slots)))
         return rx_set_error(RX_ERR_INVALID, "rx_kv_store: invalid argument");
@@ -121,9 +124,12 @@ extern "C" int rx_kv_store(const rx_kv_pool *pool, const void *k_new, const void
     return RX_OK;
 }
 
-extern "C" int rx_kv_store_fp8(const rx_kv_pool_fp8 *pool, const void *k_new, const void *v_new,
+extern "C" int rx_kv_store_fp8(const rx_kv_pool_fp8 *pool_in, const void *k_new, const void *v_new,
                                const int32_t *slots, int64_t n, int32_t *dev_status, void *stream)
 {
+    rx_kv_pool_fp8 layer_view;
+    if (const int rc = rx_pool_layer(pool_in, &layer_view, 1, "rx_kv_store_fp8")) return rc;
+    const rx_kv_pool_fp8 *pool = pool_in ? &layer_view : nullptr;
     if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0 ||
         pool->head_dim <= 0 || n < 0 || (n > 0 && (!k_new || !v_new || !slots)) ||
         !(pool->k_scale > 0.f) || !(pool->v_scale > 0.f))

@@ -229,10 +229,13 @@ extern "C" int rx_rope(void *x, const int32_t *pos, int64_t n, int32_t heads, in
     return RX_OK;
 }
 
-extern "C" int rx_kv_store_rope(const rx_kv_pool *pool, const void *k_new, const void *v_new,
+extern "C" int rx_kv_store_rope(const rx_kv_pool *pool_in, const void *k_new, const void *v_new,
                                 const int32_t *slots, const int32_t *pos, int64_t n, double base,
                                 int32_t *dev_status, void *stream)
 {
+    rx_kv_pool layer_view;
+    if (const int rc = rx_pool_layer(pool_in, &layer_view, 0, "rx_kv_store_rope")) return rc;
+    const rx_kv_pool *pool = pool_in ? &layer_view : nullptr;
     RopeTab tab;
     if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0 || n < 0 ||
         (n > 0 && (!k_new || !v_new || !slots || !pos)))

@@ -2,8 +2,10 @@
 the format's definition, round-to-nearest-even at midpoints, saturation,
 underflow, and a brute-force nearest-code check."""
 import numpy as np
+import pytest
 
 from oracle import fp8
+from prefix_shared_kv_radixattention_gb300 import inputs
 
 
 def test_table_values():
@@ -88,3 +90,58 @@ def test_quantize_with_scale():
     xs = np.random.default_rng(1).uniform(0.1, 200.0, 1000).astype(np.float32)
     r = fp8.dequantize(fp8.quantize_rows(xs, 1.0), 1.0)
     assert np.max(np.abs(r - xs) / xs) <= 2.0 ** -4
+
+
+# ---------------------------------------------------------------------------
+# attention over FP8 pools
+# ---------------------------------------------------------------------------
+
+
+def _brute_fp8(q_bits, kc, vc, ks, vs, rtt, row, kend, scale):
+    """The definition written out densely in numpy fp64 on the dequantized
+    values: softmax over keys 0 .. kend - 1 of the gathered rows."""
+    import oracle  # noqa: F401  (package import only)
+    qf = inputs.bf16_to_f32(q_bits).astype(np.float64)
+    n, hq, d = qf.shape
+    hkv = kc.shape[1]
+    G = hq // hkv
+    o = np.zeros((n, hq, d))
+    lse = np.zeros((n, hq))
+    for i in range(n):
+        slots = rtt[row[i], :kend[i]]
+        K = fp8.dequantize(kc[slots], ks)
+        V = fp8.dequantize(vc[slots], vs)
+        for h in range(hq):
+            s = K[:, h // G, :] @ qf[i, h] * scale
+            m = s.max()
+            w = np.exp(s - m)
+            o[i, h] = w @ V[:, h // G, :] / w.sum()
+            lse[i, h] = m + np.log(w.sum())
+    return o, lse
+
+
+@pytest.mark.parametrize("ks,vs", [(1.0, 1.0), (0.37, 2.6), (1 / 64, 48.0)])
+def test_fp8_attention_is_the_definition_on_dequantized_values(ks, vs):
+    rng = np.random.default_rng(int(ks * 1000) + 3)
+    S, hkv, hq, d = 40, 2, 4, 16
+    kc = rng.integers(0, 0x7F, size=(S, hkv, d)).astype(np.uint8) | (rng.integers(0, 2, size=(S, hkv, d)) << 7).astype(np.uint8)
+    vc = rng.integers(0, 0x7F, size=(S, hkv, d)).astype(np.uint8) | (rng.integers(0, 2, size=(S, hkv, d)) << 7).astype(np.uint8)
+    kc[kc & 0x7F == 0x7F] = 0                       # no NaN codes
+    vc[vc & 0x7F == 0x7F] = 0
+    rtt = np.stack([rng.permutation(S)[:24] for _ in range(3)]).astype(np.int32)
+    q = inputs.randn_bf16(rng, (5, hq, d))
+    row = np.array([0, 1, 2, 0, 2], np.int32)
+    kend = np.array([1, 7, 24, 13, 2], np.int32)
+    scale = 0.25
+    o, lse = fp8.attention(q, kc, vc, ks, vs, rtt, row, np.zeros(5, np.int32), kend, scale)
+    bo, blse = _brute_fp8(q, kc, vc, ks, vs, rtt, row, kend, scale)
+    assert np.allclose(o, bo, rtol=1e-12, atol=1e-12 * max(1.0, vs))
+    assert np.allclose(lse, blse, rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_bf16_bits_are_exact():
+    codes = np.arange(256, dtype=np.uint8)
+    finite = ~np.isnan(fp8.decode(codes))
+    back = inputs.bf16_to_f32(fp8.bf16_bits(codes)).astype(np.float64)
+    assert np.array_equal(back[finite], fp8.decode(codes)[finite])
+    assert np.isnan(back[~finite]).all()

@@ -61,3 +61,102 @@ def test_store_fp8_bad_slot_is_flagged():
     got = kd.cpu().numpy()
     assert np.array_equal(got[5], fp8.quantize_rows(inputs.bf16_to_f32(rows[0]), 1.0))
     assert not np.delete(got, 5, axis=0).any()
+
+
+# ---------------------------------------------------------------------------
+# decode over FP8 pools (rx_attn_decode_fp8)
+# ---------------------------------------------------------------------------
+
+
+def _fp8_problem(prob, k_scale, v_scale, seed):
+    """Host code pools: every row the oracle's quantizer makes of N(0, 1)
+    bf16 values (the cached rows here, the step's new rows as the store
+    must); the device pools get the cached codes uploaded and the new rows
+    through rx_kv_store_fp8."""
+    from tests import _gpu as g
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    rng = np.random.default_rng(seed)
+    S, hkv, d = prob.num_slots, prob.hkv, prob.d
+    kc = fp8.quantize_rows(inputs.bf16_to_f32(inputs.randn_bf16(rng, (S, hkv, d))), k_scale)
+    vc = fp8.quantize_rows(inputs.bf16_to_f32(inputs.randn_bf16(rng, (S, hkv, d))), v_scale)
+    kd, vd = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rx.rx_kv_store_fp8(kd, vd, k_scale, v_scale, g.to_dev(prob.new_k), g.to_dev(prob.new_v), g.i32(prob.new_slots),
+                       status)
+    kc[prob.new_slots] = fp8.quantize_rows(inputs.bf16_to_f32(prob.new_k), k_scale)
+    vc[prob.new_slots] = fp8.quantize_rows(inputs.bf16_to_f32(prob.new_v), v_scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(kd.cpu().numpy(), kc) and np.array_equal(vd.cpu().numpy(), vc)
+    return kd, vd, kc, vc, status
+
+
+def _decode_fp8(prob, kd, vd, ks, vs, status, kv_chunk=0, plan_len=None):
+    from tests import _gpu as g
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    B = len(prob.dec_req_idx)
+    lens = prob.dec_seq_len if plan_len is None else plan_len
+    buf, info = rx.rx_decode_plan_build(prob.req_to_token, prob.dec_req_idx, lens, prob.hq, prob.hkv, kv_chunk, 16)
+    assert info.n_wide == info.n_items
+    plan = rx.plan_to_device(buf, info, B)
+    max_len = int(prob.dec_seq_len.max())
+    ws = torch.empty(max(rx.rx_attn_decode_workspace(B, prob.hq, prob.hkv, prob.d, max_len, plan), 256),
+                     dtype=torch.uint8, device="cuda")
+    q = g.to_dev(prob.q_dec)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, prob.hq), dtype=torch.float32, device="cuda")
+    rx.rx_attn_decode_fp8(kd, vd, ks, vs, q, o, lse, g.i32(prob.dec_req_idx), g.i32(prob.dec_seq_len),
+                          g.i32(prob.req_to_token), max_len, prob.sm_scale, plan, ws, status)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy(), lse.cpu().numpy(), info
+
+
+@pytest.mark.parametrize("hq,d,ks,vs", [(16, 128, 1.0, 1.0), (32, 128, 0.37, 2.5), (64, 128, 1.5, 0.25),
+                                        (128, 64, 0.5, 1.0), (32, 64, 2.0, 0.75)])
+def test_decode_fp8_ragged_matches_oracle(hq, d, ks, vs):
+    """Ragged batches with shared prefixes, 8 kv heads, G = 2 .. 16: grouped
+    shared segments and single-request pieces, split rows merged."""
+    from tests import _gpu as g
+    prob = inputs.ragged(500 + hq + d, hq=hq, hkv=8, d=d, n_groups=3, per_group=3, shared_max=400,
+                         private_max=300, extend_max=1, decode=True, num_slots=6000)
+    kd, vd, kc, vc, status = _fp8_problem(prob, ks, vs, hq + d)
+    for chunk in (64, 0):
+        o, lse, info = _decode_fp8(prob, kd, vd, ks, vs, status, kv_chunk=chunk)
+        ro, rl = fp8.decode_rows(prob.q_dec, kc, vc, ks, vs, prob.req_to_token, prob.dec_req_idx, prob.dec_seq_len,
+                                 prob.sm_scale)
+        g.compare(o, ro, f"fp8 decode G={hq // 8} d={d} chunk {chunk}")
+        g.compare_lse(lse, rl, f"fp8 decode G={hq // 8} d={d} chunk {chunk}")
+    assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("shape", ["few_shot", "tree_of_thought"])
+def test_decode_fp8_workload_shapes(shape):
+    """The few-shot structure (one prefix shared by every request, long
+    private parts) and the tree-of-thought one (nested shared segments),
+    with GQA 32/8 heads; the plan built a token earlier serves the step."""
+    from tests import _gpu as g
+    if shape == "few_shot":
+        prob = inputs.few_shot_decode(hq=32, hkv=8, d=128, batch=24, shared=512, private=200, num_slots=40000)
+    else:
+        prob = inputs.tree_of_thought_decode(depth=3, fanout=3, edge=120, num_slots=40000)
+    kd, vd, kc, vc, status = _fp8_problem(prob, 0.8, 1.25, 17)
+    for plan_len in (None, prob.dec_seq_len - 1):
+        o, lse, info = _decode_fp8(prob, kd, vd, 0.8, 1.25, status, plan_len=plan_len)
+        assert info.n_segments > 0
+        ro, rl = fp8.decode_rows(prob.q_dec, kc, vc, 0.8, 1.25, prob.req_to_token, prob.dec_req_idx,
+                                 prob.dec_seq_len, prob.sm_scale)
+        g.compare(o, ro, f"fp8 decode {shape}")
+        g.compare_lse(lse, rl, f"fp8 decode {shape}")
+    assert int(status.item()) == 0
+
+
+def test_decode_fp8_bad_slot_is_flagged():
+    from tests import _gpu as g
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.few_shot_decode(hq=32, hkv=8, d=128, batch=5, shared=60, private=40, num_slots=1024)
+    prob.req_to_token = prob.req_to_token.copy()
+    prob.req_to_token[3, 80] = prob.num_slots + 9
+    kd, vd, kc, vc, status = _fp8_problem(prob, 1.0, 1.0, 3)
+    o, _, _ = _decode_fp8(prob, kd, vd, 1.0, 1.0, status, kv_chunk=64)
+    assert int(status.item()) & rx.RX_DEV_BAD_SLOT
+    assert np.isfinite(o).all()

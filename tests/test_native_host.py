@@ -39,7 +39,54 @@ def test_exports_every_declared_function():
     lib = rx.library()
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, missing
-    assert rx.version() == 1
+    assert rx.version() == 2
+
+
+def test_layer_outside_the_pool_is_rejected_before_any_launch():
+    """Every pool entry point resolves the call's layer first: a layer
+    outside the pool is RX_ERR_INVALID, returned before any device work (the
+    pointers here are never dereferenced)."""
+    import ctypes
+    lib = rx.library()
+    fake = 0x100000
+    for L, layer in ((2, 2), (0, 1), (1, 1), (3, -1), (-1, 0)):
+        pool = rx.KVPool(fake, fake, 64, 2, 64, L, layer)
+        p8 = rx.KVPoolFp8(fake, fake, 64, 2, 64, 1.0, 1.0, L, layer)
+        P = ctypes.c_void_p(fake)
+        calls = [
+            lambda: lib.rx_kv_store(ctypes.byref(pool), P, P, P, 4, None, None),
+            lambda: lib.rx_kv_store_fp8(ctypes.byref(p8), P, P, P, 4, None, None),
+            lambda: lib.rx_kv_store_rope(ctypes.byref(pool), P, P, P, P, 4, 10000.0, None, None),
+            lambda: lib.rx_attn_extend(ctypes.byref(pool), P, P, None, 2, P, P, P, P, P, 64, 1, 8, None, 0,
+                                       ctypes.c_float(0.125), None, None),
+            lambda: lib.rx_attn_decode(ctypes.byref(pool), P, P, None, 2, P, P, P, 64, 1, 8, None, None, 0,
+                                       ctypes.c_float(0.125), None, None),
+            lambda: lib.rx_attn_decode_static(ctypes.byref(pool), P, P, None, 2, P, P, P, 64, 1, 8, None,
+                                              ctypes.c_float(0.125), None, None),
+        ]
+        for call in calls:
+            assert call() == rx.RX_ERR_INVALID, (L, layer)
+            assert "layer" in rx.last_error()
+
+
+def test_fp8_decode_rejects_unsupported_heads_and_missing_plan():
+    """rx_attn_decode_fp8 checks its shapes and plan before any device work."""
+    import ctypes
+    lib = rx.library()
+    fake = 0x100000
+    P = ctypes.c_void_p(fake)
+    plan = rx.DecodePlan(fake, fake, fake, 4, 1, 4)
+    for hq, hkv, d, pl, code in ((32, 32, 128, plan, rx.RX_ERR_UNSUPPORTED), (32, 8, 96, plan, rx.RX_ERR_UNSUPPORTED),
+                                 (24, 8, 128, plan, rx.RX_ERR_UNSUPPORTED), (32, 8, 128, None, rx.RX_ERR_INVALID)):
+        pool = rx.KVPoolFp8(fake, fake, 64, hkv, d, 1.0, 1.0, 0, 0)
+        rc = lib.rx_attn_decode_fp8(ctypes.byref(pool), P, P, None, hq, P, P, P, 64, 2, 8,
+                                    ctypes.byref(pl) if pl is not None else None, P, 1 << 20, ctypes.c_float(0.1),
+                                    None, None)
+        assert rc == code, (hq, hkv, d, rx.last_error())
+    per_head = rx.DecodePlan(fake, fake, fake, 4, 1, 3)       # one item for the per-head kernel
+    pool = rx.KVPoolFp8(fake, fake, 64, 8, 128, 1.0, 1.0, 0, 0)
+    assert lib.rx_attn_decode_fp8(ctypes.byref(pool), P, P, None, 32, P, P, P, 64, 2, 8, ctypes.byref(per_head), P,
+                                  1 << 20, ctypes.c_float(0.1), None, None) == rx.RX_ERR_UNSUPPORTED
 
 
 # ---------------------------------------------------------------------------
