@@ -491,49 +491,200 @@ def job_throughput(units_per_rank_step: float, world: int, steps: int, max_ms: f
     return units_per_rank_step * world * steps / (max_ms / 1e3)
 
 
+class E2EPipeline:
+    """One step of the path as a caller drives it through the public API with
+    host buffers, its copies overlapped with the kernels: the new K/V rows,
+    their slots and the decode queries go in first on an input stream, then
+    the extend queries in request chunks; the compute stream stores the rows,
+    runs decode as soon as its queries are in, and runs each chunk's extend
+    (rx_attn_extend over that chunk's requests) as soon as the chunk's
+    queries are in; an output stream copies each result back as soon as it
+    is written.  The same calls, on the same data, as the step."""
+
+    def __init__(self, st, torch, rx, chunks=4):
+        self.st, self.torch, self.rx = st, torch, rx
+        p = st.prob
+        pin = lambda t: t.cpu().pin_memory()
+        self.h_kv = [pin(st.k_new), pin(st.v_new), pin(st.slots)]
+        self.d_kv = [st.k_new, st.v_new, st.slots]
+        self.h_in, self.h_out = list(self.h_kv), []
+        if st.has_dec:
+            self.h_qd = [pin(st.q_dec), pin(st.dec_len)]
+            self.h_od = torch.empty(st.o_dec.shape, dtype=st.o_dec.dtype, pin_memory=True)
+            self.h_in += self.h_qd
+            self.h_out.append(self.h_od)
+        self.chunks = []
+        if st.has_ext:
+            self.h_qe = pin(st.q_ext)
+            self.h_oe = torch.empty(st.o_ext.shape, dtype=st.o_ext.dtype, pin_memory=True)
+            self.h_in.append(self.h_qe)
+            self.h_out.append(self.h_oe)
+            Be = len(p.ext_req_idx)
+            cuts = sorted(set(int(x) for x in np.linspace(0, Be, min(chunks, Be) + 1)))
+            i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+            max_ctx = 0
+            for b0, b1 in zip(cuts[:-1], cuts[1:]):
+                r0, r1 = int(p.qo_indptr[b0]), int(p.qo_indptr[b1])
+                ctx = int((p.ext_prefix_len[b0:b1] + p.ext_extend_len[b0:b1]).sum())
+                max_ctx = max(max_ctx, ctx)
+                self.chunks.append(dict(
+                    rows=(r0, r1), qo=i32(p.qo_indptr[b0:b1 + 1] - r0), req=i32(p.ext_req_idx[b0:b1]),
+                    P=i32(p.ext_prefix_len[b0:b1]), E=i32(p.ext_extend_len[b0:b1]),
+                    max_E=int(p.ext_extend_len[b0:b1].max()), n=b1 - b0))
+            self.ws = torch.empty(rx.rx_attn_extend_workspace(max_ctx, max(c["n"] for c in self.chunks), p.hkv, p.d),
+                                  dtype=torch.uint8, device="cuda")
+        self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def bytes_in(self):
+        return sum(h.numel() * h.element_size() for h in self.h_in)
+
+    def bytes_out(self):
+        return sum(h.numel() * h.element_size() for h in self.h_out)
+
+    def step(self):
+        torch, rx, st, p = self.torch, self.rx, self.st, self.st.prob
+        E = torch.cuda.Event
+        comp = torch.cuda.current_stream()
+        ev_kv, ev_qd = E(), E()
+        ev_q = [E() for _ in self.chunks]
+        # the side streams fork from the compute stream (required when captured)
+        self.s_in.wait_stream(comp)
+        self.s_out.wait_stream(comp)
+        with torch.cuda.stream(self.s_in):
+            for h, d in zip(self.h_kv, self.d_kv):
+                d.copy_(h, non_blocking=True)
+            ev_kv.record()
+            if st.has_dec:
+                st.q_dec.copy_(self.h_qd[0], non_blocking=True)
+                st.dec_len.copy_(self.h_qd[1], non_blocking=True)
+                ev_qd.record()
+            for c, ev in zip(self.chunks, ev_q):
+                r0, r1 = c["rows"]
+                st.q_ext[r0:r1].copy_(self.h_qe[r0:r1], non_blocking=True)
+                ev.record()
+        comp.wait_event(ev_kv)
+        st.kv_store()
+        if st.has_dec:
+            comp.wait_event(ev_qd)
+            st.decode()
+            ev_d = E()
+            ev_d.record(comp)
+            self.s_out.wait_event(ev_d)
+            with torch.cuda.stream(self.s_out):
+                self.h_od.copy_(st.o_dec, non_blocking=True)
+        for c, ev in zip(self.chunks, ev_q):
+            r0, r1 = c["rows"]
+            comp.wait_event(ev)
+            rx.rx_attn_extend(st.k_pool, st.v_pool, st.q_ext[r0:r1], st.o_ext[r0:r1], None, c["qo"], c["req"],
+                              c["P"], c["E"], st.rtt, c["max_E"], p.sm_scale, st.status, workspace=self.ws)
+            ev_o = E()
+            ev_o.record(comp)
+            self.s_out.wait_event(ev_o)
+            with torch.cuda.stream(self.s_out):
+                self.h_oe[r0:r1].copy_(st.o_ext[r0:r1], non_blocking=True)
+        # the side streams join the compute stream (required when captured)
+        comp.wait_stream(self.s_in)
+        comp.wait_stream(self.s_out)
+
+    def capture(self):
+        """The step as one CUDA graph (copies, kernels and the events between
+        them); replaying it re-issues the same calls without host work."""
+        torch = self.torch
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.step()
+        torch.cuda.synchronize()
+
+
 def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
     """The step as a caller runs it through the public API, one step at a
     time: the step's inputs copied in from pinned host memory (new K/V rows
     and their slots, the queries, the decode lengths), the path, its outputs
     copied back, and a synchronize -- a serving loop reads every step's
     output before it can form the next step.  Host wall time per step, L2
-    flushed (untimed) before each one.  The decode plan is not rebuilt per
-    step: it was built once for the batch (its time is reported beside),
-    and each request's last piece follows its length on the device, so the
-    same plan serves the batch's later decode steps."""
+    flushed (untimed) before each one.  The copies overlap the kernels
+    (E2EPipeline) unless the step carries the optional RoPE or FP8 parts,
+    which run in the plain order.  The decode plan is not rebuilt per step:
+    it was built once for the batch (its time is reported beside), and each
+    request's last piece follows its length on the device, so the same plan
+    serves the batch's later decode steps."""
     p = st.prob
-    h_in = [st.k_new.cpu().pin_memory(), st.v_new.cpu().pin_memory(), st.slots.cpu().pin_memory()]
-    d_in = [st.k_new, st.v_new, st.slots]
-    outs = []
-    if st.has_ext:
-        h_in.append(st.q_ext.cpu().pin_memory())
-        d_in.append(st.q_ext)
-        outs.append(st.o_ext)
-    if st.has_dec:
-        h_in += [st.q_dec.cpu().pin_memory(), st.dec_len.cpu().pin_memory()]
-        d_in += [st.q_dec, st.dec_len]
-        outs.append(st.o_dec)
-    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    pipelined = not st.rope_base and not st.kv_fp8
+    if pipelined:
+        pipe = E2EPipeline(st, torch, rx)
+        run, h2d, d2h = pipe.step, pipe.bytes_in(), pipe.bytes_out()
+        for _ in range(2):   # untimed: first use of the streams and events
+            run()
+        torch.cuda.synchronize()
+        eager_ms = None
+        secs = []
+        for i in range(max(3, min(steps, 50))):
+            flush()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            run()
+            torch.cuda.synchronize()
+            secs.append(time.perf_counter() - t0)
+        eager_ms = sum(secs) / len(secs) * 1e3
+        pipe.capture()
+        run = pipe.graph.replay
+    else:
+        h_in = [st.k_new.cpu().pin_memory(), st.v_new.cpu().pin_memory(), st.slots.cpu().pin_memory()]
+        d_in = [st.k_new, st.v_new, st.slots]
+        outs = []
+        if st.has_ext:
+            h_in.append(st.q_ext.cpu().pin_memory())
+            d_in.append(st.q_ext)
+            outs.append(st.o_ext)
+        if st.has_dec:
+            h_in += [st.q_dec.cpu().pin_memory(), st.dec_len.cpu().pin_memory()]
+            d_in += [st.q_dec, st.dec_len]
+            outs.append(st.o_dec)
+        h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+
+        def run():
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            st.step()
+            for h, d in zip(h_out, outs):
+                h.copy_(d, non_blocking=True)
+        h2d = sum(h.numel() * h.element_size() for h in h_in)
+        d2h = sum(h.numel() * h.element_size() for h in h_out)
     n = max(3, min(steps, 200))
+    for _ in range(2):   # untimed: first use of the streams and events
+        run()
+    torch.cuda.synchronize()
     secs = []
     for i in range(n):
         flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for h, d in zip(h_in, d_in):
-            d.copy_(h, non_blocking=True)
-        st.step()
-        for h, d in zip(h_out, outs):
-            h.copy_(d, non_blocking=True)
+        run()
         torch.cuda.synchronize()
         secs.append(time.perf_counter() - t0)
     ms = max_over_ranks(sum(secs) / n * 1e3, dist, "cuda")
-    h2d = sum(h.numel() * h.element_size() for h in h_in)
-    d2h = sum(h.numel() * h.element_size() for h in h_out)
+    if pipelined:
+        # the overlapped schedule must return what the plain step returns
+        got = [h.clone() for h in pipe.h_out]
+        st.step()
+        torch.cuda.synchronize()
+        want = ([st.o_dec.cpu()] if st.has_dec else []) + ([st.o_ext.cpu()] if st.has_ext else [])
+        if not all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(got, want)):
+            raise RuntimeError("the overlapped end-to-end step returned other outputs than the step")
     _, unit, per_step = step_metric(p)
     out = {"value": round(job_throughput(per_step, world, 1, ms), 3), "unit": unit,
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 5),
-           "steps": n, "timing": "host wall clock per step, synchronized every step"}
+           "steps": n, "timing": "host wall clock per step, synchronized every step",
+           "schedule": ("copies on their own streams, overlapping the kernels; extend in "
+                        f"{len(pipe.chunks)} request chunks" if pipelined and pipe.chunks else
+                        "copies on their own streams, overlapping the kernels" if pipelined else
+                        "copies in, the step, copies out, in order"),
+           "launch": "the step's calls captured once in a CUDA graph, replayed per step" if pipelined else
+                     "direct calls"}
+    if pipelined:
+        out["eager"] = {"ms_per_step": round(eager_ms, 5),
+                        "value": round(job_throughput(per_step, world, 1, eager_ms), 3),
+                        "launch": "the same calls made directly every step"}
     if st.has_dec:
         out["decode_plan"] = {"built": "once per batch, reused by every later decode step",
                               "build_ms": round(st.plan_build_ms, 3)}
