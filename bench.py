@@ -702,11 +702,17 @@ PROFILED_TRAFFIC = {
     ("mixed_chat", "decode"): (
         1_665_600_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat (600,000-slot pool; "
                        "same rows): decode_gqa_kernel alone, without the merge"),
+    ("few_shot_decode", "decode"): (
+        293_400_000, "ncu --set full -k decode_kernel -c 1 and -k decode_wide_kernel -c 1 on few_shot_decode "
+                     "(262,144-slot pool; same rows): the two decode kernels, without the merge"),
+    ("tree_of_thought_decode", "decode"): (
+        383_500_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode (131,072-slot pool; "
+                     "same rows): decode_gqa_kernel alone, without the merge"),
     ("cached_prefix_extend", "staged"): (
-        585_800_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend (1M-slot pool): "
-                     "extend_kernel alone, without the staging copy"),
+        586_100_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend (36,000-slot pool; same "
+                     "staged rows): extend_kernel alone, without the staging copy"),
     ("constrained_decode", "fsm"): (
-        132_300_000, "ncu launch list of constrained_decode: fsm_scan_kernel + fsm_finish_kernel"),
+        135_800_000, "ncu --set full -k fsm_scan_kernel -c 1 on constrained_decode: the scan alone"),
 }
 
 
