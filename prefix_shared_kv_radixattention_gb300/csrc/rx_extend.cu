@@ -42,6 +42,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <climits>
 
 #include <mutex>
 #include <type_traits>
@@ -68,7 +69,7 @@ constexpr int kThreads = 32 * 12;   // no register reallocation: every warp keep
 constexpr int kStagedThreads = 32 * 10;
 constexpr int kStagedProducerWarp = 8;
 constexpr int kStagedMmaWarp = 9;
-constexpr int kStageBlock = 16;    // rows per copy unit of the staging kernel
+constexpr int kStageBlock = 4;     // rows per copy unit of the staging kernel
 constexpr uint32_t kTmemCols = 512;  // per Q tile t: S (then P as bf16) [256t, +128), O [256t + 128, +128)
 constexpr float kRescale = 8.f;      // log2 units the running max may lag
 
@@ -102,6 +103,8 @@ struct XParams {  // 64-byte aligned through its tensor maps
     CUtensorMap tm_k;
     CUtensorMap tm_v;
     const int64_t *stage_offs;  // first packed row of request b; [batch] = rows used
+    const int32_t *stage_src;   // request whose packed rows hold b's leading shared tiles
+    const int32_t *stage_share; // leading prefix tiles of b read from stage_src[b]'s rows
     int64_t stage_cap;          // rows the workspace holds
     const bf16 *q;
     bf16 *o;
@@ -127,7 +130,9 @@ struct Tile {
     int row0_pos;      // absolute position of row group 0
     int kv_end;        // keys [0, kv_end)
     int ntiles;
-    int stage_row0;    // staged path: first packed row of this request
+    int stage_row0;    // staged path: first packed row of this request's own tiles
+    int share_tiles;   // staged path: leading tiles read from another request's rows
+    int share_row0;    // ... which start at this packed row
     const int32_t *slots;
     int g;
 };
@@ -263,7 +268,8 @@ __device__ void tma_producer(const XParams &p, const Tile &T, unsigned char *sme
     int issued[2] = {0, 0};  // tiles of K, of V
     for (int j = 0; j < T.ntiles; ++j) {
         const int st = j % kStages;
-        const int row = T.stage_row0 + j * kBN;
+        // leading tiles shared with an earlier request come from its rows
+        const int row = j < T.share_tiles ? T.share_row0 + j * kBN : T.stage_row0 + (j - T.share_tiles) * kBN;
         bool stop = false;
 #pragma unroll
         for (int w = 0; w < 2; ++w) {  // K into its stage once S freed it, then V
@@ -558,6 +564,8 @@ __global__ void __launch_bounds__(kStaged ? kStagedThreads : kThreads, 1)
         // contexts larger than the workspace: nothing was staged (flagged there)
         if (p.stage_offs[gridDim.z] > p.stage_cap) return;
         T.stage_row0 = (int)p.stage_offs[b];
+        T.share_tiles = p.stage_share[b];
+        T.share_row0 = (int)p.stage_offs[p.stage_src[b]];
     }
     T.M = ntok * p.G;
     T.nqt = T.M > kRows ? 2 : 1;
@@ -633,20 +641,81 @@ __device__ __forceinline__ int64_t staged_rows(const int32_t *prefix_len, const 
     return (P + E + kBN - 1) / kBN * kBN;
 }
 
-// offs[b] = first packed row of request b (exclusive prefix sum of the
-// packed row counts), offs[batch] = rows used; more than `cap` rows is
-// flagged, and then neither the copy nor the attention kernel does anything.
+// Requests of one batch that share a cached prefix (their slot lists agree
+// on it) need its rows staged once.  For request b: src[b] = the first
+// request r < b whose slot list agrees with b's on position 0, both
+// prefixes covering the first kBN-row tile, and share[b] = the leading
+// tiles, inside both prefixes, on which b and r agree (0 when even the first
+// differs: then src[b] = b).  Such an r stages every tile of its own (an
+// earlier request agreeing with it on position 0 would be b's candidate
+// instead), so b stages only tiles share[b] .. and reads the others from r's
+// rows.  One CTA per request, in a few rounds of loads issued together:
+// the first slot id of every earlier request (a thread per candidate), then
+// every position of the shared tiles (a thread per position of a tile).
+__global__ void __launch_bounds__(kBN) stage_share_kernel(const int32_t *__restrict__ rtt, int64_t rtt_stride,
+                                                         const int32_t *__restrict__ req_idx,
+                                                         const int32_t *__restrict__ prefix_len,
+                                                         const int32_t *__restrict__ extend_len, int32_t *src,
+                                                         int32_t *share)
+{
+    __shared__ int first, diff;
+    const int b = blockIdx.x, t = threadIdx.x;
+    auto covers = [&](int i) {
+        const int64_t P = __ldg(prefix_len + i), E = __ldg(extend_len + i);
+        return P >= kBN && E >= 0 && P + E <= rtt_stride;
+    };
+    if (t == 0) {
+        first = b;
+        diff = INT_MAX;
+    }
+    __syncthreads();
+    const bool b_ok = covers(b);
+    const int32_t *rb = rtt + (int64_t)__ldg(req_idx + b) * rtt_stride;
+    if (b_ok) {
+        const int32_t s0 = __ldg(rb);
+        for (int r = t; r < b; r += kBN)
+            if (covers(r) && __ldg(rtt + (int64_t)__ldg(req_idx + r) * rtt_stride) == s0) {
+                atomicMin(&first, r);
+                break;
+            }
+    }
+    __syncthreads();
+    const int r = first;
+    int tiles = 0;
+    if (r != b) {
+        const int32_t *rr = rtt + (int64_t)__ldg(req_idx + r) * rtt_stride;
+        const int ntile = (int)(min(__ldg(prefix_len + b), __ldg(prefix_len + r)) / kBN);
+        int local = ntile;
+#pragma unroll 8
+        for (int j = 0; j < ntile; ++j)
+            if (__ldg(rr + (int64_t)j * kBN + t) != __ldg(rb + (int64_t)j * kBN + t)) local = min(local, j);
+        if (local < ntile) atomicMin(&diff, local);
+        __syncthreads();
+        tiles = min(ntile, diff);
+    }
+    if (t == 0) {
+        src[b] = tiles > 0 ? r : b;
+        share[b] = tiles;
+    }
+}
+
+// offs[b] = first packed row of request b's own tiles (exclusive prefix sum
+// of the packed row counts: its context rounded up to whole kBN-row tiles,
+// less the tiles it shares), offs[batch] = rows used; more than `cap` rows
+// is flagged, and then neither the copy nor the attention kernel does
+// anything.
 __global__ void __launch_bounds__(1024) ctx_offsets_kernel(const int32_t *prefix_len, const int32_t *extend_len,
-                                                           int batch, int64_t rtt_stride, int64_t cap,
-                                                           int64_t *offs, int32_t *status)
+                                                           const int32_t *share, int batch, int64_t rtt_stride,
+                                                           int64_t cap, int64_t *offs, int32_t *status)
 {
     __shared__ int64_t warp_tot[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int per = (batch + 1023) / 1024;
     const int b0 = threadIdx.x * per;
     int64_t local = 0;
-    for (int i = 0; i < per && b0 + i < batch; ++i) local += staged_rows(prefix_len, extend_len, b0 + i, rtt_stride);
+    for (int i = 0; i < per && b0 + i < batch; ++i)
+        local += staged_rows(prefix_len, extend_len, b0 + i, rtt_stride) - (int64_t)share[b0 + i] * kBN;
     // inclusive scan over the block: within each warp, then over warp totals
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int64_t x = local;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -668,7 +737,7 @@ __global__ void __launch_bounds__(1024) ctx_offsets_kernel(const int32_t *prefix
     int64_t run = x - local + (warp > 0 ? warp_tot[warp - 1] : 0);  // exclusive
     for (int i = 0; i < per && b0 + i < batch; ++i) {
         offs[b0 + i] = run;
-        run += staged_rows(prefix_len, extend_len, b0 + i, rtt_stride);
+        run += staged_rows(prefix_len, extend_len, b0 + i, rtt_stride) - (int64_t)share[b0 + i] * kBN;
     }
     if (threadIdx.x == 1023) {
         const int64_t total = warp_tot[31];
@@ -677,17 +746,17 @@ __global__ void __launch_bounds__(1024) ctx_offsets_kernel(const int32_t *prefix
     }
 }
 
-// Packed row offs[b] + pos = pool row req_to_token[req_idx[b]][pos] for K and
-// V (all kv heads: one contiguous row of the pool each), zeros from the end of
-// the context to the kBN-row boundary and for slot ids outside the pool
-// (flagged).  One warp per block of kStageBlock rows; every request's region
-// is a multiple of kBN rows, so a block never straddles two requests.
+// Packed row offs[b] + i = pool row req_to_token[req_idx[b]][share[b] kBN + i]
+// for K and V (all kv heads: one contiguous row of the pool each), zeros from
+// the end of the context to the kBN-row boundary and for slot ids outside the
+// pool (flagged).  One warp per block of kStageBlock rows; every request's
+// region is a multiple of kBN rows, so a block never straddles two requests.
 __global__ void __launch_bounds__(256) stage_rows_kernel(
     const bf16 *__restrict__ k_pool, const bf16 *__restrict__ v_pool, int64_t num_slots,
     const int32_t *__restrict__ rtt, int64_t rtt_stride, const int32_t *__restrict__ req_idx,
-    const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ extend_len, int batch,
-    const int64_t *__restrict__ offs, int64_t cap, bf16 *__restrict__ ks, bf16 *__restrict__ vs, int row_elems,
-    int32_t *status)
+    const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ extend_len,
+    const int32_t *__restrict__ share, int batch, const int64_t *__restrict__ offs, int64_t cap,
+    bf16 *__restrict__ ks, bf16 *__restrict__ vs, int row_elems, int32_t *status)
 {
     const int64_t total = offs[batch];
     if (total > cap) return;
@@ -702,9 +771,12 @@ __global__ void __launch_bounds__(256) stage_rows_kernel(
             const int mid = (lo + hi + 1) >> 1;
             if (offs[mid] <= row0) lo = mid; else hi = mid - 1;
         }
+        // a request that shares all its tiles has an empty region: the
+        // search above lands on the last request starting at row0, which
+        // owns it
         const int b = lo;
         const int64_t ctx = (int64_t)__ldg(prefix_len + b) + __ldg(extend_len + b);
-        const int64_t pos0 = row0 - offs[b];
+        const int64_t pos0 = row0 - offs[b] + (int64_t)share[b] * kBN;
         int32_t my_slot = -1;
         if (lane < kStageBlock && pos0 + lane < ctx) {
             const int32_t sl = __ldg(rtt + (int64_t)__ldg(req_idx + b) * rtt_stride + pos0 + lane);
@@ -739,17 +811,24 @@ int check_pool(const rx_kv_pool *pool)
     return RX_OK;
 }
 
-// Workspace of the staged path: int64 packed-row offsets [batch + 1], then the
-// packed K rows and the packed V rows, [cap][kv heads][head_dim] bf16 each,
-// every part 256-byte aligned.
+// Workspace of the staged path: int64 packed-row offsets [batch + 1], int32
+// share sources [batch] and shared tile counts [batch], then the packed K
+// rows and the packed V rows, [cap][kv heads][head_dim] bf16 each, every
+// part 256-byte aligned.
 struct StageLayout {
-    size_t off_k, off_v, bytes;
+    size_t off_src, off_share, off_k, off_v, bytes;
 };
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t stage_head(int32_t batch)
+{
+    return align256((size_t)(batch + 1) * sizeof(int64_t)) + 2 * align256((size_t)batch * sizeof(int32_t));
+}
 StageLayout stage_layout(int64_t cap, int32_t batch, int64_t row_bytes)
 {
     StageLayout l;
-    l.off_k = align256((size_t)(batch + 1) * sizeof(int64_t));
+    l.off_src = align256((size_t)(batch + 1) * sizeof(int64_t));
+    l.off_share = l.off_src + align256((size_t)batch * sizeof(int32_t));
+    l.off_k = stage_head(batch);
     const size_t region = align256((size_t)cap * (size_t)row_bytes);
     l.off_v = l.off_k + region;
     l.bytes = l.off_v + region;
@@ -758,7 +837,7 @@ StageLayout stage_layout(int64_t cap, int32_t batch, int64_t row_bytes)
 // largest row count a workspace of ws_bytes holds (TMA row coordinates are int32)
 int64_t stage_cap_for(size_t ws_bytes, int32_t batch, int64_t row_bytes)
 {
-    const size_t head = align256((size_t)(batch + 1) * sizeof(int64_t));
+    const size_t head = stage_head(batch);
     if (ws_bytes <= head) return 0;
     int64_t cap = (int64_t)((ws_bytes - head) / 2 / (size_t)row_bytes);
     cap = cap < (int64_t)INT32_MAX - 2 * kBN ? cap : (int64_t)INT32_MAX - 2 * kBN;
@@ -880,15 +959,22 @@ extern "C" int rx_attn_extend(const rx_kv_pool *pool_in, const void *q, void *o,
     bf16 *vs = reinterpret_cast<bf16 *>(static_cast<char *>(workspace) + lay.off_v);
     if ((rc = encode_stage_map(&p.tm_k, ks, cap, p.hkv, D)) != RX_OK) return rc;
     if ((rc = encode_stage_map(&p.tm_v, vs, cap, p.hkv, D)) != RX_OK) return rc;
+    int32_t *src = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + lay.off_src);
+    int32_t *share = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + lay.off_share);
     p.stage_offs = offs;
+    p.stage_src = src;
+    p.stage_share = share;
     p.stage_cap = cap;
     int dev = 0, sms = 0;
     RX_CUDA_CHECK(cudaGetDevice(&dev));
     RX_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    ctx_offsets_kernel<<<1, 1024, 0, st>>>(prefix_len, extend_len, batch, rtt_stride, cap, offs, dev_status);
+    stage_share_kernel<<<batch, kBN, 0, st>>>(rtt, rtt_stride, req_idx, prefix_len, extend_len, src, share);
+    RX_CUDA_CHECK(cudaGetLastError());
+    ctx_offsets_kernel<<<1, 1024, 0, st>>>(prefix_len, extend_len, share, batch, rtt_stride, cap, offs,
+                                           dev_status);
     RX_CUDA_CHECK(cudaGetLastError());
     stage_rows_kernel<<<sms * 8, 256, 0, st>>>(p.k_pool, p.v_pool, p.num_slots, rtt, rtt_stride, req_idx,
-                                               prefix_len, extend_len, batch, offs, cap, ks, vs,
+                                               prefix_len, extend_len, share, batch, offs, cap, ks, vs,
                                                p.hkv * D, dev_status);
     RX_CUDA_CHECK(cudaGetLastError());
     return D == 128 ? launch_extend<128, true>(p, grid, st) : launch_extend<64, true>(p, grid, st);

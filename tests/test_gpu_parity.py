@@ -132,14 +132,43 @@ def test_extend_staged_equals_gathered_bitwise():
     assert dev.status_word() == 0
 
 
+@pytest.mark.parametrize("prefix,extend", [(256, 100), (300, 70), (130, 200), (128, 1)])
+def test_extend_staged_shares_prefix_tiles(prefix, extend):
+    """Requests whose slot lists agree on whole leading 128-row prefix tiles
+    stage those tiles once and read them from the first such request's
+    rows: results bit-identical to the gather path and within tolerance of
+    the oracle, for prefixes on and off tile boundaries; plus requests with
+    a private prefix and one whose list departs from its group's inside the
+    second tile."""
+    g = _gpu()
+    prob = inputs.cached_prefix_extend(seed=prefix + extend, hq=16, hkv=4, d=128, n_prefix=3, per_prefix=3,
+                                       prefix=prefix, extend=extend, num_slots=8192)
+    prob.req_to_token = prob.req_to_token.copy()
+    if prefix >= 256:   # request 4 leaves its group at position 200 (inside the second tile)
+        free = np.setdiff1d(np.arange(prob.num_slots), prob.req_to_token[prob.req_to_token >= 0])
+        prob.req_to_token[4, 200:prefix] = free[:prefix - 200]
+    dev = g.Dev(prob)
+    dev.kv_store()
+    o1, l1 = dev.extend(staged=False)
+    o2, l2 = dev.extend(staged=True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    assert dev.status_word() == 0
+    kp, vp, rtt = dev.oracle_pools()
+    ro, rl = oracle.extend(prob.q_ext, kp, vp, rtt, prob.ext_req_idx, prob.ext_prefix_len, prob.ext_extend_len,
+                           prob.qo_indptr, prob.sm_scale)
+    g.compare(o2, ro, "staged extend with shared tiles")
+    g.compare_lse(l2, rl, "staged extend with shared tiles")
+
+
 def test_extend_staged_workspace_too_small_is_flagged():
     g = _gpu()
     from prefix_shared_kv_radixattention_gb300 import binding as rx
     prob = inputs.tiny_extend(seed=3, hq=8, hkv=2, d=128, batch=3, prefix=200, extend=40, num_slots=1024)
     dev = g.Dev(prob)
     dev.kv_store()
-    # sized for one request's context: the three need more rows than it holds
-    dev.extend(staged=True, ws_rows=240)
+    # the three contexts need 512 packed rows even with their shared first
+    # tile staged once; a workspace sized for 40 context tokens holds 421
+    dev.extend(staged=True, ws_rows=40)
     assert dev.status_word() & rx.RX_DEV_BAD_LEN
 
 

@@ -234,14 +234,15 @@ def test_match_capacity_error_code():
 
 
 def test_extend_workspace_size():
-    """Offsets [batch+1] int64, then K and V areas of (total + 127 batch) rows
-    of num_kv_heads x head_dim bf16 (every context rounded up to whole
-    128-row tiles), each part rounded up to 256 bytes."""
+    """Offsets [batch+1] int64, shared-tile sources and counts [batch] int32
+    each, then K and V areas of (total + 127 batch) rows of num_kv_heads x
+    head_dim bf16 (every context rounded up to whole 128-row tiles, none
+    shared), each part rounded up to 256 bytes."""
     def up(x):
         return (x + 255) // 256 * 256
     for total, batch, hkv, d in ((1000, 3, 8, 128), (0, 1, 4, 64), (81920, 32, 8, 128), (5, 7, 1, 64)):
         rows = max(total + 127 * batch, 128)
-        want = up((batch + 1) * 8) + 2 * up(rows * hkv * d * 2)
+        want = up((batch + 1) * 8) + 2 * up(batch * 4) + 2 * up(rows * hkv * d * 2)
         assert rx.rx_attn_extend_workspace(total, batch, hkv, d) == want
 
 
