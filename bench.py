@@ -709,8 +709,9 @@ PROFILED_TRAFFIC = {
         383_500_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode (131,072-slot pool; "
                      "same rows): decode_gqa_kernel alone, without the merge"),
     ("cached_prefix_extend", "staged"): (
-        586_100_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend (36,000-slot pool; same "
-                     "staged rows): extend_kernel alone, without the staging copy"),
+        374_900_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend (36,000-slot pool; same "
+                     "staged rows, shared prefix tiles staged once): extend_kernel alone, without the "
+                     "staging copy"),
     ("constrained_decode", "fsm"): (
         135_800_000, "ncu --set full -k fsm_scan_kernel -c 1 on constrained_decode: the scan alone"),
 }
