@@ -302,8 +302,10 @@ int rx_kv_store_fp8(const rx_kv_pool_fp8 *pool, const void *k_new, const void *v
  * theta_c = base^(-2c / head_dim) and a = p * theta_c:
  *     x'[c]                = x[c] cos a - x[c + head_dim/2] sin a
  *     x'[c + head_dim / 2] = x[c + head_dim/2] cos a + x[c] sin a
- * Angles are formed in double precision (theta_c tabulated on the host, a
- * reduced modulo 2 pi), the rotation in fp32, results rounded to bf16.
+ * theta_c / (2 pi) is tabulated on the host as a 64-bit fraction of a turn,
+ * so p * theta_c is reduced modulo 2 pi exactly in integer arithmetic (to the
+ * table's 2^-53 relative rounding) at any position; sine and cosine, and the
+ * rotation, in fp32; results rounded to bf16.
  * head_dim 64 or 128; base > 1 (10000 and 500000 are usual). */
 
 /* In place on x: device bf16 [n, heads, head_dim], 16-byte aligned; pos:

@@ -805,11 +805,30 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
     // at most kv_chunk.  Otherwise they are cut into kv_chunk pieces.
     int64_t priv_total = 0;
     for (int64_t r = 0; r < B; ++r) priv_total += seq_len[order[(size_t)r]] - priv_begin[(size_t)r];
+    // Request-group items share the all-heads kernel's queue with the
+    // private pieces, longest first; with automatic chunking a private range
+    // is not cut into pieces shorter than the longest group item, which
+    // would only add partial results to merge, not balance.
+    const bool groups = G > 1 && rx_gqa_heads(hq, hkv);
+    const int64_t RG = 16 / G;
+    auto grouped_seg = [&](const Interval &x) {
+        return groups && (x.rb - x.lb + 1 + RG - 1) / RG <= RX_DECODE_MAX_GROUPS;
+    };
+    int64_t group_len = 0;
+    for (int64_t k = 0; k < n_iv; ++k)
+        if (is_seg[(size_t)k] && grouped_seg(iv[(size_t)k]))
+            group_len = std::max<int64_t>(group_len, std::min<int64_t>(kv_chunk, iv[(size_t)k].lcp - seg_start[(size_t)k]));
     int64_t pchunk = kv_chunk;
     if (auto_chunk && wide && priv_total > 0)
         pchunk = std::min<int64_t>(RX_MAX_KV_CHUNK, std::max<int64_t>(RX_DECODE_MIN_WIDE_CHUNK,
                                    (priv_total + RX_DECODE_TARGET_WIDE_ITEMS - 1) / RX_DECODE_TARGET_WIDE_ITEMS));
-    auto npriv = [&](int64_t len) { return (len + pchunk - 1) / pchunk; };
+    auto npriv = [&](int64_t len) {
+        int64_t n = (len + pchunk - 1) / pchunk;
+        if (auto_chunk && wide && group_len > 0)
+            n = std::max<int64_t>((len + RX_MAX_KV_CHUNK - 1) / RX_MAX_KV_CHUNK,
+                                  std::min<int64_t>(n, std::max<int64_t>(1, len / group_len)));
+        return n;
+    };
     // start of private piece c of n over len positions: near-equal pieces for
     // wide items, whole kv_chunk pieces (64-key tiles) for per-head items
     auto piece = [&](int64_t len, int64_t n, int64_t c) {
@@ -841,15 +860,12 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
     };
     std::vector<Item> items;
     const int64_t R = 64 / G;  // requests per per-head item (64 query rows)
-    // groups of up to 16 / G requests (16 query rows per kv head) for the
-    // several-q-heads all-heads kernel
-    const bool groups = G > 1 && rx_gqa_heads(hq, hkv);
-    const int64_t RG = 16 / G;
+    // groups of up to RG = 16 / G requests (16 query rows per kv head) for
+    // the several-q-heads all-heads kernel
     for (int64_t k = 0; k < n_iv; ++k) {
         if (!is_seg[(size_t)k]) continue;
         const Interval &x = iv[(size_t)k];
-        const int64_t nreq = x.rb - x.lb + 1;
-        const bool grouped = groups && (nreq + RG - 1) / RG <= RX_DECODE_MAX_GROUPS;
+        const bool grouped = grouped_seg(x);
         const int64_t step = grouped ? RG : R;
         int64_t s0 = seg_start[(size_t)k], s1 = x.lcp;
         for (int64_t c = 0; c * kv_chunk < s1 - s0; ++c) {

@@ -11,14 +11,19 @@
 //
 // The work is a copy with a few flops per element, so it is laid out for
 // HBM.  A thread takes one token, one group of eight pairs and a run of
-// `cpt` chunks of four heads: it forms the eight angles once -- in double
-// precision from a host table of theta_c, reduced modulo 2 pi with 2 pi split
-// in two parts, so positions in the tens of thousands keep their accuracy --
-// and for each chunk issues all its 16-byte loads (both halves of four heads)
-// before rotating and storing them.  Small batches get one chunk a thread
-// (more threads in flight); large ones get all of a token's chunks (fewer
-// double-precision angles, the slow part on this GPU).  Consecutive threads
-// take consecutive groups of one head, so the accesses coalesce.
+// `cpt` chunks of four heads: it forms the eight angles once and for each
+// chunk issues all its 16-byte loads (both halves of four heads) before
+// rotating and storing them.  Consecutive threads take consecutive groups of
+// one head, so the accesses coalesce.
+//
+// Angles: the host tabulates f_c = theta_c / (2 pi) as a 64-bit binary
+// fraction of a turn, F_c = f_c 2^64 (f_c < 1).  Then p F_c mod 2^64 is
+// p f_c mod 1 in units of 2^-64 turn, exactly as integer arithmetic wraps,
+// so the reduction modulo 2 pi is exact up to the table's rounding (about
+// 2^-53 of f_c) at any int32 position; its top 32 bits, read as a signed
+// number, are the angle in [-pi, pi) in units of 2^-31 pi, which sincosf
+// then takes.  Two integer multiplies a pair -- this GPU runs double
+// precision at a small fraction of its fp32 and integer rates.
 #include <math.h>
 
 #include "rx_common.cuh"
@@ -30,7 +35,8 @@ using bf16 = __nv_bfloat16;
 constexpr int kMaxHalf = 64;  // head_dim 128
 
 struct RopeTab {
-    double theta[kMaxHalf];  // base^(-2c/d), c < d/2
+    uint32_t f_hi[kMaxHalf];  // theta_c / (2 pi) as a 64-bit fraction of a turn: high word
+    uint32_t f_lo[kMaxHalf];  // low word
 };
 
 struct Rot8 {
@@ -39,18 +45,19 @@ struct Rot8 {
 
 __device__ __forceinline__ Rot8 angles(const RopeTab &tab, int32_t pos, int c0)
 {
-    // 2 pi = kTwoPiHi + kTwoPiLo; kTwoPiHi has its low 22 bits zero, so
-    // n * kTwoPiHi is exact for n < 2^22 (positions below about 26 million)
-    constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
-    constexpr double kTwoPiHi = 6.2831853069365024566650390625;
-    constexpr double kTwoPiLo = 2.4308402026024770e-10;
+    // |p|, and the sine's sign: a rotation by -a is the one by a with sin negated
+    const uint32_t up = pos < 0 ? 0u - (uint32_t)pos : (uint32_t)pos;
+    const float sgn = pos < 0 ? -1.f : 1.f;
+    constexpr float kTurn = 1.4629180792671596e-9f;  // 2 pi / 2^32
     Rot8 r;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const double a = (double)pos * tab.theta[c0 + k];
-        const double n = rint(a * kInvTwoPi);
-        const float ar = (float)fma(-n, kTwoPiLo, fma(-n, kTwoPiHi, a));  // in [-pi, pi]
+        // bits 32 .. 63 of |p| F_c: the high word of |p| f_lo plus the low
+        // word of |p| f_hi (the higher words are whole turns)
+        const uint32_t t = __umulhi(up, tab.f_lo[c0 + k]) + up * tab.f_hi[c0 + k];
+        const float ar = (float)(int32_t)t * kTurn;  // in [-pi, pi)
         sincosf(ar, &r.s[k], &r.c[k]);
+        r.s[k] *= sgn;
     }
     return r;
 }
@@ -182,7 +189,14 @@ int num_sms()
 bool make_tab(int D, double base, RopeTab &tab)
 {
     if ((D != 64 && D != 128) || !(base > 1.0)) return false;
-    for (int c = 0; c < D / 2; ++c) tab.theta[c] = pow(base, -2.0 * c / D);
+    constexpr double kTwoPi = 6.283185307179586476925286766559;
+    for (int c = 0; c < D / 2; ++c) {
+        // f_c < 1 / (2 pi): f_c 2^64 < 2^62, converted exactly from the double
+        const double f = pow(base, -2.0 * c / D) / kTwoPi;
+        const uint64_t F = (uint64_t)ldexp(f, 64);
+        tab.f_hi[c] = (uint32_t)(F >> 32);
+        tab.f_lo[c] = (uint32_t)F;
+    }
     return true;
 }
 

@@ -19,9 +19,13 @@ def _g():
 
 
 def _positions(rng, n):
+    """Positions of a long context, plus the ends of the int32 range: the
+    angle is reduced exactly modulo 2 pi at any position, so rows at 10^7,
+    2^31 - 1 and negative positions must match the fp64 definition too."""
     pos = rng.integers(0, 40000, size=n).astype(np.int32)
     pos[0] = 0
     pos[-1] = 32767
+    pos[1:5] = [10_000_000, 2**31 - 1, -7, -(2**31)]
     return pos
 
 
