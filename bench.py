@@ -210,20 +210,24 @@ class GpuStep:
                 ctx = int((p.ext_prefix_len + p.ext_extend_len).sum())
                 nb = rx.rx_attn_extend_workspace(ctx, len(p.ext_req_idx), p.hkv, p.d)
                 self.ext_ws = torch.empty(nb, dtype=torch.uint8, device=dev)
-                self.launches += 2  # packed-row offsets + row copy
-        # FP8 pools (optional): the step's rows also stored as E4M3 codes
+                self.launches += 3  # shared-tile search + packed-row offsets + row copy
+        # FP8 pools (optional): the whole step on E4M3 pools
         self.kv_fp8 = kv_fp8
         if kv_fp8:
+            if rope_base:
+                raise SystemExit("--kv-fp8 and --rope do not combine (no fused rotary FP8 store)")
+            if self.has_ext and extend_path != "staged":
+                raise SystemExit("--kv-fp8 extends on the staged path only")
             # E4M3 pools (scale 1): the cached rows quantized at set-up, the
-            # step's rows stored by rx_kv_store_fp8 in the timed step; decode
-            # reads them (rx_attn_decode_fp8), extend keeps the bf16 pools
+            # step's rows stored by rx_kv_store_fp8 in the timed step (in place
+            # of the bf16 store); extend and decode read them
+            # (rx_attn_extend_fp8, rx_attn_decode_fp8)
             self.k8 = torch.zeros((p.num_slots, p.hkv, p.d), dtype=torch.uint8, device=dev)
             self.v8 = torch.zeros_like(self.k8)
             for s0 in range(0, len(idx), 1 << 16):
                 sl = idx[s0:s0 + (1 << 16)].to(torch.int32)
                 rx.rx_kv_store_fp8(self.k8, self.v8, 1.0, 1.0, self.k_pool[sl.long()], self.v_pool[sl.long()], sl,
                                    self.status)
-            self.launches += 1  # the step's FP8 store
         # rotary position embedding (optional): K rotated on its way into the
         # pool, the step's q rows rotated in place
         self.rope_base = rope_base
@@ -268,6 +272,11 @@ class GpuStep:
 
     def extend(self):
         p = self.prob
+        if self.kv_fp8:
+            self.rx.rx_attn_extend_fp8(self.k8, self.v8, 1.0, 1.0, self.q_ext, self.o_ext, None, self.qo,
+                                       self.ext_req, self.ext_P, self.ext_E, self.rtt, self.max_E, p.sm_scale,
+                                       self.ext_ws, self.status)
+            return
         self.rx.rx_attn_extend(self.k_pool, self.v_pool, self.q_ext, self.o_ext, None, self.qo,
                                self.ext_req, self.ext_P, self.ext_E, self.rtt, self.max_E, p.sm_scale,
                                self.status, workspace=self.ext_ws)
@@ -276,7 +285,7 @@ class GpuStep:
         self.rx.rx_kv_store_fp8(self.k8, self.v8, 1.0, 1.0, self.k_new, self.v_new, self.slots, self.status)
 
     def parts(self):
-        return [("store", self.kv_store)] + ([("store_fp8", self.store_fp8)] if self.kv_fp8 else []) + \
+        return ([("store_fp8", self.store_fp8)] if self.kv_fp8 else [("store", self.kv_store)]) + \
             ([("rope_q", self.rope_q)] if self.rope_base else []) + \
             ([("extend", self.extend)] if self.has_ext else []) + ([("decode", self.decode)] if self.has_dec else [])
 
@@ -402,8 +411,9 @@ def run_gpu(args, rank, world, local_rank):
         roofs["extend"] = {
             "bound": "tensor", "achieved": round(tf, 2), "peak": tflops, "unit": "TFLOP/s",
             "frac": round(tf / tflops, 4), "traffic": traffic, "traffic_source": tsrc,
-            "kernel": "rx_attn_extend (" + ("offsets + staging copy + extend_kernel"
-                                            if args.extend_path == "staged" else "extend_kernel") + ")",
+            "kernel": ("rx_attn_extend_fp8" if st.kv_fp8 else "rx_attn_extend") + " (" +
+                      ("shared-tile search + offsets + staging copy + extend_kernel"
+                       if args.extend_path == "staged" else "extend_kernel") + ")",
             "algorithmic_flops_per_launch": int(flops_ext), "launch_ms": round(ext_ms, 5),
             "peak_source": f"{peak_src} bf16_tflops (burst)",
             "frac_of_sustained": round(tf / tflops_sus, 4) if tflops_sus else None}
@@ -414,8 +424,10 @@ def run_gpu(args, rank, world, local_rank):
     # the dominant part of the step (the longer of extend and decode) is the
     # kernel the line's roofline describes; both are in "rooflines"
     dominant = max(roofs, key=lambda k: roofs[k]["launch_ms"])
-    out["kv_store"] = {"ms": ms_of["store"], "gbs": 2 * len(prob.new_slots) * kv_row / (ms_of["store"] / 1e3) / 1e9}
-    if st.kv_fp8:
+    if not st.kv_fp8:
+        out["kv_store"] = {"ms": ms_of["store"],
+                           "gbs": 2 * len(prob.new_slots) * kv_row / (ms_of["store"] / 1e3) / 1e9}
+    else:
         f8 = ms_of["store_fp8"]
         n_vals = len(prob.new_slots) * prob.hkv * prob.d
         out["kv_store_fp8"] = {"ms": f8, "gbs": 2 * n_vals * (2 + 1) / (f8 / 1e3) / 1e9}
@@ -438,8 +450,8 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk.summary(), "parts": out, "wall_s_timed_loop": round(t_wall, 3),
     }
     if st.kv_fp8:
-        line["config"]["kv_fp8"] = ("decode reads E4M3 pools (scale 1; cached rows quantized at set-up), and the "
-                                    "step also stores its K/V rows as codes (extra part); extend reads bf16 pools")
+        line["config"]["kv_fp8"] = ("the step on E4M3 pools (scale 1; cached rows quantized at set-up): its K/V "
+                                    "rows stored as codes, extend and decode over the codes")
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(prob, args.workload, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -1149,7 +1161,7 @@ def main():
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="override the pool size (profiling runs on a smaller device footprint)")
     ap.add_argument("--kv-fp8", action="store_true",
-                    help="decode over FP8 (E4M3) pools; the step also stores its K/V rows as codes")
+                    help="the step on FP8 (E4M3) pools: K/V rows stored as codes, extend and decode over them")
     ap.add_argument("--rope", type=float, default=0.0, metavar="BASE",
                     help="add rotary position embedding to the step (K fused into the store, q in place)")
     ap.add_argument("--graph", action="store_true",

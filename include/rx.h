@@ -276,8 +276,8 @@ int rx_kv_store(const rx_kv_pool *pool, const void *k_new, const void *v_new, co
  * mantissa), magnitudes past 448 saturate to 448 and NaN stays NaN.
  * k_new, v_new: device bf16 [n, Hkv, d], 16-byte aligned; pools 8-byte
  * aligned; Hkv * d a multiple of 8.  A slot id outside the pool sets
- * RX_DEV_BAD_SLOT and its row is not written.  rx_attn_decode_fp8 reads
- * such pools; extend reads bf16 pools. */
+ * RX_DEV_BAD_SLOT and its row is not written.  rx_attn_decode_fp8 and
+ * rx_attn_extend_fp8 read such pools. */
 typedef struct {
     void *k;          /* device uint8 [num_layers,] num_slots, num_kv_heads, head_dim */
     void *v;
@@ -498,7 +498,7 @@ int rx_attn_decode_static(const rx_kv_pool *pool, const void *q, void *o, float 
                           int32_t max_seq_len, const rx_decode_plan *plan_or_null, float sm_scale,
                           int32_t *dev_status, void *stream);
 
-/* ---- decode over FP8 pools ------------------------------------------------ */
+/* ---- attention over FP8 pools --------------------------------------------- */
 
 /* Decode attention over FP8 pools: rx_attn_decode's definition applied to the
  * values E4M3(code) * scale of each pool, with the same arguments (q, o and
@@ -518,6 +518,24 @@ int rx_attn_decode_fp8(const rx_kv_pool_fp8 *pool, const void *q, void *o, float
                        const int32_t *req_idx, const int32_t *seq_len, const int32_t *req_to_token,
                        int64_t rtt_stride, int32_t batch, int32_t max_seq_len, const rx_decode_plan *plan,
                        void *workspace, size_t ws_bytes, float sm_scale, int32_t *dev_status, void *stream);
+
+/* Extend attention over FP8 pools: rx_attn_extend's definition applied to
+ * the values E4M3(code) * scale of each pool, with the same arguments (q, o,
+ * lse, qo_indptr, req_idx, prefix_len, extend_len, req_to_token and
+ * max_extend_len as there).  The staged path only: a workspace of
+ * rx_attn_extend_workspace(...) bytes is required (RX_ERR_UNSUPPORTED
+ * without one).  The staging copy reads the code rows (num_kv_heads *
+ * head_dim bytes each, half a bf16 pool's) and widens them to bf16 -- exactly,
+ * since every E4M3 value is a bf16 value -- so the attention kernel runs as
+ * on a bf16 pool holding E4M3(code), with K's scale folded into the score
+ * scale and V's into the output.  With both scales 1 the result is bit for
+ * bit rx_attn_extend's on such a pool.  Pools 8-byte aligned; head_dim 64 or
+ * 128 and the head counts rx_attn_extend takes. */
+int rx_attn_extend_fp8(const rx_kv_pool_fp8 *pool, const void *q, void *o, float *lse_or_null,
+                       int32_t num_q_heads, const int32_t *qo_indptr, const int32_t *req_idx,
+                       const int32_t *prefix_len, const int32_t *extend_len, const int32_t *req_to_token,
+                       int64_t rtt_stride, int32_t batch, int32_t max_extend_len, void *workspace,
+                       size_t ws_bytes, float sm_scale, int32_t *dev_status, void *stream);
 
 /* ---- compressed finite-state machine (constrained decoding) -------------
  * Source: "SGLang: Efficient Execution of Structured Language Model

@@ -110,6 +110,8 @@ class KVPoolFp8(ctypes.Structure):
 _sig("rx_kv_store_fp8", ctypes.c_int, ctypes.POINTER(KVPoolFp8), _P, _P, _P, _I64, _P, _P)
 _sig("rx_attn_decode_fp8", ctypes.c_int, ctypes.POINTER(KVPoolFp8), _P, _P, _P, _I32, _P, _P, _P, _I64, _I32,
      _I32, _P, _P, ctypes.c_size_t, ctypes.c_float, _P, _P)
+_sig("rx_attn_extend_fp8", ctypes.c_int, ctypes.POINTER(KVPoolFp8), _P, _P, _P, _I32, _P, _P, _P, _P, _P,
+     _I64, _I32, _I32, _P, ctypes.c_size_t, ctypes.c_float, _P, _P)
 
 
 class FsmInfo(ctypes.Structure):
@@ -668,6 +670,36 @@ def rx_kv_store_fp8(k_pool, v_pool, k_scale: float, v_scale: float, k_new, v_new
                      int(layer))
     _check(_lib.rx_kv_store_fp8(ctypes.byref(pool), _ptr(k_new), _ptr(v_new), _ptr(slots), n,
                                 _ptr(dev_status), _stream(stream)))
+
+
+def rx_attn_extend_fp8(k_pool, v_pool, k_scale: float, v_scale: float, q, o, lse, qo_indptr, req_idx,
+                       prefix_len, extend_len, req_to_token, max_extend_len: int, sm_scale: float, workspace,
+                       dev_status=None, stream=None, layer: int = 0) -> None:
+    """Extend attention over uint8 E4M3 pools ([L,] S, Hkv, d) with per-pool
+    scales; the staged path only (a workspace of rx_attn_extend_workspace(...)
+    bytes is required)."""
+    torch = _torch()
+    _dev(k_pool, torch.uint8, "k_pool")
+    _dev(v_pool, torch.uint8, "v_pool")
+    for t, n in ((q, "q"), (o, "o")):
+        _dev(t, torch.bfloat16, n)
+    _dev(lse, torch.float32, "lse")
+    for t, n in ((qo_indptr, "qo_indptr"), (req_idx, "req_idx"), (prefix_len, "prefix_len"),
+                 (extend_len, "extend_len"), (req_to_token, "req_to_token")):
+        _dev(t, torch.int32, n)
+    _dev(dev_status, torch.int32, "dev_status")
+    _dev(workspace, torch.uint8, "workspace")
+    if q.dim() != 3 or q.shape != o.shape:
+        raise ValueError("q and o must be [tokens, num_q_heads, head_dim]")
+    S, hkv, d, L = _pool_dims(k_pool, v_pool, layer)
+    pool = KVPoolFp8(k_pool.data_ptr(), v_pool.data_ptr(), S, hkv, d, float(k_scale), float(v_scale), L,
+                     int(layer))
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _check(_lib.rx_attn_extend_fp8(ctypes.byref(pool), _ptr(q), _ptr(o), _ptr(lse), q.shape[1],
+                                   _ptr(qo_indptr), _ptr(req_idx), _ptr(prefix_len), _ptr(extend_len),
+                                   _ptr(req_to_token), req_to_token.shape[1], req_idx.numel(),
+                                   int(max_extend_len), _ptr(workspace), ws_bytes, float(sm_scale),
+                                   _ptr(dev_status), _stream(stream)))
 
 
 def rx_attn_decode_fp8(k_pool, v_pool, k_scale: float, v_scale: float, q, o, lse, req_idx, seq_len, req_to_token,

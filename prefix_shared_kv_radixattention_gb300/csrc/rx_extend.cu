@@ -119,7 +119,8 @@ struct XParams {  // 64-byte aligned through its tensor maps
     const int32_t *extend_len;
     const int32_t *rtt;
     int64_t rtt_stride;
-    float scale_log2;
+    float scale_log2;       // sm_scale log2(e), times K's scale for an FP8 pool
+    float v_scale;          // V's scale for an FP8 pool (multiplies o); 1 otherwise
     int32_t *status;
 };
 
@@ -509,7 +510,7 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
     const bool valid = row < T.M;
     const int G = p.G;
     const int64_t orow = (T.qbase + row / G) * p.hq + (int64_t)T.g * G + row % G;
-    const float inv = 1.f / l;
+    const float inv = p.v_scale / l;
 #pragma unroll
     for (int c4 = 0; c4 < D / 32; ++c4) {
         uint32_t r[32];
@@ -746,13 +747,32 @@ __global__ void __launch_bounds__(1024) ctx_offsets_kernel(const int32_t *prefix
     }
 }
 
+// Eight E4M3 codes (element 0 in the low byte) as eight bf16: every E4M3
+// value, subnormals included, is exact in f16 and in bf16, so the widening
+// through f16 is exact.
+__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 c)
+{
+    const uint32_t w[2] = {c.x, c.y};
+    uint32_t r[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t h = rx::e4m3x2_to_f16x2((uint16_t)(w[k >> 1] >> (16 * (k & 1))));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+        r[k] = rx::pack_bf16(f.x, f.y);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 // Packed row offs[b] + i = pool row req_to_token[req_idx[b]][share[b] kBN + i]
 // for K and V (all kv heads: one contiguous row of the pool each), zeros from
 // the end of the context to the kBN-row boundary and for slot ids outside the
 // pool (flagged).  One warp per block of kStageBlock rows; every request's
 // region is a multiple of kBN rows, so a block never straddles two requests.
+// F8: the pools hold E4M3 codes (a byte a value), widened to bf16 on the way
+// (their scales are applied by the attention kernel).
+template <bool F8>
 __global__ void __launch_bounds__(256) stage_rows_kernel(
-    const bf16 *__restrict__ k_pool, const bf16 *__restrict__ v_pool, int64_t num_slots,
+    const void *__restrict__ k_pool, const void *__restrict__ v_pool, int64_t num_slots,
     const int32_t *__restrict__ rtt, int64_t rtt_stride, const int32_t *__restrict__ req_idx,
     const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ extend_len,
     const int32_t *__restrict__ share, int batch, const int64_t *__restrict__ offs, int64_t cap,
@@ -786,14 +806,24 @@ __global__ void __launch_bounds__(256) stage_rows_kernel(
 #pragma unroll 4
         for (int r = 0; r < kStageBlock; ++r) {
             const int32_t sl = __shfl_sync(0xffffffffu, my_slot, r);
-            const uint4 *ksrc = reinterpret_cast<const uint4 *>(k_pool + (int64_t)(sl < 0 ? 0 : sl) * row_elems);
-            const uint4 *vsrc = reinterpret_cast<const uint4 *>(v_pool + (int64_t)(sl < 0 ? 0 : sl) * row_elems);
+            // source row: row_elems values of 2 bytes (bf16) or 1 (codes)
+            const int64_t src_off = (int64_t)(sl < 0 ? 0 : sl) * row_elems * (F8 ? 1 : 2);
+            const unsigned char *ksrc = static_cast<const unsigned char *>(k_pool) + src_off;
+            const unsigned char *vsrc = static_cast<const unsigned char *>(v_pool) + src_off;
             uint4 *kdst = reinterpret_cast<uint4 *>(ks + (row0 + r) * row_elems);
             uint4 *vdst = reinterpret_cast<uint4 *>(vs + (row0 + r) * row_elems);
             for (int v = lane; v < row_vecs; v += 32) {
                 const uint4 z = make_uint4(0, 0, 0, 0);
-                const uint4 kv = sl >= 0 ? __ldg(ksrc + v) : z;
-                const uint4 vv = sl >= 0 ? __ldg(vsrc + v) : z;
+                uint4 kv = z, vv = z;
+                if (sl >= 0) {
+                    if constexpr (F8) {
+                        kv = e4m3x8_to_bf16x8(__ldg(reinterpret_cast<const uint2 *>(ksrc) + v));
+                        vv = e4m3x8_to_bf16x8(__ldg(reinterpret_cast<const uint2 *>(vsrc) + v));
+                    } else {
+                        kv = __ldg(reinterpret_cast<const uint4 *>(ksrc) + v);
+                        vv = __ldg(reinterpret_cast<const uint4 *>(vsrc) + v);
+                    }
+                }
                 kdst[v] = kv;
                 vdst[v] = vv;
             }
@@ -896,63 +926,77 @@ int launch_extend(const XParams &p, dim3 grid, cudaStream_t st)
 
 }  // namespace
 
-extern "C" int rx_attn_extend(const rx_kv_pool *pool_in, const void *q, void *o, float *lse,
-                              int32_t hq, const int32_t *qo_indptr, const int32_t *req_idx,
-                              const int32_t *prefix_len, const int32_t *extend_len,
-                              const int32_t *rtt, int64_t rtt_stride, int32_t batch,
-                              int32_t max_extend_len, void *workspace, size_t ws_bytes, float sm_scale,
-                              int32_t *dev_status, void *stream)
+namespace {
+
+// One layer of the pool an extend call reads: bf16 rows, or E4M3 codes with
+// a scale per pool.
+struct ExtendPool {
+    const void *k, *v;
+    int64_t num_slots;
+    int hkv, D;
+    bool f8;
+    float k_scale, v_scale;
+};
+
+// rx_attn_extend and rx_attn_extend_fp8 after their pool checks (`who`
+// names the entry point in messages).
+int extend_call(const char *who, const ExtendPool &pool, const void *q, void *o, float *lse, int32_t hq,
+                const int32_t *qo_indptr, const int32_t *req_idx, const int32_t *prefix_len,
+                const int32_t *extend_len, const int32_t *rtt, int64_t rtt_stride, int32_t batch,
+                int32_t max_extend_len, void *workspace, size_t ws_bytes, float sm_scale, int32_t *dev_status,
+                void *stream)
 {
-    rx_kv_pool layer_view;
-    if (const int rc = rx_pool_layer(pool_in, &layer_view, 0, "rx_attn_extend")) return rc;
-    const rx_kv_pool *pool = pool_in ? &layer_view : nullptr;
-    int rc = check_pool(pool);
-    if (rc != RX_OK) return rc;
     if (!q || !o || !qo_indptr || !req_idx || !prefix_len || !extend_len || !rtt ||
         rtt_stride <= 0 || rtt_stride > INT32_MAX || batch < 0 || hq <= 0 || max_extend_len < 0 ||
         !(sm_scale > 0.f))
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_extend: invalid argument");
-    if (hq % pool->num_kv_heads != 0 || kRows % (hq / pool->num_kv_heads) != 0)
-        return rx_set_error(RX_ERR_UNSUPPORTED,
-                            "rx_attn_extend: %d q heads over %d kv heads (need G | 128)", hq,
-                            pool->num_kv_heads);
-    if (rx_misaligned16(q) || rx_misaligned16(o) || rx_misaligned16(pool->k) ||
-        rx_misaligned16(pool->v) || (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_extend: q, o and the pools must be 16-byte aligned");
+        return rx_set_error(RX_ERR_INVALID, "%s: invalid argument", who);
+    if (hq % pool.hkv != 0 || kRows % (hq / pool.hkv) != 0)
+        return rx_set_error(RX_ERR_UNSUPPORTED, "%s: %d q heads over %d kv heads (need G | 128)", who, hq,
+                            pool.hkv);
+    // bf16 rows move in 16-byte pieces; code rows in 8-byte ones
+    const uintptr_t pool_align = pool.f8 ? 7 : 15;
+    if (rx_misaligned16(q) || rx_misaligned16(o) || (reinterpret_cast<uintptr_t>(pool.k) & pool_align) != 0 ||
+        (reinterpret_cast<uintptr_t>(pool.v) & pool_align) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
+        return rx_set_error(RX_ERR_INVALID, "%s: q and o must be 16-byte aligned, the pools %d-byte aligned", who,
+                            (int)pool_align + 1);
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_extend: workspace must be 256-byte aligned");
+        return rx_set_error(RX_ERR_INVALID, "%s: workspace must be 256-byte aligned", who);
+    if (pool.f8 && !workspace)
+        return rx_set_error(RX_ERR_UNSUPPORTED, "%s: FP8 pools need a workspace (the staged path)", who);
     if (batch == 0 || max_extend_len == 0) return RX_OK;
-    if (batch > 65535 || pool->num_kv_heads > 65535)
-        return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_extend: batch or kv heads above 65535");
+    if (batch > 65535 || pool.hkv > 65535)
+        return rx_set_error(RX_ERR_UNSUPPORTED, "%s: batch or kv heads above 65535", who);
     XParams p{};
     p.q = (const bf16 *)q;
     p.o = (bf16 *)o;
     p.lse = lse;
-    p.k_pool = (const bf16 *)pool->k;
-    p.v_pool = (const bf16 *)pool->v;
-    p.num_slots = pool->num_slots;
+    p.k_pool = pool.f8 ? nullptr : (const bf16 *)pool.k;
+    p.v_pool = pool.f8 ? nullptr : (const bf16 *)pool.v;
+    p.num_slots = pool.num_slots;
     p.hq = hq;
-    p.hkv = pool->num_kv_heads;
-    p.G = hq / pool->num_kv_heads;
+    p.hkv = pool.hkv;
+    p.G = hq / pool.hkv;
     p.qo_indptr = qo_indptr;
     p.req_idx = req_idx;
     p.prefix_len = prefix_len;
     p.extend_len = extend_len;
     p.rtt = rtt;
     p.rtt_stride = rtt_stride;
-    p.scale_log2 = sm_scale * rx::kLog2e;
+    p.scale_log2 = sm_scale * pool.k_scale * rx::kLog2e;
+    p.v_scale = pool.v_scale;
     p.status = dev_status;
     const int tb = kCtaRows / p.G;
     dim3 grid((unsigned)((max_extend_len + tb - 1) / tb), (unsigned)p.hkv, (unsigned)batch);
     cudaStream_t st = (cudaStream_t)stream;
-    const int D = pool->head_dim;
+    const int D = pool.D;
+    int rc = RX_OK;
     if (!workspace)
         return D == 128 ? launch_extend<128, false>(p, grid, st) : launch_extend<64, false>(p, grid, st);
 
     // staged path: offsets, packed copy of every context, then attention
     const int64_t row_bytes = (int64_t)p.hkv * D * (int64_t)sizeof(bf16);
     const int64_t cap = stage_cap_for(ws_bytes, batch, row_bytes);
-    if (cap < kBN) return rx_set_error(RX_ERR_CAPACITY, "rx_attn_extend: workspace of %zu bytes too small", ws_bytes);
+    if (cap < kBN) return rx_set_error(RX_ERR_CAPACITY, "%s: workspace of %zu bytes too small", who, ws_bytes);
     const StageLayout lay = stage_layout(cap, batch, row_bytes);
     int64_t *offs = static_cast<int64_t *>(workspace);
     bf16 *ks = reinterpret_cast<bf16 *>(static_cast<char *>(workspace) + lay.off_k);
@@ -973,11 +1017,50 @@ extern "C" int rx_attn_extend(const rx_kv_pool *pool_in, const void *q, void *o,
     ctx_offsets_kernel<<<1, 1024, 0, st>>>(prefix_len, extend_len, share, batch, rtt_stride, cap, offs,
                                            dev_status);
     RX_CUDA_CHECK(cudaGetLastError());
-    stage_rows_kernel<<<sms * 8, 256, 0, st>>>(p.k_pool, p.v_pool, p.num_slots, rtt, rtt_stride, req_idx,
-                                               prefix_len, extend_len, share, batch, offs, cap, ks, vs,
-                                               p.hkv * D, dev_status);
+    auto stage = pool.f8 ? stage_rows_kernel<true> : stage_rows_kernel<false>;
+    stage<<<sms * 8, 256, 0, st>>>(pool.k, pool.v, p.num_slots, rtt, rtt_stride, req_idx, prefix_len, extend_len,
+                                   share, batch, offs, cap, ks, vs, p.hkv * D, dev_status);
     RX_CUDA_CHECK(cudaGetLastError());
     return D == 128 ? launch_extend<128, true>(p, grid, st) : launch_extend<64, true>(p, grid, st);
+}
+
+}  // namespace
+
+extern "C" int rx_attn_extend(const rx_kv_pool *pool_in, const void *q, void *o, float *lse,
+                              int32_t hq, const int32_t *qo_indptr, const int32_t *req_idx,
+                              const int32_t *prefix_len, const int32_t *extend_len,
+                              const int32_t *rtt, int64_t rtt_stride, int32_t batch,
+                              int32_t max_extend_len, void *workspace, size_t ws_bytes, float sm_scale,
+                              int32_t *dev_status, void *stream)
+{
+    rx_kv_pool layer_view;
+    if (const int rc = rx_pool_layer(pool_in, &layer_view, 0, "rx_attn_extend")) return rc;
+    const rx_kv_pool *pool = pool_in ? &layer_view : nullptr;
+    if (const int rc = check_pool(pool)) return rc;
+    const ExtendPool ep{pool->k, pool->v, pool->num_slots, pool->num_kv_heads, pool->head_dim, false, 1.f, 1.f};
+    return extend_call("rx_attn_extend", ep, q, o, lse, hq, qo_indptr, req_idx, prefix_len, extend_len, rtt,
+                       rtt_stride, batch, max_extend_len, workspace, ws_bytes, sm_scale, dev_status, stream);
+}
+
+extern "C" int rx_attn_extend_fp8(const rx_kv_pool_fp8 *pool_in, const void *q, void *o, float *lse,
+                                  int32_t hq, const int32_t *qo_indptr, const int32_t *req_idx,
+                                  const int32_t *prefix_len, const int32_t *extend_len, const int32_t *rtt,
+                                  int64_t rtt_stride, int32_t batch, int32_t max_extend_len, void *workspace,
+                                  size_t ws_bytes, float sm_scale, int32_t *dev_status, void *stream)
+{
+    rx_kv_pool_fp8 layer_view;
+    if (const int rc = rx_pool_layer(pool_in, &layer_view, 1, "rx_attn_extend_fp8")) return rc;
+    const rx_kv_pool_fp8 *pool = pool_in ? &layer_view : nullptr;
+    if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0 ||
+        !(pool->k_scale > 0.f) || !(pool->v_scale > 0.f))
+        return rx_set_error(RX_ERR_INVALID, "rx_attn_extend_fp8: invalid pool");
+    if (pool->head_dim != 64 && pool->head_dim != 128)
+        return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_extend_fp8: head_dim %d (supported: 64, 128)",
+                            pool->head_dim);
+    const ExtendPool ep{pool->k, pool->v, pool->num_slots, pool->num_kv_heads, pool->head_dim, true,
+                        pool->k_scale, pool->v_scale};
+    return extend_call("rx_attn_extend_fp8", ep, q, o, lse, hq, qo_indptr, req_idx, prefix_len, extend_len, rtt,
+                       rtt_stride, batch, max_extend_len, workspace, ws_bytes, sm_scale, dev_status, stream);
 }
 
 extern "C" size_t rx_attn_extend_workspace(int64_t total_ctx_tokens, int32_t batch, int32_t num_kv_heads,

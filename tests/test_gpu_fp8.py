@@ -160,3 +160,101 @@ def test_decode_fp8_bad_slot_is_flagged():
     o, _, _ = _decode_fp8(prob, kd, vd, 1.0, 1.0, status, kv_chunk=64)
     assert int(status.item()) & rx.RX_DEV_BAD_SLOT
     assert np.isfinite(o).all()
+
+
+# ---------------------------------------------------------------------------
+# extend over FP8 pools (rx_attn_extend_fp8)
+# ---------------------------------------------------------------------------
+
+
+def _extend_fp8(prob, kd, vd, ks, vs, status):
+    from tests import _gpu as g
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    B = len(prob.ext_req_idx)
+    ctx = int((prob.ext_prefix_len + prob.ext_extend_len).sum())
+    ws = torch.empty(rx.rx_attn_extend_workspace(ctx, B, prob.hkv, prob.d), dtype=torch.uint8, device="cuda")
+    q = g.to_dev(prob.q_ext)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    rx.rx_attn_extend_fp8(kd, vd, ks, vs, q, o, lse, g.i32(prob.qo_indptr), g.i32(prob.ext_req_idx),
+                          g.i32(prob.ext_prefix_len), g.i32(prob.ext_extend_len), g.i32(prob.req_to_token),
+                          int(prob.ext_extend_len.max()), prob.sm_scale, ws, status)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def _extend_rows(prob):
+    """Query rows of the extend pass for the attention oracle: new token i of
+    request b reads its slot list's positions 0 .. prefix_len[b] + i."""
+    q_row, kend = [], []
+    for b, r in enumerate(prob.ext_req_idx):
+        P, E = int(prob.ext_prefix_len[b]), int(prob.ext_extend_len[b])
+        q_row += [int(r)] * E
+        kend += list(range(P + 1, P + E + 1))
+    n = len(q_row)
+    return np.asarray(q_row, np.int32), np.zeros(n, np.int32), np.asarray(kend, np.int32)
+
+
+def _extend_problems():
+    return {
+        "tiny": lambda: inputs.tiny_extend(),
+        "ragged GQA": lambda: inputs.ragged(611, hq=32, hkv=8, d=128, n_groups=3, per_group=3, shared_max=300,
+                                            private_max=200, extend_max=300, decode=False, num_slots=8000),
+        "shared prefixes": lambda: inputs.cached_prefix_extend(hq=16, hkv=4, d=64, n_prefix=2, per_prefix=3,
+                                                               prefix=384, extend=200, num_slots=6000),
+    }
+
+
+@pytest.mark.parametrize("name,ks,vs", [("tiny", 1.0, 1.0), ("ragged GQA", 0.37, 2.5),
+                                        ("shared prefixes", 1.5, 0.25)])
+def test_extend_fp8_matches_oracle(name, ks, vs):
+    """Extend over E4M3 pools against the oracle's attention over decoded
+    codes with the pools' scales: several tiles, ragged tails, and requests
+    whose shared prefix tiles are staged once."""
+    from tests import _gpu as g
+    prob = _extend_problems()[name]()
+    kd, vd, kc, vc, status = _fp8_problem(prob, ks, vs, 41)
+    o, lse = _extend_fp8(prob, kd, vd, ks, vs, status)
+    assert int(status.item()) == 0
+    q_row, kbeg, kend = _extend_rows(prob)
+    ro, rl = fp8.attention(prob.q_ext, kc, vc, ks, vs, prob.req_to_token, q_row, kbeg, kend, prob.sm_scale)
+    g.compare(o.float().cpu().numpy(), ro, f"fp8 extend {name}")
+    g.compare_lse(lse.cpu().numpy(), rl, f"fp8 extend {name}")
+
+
+@pytest.mark.parametrize("name", ["ragged GQA", "shared prefixes"])
+def test_extend_fp8_unit_scales_equal_bf16_pool_bitwise(name):
+    """With both scales 1, extend over codes is rx_attn_extend over a bf16
+    pool that holds the decoded codes, bit for bit: the staging copy widens
+    codes exactly and the attention kernel is the same."""
+    from tests import _gpu as g
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = _extend_problems()[name]()
+    kd, vd, kc, vc, status = _fp8_problem(prob, 1.0, 1.0, 43)
+    o8, l8 = _extend_fp8(prob, kd, vd, 1.0, 1.0, status)
+    kb, vb = g.to_dev(fp8.bf16_bits(kc)), g.to_dev(fp8.bf16_bits(vc))
+    B = len(prob.ext_req_idx)
+    ctx = int((prob.ext_prefix_len + prob.ext_extend_len).sum())
+    ws = torch.empty(rx.rx_attn_extend_workspace(ctx, B, prob.hkv, prob.d), dtype=torch.uint8, device="cuda")
+    q = g.to_dev(prob.q_ext)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    rx.rx_attn_extend(kb, vb, q, o, lse, g.i32(prob.qo_indptr), g.i32(prob.ext_req_idx), g.i32(prob.ext_prefix_len),
+                      g.i32(prob.ext_extend_len), g.i32(prob.req_to_token), int(prob.ext_extend_len.max()),
+                      prob.sm_scale, status, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(g.to_host_u16(o8), g.to_host_u16(o))
+    assert np.array_equal(l8.cpu().numpy().view(np.uint32), lse.cpu().numpy().view(np.uint32))
+
+
+def test_extend_fp8_bad_slot_is_flagged():
+    from tests import _gpu as g
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.tiny_extend()
+    prob.req_to_token = prob.req_to_token.copy()
+    prob.req_to_token[int(prob.ext_req_idx[1]), 3] = prob.num_slots + 5
+    kd, vd, kc, vc, status = _fp8_problem(prob, 1.0, 1.0, 5)
+    o, _ = _extend_fp8(prob, kd, vd, 1.0, 1.0, status)
+    assert int(status.item()) & rx.RX_DEV_BAD_SLOT
+    assert torch.isfinite(o.float()).all()

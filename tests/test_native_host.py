@@ -61,6 +61,8 @@ def test_layer_outside_the_pool_is_rejected_before_any_launch():
                                        ctypes.c_float(0.125), None, None),
             lambda: lib.rx_attn_decode(ctypes.byref(pool), P, P, None, 2, P, P, P, 64, 1, 8, None, None, 0,
                                        ctypes.c_float(0.125), None, None),
+            lambda: lib.rx_attn_extend_fp8(ctypes.byref(p8), P, P, None, 2, P, P, P, P, P, 64, 1, 8, P, 1 << 20,
+                                           ctypes.c_float(0.125), None, None),
             lambda: lib.rx_attn_decode_static(ctypes.byref(pool), P, P, None, 2, P, P, P, 64, 1, 8, None,
                                               ctypes.c_float(0.125), None, None),
         ]
@@ -87,6 +89,32 @@ def test_fp8_decode_rejects_unsupported_heads_and_missing_plan():
     pool = rx.KVPoolFp8(fake, fake, 64, 8, 128, 1.0, 1.0, 0, 0)
     assert lib.rx_attn_decode_fp8(ctypes.byref(pool), P, P, None, 32, P, P, P, 64, 2, 8, ctypes.byref(per_head), P,
                                   1 << 20, ctypes.c_float(0.1), None, None) == rx.RX_ERR_UNSUPPORTED
+
+
+def test_fp8_extend_checks_before_any_launch():
+    """rx_attn_extend_fp8 needs a workspace (the staged path), valid scales,
+    head_dim 64 or 128 and 8-byte aligned pools; each is refused before any
+    device work (the pointers here are never dereferenced)."""
+    import ctypes
+    lib = rx.library()
+    fake = 0x100000
+    P = ctypes.c_void_p(fake)
+
+    def call(pool, ws=P, ws_bytes=1 << 20, hq=4):
+        return lib.rx_attn_extend_fp8(ctypes.byref(pool), P, P, None, hq, P, P, P, P, P, 64, 2, 8, ws, ws_bytes,
+                                      ctypes.c_float(0.125), None, None)
+
+    good = rx.KVPoolFp8(fake, fake, 64, 4, 128, 1.0, 1.0, 0, 0)
+    assert call(good, ws=None, ws_bytes=0) == rx.RX_ERR_UNSUPPORTED
+    assert "workspace" in rx.last_error()
+    assert call(rx.KVPoolFp8(fake, fake, 64, 4, 128, 0.0, 1.0, 0, 0)) == rx.RX_ERR_INVALID
+    assert call(rx.KVPoolFp8(fake, fake, 64, 4, 128, 1.0, -1.0, 0, 0)) == rx.RX_ERR_INVALID
+    assert call(rx.KVPoolFp8(fake, fake, 64, 4, 96, 1.0, 1.0, 0, 0)) == rx.RX_ERR_UNSUPPORTED
+    assert call(rx.KVPoolFp8(fake + 4, fake, 64, 4, 128, 1.0, 1.0, 0, 0)) == rx.RX_ERR_INVALID
+    assert call(good, hq=6) == rx.RX_ERR_UNSUPPORTED            # 6 q heads over 4 kv heads
+    # an empty batch is a no-op once the arguments check out
+    assert lib.rx_attn_extend_fp8(ctypes.byref(good), P, P, None, 4, P, P, P, P, P, 64, 0, 8, P, 1 << 20,
+                                  ctypes.c_float(0.125), None, None) == rx.RX_OK
 
 
 # ---------------------------------------------------------------------------
