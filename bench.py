@@ -505,26 +505,47 @@ def job_throughput(units_per_rank_step: float, world: int, steps: int, max_ms: f
 
 class E2EPipeline:
     """One step of the path as a caller drives it through the public API with
-    host buffers, its copies overlapped with the kernels: the new K/V rows,
-    their slots and the decode queries go in first on an input stream, then
-    the extend queries in request chunks; the compute stream stores the rows,
-    runs decode as soon as its queries are in, and runs each chunk's extend
-    (rx_attn_extend over that chunk's requests) as soon as the chunk's
-    queries are in; an output stream copies each result back as soon as it
-    is written.  The same calls, on the same data, as the step."""
+    host buffers, its copies overlapped with the kernels.  An input stream
+    brings in, in this order: the decode requests' new K/V rows, slots and
+    queries; then, per chunk of extend requests, the chunk's new K/V rows,
+    slots and queries.  The compute stream stores the decode rows and runs
+    decode as soon as they are in, and for each chunk stores its rows and
+    runs its extend (rx_kv_store and rx_attn_extend over the chunk) as soon
+    as the chunk is in; an output stream copies each result back as soon as
+    it is written.  The host link (about 200 GB/s each way on this machine)
+    is slower than the kernels, so decode goes first (its inputs are small,
+    and it runs while the first chunk arrives) and the chunks grow, then
+    shrink (little to wait for at the start, little to copy back after the
+    last kernel).  Where a chunk's new rows are not one contiguous range of
+    the step's rows, every new row goes in before the first store instead.
+    The same calls, on the same data, as the step."""
 
-    def __init__(self, st, torch, rx, chunks=4):
+    FRACTIONS = (0.14, 0.24, 0.28, 0.22, 0.12)   # extend requests per chunk, in order
+
+    def __init__(self, st, torch, rx, fractions=FRACTIONS):
         self.st, self.torch, self.rx = st, torch, rx
         p = st.prob
         pin = lambda t: t.cpu().pin_memory()
-        self.h_kv = [pin(st.k_new), pin(st.v_new), pin(st.slots)]
-        self.d_kv = [st.k_new, st.v_new, st.slots]
-        self.h_in, self.h_out = list(self.h_kv), []
+        self.h_k, self.h_v, self.h_sl = pin(st.k_new), pin(st.v_new), pin(st.slots)
+        self.h_in, self.h_out = [self.h_k, self.h_v, self.h_sl], []
+        # the new row of each slot: which rows the decode part and each chunk store
+        row_of = {int(s): i for i, s in enumerate(p.new_slots)}
+        n_new = len(p.new_slots)
+
+        def rows_of(slots):
+            idx = sorted(row_of[int(s)] for s in slots if int(s) in row_of)
+            return (idx[0], idx[-1] + 1) if idx and idx[-1] - idx[0] + 1 == len(idx) else None
+
+        covered = 0
+        self.dec_rows = (0, 0)
         if st.has_dec:
             self.h_qd = [pin(st.q_dec), pin(st.dec_len)]
             self.h_od = torch.empty(st.o_dec.shape, dtype=st.o_dec.dtype, pin_memory=True)
             self.h_in += self.h_qd
             self.h_out.append(self.h_od)
+            dec_slots = [p.req_to_token[r, L - 1] for r, L in zip(p.dec_req_idx, p.dec_seq_len)]
+            self.dec_rows = rows_of(dec_slots) or (0, 0)
+            covered += self.dec_rows[1] - self.dec_rows[0]
         self.chunks = []
         if st.has_ext:
             self.h_qe = pin(st.q_ext)
@@ -532,19 +553,29 @@ class E2EPipeline:
             self.h_in.append(self.h_qe)
             self.h_out.append(self.h_oe)
             Be = len(p.ext_req_idx)
-            cuts = sorted(set(int(x) for x in np.linspace(0, Be, min(chunks, Be) + 1)))
+            n = min(len(fractions), Be)
+            fr = np.asarray(fractions[:n], np.float64)
+            cuts = np.round(np.cumsum(np.concatenate([[0.0], fr / fr.sum()])) * Be).astype(int)
+            cuts = sorted(set(int(x) for x in cuts))
             i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
-            max_ctx = 0
+            max_ctx, max_n = 0, 0
             for b0, b1 in zip(cuts[:-1], cuts[1:]):
                 r0, r1 = int(p.qo_indptr[b0]), int(p.qo_indptr[b1])
                 ctx = int((p.ext_prefix_len[b0:b1] + p.ext_extend_len[b0:b1]).sum())
-                max_ctx = max(max_ctx, ctx)
+                max_ctx, max_n = max(max_ctx, ctx), max(max_n, b1 - b0)
+                new_slots = np.concatenate([p.req_to_token[r, P:P + E] for r, P, E in
+                                            zip(p.ext_req_idx[b0:b1], p.ext_prefix_len[b0:b1],
+                                                p.ext_extend_len[b0:b1])])
+                kv = rows_of(new_slots) or (0, 0)
+                covered += kv[1] - kv[0]
                 self.chunks.append(dict(
-                    rows=(r0, r1), qo=i32(p.qo_indptr[b0:b1 + 1] - r0), req=i32(p.ext_req_idx[b0:b1]),
+                    rows=(r0, r1), kv=kv, qo=i32(p.qo_indptr[b0:b1 + 1] - r0), req=i32(p.ext_req_idx[b0:b1]),
                     P=i32(p.ext_prefix_len[b0:b1]), E=i32(p.ext_extend_len[b0:b1]),
                     max_E=int(p.ext_extend_len[b0:b1].max()), n=b1 - b0))
-            self.ws = torch.empty(rx.rx_attn_extend_workspace(max_ctx, max(c["n"] for c in self.chunks), p.hkv, p.d),
+            self.ws = torch.empty(rx.rx_attn_extend_workspace(max_ctx, max_n, p.hkv, p.d),
                                   dtype=torch.uint8, device="cuda")
+        # per-part stores need every new row in exactly one part
+        self.split_store = covered == n_new
         self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def bytes_in(self):
@@ -553,40 +584,59 @@ class E2EPipeline:
     def bytes_out(self):
         return sum(h.numel() * h.element_size() for h in self.h_out)
 
+    def _copy_rows(self, a, b):
+        st = self.st
+        st.k_new[a:b].copy_(self.h_k[a:b], non_blocking=True)
+        st.v_new[a:b].copy_(self.h_v[a:b], non_blocking=True)
+        st.slots[a:b].copy_(self.h_sl[a:b], non_blocking=True)
+
+    def _store_rows(self, a, b):
+        st = self.st
+        if b > a:
+            self.rx.rx_kv_store(st.k_pool, st.v_pool, st.k_new[a:b], st.v_new[a:b], st.slots[a:b], st.status)
+
     def step(self):
         torch, rx, st, p = self.torch, self.rx, self.st, self.st.prob
         E = torch.cuda.Event
         comp = torch.cuda.current_stream()
-        ev_kv, ev_qd = E(), E()
-        ev_q = [E() for _ in self.chunks]
+        split = self.split_store
+        ev_dec = E()
+        ev_c = [E() for _ in self.chunks]
         # the side streams fork from the compute stream (required when captured)
         self.s_in.wait_stream(comp)
         self.s_out.wait_stream(comp)
         with torch.cuda.stream(self.s_in):
-            for h, d in zip(self.h_kv, self.d_kv):
-                d.copy_(h, non_blocking=True)
-            ev_kv.record()
+            if split:
+                self._copy_rows(*self.dec_rows)
+            else:
+                self._copy_rows(0, len(p.new_slots))
             if st.has_dec:
                 st.q_dec.copy_(self.h_qd[0], non_blocking=True)
                 st.dec_len.copy_(self.h_qd[1], non_blocking=True)
-                ev_qd.record()
-            for c, ev in zip(self.chunks, ev_q):
+            ev_dec.record()
+            for c, ev in zip(self.chunks, ev_c):
+                if split:
+                    self._copy_rows(*c["kv"])
                 r0, r1 = c["rows"]
                 st.q_ext[r0:r1].copy_(self.h_qe[r0:r1], non_blocking=True)
                 ev.record()
-        comp.wait_event(ev_kv)
-        st.kv_store()
+        comp.wait_event(ev_dec)
+        if split:
+            self._store_rows(*self.dec_rows)
+        else:
+            st.kv_store()
         if st.has_dec:
-            comp.wait_event(ev_qd)
             st.decode()
             ev_d = E()
             ev_d.record(comp)
             self.s_out.wait_event(ev_d)
             with torch.cuda.stream(self.s_out):
                 self.h_od.copy_(st.o_dec, non_blocking=True)
-        for c, ev in zip(self.chunks, ev_q):
+        for c, ev in zip(self.chunks, ev_c):
             r0, r1 = c["rows"]
             comp.wait_event(ev)
+            if split:
+                self._store_rows(*c["kv"])
             rx.rx_attn_extend(st.k_pool, st.v_pool, st.q_ext[r0:r1], st.o_ext[r0:r1], None, c["qo"], c["req"],
                               c["P"], c["E"], st.rtt, c["max_E"], p.sm_scale, st.status, workspace=self.ws)
             ev_o = E()
@@ -687,10 +737,14 @@ def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
     out = {"value": round(job_throughput(per_step, world, 1, ms), 3), "unit": unit,
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 5),
            "steps": n, "timing": "host wall clock per step, synchronized every step",
-           "schedule": ("copies on their own streams, overlapping the kernels; extend in "
-                        f"{len(pipe.chunks)} request chunks" if pipelined and pipe.chunks else
-                        "copies on their own streams, overlapping the kernels" if pipelined else
-                        "copies in, the step, copies out, in order"),
+           "schedule": ("; ".join(["copies on their own streams, overlapping the kernels"] +
+                                  (["decode's rows and queries first"] if st.has_dec and pipe.chunks else []) +
+                                  ([f"extend in {len(pipe.chunks)} request chunks (" +
+                                    ", ".join(str(c["n"]) for c in pipe.chunks) + " requests)"]
+                                   if pipe.chunks else []) +
+                                  (["each part stores its own new rows"] if pipe.split_store and pipe.chunks else
+                                   [] if pipe.split_store else ["every new row stored first"]))
+                        if pipelined else "copies in, the step, copies out, in order"),
            "launch": "the step's calls captured once in a CUDA graph, replayed per step" if pipelined else
                      "direct calls"}
     if pipelined:
