@@ -17,6 +17,33 @@ from prefix_shared_kv_radixattention_gb300 import inputs
 ATOL, RTOL, LSE_ATOL = 2e-2, 1e-2, 1e-3
 FILL = 64.0  # unused pool rows hold this, so a wrong read shows
 
+# Output canaries: every output tensor is the middle of a larger buffer whose
+# every element -- the output's own included -- starts as a NaN bit pattern.
+# After the call the regions before and after the output must still hold it
+# bit for bit (no write out of bounds), and an output element the call did
+# not write stays NaN, which no comparison with the oracle passes.
+GUARD = 4096                      # canary elements on each side
+CANARY_BF16 = -0x003F             # 0xFFC1: a bf16 NaN (exponent all ones)
+CANARY_F32 = 0x7FC0DEAD           # an fp32 NaN
+
+
+class Guarded:
+    """An output tensor of `shape` inside canary-filled guard regions."""
+
+    def __init__(self, shape, dtype, device="cuda"):
+        self.n = int(np.prod(shape))
+        self.dtype = dtype
+        bits = torch.int16 if dtype == torch.bfloat16 else torch.int32
+        fill = CANARY_BF16 if dtype == torch.bfloat16 else CANARY_F32
+        self.buf = torch.full((self.n + 2 * GUARD,), fill, dtype=bits, device=device).view(dtype)
+        self.fill, self.bits = fill, bits
+        self.t = self.buf[GUARD:GUARD + self.n].view(shape)
+
+    def check(self, what=""):
+        raw = self.buf.view(self.bits).cpu().numpy()
+        head, tail = raw[:GUARD], raw[GUARD + self.n:]
+        assert (head == self.fill).all() and (tail == self.fill).all(), f"{what}: write outside the output"
+
 
 def to_dev(a_u16: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a_u16).view(np.int16)).view(torch.bfloat16).cuda()
@@ -71,8 +98,9 @@ class Dev:
         p = self.prob
         B = len(p.dec_req_idx)
         q = to_dev(p.q_dec)
-        o = torch.empty_like(q)
-        lse = torch.empty((B, p.hq), dtype=torch.float32, device="cuda") if with_lse else None
+        og = Guarded(q.shape, torch.bfloat16)
+        lg = Guarded((B, p.hq), torch.float32) if with_lse else None
+        o, lse = og.t, (lg.t if with_lse else None)
         dp = None
         if plan:
             lens = p.dec_seq_len if plan_seq_len is None else np.asarray(plan_seq_len, np.int32)
@@ -86,6 +114,9 @@ class Dev:
         rx.rx_attn_decode(self.k_pool, self.v_pool, q, o, lse, i32(p.dec_req_idx), i32(dev_len),
                           self.rtt, max_len, p.sm_scale, dp, ws if ws_bytes else None, self.status)
         torch.cuda.synchronize()
+        og.check("decode o")
+        if with_lse:
+            lg.check("decode lse")
         return o.float().cpu().numpy(), (lse.cpu().numpy() if with_lse else None)
 
     def extend(self, with_lse: bool = True, staged: bool = False, ws_rows=None):
@@ -93,8 +124,9 @@ class Dev:
         the problem's contexts (or for ws_rows context tokens)."""
         p = self.prob
         q = to_dev(p.q_ext)
-        o = torch.empty_like(q)
-        lse = torch.empty((q.shape[0], p.hq), dtype=torch.float32, device="cuda") if with_lse else None
+        og = Guarded(q.shape, torch.bfloat16)
+        lg = Guarded((q.shape[0], p.hq), torch.float32) if with_lse else None
+        o, lse = og.t, (lg.t if with_lse else None)
         ws = None
         if staged:
             rows = int((p.ext_prefix_len + p.ext_extend_len).sum()) if ws_rows is None else int(ws_rows)
@@ -104,6 +136,9 @@ class Dev:
                           i32(p.ext_prefix_len), i32(p.ext_extend_len), self.rtt,
                           int(p.ext_extend_len.max()), p.sm_scale, self.status, workspace=ws)
         torch.cuda.synchronize()
+        og.check("extend o")
+        if with_lse:
+            lg.check("extend lse")
         return o.float().cpu().numpy(), (lse.cpu().numpy() if with_lse else None)
 
     def status_word(self) -> int:

@@ -103,11 +103,13 @@ def _decode_fp8(prob, kd, vd, ks, vs, status, kv_chunk=0, plan_len=None):
     ws = torch.empty(max(rx.rx_attn_decode_workspace(B, prob.hq, prob.hkv, prob.d, max_len, plan), 256),
                      dtype=torch.uint8, device="cuda")
     q = g.to_dev(prob.q_dec)
-    o = torch.empty_like(q)
-    lse = torch.empty((B, prob.hq), dtype=torch.float32, device="cuda")
+    og, lg = g.Guarded(q.shape, torch.bfloat16), g.Guarded((B, prob.hq), torch.float32)
+    o, lse = og.t, lg.t
     rx.rx_attn_decode_fp8(kd, vd, ks, vs, q, o, lse, g.i32(prob.dec_req_idx), g.i32(prob.dec_seq_len),
                           g.i32(prob.req_to_token), max_len, prob.sm_scale, plan, ws, status)
     torch.cuda.synchronize()
+    og.check("fp8 decode o")
+    lg.check("fp8 decode lse")
     return o.float().cpu().numpy(), lse.cpu().numpy(), info
 
 
@@ -174,12 +176,14 @@ def _extend_fp8(prob, kd, vd, ks, vs, status):
     ctx = int((prob.ext_prefix_len + prob.ext_extend_len).sum())
     ws = torch.empty(rx.rx_attn_extend_workspace(ctx, B, prob.hkv, prob.d), dtype=torch.uint8, device="cuda")
     q = g.to_dev(prob.q_ext)
-    o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    og, lg = g.Guarded(q.shape, torch.bfloat16), g.Guarded(tuple(q.shape[:2]), torch.float32)
+    o, lse = og.t, lg.t
     rx.rx_attn_extend_fp8(kd, vd, ks, vs, q, o, lse, g.i32(prob.qo_indptr), g.i32(prob.ext_req_idx),
                           g.i32(prob.ext_prefix_len), g.i32(prob.ext_extend_len), g.i32(prob.req_to_token),
                           int(prob.ext_extend_len.max()), prob.sm_scale, ws, status)
     torch.cuda.synchronize()
+    og.check("fp8 extend o")
+    lg.check("fp8 extend lse")
     return o, lse
 
 
