@@ -394,7 +394,8 @@ def run_gpu(args, rank, world, local_rank):
         roofs["decode"] = {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "traffic": traffic, "traffic_source": tsrc,
-            "kernel": ("rx_attn_decode_fp8 (decode_gqa_kernel<F8> + merge_kernel)" if st.kv_fp8 else
+            "kernel": ("rx_attn_decode_fp8 (" + " + ".join(k if k == "merge_kernel" else k + "<F8>"
+                                                           for k in st.decode_kernels) + ")" if st.kv_fp8 else
                        "rx_attn_decode (" + " + ".join(st.decode_kernels) + ")"),
             "algorithmic_bytes_per_launch": int(uniq_bytes), "launch_ms": round(dec_ms, 5),
             "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)", "frac_of_8000": round(achieved / 8000.0, 4)}

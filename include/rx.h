@@ -501,19 +501,19 @@ int rx_attn_decode_static(const rx_kv_pool *pool, const void *q, void *o, float 
 /* ---- attention over FP8 pools --------------------------------------------- */
 
 /* Decode attention over FP8 pools: rx_attn_decode's definition applied to the
- * values E4M3(code) * scale of each pool, with the same arguments (q, o and
- * lse as there).  A plan is required, and all its items must go to the
- * all-heads kernel (rx_decode_plan_info.n_wide == n_items, which the plan
- * builder gives for these head counts unless a shared segment's requests
- * make more than 16 groups); so is a workspace of
- * rx_attn_decode_workspace(...) bytes.  Supported: 8 kv heads with 2, 4, 8
- * or 16 q heads each, head_dim 64 or 128 (RX_ERR_UNSUPPORTED otherwise).
- * The products run in f16 with fp32 sums: codes widen to f16 exactly, q is
- * converted to f16 (exact for |q| within f16's range, which q must respect;
- * values below 2^-14 round to f16 subnormals), and the softmax weights are
- * rounded to f16 rather than bf16.  K's scale multiplies the scores, V's the
- * output.  Each slot row read is num_kv_heads * head_dim bytes, half a bf16
- * pool's. */
+ * values E4M3(code) * scale of each pool, with the same arguments (q, o, lse,
+ * the plan or NULL, and a workspace of rx_attn_decode_workspace(...) bytes
+ * as there) and the same head counts and head dims.  The work goes to the
+ * same kernels as over a bf16 pool, each reading code rows (num_kv_heads *
+ * head_dim bytes, half a bf16 row's): the per-head kernel and the all-heads
+ * kernel for one q head per kv head widen codes exactly (to bf16 tiles, to
+ * fp32) and compute as on a bf16 pool holding E4M3(code) -- with both scales
+ * 1, bit for bit rx_attn_decode's result on such a pool -- while the
+ * all-heads kernel for 8 kv heads with 2 to 16 q heads each runs its products
+ * in f16 with fp32 sums: codes widen to f16 exactly, q is converted to f16
+ * (exact for |q| within f16's range, which q must respect; values below
+ * 2^-14 round to f16 subnormals), and the softmax weights are rounded to f16
+ * rather than bf16.  K's scale multiplies the scores, V's the output. */
 int rx_attn_decode_fp8(const rx_kv_pool_fp8 *pool, const void *q, void *o, float *lse, int32_t num_q_heads,
                        const int32_t *req_idx, const int32_t *seq_len, const int32_t *req_to_token,
                        int64_t rtt_stride, int32_t batch, int32_t max_seq_len, const rx_decode_plan *plan,

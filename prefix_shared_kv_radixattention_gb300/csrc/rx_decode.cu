@@ -77,9 +77,12 @@ struct Desc {
     int qrow[kMaxRows];                      // q/o row of each request of the item
 };
 
-template <int D>
+// F8: the pools hold E4M3 codes; the ring's tiles stay bf16 (codes widened on
+// the way in), with one stage fewer at d 128 to make room for two buffers of
+// a stage's codes.
+template <int D, bool F8 = false>
 struct Layout {
-    static constexpr int NST = (D == 128) ? 4 : 8;      // K/V ring stages
+    static constexpr int NST = (D == 128) ? (F8 ? 3 : 4) : 8;  // K/V ring stages
     static constexpr int RS = D + 8;                    // padded row stride (elements)
     static constexpr int TILE = kBN * RS;               // elements of one K (or V) stage
     static constexpr int QSLOT = kMaxRows * RS;         // elements of one Q slot
@@ -97,10 +100,15 @@ struct Layout {
                          B_ITFULL = B_SLEMPTY + kNSL, B_ITEMPTY = B_ITFULL + kNIT,
                          B_RED = B_ITEMPTY + kNIT, N_BAR = B_RED + 1;
     static constexpr int OFF_ABORT = OFF_BAR + N_BAR * 8;
-    static constexpr int BYTES = OFF_ABORT + 16;
+    // FP8: two buffers of one stage's codes, K then V (kBN rows of D bytes)
+    static constexpr int CODE_STAGE = 2 * kBN * D;
+    static constexpr int OFF_CODE = (OFF_ABORT + 16 + 127) / 128 * 128;
+    static constexpr int BYTES = F8 ? OFF_CODE + 2 * CODE_STAGE : OFF_ABORT + 16;
 };
 static_assert(Layout<128>::BYTES <= 227 * 1024, "shared memory budget");
 static_assert(Layout<64>::BYTES <= 227 * 1024, "shared memory budget");
+static_assert(Layout<128, true>::BYTES <= 227 * 1024, "shared memory budget");
+static_assert(Layout<64, true>::BYTES <= 227 * 1024, "shared memory budget");
 
 struct Params {
     const bf16 *q;
@@ -228,10 +236,10 @@ __device__ __forceinline__ int shfl(int v, int src) { return __shfl_sync(0xfffff
 // scheduler warp: descriptors and slot ids
 // ---------------------------------------------------------------------------
 
-template <int D, bool PLAN>
+template <int D, bool PLAN, bool F8>
 __device__ void scheduler(const Params &p, unsigned char *smem)
 {
-    using L = Layout<D>;
+    using L = Layout<D, F8>;
     Desc *descs = reinterpret_cast<Desc *>(smem + L::OFF_DESC);
     int32_t *slotbuf = reinterpret_cast<int32_t *>(smem + L::OFF_SLOT);
     const uint32_t bar = rx::smem_u32(smem + L::OFF_BAR);
@@ -311,11 +319,32 @@ __device__ void scheduler(const Params &p, unsigned char *smem)
 // copier warp: Q rows and K/V stages
 // ---------------------------------------------------------------------------
 
-template <int D>
+// Eight E4M3 codes (element 0 in the low byte) as eight bf16: every E4M3
+// value, subnormals included, is exact in f16 and in bf16.
+__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint32_t lo, uint32_t hi)
+{
+    const uint32_t w[2] = {lo, hi};
+    uint32_t r[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t h = rx::e4m3x2_to_f16x2((uint16_t)(w[k >> 1] >> (16 * (k & 1))));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+        r[k] = rx::pack_bf16(f.x, f.y);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// F8: each copier thread lands its 16-byte chunks of a tile's codes in code
+// buffer (tile & 1) with cp.async, and once they are in (one tile later, or
+// at the item's end) widens exactly those chunks into the tile's bf16 rows
+// and arrives on its full barrier itself -- no thread reads codes another
+// copied, so nothing but the thread's own cp.async groups orders the steps.
+template <int D, bool F8>
 __device__ void copier(const Params &p, unsigned char *smem)
 {
-    using L = Layout<D>;
-    constexpr int CPR = D / 8;                          // 16-byte chunks per row
+    using L = Layout<D, F8>;
+    constexpr int CPR = F8 ? D / 16 : D / 8;            // 16-byte chunks per row (codes or bf16)
+    constexpr int QCPR = D / 8;                         // 16-byte chunks per query row
     constexpr int NCT = 32 * kCopiers;                  // copier threads
     bf16 *Ks = reinterpret_cast<bf16 *>(smem + L::OFF_K);
     bf16 *Vs = reinterpret_cast<bf16 *>(smem + L::OFF_V);
@@ -338,8 +367,8 @@ __device__ void copier(const Params &p, unsigned char *smem)
                 break;
             const int Mpad = mpad_of(M);
             bf16 *qd = Qs + qs * L::QSLOT;
-            for (int idx = ct; idx < Mpad * CPR; idx += NCT) {
-                const int m = idx / CPR, c = idx % CPR;
+            for (int idx = ct; idx < Mpad * QCPR; idx += NCT) {
+                const int m = idx / QCPR, c = idx % QCPR;
                 const uint32_t dst = rx::smem_u32(qd + m * L::RS + c * 8);
                 if (m < M) {
                     const int64_t qr = d->qrow[m / p.G];
@@ -356,33 +385,91 @@ __device__ void copier(const Params &p, unsigned char *smem)
         // K/V stages: the copier threads stride over the stage's 16-byte chunks
         const int ntiles = (p1 - p0 + kBN - 1) / kBN;
         bool ok_all = true;
+        int64_t pend = -1;  // F8: the tile whose codes this thread has in flight
+        // F8: this thread's chunks of tile nt's codes -> the tile's bf16 rows,
+        // once the ring stage is free; then its arrival on the stage's full barrier
+        auto widen = [&](uint32_t nt) -> bool {
+            const uint32_t s = nt % L::NST;
+            if (!wait_or_abort(bar + 8 * (L::B_EMPTY + s), ((nt / L::NST) & 1) ^ 1, abort_flag, p.status,
+                               p.wait_cycles))
+                return false;
+            const unsigned char *cb = smem + L::OFF_CODE + (nt & 1) * L::CODE_STAGE;
+            bf16 *kd = Ks + s * L::TILE;
+            bf16 *vd = Vs + s * L::TILE;
+            for (int idx = ct; idx < kBN * CPR; idx += NCT) {
+                const int r = idx / CPR, c = idx % CPR;
+#pragma unroll
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(cb + kv * kBN * D + r * D + c * 16);
+                    uint4 *dst = reinterpret_cast<uint4 *>((kv ? vd : kd) + r * L::RS + c * 16);
+                    dst[0] = e4m3x8_to_bf16x8(w.x, w.y);
+                    dst[1] = e4m3x8_to_bf16x8(w.z, w.w);
+                }
+            }
+            rx::mbar_arrive(bar + 8 * (L::B_FULL + s));
+            return true;
+        };
         for (int t = 0; t < ntiles; ++t, ++n_tile) {
             const uint32_t sb = n_tile % kNSL, s = n_tile % L::NST;
             if (!wait_or_abort(bar + 8 * (L::B_SLFULL + sb), (n_tile / kNSL) & 1, abort_flag, p.status, p.wait_cycles) ||
-                !wait_or_abort(bar + 8 * (L::B_EMPTY + s), ((n_tile / L::NST) & 1) ^ 1, abort_flag,
-                               p.status, p.wait_cycles)) {
+                (!F8 && !wait_or_abort(bar + 8 * (L::B_EMPTY + s), ((n_tile / L::NST) & 1) ^ 1, abort_flag,
+                                       p.status, p.wait_cycles))) {
                 ok_all = false;
                 break;
             }
             const int base = p0 + t * kBN;
             const int32_t *sl = slotbuf + sb * kBN;
-            bf16 *kd = Ks + s * L::TILE;
-            bf16 *vd = Vs + s * L::TILE;
+            if constexpr (F8) {
+                unsigned char *cb = smem + L::OFF_CODE + (n_tile & 1) * L::CODE_STAGE;
 #pragma unroll 4
-            for (int idx = ct; idx < kBN * CPR; idx += NCT) {
-                const int r = idx / CPR, c = idx % CPR;
-                const int32_t slot = sl[r];
-                const bool inside = base + r < p1;
-                const bool ok = inside && slot >= 0 && (int64_t)slot < p.num_slots;
-                if (inside && !ok && c == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
-                const int64_t off = ok ? (((int64_t)slot * p.hkv + g) * D + c * 8) : 0;
-                const int dsto = r * L::RS + c * 8;
-                rx::cp_async_16(rx::smem_u32(kd + dsto), p.k_pool + off, ok ? 16 : 0);
-                rx::cp_async_16(rx::smem_u32(vd + dsto), p.v_pool + off, ok ? 16 : 0);
+                for (int idx = ct; idx < kBN * CPR; idx += NCT) {
+                    const int r = idx / CPR, c = idx % CPR;
+                    const int32_t slot = sl[r];
+                    const bool inside = base + r < p1;
+                    const bool ok = inside && slot >= 0 && (int64_t)slot < p.num_slots;
+                    if (inside && !ok && c == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
+                    const int64_t off = ok ? (((int64_t)slot * p.hkv + g) * D + c * 16) : 0;
+                    rx::cp_async_16(rx::smem_u32(cb + r * D + c * 16), p.kb + off, ok ? 16 : 0);
+                    rx::cp_async_16(rx::smem_u32(cb + kBN * D + r * D + c * 16), p.vb + off, ok ? 16 : 0);
+                }
+                rx::cp_async_commit();
+            } else {
+                bf16 *kd = Ks + s * L::TILE;
+                bf16 *vd = Vs + s * L::TILE;
+#pragma unroll 4
+                for (int idx = ct; idx < kBN * CPR; idx += NCT) {
+                    const int r = idx / CPR, c = idx % CPR;
+                    const int32_t slot = sl[r];
+                    const bool inside = base + r < p1;
+                    const bool ok = inside && slot >= 0 && (int64_t)slot < p.num_slots;
+                    if (inside && !ok && c == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
+                    const int64_t off = ok ? (((int64_t)slot * p.hkv + g) * D + c * 8) : 0;
+                    const int dsto = r * L::RS + c * 8;
+                    rx::cp_async_16(rx::smem_u32(kd + dsto), p.k_pool + off, ok ? 16 : 0);
+                    rx::cp_async_16(rx::smem_u32(vd + dsto), p.v_pool + off, ok ? 16 : 0);
+                }
             }
             __syncwarp();
             if (lane == 0) rx::mbar_arrive(bar + 8 * (L::B_SLEMPTY + sb));
-            rx::cp_async_mbar_arrive(bar + 8 * (L::B_FULL + s));
+            if constexpr (F8) {
+                // the previous tile's codes are in once only this tile's group
+                // may still be pending
+                if (pend >= 0) {
+                    rx::cp_async_wait<1>();
+                    if (!widen((uint32_t)pend)) {
+                        ok_all = false;
+                        break;
+                    }
+                }
+                pend = n_tile;
+            } else {
+                rx::cp_async_mbar_arrive(bar + 8 * (L::B_FULL + s));
+            }
+        }
+        // F8: the item's last tile, before anything that waits on the consumers
+        if (F8 && ok_all && pend >= 0) {
+            rx::cp_async_wait<0>();
+            ok_all = widen((uint32_t)pend);
         }
         if (!ok_all) break;
     }
@@ -393,11 +480,11 @@ __device__ void copier(const Params &p, unsigned char *smem)
 // consumer warps
 // ---------------------------------------------------------------------------
 
-template <int D, int WM>
+template <int D, int WM, bool F8>
 __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uint32_t &n_tile,
                         uint32_t &qi, uint32_t &n_red)
 {
-    using L = Layout<D>;
+    using L = Layout<D, F8>;
     constexpr int WK = kConsumers / WM;   // warps along keys
     constexpr int KW = kBN / WK;          // keys per warp per stage
     constexpr int NT = KW / 8;            // S n-tiles per warp
@@ -539,7 +626,7 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
             const int r = wm * 16 + gid + half * 8;
             if (r >= M) continue;
             const int64_t orow = out_row(r);
-            const float inv = 1.f / l_r[half];
+            const float inv = p.v_scale / l_r[half];  // V's scale: 1 for a bf16 pool
             if (fin) {
                 bf16 *dst = p.o + orow * D;
 #pragma unroll
@@ -594,6 +681,7 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
                 ot += red_o[(k * Mpad + r) * D + c] * f;
             }
             const int64_t orow = out_row(r);
+            ot *= p.v_scale;  // V's scale: 1 for a bf16 pool
             if (fin) {
                 p.o[orow * D + c] = __float2bfloat16_rn(ot / lt);
                 if (p.lse && c == 0) p.lse[orow] = (mt + log2f(lt)) * rx::kLn2;
@@ -611,10 +699,10 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
     return true;
 }
 
-template <int D, bool PLAN>
+template <int D, bool PLAN, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p)
 {
-    using L = Layout<D>;
+    using L = Layout<D, F8>;
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t bar = rx::smem_u32(smem + L::OFF_BAR);
     // the kernels after this one in the call do not wait for it to start
@@ -644,11 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p)
     __syncthreads();
     const int warp = threadIdx.x >> 5;
     if (warp == 0) {
-        scheduler<D, PLAN>(p, smem);
+        scheduler<D, PLAN, F8>(p, smem);
         return;
     }
     if (warp <= kCopiers) {
-        copier<D>(p, smem);
+        copier<D, F8>(p, smem);
         return;
     }
     const Desc *descs = reinterpret_cast<const Desc *>(smem + L::OFF_DESC);
@@ -663,11 +751,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p)
         if (M == 0) return;
         bool ok;
         if (M <= 16)
-            ok = consume<D, 1>(p, d, smem, n_tile, qi, n_red);
+            ok = consume<D, 1, F8>(p, d, smem, n_tile, qi, n_red);
         else if (M <= 32)
-            ok = consume<D, 2>(p, d, smem, n_tile, qi, n_red);
+            ok = consume<D, 2, F8>(p, d, smem, n_tile, qi, n_red);
         else
-            ok = consume<D, 4>(p, d, smem, n_tile, qi, n_red);
+            ok = consume<D, 4, F8>(p, d, smem, n_tile, qi, n_red);
         if (!ok) return;
         __syncwarp();
         if (lane == 0) rx::mbar_arrive(bar + 8 * (L::B_ITEMPTY + di));
@@ -880,6 +968,36 @@ __device__ __forceinline__ void load_bf16(const unsigned char *src, float (&out)
     }
 }
 
+// E consecutive E4M3 codes of shared memory as floats (E = 2, 4, 8 or 16:
+// one 2-, 4-, 8- or 16-byte load); exact, through f16.
+template <int E>
+__device__ __forceinline__ void load_e4m3(const unsigned char *src, float (&out)[E])
+{
+    uint32_t w[E >= 4 ? E / 4 : 1];
+    if constexpr (E == 16) {
+        const uint4 r = *reinterpret_cast<const uint4 *>(src);
+        w[0] = r.x;
+        w[1] = r.y;
+        w[2] = r.z;
+        w[3] = r.w;
+    } else if constexpr (E == 8) {
+        const uint2 r = *reinterpret_cast<const uint2 *>(src);
+        w[0] = r.x;
+        w[1] = r.y;
+    } else if constexpr (E == 4) {
+        w[0] = *reinterpret_cast<const uint32_t *>(src);
+    } else {
+        w[0] = *reinterpret_cast<const uint16_t *>(src);
+    }
+#pragma unroll
+    for (int k = 0; k < E / 2; ++k) {
+        const uint32_t h = rx::e4m3x2_to_f16x2((uint16_t)(w[k >> 1] >> (16 * (k & 1))));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+        out[2 * k] = f.x;
+        out[2 * k + 1] = f.y;
+    }
+}
+
 // Producer warp of an all-heads kernel (layout WL, NP positions a stage,
 // one lane per position; GROUPS: items may hold up to 16 / G requests,
 // else one).  Items come from a global counter, first come
@@ -1049,7 +1167,10 @@ __device__ void wide_copier(const Params &p, unsigned char *smem, uint32_t sbase
 
 constexpr int kWideCopyWarps = 2;  // copy warps of the one-q-head-per-kv-head kernel
 
-template <int D, int LOG_NP, int HPW, int CW>
+// F8: the pools hold E4M3 codes (one byte a value, so twice the positions a
+// stage); the consumers widen them to floats exactly as they load them, K's
+// scale is in scale_log2 and V's multiplies the output.
+template <int D, int LOG_NP, int HPW, int CW, bool F8>
 __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide_kernel(const Params p)
 {
     using WL = WideLayout;
@@ -1062,7 +1183,8 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + WL::OFF_ABORT);
     int *okf = reinterpret_cast<int *>(smem + WL::OFF_OK);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int RB = p.hkv * D * 2;          // bytes of one slot row
+    const int RB = (int)p.row_bytes;       // bytes of one slot row (hkv * D values)
+    constexpr int EB = F8 ? 1 : 2;         // bytes a value
     // runs beside the per-head kernel (it reads none of that kernel's
     // results) and ends after it; the merge may be launched at once
     rx::PdlWaitOnExit ends_after_per_head;
@@ -1118,7 +1240,7 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
         // the current item's result for this lane's head
         auto write_out = [&]() {
             const int64_t orow = (int64_t)b * p.hq + head;
-            const float inv = 1.f / l;
+            const float inv = p.v_scale / l;  // V's scale: 1 for a bf16 pool
             if (fin) {
                 bf16 *dst = p.o + orow * D + hl * DO;
 #pragma unroll
@@ -1178,12 +1300,15 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
 #pragma unroll
                 for (int i = 0; i < NPS; ++i) vmask |= (i < ns && okp[sub * NPS + i] != 0) ? (1u << i) : 0u;
                 // this lane's quarter of the dot product of its pair
-                const unsigned char *kr = kst + pi * RB + head * D * 2 + qd * DQ * 2;
+                const unsigned char *kr = kst + pi * RB + head * D * EB + qd * DQ * EB;
                 float sc = 0.f;
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
                     float kf[8];
-                    load_bf16<8>(kr + 16 * chunk_at(c), kf);
+                    if constexpr (F8)
+                        load_e4m3<8>(kr + 8 * chunk_at(c), kf);
+                    else
+                        load_bf16<8>(kr + 16 * chunk_at(c), kf);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) sc = fmaf(q[c][e], kf[e], sc);
                 }
@@ -1206,7 +1331,7 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
 #pragma unroll
                 for (int e = 0; e < DO; ++e) o[e] *= al;
                 const float pv = okx ? pw : 0.f;  // weight of this lane's pair for V
-                const unsigned char *vr = vst + head * D * 2 + hl * DO * 2;
+                const unsigned char *vr = vst + head * D * EB + hl * DO * EB;
 #pragma unroll
                 for (int i = 0; i < NPS; ++i) {
                     const float w = __shfl_sync(0xffffffffu, pv, ((hh << LOG_NPS) + i) << 2);
@@ -1214,7 +1339,10 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
                     // written in this stage: skip them (0 * stale NaN is NaN)
                     if (!((vmask >> i) & 1u)) continue;
                     float vf[DO];
-                    load_bf16<DO>(vr + i * RB, vf);
+                    if constexpr (F8)
+                        load_e4m3<DO>(vr + i * RB, vf);
+                    else
+                        load_bf16<DO>(vr + i * RB, vf);
 #pragma unroll
                     for (int e = 0; e < DO; ++e) o[e] = fmaf(w, vf[e], o[e]);
                 }
@@ -1608,17 +1736,17 @@ int launch_decode_gqa(const Params &p, cudaStream_t st, bool dependent)
     return launch_on(decode_gqa_kernel<D, F8>, grid, 32 * (1 + kGqaCopyWarps + kGqaWarps), bytes, st, dependent, p);
 }
 
-template <int D, int LOG_NP, int HPW, int CW>
+template <int D, int LOG_NP, int HPW, int CW, bool F8>
 int launch_decode_wide_cfg(const Params &p, cudaStream_t st, bool dependent)
 {
     static bool configured = false;
     if (!configured) {
-        RX_CUDA_CHECK(cudaFuncSetAttribute(decode_wide_kernel<D, LOG_NP, HPW, CW>,
+        RX_CUDA_CHECK(cudaFuncSetAttribute(decode_wide_kernel<D, LOG_NP, HPW, CW, F8>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, WideLayout::BYTES));
         configured = true;
     }
     const int grid = p.n_wide < num_sms() ? p.n_wide : num_sms();
-    return launch_on(decode_wide_kernel<D, LOG_NP, HPW, CW>, grid, 32 * (1 + kWideCopyWarps + CW),
+    return launch_on(decode_wide_kernel<D, LOG_NP, HPW, CW, F8>, grid, 32 * (1 + kWideCopyWarps + CW),
                      WideLayout::BYTES, st, dependent, p);
 }
 
@@ -1630,38 +1758,45 @@ bool wide_supported(int hq, int hkv, int D)
     return hq == hkv && (hq == 8 || hq == 16 || hq == 32 || hq == 64) && (D == 64 || D == 128);
 }
 
-template <int D>
+template <int D, bool F8>
 int launch_decode_wide(const Params &p, cudaStream_t st, bool dependent)
 {
-    constexpr int L0 = D == 128 ? 4 : 5;  // log2 positions per stage at 8 heads
+    // log2 positions per stage at 8 heads: a stage holds 32 KB of K rows
+    // (twice the positions for code rows), at most kWideMaxPos positions (one
+    // producer lane each)
+    constexpr int L0r = (D == 128 ? 4 : 5) + (F8 ? 1 : 0);
+    constexpr int L0 = L0r > 5 ? 5 : L0r;
+    static_assert((1 << L0) <= kWideMaxPos, "one producer lane a position");
     switch (p.hq) {
-    case 8: return launch_decode_wide_cfg<D, L0, 1, 8>(p, st, dependent);
-    case 16: return launch_decode_wide_cfg<D, L0 - 1, 1, 16>(p, st, dependent);
-    case 32: return launch_decode_wide_cfg<D, L0 - 2, 2, 16>(p, st, dependent);
-    default: return launch_decode_wide_cfg<D, L0 - 3, 4, 16>(p, st, dependent);
+    case 8: return launch_decode_wide_cfg<D, L0, 1, 8, F8>(p, st, dependent);
+    case 16: return launch_decode_wide_cfg<D, L0 - 1, 1, 16, F8>(p, st, dependent);
+    case 32: return launch_decode_wide_cfg<D, L0 - 2, 2, 16, F8>(p, st, dependent);
+    default: return launch_decode_wide_cfg<D, L0 - 3, 4, 16, F8>(p, st, dependent);
     }
 }
 
 // the all-heads kernel for the plan's single-request items
+template <bool F8>
 int launch_all_heads(const Params &p, int D, cudaStream_t st, bool dependent)
 {
     if (p.G == 1)
-        return D == 128 ? launch_decode_wide<128>(p, st, dependent) : launch_decode_wide<64>(p, st, dependent);
-    return D == 128 ? launch_decode_gqa<128>(p, st, dependent) : launch_decode_gqa<64>(p, st, dependent);
+        return D == 128 ? launch_decode_wide<128, F8>(p, st, dependent)
+                        : launch_decode_wide<64, F8>(p, st, dependent);
+    return D == 128 ? launch_decode_gqa<128, F8>(p, st, dependent) : launch_decode_gqa<64, F8>(p, st, dependent);
 }
 
-template <int D, bool PLAN>
+template <int D, bool PLAN, bool F8>
 int launch_decode(const Params &p, cudaStream_t st)
 {
     static bool configured = false;
     if (!configured) {
-        RX_CUDA_CHECK(cudaFuncSetAttribute(decode_kernel<D, PLAN>,
+        RX_CUDA_CHECK(cudaFuncSetAttribute(decode_kernel<D, PLAN, F8>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           Layout<D>::BYTES));
+                                           Layout<D, F8>::BYTES));
         configured = true;
     }
     const int grid = p.total_work < num_sms() ? p.total_work : num_sms();
-    return launch_on(decode_kernel<D, PLAN>, grid, kThreads, Layout<D>::BYTES, st, false, p);
+    return launch_on(decode_kernel<D, PLAN, F8>, grid, kThreads, Layout<D, F8>::BYTES, st, false, p);
 }
 
 template <int D>
@@ -1714,25 +1849,35 @@ extern "C" int rx_decode_set_wait_limit(int64_t cycles)
     return RX_OK;
 }
 
-// Argument checks shared by rx_attn_decode and rx_attn_decode_static (`who`
-// names the entry point in the message).
-static int check_decode_args(const char *who, const rx_kv_pool *pool, const void *q, const void *o, const float *lse,
+namespace {
+
+// One layer of the pool a decode call reads: bf16 rows, or E4M3 codes with a
+// scale per pool.
+struct DecodePool {
+    const void *k, *v;
+    int64_t num_slots;
+    int hkv, D;
+    bool f8;
+    float k_scale, v_scale;
+};
+
+// Argument checks shared by the decode entry points (`who` names the entry
+// point in the message), after each has checked its pool struct.
+int check_decode_args(const char *who, const DecodePool &pool, const void *q, const void *o, const float *lse,
                       int32_t hq, const int32_t *req_idx, const int32_t *seq_len, const int32_t *rtt,
                       int64_t rtt_stride, int32_t batch, int32_t max_seq_len, const rx_decode_plan *plan,
                       float sm_scale)
 {
-    if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0)
-        return rx_set_error(RX_ERR_INVALID, "%s: invalid pool", who);
-    if (pool->head_dim != 64 && pool->head_dim != 128)
-        return rx_set_error(RX_ERR_UNSUPPORTED, "%s: head_dim %d (supported: 64, 128)", who, pool->head_dim);
+    if (pool.D != 64 && pool.D != 128)
+        return rx_set_error(RX_ERR_UNSUPPORTED, "%s: head_dim %d (supported: 64, 128)", who, pool.D);
     if (!q || !o || !req_idx || !seq_len || !rtt || rtt_stride <= 0 || rtt_stride > INT32_MAX ||
         batch < 0 || hq <= 0 || max_seq_len <= 0 || max_seq_len > rtt_stride || !(sm_scale > 0.f))
         return rx_set_error(RX_ERR_INVALID, "%s: invalid argument", who);
-    if (hq % pool->num_kv_heads != 0 || 64 % (hq / pool->num_kv_heads) != 0)
+    if (hq % pool.hkv != 0 || 64 % (hq / pool.hkv) != 0)
         return rx_set_error(RX_ERR_UNSUPPORTED, "%s: %d q heads over %d kv heads (need G | 64)", who, hq,
-                            pool->num_kv_heads);
-    if (rx_misaligned16(q) || rx_misaligned16(o) || rx_misaligned16(pool->k) ||
-        rx_misaligned16(pool->v) || (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
+                            pool.hkv);
+    if (rx_misaligned16(q) || rx_misaligned16(o) || rx_misaligned16(pool.k) ||
+        rx_misaligned16(pool.v) || (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
         return rx_set_error(RX_ERR_INVALID, "%s: q, o and the pools must be 16-byte aligned", who);
     if (plan && (!plan->order || !plan->nparts || !plan->items || plan->n_items < 0 ||
                  plan->max_parts < 1 || plan->n_wide < 0 || plan->n_wide > plan->n_items))
@@ -1740,41 +1885,47 @@ static int check_decode_args(const char *who, const rx_kv_pool *pool, const void
     return RX_OK;
 }
 
-extern "C" int rx_attn_decode(const rx_kv_pool *pool_in, const void *q, void *o, float *lse,
-                              int32_t hq, const int32_t *req_idx, const int32_t *seq_len,
-                              const int32_t *rtt, int64_t rtt_stride, int32_t batch,
-                              int32_t max_seq_len, const rx_decode_plan *plan, void *workspace,
-                              size_t ws_bytes, float sm_scale, int32_t *dev_status, void *stream)
+int bf16_pool(const char *who, const rx_kv_pool *pool, DecodePool &out)
 {
-    rx_kv_pool layer_view;
-    if (const int rc = rx_pool_layer(pool_in, &layer_view, 0, "rx_attn_decode")) return rc;
-    const rx_kv_pool *pool = pool_in ? &layer_view : nullptr;
-    const int chk = check_decode_args("rx_attn_decode", pool, q, o, lse, hq, req_idx, seq_len, rtt, rtt_stride,
-                                      batch, max_seq_len, plan, sm_scale);
-    if (chk != RX_OK) return chk;
+    if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0)
+        return rx_set_error(RX_ERR_INVALID, "%s: invalid pool", who);
+    out = DecodePool{pool->k, pool->v, pool->num_slots, pool->num_kv_heads, pool->head_dim, false, 1.f, 1.f};
+    return RX_OK;
+}
+
+// The decode call on either pool type, after the checks: the per-head
+// kernel takes the plan's items of several requests (or, without a plan,
+// the fixed split of every request), the all-heads kernel the plan's
+// single-request items where it has a variant for the head counts, and the
+// merge combines split rows.
+int decode_call(const char *who, const DecodePool &pool, const void *q, void *o, float *lse, int32_t hq,
+                const int32_t *req_idx, const int32_t *seq_len, const int32_t *rtt, int64_t rtt_stride,
+                int32_t batch, int32_t max_seq_len, const rx_decode_plan *plan, void *workspace, size_t ws_bytes,
+                float sm_scale, int32_t *dev_status, void *stream)
+{
     if (batch == 0) return RX_OK;
-    const int D = pool->head_dim;
+    const int D = pool.D;
     Params p{};
     p.q = (const bf16 *)q;
     p.o = (bf16 *)o;
     p.lse = lse;
-    p.k_pool = (const bf16 *)pool->k;
-    p.v_pool = (const bf16 *)pool->v;
-    p.kb = (const unsigned char *)pool->k;
-    p.vb = (const unsigned char *)pool->v;
-    p.row_bytes = (int64_t)pool->num_kv_heads * pool->head_dim * 2;
-    p.v_scale = 1.f;
-    p.num_slots = pool->num_slots;
+    p.k_pool = pool.f8 ? nullptr : (const bf16 *)pool.k;
+    p.v_pool = pool.f8 ? nullptr : (const bf16 *)pool.v;
+    p.kb = (const unsigned char *)pool.k;
+    p.vb = (const unsigned char *)pool.v;
+    p.row_bytes = (int64_t)pool.hkv * D * (pool.f8 ? 1 : 2);
+    p.v_scale = pool.v_scale;
+    p.num_slots = pool.num_slots;
     p.hq = hq;
-    p.hkv = pool->num_kv_heads;
-    p.G = hq / pool->num_kv_heads;
+    p.hkv = pool.hkv;
+    p.G = hq / pool.hkv;
     p.head_dim = D;
     p.req_idx = req_idx;
     p.seq_len = seq_len;
     p.rtt = rtt;
     p.rtt_stride = rtt_stride;
     p.batch = batch;
-    p.scale_log2 = sm_scale * rx::kLog2e;
+    p.scale_log2 = sm_scale * pool.k_scale * rx::kLog2e;
     p.status = dev_status;
     const long long limit = g_decode_wait_cycles.load();
     p.wait_cycles = limit > 0 ? limit : rx::kWaitCycles;
@@ -1785,7 +1936,7 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool_in, const void *q, void *o,
         p.items = plan->items;
         p.max_parts = plan->max_parts;
         // the plan's last n_wide items hold one request each; they go to the
-        // wide kernel for the head counts it is built for (else to the
+        // all-heads kernel for the head counts it is built for (else to the
         // per-head kernel with the rest)
         p.n_wide = (wide_supported(hq, p.hkv, D) || gqa_supported(hq, p.hkv, D)) ? plan->n_wide : 0;
         p.wide0 = plan->n_items - p.n_wide;
@@ -1796,18 +1947,16 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool_in, const void *q, void *o,
         p.max_parts = p.n_chunks;
         total = (int64_t)batch * p.n_chunks * p.hkv;
     }
-    if (total > INT32_MAX)
-        return rx_set_error(RX_ERR_UNSUPPORTED, "rx_attn_decode: %lld work items", (long long)total);
+    if (total > INT32_MAX) return rx_set_error(RX_ERR_UNSUPPORTED, "%s: %lld work items", who, (long long)total);
     if (total == 0 && p.n_wide == 0) return RX_OK;
     p.total_work = (int)total;
     const size_t need = rx_attn_decode_workspace(batch, hq, p.hkv, D, max_seq_len, plan);
     const bool merge = p.max_parts > 1;
     if (need > 0) {
         if (!workspace || ws_bytes < need)
-            return rx_set_error(RX_ERR_CAPACITY, "rx_attn_decode: workspace needs %zu bytes, got %zu",
-                                need, ws_bytes);
+            return rx_set_error(RX_ERR_CAPACITY, "%s: workspace needs %zu bytes, got %zu", who, need, ws_bytes);
         if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
-            return rx_set_error(RX_ERR_INVALID, "rx_attn_decode: workspace must be 256-byte aligned");
+            return rx_set_error(RX_ERR_INVALID, "%s: workspace must be 256-byte aligned", who);
         if (merge) {
             p.ws_o = (float *)workspace;
             p.ws_lse = p.ws_o + (int64_t)batch * hq * p.max_parts * D;
@@ -1817,8 +1966,12 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool_in, const void *q, void *o,
     cudaStream_t st = (cudaStream_t)stream;
     int rc = RX_OK;
     auto per_head = [&](cudaStream_t s) {
-        if (D == 128) return plan ? launch_decode<128, true>(p, s) : launch_decode<128, false>(p, s);
-        return plan ? launch_decode<64, true>(p, s) : launch_decode<64, false>(p, s);
+        if (pool.f8) {
+            if (D == 128) return plan ? launch_decode<128, true, true>(p, s) : launch_decode<128, false, true>(p, s);
+            return plan ? launch_decode<64, true, true>(p, s) : launch_decode<64, false, true>(p, s);
+        }
+        if (D == 128) return plan ? launch_decode<128, true, false>(p, s) : launch_decode<128, false, false>(p, s);
+        return plan ? launch_decode<64, true, false>(p, s) : launch_decode<64, false, false>(p, s);
     };
     // One stream, up to three kernels.  The per-head items (shared segments)
     // and the single-request items run side by side: the all-heads kernel is
@@ -1828,20 +1981,42 @@ extern "C" int rx_attn_decode(const rx_kv_pool *pool_in, const void *q, void *o,
     // for both) before it reads their partial results.
     if (p.n_wide > 0) RX_CUDA_CHECK(cudaMemsetAsync(p.wide_counter, 0, sizeof(int), st));
     if (p.total_work > 0) rc = per_head(st);
-    if (rc == RX_OK && p.n_wide > 0) rc = launch_all_heads(p, D, st, p.total_work > 0);
+    if (rc == RX_OK && p.n_wide > 0)
+        rc = pool.f8 ? launch_all_heads<true>(p, D, st, p.total_work > 0)
+                     : launch_all_heads<false>(p, D, st, p.total_work > 0);
     if (rc != RX_OK || !merge) return rc;
     return D == 128 ? launch_merge<128>(p, plan != nullptr, st) : launch_merge<64>(p, plan != nullptr, st);
+}
+
+}  // namespace
+
+extern "C" int rx_attn_decode(const rx_kv_pool *pool_in, const void *q, void *o, float *lse,
+                              int32_t hq, const int32_t *req_idx, const int32_t *seq_len,
+                              const int32_t *rtt, int64_t rtt_stride, int32_t batch,
+                              int32_t max_seq_len, const rx_decode_plan *plan, void *workspace,
+                              size_t ws_bytes, float sm_scale, int32_t *dev_status, void *stream)
+{
+    rx_kv_pool layer_view;
+    if (const int rc = rx_pool_layer(pool_in, &layer_view, 0, "rx_attn_decode")) return rc;
+    DecodePool pool;
+    if (const int rc = bf16_pool("rx_attn_decode", pool_in ? &layer_view : nullptr, pool)) return rc;
+    if (const int rc = check_decode_args("rx_attn_decode", pool, q, o, lse, hq, req_idx, seq_len, rtt, rtt_stride,
+                                         batch, max_seq_len, plan, sm_scale))
+        return rc;
+    return decode_call("rx_attn_decode", pool, q, o, lse, hq, req_idx, seq_len, rtt, rtt_stride, batch,
+                       max_seq_len, plan, workspace, ws_bytes, sm_scale, dev_status, stream);
 }
 
 // ---------------------------------------------------------------------------
 // Decode over FP8 (E4M3) pools
 // ---------------------------------------------------------------------------
 //
-// The all-heads GQA kernel reads whole slot rows of codes (half the bytes of
-// a bf16 pool) and widens them to f16 on the way to the tensor cores; the
-// plan's items are the same as for a bf16 pool of the same head counts, and
-// split rows merge as usual.  K's scale joins the score scale, V's the
-// output.
+// The same items and kernels as over a bf16 pool, each in an FP8 variant:
+// the per-head kernel's copiers widen the code rows into its bf16 tiles, the
+// one-q-head all-heads kernel widens codes to floats as it loads them, and
+// the GQA all-heads kernel reads whole code rows and widens them to f16 on
+// the way to the tensor cores.  K's scale joins the score scale, V's the
+// output; split rows merge as usual.
 
 extern "C" int rx_attn_decode_fp8(const rx_kv_pool_fp8 *pool_in, const void *q, void *o, float *lse,
                                   int32_t hq, const int32_t *req_idx, const int32_t *seq_len,
@@ -1855,72 +2030,13 @@ extern "C" int rx_attn_decode_fp8(const rx_kv_pool_fp8 *pool_in, const void *q, 
     if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0 ||
         !(pool->k_scale > 0.f) || !(pool->v_scale > 0.f))
         return rx_set_error(RX_ERR_INVALID, "rx_attn_decode_fp8: invalid pool");
-    const int D = pool->head_dim;
-    if ((D != 64 && D != 128) || !rx_gqa_heads(hq, pool->num_kv_heads))
-        return rx_set_error(RX_ERR_UNSUPPORTED,
-                            "rx_attn_decode_fp8: %d q heads over %d kv heads, head_dim %d (supported: 8 kv heads "
-                            "with 2, 4, 8 or 16 q heads each, head_dim 64 or 128)",
-                            hq, pool->num_kv_heads, D);
-    if (!q || !o || !req_idx || !seq_len || !rtt || rtt_stride <= 0 || rtt_stride > INT32_MAX || batch < 0 ||
-        max_seq_len <= 0 || max_seq_len > rtt_stride || !(sm_scale > 0.f))
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode_fp8: invalid argument");
-    if (rx_misaligned16(q) || rx_misaligned16(o) || rx_misaligned16(pool->k) || rx_misaligned16(pool->v) ||
-        (reinterpret_cast<uintptr_t>(lse) & 3) != 0)
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode_fp8: q, o and the pools must be 16-byte aligned");
-    if (!plan || !plan->order || !plan->nparts || !plan->items || plan->n_items < 0 || plan->max_parts < 1 ||
-        plan->n_wide < 0 || plan->n_wide > plan->n_items)
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode_fp8: a valid decode plan is required");
-    if (plan->n_wide != plan->n_items)
-        return rx_set_error(RX_ERR_UNSUPPORTED,
-                            "rx_attn_decode_fp8: the plan has %d items for the per-head kernel; over FP8 pools "
-                            "every item must go to the all-heads kernel (shared segments in at most %d groups)",
-                            plan->n_items - plan->n_wide, RX_DECODE_MAX_GROUPS);
-    if (batch == 0 || plan->n_items == 0) return RX_OK;
-    Params p{};
-    p.q = (const bf16 *)q;
-    p.o = (bf16 *)o;
-    p.lse = lse;
-    p.kb = (const unsigned char *)pool->k;
-    p.vb = (const unsigned char *)pool->v;
-    p.row_bytes = (int64_t)pool->num_kv_heads * D;
-    p.v_scale = pool->v_scale;
-    p.num_slots = pool->num_slots;
-    p.hq = hq;
-    p.hkv = pool->num_kv_heads;
-    p.G = hq / pool->num_kv_heads;
-    p.head_dim = D;
-    p.req_idx = req_idx;
-    p.seq_len = seq_len;
-    p.rtt = rtt;
-    p.rtt_stride = rtt_stride;
-    p.batch = batch;
-    p.scale_log2 = sm_scale * pool->k_scale * rx::kLog2e;
-    p.status = dev_status;
-    const long long limit = g_decode_wait_cycles.load();
-    p.wait_cycles = limit > 0 ? limit : rx::kWaitCycles;
-    p.order = plan->order;
-    p.nparts = plan->nparts;
-    p.items = plan->items;
-    p.max_parts = plan->max_parts;
-    p.n_wide = plan->n_wide;
-    p.wide0 = 0;
-    const size_t need = rx_attn_decode_workspace(batch, hq, p.hkv, D, max_seq_len, plan);
-    if (!workspace || ws_bytes < need)
-        return rx_set_error(RX_ERR_CAPACITY, "rx_attn_decode_fp8: workspace needs %zu bytes, got %zu", need,
-                            ws_bytes);
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
-        return rx_set_error(RX_ERR_INVALID, "rx_attn_decode_fp8: workspace must be 256-byte aligned");
-    const bool merge = p.max_parts > 1;
-    if (merge) {
-        p.ws_o = (float *)workspace;
-        p.ws_lse = p.ws_o + (int64_t)batch * hq * p.max_parts * D;
-    }
-    p.wide_counter = reinterpret_cast<int *>(static_cast<char *>(workspace) + need - 256);
-    cudaStream_t st = (cudaStream_t)stream;
-    RX_CUDA_CHECK(cudaMemsetAsync(p.wide_counter, 0, sizeof(int), st));
-    int rc = D == 128 ? launch_decode_gqa<128, true>(p, st, false) : launch_decode_gqa<64, true>(p, st, false);
-    if (rc != RX_OK || !merge) return rc;
-    return D == 128 ? launch_merge<128>(p, 1, st) : launch_merge<64>(p, 1, st);
+    const DecodePool dp{pool->k, pool->v, pool->num_slots, pool->num_kv_heads, pool->head_dim, true,
+                        pool->k_scale, pool->v_scale};
+    if (const int rc = check_decode_args("rx_attn_decode_fp8", dp, q, o, lse, hq, req_idx, seq_len, rtt,
+                                         rtt_stride, batch, max_seq_len, plan, sm_scale))
+        return rc;
+    return decode_call("rx_attn_decode_fp8", dp, q, o, lse, hq, req_idx, seq_len, rtt, rtt_stride, batch,
+                       max_seq_len, plan, workspace, ws_bytes, sm_scale, dev_status, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -1961,7 +2077,9 @@ extern "C" int rx_attn_decode_static(const rx_kv_pool *pool_in, const void *q, v
     const rx_kv_pool *pool = pool_in ? &layer_view : nullptr;
     // the same checks as rx_attn_decode first, so that a malformed call is
     // reported as such rather than as a batch too big for the array
-    const int chk = check_decode_args("rx_attn_decode_static", pool, q, o, lse, num_q_heads, req_idx, seq_len,
+    DecodePool dp;
+    if (const int rc = bf16_pool("rx_attn_decode_static", pool, dp)) return rc;
+    const int chk = check_decode_args("rx_attn_decode_static", dp, q, o, lse, num_q_heads, req_idx, seq_len,
                                       req_to_token, rtt_stride, batch, max_seq_len, plan_or_null, sm_scale);
     if (chk != RX_OK) return chk;
     if (batch == 0) return RX_OK;

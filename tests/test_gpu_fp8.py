@@ -91,21 +91,29 @@ def _fp8_problem(prob, k_scale, v_scale, seed):
     return kd, vd, kc, vc, status
 
 
-def _decode_fp8(prob, kd, vd, ks, vs, status, kv_chunk=0, plan_len=None):
+def _decode_fp8(prob, kd, vd, ks, vs, status, kv_chunk=0, plan_len=None, use_plan=True, bf16_pools=None):
+    """Decode over the code pools (or, with bf16_pools = (k, v), the bf16
+    path over those pools with the same plan) -> (o, lse, plan info)."""
     from tests import _gpu as g
     from prefix_shared_kv_radixattention_gb300 import binding as rx
     B = len(prob.dec_req_idx)
     lens = prob.dec_seq_len if plan_len is None else plan_len
-    buf, info = rx.rx_decode_plan_build(prob.req_to_token, prob.dec_req_idx, lens, prob.hq, prob.hkv, kv_chunk, 16)
-    assert info.n_wide == info.n_items
-    plan = rx.plan_to_device(buf, info, B)
+    plan, info = None, None
+    if use_plan:
+        buf, info = rx.rx_decode_plan_build(prob.req_to_token, prob.dec_req_idx, lens, prob.hq, prob.hkv,
+                                            kv_chunk, 16)
+        plan = rx.plan_to_device(buf, info, B)
     max_len = int(prob.dec_seq_len.max())
     ws = torch.empty(max(rx.rx_attn_decode_workspace(B, prob.hq, prob.hkv, prob.d, max_len, plan), 256),
                      dtype=torch.uint8, device="cuda")
     q = g.to_dev(prob.q_dec)
     og, lg = g.Guarded(q.shape, torch.bfloat16), g.Guarded((B, prob.hq), torch.float32)
     o, lse = og.t, lg.t
-    rx.rx_attn_decode_fp8(kd, vd, ks, vs, q, o, lse, g.i32(prob.dec_req_idx), g.i32(prob.dec_seq_len),
+    if bf16_pools is None:
+        rx.rx_attn_decode_fp8(kd, vd, ks, vs, q, o, lse, g.i32(prob.dec_req_idx), g.i32(prob.dec_seq_len),
+                              g.i32(prob.req_to_token), max_len, prob.sm_scale, plan, ws, status)
+    else:
+        rx.rx_attn_decode(bf16_pools[0], bf16_pools[1], q, o, lse, g.i32(prob.dec_req_idx), g.i32(prob.dec_seq_len),
                           g.i32(prob.req_to_token), max_len, prob.sm_scale, plan, ws, status)
     torch.cuda.synchronize()
     og.check("fp8 decode o")
@@ -144,11 +152,65 @@ def test_decode_fp8_workload_shapes(shape):
     kd, vd, kc, vc, status = _fp8_problem(prob, 0.8, 1.25, 17)
     for plan_len in (None, prob.dec_seq_len - 1):
         o, lse, info = _decode_fp8(prob, kd, vd, 0.8, 1.25, status, plan_len=plan_len)
-        assert info.n_segments > 0
+        assert info.n_segments > 0 and info.n_wide == info.n_items
         ro, rl = fp8.decode_rows(prob.q_dec, kc, vc, 0.8, 1.25, prob.req_to_token, prob.dec_req_idx,
                                  prob.dec_seq_len, prob.sm_scale)
         g.compare(o, ro, f"fp8 decode {shape}")
         g.compare_lse(lse, rl, f"fp8 decode {shape}")
+    assert int(status.item()) == 0
+
+
+def _mha_shapes():
+    return {
+        # one prefix shared by every request (per-head kernel, FP8 copiers),
+        # private pieces on the one-q-head all-heads kernel
+        "few-shot MHA 32x128": lambda: inputs.few_shot_decode(hq=32, hkv=32, d=128, batch=12, shared=300,
+                                                              private=150, num_slots=8000),
+        "few-shot MHA 8x64": lambda: inputs.few_shot_decode(hq=8, hkv=8, d=64, batch=9, shared=200,
+                                                            private=90, num_slots=4000),
+        # G = 2 over 4 kv heads: the per-head kernel takes every item
+        "ragged G=2": lambda: inputs.ragged(733, hq=8, hkv=4, d=128, n_groups=3, per_group=4, shared_max=300,
+                                            private_max=200, extend_max=1, decode=True, num_slots=6000),
+        # a prefix shared by 20 groups of 4: per-head FP8 items beside GQA FP8 ones
+        "wide-shared GQA": lambda: inputs.few_shot_decode(hq=32, hkv=8, d=128, batch=80, shared=256,
+                                                          private=70, num_slots=20000),
+    }
+
+
+@pytest.mark.parametrize("name", list(_mha_shapes()))
+def test_decode_fp8_all_layouts_match_oracle(name):
+    """FP8 decode on the layouts beyond 8 kv heads' all-heads kernel: one q
+    head per kv head, G = 2 over 4 kv heads, a segment too widely shared for
+    request groups; with and without a plan, against the oracle."""
+    from tests import _gpu as g
+    prob = _mha_shapes()[name]()
+    kd, vd, kc, vc, status = _fp8_problem(prob, 0.6, 1.7, 29)
+    ro, rl = fp8.decode_rows(prob.q_dec, kc, vc, 0.6, 1.7, prob.req_to_token, prob.dec_req_idx, prob.dec_seq_len,
+                             prob.sm_scale)
+    for use_plan in (True, False):
+        o, lse, info = _decode_fp8(prob, kd, vd, 0.6, 1.7, status, use_plan=use_plan)
+        g.compare(o, ro, f"fp8 decode {name} plan={use_plan}")
+        g.compare_lse(lse, rl, f"fp8 decode {name} plan={use_plan}")
+        if use_plan and name != "ragged G=2":
+            assert info.n_items > info.n_wide > 0   # both kernels ran
+    assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("name", ["few-shot MHA 32x128", "few-shot MHA 8x64", "ragged G=2"])
+def test_decode_fp8_unit_scales_equal_bf16_pool_bitwise(name):
+    """Where the FP8 kernels widen codes exactly into the bf16 kernels'
+    arithmetic (the per-head kernel's tiles, the one-q-head all-heads
+    kernel's floats), unit scales give rx_attn_decode's result on a pool of
+    the decoded values, bit for bit."""
+    from tests import _gpu as g
+    prob = _mha_shapes()[name]()
+    kd, vd, kc, vc, status = _fp8_problem(prob, 1.0, 1.0, 31)
+    pools = (g.to_dev(fp8.bf16_bits(kc)), g.to_dev(fp8.bf16_bits(vc)))
+    for use_plan in (True, False):
+        o8, l8, _ = _decode_fp8(prob, kd, vd, 1.0, 1.0, status, use_plan=use_plan)
+        ob, lb, _ = _decode_fp8(prob, kd, vd, 1.0, 1.0, status, use_plan=use_plan, bf16_pools=pools)
+        assert np.array_equal(o8.view(np.uint32), ob.view(np.uint32)), (name, use_plan)
+        assert np.array_equal(l8.view(np.uint32), lb.view(np.uint32)), (name, use_plan)
     assert int(status.item()) == 0
 
 

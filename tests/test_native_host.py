@@ -71,24 +71,31 @@ def test_layer_outside_the_pool_is_rejected_before_any_launch():
             assert "layer" in rx.last_error()
 
 
-def test_fp8_decode_rejects_unsupported_heads_and_missing_plan():
-    """rx_attn_decode_fp8 checks its shapes and plan before any device work."""
+def test_fp8_decode_rejects_bad_shapes_and_scales():
+    """rx_attn_decode_fp8 takes the head counts and plans rx_attn_decode
+    takes (no plan included) and checks its shapes, scales and plan before
+    any device work (the pointers here are never dereferenced)."""
     import ctypes
     lib = rx.library()
     fake = 0x100000
     P = ctypes.c_void_p(fake)
     plan = rx.DecodePlan(fake, fake, fake, 4, 1, 4)
-    for hq, hkv, d, pl, code in ((32, 32, 128, plan, rx.RX_ERR_UNSUPPORTED), (32, 8, 96, plan, rx.RX_ERR_UNSUPPORTED),
-                                 (24, 8, 128, plan, rx.RX_ERR_UNSUPPORTED), (32, 8, 128, None, rx.RX_ERR_INVALID)):
-        pool = rx.KVPoolFp8(fake, fake, 64, hkv, d, 1.0, 1.0, 0, 0)
-        rc = lib.rx_attn_decode_fp8(ctypes.byref(pool), P, P, None, hq, P, P, P, 64, 2, 8,
-                                    ctypes.byref(pl) if pl is not None else None, P, 1 << 20, ctypes.c_float(0.1),
-                                    None, None)
-        assert rc == code, (hq, hkv, d, rx.last_error())
-    per_head = rx.DecodePlan(fake, fake, fake, 4, 1, 3)       # one item for the per-head kernel
-    pool = rx.KVPoolFp8(fake, fake, 64, 8, 128, 1.0, 1.0, 0, 0)
-    assert lib.rx_attn_decode_fp8(ctypes.byref(pool), P, P, None, 32, P, P, P, 64, 2, 8, ctypes.byref(per_head), P,
-                                  1 << 20, ctypes.c_float(0.1), None, None) == rx.RX_ERR_UNSUPPORTED
+
+    def call(hq, hkv, d, ks=1.0, vs=1.0, pl=plan, batch=2):
+        pool = rx.KVPoolFp8(fake, fake, 64, hkv, d, ks, vs, 0, 0)
+        return lib.rx_attn_decode_fp8(ctypes.byref(pool), P, P, None, hq, P, P, P, 64, batch, 8,
+                                      ctypes.byref(pl) if pl is not None else None, P, 1 << 20,
+                                      ctypes.c_float(0.1), None, None)
+
+    assert call(32, 8, 96) == rx.RX_ERR_UNSUPPORTED             # head_dim
+    assert call(24, 8, 128) == rx.RX_ERR_UNSUPPORTED            # G = 3 does not divide 64
+    assert call(32, 8, 128, ks=0.0) == rx.RX_ERR_INVALID
+    assert call(32, 8, 128, vs=-1.0) == rx.RX_ERR_INVALID
+    bad_plan = rx.DecodePlan(fake, fake, fake, 4, 0, 4)         # max_parts 0
+    assert call(32, 8, 128, pl=bad_plan) == rx.RX_ERR_INVALID
+    # valid shapes, with or without a plan, MHA included: an empty batch is a no-op
+    for hq, hkv, pl in ((32, 32, plan), (32, 32, None), (8, 4, None), (32, 8, plan)):
+        assert call(hq, hkv, 128, pl=pl, batch=0) == rx.RX_OK, (hq, hkv, rx.last_error())
 
 
 def test_fp8_extend_checks_before_any_launch():
