@@ -510,10 +510,13 @@ class E2EPipeline:
     brings in, in this order: the decode requests' new K/V rows, slots and
     queries; then, per chunk of extend requests, the chunk's new K/V rows,
     slots and queries.  The compute stream stores the decode rows and runs
-    decode as soon as they are in, and for each chunk stores its rows and
-    runs its extend (rx_kv_store and rx_attn_extend over the chunk) as soon
-    as the chunk is in; an output stream copies each result back as soon as
-    it is written.  The host link (about 200 GB/s each way on this machine)
+    decode as soon as they are in; each chunk's rows are stored and its
+    extend run (rx_kv_store and rx_attn_extend over the chunk) as soon as the
+    chunk is in, the chunks alternating between two compute streams with a
+    staging workspace each (different chunks touch disjoint rows and slots,
+    so one chunk's staging and last wave overlap the next one's attention);
+    an output stream copies each result back as soon as it is written.  The
+    host link (about 200 GB/s each way on this machine)
     is slower than the kernels, so decode goes first (its inputs are small,
     and it runs while the first chunk arrives) and the chunks grow, then
     shrink (little to wait for at the start, little to copy back after the
@@ -521,7 +524,7 @@ class E2EPipeline:
     the step's rows, every new row goes in before the first store instead.
     The same calls, on the same data, as the step."""
 
-    FRACTIONS = (0.14, 0.24, 0.28, 0.22, 0.12)   # extend requests per chunk, in order
+    FRACTIONS = (0.12, 0.2, 0.24, 0.2, 0.14, 0.1)   # extend requests per chunk, in order
 
     def __init__(self, st, torch, rx, fractions=FRACTIONS):
         self.st, self.torch, self.rx = st, torch, rx
@@ -573,11 +576,13 @@ class E2EPipeline:
                     rows=(r0, r1), kv=kv, qo=i32(p.qo_indptr[b0:b1 + 1] - r0), req=i32(p.ext_req_idx[b0:b1]),
                     P=i32(p.ext_prefix_len[b0:b1]), E=i32(p.ext_extend_len[b0:b1]),
                     max_E=int(p.ext_extend_len[b0:b1].max()), n=b1 - b0))
-            self.ws = torch.empty(rx.rx_attn_extend_workspace(max_ctx, max_n, p.hkv, p.d),
-                                  dtype=torch.uint8, device="cuda")
+            # one staging workspace per compute stream (the chunks alternate)
+            nb = rx.rx_attn_extend_workspace(max_ctx, max_n, p.hkv, p.d)
+            self.ws = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(2)]
         # per-part stores need every new row in exactly one part
         self.split_store = covered == n_new
         self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        self.s_comp2 = torch.cuda.Stream()
 
     def bytes_in(self):
         return sum(h.numel() * h.element_size() for h in self.h_in)
@@ -606,6 +611,7 @@ class E2EPipeline:
         # the side streams fork from the compute stream (required when captured)
         self.s_in.wait_stream(comp)
         self.s_out.wait_stream(comp)
+        self.s_comp2.wait_stream(comp)
         with torch.cuda.stream(self.s_in):
             if split:
                 self._copy_rows(*self.dec_rows)
@@ -633,19 +639,27 @@ class E2EPipeline:
             self.s_out.wait_event(ev_d)
             with torch.cuda.stream(self.s_out):
                 self.h_od.copy_(st.o_dec, non_blocking=True)
-        for c, ev in zip(self.chunks, ev_c):
+        # the chunks alternate between two compute streams: the requests of
+        # different chunks read and write disjoint rows and slots, so one
+        # chunk's staging and last wave overlap the next chunk's attention
+        streams = (comp, self.s_comp2)
+        for i, (c, ev) in enumerate(zip(self.chunks, ev_c)):
             r0, r1 = c["rows"]
-            comp.wait_event(ev)
-            if split:
-                self._store_rows(*c["kv"])
-            rx.rx_attn_extend(st.k_pool, st.v_pool, st.q_ext[r0:r1], st.o_ext[r0:r1], None, c["qo"], c["req"],
-                              c["P"], c["E"], st.rtt, c["max_E"], p.sm_scale, st.status, workspace=self.ws)
+            cs = streams[i % 2]
+            cs.wait_event(ev)
+            with torch.cuda.stream(cs):
+                if split:
+                    self._store_rows(*c["kv"])
+                rx.rx_attn_extend(st.k_pool, st.v_pool, st.q_ext[r0:r1], st.o_ext[r0:r1], None, c["qo"],
+                                  c["req"], c["P"], c["E"], st.rtt, c["max_E"], p.sm_scale, st.status,
+                                  workspace=self.ws[i % 2], stream=cs)
             ev_o = E()
-            ev_o.record(comp)
+            ev_o.record(cs)
             self.s_out.wait_event(ev_o)
             with torch.cuda.stream(self.s_out):
                 self.h_oe[r0:r1].copy_(st.o_ext[r0:r1], non_blocking=True)
         # the side streams join the compute stream (required when captured)
+        comp.wait_stream(self.s_comp2)
         comp.wait_stream(self.s_in)
         comp.wait_stream(self.s_out)
 
@@ -741,7 +755,8 @@ def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
            "schedule": ("; ".join(["copies on their own streams, overlapping the kernels"] +
                                   (["decode's rows and queries first"] if st.has_dec and pipe.chunks else []) +
                                   ([f"extend in {len(pipe.chunks)} request chunks (" +
-                                    ", ".join(str(c["n"]) for c in pipe.chunks) + " requests)"]
+                                    ", ".join(str(c["n"]) for c in pipe.chunks) +
+                                    " requests) alternating over two compute streams"]
                                    if pipe.chunks else []) +
                                   (["each part stores its own new rows"] if pipe.split_store and pipe.chunks else
                                    [] if pipe.split_store else ["every new row stored first"]))
