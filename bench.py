@@ -390,7 +390,7 @@ def run_gpu(args, rank, world, local_rank):
         dec_ms = ms_of["decode"]
         uniq_bytes = st.plan_info.tokens_read * (kv_row // 2 if st.kv_fp8 else kv_row)
         achieved = uniq_bytes / (dec_ms / 1e3) / 1e9
-        traffic, tsrc = profiled_traffic(args.workload, "decode")
+        traffic, tsrc = profiled_traffic(args.workload, "decode_fp8" if st.kv_fp8 else "decode")
         roofs["decode"] = {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "traffic": traffic, "traffic_source": tsrc,
@@ -408,7 +408,7 @@ def run_gpu(args, rank, world, local_rank):
     if st.has_ext:
         ext_ms = ms_of["extend"]
         tf = flops_ext / (ext_ms / 1e3) / 1e12
-        traffic, tsrc = profiled_traffic(args.workload, args.extend_path)
+        traffic, tsrc = profiled_traffic(args.workload, args.extend_path + ("_fp8" if st.kv_fp8 else ""))
         roofs["extend"] = {
             "bound": "tensor", "achieved": round(tf, 2), "peak": tflops, "unit": "TFLOP/s",
             "frac": round(tf / tflops, 4), "traffic": traffic, "traffic_source": tsrc,
@@ -797,6 +797,22 @@ PROFILED_TRAFFIC = {
                      "staging copy"),
     ("constrained_decode", "fsm"): (
         135_800_000, "ncu --set full -k fsm_scan_kernel -c 1 on constrained_decode: the scan alone"),
+    # FP8 (E4M3) pools (--kv-fp8)
+    ("few_shot_decode", "decode_fp8"): (
+        147_600_000, "ncu --set full -k decode_kernel -c 1 and -k decode_wide_kernel -c 1 on few_shot_decode "
+                     "--kv-fp8 (262,144-slot pool; same rows): the two FP8 decode kernels, without the merge"),
+    ("tree_of_thought_decode", "decode_fp8"): (
+        196_600_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode --kv-fp8 (131,072-slot "
+                     "pool; same rows): decode_gqa_kernel<F8> alone, without the merge"),
+    ("mixed_chat", "decode_fp8"): (
+        843_200_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat --kv-fp8 (600,000-slot pool; same "
+                     "rows): decode_gqa_kernel<F8> alone, without the merge"),
+    ("cached_prefix_extend", "staged_fp8"): (
+        375_000_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend --kv-fp8 (36,000-slot pool; "
+                     "same staged rows): extend_kernel alone, without the staging copy"),
+    ("mixed_chat", "staged_fp8"): (
+        846_300_000, "ncu --set full -k extend_kernel -c 1 on mixed_chat --kv-fp8 (600,000-slot pool; same "
+                     "staged rows): extend_kernel alone, without the staging copy"),
 }
 
 
