@@ -214,8 +214,6 @@ class GpuStep:
         # FP8 pools (optional): the whole step on E4M3 pools
         self.kv_fp8 = kv_fp8
         if kv_fp8:
-            if rope_base:
-                raise SystemExit("--kv-fp8 and --rope do not combine (no fused rotary FP8 store)")
             if self.has_ext and extend_path != "staged":
                 raise SystemExit("--kv-fp8 extends on the staged path only")
             # E4M3 pools (scale 1): the cached rows quantized at set-up, the
@@ -282,7 +280,11 @@ class GpuStep:
                                self.status, workspace=self.ext_ws)
 
     def store_fp8(self):
-        self.rx.rx_kv_store_fp8(self.k8, self.v8, 1.0, 1.0, self.k_new, self.v_new, self.slots, self.status)
+        if self.rope_base:
+            self.rx.rx_kv_store_rope_fp8(self.k8, self.v8, 1.0, 1.0, self.k_new, self.v_new, self.slots,
+                                         self.pos_new, self.rope_base, self.status)
+        else:
+            self.rx.rx_kv_store_fp8(self.k8, self.v8, 1.0, 1.0, self.k_new, self.v_new, self.slots, self.status)
 
     def parts(self):
         return ([("store_fp8", self.store_fp8)] if self.kv_fp8 else [("store", self.kv_store)]) + \
@@ -437,7 +439,7 @@ def run_gpu(args, rank, world, local_rank):
         # write of every q row
         q_bytes = 2 * (prob.q_ext.size + prob.q_dec.size) * 2
         rq = ms_of["rope_q"]
-        out["kv_store"]["rope_base"] = st.rope_base
+        out["kv_store_fp8" if st.kv_fp8 else "kv_store"]["rope_base"] = st.rope_base
         out["rope_q"] = {"ms": rq, "gbs": q_bytes / (rq / 1e3) / 1e9}
     line = {
         "metric": f"prefix-shared attn: {metric}", "value": round(value, 3), "unit": unit,

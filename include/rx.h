@@ -319,6 +319,14 @@ int rx_rope(void *x, const int32_t *pos, int64_t n, int32_t heads, int32_t head_
 int rx_kv_store_rope(const rx_kv_pool *pool, const void *k_new, const void *v_new, const int32_t *slots,
                      const int32_t *pos, int64_t n, double base, int32_t *dev_status, void *stream);
 
+/* rx_kv_store_rope into FP8 pools: K[slots[i]] = the codes rx_kv_store_fp8
+ * stores for rope(k_new[i], pos[i]) as rx_rope computes it (rotated, rounded
+ * to bf16), V[slots[i]] = the codes of v_new[i].  Same buffers and errors as
+ * rx_kv_store_fp8, plus pos and base as in rx_kv_store_rope. */
+int rx_kv_store_rope_fp8(const rx_kv_pool_fp8 *pool, const void *k_new, const void *v_new,
+                         const int32_t *slots, const int32_t *pos, int64_t n, double base, int32_t *dev_status,
+                         void *stream);
+
 /* Extend attention.  Request b (b < batch) has prefix_len[b] cached tokens and
  * extend_len[b] new ones whose K/V are already in the pool; the slot list is
  * req_to_token row req_idx[b], positions 0 .. prefix_len[b]+extend_len[b]-1.

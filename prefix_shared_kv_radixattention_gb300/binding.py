@@ -112,6 +112,7 @@ _sig("rx_attn_decode_fp8", ctypes.c_int, ctypes.POINTER(KVPoolFp8), _P, _P, _P, 
      _I32, _P, _P, ctypes.c_size_t, ctypes.c_float, _P, _P)
 _sig("rx_attn_extend_fp8", ctypes.c_int, ctypes.POINTER(KVPoolFp8), _P, _P, _P, _I32, _P, _P, _P, _P, _P,
      _I64, _I32, _I32, _P, ctypes.c_size_t, ctypes.c_float, _P, _P)
+_sig("rx_kv_store_rope_fp8", ctypes.c_int, ctypes.POINTER(KVPoolFp8), _P, _P, _P, _P, _I64, ctypes.c_double, _P, _P)
 
 
 class FsmInfo(ctypes.Structure):
@@ -436,6 +437,27 @@ def rx_kv_store_rope(k_pool, v_pool, k_new, v_new, slots, pos, base: float, dev_
         raise ValueError("k_new/v_new must be [n, num_kv_heads, head_dim] and pos [n]")
     _check(_lib.rx_kv_store_rope(ctypes.byref(pool), _ptr(k_new), _ptr(v_new), _ptr(slots), _ptr(pos), n,
                                  float(base), _ptr(dev_status), _stream(stream)))
+
+
+def rx_kv_store_rope_fp8(k_pool, v_pool, k_scale: float, v_scale: float, k_new, v_new, slots, pos, base: float,
+                         dev_status=None, stream=None, layer: int = 0) -> None:
+    """rx_kv_store_rope into uint8 E4M3 pools ([L,] S, Hkv, d) with per-pool scales."""
+    torch = _torch()
+    _dev(k_pool, torch.uint8, "k_pool")
+    _dev(v_pool, torch.uint8, "v_pool")
+    _dev(k_new, torch.bfloat16, "k_new")
+    _dev(v_new, torch.bfloat16, "v_new")
+    _dev(slots, torch.int32, "slots")
+    _dev(pos, torch.int32, "pos")
+    _dev(dev_status, torch.int32, "dev_status")
+    S, hkv, d, L = _pool_dims(k_pool, v_pool, layer)
+    n = slots.numel()
+    if k_new.shape != (n, hkv, d) or v_new.shape != k_new.shape or pos.numel() != n:
+        raise ValueError("k_new/v_new must be [n, num_kv_heads, head_dim] and pos [n]")
+    pool = KVPoolFp8(k_pool.data_ptr(), v_pool.data_ptr(), S, hkv, d, float(k_scale), float(v_scale), L,
+                     int(layer))
+    _check(_lib.rx_kv_store_rope_fp8(ctypes.byref(pool), _ptr(k_new), _ptr(v_new), _ptr(slots), _ptr(pos), n,
+                                     float(base), _ptr(dev_status), _stream(stream)))
 
 
 def rx_attn_extend_workspace(total_ctx_tokens: int, batch: int, num_kv_heads: int, head_dim: int) -> int:

@@ -94,6 +94,28 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes)
     return r;
 }
 
+// Eight bf16 values (16 bytes, element 0 in the low half of x) stored as
+// E4M3 codes of value / scale (8 bytes, element 0 in the low byte): a
+// correctly rounded fp32 division, then round to nearest even with
+// magnitudes past 448 saturated to 448.
+__device__ __forceinline__ uint2 e4m3x8_from_bf16x8(uint4 v, float scale)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t codes[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint16_t pair[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[2 * h + q]));
+            const float lo = __fdiv_rn(f.x, scale), hi = __fdiv_rn(f.y, scale);
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(pair[q]) : "f"(hi), "f"(lo));
+        }
+        codes[h] = (uint32_t)pair[0] | ((uint32_t)pair[1] << 16);
+    }
+    return make_uint2(codes[0], codes[1]);
+}
+
 // Two floats -> packed f16x2 (round to nearest even), low half = lo.
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi)
 {

@@ -62,21 +62,8 @@ __global__ void __launch_bounds__(256) kv_store_fp8_kernel(const uint4 *__restri
             continue;
         }
         const uint4 val = is_v ? __ldg(v_new + j) : __ldg(k_new + j);
-        const float scale = is_v ? v_scale : k_scale;
-        const uint32_t w[4] = {val.x, val.y, val.z, val.w};
-        uint32_t codes[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint16_t pair[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[2 * h + q]));
-                const float lo = __fdiv_rn(f.x, scale), hi = __fdiv_rn(f.y, scale);
-                asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(pair[q]) : "f"(hi), "f"(lo));
-            }
-            codes[h] = (uint32_t)pair[0] | ((uint32_t)pair[1] << 16);
-        }
-        (is_v ? v_pool : k_pool)[(int64_t)s * chunks_per_row + c] = make_uint2(codes[0], codes[1]);
+        (is_v ? v_pool : k_pool)[(int64_t)s * chunks_per_row + c] =
+            rx::e4m3x8_from_bf16x8(val, is_v ? v_scale : k_scale);
     }
 }
 

@@ -26,6 +26,8 @@
 // precision at a small fraction of its fp32 and integer rates.
 #include <math.h>
 
+#include <type_traits>
+
 #include "rx_common.cuh"
 
 namespace {
@@ -118,14 +120,22 @@ __global__ void __launch_bounds__(256) rope_kernel(uint4 *__restrict__ x, const 
     }
 }
 
+// F8: the pools hold E4M3 codes; the rotated K row (rounded to bf16 as
+// above) and the V row are stored as rx_kv_store_fp8 stores rows: value /
+// scale, correctly rounded, to the nearest code (8 codes per 8 values).
+template <bool F8>
 __global__ void __launch_bounds__(256) kv_store_rope_kernel(const uint4 *__restrict__ k_new,
                                                             const uint4 *__restrict__ v_new,
                                                             const int32_t *__restrict__ slots,
                                                             const int32_t *__restrict__ pos, int64_t n,
-                                                            int hkv, int D, uint4 *__restrict__ k_pool,
-                                                            uint4 *__restrict__ v_pool, int64_t num_slots,
-                                                            int32_t *status, int cpt, const RopeTab tab)
+                                                            int hkv, int D, void *__restrict__ k_pool_,
+                                                            void *__restrict__ v_pool_, int64_t num_slots,
+                                                            int32_t *status, int cpt, const RopeTab tab,
+                                                            float k_scale, float v_scale)
 {
+    using Chunk = std::conditional_t<F8, uint2, uint4>;  // 8 values of the pool
+    Chunk *k_pool = static_cast<Chunk *>(k_pool_);
+    Chunk *v_pool = static_cast<Chunk *>(v_pool_);
     const int groups = D / 16;
     const int64_t cpr = (int64_t)D / 8;
     const int64_t row_chunks = hkv * cpr;  // one slot row: every kv head
@@ -145,8 +155,8 @@ __global__ void __launch_bounds__(256) kv_store_rope_kernel(const uint4 *__restr
         const Rot8 r = angles(tab, __ldg(pos + i), gi * 8);
         const uint4 *ks = k_new + i * row_chunks;
         const uint4 *vs = v_new + i * row_chunks;
-        uint4 *kd = k_pool + (int64_t)s * row_chunks;
-        uint4 *vd = v_pool + (int64_t)s * row_chunks;
+        Chunk *kd = k_pool + (int64_t)s * row_chunks;
+        Chunk *vd = v_pool + (int64_t)s * row_chunks;
         for (int hc = run * cpt; hc < min(hchunks, (run + 1) * cpt); ++hc) {
         uint4 klo[kHeadsPerThread], khi[kHeadsPerThread], vlo[kHeadsPerThread], vhi[kHeadsPerThread];
 #pragma unroll
@@ -164,10 +174,17 @@ __global__ void __launch_bounds__(256) kv_store_rope_kernel(const uint4 *__restr
             const int h = hc * kHeadsPerThread + k;
             if (h < hkv) {
                 rotate(r, klo[k], khi[k]);
-                kd[h * cpr + gi] = klo[k];
-                kd[h * cpr + groups + gi] = khi[k];
-                vd[h * cpr + gi] = vlo[k];
-                vd[h * cpr + groups + gi] = vhi[k];
+                if constexpr (F8) {
+                    kd[h * cpr + gi] = rx::e4m3x8_from_bf16x8(klo[k], k_scale);
+                    kd[h * cpr + groups + gi] = rx::e4m3x8_from_bf16x8(khi[k], k_scale);
+                    vd[h * cpr + gi] = rx::e4m3x8_from_bf16x8(vlo[k], v_scale);
+                    vd[h * cpr + groups + gi] = rx::e4m3x8_from_bf16x8(vhi[k], v_scale);
+                } else {
+                    kd[h * cpr + gi] = klo[k];
+                    kd[h * cpr + groups + gi] = khi[k];
+                    vd[h * cpr + gi] = vlo[k];
+                    vd[h * cpr + groups + gi] = vhi[k];
+                }
             }
         }
         }
@@ -263,9 +280,38 @@ extern "C" int rx_kv_store_rope(const rx_kv_pool *pool_in, const void *k_new, co
     const int cpt = chunks_per_thread(n, pool->num_kv_heads, pool->head_dim);
     const int hchunks = (pool->num_kv_heads + kHeadsPerThread - 1) / kHeadsPerThread;
     const int64_t work = n * ((hchunks + cpt - 1) / cpt) * (pool->head_dim / 16);
-    kv_store_rope_kernel<<<grid_for(work), 256, 0, (cudaStream_t)stream>>>(
+    kv_store_rope_kernel<false><<<grid_for(work), 256, 0, (cudaStream_t)stream>>>(
         (const uint4 *)k_new, (const uint4 *)v_new, slots, pos, n, pool->num_kv_heads, pool->head_dim,
-        (uint4 *)pool->k, (uint4 *)pool->v, pool->num_slots, dev_status, cpt, tab);
+        pool->k, pool->v, pool->num_slots, dev_status, cpt, tab, 1.f, 1.f);
+    RX_CUDA_CHECK(cudaGetLastError());
+    return RX_OK;
+}
+
+extern "C" int rx_kv_store_rope_fp8(const rx_kv_pool_fp8 *pool_in, const void *k_new, const void *v_new,
+                                    const int32_t *slots, const int32_t *pos, int64_t n, double base,
+                                    int32_t *dev_status, void *stream)
+{
+    rx_kv_pool_fp8 layer_view;
+    if (const int rc = rx_pool_layer(pool_in, &layer_view, 1, "rx_kv_store_rope_fp8")) return rc;
+    const rx_kv_pool_fp8 *pool = pool_in ? &layer_view : nullptr;
+    RopeTab tab;
+    if (!pool || !pool->k || !pool->v || pool->num_slots <= 0 || pool->num_kv_heads <= 0 || n < 0 ||
+        !(pool->k_scale > 0.f) || !(pool->v_scale > 0.f) || (n > 0 && (!k_new || !v_new || !slots || !pos)))
+        return rx_set_error(RX_ERR_INVALID, "rx_kv_store_rope_fp8: invalid argument");
+    if (!make_tab(pool->head_dim, base, tab))
+        return rx_set_error(RX_ERR_UNSUPPORTED,
+                            "rx_kv_store_rope_fp8: head_dim %d, base %g (need 64 or 128, base > 1)",
+                            pool->head_dim, base);
+    if ((reinterpret_cast<uintptr_t>(pool->k) & 7) != 0 || (reinterpret_cast<uintptr_t>(pool->v) & 7) != 0 ||
+        misaligned(k_new) || misaligned(v_new))
+        return rx_set_error(RX_ERR_INVALID, "rx_kv_store_rope_fp8: pools must be 8-byte and new rows 16-byte aligned");
+    if (n == 0) return RX_OK;
+    const int cpt = chunks_per_thread(n, pool->num_kv_heads, pool->head_dim);
+    const int hchunks = (pool->num_kv_heads + kHeadsPerThread - 1) / kHeadsPerThread;
+    const int64_t work = n * ((hchunks + cpt - 1) / cpt) * (pool->head_dim / 16);
+    kv_store_rope_kernel<true><<<grid_for(work), 256, 0, (cudaStream_t)stream>>>(
+        (const uint4 *)k_new, (const uint4 *)v_new, slots, pos, n, pool->num_kv_heads, pool->head_dim,
+        pool->k, pool->v, pool->num_slots, dev_status, cpt, tab, pool->k_scale, pool->v_scale);
     RX_CUDA_CHECK(cudaGetLastError());
     return RX_OK;
 }

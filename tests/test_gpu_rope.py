@@ -75,6 +75,38 @@ def test_kv_store_rope(hkv, d):
     assert np.array_equal(k_got[rest], kp[rest]) and np.array_equal(v_got[rest], vp[rest])
 
 
+@pytest.mark.parametrize("hkv,d,ks,vs", [(8, 128, 0.5, 2.0), (4, 64, 1.0, 1.0)])
+def test_kv_store_rope_fp8_is_the_rope_store_then_the_fp8_store(hkv, d, ks, vs):
+    """The rotary FP8 scatter stores, bit for bit, the codes rx_kv_store_fp8
+    makes of the rows rx_kv_store_rope writes to a bf16 pool; other rows and
+    bad slots are left alone."""
+    g = _g()
+    from oracle import fp8
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    rng = np.random.default_rng(19 + hkv)
+    S, n, base = 3000, 211, 500000.0
+    k_new = inputs.randn_bf16(rng, (n, hkv, d))
+    v_new = inputs.randn_bf16(rng, (n, hkv, d))
+    slots = rng.permutation(S)[:n].astype(np.int32)
+    pos = _positions(rng, n)
+    kb = g.to_dev(np.zeros((S, hkv, d), np.uint16))
+    vb = g.to_dev(np.zeros((S, hkv, d), np.uint16))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rx.rx_kv_store_rope(kb, vb, g.to_dev(k_new), g.to_dev(v_new), g.i32(slots), g.i32(pos), base, status)
+    init = rng.integers(0, 256, size=(S, hkv, d), dtype=np.uint8)
+    k8, v8 = torch.from_numpy(init.copy()).cuda(), torch.from_numpy(init.copy()).cuda()
+    rx.rx_kv_store_rope_fp8(k8, v8, ks, vs, g.to_dev(k_new), g.to_dev(v_new), g.i32(slots), g.i32(pos), base,
+                            status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rotated = g.to_host_u16(kb)[slots]
+    got_k, got_v = k8.cpu().numpy(), v8.cpu().numpy()
+    assert np.array_equal(got_k[slots], fp8.quantize_rows(inputs.bf16_to_f32(rotated), ks))
+    assert np.array_equal(got_v[slots], fp8.quantize_rows(inputs.bf16_to_f32(v_new), vs))
+    rest = np.setdiff1d(np.arange(S), slots)
+    assert np.array_equal(got_k[rest], init[rest]) and np.array_equal(got_v[rest], init[rest])
+
+
 def test_kv_store_rope_bad_slot_is_flagged():
     g = _g()
     from prefix_shared_kv_radixattention_gb300 import binding as rx

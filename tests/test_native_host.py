@@ -57,6 +57,7 @@ def test_layer_outside_the_pool_is_rejected_before_any_launch():
             lambda: lib.rx_kv_store(ctypes.byref(pool), P, P, P, 4, None, None),
             lambda: lib.rx_kv_store_fp8(ctypes.byref(p8), P, P, P, 4, None, None),
             lambda: lib.rx_kv_store_rope(ctypes.byref(pool), P, P, P, P, 4, 10000.0, None, None),
+            lambda: lib.rx_kv_store_rope_fp8(ctypes.byref(p8), P, P, P, P, 4, 10000.0, None, None),
             lambda: lib.rx_attn_extend(ctypes.byref(pool), P, P, None, 2, P, P, P, P, P, 64, 1, 8, None, 0,
                                        ctypes.c_float(0.125), None, None),
             lambda: lib.rx_attn_decode(ctypes.byref(pool), P, P, None, 2, P, P, P, 64, 1, 8, None, None, 0,
