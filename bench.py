@@ -214,8 +214,6 @@ class GpuStep:
         # FP8 pools (optional): the whole step on E4M3 pools
         self.kv_fp8 = kv_fp8
         if kv_fp8:
-            if self.has_ext and extend_path != "staged":
-                raise SystemExit("--kv-fp8 extends on the staged path only")
             # E4M3 pools (scale 1): the cached rows quantized at set-up, the
             # step's rows stored by rx_kv_store_fp8 in the timed step (in place
             # of the bf16 store); extend and decode read them

@@ -530,13 +530,13 @@ int rx_attn_decode_fp8(const rx_kv_pool_fp8 *pool, const void *q, void *o, float
 /* Extend attention over FP8 pools: rx_attn_extend's definition applied to
  * the values E4M3(code) * scale of each pool, with the same arguments (q, o,
  * lse, qo_indptr, req_idx, prefix_len, extend_len, req_to_token and
- * max_extend_len as there).  The staged path only: a workspace of
- * rx_attn_extend_workspace(...) bytes is required (RX_ERR_UNSUPPORTED
- * without one).  The staging copy reads the code rows (num_kv_heads *
- * head_dim bytes each, half a bf16 pool's) and widens them to bf16 -- exactly,
- * since every E4M3 value is a bf16 value -- so the attention kernel runs as
- * on a bf16 pool holding E4M3(code), with K's scale folded into the score
- * scale and V's into the output.  With both scales 1 the result is bit for
+ * max_extend_len, and the workspace or NULL, as there).  Both paths read
+ * the code rows (num_kv_heads * head_dim bytes each, half a bf16 pool's) and
+ * widen them to bf16 -- exactly, since every E4M3 value is a bf16 value --
+ * the staged path in its staging copy, the gather path in the attention
+ * kernel's producer warps; the attention then runs as on a bf16 pool holding
+ * E4M3(code), with K's scale folded into the score scale and V's into the
+ * output, and both paths give the same result.  With both scales 1 the result is bit for
  * bit rx_attn_extend's on such a pool.  Pools 8-byte aligned; head_dim 64 or
  * 128 and the head counts rx_attn_extend takes. */
 int rx_attn_extend_fp8(const rx_kv_pool_fp8 *pool, const void *q, void *o, float *lse_or_null,

@@ -698,8 +698,8 @@ def rx_attn_extend_fp8(k_pool, v_pool, k_scale: float, v_scale: float, q, o, lse
                        prefix_len, extend_len, req_to_token, max_extend_len: int, sm_scale: float, workspace,
                        dev_status=None, stream=None, layer: int = 0) -> None:
     """Extend attention over uint8 E4M3 pools ([L,] S, Hkv, d) with per-pool
-    scales; the staged path only (a workspace of rx_attn_extend_workspace(...)
-    bytes is required)."""
+    scales; `workspace` (at least rx_attn_extend_workspace(...) bytes, or
+    None for the gather path) as in rx_attn_extend."""
     torch = _torch()
     _dev(k_pool, torch.uint8, "k_pool")
     _dev(v_pool, torch.uint8, "v_pool")

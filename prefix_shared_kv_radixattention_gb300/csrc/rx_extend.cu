@@ -111,6 +111,8 @@ struct XParams {  // 64-byte aligned through its tensor maps
     float *lse;
     const bf16 *k_pool;
     const bf16 *v_pool;
+    const unsigned char *k8;   // FP8 pools (gather path): E4M3 codes, else null
+    const unsigned char *v8;
     int64_t num_slots;
     int hq, hkv, G;
     const int32_t *qo_indptr;
@@ -180,11 +182,28 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int32_
     if (status) atomicOr(status, RX_DEV_TIMEOUT);
 }
 
+// Eight E4M3 codes (element 0 in the low byte) as eight bf16: every E4M3
+// value, subnormals included, is exact in f16 and in bf16, so the widening
+// through f16 is exact.
+__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 c)
+{
+    const uint32_t w[2] = {c.x, c.y};
+    uint32_t r[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t h = rx::e4m3x2_to_f16x2((uint16_t)(w[k >> 1] >> (16 * (k & 1))));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+        r[k] = rx::pack_bf16(f.x, f.y);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 // ---------------------------------------------------------------------------
 // producer warps: K and V tiles through the slot list
 // ---------------------------------------------------------------------------
 
-template <int D>
+// F8: the pools hold E4M3 codes (p.k8, p.v8), widened here to the bf16 tiles.
+template <int D, bool F8>
 __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, uint32_t sbase)
 {
     using L = XL<D>;
@@ -234,18 +253,61 @@ __device__ void producer(const XParams &p, const Tile &T, unsigned char *smem, u
                 }
             }
             const uint32_t dst = sbase + (w ? L::OFF_V : L::OFF_K) + st * L::NB * L::KBLK;
-            const bf16 *pool = w ? p.v_pool : p.k_pool;
-            for (int idx = pt; idx < kBN * CPR; idx += kProducers) {
-                const int r = idx / CPR, c = idx % CPR;
-                const int pos = j * kBN + r;
-                const int32_t s = sl[r];
-                const bool inside = pos < T.kv_end;
-                const bool ok = inside && s >= 0 && (int64_t)s < p.num_slots;
-                if (w == 0 && inside && !ok && c == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
-                const int64_t off = ok ? (((int64_t)s * p.hkv + T.g) * D + c * 8) : 0;
-                rx::cp_async_16(dst + sw128(r, c, L::KBLK), pool + off, ok ? 16 : 0);
+            if constexpr (F8) {
+                // FP8 pools: 16 codes a chunk, loaded (two 8-byte loads,
+                // four chunks in flight), widened exactly to bf16 and stored
+                // as the tile's two 16-byte chunks; then this thread's arrival
+                constexpr int CPR8 = D / 16;
+                const unsigned char *pool8 = w ? p.v8 : p.k8;
+                unsigned char *tile = smem + (dst - sbase);
+                for (int i0 = pt; i0 < kBN * CPR8; i0 += 4 * kProducers) {
+                    uint2 lo[4], hi[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int idx = i0 + u * kProducers;
+                        lo[u] = hi[u] = make_uint2(0u, 0u);
+                        if (idx < kBN * CPR8) {
+                            const int r = idx / CPR8, c = idx % CPR8;
+                            const int pos = j * kBN + r;
+                            const int32_t s = sl[r];
+                            const bool inside = pos < T.kv_end;
+                            const bool ok = inside && s >= 0 && (int64_t)s < p.num_slots;
+                            if (w == 0 && inside && !ok && c == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
+                            if (ok) {
+                                const uint2 *src = reinterpret_cast<const uint2 *>(
+                                    pool8 + ((int64_t)s * p.hkv + T.g) * D + c * 16);
+                                lo[u] = __ldg(src);
+                                hi[u] = __ldg(src + 1);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int idx = i0 + u * kProducers;
+                        if (idx < kBN * CPR8) {
+                            const int r = idx / CPR8, c = idx % CPR8;
+                            *reinterpret_cast<uint4 *>(tile + sw128(r, 2 * c, L::KBLK)) =
+                                e4m3x8_to_bf16x8(lo[u]);
+                            *reinterpret_cast<uint4 *>(tile + sw128(r, 2 * c + 1, L::KBLK)) =
+                                e4m3x8_to_bf16x8(hi[u]);
+                        }
+                    }
+                }
+                rx::mbar_arrive(bar + 8 * ((w ? L::B_VFULL : L::B_KFULL) + st));
+            } else {
+                const bf16 *pool = w ? p.v_pool : p.k_pool;
+                for (int idx = pt; idx < kBN * CPR; idx += kProducers) {
+                    const int r = idx / CPR, c = idx % CPR;
+                    const int pos = j * kBN + r;
+                    const int32_t s = sl[r];
+                    const bool inside = pos < T.kv_end;
+                    const bool ok = inside && s >= 0 && (int64_t)s < p.num_slots;
+                    if (w == 0 && inside && !ok && c == 0 && p.status) atomicOr(p.status, RX_DEV_BAD_SLOT);
+                    const int64_t off = ok ? (((int64_t)s * p.hkv + T.g) * D + c * 8) : 0;
+                    rx::cp_async_16(dst + sw128(r, c, L::KBLK), pool + off, ok ? 16 : 0);
+                }
+                rx::cp_async_mbar_arrive(bar + 8 * ((w ? L::B_VFULL : L::B_KFULL) + st));
             }
-            rx::cp_async_mbar_arrive(bar + 8 * ((w ? L::B_VFULL : L::B_KFULL) + st));
         }
         if (stop) break;
         rx::named_bar_sync(1, kProducers);          // slot entry j % kNSL is read: refill allowed
@@ -532,7 +594,7 @@ __device__ void softmax_rows(const XParams &p, const Tile &T, unsigned char *sme
     if (valid && p.lse) p.lse[orow] = (m_used + log2f(l)) * rx::kLn2;
 }
 
-template <int D, bool kStaged>
+template <int D, bool kStaged, bool F8 = false>
 __global__ void __launch_bounds__(kStaged ? kStagedThreads : kThreads, 1)
     extend_kernel(const __grid_constant__ XParams p)
 {
@@ -609,7 +671,7 @@ __global__ void __launch_bounds__(kStaged ? kStagedThreads : kThreads, 1)
     } else {
         if (warp < mma_warp) {
             if (!kStaged) {
-                producer<D>(p, T, smem, sbase);
+                producer<D, F8>(p, T, smem, sbase);
             } else if (warp == kStagedProducerWarp) {
                 if ((threadIdx.x & 31) == 0) tma_producer<D>(p, T, smem, sbase);
                 __syncwarp();
@@ -745,22 +807,6 @@ __global__ void __launch_bounds__(1024) ctx_offsets_kernel(const int32_t *prefix
         offs[batch] = total;
         if (total > cap && status) atomicOr(status, RX_DEV_BAD_LEN);
     }
-}
-
-// Eight E4M3 codes (element 0 in the low byte) as eight bf16: every E4M3
-// value, subnormals included, is exact in f16 and in bf16, so the widening
-// through f16 is exact.
-__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 c)
-{
-    const uint32_t w[2] = {c.x, c.y};
-    uint32_t r[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t h = rx::e4m3x2_to_f16x2((uint16_t)(w[k >> 1] >> (16 * (k & 1))));
-        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
-        r[k] = rx::pack_bf16(f.x, f.y);
-    }
-    return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
 // Packed row offs[b] + i = pool row req_to_token[req_idx[b]][share[b] kBN + i]
@@ -910,16 +956,16 @@ int encode_stage_map(CUtensorMap *m, void *base, int64_t cap, int hkv, int D)
     return RX_OK;
 }
 
-template <int D, bool kStaged>
+template <int D, bool kStaged, bool F8 = false>
 int launch_extend(const XParams &p, dim3 grid, cudaStream_t st)
 {
     static bool configured = false;
     if (!configured) {
-        RX_CUDA_CHECK(cudaFuncSetAttribute(extend_kernel<D, kStaged>,
+        RX_CUDA_CHECK(cudaFuncSetAttribute(extend_kernel<D, kStaged, F8>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, XL<D>::BYTES));
         configured = true;
     }
-    extend_kernel<D, kStaged><<<grid, kStaged ? kStagedThreads : kThreads, XL<D>::BYTES, st>>>(p);
+    extend_kernel<D, kStaged, F8><<<grid, kStaged ? kStagedThreads : kThreads, XL<D>::BYTES, st>>>(p);
     RX_CUDA_CHECK(cudaGetLastError());
     return RX_OK;
 }
@@ -961,8 +1007,6 @@ int extend_call(const char *who, const ExtendPool &pool, const void *q, void *o,
                             (int)pool_align + 1);
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
         return rx_set_error(RX_ERR_INVALID, "%s: workspace must be 256-byte aligned", who);
-    if (pool.f8 && !workspace)
-        return rx_set_error(RX_ERR_UNSUPPORTED, "%s: FP8 pools need a workspace (the staged path)", who);
     if (batch == 0 || max_extend_len == 0) return RX_OK;
     if (batch > 65535 || pool.hkv > 65535)
         return rx_set_error(RX_ERR_UNSUPPORTED, "%s: batch or kv heads above 65535", who);
@@ -972,6 +1016,8 @@ int extend_call(const char *who, const ExtendPool &pool, const void *q, void *o,
     p.lse = lse;
     p.k_pool = pool.f8 ? nullptr : (const bf16 *)pool.k;
     p.v_pool = pool.f8 ? nullptr : (const bf16 *)pool.v;
+    p.k8 = pool.f8 ? (const unsigned char *)pool.k : nullptr;
+    p.v8 = pool.f8 ? (const unsigned char *)pool.v : nullptr;
     p.num_slots = pool.num_slots;
     p.hq = hq;
     p.hkv = pool.hkv;
@@ -990,8 +1036,11 @@ int extend_call(const char *who, const ExtendPool &pool, const void *q, void *o,
     cudaStream_t st = (cudaStream_t)stream;
     const int D = pool.D;
     int rc = RX_OK;
-    if (!workspace)
+    if (!workspace) {
+        if (pool.f8)
+            return D == 128 ? launch_extend<128, false, true>(p, grid, st) : launch_extend<64, false, true>(p, grid, st);
         return D == 128 ? launch_extend<128, false>(p, grid, st) : launch_extend<64, false>(p, grid, st);
+    }
 
     // staged path: offsets, packed copy of every context, then attention
     const int64_t row_bytes = (int64_t)p.hkv * D * (int64_t)sizeof(bf16);

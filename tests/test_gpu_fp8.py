@@ -231,12 +231,13 @@ def test_decode_fp8_bad_slot_is_flagged():
 # ---------------------------------------------------------------------------
 
 
-def _extend_fp8(prob, kd, vd, ks, vs, status):
+def _extend_fp8(prob, kd, vd, ks, vs, status, staged=True):
     from tests import _gpu as g
     from prefix_shared_kv_radixattention_gb300 import binding as rx
     B = len(prob.ext_req_idx)
     ctx = int((prob.ext_prefix_len + prob.ext_extend_len).sum())
-    ws = torch.empty(rx.rx_attn_extend_workspace(ctx, B, prob.hkv, prob.d), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(rx.rx_attn_extend_workspace(ctx, B, prob.hkv, prob.d), dtype=torch.uint8,
+                     device="cuda") if staged else None
     q = g.to_dev(prob.q_ext)
     og, lg = g.Guarded(q.shape, torch.bfloat16), g.Guarded(tuple(q.shape[:2]), torch.float32)
     o, lse = og.t, lg.t
@@ -286,6 +287,26 @@ def test_extend_fp8_matches_oracle(name, ks, vs):
     ro, rl = fp8.attention(prob.q_ext, kc, vc, ks, vs, prob.req_to_token, q_row, kbeg, kend, prob.sm_scale)
     g.compare(o.float().cpu().numpy(), ro, f"fp8 extend {name}")
     g.compare_lse(lse.cpu().numpy(), rl, f"fp8 extend {name}")
+
+
+@pytest.mark.parametrize("name,ks,vs", [("tiny", 0.8, 1.3), ("ragged GQA", 0.37, 2.5),
+                                        ("shared prefixes", 1.5, 0.25)])
+def test_extend_fp8_gather_path_equals_staged_bitwise(name, ks, vs):
+    """Without a workspace the attention kernel's producer warps widen the
+    code rows themselves: the same tiles, so the same result as the staged
+    path bit for bit, and the oracle's."""
+    from tests import _gpu as g
+    prob = _extend_problems()[name]()
+    kd, vd, kc, vc, status = _fp8_problem(prob, ks, vs, 47)
+    o_s, l_s = _extend_fp8(prob, kd, vd, ks, vs, status, staged=True)
+    o_g, l_g = _extend_fp8(prob, kd, vd, ks, vs, status, staged=False)
+    assert int(status.item()) == 0
+    assert np.array_equal(g.to_host_u16(o_g), g.to_host_u16(o_s))
+    assert np.array_equal(l_g.cpu().numpy().view(np.uint32), l_s.cpu().numpy().view(np.uint32))
+    q_row, kbeg, kend = _extend_rows(prob)
+    ro, rl = fp8.attention(prob.q_ext, kc, vc, ks, vs, prob.req_to_token, q_row, kbeg, kend, prob.sm_scale)
+    g.compare(o_g.float().cpu().numpy(), ro, f"fp8 extend gather {name}")
+    g.compare_lse(l_g.cpu().numpy(), rl, f"fp8 extend gather {name}")
 
 
 @pytest.mark.parametrize("name", ["ragged GQA", "shared prefixes"])
