@@ -796,7 +796,8 @@ PROFILED_TRAFFIC = {
                      "staged rows, shared prefix tiles staged once): extend_kernel alone, without the "
                      "staging copy"),
     ("constrained_decode", "fsm"): (
-        135_800_000, "ncu --set full -k fsm_scan_kernel -c 1 on constrained_decode: the scan alone"),
+        135_200_000, "ncu --set full -k fsm_scan_kernel -c 1 on constrained_decode: the scan with the finish "
+                     "in its last CTA (the whole step)"),
     # FP8 (E4M3) pools (--kv-fp8)
     ("few_shot_decode", "decode_fp8"): (
         147_600_000, "ncu --set full -k decode_kernel -c 1 and -k decode_wide_kernel -c 1 on few_shot_decode "
@@ -1154,14 +1155,15 @@ def run_gpu_fsm(args, rank, world, local_rank):
         "config": fsm_config(a, world),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": traffic, "traffic_source": tsrc,
-                     "kernel": "rx_fsm_step (fsm_scan_kernel + fsm_finish_kernel)",
+                     "kernel": ("rx_fsm_step (fsm_scan_kernel; its last CTA finishes every request)" if B <= 512
+                                else "rx_fsm_step (fsm_scan_kernel + fsm_finish_kernel)"),
                      "algorithmic_bytes_per_launch": int(algo),
                      "launch_ms": round(k_ms, 5), "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"},
         "e2e": {"value": round(job_throughput(B, world, n, e2e_ms), 3), "unit": "req/s",
                 "h2d_bytes_per_step": int(logits.nbytes + state0.nbytes),
                 "d2h_bytes_per_step": int(out.numel() * 4 + cnt.numel() * 4), "ms_per_step": round(e2e_ms / n, 5),
                 "steps": n},
-        "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
+        "gpu_launches": (1 if B <= 512 else 2) * args.steps, "clocks": clk.summary(),
         "parts": {"fsm_step": {"ms": k_ms, "tokens_per_step": float(emitted.mean()),
                                "jump_tokens_per_step": float(emitted.mean() - 1.0)}},
         "wall_s_timed_loop": round(t_wall, 3),

@@ -90,7 +90,8 @@ extern "C" {
 /* Message for the last failed call on this thread ("" if none). */
 const char *rx_last_error(void);
 
-/* ABI version (bumped on any signature change). */
+/* ABI version (bumped on any change of a signature or of a buffer
+ * contract, such as a workspace size). */
 int rx_version(void);
 
 /* ---- radix tree (host) --------------------------------------------------
@@ -617,11 +618,13 @@ typedef struct {
  *   logits: device fp32 rows of logits_stride floats (>= vocab, a multiple
  *   of 4, rows 16-byte aligned); state: device int32 [batch], updated in
  *   place; out_tokens: device int32 [batch][1 + max_jump]; out_count: device
- *   int32 [batch]; workspace: device uint64 [batch], 8-byte aligned, all
- *   zero before the first call -- every call leaves it zero (the per-request
- *   best candidate while the call runs).  Rows are read once, as 16-byte
- *   vectors.  Two kernels on `stream`: the scan, then the finish as its
- *   programmatic dependent. */
+ *   int32 [batch]; workspace: device uint64 [batch + 1], 8-byte aligned,
+ *   all zero before the first call -- every call leaves it zero (the
+ *   per-request best candidate, and a count of the scan's finished CTAs,
+ *   while the call runs).  Rows are read once, as 16-byte vectors.  Up to
+ *   512 requests, one kernel on `stream`: the scan, whose last CTA to finish
+ *   follows every request's chosen edge; larger batches, the scan and then a
+ *   finish kernel as its programmatic dependent. */
 int rx_fsm_step(const rx_fsm *fsm, const float *logits, int64_t logits_stride, int32_t batch,
                 int32_t *state, int32_t *out_tokens, int32_t *out_count, uint64_t *workspace,
                 int32_t *dev_status, void *stream);

@@ -640,10 +640,11 @@ class Fsm:
 
 
 def fsm_workspace(batch: int):
-    """The zeroed device workspace rx_fsm_step needs for `batch` requests
-    (every call leaves it zero, so it can be kept and reused)."""
+    """The zeroed device workspace rx_fsm_step needs for `batch` requests:
+    batch + 1 words (every call leaves it zero, so it can be kept and
+    reused)."""
     torch = _torch()
-    return torch.zeros(max(1, int(batch)), dtype=torch.int64, device="cuda")
+    return torch.zeros(max(1, int(batch)) + 1, dtype=torch.int64, device="cuda")
 
 
 def rx_fsm_step(fsm: Fsm, logits, state, out_tokens, out_count, workspace, dev_status=None,

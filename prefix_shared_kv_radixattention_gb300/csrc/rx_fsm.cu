@@ -18,15 +18,19 @@
 //     follows that edge, and emits the jump of the state it reaches in the
 //     same step (rx_fsm_step, on the device).
 //
-// The step is a streaming pass over each request's logits row (HBM-bound),
-// in two kernels on one stream.  The scan kernel's CTAs (one resident wave)
-// walk (request, 16384-id tile) pairs with 16-byte loads of logits and of
-// the 32-bit allowed-token mask words of the request's state, and fold each
-// tile's allowed candidates into the request's best (value, id) key with a
-// 64-bit atomicMax.  The finish kernel, a programmatic dependent of the scan,
-// gives each request a warp that follows the chosen edge without a search
-// (a per-word prefix count of the state's edges), writes the jump, and sets
-// the request's key back to zero for the next call.
+// The step is a streaming pass over each request's logits row (HBM-bound).
+// The scan kernel's CTAs (one resident wave) walk (request, 16384-id tile)
+// pairs with 16-byte loads of logits and of the 32-bit allowed-token mask
+// words of the request's state, and fold each tile's allowed candidates into
+// the request's best (value, id) key with a 64-bit atomicMax.  Then each
+// request follows the chosen edge without a search (a per-word prefix count
+// of the state's edges), writes the jump, and sets its key back to zero for
+// the next call.  For up to kScanThreads requests that finish runs in the
+// scan kernel itself: every CTA counts itself done on a counter once its
+// warps' key updates are fenced, and the CTA that completes the count -- the
+// last one, which then sees every key -- finishes all requests, one a
+// thread, and re-arms the counter.  Larger batches use a second kernel, a
+// programmatic dependent of the scan, with a warp per request.
 #include <algorithm>
 #include <climits>
 #include <cmath>
@@ -59,8 +63,10 @@ struct FsmParams {
     int32_t *out_tokens;
     int32_t *out_count;
     unsigned long long *best;
+    unsigned long long *done;   // CTAs of the scan done (the finish in the scan)
     int32_t *status;
     int32_t n_states, vocab, max_jump, words, batch, tiles_per_row;
+    int32_t fused;              // the last scan CTA finishes every request
 };
 
 // Order-preserving key of a candidate (value v, id i): a larger value, then
@@ -73,6 +79,54 @@ __device__ __forceinline__ unsigned long long key_of(float v, int i)
     uint32_t u = __float_as_uint(v);
     u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i);
+}
+
+// The edge of state s for token bi, and the jump of the state it leads to:
+// s1 = -1 when the mask and the edge list disagree or the jump is malformed.
+__device__ __forceinline__ void follow_edge(const FsmParams &p, int s, int bi, int &s1, int &jl, int64_t &off)
+{
+    s1 = -1;
+    jl = 0;
+    off = 0;
+    if (bi < 0 || bi >= p.vocab) return;
+    // the state's edges below bi's mask word, plus the allowed ids below it
+    // within the word (no search)
+    const int64_t wrd = (int64_t)s * p.words + (bi >> 5);
+    const int64_t e = __ldg(p.row_ptr + s) + __ldg(p.rank + wrd) + __popc(__ldg(p.mask + wrd) & ((1u << (bi & 31)) - 1u));
+    if (e < __ldg(p.row_ptr + s + 1) && __ldg(p.tok + e) == bi) s1 = __ldg(p.nxt + e);
+    if (s1 >= 0 && s1 < p.n_states) {
+        jl = __ldg(p.jump_len + s1);
+        off = __ldg(p.jump_off + s1);
+        if (jl < 0 || jl > p.max_jump) s1 = -1;
+    } else {
+        s1 = -1;
+    }
+}
+
+// Finish of request b by one thread, given its best key (0: no token allowed).
+__device__ void finish_request(const FsmParams &p, int b, unsigned long long key)
+{
+    const int s = p.state[b];
+    const bool good = s >= 0 && s < p.n_states;
+    if (!good || key == 0ull) {  // a bad state, or no token allowed (the text is complete)
+        p.out_count[b] = 0;
+        if (p.status) atomicOr(p.status, good ? RX_DEV_FSM_DONE : RX_DEV_BAD_STATE);
+        return;
+    }
+    const int bi = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+    int s1, jl;
+    int64_t off;
+    follow_edge(p, s, bi, s1, jl, off);
+    if (s1 < 0) {  // mask and edge list disagree, or a malformed jump
+        p.out_count[b] = 0;
+        if (p.status) atomicOr(p.status, RX_DEV_BAD_STATE);
+        return;
+    }
+    int32_t *out = p.out_tokens + (int64_t)b * (1 + p.max_jump);
+    out[0] = bi;
+    for (int k = 0; k < jl; ++k) out[1 + k] = __ldg(p.jump_tok + off + k);
+    p.out_count[b] = 1 + jl;
+    p.state[b] = __ldg(p.jump_end + s1);
 }
 
 // Scan: CTAs walk (request, tile) pairs and fold each tile's allowed
@@ -122,6 +176,23 @@ __global__ void __launch_bounds__(kScanThreads, kScanCtasPerSm) fsm_scan_kernel(
         for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
         if (lane == 0 && best) atomicMax(p.best + b, best);
     }
+    if (!p.fused) return;
+    // this CTA's key updates (made by each warp's lane 0) are visible device
+    // wide before it counts itself done
+    __shared__ int is_last;
+    if (lane == 0) __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(p.done, 1ull) == (unsigned long long)gridDim.x - 1;
+    __syncthreads();
+    if (!is_last) return;
+    // the last CTA: every other CTA's keys are in; read them past L1
+    __threadfence();
+    for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
+        const unsigned long long key = __ldcg(p.best + b);
+        p.best[b] = 0ull;
+        finish_request(p, b, key);
+    }
+    if (threadIdx.x == 0) *p.done = 0ull;  // re-armed for the next call
 }
 
 // Finish: one warp per request follows the chosen edge and writes the jump,
@@ -151,21 +222,7 @@ __global__ void __launch_bounds__(kFinishThreads) fsm_finish_kernel(const FsmPar
     const int bi = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
     int s1 = -1, jl = 0;
     int64_t off = 0;
-    if (lane == 0 && bi >= 0 && bi < p.vocab) {
-        // the chosen token's edge: the state's edges below its mask word,
-        // plus the allowed ids below it within the word (no search)
-        const int64_t wrd = (int64_t)s * p.words + (bi >> 5);
-        const int64_t e = __ldg(p.row_ptr + s) + __ldg(p.rank + wrd) +
-                          __popc(__ldg(p.mask + wrd) & ((1u << (bi & 31)) - 1u));
-        if (e < __ldg(p.row_ptr + s + 1) && __ldg(p.tok + e) == bi) s1 = __ldg(p.nxt + e);
-        if (s1 >= 0 && s1 < p.n_states) {
-            jl = __ldg(p.jump_len + s1);
-            off = __ldg(p.jump_off + s1);
-            if (jl < 0 || jl > p.max_jump) s1 = -1;
-        } else {
-            s1 = -1;
-        }
-    }
+    if (lane == 0) follow_edge(p, s, bi, s1, jl, off);
     s1 = __shfl_sync(0xffffffffu, s1, 0);
     jl = __shfl_sync(0xffffffffu, jl, 0);
     off = __shfl_sync(0xffffffffu, off, 0);
@@ -319,6 +376,7 @@ extern "C" int rx_fsm_step(const rx_fsm *fsm, const float *logits, int64_t logit
     p.out_tokens = out_tokens;
     p.out_count = out_count;
     p.best = reinterpret_cast<unsigned long long *>(workspace);
+    p.done = p.best + batch;
     p.status = dev_status;
     p.n_states = fsm->n_states;
     p.vocab = fsm->vocab;
@@ -328,6 +386,7 @@ extern "C" int rx_fsm_step(const rx_fsm *fsm, const float *logits, int64_t logit
     p.tiles_per_row = (fsm->vocab + kTileIds - 1) / kTileIds;
     const int64_t tiles = (int64_t)batch * p.tiles_per_row;
     if (tiles > INT32_MAX) return rx_set_error(RX_ERR_UNSUPPORTED, "rx_fsm_step: batch too large");
+    p.fused = batch <= kScanThreads;
     cudaStream_t st = (cudaStream_t)stream;
     // scan: one resident wave of CTAs walking the (request, tile) pairs
     const int64_t resident = (int64_t)kScanCtasPerSm * fsm_num_sms();
@@ -337,6 +396,7 @@ extern "C" int rx_fsm_step(const rx_fsm *fsm, const float *logits, int64_t logit
     cfg.blockDim = dim3(kScanThreads);
     cfg.stream = st;
     RX_CUDA_CHECK(cudaLaunchKernelEx(&cfg, fsm_scan_kernel, p));
+    if (p.fused) return RX_OK;  // the last scan CTA finished every request
     // finish: a programmatic dependent of the scan, waiting on the device
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -3,7 +3,7 @@
 
 #include <stdint.h>
 
-#define RX_ABI_VERSION 2
+#define RX_ABI_VERSION 3
 
 // Longest position range one decode work item covers (the plan builder and
 // the no-plan split both stay at or below it).

@@ -100,7 +100,9 @@ def test_terminal_and_bad_states_are_flagged():
     assert int(status.item()) == rx.RX_DEV_FSM_DONE | rx.RX_DEV_BAD_STATE
 
 
-@pytest.mark.parametrize("vocab,batch", [(128256, 64), (32000, 300), (5003, 3)])
+# batches up to 512 finish in the scan kernel's last CTA; 700 takes the
+# separate finish kernel
+@pytest.mark.parametrize("vocab,batch", [(128256, 64), (32000, 300), (5003, 3), (5003, 512), (5003, 700)])
 def test_json_workload_matches_oracle(vocab, batch):
     """The synthetic JSON constraint at a real vocabulary size: every slice
     split (cluster sizes 1 to 8 across these shapes) gives the oracle's

@@ -39,7 +39,7 @@ def test_exports_every_declared_function():
     lib = rx.library()
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, missing
-    assert rx.version() == 2
+    assert rx.version() == 3
 
 
 def test_layer_outside_the_pool_is_rejected_before_any_launch():
