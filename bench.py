@@ -185,6 +185,15 @@ class GpuStep:
             self.plan_build_ms = (time.perf_counter() - t0) * 1e3
             self.plan_info = info
             self.plan = rx.plan_to_device(buf, info, B)
+            # bytes the call moves besides the unique K/V rows: q read, o
+            # written, the plan and slot ids read, and the fp32 partials
+            # (o and log2-sum-exp) of split rows, written once and read back
+            nparts = np.asarray(buf[B:2 * B], np.int64)
+            split = nparts[nparts > 1]
+            self.overhead_bytes = {
+                "q": int(B * p.hq * p.d * 2), "o": int(B * p.hq * p.d * 2),
+                "plan_and_slot_ids": int(len(buf) * 4 + info.tokens_read * 4),
+                "partials": int(2 * split.sum() * p.hq * (p.d + 1) * 4)}
             ws = rx.rx_attn_decode_workspace(B, p.hq, p.hkv, p.d, self.max_len, self.plan)
             self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev) if ws else None
             # per-head kernel (items of several requests), all-heads kernel
@@ -404,7 +413,8 @@ def run_gpu(args, rank, world, local_rank):
                          "dense_kv_bytes": int(prob.decode_dense_tokens() * kv_row),
                          "ms": dec_ms, "segments": st.plan_info.n_segments,
                          "work_items": st.plan_info.n_items, "kv_chunk": st.plan_info.kv_chunk,
-                         "plan_build_ms_once_per_batch": round(st.plan_build_ms, 3)}
+                         "plan_build_ms_once_per_batch": round(st.plan_build_ms, 3),
+                         "overhead_bytes": st.overhead_bytes}
     if st.has_ext:
         ext_ms = ms_of["extend"]
         tf = flops_ext / (ext_ms / 1e3) / 1e12
