@@ -604,6 +604,11 @@ __global__ void __launch_bounds__(kStaged ? kStagedThreads : kThreads, 1)
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned swizzle atoms
     const uint32_t sbase = rx::smem_u32(smem);
 
+    // staged: launched as a programmatic dependent of the copy; every CTA
+    // waits for the staging kernels (so this grid completes after them)
+    // before anything else
+    if (kStaged) rx::pdl_wait();
+
     // which rows: 256 / G tokens of request b times the G q-heads of kv head g
     Tile T;
     const int b = blockIdx.z;
@@ -723,6 +728,7 @@ __global__ void __launch_bounds__(kBN) stage_share_kernel(const int32_t *__restr
 {
     __shared__ int first, diff;
     const int b = blockIdx.x, t = threadIdx.x;
+    rx::pdl_launch_dependents();  // the offsets kernel may launch and wait on the device
     auto covers = [&](int i) {
         const int64_t P = __ldg(prefix_len + i), E = __ldg(extend_len + i);
         return P >= kBN && E >= 0 && P + E <= rtt_stride;
@@ -773,6 +779,8 @@ __global__ void __launch_bounds__(1024) ctx_offsets_kernel(const int32_t *prefix
 {
     __shared__ int64_t warp_tot[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    rx::pdl_launch_dependents();
+    rx::pdl_wait();  // the share counts are written by the kernel before this one
     const int per = (batch + 1023) / 1024;
     const int b0 = threadIdx.x * per;
     int64_t local = 0;
@@ -824,6 +832,8 @@ __global__ void __launch_bounds__(256) stage_rows_kernel(
     const int32_t *__restrict__ share, int batch, const int64_t *__restrict__ offs, int64_t cap,
     bf16 *__restrict__ ks, bf16 *__restrict__ vs, int row_elems, int32_t *status)
 {
+    rx::pdl_launch_dependents();
+    rx::pdl_wait();  // the packed-row offsets are written by the kernel before this one
     const int64_t total = offs[batch];
     if (total > cap) return;
     const int lane = threadIdx.x & 31;
@@ -956,6 +966,27 @@ int encode_stage_map(CUtensorMap *m, void *base, int64_t cap, int hkv, int D)
     return RX_OK;
 }
 
+// Launches `kernel` on `st` as a programmatic dependent of the kernel
+// enqueued just before it: it may start while that one runs and orders
+// itself with pdl_wait.
+template <typename... KArgs, typename... Args>
+int launch_dependent(void (*kernel)(KArgs...), dim3 grid, unsigned block, size_t smem, cudaStream_t st,
+                     Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    RX_CUDA_CHECK(cudaLaunchKernelEx(&cfg, kernel, args...));
+    return RX_OK;
+}
+
 template <int D, bool kStaged, bool F8 = false>
 int launch_extend(const XParams &p, dim3 grid, cudaStream_t st)
 {
@@ -965,7 +996,10 @@ int launch_extend(const XParams &p, dim3 grid, cudaStream_t st)
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, XL<D>::BYTES));
         configured = true;
     }
-    extend_kernel<D, kStaged, F8><<<grid, kStaged ? kStagedThreads : kThreads, XL<D>::BYTES, st>>>(p);
+    // staged: a programmatic dependent of the staging copy
+    if (kStaged)
+        return launch_dependent(extend_kernel<D, kStaged, F8>, grid, kStagedThreads, XL<D>::BYTES, st, p);
+    extend_kernel<D, kStaged, F8><<<grid, kThreads, XL<D>::BYTES, st>>>(p);
     RX_CUDA_CHECK(cudaGetLastError());
     return RX_OK;
 }
@@ -1063,13 +1097,16 @@ int extend_call(const char *who, const ExtendPool &pool, const void *q, void *o,
     RX_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     stage_share_kernel<<<batch, kBN, 0, st>>>(rtt, rtt_stride, req_idx, prefix_len, extend_len, src, share);
     RX_CUDA_CHECK(cudaGetLastError());
-    ctx_offsets_kernel<<<1, 1024, 0, st>>>(prefix_len, extend_len, share, batch, rtt_stride, cap, offs,
-                                           dev_status);
-    RX_CUDA_CHECK(cudaGetLastError());
+    // the offsets, the copy and the attention kernel are each a programmatic
+    // dependent of the kernel before: each waits on the device for what it reads
+    if ((rc = launch_dependent(ctx_offsets_kernel, dim3(1), 1024, 0, st, prefix_len, extend_len,
+                               (const int32_t *)share, batch, rtt_stride, cap, offs, dev_status)) != RX_OK)
+        return rc;
     auto stage = pool.f8 ? stage_rows_kernel<true> : stage_rows_kernel<false>;
-    stage<<<sms * 8, 256, 0, st>>>(pool.k, pool.v, p.num_slots, rtt, rtt_stride, req_idx, prefix_len, extend_len,
-                                   share, batch, offs, cap, ks, vs, p.hkv * D, dev_status);
-    RX_CUDA_CHECK(cudaGetLastError());
+    if ((rc = launch_dependent(stage, dim3(sms * 8), 256, 0, st, pool.k, pool.v, p.num_slots, rtt, rtt_stride,
+                               req_idx, prefix_len, extend_len, (const int32_t *)share, batch,
+                               (const int64_t *)offs, cap, ks, vs, p.hkv * D, dev_status)) != RX_OK)
+        return rc;
     return D == 128 ? launch_extend<128, true>(p, grid, st) : launch_extend<64, true>(p, grid, st);
 }
 
