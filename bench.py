@@ -789,7 +789,7 @@ def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
 # that an old count is never reported for new code.
 PROFILED_TRAFFIC = {
     ("mixed_chat", "staged"): (
-        846_600_000, "ncu --set full -k extend_kernel -c 1 on mixed_chat (600,000-slot pool; the kernel "
+        846_800_000, "ncu --set full -k extend_kernel -c 1 on mixed_chat (600,000-slot pool; the kernel "
                      "reads the same staged rows, Q and O at any pool size): extend_kernel alone"),
     ("mixed_chat", "decode"): (
         1_665_600_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat (600,000-slot pool; "
@@ -819,10 +819,10 @@ PROFILED_TRAFFIC = {
         843_200_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat --kv-fp8 (600,000-slot pool; same "
                      "rows): decode_gqa_kernel<F8> alone, without the merge"),
     ("cached_prefix_extend", "staged_fp8"): (
-        375_000_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend --kv-fp8 (36,000-slot pool; "
+        375_100_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend --kv-fp8 (36,000-slot pool; "
                      "same staged rows): extend_kernel alone, without the staging copy"),
     ("mixed_chat", "staged_fp8"): (
-        846_300_000, "ncu --set full -k extend_kernel -c 1 on mixed_chat --kv-fp8 (600,000-slot pool; same "
+        846_800_000, "ncu --set full -k extend_kernel -c 1 on mixed_chat --kv-fp8 (600,000-slot pool; same "
                      "staged rows): extend_kernel alone, without the staging copy"),
 }
 
