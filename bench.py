@@ -792,15 +792,15 @@ PROFILED_TRAFFIC = {
         846_800_000, "ncu --set full -k extend_kernel -c 1 on mixed_chat (600,000-slot pool; the kernel "
                      "reads the same staged rows, Q and O at any pool size): extend_kernel alone"),
     ("mixed_chat", "decode"): (
-        1_665_600_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat (600,000-slot pool; "
-                       "same rows): decode_gqa_kernel alone, without the merge"),
+        1_655_900_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat (600,000-slot pool; "
+                       "same rows; items longest first): decode_gqa_kernel alone, without the merge"),
     ("few_shot_decode", "decode"): (
         293_400_000, "ncu --set full -k decode_kernel -c 1 and -k decode_wide_kernel -c 1 on few_shot_decode "
                      "(262,144-slot pool; same rows): the two decode kernels, without the merge"),
     ("tree_of_thought_decode", "decode"): (
-        379_700_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode (131,072-slot pool; "
-                     "same rows; private ranges whole, 4 parts a row): decode_gqa_kernel alone, without "
-                     "the merge"),
+        369_700_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode (131,072-slot pool; "
+                     "same rows; private ranges whole, 4 parts a row, items longest first): "
+                     "decode_gqa_kernel alone, without the merge"),
     ("cached_prefix_extend", "staged"): (
         374_900_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend (36,000-slot pool; same "
                      "staged rows, shared prefix tiles staged once): extend_kernel alone, without the "

@@ -897,16 +897,20 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
         }
     }
     // per-head items first, then the all-heads items (read across all kv
-    // heads at once); within each, items of several requests before
-    // single-request ones, and each of those longest first, so that the tail
-    // of a grid holds the short items
+    // heads at once).  The per-head kernel's CTAs walk their items in a
+    // static round-robin: items of several requests before single-request
+    // ones, each of those longest first.  The all-heads kernel hands its
+    // items out first come first served, so they go longest first whatever
+    // their request count (the tail of the grid then holds the short items;
+    // equal lengths keep their order, so a shared chunk's request groups stay
+    // together and all but the first find it in L2).
     auto item_end = [&](const Item &x) -> int64_t {
         return x.v[3] == RX_PLAN_OPEN_END ? (int64_t)seq_len[x.v[7]] : (int64_t)x.v[3];
     };
     std::stable_sort(items.begin(), items.end(), [&](const Item &a, const Item &b) {
         if (a.all != b.all) return b.all;
         const bool sa = a.v[1] == 1, sb = b.v[1] == 1;
-        if (sa != sb) return sb;
+        if (!a.all && sa != sb) return sb;
         int64_t la = item_end(a) - a.v[2], lb = item_end(b) - b.v[2];
         if (la != lb) return la > lb;
         return a.v[1] > b.v[1];

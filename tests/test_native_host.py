@@ -400,8 +400,9 @@ def check_plan(prob, order, nparts, items, info, auto=False):
     # per-head items first, then the n_wide all-heads ones: for the head
     # counts with an all-heads kernel every single-request item, and with
     # G > 1 also groups of up to 16 / G requests (16 query rows per kv head);
-    # otherwise none.  Within each part, items of several requests come
-    # before single-request ones, each of those longest first.
+    # otherwise none.  Per-head items: those of several requests before
+    # single-request ones, each of those longest first; all-heads items
+    # (handed out first come first served): longest first.
     n_wide = int(info.n_wide)
     items = items.copy()
     is_open = items[:, 3] == rx.RX_PLAN_OPEN_END
@@ -412,13 +413,12 @@ def check_plan(prob, order, nparts, items, info, auto=False):
     else:
         assert not np.any(head[:, 1] == 1)
         assert np.all(tail[:, 1] * G <= 16) if G > 1 else np.all(tail[:, 1] == 1)
-    for part in (head, tail):
-        single = part[:, 1] == 1
-        k = int(single.sum())
-        assert np.all(single[len(part) - k:]) and not np.any(single[:len(part) - k])
-        for grp in (part[~single], part[single]):
-            lens = grp[:, 3] - grp[:, 2]
-            assert np.all(lens[:-1] >= lens[1:])
+    single = head[:, 1] == 1
+    k = int(single.sum())
+    assert np.all(single[len(head) - k:]) and not np.any(single[:len(head) - k])
+    for grp in (head[~single], head[single], tail):
+        lens = grp[:, 3] - grp[:, 2]
+        assert np.all(lens[:-1] >= lens[1:])
 
 
 @pytest.mark.parametrize("seed", range(15))
