@@ -729,8 +729,8 @@ def rx_attn_decode_fp8(k_pool, v_pool, k_scale: float, v_scale: float, q, o, lse
                        max_seq_len: int, sm_scale: float, plan: DevicePlan, workspace, dev_status=None, stream=None,
                        layer: int = 0) -> None:
     """Decode attention over uint8 E4M3 pools ([L,] S, Hkv, d) with per-pool
-    scales; a decode plan whose items all go to the all-heads kernel, and a
-    workspace of rx_attn_decode_workspace(...) bytes, are required."""
+    scales; the plan (or None) and the workspace (rx_attn_decode_workspace
+    bytes, or None when no row is split) as in rx_attn_decode."""
     torch = _torch()
     _dev(k_pool, torch.uint8, "k_pool")
     _dev(v_pool, torch.uint8, "v_pool")

@@ -270,6 +270,54 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// L2 eviction policies (createpolicy) for the cache-hint forms below:
+// evict_first for rows a call reads once, evict_last for scratch results
+// that the same call reads back shortly after.
+__device__ __forceinline__ uint64_t l2_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_normal()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+// bulk_g2s with an L2 eviction policy for the source lines
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                              uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;\n" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+// Global stores of one or two floats with an L2 eviction policy.
+__device__ __forceinline__ void st_hint(float *p, float a, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;\n" ::"l"(p), "f"(a), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_hint(float *p, float a, float b, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(p), "f"(a), "f"(b), "l"(pol)
+                 : "memory");
+}
+// Drops the 128-byte L2 line at p (128-byte aligned) without writing it
+// back: for scratch whose contents are no longer needed.
+__device__ __forceinline__ void discard_l2(const void *p)
+{
+    asm volatile("discard.global.L2 [%0], 128;\n" ::"l"(p) : "memory");
+}
+
 // TMA tiled load of one box of a 3-D tensor map at coordinates (c0, c1, c2)
 // (c0 innermost) into dst, the map's swizzle applied; the bytes complete a
 // transaction on mbarrier bar.  Elements outside the map land as zeros.

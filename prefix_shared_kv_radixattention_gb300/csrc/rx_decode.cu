@@ -637,11 +637,11 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
             } else {
                 const int64_t prow = orow * p.max_parts + part;
                 float *dst = p.ws_o + prow * D;
+                const uint64_t keep = rx::l2_evict_last();  // the merge reads it back
 #pragma unroll
                 for (int dt = 0; dt < DT; ++dt)
-                    *reinterpret_cast<float2 *>(dst + dt * 8 + tig * 2) =
-                        make_float2(oacc[dt][2 * half] * inv, oacc[dt][2 * half + 1] * inv);
-                if (tig == 0) p.ws_lse[prow] = m_r[half] + log2f(l_r[half]);
+                    rx::st_hint(dst + dt * 8 + tig * 2, oacc[dt][2 * half] * inv, oacc[dt][2 * half + 1] * inv, keep);
+                if (tig == 0) rx::st_hint(p.ws_lse + prow, m_r[half] + log2f(l_r[half]), keep);
             }
         }
     } else {
@@ -687,8 +687,9 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
                 if (p.lse && c == 0) p.lse[orow] = (mt + log2f(lt)) * rx::kLn2;
             } else {
                 const int64_t prow = orow * p.max_parts + part;
-                p.ws_o[prow * D + c] = ot / lt;
-                if (c == 0) p.ws_lse[prow] = mt + log2f(lt);
+                const uint64_t keep = rx::l2_evict_last();  // the merge reads it back
+                rx::st_hint(p.ws_o + prow * D + c, ot / lt, keep);
+                if (c == 0) rx::st_hint(p.ws_lse + prow, mt + log2f(lt), keep);
             }
         }
         __syncwarp();  // the next item may overwrite the buffer once every warp is here
@@ -849,6 +850,14 @@ __global__ void __launch_bounds__(128) merge_kernel(const Params p, int use_plan
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    // every lane's loads of the parts have been used: their L2 lines (whole
+    // 128-byte lines, D * 4 bytes a part) are dropped without a write-back
+    __syncwarp();
+    {
+        constexpr int LPP = D * 4 / 128;  // lines a part
+        const char *base = reinterpret_cast<const char *>(p.ws_o + row * p.max_parts * D);
+        for (int li = lane; li < np * LPP; li += 32) rx::discard_l2(base + (int64_t)li * 128);
+    }
     const float inv = 1.f / wsum;
     bf16 *dst = p.o + row * D + lane * PER;
 #pragma unroll
@@ -906,7 +915,7 @@ struct WideLayoutT {
     static constexpr int OFF_OK = 2 * STAGES * STAGE_BYTES;               // int [stage][pos]: row valid
     static constexpr int OFF_SLOT = OFF_OK + STAGES * kWideMaxPos * 4;    // int [stage][pos]: slot id or -1
     static constexpr int OFF_HDR = OFF_SLOT + STAGES * kWideMaxPos * 4;   // int4 [stage]: item, first
-                                                                          // position, item end, 0
+                                                                          // position, item end, requests
     static constexpr int OFF_Q = (OFF_HDR + STAGES * 16 + 127) / 128 * 128;  // NQ x the item's query rows
     static constexpr int QBYTES = QBYTES_;                                // bytes of one q slot
     static constexpr int OFF_BAR = OFF_Q + NQ * QBYTES;
@@ -1094,7 +1103,7 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
             okf[st * kWideMaxPos + lane] = ok ? 1 : 0;
             slotf[st * kWideMaxPos + lane] = ok ? s0 : -1;
         }
-        if (lane == 0) hdr[st] = make_int4(end ? -1 : c0.it, c0.q0, c0.p1, 0);
+        if (lane == 0) hdr[st] = make_int4(end ? -1 : c0.it, c0.q0, c0.p1, end ? 0 : c0.nr);
         const int nok = __popc(__ballot_sync(0xffffffffu, ok));
         __syncwarp();  // flags and header are written before lane 0's arrive releases them
         if (lane == 0)
@@ -1111,9 +1120,13 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
             // copies costs each warp tens of nanoseconds apiece)
             if (lane == 0) rx::mbar_arrive(bar + 8 * (WL::B_DESC + st));
         } else if (ok) {
+            // a single request's rows are read once: first out of L2
+            const uint64_t pol = c0.nr == 1 ? rx::l2_evict_first() : rx::l2_evict_normal();
             const uint32_t off = (uint32_t)(st * WL::STAGE_BYTES + lane * row_stride);
-            rx::bulk_g2s(sbase + WL::OFF_K + off, p.kb + (int64_t)s0 * p.row_bytes, (uint32_t)RB, bar + 8 * st);
-            rx::bulk_g2s(sbase + WL::OFF_V + off, p.vb + (int64_t)s0 * p.row_bytes, (uint32_t)RB, bar + 8 * st);
+            rx::bulk_g2s_hint(sbase + WL::OFF_K + off, p.kb + (int64_t)s0 * p.row_bytes, (uint32_t)RB, bar + 8 * st,
+                              pol);
+            rx::bulk_g2s_hint(sbase + WL::OFF_V + off, p.vb + (int64_t)s0 * p.row_bytes, (uint32_t)RB, bar + 8 * st,
+                              pol);
         }
         if (end) {
             ++j;
@@ -1141,7 +1154,10 @@ __device__ void wide_producer(const Params &p, unsigned char *smem, uint32_t sba
 // Copy warp h of NH of an all-heads kernel: for every stage the producer
 // described, issues the K and V row copies of positions h, h + NH, ... (one
 // lane each) onto the stage's full barrier.  It stops at the stage whose
-// header holds no item; the producer's drain covers its copies.
+// header holds no item; the producer's drain covers its copies.  Rows of a
+// single-request item (a request's own positions, read by nothing else in
+// the call) are fetched evict-first, so that they do not push out of L2 the
+// rows a request group re-reads or the partial results the merge reads back.
 template <class WL, int NP, int NH>
 __device__ void wide_copier(const Params &p, unsigned char *smem, uint32_t sbase, volatile int *abort_flag,
                             int row_stride, int h)
@@ -1152,15 +1168,18 @@ __device__ void wide_copier(const Params &p, unsigned char *smem, uint32_t sbase
     const int lane = threadIdx.x & 31;
     const uint32_t RB = (uint32_t)p.row_bytes;
     const int pos = lane * NH + h;
+    const uint64_t once = rx::l2_evict_first(), shared = rx::l2_evict_normal();
     for (int j = 0;; ++j) {
         const int st = j % WL::STAGES;
         if (!wait_or_abort(bar + 8 * (WL::B_DESC + st), (j / WL::STAGES) & 1, abort_flag, p.status, p.wait_cycles)) return;
-        if (hdr[st].x < 0) return;
+        const int4 h4 = hdr[st];
+        if (h4.x < 0) return;
         const int s = pos < NP ? slotf[st * kWideMaxPos + pos] : -1;
         if (s >= 0) {
+            const uint64_t pol = h4.w == 1 ? once : shared;
             const uint32_t off = (uint32_t)(st * WL::STAGE_BYTES + pos * row_stride);
-            rx::bulk_g2s(sbase + WL::OFF_K + off, p.kb + (int64_t)s * p.row_bytes, RB, bar + 8 * st);
-            rx::bulk_g2s(sbase + WL::OFF_V + off, p.vb + (int64_t)s * p.row_bytes, RB, bar + 8 * st);
+            rx::bulk_g2s_hint(sbase + WL::OFF_K + off, p.kb + (int64_t)s * p.row_bytes, RB, bar + 8 * st, pol);
+            rx::bulk_g2s_hint(sbase + WL::OFF_V + off, p.vb + (int64_t)s * p.row_bytes, RB, bar + 8 * st, pol);
         }
     }
 }
@@ -1222,6 +1241,7 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
         constexpr int NCH = DQ / 8;        // its 16-byte chunks (4 at d 128, 2 at d 64)
         constexpr int DO = D * HPW / 32;   // output dims per lane
         static_assert(NCH == 2 || NCH == 4, "quarter of 2 or 4 chunks");
+        static_assert(DO % 2 == 0, "output dims stored in pairs");
         const int cw = warp - 1 - kWideCopyWarps;
         const int h0 = cw * HPW;
         const int x = lane >> 2, qd = lane & 3;
@@ -1250,9 +1270,10 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
             } else {
                 const int64_t prow = orow * p.max_parts + part_idx;
                 float *dst = p.ws_o + prow * D + hl * DO;
+                const uint64_t keep = rx::l2_evict_last();  // the merge reads it back
 #pragma unroll
-                for (int e = 0; e < DO; ++e) dst[e] = o[e] * inv;
-                if (hl == 0) p.ws_lse[prow] = m + log2f(l);
+                for (int e = 0; e < DO; e += 2) rx::st_hint(dst + e, o[e] * inv, o[e + 1] * inv, keep);
+                if (hl == 0) rx::st_hint(p.ws_lse + prow, m + log2f(l), keep);
             }
         };
         for (int j = 0;; ++j) {
@@ -1472,11 +1493,11 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
             } else {
                 const int64_t prow = orow * p.max_parts + part_idx;
                 float *dst = p.ws_o + prow * D;
+                const uint64_t keep = rx::l2_evict_last();  // the merge reads it back
 #pragma unroll
                 for (int dt = 0; dt < DT; ++dt)
-                    *reinterpret_cast<float2 *>(dst + dt * 8 + tig * 2) =
-                        make_float2(oacc[dt][2 * half] * inv, oacc[dt][2 * half + 1] * inv);
-                if (tig == 0) p.ws_lse[prow] = m_r[half] + log2f(ls[half]);
+                    rx::st_hint(dst + dt * 8 + tig * 2, oacc[dt][2 * half] * inv, oacc[dt][2 * half + 1] * inv, keep);
+                if (tig == 0) rx::st_hint(p.ws_lse + prow, m_r[half] + log2f(ls[half]), keep);
             }
         }
     };

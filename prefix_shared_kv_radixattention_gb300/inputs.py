@@ -496,6 +496,63 @@ def ragged(seed: int, hq: int, hkv: int, d: int, n_groups: int, per_group: int, 
                    np.concatenate(new_slots), ext, dec)
 
 
+def random_tree(seed: int, hq: int, hkv: int, d: int, decode: bool, max_requests: int = 40,
+                max_depth: int = 4, max_children: int = 4, edge_max: int = 300, private_max: int = 200,
+                extend_max: int = 120, slack: int = 500) -> Problem:
+    """Random radix forest: nested shared prefixes of random lengths (empty
+    edges included) with random fan-outs; a request at every leaf and, at
+    random, at inner nodes too (a context that ends inside another's shared
+    prefix plus a tail of its own).  Each request adds a random private part
+    and one decode token or a random causal extend; the batch lists the
+    requests in a shuffled order, so batch index and req_to_token row differ.
+    The pool holds every token plus `slack` unused rows."""
+    rng = np.random.default_rng(seed)
+    paths = []      # per request: the edge ids of its shared prefix, root first
+    edge_len = []
+
+    def grow(path, depth):
+        if len(paths) >= max_requests:
+            return
+        lo = 2 if depth == 0 else 0   # a forest of at least two trees
+        n_kids = 0 if depth >= max_depth else int(rng.integers(lo, max(lo, max_children) + 1))
+        if n_kids == 0 or (path and rng.random() < 0.2):
+            paths.append(list(path))
+        for _ in range(n_kids):
+            if len(paths) >= max_requests:
+                break
+            e = len(edge_len)
+            edge_len.append(int(rng.integers(0, edge_max + 1)))
+            grow(path + [e], depth + 1)
+
+    grow([], 0)
+    B = len(paths)
+    p_len = rng.integers(0, private_max + 1, size=B)
+    e_len = np.ones(B, np.int64) if decode else rng.integers(1, extend_max + 1, size=B)
+    total = sum(edge_len) + int(p_len.sum()) + int(e_len.sum())
+    src = _SlotSource(rng, total + slack)
+    edge_tok = [_tokens(rng, n, 1_000_000 + 10_000 * e) for e, n in enumerate(edge_len)]
+    edge_slots = [src.take(n) for n in edge_len]
+    priv_slots = [src.take(int(n)) for n in p_len]
+    new_slots = [src.take(int(n)) for n in e_len]
+    rows = []
+    for b in range(B):
+        own = _tokens(rng, int(p_len[b] + e_len[b]), 900_000_000 + 100_000 * b)
+        rows.append((np.concatenate([edge_tok[e] for e in paths[b]] + [own]).astype(np.int64),
+                     np.concatenate([edge_slots[e] for e in paths[b]] + [priv_slots[b], new_slots[b]])
+                     .astype(np.int32)))
+    order = rng.permutation(B)
+    ext, dec = [], []
+    for b in order:
+        P = len(rows[b][1]) - int(e_len[b])
+        if decode:
+            dec.append((int(b), P + 1))
+        else:
+            ext.append((int(b), P, int(e_len[b])))
+    cached = np.concatenate(edge_slots + priv_slots) if total > int(e_len.sum()) else _empty_i32()
+    return _finish("random_tree", seed, rng, hq, hkv, d, total + slack, rows, cached,
+                   np.concatenate(new_slots), ext, dec)
+
+
 FULL_SIZE = {
     "tiny_extend": tiny_extend,
     "few_shot_decode": few_shot_decode,
