@@ -542,6 +542,16 @@ class E2EPipeline:
         pin = lambda t: t.cpu().pin_memory()
         self.h_k, self.h_v, self.h_sl = pin(st.k_new), pin(st.v_new), pin(st.slots)
         self.h_in, self.h_out = [self.h_k, self.h_v, self.h_sl], []
+        # with RoPE the positions are inputs of the step too: of the new
+        # rows, of the decode queries and of the extend queries
+        self.h_pos = {}
+        if st.rope_base:
+            self.h_pos["new"] = pin(st.pos_new)
+            if st.has_dec:
+                self.h_pos["dec"] = pin(st.pos_dec)
+            if st.has_ext:
+                self.h_pos["ext"] = pin(st.pos_ext)
+            self.h_in += list(self.h_pos.values())
         # the new row of each slot: which rows the decode part and each chunk store
         row_of = {int(s): i for i, s in enumerate(p.new_slots)}
         n_new = len(p.new_slots)
@@ -605,11 +615,37 @@ class E2EPipeline:
         st.k_new[a:b].copy_(self.h_k[a:b], non_blocking=True)
         st.v_new[a:b].copy_(self.h_v[a:b], non_blocking=True)
         st.slots[a:b].copy_(self.h_sl[a:b], non_blocking=True)
+        if "new" in self.h_pos:
+            st.pos_new[a:b].copy_(self.h_pos["new"][a:b], non_blocking=True)
 
     def _store_rows(self, a, b):
+        """Stores new rows a .. b - 1 as the step's store does (bf16 or E4M3
+        pools, K rotated on the way in when the step carries RoPE)."""
+        st, rx = self.st, self.rx
+        if b <= a:
+            return
+        k, v, sl = st.k_new[a:b], st.v_new[a:b], st.slots[a:b]
+        if st.kv_fp8 and st.rope_base:
+            rx.rx_kv_store_rope_fp8(st.k8, st.v8, 1.0, 1.0, k, v, sl, st.pos_new[a:b], st.rope_base, st.status)
+        elif st.kv_fp8:
+            rx.rx_kv_store_fp8(st.k8, st.v8, 1.0, 1.0, k, v, sl, st.status)
+        elif st.rope_base:
+            rx.rx_kv_store_rope(st.k_pool, st.v_pool, k, v, sl, st.pos_new[a:b], st.rope_base, st.status)
+        else:
+            rx.rx_kv_store(st.k_pool, st.v_pool, k, v, sl, st.status)
+
+    def load_inputs(self):
+        """The step's inputs copied in from the host buffers, in order."""
         st = self.st
-        if b > a:
-            self.rx.rx_kv_store(st.k_pool, st.v_pool, st.k_new[a:b], st.v_new[a:b], st.slots[a:b], st.status)
+        self._copy_rows(0, len(st.prob.new_slots))
+        if st.has_dec:
+            st.q_dec.copy_(self.h_qd[0])
+            st.dec_len.copy_(self.h_qd[1])
+        if st.has_ext:
+            st.q_ext.copy_(self.h_qe)
+        for k, t in (("dec", "pos_dec"), ("ext", "pos_ext")):
+            if k in self.h_pos:
+                getattr(st, t).copy_(self.h_pos[k])
 
     def step(self):
         torch, rx, st, p = self.torch, self.rx, self.st, self.st.prob
@@ -630,19 +666,25 @@ class E2EPipeline:
             if st.has_dec:
                 st.q_dec.copy_(self.h_qd[0], non_blocking=True)
                 st.dec_len.copy_(self.h_qd[1], non_blocking=True)
+                if "dec" in self.h_pos:
+                    st.pos_dec.copy_(self.h_pos["dec"], non_blocking=True)
             ev_dec.record()
             for c, ev in zip(self.chunks, ev_c):
                 if split:
                     self._copy_rows(*c["kv"])
                 r0, r1 = c["rows"]
                 st.q_ext[r0:r1].copy_(self.h_qe[r0:r1], non_blocking=True)
+                if "ext" in self.h_pos:
+                    st.pos_ext[r0:r1].copy_(self.h_pos["ext"][r0:r1], non_blocking=True)
                 ev.record()
         comp.wait_event(ev_dec)
         if split:
             self._store_rows(*self.dec_rows)
         else:
-            st.kv_store()
+            st.store_fp8() if st.kv_fp8 else st.kv_store()
         if st.has_dec:
+            if st.rope_base:
+                rx.rx_rope(st.q_dec, st.pos_dec, st.rope_base)
             st.decode()
             ev_d = E()
             ev_d.record(comp)
@@ -660,9 +702,16 @@ class E2EPipeline:
             with torch.cuda.stream(cs):
                 if split:
                     self._store_rows(*c["kv"])
-                rx.rx_attn_extend(st.k_pool, st.v_pool, st.q_ext[r0:r1], st.o_ext[r0:r1], None, c["qo"],
-                                  c["req"], c["P"], c["E"], st.rtt, c["max_E"], p.sm_scale, st.status,
-                                  workspace=self.ws[i % 2], stream=cs)
+                if st.rope_base:
+                    rx.rx_rope(st.q_ext[r0:r1], st.pos_ext[r0:r1], st.rope_base)
+                if st.kv_fp8:
+                    rx.rx_attn_extend_fp8(st.k8, st.v8, 1.0, 1.0, st.q_ext[r0:r1], st.o_ext[r0:r1], None,
+                                          c["qo"], c["req"], c["P"], c["E"], st.rtt, c["max_E"], p.sm_scale,
+                                          self.ws[i % 2], st.status, stream=cs)
+                else:
+                    rx.rx_attn_extend(st.k_pool, st.v_pool, st.q_ext[r0:r1], st.o_ext[r0:r1], None, c["qo"],
+                                      c["req"], c["P"], c["E"], st.rtt, c["max_E"], p.sm_scale, st.status,
+                                      workspace=self.ws[i % 2], stream=cs)
             ev_o = E()
             ev_o.record(cs)
             self.s_out.wait_event(ev_o)
@@ -690,93 +739,62 @@ def run_e2e(st, torch, rx, steps, flush, dist=None, world=1):
     copied back, and a synchronize -- a serving loop reads every step's
     output before it can form the next step.  Host wall time per step, L2
     flushed (untimed) before each one.  The copies overlap the kernels
-    (E2EPipeline) unless the step carries the optional RoPE or FP8 parts,
-    which run in the plain order.  The decode plan is not rebuilt per step:
+    (E2EPipeline), on bf16 or FP8 pools, with or without RoPE.  The decode
+    plan is not rebuilt per step:
     it was built once for the batch (its time is reported beside), and each
     request's last piece follows its length on the device, so the same plan
     serves the batch's later decode steps."""
     p = st.prob
-    pipelined = not st.rope_base and not st.kv_fp8
-    if pipelined:
-        pipe = E2EPipeline(st, torch, rx)
-        run, h2d, d2h = pipe.step, pipe.bytes_in(), pipe.bytes_out()
-        for _ in range(2):   # untimed: first use of the streams and events
-            run()
-        torch.cuda.synchronize()
-        eager_ms = None
+    pipe = E2EPipeline(st, torch, rx)
+    h2d, d2h = pipe.bytes_in(), pipe.bytes_out()
+    for _ in range(2):   # untimed: first use of the streams and events
+        pipe.step()
+    torch.cuda.synchronize()
+
+    def timed(run, n):
         secs = []
-        for i in range(max(3, min(steps, 50))):
+        for _ in range(n):
             flush()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             run()
             torch.cuda.synchronize()
             secs.append(time.perf_counter() - t0)
-        eager_ms = sum(secs) / len(secs) * 1e3
-        pipe.capture()
-        run = pipe.graph.replay
-    else:
-        h_in = [st.k_new.cpu().pin_memory(), st.v_new.cpu().pin_memory(), st.slots.cpu().pin_memory()]
-        d_in = [st.k_new, st.v_new, st.slots]
-        outs = []
-        if st.has_ext:
-            h_in.append(st.q_ext.cpu().pin_memory())
-            d_in.append(st.q_ext)
-            outs.append(st.o_ext)
-        if st.has_dec:
-            h_in += [st.q_dec.cpu().pin_memory(), st.dec_len.cpu().pin_memory()]
-            d_in += [st.q_dec, st.dec_len]
-            outs.append(st.o_dec)
-        h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        return sum(secs) / n * 1e3
 
-        def run():
-            for h, d in zip(h_in, d_in):
-                d.copy_(h, non_blocking=True)
-            st.step()
-            for h, d in zip(h_out, outs):
-                h.copy_(d, non_blocking=True)
-        h2d = sum(h.numel() * h.element_size() for h in h_in)
-        d2h = sum(h.numel() * h.element_size() for h in h_out)
+    eager_ms = timed(pipe.step, max(3, min(steps, 50)))
+    pipe.capture()
+    run = pipe.graph.replay
     n = max(3, min(steps, 200))
-    for _ in range(2):   # untimed: first use of the streams and events
+    for _ in range(2):
         run()
     torch.cuda.synchronize()
-    secs = []
-    for i in range(n):
-        flush()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        run()
-        torch.cuda.synchronize()
-        secs.append(time.perf_counter() - t0)
-    ms = max_over_ranks(sum(secs) / n * 1e3, dist, "cuda")
-    if pipelined:
-        # the overlapped schedule must return what the plain step returns
-        got = [h.clone() for h in pipe.h_out]
-        st.step()
-        torch.cuda.synchronize()
-        want = ([st.o_dec.cpu()] if st.has_dec else []) + ([st.o_ext.cpu()] if st.has_ext else [])
-        if not all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(got, want)):
-            raise RuntimeError("the overlapped end-to-end step returned other outputs than the step")
+    ms = max_over_ranks(timed(run, n), dist, "cuda")
+    # the overlapped schedule must return what the plain step returns on the
+    # same inputs (the step rotates q in place when it carries RoPE)
+    got = [h.clone() for h in pipe.h_out]
+    pipe.load_inputs()
+    st.step()
+    torch.cuda.synchronize()
+    want = ([st.o_dec.cpu()] if st.has_dec else []) + ([st.o_ext.cpu()] if st.has_ext else [])
+    if not all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(got, want)):
+        raise RuntimeError("the overlapped end-to-end step returned other outputs than the step")
     _, unit, per_step = step_metric(p)
     out = {"value": round(job_throughput(per_step, world, 1, ms), 3), "unit": unit,
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 5),
            "steps": n, "timing": "host wall clock per step, synchronized every step",
-           "schedule": ("; ".join(["copies on their own streams, overlapping the kernels"] +
-                                  (["decode's rows and queries first"] if st.has_dec and pipe.chunks else []) +
-                                  ([f"extend in {len(pipe.chunks)} request chunks (" +
-                                    ", ".join(str(c["n"]) for c in pipe.chunks) +
-                                    " requests) alternating over two compute streams"]
-                                   if pipe.chunks else []) +
-                                  (["each part stores its own new rows"] if pipe.split_store and pipe.chunks else
-                                   [] if pipe.split_store else ["every new row stored first"]))
-                        if pipelined else "copies in, the step, copies out, in order"),
-           "launch": "the step's calls captured once in a CUDA graph, replayed per step" if pipelined else
-                     "direct calls"}
-    if pipelined:
-        out["eager"] = {"ms_per_step": round(eager_ms, 5),
-                        "value": round(job_throughput(per_step, world, 1, eager_ms), 3),
-                        "launch": "the same calls made directly every step"}
+           "schedule": "; ".join(["copies on their own streams, overlapping the kernels"] +
+                                 (["decode's rows and queries first"] if st.has_dec and pipe.chunks else []) +
+                                 ([f"extend in {len(pipe.chunks)} request chunks (" +
+                                   ", ".join(str(c["n"]) for c in pipe.chunks) +
+                                   " requests) alternating over two compute streams"]
+                                  if pipe.chunks else []) +
+                                 (["each part stores its own new rows"] if pipe.split_store and pipe.chunks else
+                                  [] if pipe.split_store else ["every new row stored first"])),
+           "launch": "the step's calls captured once in a CUDA graph, replayed per step",
+           "eager": {"ms_per_step": round(eager_ms, 5),
+                     "value": round(job_throughput(per_step, world, 1, eager_ms), 3),
+                     "launch": "the same calls made directly every step"}}
     if st.has_dec:
         out["decode_plan"] = {"built": "once per batch, reused by every later decode step",
                               "build_ms": round(st.plan_build_ms, 3)}
@@ -792,15 +810,17 @@ PROFILED_TRAFFIC = {
         846_800_000, "ncu --set full -k extend_kernel -c 1 on mixed_chat (600,000-slot pool; the kernel "
                      "reads the same staged rows, Q and O at any pool size): extend_kernel alone"),
     ("mixed_chat", "decode"): (
-        1_655_900_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat (600,000-slot pool; "
-                       "same rows; items longest first): decode_gqa_kernel alone, without the merge"),
+        1_649_500_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat (600,000-slot pool; "
+                       "same rows; items longest first, private rows evict-first, partials evict-last): "
+                       "decode_gqa_kernel alone, without the merge"),
     ("few_shot_decode", "decode"): (
-        293_400_000, "ncu --set full -k decode_kernel -c 1 and -k decode_wide_kernel -c 1 on few_shot_decode "
-                     "(262,144-slot pool; same rows): the two decode kernels, without the merge"),
+        290_300_000, "ncu --set full -k decode_kernel -c 1 and -k decode_wide_kernel -c 1 on few_shot_decode "
+                     "(262,144-slot pool; same rows; private rows evict-first, partials evict-last): the two "
+                     "decode kernels, without the merge"),
     ("tree_of_thought_decode", "decode"): (
-        369_700_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode (131,072-slot pool; "
-                     "same rows; private ranges whole, 4 parts a row, items longest first): "
-                     "decode_gqa_kernel alone, without the merge"),
+        363_800_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode (131,072-slot pool; "
+                     "same rows; private ranges whole, 4 parts a row, items longest first, private rows "
+                     "evict-first, partials evict-last): decode_gqa_kernel alone, without the merge"),
     ("cached_prefix_extend", "staged"): (
         374_900_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend (36,000-slot pool; same "
                      "staged rows, shared prefix tiles staged once): extend_kernel alone, without the "
@@ -809,15 +829,6 @@ PROFILED_TRAFFIC = {
         135_200_000, "ncu --set full -k fsm_scan_kernel -c 1 on constrained_decode: the scan with the finish "
                      "in its last CTA (the whole step)"),
     # FP8 (E4M3) pools (--kv-fp8)
-    ("few_shot_decode", "decode_fp8"): (
-        147_600_000, "ncu --set full -k decode_kernel -c 1 and -k decode_wide_kernel -c 1 on few_shot_decode "
-                     "--kv-fp8 (262,144-slot pool; same rows): the two FP8 decode kernels, without the merge"),
-    ("tree_of_thought_decode", "decode_fp8"): (
-        196_600_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode --kv-fp8 (131,072-slot "
-                     "pool; same rows): decode_gqa_kernel<F8> alone, without the merge"),
-    ("mixed_chat", "decode_fp8"): (
-        843_200_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat --kv-fp8 (600,000-slot pool; same "
-                     "rows): decode_gqa_kernel<F8> alone, without the merge"),
     ("cached_prefix_extend", "staged_fp8"): (
         375_100_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend --kv-fp8 (36,000-slot pool; "
                      "same staged rows): extend_kernel alone, without the staging copy"),
