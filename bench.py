@@ -829,6 +829,18 @@ PROFILED_TRAFFIC = {
         135_200_000, "ncu --set full -k fsm_scan_kernel -c 1 on constrained_decode: the scan with the finish "
                      "in its last CTA (the whole step)"),
     # FP8 (E4M3) pools (--kv-fp8)
+    ("few_shot_decode", "decode_fp8"): (
+        147_500_000, "ncu --set full -k decode_kernel -c 1 and -k decode_wide_kernel -c 1 on few_shot_decode "
+                     "--kv-fp8 (262,144-slot pool; same rows; private rows evict-first, partials evict-last): the "
+                     "two FP8 decode kernels, without the merge"),
+    ("tree_of_thought_decode", "decode_fp8"): (
+        184_500_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode --kv-fp8 (131,072-slot "
+                     "pool; same rows; private rows evict-first, partials evict-last): decode_gqa_kernel<F8> "
+                     "alone, without the merge"),
+    ("mixed_chat", "decode_fp8"): (
+        827_200_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat --kv-fp8 (600,000-slot pool; same "
+                     "rows; private rows evict-first, partials evict-last): decode_gqa_kernel<F8> alone, without "
+                     "the merge"),
     ("cached_prefix_extend", "staged_fp8"): (
         375_100_000, "ncu --set full -k extend_kernel -c 1 on cached_prefix_extend --kv-fp8 (36,000-slot pool; "
                      "same staged rows): extend_kernel alone, without the staging copy"),
