@@ -466,7 +466,9 @@ size_t rx_attn_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t num_
  *   plan_or_null: device plan from rx_decode_plan_build for this batch, or
  *   NULL for one work split per request;
  *   workspace: device, >= rx_attn_decode_workspace(...) bytes, 256-byte
- *   aligned, contents ignored on entry (partial results of split work).
+ *   aligned, contents ignored on entry and undefined after the call
+ *   (partial results of split work, whose cache lines the merge discards
+ *   once read).
  * Requires head_dim in {64, 128}, num_q_heads % num_kv_heads == 0 and
  * 64 % (num_q_heads / num_kv_heads) == 0. */
 int rx_attn_decode(const rx_kv_pool *pool, const void *q, void *o, float *lse_or_null,

@@ -763,9 +763,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p)
     }
 }
 
-constexpr int kMergeFew = 12;  // parts up to which a row's partials are loaded in one go
+constexpr int kMergeFew = 12;    // parts up to which a row's partials are loaded in one go
+constexpr int kMergeBatch = 16;  // rows a batch above that (up to 64 parts)
 
-template <int D>
+// FEW (4, 8 or kMergeFew): the parts a row may have for the one-round-trip
+// path, the call's max_parts rounded up; MANY: rows may have more than
+// kMergeFew parts, and only then is the batched path built.  Registers grow
+// with both, and a merge of many rows with few parts each (thousands of
+// warps) wants them small, so that its CTAs fit the GPU in one wave.
+template <int D, int FEW, bool MANY>
 __global__ void __launch_bounds__(128) merge_kernel(const Params p, int use_plan)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -778,20 +784,22 @@ __global__ void __launch_bounds__(128) merge_kernel(const Params p, int use_plan
     }
     // the partials are written by the decode kernels just before this one
     rx::pdl_wait();
-    if (!live || np <= 1 || np > p.max_parts) return;  // > max_parts: flagged by the decode kernel
+    // > max_parts: flagged by the decode kernel; > FEW without MANY: not
+    // launched for such rows (FEW is at least max_parts then)
+    if (!live || np <= 1 || np > p.max_parts || (!MANY && np > FEW)) return;
     const float *lp = p.ws_lse + row * p.max_parts;
     constexpr int PER = D / 32;
     float acc[PER];
 #pragma unroll
     for (int j = 0; j < PER; ++j) acc[j] = 0.f;
     float m = -INFINITY, wsum = 0.f;
-    if (np <= kMergeFew) {
+    if (np <= FEW) {
         // few parts: their rows and log2-sum-exps are loaded together (one
         // round trip to L2), then weighted
         const float *src0 = p.ws_o + row * p.max_parts * D + lane * PER;
-        float v[kMergeFew][PER];
+        float v[FEW][PER];
 #pragma unroll
-        for (int k = 0; k < kMergeFew; ++k) {
+        for (int k = 0; k < FEW; ++k) {
             if (k < np) {
                 if constexpr (PER == 4) {
                     const float4 t = *reinterpret_cast<const float4 *>(src0 + (int64_t)k * D);
@@ -813,11 +821,66 @@ __global__ void __launch_bounds__(128) merge_kernel(const Params p, int use_plan
         const float wl = lane < np ? rx::fast_exp2(ll - m) : 0.f;
         wsum = wl;
 #pragma unroll
-        for (int k = 0; k < kMergeFew; ++k) {
+        for (int k = 0; k < FEW; ++k) {
             const float wgt = __shfl_sync(0xffffffffu, wl, k);
             if (k < np)
 #pragma unroll
                 for (int j = 0; j < PER; ++j) acc[j] = fmaf(wgt, v[k][j], acc[j]);
+        }
+    } else if constexpr (!MANY) {
+        // not reached: np <= FEW above
+    } else if (np <= 2 * 32) {
+        // up to 64 parts: every log2-sum-exp (two a lane) and the first 16
+        // rows are loaded together; each later batch of 16 rows is loaded
+        // before the previous one is weighted, so about np / 16 round trips
+        // to L2 remain
+        constexpr int NB = kMergeBatch;
+        const float *src0 = p.ws_o + row * p.max_parts * D + lane * PER;
+        auto load = [&](float (&v)[NB][PER], int base) {
+#pragma unroll
+            for (int k = 0; k < NB; ++k) {
+                if (base + k < np) {
+                    const float *src = src0 + (int64_t)(base + k) * D;
+                    if constexpr (PER == 4) {
+                        const float4 t = *reinterpret_cast<const float4 *>(src);
+                        v[k][0] = t.x;
+                        v[k][1] = t.y;
+                        v[k][2] = t.z;
+                        v[k][3] = t.w;
+                    } else {
+                        const float2 t = *reinterpret_cast<const float2 *>(src);
+                        v[k][0] = t.x;
+                        v[k][1] = t.y;
+                    }
+                }
+            }
+        };
+        float va[NB][PER], vb[NB][PER];
+        const float l0 = lane < np ? lp[lane] : -INFINITY;
+        const float l1 = lane + 32 < np ? lp[lane + 32] : -INFINITY;
+        load(va, 0);
+        m = fmaxf(l0, l1);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float w0 = lane < np ? rx::fast_exp2(l0 - m) : 0.f;
+        const float w1 = lane + 32 < np ? rx::fast_exp2(l1 - m) : 0.f;
+        wsum = w0 + w1;
+        auto weigh = [&](const float (&v)[NB][PER], int base) {
+#pragma unroll
+            for (int k = 0; k < NB; ++k) {
+                const int i = base + k;  // warp-uniform
+                const float wgt = __shfl_sync(0xffffffffu, i < 32 ? w0 : w1, i & 31);
+                if (i < np)
+#pragma unroll
+                    for (int j = 0; j < PER; ++j) acc[j] = fmaf(wgt, v[k][j], acc[j]);
+            }
+        };
+        for (int base = 0; base < np; base += 2 * NB) {
+            if (base + NB < np) load(vb, base + NB);
+            weigh(va, base);
+            if (base + NB >= np) break;
+            if (base + 2 * NB < np) load(va, base + 2 * NB);
+            weigh(vb, base + NB);
         }
     } else {
         for (int i = lane; i < np; i += 32) m = fmaxf(m, lp[i]);
@@ -1824,7 +1887,12 @@ template <int D>
 int launch_merge(const Params &p, int use_plan, cudaStream_t st)
 {
     const int64_t rows = (int64_t)p.batch * p.hq;
-    return launch_on(merge_kernel<D>, (unsigned)((rows + 3) / 4), 128, 0, st, true, p, use_plan);
+    const unsigned grid = (unsigned)((rows + 3) / 4);
+    if (p.max_parts > kMergeFew)
+        return launch_on(merge_kernel<D, kMergeFew, true>, grid, 128, 0, st, true, p, use_plan);
+    if (p.max_parts > 8) return launch_on(merge_kernel<D, kMergeFew, false>, grid, 128, 0, st, true, p, use_plan);
+    if (p.max_parts > 4) return launch_on(merge_kernel<D, 8, false>, grid, 128, 0, st, true, p, use_plan);
+    return launch_on(merge_kernel<D, 4, false>, grid, 128, 0, st, true, p, use_plan);
 }
 
 }  // namespace

@@ -226,6 +226,21 @@ def test_decode_split_rows_merged(hq, shared, private):
     _check_decode(prob, plan=True, kv_chunk=64)
 
 
+@pytest.mark.parametrize("hq,hkv,d,private,parts", [(8, 8, 64, 300, (13, 64)), (32, 8, 128, 900, (13, 64)),
+                                                    (8, 8, 128, 3000, (65, 400)), (32, 8, 64, 2500, (65, 400))])
+def test_decode_merge_part_counts(hq, hkv, d, private, parts):
+    """The merge's three ways through a row's parts: the plan's automatic
+    pieces give every row 13 to 64 parts (loaded in batches of 16) or more
+    than 64 (the general loop), at d 64 and 128; the rows then match the
+    oracle."""
+    from prefix_shared_kv_radixattention_gb300 import binding as rx
+    prob = inputs.few_shot_decode(hq=hq, hkv=hkv, d=d, batch=2, shared=0, private=private, num_slots=8192)
+    buf, info = rx.rx_decode_plan_build(prob.req_to_token, prob.dec_req_idx, prob.dec_seq_len, hq, hkv)
+    nparts = np.asarray(buf[2:4])
+    assert parts[0] <= nparts.min() and nparts.max() <= parts[1], nparts
+    _check_decode(prob, plan=True)
+
+
 def test_decode_tree_of_thought_reduced():
     prob = inputs.tree_of_thought_decode(depth=3, fanout=3, edge=70, num_slots=8192)
     _check_decode(prob, plan=True, kv_chunk=64, min_shared=16)
