@@ -637,11 +637,11 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
             } else {
                 const int64_t prow = orow * p.max_parts + part;
                 float *dst = p.ws_o + prow * D;
-                const uint64_t keep = rx::l2_evict_last();  // the merge reads it back
+                const uint64_t keep = rx::l2_evict_last();  // the merge reads them back, then discards the lines
 #pragma unroll
                 for (int dt = 0; dt < DT; ++dt)
                     rx::st_hint(dst + dt * 8 + tig * 2, oacc[dt][2 * half] * inv, oacc[dt][2 * half + 1] * inv, keep);
-                if (tig == 0) rx::st_hint(p.ws_lse + prow, m_r[half] + log2f(l_r[half]), keep);
+                if (tig == 0) p.ws_lse[prow] = m_r[half] + log2f(l_r[half]);
             }
         }
     } else {
@@ -687,9 +687,9 @@ __device__ bool consume(const Params &p, const Desc *d, unsigned char *smem, uin
                 if (p.lse && c == 0) p.lse[orow] = (mt + log2f(lt)) * rx::kLn2;
             } else {
                 const int64_t prow = orow * p.max_parts + part;
-                const uint64_t keep = rx::l2_evict_last();  // the merge reads it back
+                const uint64_t keep = rx::l2_evict_last();  // the merge reads them back, then discards the lines
                 rx::st_hint(p.ws_o + prow * D + c, ot / lt, keep);
-                if (c == 0) rx::st_hint(p.ws_lse + prow, mt + log2f(lt), keep);
+                if (c == 0) p.ws_lse[prow] = mt + log2f(lt);
             }
         }
         __syncwarp();  // the next item may overwrite the buffer once every warp is here
@@ -1333,10 +1333,10 @@ __global__ void __launch_bounds__(32 * (1 + kWideCopyWarps + CW), 1) decode_wide
             } else {
                 const int64_t prow = orow * p.max_parts + part_idx;
                 float *dst = p.ws_o + prow * D + hl * DO;
-                const uint64_t keep = rx::l2_evict_last();  // the merge reads it back
+                const uint64_t keep = rx::l2_evict_last();  // the merge reads them back, then discards the lines
 #pragma unroll
                 for (int e = 0; e < DO; e += 2) rx::st_hint(dst + e, o[e] * inv, o[e + 1] * inv, keep);
-                if (hl == 0) rx::st_hint(p.ws_lse + prow, m + log2f(l), keep);
+                if (hl == 0) p.ws_lse[prow] = m + log2f(l);
             }
         };
         for (int j = 0;; ++j) {
@@ -1556,11 +1556,11 @@ __global__ void __launch_bounds__(32 * (1 + kGqaCopyWarps + kGqaWarps), 1) decod
             } else {
                 const int64_t prow = orow * p.max_parts + part_idx;
                 float *dst = p.ws_o + prow * D;
-                const uint64_t keep = rx::l2_evict_last();  // the merge reads it back
+                const uint64_t keep = rx::l2_evict_last();  // the merge reads them back, then discards the lines
 #pragma unroll
                 for (int dt = 0; dt < DT; ++dt)
                     rx::st_hint(dst + dt * 8 + tig * 2, oacc[dt][2 * half] * inv, oacc[dt][2 * half + 1] * inv, keep);
-                if (tig == 0) rx::st_hint(p.ws_lse + prow, m_r[half] + log2f(ls[half]), keep);
+                if (tig == 0) p.ws_lse[prow] = m_r[half] + log2f(ls[half]);
             }
         }
     };

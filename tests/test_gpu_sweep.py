@@ -32,7 +32,7 @@ def _setting(seed):
     return kv_chunk, min_shared
 
 
-@pytest.mark.parametrize("seed", range(10))
+@pytest.mark.parametrize("seed", range(16))
 def test_decode_random_forest(seed):
     """bf16 pools: without a plan, with the automatic plan, and with the
     seed's chunk and minimum segment length."""
@@ -73,7 +73,7 @@ def test_decode_fp8_random_forest(seed):
     assert int(status.item()) == 0
 
 
-@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("seed", range(10))
 def test_extend_random_forest(seed):
     """bf16 pools, both operand paths: the oracle's result, and the two
     paths bit for bit equal."""
