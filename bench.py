@@ -519,15 +519,16 @@ class E2EPipeline:
     host buffers, its copies overlapped with the kernels.  An input stream
     brings in, in this order: the decode requests' new K/V rows, slots and
     queries; then, per chunk of extend requests, the chunk's new K/V rows,
-    slots and queries.  The compute stream stores the decode rows and runs
-    decode as soon as they are in; each chunk's rows are stored and its
-    extend run (rx_kv_store and rx_attn_extend over the chunk) as soon as the
-    chunk is in, the chunks alternating between two compute streams with a
-    staging workspace each (different chunks touch disjoint rows and slots,
-    so one chunk's staging and last wave overlap the next one's attention);
-    an output stream copies each result back as soon as it is written.  The
-    host link (about 200 GB/s each way on this machine)
-    is slower than the kernels, so decode goes first (its inputs are small,
+    slots and queries.  The compute stream stores the decode rows as soon as
+    they are in (while the queries arrive) and runs decode once its queries
+    are in too; each chunk's rows are stored as soon as they are in, and its
+    extend run (rx_attn_extend over the chunk) once its queries are in, the
+    chunks alternating between two compute streams with a staging workspace
+    each (different chunks touch disjoint rows and slots, so one chunk's
+    staging and last wave overlap the next one's attention); an output
+    stream copies each result back as soon as it is written.  The host link
+    (about 200 GB/s each way on this machine) is slower than the kernels,
+    so decode goes first (its inputs are small,
     and it runs while the first chunk arrives) and the chunks grow, then
     shrink (little to wait for at the start, little to copy back after the
     last kernel).  Where a chunk's new rows are not one contiguous range of
@@ -652,8 +653,9 @@ class E2EPipeline:
         E = torch.cuda.Event
         comp = torch.cuda.current_stream()
         split = self.split_store
-        ev_dec = E()
+        ev_dec, ev_dec_rows = E(), E()
         ev_c = [E() for _ in self.chunks]
+        ev_c_rows = [E() for _ in self.chunks]   # a part's new rows are in: its store may start
         # the side streams fork from the compute stream (required when captured)
         self.s_in.wait_stream(comp)
         self.s_out.wait_stream(comp)
@@ -663,25 +665,29 @@ class E2EPipeline:
                 self._copy_rows(*self.dec_rows)
             else:
                 self._copy_rows(0, len(p.new_slots))
+            ev_dec_rows.record()
             if st.has_dec:
                 st.q_dec.copy_(self.h_qd[0], non_blocking=True)
                 st.dec_len.copy_(self.h_qd[1], non_blocking=True)
                 if "dec" in self.h_pos:
                     st.pos_dec.copy_(self.h_pos["dec"], non_blocking=True)
             ev_dec.record()
-            for c, ev in zip(self.chunks, ev_c):
+            for c, ev, ev_r in zip(self.chunks, ev_c, ev_c_rows):
                 if split:
                     self._copy_rows(*c["kv"])
+                ev_r.record()
                 r0, r1 = c["rows"]
                 st.q_ext[r0:r1].copy_(self.h_qe[r0:r1], non_blocking=True)
                 if "ext" in self.h_pos:
                     st.pos_ext[r0:r1].copy_(self.h_pos["ext"][r0:r1], non_blocking=True)
                 ev.record()
-        comp.wait_event(ev_dec)
+        # each store runs as soon as its rows are in, while its queries arrive
+        comp.wait_event(ev_dec_rows)
         if split:
             self._store_rows(*self.dec_rows)
         else:
             st.store_fp8() if st.kv_fp8 else st.kv_store()
+        comp.wait_event(ev_dec)
         if st.has_dec:
             if st.rope_base:
                 rx.rx_rope(st.q_dec, st.pos_dec, st.rope_base)
@@ -695,13 +701,15 @@ class E2EPipeline:
         # different chunks read and write disjoint rows and slots, so one
         # chunk's staging and last wave overlap the next chunk's attention
         streams = (comp, self.s_comp2)
-        for i, (c, ev) in enumerate(zip(self.chunks, ev_c)):
+        for i, (c, ev, ev_r) in enumerate(zip(self.chunks, ev_c, ev_c_rows)):
             r0, r1 = c["rows"]
             cs = streams[i % 2]
-            cs.wait_event(ev)
+            cs.wait_event(ev_r)
             with torch.cuda.stream(cs):
                 if split:
                     self._store_rows(*c["kv"])
+            cs.wait_event(ev)
+            with torch.cuda.stream(cs):
                 if st.rope_base:
                     rx.rx_rope(st.q_ext[r0:r1], st.pos_ext[r0:r1], st.rope_base)
                 if st.kv_fp8:
