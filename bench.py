@@ -826,7 +826,7 @@ PROFILED_TRAFFIC = {
                      "(262,144-slot pool; same rows; private rows evict-first, partials evict-last): the two "
                      "decode kernels, without the merge"),
     ("tree_of_thought_decode", "decode"): (
-        363_800_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode (131,072-slot pool; "
+        364_000_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode (131,072-slot pool; "
                      "same rows; private ranges whole, 4 parts a row, items longest first, private rows "
                      "evict-first, partials evict-last): decode_gqa_kernel alone, without the merge"),
     ("cached_prefix_extend", "staged"): (
@@ -842,11 +842,11 @@ PROFILED_TRAFFIC = {
                      "--kv-fp8 (262,144-slot pool; same rows; private rows evict-first, partials evict-last): the "
                      "two FP8 decode kernels, without the merge"),
     ("tree_of_thought_decode", "decode_fp8"): (
-        184_500_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode --kv-fp8 (131,072-slot "
+        184_700_000, "ncu --set full -k decode_gqa_kernel -c 1 on tree_of_thought_decode --kv-fp8 (131,072-slot "
                      "pool; same rows; private rows evict-first, partials evict-last): decode_gqa_kernel<F8> "
                      "alone, without the merge"),
     ("mixed_chat", "decode_fp8"): (
-        827_200_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat --kv-fp8 (600,000-slot pool; same "
+        827_500_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat --kv-fp8 (600,000-slot pool; same "
                      "rows; private rows evict-first, partials evict-last): decode_gqa_kernel<F8> alone, without "
                      "the merge"),
     ("cached_prefix_extend", "staged_fp8"): (
