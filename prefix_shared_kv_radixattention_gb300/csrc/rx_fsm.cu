@@ -71,14 +71,18 @@ struct FsmParams {
 
 // Order-preserving key of a candidate (value v, id i): a larger value, then
 // a smaller id, gives a larger key.  NaN counts as -inf and -0 as +0 (equal
-// values tie); every candidate's key is above 0, which means "none".
-__device__ __forceinline__ unsigned long long key_of(float v, int i)
+// values tie); every candidate's key is above 0, which means "none".  The
+// value's half: fmaxf returns its other operand for a NaN, and -0 + 0 is
+// +0; then the sign-magnitude bits are made to order as unsigned integers.
+__device__ __forceinline__ uint32_t value_key(float v)
 {
-    if (v != v) v = -INFINITY;
-    if (v == 0.f) v = 0.f;
-    uint32_t u = __float_as_uint(v);
-    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i);
+    v = fmaxf(v, -INFINITY) + 0.f;
+    const uint32_t u = __float_as_uint(v);
+    return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
+__device__ __forceinline__ unsigned long long key_of(uint32_t vk, int i)
+{
+    return ((unsigned long long)vk << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i);
 }
 
 // The edge of state s for token bi, and the jump of the state it leads to:
@@ -132,7 +136,10 @@ __device__ void finish_request(const FsmParams &p, int b, unsigned long long key
 // Scan: CTAs walk (request, tile) pairs and fold each tile's allowed
 // candidates into the request's best key with a 64-bit atomicMax, one per
 // warp and tile.  16-byte loads of logits and of the state's mask words,
-// four groups in flight per thread.
+// four groups in flight per thread.  A thread keeps its best value key and
+// id in 32-bit registers (it visits ids in increasing order, so a strict
+// comparison keeps the smaller id of a tie) and forms the 64-bit key once
+// per tile.
 __global__ void __launch_bounds__(kScanThreads, kScanCtasPerSm) fsm_scan_kernel(const FsmParams p)
 {
     rx::pdl_launch_dependents();  // the finish kernel may launch now and wait on the device
@@ -149,29 +156,43 @@ __global__ void __launch_bounds__(kScanThreads, kScanCtasPerSm) fsm_scan_kernel(
         // whole 16-byte groups: a row holds at least vocab rounded up to four
         // ids, and ids past vocab have no mask bit; a tile starts on a word
         const int g1 = (hi + 3) / 4;
-        unsigned long long best = 0;
+        uint32_t bv = 0u;  // best value key so far (0: none)
+        int bi = 0;        // its id
         for (int g = lo / 4 + (int)threadIdx.x; g < g1; g += kScanThreads * kScanUnroll) {
             float4 x[kScanUnroll];
-            uint32_t m[kScanUnroll];
+            uint32_t mw[kScanUnroll];  // the mask word of each group, its 4 bits at 4 * (gg % 8)
 #pragma unroll
             for (int u = 0; u < kScanUnroll; ++u) {
                 const int gg = g + u * kScanThreads;
-                m[u] = 0u;
+                mw[u] = 0u;
                 if (gg < g1) {
-                    m[u] = (__ldg(mrow + (gg >> 3)) >> ((4 * gg) & 31)) & 0xFu;
+                    mw[u] = __ldg(mrow + (gg >> 3));
                     x[u] = __ldg(row + gg);
                 }
             }
+            // every group of one pass sits at the same place in its word (the
+            // groups are kScanThreads apart, a multiple of 8)
+            static_assert(kScanThreads % 8 == 0, "groups of a pass share their bit position");
+            const int sh = (4 * g) & 31;
 #pragma unroll
             for (int u = 0; u < kScanUnroll; ++u) {
-                if (!m[u]) continue;
+                const uint32_t mu = (mw[u] >> sh) & 0xFu;
+                if (!mu) continue;
                 const int i = 4 * (g + u * kScanThreads);
-                if (m[u] & 1u) best = max(best, key_of(x[u].x, i));
-                if (m[u] & 2u) best = max(best, key_of(x[u].y, i + 1));
-                if (m[u] & 4u) best = max(best, key_of(x[u].z, i + 2));
-                if (m[u] & 8u) best = max(best, key_of(x[u].w, i + 3));
+                auto consider = [&](float v, int id) {
+                    const uint32_t k = value_key(v);
+                    if (k > bv) {
+                        bv = k;
+                        bi = id;
+                    }
+                };
+                if (mu & 1u) consider(x[u].x, i);
+                if (mu & 2u) consider(x[u].y, i + 1);
+                if (mu & 4u) consider(x[u].z, i + 2);
+                if (mu & 8u) consider(x[u].w, i + 3);
             }
         }
+        unsigned long long best = bv ? key_of(bv, bi) : 0ull;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
         if (lane == 0 && best) atomicMax(p.best + b, best);
