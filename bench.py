@@ -834,8 +834,8 @@ PROFILED_TRAFFIC = {
                      "staged rows, shared prefix tiles staged once): extend_kernel alone, without the "
                      "staging copy"),
     ("constrained_decode", "fsm"): (
-        135_200_000, "ncu --set full -k fsm_scan_kernel -c 1 on constrained_decode: the scan with the finish "
-                     "in its last CTA (the whole step)"),
+        135_200_000, "ncu --set full -k fsm_scan_kernel -c 1 on constrained_decode: the scan (32-bit value keys "
+                     "per thread) with the finish in its last CTA (the whole step)"),
     # FP8 (E4M3) pools (--kv-fp8)
     ("few_shot_decode", "decode_fp8"): (
         147_500_000, "ncu --set full -k decode_kernel -c 1 and -k decode_wide_kernel -c 1 on few_shot_decode "
