@@ -77,6 +77,23 @@ def test_ties_nan_and_inf():
     assert got == em and st == ns and status == 0
 
 
+def test_signed_zero_ties():
+    """-0 and +0 are equal values: where the largest allowed logit is zero,
+    the smallest allowed id holding a zero of either sign wins."""
+    rng = np.random.default_rng(11)
+    S, V = 24, 300
+    args = random_automaton(rng, S, V, p_single=0.0)
+    live = [s for s in range(S) if args[0][s + 1] > args[0][s]]
+    B = 48
+    state = np.array([live[i % len(live)] for i in range(B)], np.int32)
+    logits = np.full((B, V), -1.0, np.float32)
+    logits[:, ::2] = -0.0
+    logits[:, 1::4] = 0.0
+    logits[::3, ::5] = np.nan
+    (got, st, status), (em, ns, _) = _run(S, V, *args, 3, state, logits)
+    assert got == em and st == ns and status == 0
+
+
 def test_terminal_and_bad_states_are_flagged():
     rx = _rx()
     from tests.test_fsm_oracle import EX
