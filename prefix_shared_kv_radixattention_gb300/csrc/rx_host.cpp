@@ -801,8 +801,9 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
     auto nchunks = [&](int64_t len) { return (len + kv_chunk - 1) / kv_chunk; };
     // With wide items, a request's own (private) positions are cut into
     // near-equal pieces: with automatic chunking, of about priv_total /
-    // RX_DECODE_TARGET_WIDE_ITEMS positions (16 .. RX_MAX_KV_CHUNK), else of
-    // at most kv_chunk.  Otherwise they are cut into kv_chunk pieces.
+    // RX_DECODE_TARGET_WIDE_ITEMS (or _GROUPED) positions (16 ..
+    // RX_MAX_KV_CHUNK), else of at most kv_chunk.  Otherwise they are cut
+    // into kv_chunk pieces.
     int64_t priv_total = 0;
     for (int64_t r = 0; r < B; ++r) priv_total += seq_len[order[(size_t)r]] - priv_begin[(size_t)r];
     // Request-group items share the all-heads kernel's queue with the
@@ -815,13 +816,22 @@ extern "C" int rx_decode_plan_build(const int32_t *rtt, int64_t stride, const in
         return groups && (x.rb - x.lb + 1 + RG - 1) / RG <= RX_DECODE_MAX_GROUPS;
     };
     int64_t group_len = 0;
-    for (int64_t k = 0; k < n_iv; ++k)
-        if (is_seg[(size_t)k] && grouped_seg(iv[(size_t)k]))
+    bool per_head_segs = false;  // a shared segment goes to the per-head kernel
+    for (int64_t k = 0; k < n_iv; ++k) {
+        if (!is_seg[(size_t)k]) continue;
+        if (grouped_seg(iv[(size_t)k]))
             group_len = std::max<int64_t>(group_len, std::min<int64_t>(kv_chunk, iv[(size_t)k].lcp - seg_start[(size_t)k]));
+        else
+            per_head_segs = true;
+    }
+    // fewer, longer private pieces when group items (and nothing else) share
+    // the all-heads kernel's queue with them
+    const int64_t wide_target = group_len > 0 && !per_head_segs ? RX_DECODE_TARGET_WIDE_ITEMS_GROUPED
+                                                                 : RX_DECODE_TARGET_WIDE_ITEMS;
     int64_t pchunk = kv_chunk;
     if (auto_chunk && wide && priv_total > 0)
         pchunk = std::min<int64_t>(RX_MAX_KV_CHUNK, std::max<int64_t>(RX_DECODE_MIN_WIDE_CHUNK,
-                                   (priv_total + RX_DECODE_TARGET_WIDE_ITEMS - 1) / RX_DECODE_TARGET_WIDE_ITEMS));
+                                   (priv_total + wide_target - 1) / wide_target));
     auto npriv = [&](int64_t len) {
         int64_t n = (len + pchunk - 1) / pchunk;
         if (auto_chunk && wide && group_len > 0)

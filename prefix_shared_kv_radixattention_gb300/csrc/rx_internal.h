@@ -22,6 +22,14 @@
 // wave of (kv head, chunk) pairs.  Measured on few-shot decode: 304 / 152
 // beats 608 / 304 by 7 %, and 76 per-head items beat 152 by 6 %.
 #define RX_DECODE_TARGET_WIDE_ITEMS 304
+// When every shared chunk goes to the all-heads kernel as request groups (no
+// per-head kernel beside it), the short group items, handed out last, fill
+// the end of the schedule, and fewer, longer private pieces do better:
+// measured on the long-chat decode (16 requests of 24,577 private
+// positions), 228 / 190 / 152 targets take 0.273 / 0.315 / 0.369 ms against
+// 0.281 for 304; tree-of-thought decode keeps its private ranges whole
+// either way.
+#define RX_DECODE_TARGET_WIDE_ITEMS_GROUPED 228
 #define RX_DECODE_MIN_WIDE_CHUNK 16
 #define RX_DECODE_TARGET_SHARED_ITEMS 76
 #define RX_DECODE_TARGET_GROUP_CHUNKS 152
