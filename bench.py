@@ -818,9 +818,9 @@ PROFILED_TRAFFIC = {
         846_800_000, "ncu --set full -k extend_kernel -c 1 on mixed_chat (600,000-slot pool; the kernel "
                      "reads the same staged rows, Q and O at any pool size): extend_kernel alone"),
     ("mixed_chat", "decode"): (
-        1_649_500_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat (600,000-slot pool; "
-                       "same rows; items longest first, private rows evict-first, partials evict-last): "
-                       "decode_gqa_kernel alone, without the merge"),
+        1_649_400_000, "ncu --set full -k decode_gqa_kernel -c 1 on mixed_chat (600,000-slot pool; "
+                       "same rows; 240 private pieces and 152 group items, longest first; private rows "
+                       "evict-first, partials evict-last): decode_gqa_kernel alone, without the merge"),
     ("few_shot_decode", "decode"): (
         290_300_000, "ncu --set full -k decode_kernel -c 1 and -k decode_wide_kernel -c 1 on few_shot_decode "
                      "(262,144-slot pool; same rows; private rows evict-first, partials evict-last): the two "
